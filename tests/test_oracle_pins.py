@@ -1,0 +1,470 @@
+"""Pins for the CPU oracle: the pages' worked examples, closed forms, invariants, exact arithmetic
+(Python's decimal / fractions) and brute force against numpy on tiny inputs.
+
+These run without a GPU. Each check is chosen so that a plausible slip in the oracle -- a wrong
+stride order, a transposed operand, a dropped rounding, ties away from zero instead of to even,
+the wrong quantization axis -- fails at least one of them.
+"""
+
+import itertools
+import math
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import load_golden
+
+getcontext().prec = 80
+
+
+# ---------------------------------------------------------------------------------------------
+# helpers (test-side, independent of the oracle): logical <-> physical buffers via numpy
+# ---------------------------------------------------------------------------------------------
+def to_physical(arr, m2m):
+    order = list(reversed(m2m))  # major -> minor
+    return np.ascontiguousarray(np.transpose(arr, order)).ravel()
+
+
+def from_physical(buf, dims, m2m):
+    order = list(reversed(m2m))
+    phys = np.asarray(buf).reshape([dims[d] for d in order])
+    return np.transpose(phys, np.argsort(order))
+
+
+def all_layouts(rank):
+    return [list(p) for p in itertools.permutations(range(rank))]
+
+
+def f32_neighbors(y):
+    y = np.float32(y)
+    return np.nextafter(y, np.float32(-np.inf)), np.nextafter(y, np.float32(np.inf))
+
+
+def exact_between_midpoints(exact: Decimal, y: float, lo: float, hi: float) -> bool:
+    """True if `exact` lies strictly inside the rounding interval of y (between the midpoints to its
+    neighbours lo and hi); midpoints are computed exactly in Decimal."""
+    y, lo, hi = Decimal(float(y)), Decimal(float(lo)), Decimal(float(hi))
+    return (y + lo) / 2 < exact < (y + hi) / 2
+
+
+# ---------------------------------------------------------------------------------------------
+# layout addressing (XLA Shapes and Layout, "Layout")
+# ---------------------------------------------------------------------------------------------
+def test_layout_2x3_memory_orders(orc):
+    g = load_golden("layout_2x3.txt")
+    letters = g["logical"][0] + g["logical"][1]
+    logical = np.arange(6, dtype=np.int8)  # a..f in row order: a=0 ... f=5
+    for key, memory in g["memory"].items():
+        m2m = [int(v) for v in key.split(",")]
+        # offsets of each logical element
+        mem = [None] * 6
+        for i in range(2):
+            for j in range(3):
+                mem[orc.linear_offset(g["dims"], m2m, [i, j])] = g["logical"][i][j]
+        assert mem == memory
+        # and the same through a layout conversion of the row-major buffer
+        out = orc.layout_convert(logical, g["dims"], "s8", [1, 0], m2m)
+        assert [letters[v] for v in out] == memory
+
+
+def test_default_layout_is_major_to_minor(orc):
+    g = load_golden("layout_2x3.txt")
+    assert orc.default_m2m(3) == g["default_m2m_rank3"]
+
+
+@pytest.mark.parametrize("dims", [[3, 4, 5], [2, 1, 3, 2], [5, 7]])
+def test_linear_offset_matches_numpy_strides(orc, dims):
+    for m2m in all_layouts(len(dims)):
+        order = list(reversed(m2m))
+        phys_shape = [dims[d] for d in order]
+        for idx in itertools.product(*[range(d) for d in dims]):
+            want = np.ravel_multi_index(tuple(idx[d] for d in order), phys_shape)
+            assert orc.linear_offset(dims, m2m, idx) == want
+
+
+def test_layout_convert_roundtrip_and_numpy(orc):
+    g = np.random.default_rng(5)
+    dims = [3, 5, 4]
+    logical = g.integers(-100, 100, size=dims).astype(np.int8)
+    for a in all_layouts(3):
+        buf_a = to_physical(logical, a)
+        for b in all_layouts(3):
+            out = orc.layout_convert(buf_a, dims, "s8", a, b)
+            assert np.array_equal(out, to_physical(logical, b))
+            back = orc.layout_convert(out, dims, "s8", b, a)
+            assert np.array_equal(back, buf_a)
+
+
+def test_layout_convert_sizes_zero_and_one(orc):
+    assert orc.layout_convert(np.zeros(0, np.float32), [0, 3], "f32", [1, 0], [0, 1]).size == 0
+    x = np.arange(5, dtype=np.float32)
+    assert np.array_equal(orc.layout_convert(x, [1, 5], "f32", [1, 0], [0, 1]), x)
+
+
+# ---------------------------------------------------------------------------------------------
+# transpose (XLA:GPU Emitters, "Indexing transformations" / "Transpose emitter")
+# ---------------------------------------------------------------------------------------------
+def test_transpose_map_20x40(orc):
+    g = load_golden("transpose_maps.txt")["map_2d"]
+    x = np.arange(20 * 40, dtype=np.float32)  # in[d1', d0'] = 40*d1' + d0'
+    out = orc.transpose(x, g["in_dims"], "f32", g["permutation"]).reshape(g["out_dims"])
+    for d0 in range(40):
+        for d1 in range(20):
+            assert out[d0, d1] == x[d1 * 40 + d0]  # output (d0, d1) reads input (d1, d0)
+
+
+def test_transpose_emitter_example_exp_abs(orc):
+    g = load_golden("transpose_maps.txt")["emitter_3d"]
+    rng = np.random.default_rng(3)
+    dims = g["in_dims"]
+    x = rng.uniform(-3, 3, size=int(np.prod(dims))).astype(np.float32)
+    out = orc.transpose(x, dims, "f32", g["permutation"], prologue={"ops": ["exp"]},
+                        epilogue={"ops": ["abs"]}).reshape(g["out_dims"])
+    xl = x.reshape(dims)
+    # exact exp rounded to f32 checked on a sample through Decimal
+    for (i, j, k) in [(0, 0, 0), (19, 159, 169), (7, 80, 3), (11, 2, 150)]:
+        v = float(xl[i, j, k])
+        y = float(out[k, j, i])
+        lo, hi = f32_neighbors(y)
+        assert exact_between_midpoints(Decimal(v).exp(), y, lo, hi)
+    # the whole mapping: out[k, j, i] == |f32(exp(x[i, j, k]))| within 1 ulp of numpy's exp
+    ref = np.abs(np.exp(xl.astype(np.float64)).astype(np.float32)).transpose(2, 1, 0)
+    assert np.array_equal(out.shape, ref.shape)
+    assert np.max(np.abs(out.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))) <= 1
+
+
+@pytest.mark.parametrize("rank", [1, 2, 3, 4])
+def test_transpose_all_permutations_vs_numpy(orc, rank):
+    rng = np.random.default_rng(rank)
+    dims = [2, 3, 4, 5][:rank]
+    logical = rng.integers(-1000, 1000, size=dims).astype(np.float32)
+    layouts = all_layouts(rank)
+    for perm in itertools.permutations(range(rank)):
+        out_dims = [dims[p] for p in perm]
+        in_m2m = layouts[(sum(perm) + 1) % len(layouts)]
+        out_m2m = layouts[(perm[0] + 2) % len(layouts)]
+        buf = to_physical(logical, in_m2m)
+        out = orc.transpose(buf, dims, "f32", list(perm), m2m=in_m2m, out_m2m=out_m2m,
+                            prologue={"ops": ["neg"]})
+        want = -np.transpose(logical, perm)
+        assert np.array_equal(from_physical(out, out_dims, out_m2m), want)
+
+
+def test_transpose_self_add(orc):
+    rng = np.random.default_rng(7)
+    n = 9
+    x = rng.uniform(-5, 5, size=(n, n)).astype(np.float32)
+    out = orc.transpose(x.ravel(), [n, n], "f32", [1, 0], self_add=True,
+                        prologue={"ops": ["abs"]}).reshape(n, n)
+    want = (np.abs(x).astype(np.float64) + np.abs(x).T.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(out, want)
+
+
+def test_transpose_self_add_log_symmetric_and_correct(orc):
+    rng = np.random.default_rng(11)
+    n = 17
+    p = rng.uniform(0.5, 2.0, size=n * n).astype(np.float32)
+    out = orc.transpose(p, [n, n], "f32", [1, 0], self_add=True, prologue={"ops": ["log"]}).reshape(n, n)
+    assert np.array_equal(out.view(np.uint32), out.T.view(np.uint32))  # bitwise symmetric
+    P = p.reshape(n, n)
+    for i, j in [(0, 0), (3, 5), (16, 2)]:
+        li, lj = orc.log(P[i, j], "f32"), orc.log(P[j, i], "f32")
+        assert out[i, j] == np.float32(np.float64(li) + np.float64(lj))
+
+
+# ---------------------------------------------------------------------------------------------
+# reduce (StableHLO Specification "reduce"; XLA Operation Semantics "Reduce")
+# ---------------------------------------------------------------------------------------------
+def test_reduce_spec_example(orc):
+    g = load_golden("reduce_examples.txt")["spec"]
+    x = np.array(g["input"], dtype=np.float32).ravel()
+    out = orc.reduce(x, [1, 6], "f32", g["dimensions"], "add", g["init"], "f32")
+    assert out.tolist() == g["result"]
+
+
+@pytest.mark.parametrize("m2m", all_layouts(3))
+def test_reduce_xla_3d_examples(orc, m2m):
+    g = load_golden("reduce_examples.txt")["xla_3d"]
+    logical = np.array([g["slab"]] * g["replicas"], dtype=np.float32)  # [4, 2, 3]
+    buf = to_physical(logical, m2m)
+    for case in g["cases"]:
+        out = orc.reduce(buf, [4, 2, 3], "f32", case["dimensions"], "add", 0.0, "f32", m2m=m2m)
+        want = np.array(case["result"], dtype=np.float32).ravel()
+        assert np.array_equal(out, want), (case, m2m)
+
+
+def test_reduce_closed_forms(orc):
+    n = 1000
+    iota = np.arange(n, dtype=np.float32)
+    assert orc.reduce(iota, [n], "f32", [0], "add", 0.0, "f32")[0] == n * (n - 1) / 2
+    assert orc.reduce(iota, [n], "f32", [0], "max", -np.inf, "f32")[0] == n - 1
+    assert orc.reduce(np.ones(n, np.float32), [n], "f32", [0], "add", 3.0, "f32")[0] == n + 3  # init once
+    # empty reduced dimension: the init value
+    assert orc.reduce(np.zeros(0, np.float32), [0], "f32", [0], "add", 2.5, "f32")[0] == 2.5
+    assert orc.reduce(np.zeros(0, np.float32), [4, 0], "f32", [1], "max", -np.inf, "f32").tolist() == [-np.inf] * 4
+
+
+@pytest.mark.parametrize("kind", ["add", "max"])
+def test_reduce_brute_force_vs_numpy(orc, kind):
+    rng = np.random.default_rng(13)
+    dims = [3, 4, 5]
+    logical = rng.standard_normal(dims).astype(np.float32)
+    for m2m in all_layouts(3):
+        buf = to_physical(logical, m2m)
+        for r in range(1, 4):
+            for red in itertools.combinations(range(3), r):
+                kept = [d for d in range(3) if d not in red]
+                out_m2m = orc.default_m2m(len(kept))
+                init = 0.0 if kind == "add" else -np.inf
+                out = orc.reduce(buf, dims, "f32", list(red), kind, init, "f64", m2m=m2m)
+                if kind == "add":
+                    want = logical.astype(np.float64).sum(axis=red)
+                    assert np.allclose(out, np.ravel(want), rtol=1e-15, atol=1e-15)
+                else:
+                    want = logical.max(axis=red).astype(np.float64)
+                    assert np.array_equal(out, np.ravel(want))
+                del out_m2m
+
+
+def test_reduce_output_layout(orc):
+    rng = np.random.default_rng(17)
+    dims = [4, 6, 5]
+    logical = rng.integers(-9, 9, size=dims).astype(np.float32)
+    want = logical.sum(axis=1)  # [4, 5]
+    for out_m2m in ([1, 0], [0, 1]):
+        out = orc.reduce(logical.ravel(), dims, "f32", [1], "add", 0.0, "f32", out_m2m=out_m2m)
+        assert np.array_equal(from_physical(out, [4, 5], out_m2m), want)
+
+
+def test_maximum_semantics(orc):
+    g = load_golden("elementwise_examples.txt")["maximum"]
+    for a, b, c in zip(np.ravel(g["lhs"]), np.ravel(g["rhs"]), np.ravel(g["result"])):
+        assert orc.maximum(a, b) == c
+    assert math.isnan(orc.maximum(float("nan"), 1.0)) and math.isnan(orc.maximum(1.0, float("nan")))
+    assert math.copysign(1.0, orc.maximum(-0.0, 0.0)) == 1.0
+    assert math.copysign(1.0, orc.maximum(0.0, -0.0)) == 1.0
+    # a NaN anywhere in a reduced column propagates
+    x = np.array([1.0, np.nan, 3.0, 2.0], dtype=np.float32)
+    assert math.isnan(orc.reduce(x, [4], "f32", [0], "max", -np.inf, "f32")[0])
+    x = np.array([-0.0, 0.0, -0.0], dtype=np.float32)
+    r = orc.reduce(x, [3], "f32", [0], "max", -np.inf, "f32")[0]
+    assert r == 0 and not np.signbit(r)
+
+
+def test_max_reduce_to_bf16_is_exact_member(orc):
+    import transpose_heroes_gb300.inputs as inp
+
+    rng = inp.rng(2)
+    x = inp.normal_bf16(rng, 64 * 33)
+    out = orc.reduce(x, [64, 33], "bf16", [0], "max", -np.inf, "bf16")
+    xf = inp.bf16_bits_to_f32(x).reshape(64, 33)
+    assert np.array_equal(inp.bf16_bits_to_f32(out), xf.max(axis=0))
+
+
+# ---------------------------------------------------------------------------------------------
+# broadcast_in_dim and add
+# ---------------------------------------------------------------------------------------------
+def test_broadcast_in_dim_example(orc):
+    g = load_golden("broadcast_example.txt")
+    out = orc.broadcast_in_dim(np.array(g["operand"], np.int32).ravel(), g["operand_dims"], "s32",
+                               g["broadcast_dimensions"], g["result_dims"])
+    assert out.reshape(g["result_dims"]).tolist() == g["result"]
+
+
+def test_add_example_through_broadcast_operand(orc):
+    g = load_golden("elementwise_examples.txt")["add"]
+    lhs = np.array(g["lhs"], np.float32).ravel()
+    rhs = np.array(g["rhs"], np.float32).ravel()
+    chain = {"ops": ["add_bcast"], "bcast": {"data": rhs, "dims": [2, 2], "dtype": "f32",
+                                             "broadcast_dimensions": [0, 1]}}
+    out = orc.transpose(lhs, [2, 2], "f32", [0, 1], prologue=chain)
+    assert out.reshape(2, 2).tolist() == g["result"]
+
+
+def test_bcast_on_reduced_dim_with_layout(orc):
+    # add(x, broadcast(b, {3})) reduced over dim 3, with the {3,2,0,1} layout: compared against numpy
+    import transpose_heroes_gb300.inputs as inp
+
+    rng = np.random.default_rng(23)
+    dims = [2, 1, 3, 7]
+    logical = rng.integers(-4, 4, size=dims).astype(np.float32)
+    b = rng.integers(-4, 4, size=7).astype(np.float32)
+    m2m = [3, 2, 0, 1]
+    chain = {"ops": ["add_bcast"], "bcast": {"data": b, "dims": [7], "dtype": "f32", "broadcast_dimensions": [3]}}
+    out = orc.reduce(to_physical(logical, m2m), dims, "f32", [3], "add", 0.0, "f32", m2m=m2m, prologue=chain)
+    want = (logical + b.reshape(1, 1, 1, 7)).sum(axis=3)
+    assert np.array_equal(out, want.ravel())
+    del inp
+
+
+# ---------------------------------------------------------------------------------------------
+# exp / log: the spec's printed values, and correct rounding checked exactly with Decimal
+# ---------------------------------------------------------------------------------------------
+def test_exp_log_printed_values(orc):
+    g = load_golden("elementwise_examples.txt")
+    for x, y in zip(g["exp"]["x"], g["exp"]["y"]):
+        assert orc.exp(x, "f64") == y
+        assert orc.exp(x, "f32") == float(np.float32(y))
+    for x, y in zip(g["log"]["x"], g["log"]["y"]):
+        assert orc.log(x, "f64") == y
+        assert orc.log(x, "f32") == float(np.float32(y))
+
+
+def test_log_f32_correctly_rounded_vs_decimal(orc):
+    rng = np.random.default_rng(29)
+    xs = np.concatenate([rng.uniform(0.5, 2.0, 400), np.exp(rng.uniform(-80, 80, 200)),
+                         1.0 + rng.uniform(-1e-3, 1e-3, 100)]).astype(np.float32)
+    for x in xs:
+        y = orc.log(float(x), "f32")
+        lo, hi = f32_neighbors(y)
+        assert exact_between_midpoints(Decimal(float(x)).ln(), y, lo, hi), x
+    assert orc.log(1.0, "f32") == 0.0
+    assert orc.log(0.0, "f32") == -math.inf
+    assert math.isnan(orc.log(-1.0, "f32"))
+    assert orc.log(math.inf, "f32") == math.inf
+
+
+def test_exp_f32_and_bf16_correctly_rounded_vs_decimal(orc):
+    import transpose_heroes_gb300.inputs as inp
+
+    rng = np.random.default_rng(31)
+    xs = rng.uniform(-20, 20, 300).astype(np.float32)
+    for x in xs:
+        y = orc.exp(float(x), "f32")
+        lo, hi = f32_neighbors(y)
+        assert exact_between_midpoints(Decimal(float(x)).exp(), y, lo, hi), x
+    # every bf16 input in [-8, 8]: exp rounded straight to bf16
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = inp.bf16_bits_to_f32(bits)
+    sel = np.isfinite(vals) & (np.abs(vals) <= 8)
+    for x in vals[sel][::7]:
+        y = orc.exp(float(x), "bf16")
+        q = 2.0 ** (math.frexp(y)[1] - 8)  # bf16 quantum at y
+        assert exact_between_midpoints(Decimal(float(x)).exp(), y, y - q if y != 2.0 ** (math.frexp(y)[1] - 1) else y - q / 2, y + q), x
+
+
+def test_round_to_bf16_is_nearest_even(orc):
+    rng = np.random.default_rng(37)
+    for v in np.concatenate([rng.standard_normal(500) * 10, [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8)]]):
+        r = orc.round_to(float(v), "bf16")
+        e = math.frexp(v)[1]
+        q = Fraction(2) ** (e - 8)
+        fv = Fraction(float(v))
+        lo = (fv / q).__floor__() * q
+        cands = [lo, lo + q]
+        dist = [abs(fv - c) for c in cands]
+        if dist[0] == dist[1]:  # tie: even significand
+            want = cands[0] if (lo / q) % 2 == 0 else cands[1]
+        else:
+            want = cands[int(dist[1] < dist[0])]
+        assert Fraction(r) == want, v
+
+
+def test_bf16_spec_chain_terms(orc):
+    """exp then add of a broadcast, each rounded to bf16 (the spec's types), summed exactly."""
+    import transpose_heroes_gb300.inputs as inp
+
+    rng = inp.rng(41)
+    n = 257
+    x = inp.normal_bf16(rng, n)
+    b = inp.uniform_bf16(rng, n, -1, 1)
+    chain = {"ops": ["exp", "add_bcast"], "round_each": True,
+             "bcast": {"data": b, "dims": [n], "dtype": "bf16", "broadcast_dimensions": [1]}}
+    out, asum = orc.reduce(x, [1, n], "bf16", [1], "add", 0.0, "f64", prologue=chain, want_abs_sum=True)
+    xf, bf = inp.bf16_bits_to_f32(x), inp.bf16_bits_to_f32(b)
+
+    def rn_bf16(fr: Fraction) -> Fraction:
+        if fr == 0:
+            return fr
+        e = math.frexp(float(fr))[1]
+        q = Fraction(2) ** (e - 8)
+        lo = (fr / q).__floor__() * q
+        d0, d1 = fr - lo, lo + q - fr
+        if d0 == d1:
+            return lo if (lo / q) % 2 == 0 else lo + q
+        return lo if d0 < d1 else lo + q
+
+    total = Fraction(0)
+    for xi, bi in zip(xf, bf):
+        e = Fraction(Decimal(float(xi)).exp())
+        t = rn_bf16(rn_bf16(e) + Fraction(float(bi)))
+        total += t
+    assert out[0] == float(total)  # f64 output of an exact-enough long-double sum of bf16 terms
+
+
+# ---------------------------------------------------------------------------------------------
+# rounding and clamping as used by quantize
+# ---------------------------------------------------------------------------------------------
+def test_round_nearest_even_example(orc):
+    g = load_golden("rounding_clamp_examples.txt")
+    q = {"scales": [1.0], "zero_points": [0], "storage_min": -128, "storage_max": 127}
+    got = [orc.quantize(q, x) for x in g["round_nearest_even"]["x"]]
+    assert got == g["round_nearest_even"]["y"]
+    assert got != g["round_nearest_afz"]["y"]
+
+
+def test_clamp_example(orc):
+    g = load_golden("rounding_clamp_examples.txt")["clamp"]
+    got = []
+    for lo, x, hi in zip(g["min"], g["operand"], g["max"]):
+        q = {"scales": [1.0], "zero_points": [lo], "storage_min": lo, "storage_max": hi}
+        got.append(orc.quantize(q, float(x - lo)))  # zero point lo: code = clamp(x - lo + lo)
+    assert got == g["result"]
+
+
+# ---------------------------------------------------------------------------------------------
+# quantization (StableHLO Quantization; spec "Types")
+# ---------------------------------------------------------------------------------------------
+def test_per_tensor_example(orc):
+    g = load_golden("quant_examples.txt")["per_tensor"]
+    q = {"scales": [g["scale"]], "zero_points": [g["zero_point"]]}
+    assert orc.dequantize(q, g["zero_code"]) == 0.0
+    assert orc.quantize(q, 0.0) == g["zero_code"]
+    assert orc.dequantize(q, g["zero_code"] - 100) == -1.0
+    assert orc.quantize(q, -1.0) == g["zero_code"] - 100
+    assert orc.quantize(q, 0.5) == g["zero_code"] + 50
+    assert orc.quantize(q, 100.0) == 127 and orc.quantize(q, -100.0) == -128  # saturation
+
+
+def test_per_axis_example_slices(orc):
+    g = load_golden("quant_examples.txt")["per_axis"]
+    dims, ax = g["dims"], g["quantization_dimension"]
+    zps = np.array(g["zero_points"], np.int32)
+    codes = np.zeros(dims, np.int8)
+    for i in range(dims[ax]):
+        codes[:, i, :] = zps[i] + 5
+    spec = {"scales": np.array(g["scales"], np.float32), "zero_points": zps, "quantization_dimension": ax}
+    real = orc.quant_fusion(codes.ravel(), dims, "s8", spec, [2, 1, 0], "f32").reshape(dims)
+    # 5 * f32(0.2) = 1.0, 5 * f32(0.1) = 0.5, 5 * f32(0.3) = 1.5 (an exact tie, rounded to even)
+    for i, want in enumerate([1.0, 0.5, 1.5]):
+        assert np.all(real[:, i, :] == want)
+    # each slice uses its own zero point: codes equal to the zero point give 0
+    for i in range(dims[ax]):
+        codes[:, i, :] = zps[i]
+    real = orc.quant_fusion(codes.ravel(), dims, "s8", spec, [2, 1, 0], "f32")
+    assert np.all(real == 0.0)
+
+
+def test_dequant_quant_identity_all_codes(orc):
+    rng = np.random.default_rng(43)
+    for _ in range(20):
+        s = float(np.float32(rng.uniform(0.001, 0.5)))
+        z = int(rng.integers(-20, 21))
+        q = {"scales": [s], "zero_points": [z]}
+        for code in range(-128, 128):
+            assert orc.quantize(q, orc.dequantize(q, code)) == code
+
+
+def test_quant_fusion_relayout_vs_numpy(orc):
+    import transpose_heroes_gb300.inputs as inp
+
+    f = inp.small("quant_relayout", n0=37, n1=29)
+    out = orc.quant_fusion(f.data, f.dims, "s8", f.in_q, f.out_m2m, "s8", out_q=f.out_q)
+    q = f.data.reshape(f.dims).astype(np.int32)
+    sc, zp = f.in_q["scales"], f.in_q["zero_points"]
+    real = (sc[None, :] * (q - zp[None, :]).astype(np.float32)).astype(np.float32)  # f32 multiply
+    ratio = (real / np.float32(0.05)).astype(np.float32)                               # f32 divide
+    want = np.clip(np.rint(ratio), -128, 127).astype(np.int8)                          # ties to even
+    assert np.array_equal(from_physical(out, f.dims, f.out_m2m), want)
