@@ -27,8 +27,8 @@
 //     storage_min, storage_max) in the expressed type f32.
 //
 // Floating point: reductions accumulate in f64; elementwise ops are evaluated in f64 (or long double
-// where the f64 value lies too close to a rounding boundary of the element type) and rounded once to
-// the element type; the quantization chain is evaluated in f32 IEEE operations because its expressed
+// where the f64 value lies within 2^-50 relative of a rounding boundary of the element type) and
+// rounded once to the element type; the quantization chain is evaluated in f32 IEEE operations because its expressed
 // type is f32. Build with -O2 -fno-fast-math -ffp-contract=off so that no operation is contracted.
 //
 // Parallelism: OpenMP over independent output elements only; no cross-thread reduction, so results do
@@ -45,7 +45,7 @@
 #include <omp.h>
 #endif
 
-extern "C" {
+// Exported functions carry extern "C"; everything else has internal linkage.
 
 // ----------------------------------------------------------------------------------------------
 // Descriptors (the oracle's own; plain C layout, mirrored by oracle/__init__.py with ctypes).
@@ -131,7 +131,7 @@ static bool valid_arr(const orc_arr* a) {
 }
 
 // Linear offset (in elements) of logical index idx in array a.
-int orc_linear_offset(const orc_arr* a, const int64_t* idx, int64_t* out) {
+extern "C" int orc_linear_offset(const orc_arr* a, const int64_t* idx, int64_t* out) {
   if (!valid_arr(a)) return ORC_EINVAL;
   int64_t stride[ORC_MAX_RANK];
   strides_of(a, stride);
@@ -157,17 +157,18 @@ static void lex_index(int rank, const int64_t* dims, int64_t n, int64_t* idx) {
 // Rounding to a binary floating-point format with round-to-nearest, ties to even.
 // prec = significand bits (24 for f32, 8 for bf16, 11 for f16), emin/emax = exponent range.
 // ----------------------------------------------------------------------------------------------
-static long double round_to_format(long double v, int prec, int emin, int emax) {
+template <typename T>
+static T round_to_format(T v, int prec, int emin, int emax) {
   if (v == 0 || std::isnan(v) || std::isinf(v)) return v;
   int e;
   std::frexp(v, &e);            // v = f * 2^e, 0.5 <= |f| < 1, so the leading bit has weight 2^(e-1)
   int lead = e - 1;
   if (lead < emin) lead = emin;  // gradual underflow: fixed quantum below the normal range
-  long double quantum = std::ldexp((long double)1, lead - prec + 1);
-  long double scaled = v / quantum;          // exact: division by a power of two
-  long double r = std::nearbyint(scaled);    // default rounding mode: ties to even
-  long double out = r * quantum;
-  long double maxv = std::ldexp((long double)1, emax) * (2 - std::ldexp((long double)1, 1 - prec));
+  T quantum = std::ldexp((T)1, lead - prec + 1);
+  T scaled = v / quantum;          // exact: division by a power of two
+  T r = std::nearbyint(scaled);    // default rounding mode: ties to even
+  T out = r * quantum;
+  T maxv = std::ldexp((T)1, emax) * (2 - std::ldexp((T)1, 1 - prec));
   if (std::fabs(out) > maxv) return v > 0 ? INFINITY : -INFINITY;
   return out;
 }
@@ -175,26 +176,28 @@ static long double round_to_format(long double v, int prec, int emin, int emax) 
 // Distance-to-boundary test: true when v lies within rel*|v| of a rounding boundary (a midpoint
 // between two neighbours) of the format, so that an approximation of v with that relative error
 // could round either way.
-static bool near_boundary(long double v, int prec, int emin, long double rel) {
+template <typename T>
+static bool near_boundary(T v, int prec, int emin, T rel) {
   if (v == 0 || std::isnan(v) || std::isinf(v)) return false;
   int e;
   std::frexp(v, &e);
   int lead = e - 1;
   if (lead < emin) lead = emin;
-  long double quantum = std::ldexp((long double)1, lead - prec + 1);
-  long double scaled = v / quantum;
-  long double frac = scaled - std::floor(scaled);  // position between two representable neighbours
-  long double tol = std::fabs(v) * rel / quantum + std::ldexp((long double)1, -60);
-  return std::fabs(frac - 0.5L) <= tol;
+  T quantum = std::ldexp((T)1, lead - prec + 1);
+  T scaled = v / quantum;                 // exact
+  T frac = scaled - std::floor(scaled);   // position between two representable neighbours (exact)
+  T tol = std::fabs(v) * rel / quantum;
+  return std::fabs(frac - (T)0.5) <= tol;
 }
 
 static int prec_of(int dt) { return dt == ORC_BF16 ? 8 : dt == ORC_F16 ? 11 : dt == ORC_F64 ? 53 : 24; }
 static int emin_of(int dt) { return dt == ORC_F16 ? -14 : dt == ORC_F64 ? -1022 : -126; }
 static int emax_of(int dt) { return dt == ORC_F16 ? 15 : dt == ORC_F64 ? 1023 : 127; }
 
-static long double round_to(long double v, int dt) {
-  if (dt == ORC_F64) return (double)v;
-  return round_to_format(v, prec_of(dt), emin_of(dt), emax_of(dt));
+template <typename T>
+static T round_to(T v, int dt) {
+  if (dt == ORC_F64) return (T)(double)v;
+  return round_to_format<T>(v, prec_of(dt), emin_of(dt), emax_of(dt));
 }
 
 // Elements that could not be rounded with certainty even in long double are counted here.
@@ -202,39 +205,39 @@ static int g_unresolved = 0;
 
 // Correctly rounded exp / log into format dt. The f64 libm value (error well under one f64 ulp) is
 // trusted unless it lies close to a rounding boundary of dt; then long double decides.
-static long double cr_exp(long double x, int dt) {
-  double d = std::exp((double)x);
-  if (!near_boundary(d, prec_of(dt), emin_of(dt), std::ldexp(1.0L, -50))) return round_to(d, dt);
-  long double l = std::exp(x);
-  if (near_boundary(l, prec_of(dt), emin_of(dt), std::ldexp(1.0L, -60))) {
+static double cr_exp(double x, int dt) {
+  double d = std::exp(x);
+  if (!near_boundary<double>(d, prec_of(dt), emin_of(dt), std::ldexp(1.0, -50))) return round_to<double>(d, dt);
+  long double l = std::exp((long double)x);
+  if (near_boundary<long double>(l, prec_of(dt), emin_of(dt), std::ldexp(1.0L, -60))) {
 #pragma omp atomic
     g_unresolved++;
   }
-  return round_to(l, dt);
+  return (double)round_to<long double>(l, dt);
 }
 
-static long double cr_log(long double x, int dt) {
+static double cr_log(double x, int dt) {
   if (std::isnan(x)) return x;
   if (x < 0) return NAN;                 // IEEE log of a negative number: invalid
   if (x == 0) return -INFINITY;          // log(+-0) = -inf
   if (std::isinf(x)) return INFINITY;
-  double d = std::log((double)x);
-  if (!near_boundary(d, prec_of(dt), emin_of(dt), std::ldexp(1.0L, -50))) return round_to(d, dt);
-  long double l = std::log(x);
-  if (near_boundary(l, prec_of(dt), emin_of(dt), std::ldexp(1.0L, -60))) {
+  double d = std::log(x);
+  if (!near_boundary<double>(d, prec_of(dt), emin_of(dt), std::ldexp(1.0, -50))) return round_to<double>(d, dt);
+  long double l = std::log((long double)x);
+  if (near_boundary<long double>(l, prec_of(dt), emin_of(dt), std::ldexp(1.0L, -60))) {
 #pragma omp atomic
     g_unresolved++;
   }
-  return round_to(l, dt);
+  return (double)round_to<long double>(l, dt);
 }
 
-int orc_unresolved_count(void) { return g_unresolved; }
-void orc_reset_unresolved(void) { g_unresolved = 0; }
+extern "C" int orc_unresolved_count(void) { return g_unresolved; }
+extern "C" void orc_reset_unresolved(void) { g_unresolved = 0; }
 
 // ----------------------------------------------------------------------------------------------
 // Element loads and stores.
 // ----------------------------------------------------------------------------------------------
-static long double load_elem(const void* base, int dt, int64_t off) {
+static double load_elem(const void* base, int dt, int64_t off) {
   switch (dt) {
     case ORC_F32: { float v; std::memcpy(&v, (const char*)base + off * 4, 4); return v; }
     case ORC_F64: { double v; std::memcpy(&v, (const char*)base + off * 8, 8); return v; }
@@ -245,21 +248,21 @@ static long double load_elem(const void* base, int dt, int64_t off) {
     case ORC_F16: {
       uint16_t h; std::memcpy(&h, (const char*)base + off * 2, 2);
       int sign = h >> 15, ex = (h >> 10) & 31, man = h & 1023;
-      long double v;
-      if (ex == 0) v = std::ldexp((long double)man, -24);
+      double v;
+      if (ex == 0) v = std::ldexp((double)man, -24);
       else if (ex == 31) v = man ? NAN : INFINITY;
-      else v = std::ldexp((long double)(man + 1024), ex - 25);
+      else v = std::ldexp((double)(man + 1024), ex - 25);
       return sign ? -v : v;
     }
-    case ORC_S8: return (long double)((const int8_t*)base)[off];
-    case ORC_U8: return (long double)((const uint8_t*)base)[off];
-    case ORC_S32: return (long double)((const int32_t*)base)[off];
+    case ORC_S8: return (double)((const int8_t*)base)[off];
+    case ORC_U8: return (double)((const uint8_t*)base)[off];
+    case ORC_S32: return (double)((const int32_t*)base)[off];
   }
   return 0;
 }
 
 // Stores v, which must already be representable in dt (callers round first).
-static void store_elem(void* base, int dt, int64_t off, long double v) {
+static void store_elem(void* base, int dt, int64_t off, double v) {
   switch (dt) {
     case ORC_F32: { float f = (float)v; std::memcpy((char*)base + off * 4, &f, 4); return; }
     case ORC_F64: { double f = (double)v; std::memcpy((char*)base + off * 8, &f, 8); return; }
@@ -274,10 +277,10 @@ static void store_elem(void* base, int dt, int64_t off, long double v) {
       if (std::isnan(v)) h = 0x7E00;
       else {
         int sign = std::signbit(v) ? 1 : 0;
-        long double a = std::fabs(v);
+        double a = std::fabs(v);
         if (std::isinf(a)) h = 0x7C00;
-        else if (a < std::ldexp(1.0L, -14)) h = (uint16_t)(long)(a * std::ldexp(1.0L, 24));
-        else { int e; long double m = std::frexp(a, &e); h = (uint16_t)(((e + 14) << 10) | ((long)(m * 2048) - 1024)); }
+        else if (a < std::ldexp(1.0, -14)) h = (uint16_t)(long)(a * std::ldexp(1.0, 24));
+        else { int e; double m = std::frexp(a, &e); h = (uint16_t)(((e + 14) << 10) | ((long)(m * 2048) - 1024)); }
         h |= (uint16_t)(sign << 15);
       }
       std::memcpy((char*)base + off * 2, &h, 2); return;
@@ -303,7 +306,7 @@ static int64_t bcast_offset(const orc_chain* c, const int64_t* result_index) {
 }
 
 // Materialises broadcast_in_dim(operand) into result (both described by layouts), for pinning.
-int orc_broadcast_in_dim(const orc_arr* operand, const void* operand_data,
+extern "C" int orc_broadcast_in_dim(const orc_arr* operand, const void* operand_data,
                          const int64_t* broadcast_dimensions, const orc_arr* result, void* result_data) {
   if (!valid_arr(operand) || !valid_arr(result) || operand->dtype != result->dtype) return ORC_EINVAL;
   for (int d = 0; d < operand->rank; ++d) {
@@ -340,7 +343,7 @@ static int working_type(const orc_chain* c, int dt) {
   return (dt == ORC_BF16 || dt == ORC_F16) ? ORC_F32 : dt;
 }
 
-static long double apply_chain(const orc_chain* c, long double v, int dt, const int64_t* index) {
+static double apply_chain(const orc_chain* c, double v, int dt, const int64_t* index) {
   if (!c) return v;
   int wt = working_type(c, dt);
   for (int k = 0; k < c->n_ops; ++k) {
@@ -350,8 +353,9 @@ static long double apply_chain(const orc_chain* c, long double v, int dt, const 
       case ORC_OP_ABS: v = std::fabs(v); break;
       case ORC_OP_NEG: v = -v; break;
       case ORC_OP_ADD_BCAST: {
-        long double b = load_elem(c->bcast_data, c->bcast.dtype, bcast_offset(c, index));
-        v = round_to(v + b, wt);  // exact sum of two short floats in long double, rounded once
+        double b = load_elem(c->bcast_data, c->bcast.dtype, bcast_offset(c, index));
+        v = round_to<double>(v + b, wt);  // f64 sum of two short floats, then the element type: the
+                                          // double rounding is innocuous (53 >= 2 * 24 + 2)
         break;
       }
       default: break;
@@ -381,16 +385,15 @@ static bool valid_chain(const orc_chain* c, const orc_arr* fused) {
 // ----------------------------------------------------------------------------------------------
 // reduce ("StableHLO Specification", section "reduce"; "XLA Operation Semantics", section "Reduce").
 // out[j] = init (+) term(slice_j[0]) (+) term(slice_j[1]) (+) ... in lexicographic slice order,
-// accumulated in long double for add (exact enough to be the reference sum) and with IEEE maximum
-// for max. abs_sum (optional) receives sum |term| per output element, used by the tolerance.
+// accumulated in f64 for add and with IEEE maximum for max. abs_sum (optional) receives sum |term| per output element, used by the tolerance.
 // ----------------------------------------------------------------------------------------------
-static long double ieee_maximum(long double a, long double b) {
+static double ieee_maximum(double a, double b) {
   if (std::isnan(a) || std::isnan(b)) return NAN;
   if (a == 0 && b == 0) return std::signbit(a) ? b : a;  // maximum(-0, +0) = +0
   return a > b ? a : b;
 }
 
-int orc_reduce(const orc_arr* in, const void* in_data, const orc_chain* chain,
+extern "C" int orc_reduce(const orc_arr* in, const void* in_data, const orc_chain* chain,
                const int64_t* dimensions, int n_dimensions, int kind, double init,
                const orc_arr* out, void* out_data, double* abs_sum) {
   if (!valid_arr(in) || !valid_arr(out) || !valid_chain(chain, in)) return ORC_EINVAL;
@@ -424,20 +427,20 @@ int orc_reduce(const orc_arr* in, const void* in_data, const orc_chain* chain,
     int64_t kidx[ORC_MAX_RANK], ridx[ORC_MAX_RANK], full[ORC_MAX_RANK];
     lex_index(nk, kdims, o, kidx);
     for (int k = 0; k < nk; ++k) full[kept[k]] = kidx[k];
-    long double acc = init, asum = 0;
+    double acc = init, asum = 0;
     for (int64_t t = 0; t < n_red; ++t) {
       lex_index(nr, rdims, t, ridx);
       for (int k = 0; k < nr; ++k) full[red[k]] = ridx[k];
       int64_t off = 0;
       for (int d = 0; d < in->rank; ++d) off += full[d] * istride[d];
-      long double v = apply_chain(chain, load_elem(in_data, in->dtype, off), in->dtype, full);
+      double v = apply_chain(chain, load_elem(in_data, in->dtype, off), in->dtype, full);
       if (kind == ORC_RED_ADD) acc += v;
       else acc = ieee_maximum(acc, v);
       asum += std::fabs(v);
     }
     int64_t ooff = 0;
     for (int k = 0; k < nk; ++k) ooff += kidx[k] * ostride[k];
-    store_elem(out_data, out->dtype, ooff, round_to(acc, out->dtype));
+    store_elem(out_data, out->dtype, ooff, round_to<double>(acc, out->dtype));
     if (abs_sum) abs_sum[ooff] = (double)asum;
   }
   return ORC_OK;
@@ -448,7 +451,7 @@ int orc_reduce(const orc_arr* in, const void* in_data, const orc_chain* chain,
 // out = epilogue(prologue(in) + T(prologue(in))) where T permutes dimensions:
 // dims(out)[k] = dims(in)[perm[k]] and T(x)[r] = x[i] with i[perm[k]] = r[k].
 // ----------------------------------------------------------------------------------------------
-int orc_transpose(const orc_arr* in, const void* in_data, const orc_chain* prologue,
+extern "C" int orc_transpose(const orc_arr* in, const void* in_data, const orc_chain* prologue,
                   const int64_t* perm, int self_add, const orc_chain* epilogue,
                   const orc_arr* out, void* out_data) {
   if (!valid_arr(in) || !valid_arr(out) || in->rank != out->rank) return ORC_EINVAL;
@@ -478,14 +481,14 @@ int orc_transpose(const orc_arr* in, const void* in_data, const orc_chain* prolo
       roff_in += r[d] * istride[d];
       ooff += r[d] * ostride[d];
     }
-    long double t = apply_chain(prologue, load_elem(in_data, dt, ioff), dt, i);
-    long double v = t;
+    double t = apply_chain(prologue, load_elem(in_data, dt, ioff), dt, i);
+    double v = t;
     if (self_add) {
-      long double s = apply_chain(prologue, load_elem(in_data, dt, roff_in), dt, r);
-      v = round_to(s + t, wt);  // add of two values of the working type, rounded once
+      double s = apply_chain(prologue, load_elem(in_data, dt, roff_in), dt, r);
+      v = round_to<double>(s + t, wt);  // add of two values of the working type, rounded once
     }
     v = apply_chain(epilogue, v, dt, r);
-    store_elem(out_data, out->dtype, ooff, round_to(v, dt));
+    store_elem(out_data, out->dtype, ooff, round_to<double>(v, dt));
   }
   return ORC_OK;
 }
@@ -493,7 +496,7 @@ int orc_transpose(const orc_arr* in, const void* in_data, const orc_chain* prolo
 // ----------------------------------------------------------------------------------------------
 // Layout conversion: same logical array, new minor_to_major. out[off_out(i)] = in[off_in(i)].
 // ----------------------------------------------------------------------------------------------
-int orc_layout_convert(const orc_arr* in, const void* in_data, const int64_t* out_m2m, void* out_data) {
+extern "C" int orc_layout_convert(const orc_arr* in, const void* in_data, const int64_t* out_m2m, void* out_data) {
   if (!valid_arr(in)) return ORC_EINVAL;
   orc_arr out = *in;
   for (int k = 0; k < in->rank; ++k) out.m2m[k] = out_m2m[k];
@@ -559,7 +562,7 @@ static int32_t quantize_one(const orc_quant* q, float real, const int64_t* idx) 
 
 // dequant(in) -> float chain (f32) -> relayout to out->m2m -> quant(out_q), or f32 out if out_q is
 // NULL. out->dims must equal in->dims (a layout change keeps the logical shape).
-int orc_quant_fusion(const orc_arr* in, const void* in_data, const orc_quant* in_q,
+extern "C" int orc_quant_fusion(const orc_arr* in, const void* in_data, const orc_quant* in_q,
                      const orc_chain* float_ops, const orc_arr* out, void* out_data,
                      const orc_quant* out_q) {
   if (!valid_arr(in) || !valid_arr(out) || in->rank != out->rank) return ORC_EINVAL;
@@ -581,7 +584,7 @@ int orc_quant_fusion(const orc_arr* in, const void* in_data, const orc_quant* in
     int32_t code = (int32_t)load_elem(in_data, in->dtype, io);
     float real = dequantize_one(in_q, code, idx);
     real = (float)apply_chain(float_ops, real, ORC_F32, idx);
-    if (out_q) store_elem(out_data, out->dtype, oo, (long double)quantize_one(out_q, real, idx));
+    if (out_q) store_elem(out_data, out->dtype, oo, (double)quantize_one(out_q, real, idx));
     else store_elem(out_data, ORC_F32, oo, real);
   }
   return ORC_OK;
@@ -590,18 +593,18 @@ int orc_quant_fusion(const orc_arr* in, const void* in_data, const orc_quant* in
 // ----------------------------------------------------------------------------------------------
 // Scalar entry points used to pin the elementwise rules.
 // ----------------------------------------------------------------------------------------------
-double orc_round_to(double v, int dtype) { return (double)round_to(v, dtype); }
-double orc_exp(double x, int dtype) { return (double)cr_exp(round_to(x, dtype), dtype); }
-double orc_log(double x, int dtype) { return (double)cr_log(round_to(x, dtype), dtype); }
-double orc_maximum(double a, double b) { return (double)ieee_maximum(a, b); }
-int orc_quantize(const orc_quant* q, float real, const int64_t* idx) { return quantize_one(q, real, idx); }
-float orc_dequantize(const orc_quant* q, int32_t code, const int64_t* idx) { return dequantize_one(q, code, idx); }
+extern "C" double orc_round_to(double v, int dtype) { return round_to<double>(v, dtype); }
+extern "C" double orc_exp(double x, int dtype) { return cr_exp(round_to<double>(x, dtype), dtype); }
+extern "C" double orc_log(double x, int dtype) { return cr_log(round_to<double>(x, dtype), dtype); }
+extern "C" double orc_maximum(double a, double b) { return (double)ieee_maximum(a, b); }
+extern "C" int orc_quantize(const orc_quant* q, float real, const int64_t* idx) { return quantize_one(q, real, idx); }
+extern "C" float orc_dequantize(const orc_quant* q, int32_t code, const int64_t* idx) { return dequantize_one(q, code, idx); }
 
 // Exhaustive check helper: for count consecutive f32 bit patterns starting at first_bits, compares
 // cand[i] (bit pattern of a claimed correctly rounded f32 log) with the oracle's value. NaN results
 // match any NaN pattern. Returns the number of mismatches; the first max_report mismatching input
 // patterns (in ascending order) are written to report.
-int64_t orc_check_log_f32(uint32_t first_bits, int64_t count, const uint32_t* cand,
+extern "C" int64_t orc_check_log_f32(uint32_t first_bits, int64_t count, const uint32_t* cand,
                           uint32_t* report, int64_t max_report) {
   std::vector<uint8_t> bad_flag((size_t)count, 0);
 #pragma omp parallel for schedule(static)
@@ -623,7 +626,7 @@ int64_t orc_check_log_f32(uint32_t first_bits, int64_t count, const uint32_t* ca
   return bad;
 }
 
-void orc_set_num_threads(int n) {
+extern "C" void orc_set_num_threads(int n) {
 #ifdef _OPENMP
   omp_set_num_threads(n);
 #else
@@ -631,7 +634,7 @@ void orc_set_num_threads(int n) {
 #endif
 }
 
-int orc_max_threads(void) {
+extern "C" int orc_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
 #else
@@ -639,4 +642,3 @@ int orc_max_threads(void) {
 #endif
 }
 
-}  // extern "C"
