@@ -1,0 +1,376 @@
+"""Benchmark: the five HLO hero fusions on one GB300, one JSON line.
+
+A step is one pass of the whole hot path: the five fusions, each launched once through the C ABI on
+its seeded synthetic full-size inputs (already resident in HBM), in a fixed order:
+  row_reduce_exp     f32[256,512]                       exp, reduce-add over dim 1
+  transpose_log      f32[8192,8192]                     log(p) + transpose(log(p))
+  col_reduce_max     bf16[8192,16384]                   reduce-max over dim 0 (f32 accumulation)
+  bcast_exp_reduce   bf16[8,1,1280,16384]{3,2,0,1}      exp, + broadcast b, reduce-add over dim 3
+  quant_relayout     s8[4096,4096]                      dequant (per-axis) -> {0,1} -> quant (per-tensor)
+value = algorithmic bytes of the step / step time (GB/s); per-fusion GB/s, fraction of the measured HBM
+copy peak and elements/s are reported alongside. L2 is flushed (a 256 MiB write) before every timed
+step, outside the timed interval.
+
+Multi-GPU (torchrun): every rank runs its own replica of the step (weak scaling, no collective); value
+= bytes processed by all ranks / max over ranks of the timed region.
+
+--impl reference times the CPU oracle (the plain C++ reference of the same fusions) on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from transpose_heroes_gb300 import inputs as inp  # noqa: E402
+
+METRIC = "achieved HBM GB/s per fusion and fraction of GB300 peak; elements/s"
+ORDER = ["row_reduce_exp", "transpose_log", "col_reduce_max", "bcast_exp_reduce", "quant_relayout"]
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("HLO hero fusions, one launch each per step: row_reduce_exp f32[256,512]{1,0}; "
+            "transpose_selfadd_log f32[8192,8192]{1,0}; col_reduce_max bf16[8192,16384]{1,0}; "
+            "bcast_exp_row_reduce bf16[8,1,1280,16384]{3,2,0,1}+bf16[16384]; "
+            "quant_relayout s8[4096,4096]{1,0}->{0,1}")
+L2_NOTE = "L2 flushed by a 256 MiB device write before every timed step (outside the timed interval)"
+# kernel each fusion launches (for the launch list / roofline)
+KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_pair_kernel",
+           "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_reduce_kernel",
+           "quant_relayout": "quant_tile_kernel"}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel_file_hash):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it was taken on
+    the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha256") != kernel_file_hash:
+        return None
+    return d
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transpose_heroes_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".inc")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU works (reads only)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = f"/tmp/hlofusion_clocks_{os.getpid()}.csv"
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.remove(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def aggregate(values, reduce_fn):
+    """Combines one float per rank (max for times, sum for bytes) through torch.distributed when
+    initialised, else returns the local value."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return values
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(values)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if reduce_fn == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------------------
+# CPU baseline (the oracle as it stands)
+# ------------------------------------------------------------------------------------------------------
+def cpu_sample_fusions(fraction: float):
+    """A bounded sample of the same workload: each fusion on a leading fraction of its rows (whole rows,
+    so every output is complete), the row-reduce in full."""
+    fr = max(min(fraction, 1.0), 1e-4)
+    out = [inp.row_reduce_exp(seed=1)]
+    n = max(64, int(8192 * fr ** 0.5) // 64 * 64)
+    out.append(inp.transpose_log(seed=1, n=n))
+    out.append(inp.col_reduce_max(seed=1, rows=max(8, int(8192 * fr)), cols=16384))
+    out.append(inp.bcast_exp_reduce(seed=1, d0=1, d2=max(1, int(10240 * fr)), d3=16384))
+    out.append(inp.quant_relayout(seed=1, n0=max(16, int(4096 * fr) // 16 * 16), n1=4096))
+    return out
+
+
+def run_oracle_once(fusions):
+    import oracle
+
+    t0 = time.perf_counter()
+    nbytes = 0
+    for f in fusions:
+        if f.kind == "reduce":
+            oracle.reduce(f.data, f.dims, f.dtype, f.dimensions, f.reduce_kind, f.init, f.out_dtype, m2m=f.m2m,
+                          out_m2m=f.out_m2m, prologue=f.prologue)
+        elif f.kind == "transpose":
+            oracle.transpose(f.data, f.dims, f.dtype, f.permutation, m2m=f.m2m, out_m2m=f.out_m2m,
+                             self_add=f.self_add, prologue=f.prologue, epilogue=f.epilogue)
+        else:
+            oracle.quant_fusion(f.data, f.dims, f.dtype, f.in_q, f.out_m2m, f.out_dtype, out_q=f.out_q, m2m=f.m2m)
+        nbytes += f.algorithmic_bytes
+    return nbytes, time.perf_counter() - t0
+
+
+def cpu_baseline(fraction=1.0 / 16):
+    import oracle
+
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_num_threads(cores)
+    fusions = cpu_sample_fusions(fraction)
+    nbytes, dt = run_oracle_once(fusions)
+    sample = ("one pass of the five fusions on a leading slice of each workload: " +
+              "; ".join(f"{f.name}" for f in fusions))
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "seconds": dt}
+
+
+def reference_arm(args):
+    rank, world, local = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_num_threads(cores)
+    # size the per-step sample so that warmup + steps take about a minute on these cores
+    probe = cpu_sample_fusions(1.0 / 256)
+    pbytes, pdt = run_oracle_once(probe)
+    per_step_budget = 60.0 / max(1, args.steps + args.warmup)
+    fraction = min(1.0, (1.0 / 256) * per_step_budget / max(pdt, 1e-3))
+    fusions = cpu_sample_fusions(fraction)
+    for _ in range(args.warmup):
+        run_oracle_once(fusions)
+    total_bytes, total_t = 0, 0.0
+    for _ in range(args.steps):
+        b, dt = run_oracle_once(fusions)
+        total_bytes += b
+        total_t += dt
+    value = total_bytes / total_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_fraction_of_rows": fraction, "seed": 1},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"leading {fraction:.4g} of each fusion's rows (row_reduce_exp in full), "
+                                   "the plain C++ oracle, OpenMP over independent outputs"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------------
+def ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from transpose_heroes_gb300 import build as libbuild
+    from transpose_heroes_gb300.runner import DeviceFusion
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    libbuild.build()
+    dev = f"cuda:{local}"
+    fusions = [inp.full(n, seed=args.seed) for n in ORDER]
+    devs = [DeviceFusion(f, device=dev, pin_host=True) for f in fusions]
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    step_bytes = sum(f.algorithmic_bytes for f in fusions)
+    step_elems = sum(f.elements for f in fusions)
+
+    def step(evs=None):
+        for i, d in enumerate(devs):
+            if evs is not None:
+                evs[i].record(stream)
+            d.run(stream=stream)
+        if evs is not None:
+            evs[len(devs)].record(stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(devs) + 1)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        step(ev[k])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    per_fusion_ms = [[ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)] for i in range(len(devs))]
+    step_ms = [ev[k][0].elapsed_time(ev[k][len(devs)]) for k in range(args.steps)]
+    local_total_s = sum(step_ms) / 1e3
+    total_s = aggregate(local_total_s, "max")
+    all_bytes = aggregate(float(step_bytes * args.steps), "sum")
+    value = all_bytes / total_s / 1e9
+
+    hbm, peak_src = peaks()
+    per = {}
+    for i, f in enumerate(fusions):
+        ms = statistics.mean(per_fusion_ms[i])
+        gbs = f.algorithmic_bytes / (ms / 1e3) / 1e9
+        per[ORDER[i]] = {"kernel": KERNELS[ORDER[i]], "us": 1e3 * ms, "us_min": 1e3 * min(per_fusion_ms[i]),
+                         "algorithmic_bytes": f.algorithmic_bytes, "gbs": gbs, "frac_of_" + peak_src: gbs / hbm,
+                         "elements_per_s": f.elements / (ms / 1e3)}
+    dom = max(per, key=lambda k: per[k]["us"])
+    dom_gbs = per[dom]["gbs"]
+    tr = traffic_record(source_hash())
+    roofline = {"bound": "hbm", "kernel": per[dom]["kernel"], "fusion": dom, "achieved": dom_gbs, "peak": hbm,
+                "peak_source": peak_src, "unit": "GB/s", "frac": dom_gbs / hbm,
+                "traffic": (tr["dram_bytes_per_launch"] if tr and tr.get("fusion") == dom else None),
+                "algorithmic_bytes_per_launch": per[dom]["algorithmic_bytes"]}
+
+    # end to end through the same C-ABI calls: pinned host inputs -> device, fusions, outputs -> host
+    e2e_steps = max(1, min(args.steps, 20))
+    h2d = sum(d.h2d_bytes for d in devs)
+    d2h = sum(d.d2h_bytes for d in devs)
+    for d in devs:
+        d.h2d()
+        d.run(stream=stream)
+        d.d2h()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for d in devs:
+            d.h2d()
+            d.run(stream=stream)
+            d.d2h()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = aggregate(e0.elapsed_time(e1) / 1e3, "max")
+    e2e_bytes = aggregate(float(step_bytes * e2e_steps), "sum")
+    e2e = {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": e2e_steps}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": world, "l2": L2_NOTE, "seed": args.seed,
+                       "parallelism": f"replicas{world}"},
+            "elements_per_s": aggregate(float(step_elems * args.steps), "sum") / total_s,
+            "per_fusion": per, "roofline": roofline, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": len(devs) * args.steps,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+    return ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

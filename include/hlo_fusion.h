@@ -1,0 +1,227 @@
+/*
+ * hlo_fusion.h -- C ABI of libhlofusion: HLO fusions whose hero is a reduce, a transpose or a layout
+ * change, executed on one GB300 GPU (sm_103a) by hand-written CUDA kernels.
+ *
+ * Every fusion reads its inputs from HBM once and writes its output once; the elementwise prologue
+ * and epilogue (exp, log, abs, negate, add of a broadcast operand) and uniform (de)quantization are
+ * applied in registers.
+ *
+ * Conventions shared by all entry points
+ * --------------------------------------
+ *  - Arrays are described by hlo_array: a logical shape (dims, numbered 0..rank-1, each >= 0; size 0
+ *    is valid) and a physical layout minor_to_major, a permutation of 0..rank-1 whose first entry is
+ *    the minor-most dimension (the one that changes fastest in linear memory). Source: "XLA Shapes and
+ *    Layout", sections "Shapes" and "Layout" (minor-to-major ordering, the [2 x 3] example), and
+ *    "Default minor-to-major ordering" ([rank-1, ..., 0], i.e. row-major).
+ *  - Data pointers (in_ptr, out_ptr, hlo_ew_chain.bcast_ptr, hlo_quant.scales/zero_points) are
+ *    DEVICE pointers to dense buffers in that layout. Descriptors are host memory, read during the
+ *    call only. The caller owns every buffer; the library allocates no device memory and keeps no
+ *    pointer after the call returns.
+ *  - stream is a cudaStream_t (NULL = the legacy default stream). Calls are asynchronous: they
+ *    validate, enqueue one or more kernels on the stream and return. The output is defined once the
+ *    stream reaches that point.
+ *  - Inputs and outputs must not overlap (HLO_ERR_INVALID_ARG). Alignment is not required: buffers
+ *    that are not 16-byte aligned, or rows whose byte length is not a multiple of 16, take a
+ *    narrower-access variant of the same kernel.
+ *  - On any error nothing is enqueued, except HLO_ERR_CUDA, which reports a failed launch.
+ *    hlo_last_error() returns a thread-local message naming the violated constraint.
+ *  - Floating point: reductions accumulate in f32; the order of accumulation is implementation
+ *    defined, as the reduce semantics allow ("StableHLO Specification", section "reduce"). log is
+ *    correctly rounded in f32; transposes, layout changes and quantization are bit-exact.
+ */
+#ifndef HLO_FUSION_H
+#define HLO_FUSION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HLO_MAX_RANK 8
+#define HLO_MAX_EW_OPS 4
+
+typedef enum {
+  HLO_OK = 0,
+  HLO_ERR_INVALID_ARG = 1, /* a constraint of the op's semantics or of this ABI is violated */
+  HLO_ERR_UNSUPPORTED = 2, /* valid, but this library has no kernel for it (e.g. an element type) */
+  HLO_ERR_CUDA = 3,        /* a CUDA call failed; the message carries cudaGetErrorString */
+  HLO_ERR_WORKSPACE = 4    /* the workspace passed is smaller than hlo_reduce_workspace_size() */
+} hlo_status;
+
+/* Element types ("StableHLO Specification", section "Types"). */
+typedef enum {
+  HLO_F32 = 0,
+  HLO_BF16 = 1,
+  HLO_S8 = 2,
+  HLO_F16 = 3,
+  HLO_S32 = 4
+} hlo_dtype;
+
+/* A dense array: logical shape plus physical layout. */
+typedef struct {
+  int32_t rank;                            /* 0..HLO_MAX_RANK */
+  int32_t dtype;                           /* hlo_dtype */
+  int64_t dims[HLO_MAX_RANK];              /* dims[0..rank-1], each >= 0 */
+  int64_t minor_to_major[HLO_MAX_RANK];    /* a permutation of 0..rank-1, minor-most first */
+} hlo_array;
+
+/* Elementwise ops of a prologue/epilogue chain. Each is the IEEE-754 operation on the element type
+ * ("StableHLO Specification", sections "exponential", "log", "abs", "negate", "add"); the result type
+ * equals the operand type (constraint C1 of each op). */
+typedef enum {
+  HLO_EW_EXP = 1,
+  HLO_EW_LOG = 2,
+  HLO_EW_ABS = 3,
+  HLO_EW_NEG = 4,
+  HLO_EW_ADD_BCAST = 5 /* x + broadcast_in_dim(bcast, bcast_dimensions) */
+} hlo_ew_kind;
+
+/* A chain of up to HLO_MAX_EW_OPS elementwise ops applied in order to every element of the array
+ * it is attached to. n_ops == 0 (or a NULL chain pointer) is the identity.
+ *
+ * HLO_EW_ADD_BCAST adds broadcast_in_dim(bcast, bcast_dimensions) ("StableHLO Specification", section
+ * "broadcast_in_dim"): the operand element read for array index i has, in each operand dimension d,
+ * index 0 if bcast.dims[d] == 1 and i[bcast_dimensions[d]] otherwise (constraints C2-C5 are checked:
+ * one entry per operand dimension, each in range and unique, and bcast.dims[d] is 1 or equal to the
+ * array's dimension). bcast.dtype must equal the array's element type (add, constraint C1).
+ *
+ * round_intermediates selects the precision of values between ops for 16-bit float arrays:
+ *   1 -- every op result is rounded to the element type (the spec's types: exp of bf16 is bf16);
+ *   0 -- intermediates stay in f32 and only the hero sees them.
+ * For f32 arrays the two are the same. */
+typedef struct {
+  int32_t n_ops;
+  int32_t ops[HLO_MAX_EW_OPS];             /* hlo_ew_kind */
+  int32_t round_intermediates;
+  const void* bcast_ptr;                   /* device pointer; used by HLO_EW_ADD_BCAST only */
+  hlo_array bcast;
+  int64_t bcast_dimensions[HLO_MAX_RANK];
+} hlo_ew_chain;
+
+typedef enum { HLO_RED_ADD = 0, HLO_RED_MAX = 1 } hlo_reduce_kind;
+
+/* Uniform quantization parameters ("StableHLO Specification", section "Types", quantized element
+ * types; "StableHLO Quantization", per-tensor and per-axis quantization):
+ *   real = scale * (q - zero_point),
+ * one (scale, zero_point) pair for the whole tensor (quantization_dimension = -1, n = 1) or one pair
+ * per slice t[..., i, ...] along quantization_dimension (n = dims[quantization_dimension]).
+ * scales / zero_points point to n values on the DEVICE. host_scales / host_zero_points optionally
+ * point to a host copy of the same values: when given, the library checks the spec's constraints on
+ * them (C6 scale > 0, C7 finite, C8 storage_min <= zero_point <= storage_max); when NULL those value
+ * constraints are the caller's responsibility. For per-tensor parameters the host copy alone is
+ * enough (the device pointers may then be NULL). storage_min < storage_max must lie within the
+ * storage type's range (C4). */
+typedef struct {
+  int32_t quantization_dimension;          /* -1: per-tensor */
+  int64_t n;
+  const float* scales;                     /* device */
+  const int32_t* zero_points;              /* device */
+  const float* host_scales;                /* optional host copy */
+  const int32_t* host_zero_points;         /* optional host copy */
+  int32_t storage_min;
+  int32_t storage_max;
+} hlo_quant;
+
+/* ------------------------------------------------------------------------------------------------
+ * hlo_reduce_fusion -- out = reduce(prologue(in), init_value, dimensions, kind).
+ *
+ * Semantics: "StableHLO Specification", section "reduce" (inputs I1-I4, constraints C1-C8), with the
+ * body add or maximum ("StableHLO Specification", section "maximum": IEEE-754 maximum, NaN propagates,
+ * -0 < +0) and "XLA Operation Semantics", section "Reduce". Every output element is the reduction of
+ * the prologue applied to its slice; init_value is applied exactly once. The dimensions kept form the
+ * output in their original relative order (C7); out describes that shape with any layout.
+ *
+ *   in, in_ptr       input array (f32, bf16 or f16) and its device data
+ *   prologue         elementwise chain applied to every input element first (may be NULL)
+ *   dimensions       n_dimensions unique dimension numbers of in to reduce (C4, C5); may be 0 of them
+ *   kind             HLO_RED_ADD or HLO_RED_MAX
+ *   init_value       the init value, converted to the accumulation type
+ *   accum_dtype      must be HLO_F32 (the body's element type; inputs are promoted to it, C6)
+ *   out, out_ptr     output array (f32, bf16 or f16); the f32 result is rounded to nearest even
+ *   workspace        device scratch of at least hlo_reduce_workspace_size() bytes (NULL if 0)
+ *
+ * A reduced dimension of size 0 yields init_value. Reductions whose reduced dimensions are the
+ * minor-most physical dimensions run as row reductions, those with kept dimensions on both sides
+ * as column reductions (thread-block clusters combine row slabs through distributed shared memory);
+ * any other pattern runs a general kernel.
+ * ---------------------------------------------------------------------------------------------- */
+hlo_status hlo_reduce_fusion(const hlo_array* in, const void* in_ptr, const hlo_ew_chain* prologue,
+                             const int64_t* dimensions, int32_t n_dimensions, int32_t kind,
+                             double init_value, int32_t accum_dtype, const hlo_array* out,
+                             void* out_ptr, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device scratch bytes hlo_reduce_fusion needs for this input and reduction (0 for every plan this
+ * library currently selects). Returns 0 for invalid arguments as well. */
+size_t hlo_reduce_workspace_size(const hlo_array* in, const int64_t* dimensions, int32_t n_dimensions,
+                                 int32_t accum_dtype);
+
+/* ------------------------------------------------------------------------------------------------
+ * hlo_transpose_fusion -- out = epilogue(transpose(prologue(in), permutation)), or with
+ * self_add_epilogue != 0: out = epilogue(prologue(in) + transpose(prologue(in), permutation)).
+ *
+ * Semantics: transpose maps output index r to input index i with i[permutation[k]] = r[k], so
+ * dims(out)[k] = dims(in)[permutation[k]] -- the output-to-input indexing map of "XLA:GPU Emitters",
+ * section "Indexing transformations" ([20,40] -> [40,20] reads (d0, d1) -> (d1, d0)). The self-add form
+ * is the fusion of "XLA:GPU Emitters", section "Partitioning": log(param) feeding both a transpose and
+ * an add; it requires dims(out) == dims(in). Its prologue is evaluated once per input element (the
+ * kernel loads the tile pair (I,J), (J,I) once and reuses both), and add is the IEEE f32 add, so the
+ * result is bitwise symmetric for a 2-D square input.
+ *
+ *   in, in_ptr       input array; element types f32, bf16, f16 (with chains) or any (no chains)
+ *   prologue         chain applied to the input elements (may be NULL)
+ *   permutation      rank entries, a permutation of 0..rank-1
+ *   epilogue         chain applied to the output elements (may be NULL; no HLO_EW_ADD_BCAST)
+ *   out, out_ptr     output array: same element type, dims as above, any layout
+ * ---------------------------------------------------------------------------------------------- */
+hlo_status hlo_transpose_fusion(const hlo_array* in, const void* in_ptr, const hlo_ew_chain* prologue,
+                                const int64_t* permutation, int32_t self_add_epilogue,
+                                const hlo_ew_chain* epilogue, const hlo_array* out, void* out_ptr,
+                                void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * hlo_layout_convert -- the same logical array written with another minor_to_major ("XLA Shapes and
+ * Layout", section "Layout"): for every index i, out[offset(i, out_minor_to_major)] =
+ * in[offset(i, in->minor_to_major)]. Any element type; bit-exact.
+ *   out_minor_to_major   in->rank entries, a permutation of 0..rank-1
+ * ---------------------------------------------------------------------------------------------- */
+hlo_status hlo_layout_convert(const hlo_array* in, const void* in_ptr, const int64_t* out_minor_to_major,
+                              void* out_ptr, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * hlo_quant_fusion -- dequantize -> elementwise float ops -> layout change -> quantize.
+ *
+ *   real = scale[j] * (q - zero_point[j])                       (f32: exact difference, one rounding)
+ *   real = float_ops(real)                                      (f32 chain, may be NULL)
+ *   out  = clamp(round_nearest_even(real / out_scale[j']) + out_zero_point[j'],
+ *                storage_min, storage_max)                      (f32 IEEE division)
+ * with j / j' the index along the input / output quantization_dimension (0 per-tensor). This is the
+ * dequantize -> float op -> quantize pattern of "StableHLO Quantization" (quantized ops expressed as
+ * dequantize_op_quantize) with the relation real = scale * (q - zero_point); rounding is
+ * roundToIntegralTiesToEven ("StableHLO Specification", section "round_nearest_even") and saturation is
+ * clamp ("StableHLO Specification", section "clamp"). With out_q == NULL the output is the f32 real.
+ *
+ *   in, in_ptr           storage array, dtype HLO_S8
+ *   in_q                 its quantization parameters (required)
+ *   float_ops            f32 chain applied to the dequantized values (may be NULL)
+ *   out_minor_to_major   output layout (rank entries); must equal out->minor_to_major
+ *   out, out_ptr         output array: dims equal to in's, dtype HLO_S8 (quantized) or HLO_F32
+ *   out_q                output quantization parameters, or NULL for f32 output
+ * Bit-exact: both the dequantize product and the quantize division are single IEEE f32 operations.
+ * ---------------------------------------------------------------------------------------------- */
+hlo_status hlo_quant_fusion(const hlo_array* in, const void* in_ptr, const hlo_quant* in_q,
+                            const hlo_ew_chain* float_ops, const int64_t* out_minor_to_major,
+                            const hlo_array* out, void* out_ptr, const hlo_quant* out_q, void* stream);
+
+/* Thread-local description of the last error returned on this thread ("" if none). */
+const char* hlo_last_error(void);
+
+/* Library version string. */
+const char* hlo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HLO_FUSION_H */

@@ -1,0 +1,414 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs.
+
+Bars (from the fusion semantics):
+  * transposes, layout changes and quantized relayouts: bit-exact (log is correctly rounded in f32);
+  * float reductions with add: |gpu - oracle| <= 1e-5 * sum|terms| + 1e-6 (f32 accumulation against the
+    oracle's long-double sum), plus half an output ulp when the output type is 16-bit;
+  * reductions with max: bit-exact.
+Sizes: scaled-down shapes that span several tiles and end in ragged tails, the full-size workloads in
+the launch configuration the benchmark times, and edge cases (empty, unit and unaligned).
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import transpose_heroes_gb300 as hf
+from transpose_heroes_gb300 import inputs as inp
+from transpose_heroes_gb300.runner import DeviceFusion
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transpose_heroes_gb300 import build
+
+    build.build()
+    oracle.build()
+    hf.lib()
+
+
+def run_gpu(f):
+    d = DeviceFusion(f)
+    d.run()
+    torch.cuda.synchronize()
+    return d.output_numpy()
+
+
+def run_oracle(f):
+    if f.kind == "reduce":
+        return oracle.reduce(f.data, f.dims, f.dtype, f.dimensions, f.reduce_kind, f.init, f.out_dtype, m2m=f.m2m,
+                             out_m2m=f.out_m2m, prologue=f.prologue, want_abs_sum=True)
+    if f.kind == "transpose":
+        return oracle.transpose(f.data, f.dims, f.dtype, f.permutation, m2m=f.m2m, out_m2m=f.out_m2m,
+                                self_add=f.self_add, prologue=f.prologue, epilogue=f.epilogue), None
+    if f.kind == "layout":
+        return oracle.layout_convert(f.data, f.dims, f.dtype, f.m2m, f.out_m2m), None
+    if f.kind == "quant":
+        return oracle.quant_fusion(f.data, f.dims, f.dtype, f.in_q, f.out_m2m, f.out_dtype, out_q=f.out_q,
+                                   m2m=f.m2m, float_ops=f.prologue), None
+    raise ValueError(f.kind)
+
+
+def as_f32(buf, dtype):
+    if dtype in ("bf16",):
+        return inp.bf16_bits_to_f32(buf)
+    if dtype == "f16":
+        return np.asarray(buf, np.uint16).view(np.float16).astype(np.float32)
+    return np.asarray(buf, np.float32)
+
+
+def check(f, gpu, ref, asum):
+    assert gpu.shape == ref.shape
+    if f.kind == "reduce" and f.reduce_kind == "add":
+        g = as_f32(gpu, f.out_dtype).astype(np.float64)
+        r = as_f32(ref, f.out_dtype).astype(np.float64)
+        tol = 1e-5 * asum + 1e-6
+        if f.out_dtype in ("bf16", "f16"):
+            tol = tol + np.abs(r) * (2.0 ** -8 if f.out_dtype == "bf16" else 2.0 ** -11)
+        err = np.abs(g - r)
+        bad = ~(err <= tol)
+        assert not bad.any(), f"{bad.sum()} outputs out of tolerance; worst err {err.max()} tol {tol[np.argmax(err)]}"
+    else:
+        if f.out_dtype in ("f32",):
+            g, r = gpu.view(np.uint32), ref.view(np.uint32)
+            nan_g, nan_r = np.isnan(gpu), np.isnan(ref)
+            assert np.array_equal(nan_g, nan_r)
+            same = (g == r) | nan_g
+        elif f.out_dtype in ("bf16", "f16"):
+            gf, rf = as_f32(gpu, f.out_dtype), as_f32(ref, f.out_dtype)
+            same = (gpu.view(np.uint16) == ref.view(np.uint16)) | (np.isnan(gf) & np.isnan(rf))
+        else:
+            same = gpu == ref
+        nbad = int((~same).sum())
+        assert nbad == 0, f"{nbad} of {same.size} outputs differ; first at {np.argmax(~same)}"
+
+
+NAMES = list(inp.FULL)
+
+
+@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("seed", [1, 2])
+def test_small_configs(name, seed):
+    f = inp.small(name, seed=seed)
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_full_size_configs(name):
+    """The full-size workloads, as the benchmark launches them, against the oracle on every output."""
+    f = inp.full(name, seed=1)
+    ref, asum = run_oracle(f)
+    gpu = run_gpu(f)
+    check(f, gpu, ref, asum)
+    if name == "transpose_log":
+        n = f.dims[0]
+        g = gpu.view(np.uint32).reshape(n, n)
+        assert np.array_equal(g, g.T)  # bitwise symmetric
+    assert oracle.unresolved_count() == 0
+
+
+# ---- more shapes through the same kernels -----------------------------------------------------------
+@pytest.mark.parametrize("rows,cols", [(1, 1), (1, 7), (5, 3), (3, 4096 + 8), (2, 100003), (1000, 24)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_row_reduce_shapes(rows, cols, dtype):
+    g = inp.rng(rows * 7 + cols)
+    n = rows * cols
+    data = inp.uniform_f32(g, n, -1, 1) if dtype == "f32" else inp.normal_bf16(g, n)
+    for kind, init in (("add", 0.0), ("max", -math.inf), ("add", 2.5)):
+        f = inp.Fusion(name="row", kind="reduce", dims=[rows, cols], m2m=[1, 0], dtype=dtype, data=data,
+                       dimensions=[1], reduce_kind=kind, init=init,
+                       prologue={"ops": ["exp"], "round_each": True} if kind == "add" else None,
+                       out_dims=[rows], out_m2m=[0], out_dtype="f32")
+        ref, asum = run_oracle(f)
+        check(f, run_gpu(f), ref, asum)
+
+
+@pytest.mark.parametrize("a,r,b", [(1, 1, 1), (1, 9, 5), (3, 33, 264), (2, 1000, 7), (1, 4097, 2048)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_col_reduce_shapes(a, r, b, dtype):
+    g = inp.rng(a * 1000 + r + b)
+    n = a * r * b
+    data = inp.uniform_f32(g, n, -4, 4) if dtype == "f32" else inp.normal_bf16(g, n)
+    for kind, init in (("max", -math.inf), ("add", 0.0)):
+        f = inp.Fusion(name="col", kind="reduce", dims=[a, r, b], m2m=[2, 1, 0], dtype=dtype, data=data,
+                       dimensions=[1], reduce_kind=kind, init=init, out_dims=[a, b], out_m2m=[1, 0],
+                       out_dtype=dtype if kind == "max" else "f32")
+        ref, asum = run_oracle(f)
+        check(f, run_gpu(f), ref, asum)
+
+
+def test_reduce_general_patterns_and_layouts():
+    g = inp.rng(99)
+    dims = [4, 6, 5, 3]
+    data = inp.uniform_f32(g, int(np.prod(dims)), -2, 2)
+    cases = [([0, 2], [3, 2, 1, 0], [1, 0]), ([1, 3], [0, 1, 2, 3], [0, 1]), ([0, 1, 2, 3], [2, 0, 3, 1], []),
+             ([2], [1, 3, 0, 2], [0, 2, 1]), ([3, 0], [3, 2, 1, 0], [1, 0]), ([], [3, 2, 1, 0], [3, 2, 1, 0])]
+    for dimsred, m2m, out_m2m in cases:
+        kept = [d for d in range(4) if d not in dimsred]
+        for kind, init in (("add", 0.0), ("max", -math.inf)):
+            f = inp.Fusion(name="gen", kind="reduce", dims=dims, m2m=m2m, dtype="f32", data=data,
+                           dimensions=dimsred, reduce_kind=kind, init=init,
+                           prologue={"ops": ["abs", "log"]} if kind == "add" else None,
+                           out_dims=[dims[d] for d in kept], out_m2m=out_m2m, out_dtype="f32")
+            ref, asum = run_oracle(f)
+            check(f, run_gpu(f), ref, asum)
+
+
+def test_reduce_empty_and_unit():
+    z = np.zeros(0, np.float32)
+    f = inp.Fusion(name="e", kind="reduce", dims=[4, 0], m2m=[1, 0], dtype="f32", data=z, dimensions=[1],
+                   reduce_kind="add", init=1.5, out_dims=[4], out_m2m=[0], out_dtype="f32")
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+    f = inp.Fusion(name="e", kind="reduce", dims=[0, 5], m2m=[1, 0], dtype="f32", data=z, dimensions=[1],
+                   reduce_kind="add", init=1.5, out_dims=[0], out_m2m=[0], out_dtype="f32")
+    assert run_gpu(f).size == 0
+
+
+def test_max_nan_and_signed_zero():
+    rows, cols = 8, 64
+    x = np.zeros((rows, cols), np.float32)
+    x[0, 5] = np.nan
+    x[1] = -0.0
+    x[1, 7] = 0.0
+    x[2] = -0.0
+    x[3, :] = -np.inf
+    x[4, 9] = np.inf
+    for dims, red, data in (([rows, cols], [1], x.ravel()), ([cols, rows], [0], x.T.copy().ravel())):
+        f = inp.Fusion(name="m", kind="reduce", dims=dims, m2m=[1, 0], dtype="f32", data=data, dimensions=red,
+                       reduce_kind="max", init=-math.inf, out_dims=[rows], out_m2m=[0], out_dtype="f32")
+        ref, _ = run_oracle(f)
+        gpu = run_gpu(f)
+        check(f, gpu, ref, None)
+        assert np.isnan(gpu[0]) and gpu[1] == 0 and not np.signbit(gpu[1]) and np.signbit(gpu[2])
+
+
+def test_bcast_row_reduce_variants():
+    g = inp.rng(5)
+    d0, d2, d3 = 2, 7, 515
+    x = inp.normal_bf16(g, d0 * d2 * d3)
+    b = inp.uniform_bf16(g, d3, -1, 1)
+    for round_each in (True, False):
+        f = inp.bcast_exp_reduce(seed=5, d0=d0, d2=d2, d3=d3)
+        f.prologue = dict(f.prologue)
+        f.prologue["round_each"] = round_each
+        ref, asum = run_oracle(f)
+        check(f, run_gpu(f), ref, asum)
+    # broadcast along a kept dimension (one value per row)
+    bk = inp.uniform_bf16(g, d2, -1, 1)
+    f = inp.Fusion(name="perrow", kind="reduce", dims=[d0, 1, d2, d3], m2m=[3, 2, 0, 1], dtype="bf16", data=x,
+                   dimensions=[3], reduce_kind="add", init=0.0,
+                   prologue={"ops": ["add_bcast", "exp"], "round_each": True,
+                             "bcast": {"data": bk, "dims": [d2], "m2m": [0], "dtype": "bf16",
+                                       "broadcast_dimensions": [2]}},
+                   out_dims=[d0, 1, d2], out_m2m=[2, 1, 0], out_dtype="f32")
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+    del b
+
+
+# ---- transposes -----------------------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [1, 2, 63, 64, 65, 130, 257])
+def test_selfadd_log_sizes(n):
+    f = inp.transpose_log(seed=n, n=n)
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
+def test_selfadd_other_forms():
+    g = inp.rng(8)
+    n = 70
+    data = inp.uniform_f32(g, n * n, 0.1, 3.0)
+    for m2m in ([1, 0], [0, 1]):
+        for pro, epi in ((None, None), ({"ops": ["log", "neg"]}, {"ops": ["abs"]})):
+            f = inp.Fusion(name="sa", kind="transpose", dims=[n, n], m2m=m2m, dtype="f32", data=data,
+                           permutation=[1, 0], self_add=True, prologue=pro, epilogue=epi, out_dims=[n, n],
+                           out_m2m=m2m, out_dtype="f32")
+            ref, _ = run_oracle(f)
+            check(f, run_gpu(f), ref, None)
+    # self add with different layouts (general path) and rank 3 with unit dims
+    f = inp.Fusion(name="sa2", kind="transpose", dims=[n, n], m2m=[1, 0], dtype="f32", data=data, permutation=[1, 0],
+                   self_add=True, prologue={"ops": ["log"]}, out_dims=[n, n], out_m2m=[0, 1], out_dtype="f32")
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+    f = inp.Fusion(name="sa3", kind="transpose", dims=[n, 1, n], m2m=[2, 1, 0], dtype="f32", data=data,
+                   permutation=[2, 1, 0], self_add=True, prologue={"ops": ["log"]}, out_dims=[n, 1, n],
+                   out_m2m=[2, 1, 0], out_dtype="f32")
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "s8", "s32"])
+def test_transpose_rank3_all_perms_and_layouts(dtype):
+    import itertools
+
+    g = inp.rng(17)
+    dims = [5, 40, 33]
+    n = int(np.prod(dims))
+    if dtype == "f32":
+        data = inp.uniform_f32(g, n, -10, 10)
+    elif dtype == "bf16":
+        data = inp.normal_bf16(g, n)
+    elif dtype == "s8":
+        data = inp.integers(g, n, -128, 127, np.int8)
+    else:
+        data = inp.integers(g, n, -2 ** 31, 2 ** 31 - 1, np.int32)
+    layouts = [list(p) for p in itertools.permutations(range(3))]
+    for pi, perm in enumerate(itertools.permutations(range(3))):
+        for m2m in (layouts[pi], layouts[(pi + 2) % 6]):
+            out_m2m = layouts[(pi + 3) % 6]
+            f = inp.Fusion(name="t3", kind="transpose", dims=dims, m2m=m2m, dtype=dtype, data=data,
+                           permutation=list(perm), out_dims=[dims[p] for p in perm], out_m2m=out_m2m,
+                           out_dtype=dtype)
+            ref, _ = run_oracle(f)
+            check(f, run_gpu(f), ref, None)
+
+
+def test_transpose_emitter_example_exp_abs():
+    """The transpose-emitter example: f32[20,160,170] -> exp -> transpose {2,1,0} -> abs. exp here is CUDA's
+    expf (not correctly rounded), so the bar is 2 ulp, not bit equality."""
+    g = inp.rng(21)
+    dims = [20, 160, 170]
+    data = inp.uniform_f32(g, int(np.prod(dims)), -3, 3)
+    f = inp.Fusion(name="emit", kind="transpose", dims=dims, m2m=[2, 1, 0], dtype="f32", data=data,
+                   permutation=[2, 1, 0], prologue={"ops": ["exp"]}, epilogue={"ops": ["abs"]},
+                   out_dims=[170, 160, 20], out_m2m=[2, 1, 0], out_dtype="f32")
+    ref, _ = run_oracle(f)
+    gpu = run_gpu(f)
+    ulps = np.abs(gpu.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    assert ulps.max() <= 2
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "s8"])
+def test_layout_convert_rank4(dtype):
+    import itertools
+
+    g = inp.rng(3)
+    dims = [3, 1, 37, 66]
+    n = int(np.prod(dims))
+    data = (inp.uniform_f32(g, n, -1, 1) if dtype == "f32" else
+            inp.normal_bf16(g, n) if dtype == "bf16" else inp.integers(g, n, -128, 127, np.int8))
+    for m2m in ([3, 2, 1, 0], [0, 1, 2, 3], [3, 2, 0, 1]):
+        for out_m2m in itertools.islice(itertools.permutations(range(4)), 0, 24, 5):
+            f = inp.Fusion(name="lc", kind="layout", dims=dims, m2m=m2m, dtype=dtype, data=data, out_dims=dims,
+                           out_m2m=list(out_m2m), out_dtype=dtype)
+            ref, _ = run_oracle(f)
+            check(f, run_gpu(f), ref, None)
+
+
+def test_unaligned_pointers():
+    """Operands that start 1 element past an aligned address take the narrow-access variants."""
+    g = inp.rng(4)
+    rows, cols = 33, 520
+    base = torch.from_numpy(inp.uniform_f32(g, rows * cols + 1, -1, 1)).cuda()
+    x = base[1:]
+    out = torch.empty(rows + 1, dtype=torch.float32, device="cuda")[1:]
+    hf.reduce_fusion(x, [rows, cols], "f32", [1], "add", 0.0, out, "f32", prologue={"ops": ["exp"]})
+    f = inp.Fusion(name="u", kind="reduce", dims=[rows, cols], m2m=[1, 0], dtype="f32", data=x.cpu().numpy(),
+                   dimensions=[1], reduce_kind="add", init=0.0, prologue={"ops": ["exp"]}, out_dims=[rows],
+                   out_m2m=[0], out_dtype="f32")
+    ref, asum = run_oracle(f)
+    torch.cuda.synchronize()
+    check(f, out.cpu().numpy(), ref, asum)
+    n = 68
+    p = torch.from_numpy(inp.uniform_f32(g, n * n + 1, 0.5, 2)).cuda()[1:]
+    o = torch.empty(n * n + 1, dtype=torch.float32, device="cuda")[1:]
+    hf.transpose_fusion(p, [n, n], "f32", [1, 0], o, prologue={"ops": ["log"]}, self_add=True)
+    f = inp.Fusion(name="u2", kind="transpose", dims=[n, n], m2m=[1, 0], dtype="f32", data=p.cpu().numpy(),
+                   permutation=[1, 0], self_add=True, prologue={"ops": ["log"]}, out_dims=[n, n], out_m2m=[1, 0],
+                   out_dtype="f32")
+    ref, _ = run_oracle(f)
+    torch.cuda.synchronize()
+    check(f, o.cpu().numpy(), ref, None)
+
+
+# ---- quantized relayout ----------------------------------------------------------------------------------
+def _qspec(g, n, per_axis_dim, smin=-128, smax=127):
+    if per_axis_dim is None:
+        return {"scales": np.array([np.float32(g.uniform(0.01, 0.2))], np.float32),
+                "zero_points": np.array([int(g.integers(-5, 6))], np.int32), "quantization_dimension": None,
+                "storage_min": smin, "storage_max": smax}
+    return {"scales": inp.uniform_f32(g, n, 0.001, 0.1), "zero_points": inp.integers(g, n, -20, 20, np.int32),
+            "quantization_dimension": per_axis_dim, "storage_min": smin, "storage_max": smax}
+
+
+@pytest.mark.parametrize("n0,n1", [(128, 128), (256, 384), (130, 200), (7, 3), (4096, 16)])
+def test_quant_relayout_variants(n0, n1):
+    g = inp.rng(n0 + n1)
+    q = inp.integers(g, n0 * n1, -128, 127, np.int8)
+    dims = [n0, n1]
+    for qin_dim, qout_dim in ((1, None), (0, None), (None, None), (1, 0), (None, 1)):
+        qin = _qspec(g, dims[qin_dim] if qin_dim is not None else 1, qin_dim)
+        qout = _qspec(g, dims[qout_dim] if qout_dim is not None else 1, qout_dim, smin=-100, smax=90)
+        for out_m2m in ([0, 1], [1, 0]):
+            f = inp.Fusion(name="q", kind="quant", dims=dims, m2m=[1, 0], dtype="s8", data=q, in_q=qin,
+                           out_q=qout, out_dims=dims, out_m2m=out_m2m, out_dtype="s8")
+            ref, _ = run_oracle(f)
+            check(f, run_gpu(f), ref, None)
+    # float output and a float op between dequantize and quantize
+    qin = _qspec(g, n1, 1)
+    f = inp.Fusion(name="qf", kind="quant", dims=dims, m2m=[1, 0], dtype="s8", data=q, in_q=qin, out_q=None,
+                   out_dims=dims, out_m2m=[0, 1], out_dtype="f32")
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+    f = inp.Fusion(name="qn", kind="quant", dims=dims, m2m=[1, 0], dtype="s8", data=q, in_q=qin,
+                   out_q=_qspec(g, 1, None), prologue={"ops": ["neg", "abs"]}, out_dims=dims, out_m2m=[0, 1],
+                   out_dtype="s8")
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
+def test_quant_division_ties():
+    """Reals that land exactly on half-integers after division take the exact-division branch and round
+    to even: scale_in = scale_out * k/2 for odd k."""
+    n0, n1 = 256, 256
+    g = inp.rng(6)
+    q = inp.integers(g, n0 * n1, -128, 127, np.int8)
+    qin = {"scales": np.full(n1, 0.025, np.float32), "zero_points": np.zeros(n1, np.int32),
+           "quantization_dimension": 1}
+    qout = {"scales": np.array([0.05], np.float32), "zero_points": np.array([0], np.int32),
+            "quantization_dimension": None}
+    f = inp.Fusion(name="qt", kind="quant", dims=[n0, n1], m2m=[1, 0], dtype="s8", data=q, in_q=qin, out_q=qout,
+                   out_dims=[n0, n1], out_m2m=[0, 1], out_dtype="s8")
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
+# ---- the correctly rounded log ------------------------------------------------------------------------------
+def _gpu_log_bits(first: int, count: int) -> np.ndarray:
+    x = torch.arange(first, first + count, dtype=torch.int64, device="cuda").to(torch.int32).view(torch.float32)
+    y = torch.empty_like(x)
+    hf.transpose_fusion(x, [count], "f32", [0], y, prologue={"ops": ["log"]})
+    torch.cuda.synchronize()
+    return y.view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+def test_log_exhaustive_on_the_input_range():
+    """Every f32 in [0.5, 2) -- the range the transpose workload draws from -- bit-exact."""
+    first, last = 0x3F000000, 0x40000000
+    bad, examples = oracle.check_log_f32(first, _gpu_log_bits(first, last - first))
+    assert bad == 0, [hex(v) for v in examples]
+
+
+def test_log_exhaustive_all_floats():
+    """Every f32 bit pattern with the sign bit clear (zero, subnormals, normals, inf, NaNs), bit-exact;
+    and a sample of negative inputs (NaN)."""
+    chunk = 1 << 27
+    total_bad = 0
+    examples = []
+    for first in range(0, 1 << 31, chunk):
+        bad, ex = oracle.check_log_f32(first, _gpu_log_bits(first, chunk))
+        total_bad += bad
+        examples += ex
+    assert total_bad == 0, [hex(v) for v in examples[:16]]
+    bad, ex = oracle.check_log_f32(0x80000000, _gpu_log_bits(0x80000000 - (1 << 32), 1 << 20))
+    assert bad == 0

@@ -1,0 +1,144 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every entry point the header
+declares, and rejects invalid arguments (the spec's constraints) before touching the device."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+import transpose_heroes_gb300 as hf
+from transpose_heroes_gb300 import build as hbuild
+
+HEADER = os.path.join(ROOT, "include", "hlo_fusion.h")
+FAKE_IN, FAKE_OUT = 0x100000, 0x900000  # never dereferenced: every call below fails validation first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    hbuild.build()
+    return hf.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:hlo_status|size_t|const char\*)\s+(hlo_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(hf.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert "sm_103a" in hf.version()
+
+
+def test_library_is_built_for_sm_103a_only():
+    text = open(hbuild.__file__).read()
+    assert "arch=compute_103a,code=sm_103a" in text
+
+
+def _status(call):
+    with pytest.raises(hf.HloError) as e:
+        call()
+    return e.value.status, str(e.value)
+
+
+def test_reduce_validation(lib):
+    x = FAKE_IN
+    out = FAKE_OUT
+    # C5: repeated dimension
+    st, msg = _status(lambda: hf.reduce_fusion(x, [4, 5], "f32", [1, 1], "add", 0.0, out, "f32", stream=0))
+    assert st == 1 and "C5" in msg
+    # C4: dimension out of range
+    st, msg = _status(lambda: hf.reduce_fusion(x, [4, 5], "f32", [2], "add", 0.0, out, "f32", stream=0))
+    assert st == 1 and "C4" in msg
+    # layout not a permutation
+    st, msg = _status(lambda: hf.reduce_fusion(x, [4, 5], "f32", [1], "add", 0.0, out, "f32", in_m2m=[0, 0],
+                                               stream=0))
+    assert st == 1 and "minor_to_major" in msg
+    # integer input is not supported by the reduce kernels
+    st, _ = _status(lambda: hf.reduce_fusion(x, [4, 5], "s32", [1], "add", 0.0, out, "f32", stream=0))
+    assert st == 2
+    # input and output overlap
+    st, msg = _status(lambda: hf.reduce_fusion(x, [4, 5], "f32", [1], "add", 0.0, x + 8, "f32", stream=0))
+    assert st == 1 and "overlap" in msg
+
+
+def test_reduce_output_shape_rule_c7(lib):
+    a = hf.make_array([4, 5], None, "f32")
+    o = hf.make_array([5], None, "f32")  # kept dim 0 has size 4, not 5
+    dims = (ctypes.c_int64 * 1)(1)
+    st = lib.hlo_reduce_fusion(ctypes.byref(a), FAKE_IN, None, dims, 1, 0, 0.0, 0, ctypes.byref(o), FAKE_OUT,
+                               None, 0, 0)
+    assert st == 1 and "C7" in hf.last_error()
+    # f64 accumulation is not implemented
+    o = hf.make_array([4], None, "f32")
+    st = lib.hlo_reduce_fusion(ctypes.byref(a), FAKE_IN, None, dims, 1, 0, 0.0, 3, ctypes.byref(o), FAKE_OUT,
+                               None, 0, 0)
+    assert st == 2
+
+
+def test_broadcast_validation(lib):
+    bad_c5 = {"ops": ["add_bcast"], "bcast": {"tensor": 0x5000, "dims": [7], "dtype": "f32",
+                                               "broadcast_dimensions": [1]}}
+    st, msg = _status(lambda: hf.reduce_fusion(FAKE_IN, [4, 5], "f32", [1], "add", 0.0, FAKE_OUT, "f32",
+                                               prologue=bad_c5, stream=0))
+    assert st == 1 and "C5" in msg
+    bad_c3 = {"ops": ["add_bcast"], "bcast": {"tensor": 0x5000, "dims": [5], "dtype": "f32",
+                                               "broadcast_dimensions": [2]}}
+    st, msg = _status(lambda: hf.reduce_fusion(FAKE_IN, [4, 5], "f32", [1], "add", 0.0, FAKE_OUT, "f32",
+                                               prologue=bad_c3, stream=0))
+    assert st == 1 and "C3" in msg
+    bad_type = {"ops": ["add_bcast"], "bcast": {"tensor": 0x5000, "dims": [5], "dtype": "bf16",
+                                                 "broadcast_dimensions": [1]}}
+    st, msg = _status(lambda: hf.reduce_fusion(FAKE_IN, [4, 5], "f32", [1], "add", 0.0, FAKE_OUT, "f32",
+                                               prologue=bad_type, stream=0))
+    assert st == 1 and "C1" in msg
+
+
+def test_transpose_validation(lib):
+    st, msg = _status(lambda: hf.transpose_fusion(FAKE_IN, [3, 4], "f32", [0, 0], FAKE_OUT, stream=0))
+    assert st == 1 and "permutation" in msg
+    st, msg = _status(lambda: hf.transpose_fusion(FAKE_IN, [3, 4], "f32", [1, 0], FAKE_OUT, self_add=True, stream=0))
+    assert st == 1 and "self-add" in msg
+    st, _ = _status(lambda: hf.transpose_fusion(FAKE_IN, [3, 4], "s8", [1, 0], FAKE_OUT,
+                                                prologue={"ops": ["log"]}, stream=0))
+    assert st == 1
+    st, _ = _status(lambda: hf.layout_convert(FAKE_IN, [3, 4], "f32", [1, 0], [1, 1], FAKE_OUT, stream=0))
+    assert st == 1
+
+
+def _q(scales, zps, qd=None, smin=-128, smax=127):
+    return {"host_scales": np.array(scales, np.float32), "host_zero_points": np.array(zps, np.int32),
+            "scales": 0x7000 if qd is not None else None, "zero_points": 0x8000 if qd is not None else None,
+            "quantization_dimension": qd, "storage_min": smin, "storage_max": smax}
+
+
+def test_quant_validation(lib):
+    out_q = _q([0.05], [0])
+    cases = [
+        (_q([0.1, 0.2], [0, 0]), "C11"),                     # per-tensor with two scales
+        (_q([0.1, 0.2, 0.3], [0, 0, 0], qd=1), "C13"),       # per-axis size mismatch
+        (_q([0.0], [0]), "C6"),                              # scale must be > 0
+        (_q([float("inf")], [0]), "C7"),                     # finite
+        (_q([0.1], [200]), "C8"),                            # zero point in storage range
+        (_q([0.1], [0], smin=5, smax=5), "C4"),              # storage_min < storage_max
+        (_q([0.1], [0], qd=4), "C12"),                       # quantization_dimension in range
+    ]
+    for in_q, tag in cases:
+        st, msg = _status(lambda: hf.quant_fusion(FAKE_IN, [4, 5], in_q, [0, 1], FAKE_OUT, out_q=out_q, stream=0))
+        assert st == 1 and tag in msg, (tag, msg)
+    # float output requires f32
+    st, _ = _status(lambda: hf.quant_fusion(FAKE_IN, [4, 5], _q([0.1], [0]), [0, 1], FAKE_OUT, out_dtype="s8",
+                                            out_q=None, stream=0))
+    assert st == 1
+
+
+def test_workspace_size_is_zero(lib):
+    assert hf.reduce_workspace_size([8192, 16384], "bf16", [0]) == 0

@@ -1,0 +1,195 @@
+// Correctly rounded single-precision natural logarithm for sm_103a.
+//
+// The spec defines log as the IEEE-754 log of the element type ("StableHLO Specification", section
+// "log"); IEEE-754 recommends correct rounding, which makes the f32 result unique, so the fused
+// transpose can be bit-exact. The implementation is written from the mathematics:
+//
+//   x = 2^e * m, m in [OFF, 2*OFF) with OFF ~ 0.706; c = the centre of m's table interval,
+//   log x = e*ln2 + log(c) + log1p(r),  r = m * inv_c - 1 (exact: see gen_log_table.py),
+//   log1p(r) = r - r^2/2 + r^3 * (1/3 - r/4 + r^2/5 - r^3/6) + O(r^7).
+//
+// Stage 1 evaluates this sum in float-float arithmetic (Fast2Sum, exact FMA products) to an error
+// below 2^-42 |y| + 2^-23 |r|^3, then applies a rounding test (Ziv's strategy): if the error interval
+// around the float-float value contains no rounding boundary of f32, the leading float is the
+// correctly rounded result. Otherwise (probability ~2^-17 per element) stage 2 recomputes log x in
+// double-double arithmetic via log m = 2 atanh((m-1)/(m+1)) to ~2^-75 relative and rounds that.
+// Special operands (0, negative, subnormal, inf, NaN, exactly 1) also take stage 2.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "log_table.inc"
+
+namespace hlo {
+
+// ------------------------------------------------------------------------------------------------
+// double-double helpers (Dekker / Knuth error-free transformations)
+// ------------------------------------------------------------------------------------------------
+struct dd {
+  double hi, lo;
+};
+
+__device__ __forceinline__ dd dd_two_sum(double a, double b) {
+  double s = __dadd_rn(a, b);
+  double bb = __dsub_rn(s, a);
+  double err = __dadd_rn(__dsub_rn(a, __dsub_rn(s, bb)), __dsub_rn(b, bb));
+  return {s, err};
+}
+
+__device__ __forceinline__ dd dd_fast_two_sum(double a, double b) {  // requires |a| >= |b|
+  double s = __dadd_rn(a, b);
+  return {s, __dsub_rn(b, __dsub_rn(s, a))};
+}
+
+__device__ __forceinline__ dd dd_two_prod(double a, double b) {
+  double p = __dmul_rn(a, b);
+  return {p, __fma_rn(a, b, -p)};
+}
+
+__device__ __forceinline__ dd dd_add(dd x, dd y) {  // accurate: two_sum on both components
+  dd s = dd_two_sum(x.hi, y.hi);
+  dd t = dd_two_sum(x.lo, y.lo);
+  s.lo = __dadd_rn(s.lo, t.hi);
+  s = dd_fast_two_sum(s.hi, s.lo);
+  s.lo = __dadd_rn(s.lo, t.lo);
+  return dd_fast_two_sum(s.hi, s.lo);
+}
+
+__device__ __forceinline__ dd dd_mul(dd x, dd y) {
+  dd p = dd_two_prod(x.hi, y.hi);
+  p.lo = __fma_rn(x.hi, y.lo, p.lo);
+  p.lo = __fma_rn(x.lo, y.hi, p.lo);
+  return dd_fast_two_sum(p.hi, p.lo);
+}
+
+__device__ __forceinline__ dd dd_recip_int(double k) {  // 1/k as a double-double, k a small integer
+  double h = __drcp_rn(k);
+  double l = __ddiv_rn(__fma_rn(-h, k, 1.0), k);
+  return {h, l};
+}
+
+// Rounds the double-double value y (|y.lo| <= ulp(y.hi)/2) to the nearest f32, ties to even.
+__device__ __forceinline__ float dd_to_f32_rn(dd y) {
+  float f = __double2float_rn(y.hi);
+  double d = __dadd_rn(__dsub_rn(y.hi, (double)f), y.lo);  // y - f; the first difference is exact
+  if (d == 0.0) return f;
+  float nb = d > 0 ? __int_as_float(__float_as_int(f) + ((f >= 0.0f) ? 1 : -1))
+                   : __int_as_float(__float_as_int(f) + ((f > 0.0f) ? -1 : 1));
+  if (f == 0.0f) nb = d > 0 ? 1e-45f : -1e-45f;
+  double half = __dmul_rn(__dsub_rn((double)nb, (double)f), 0.5);  // signed half gap towards d
+  double ad = fabs(d), ah = fabs(half);
+  if (ad < ah) return f;
+  if (ad > ah) return nb;
+  return (__float_as_uint(f) & 1u) ? nb : f;  // exact tie: even significand
+}
+
+// ------------------------------------------------------------------------------------------------
+// Stage 2: double-double evaluation (also handles every special operand).
+// ------------------------------------------------------------------------------------------------
+static __device__ __noinline__ float cr_logf_accurate(float x) {
+  uint32_t ix = __float_as_uint(x);
+  if (x != x) return x;                                   // NaN stays NaN
+  if ((ix & 0x7FFFFFFFu) == 0) return __int_as_float(0xFF800000);  // log(+-0) = -inf
+  if (ix >> 31) return __int_as_float(0x7FC00000);        // negative: invalid, quiet NaN
+  if (ix == 0x7F800000u) return x;                        // log(+inf) = +inf
+  if (ix == 0x3F800000u) return 0.0f;                     // log(1) = +0
+  int eadj = 0;
+  if (ix < 0x00800000u) {                                 // subnormal: scale into the normal range
+    ix = __float_as_uint(x * 8388608.0f);
+    eadj = -23;
+  }
+  uint32_t tmp = ix - HLO_LOG_OFF;
+  int e = ((int)tmp >> 23) + eadj;
+  double m = (double)__uint_as_float(ix - (tmp & 0xFF800000u));
+  // s = (m - 1) / (m + 1) as a double-double; numerator and denominator are exact doubles
+  double num = __dsub_rn(m, 1.0), den = __dadd_rn(m, 1.0);
+  double sh = __ddiv_rn(num, den);
+  double sl = __ddiv_rn(__fma_rn(-sh, den, num), den);
+  dd s = dd_fast_two_sum(sh, sl);
+  dd z = dd_mul(s, s);
+  // U = z/3 + z^2/5 + z^3/7 + z^4 W(z): W in double, the rest in double-double (|z| < 0.03)
+  double zd = z.hi;
+  double w = 1.0 / 35.0;
+  w = __fma_rn(w, zd, 1.0 / 33.0);
+  w = __fma_rn(w, zd, 1.0 / 31.0);
+  w = __fma_rn(w, zd, 1.0 / 29.0);
+  w = __fma_rn(w, zd, 1.0 / 27.0);
+  w = __fma_rn(w, zd, 1.0 / 25.0);
+  w = __fma_rn(w, zd, 1.0 / 23.0);
+  w = __fma_rn(w, zd, 1.0 / 21.0);
+  w = __fma_rn(w, zd, 1.0 / 19.0);
+  w = __fma_rn(w, zd, 1.0 / 17.0);
+  w = __fma_rn(w, zd, 1.0 / 15.0);
+  w = __fma_rn(w, zd, 1.0 / 13.0);
+  w = __fma_rn(w, zd, 1.0 / 11.0);
+  w = __fma_rn(w, zd, 1.0 / 9.0);
+  dd u = {w, 0.0};
+  u = dd_add(dd_mul(u, z), dd_recip_int(7.0));
+  u = dd_add(dd_mul(u, z), dd_recip_int(5.0));
+  u = dd_add(dd_mul(u, z), dd_recip_int(3.0));
+  u = dd_mul(u, z);                                       // U
+  dd one_u = dd_add({1.0, 0.0}, u);
+  dd two_s = {__dmul_rn(2.0, s.hi), __dmul_rn(2.0, s.lo)};
+  dd logm = dd_mul(two_s, one_u);                         // log m = 2 s (1 + U)
+  // e * ln2 with ln2 as a double-double constant
+  const dd ln2 = {0x1.62e42fefa39efp-1, 0x1.abc9e3b39803fp-56};
+  double ed = (double)e;
+  dd eln2 = dd_two_prod(ln2.hi, ed);
+  eln2.lo = __fma_rn(ln2.lo, ed, eln2.lo);
+  eln2 = dd_fast_two_sum(eln2.hi, eln2.lo);
+  dd y = dd_add(eln2, logm);
+  return dd_to_f32_rn(y);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Stage 1. ctab/etab may point to shared or global copies of kLogCTab / kLogETab.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ float cr_logf(float x, const float4* __restrict__ ctab,
+                                         const float2* __restrict__ etab) {
+  uint32_t ix = __float_as_uint(x);
+  if (ix - 0x00800000u >= 0x7F000000u) return cr_logf_accurate(x);  // not a positive normal
+  uint32_t tmp = ix - HLO_LOG_OFF;
+  int e = (int)tmp >> 23;
+  uint32_t i = (tmp >> HLO_LOG_SHIFT) & (HLO_LOG_NC - 1);
+  float m = __uint_as_float(ix - (tmp & 0xFF800000u));
+  float4 c = ctab[i];                       // inv_c, log c hi, log c lo
+  float2 E = etab[e - HLO_LOG_EMIN];        // e*ln2 hi, lo
+  float r = __fmaf_rn(m, c.x, -1.0f);       // exact by table construction
+  // s1 = E_hi + logc_hi: E_hi is 0 or dominates, so Fast2Sum is exact
+  float s1 = __fadd_rn(E.x, c.y);
+  float e1 = __fsub_rn(c.y, __fsub_rn(s1, E.x));
+  // s2 = s1 + r: s1 is 0 or |s1| >= |r| (table check / |e*ln2| - |log c| > |r|)
+  float s2 = __fadd_rn(s1, r);
+  float e2 = __fsub_rn(r, __fsub_rn(s2, s1));
+  // -r^2/2 split exactly into qh + ql
+  float hr = -0.5f * r;
+  float qh = __fmul_rn(hr, r);
+  float ql = __fmaf_rn(hr, r, -qh);
+  float s3 = __fadd_rn(s2, qh);
+  float e3 = __fsub_rn(qh, __fsub_rn(s3, s2));
+  // r^3 (1/3 - r/4 + r^2/5 - r^3/6)
+  float p = __fmaf_rn(r, -0.16666667f, 0.2f);
+  p = __fmaf_rn(r, p, -0.25f);
+  p = __fmaf_rn(r, p, 0.33333334f);
+  float r3 = __fmul_rn(__fmul_rn(r, r), r);
+  float lo = __fmaf_rn(r3, p, ql);
+  lo = __fadd_rn(lo, __fadd_rn(E.y, c.z));
+  lo = __fadd_rn(lo, __fadd_rn(__fadd_rn(e1, e2), e3));
+  float yh = __fadd_rn(s3, lo);
+  float yl = __fsub_rn(lo, __fsub_rn(yh, s3));
+  // rounding test: boundary at half an ulp of yh; powers of two and y = 0 go to stage 2
+  float err = __fmaf_rn(fabsf(yh), 0x1p-42f, __fmul_rn(fabsf(r3), 0x1p-23f));
+  uint32_t yb = __float_as_uint(yh);
+  float half_ulp = __uint_as_float((yb & 0x7F800000u) - (24u << 23));
+  bool ambiguous = (__fadd_rn(fabsf(yl), err) >= half_ulp) | ((yb & 0x007FFFFFu) == 0u);
+  if (ambiguous) return cr_logf_accurate(x);
+  return yh;
+}
+
+// Loads the tables into shared memory (called by all threads of a block, followed by a barrier).
+__device__ __forceinline__ void load_log_tables(float4* sc, float2* se) {
+  for (int i = threadIdx.x; i < HLO_LOG_NC; i += blockDim.x) sc[i] = kLogCTab[i];
+  for (int i = threadIdx.x; i < HLO_LOG_NE; i += blockDim.x) se[i] = kLogETab[i];
+}
+
+}  // namespace hlo

@@ -1,0 +1,733 @@
+// C-ABI entry points of libhlofusion: argument validation against the spec's constraints, layout
+// canonicalization (unit dimensions dropped, dimensions adjacent in both memory orders merged), plan
+// selection and kernel launch. No device memory is allocated here.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "hlo_fusion.h"
+#include "hlo_internal.h"
+
+using namespace hlo;
+
+namespace {
+
+thread_local std::string g_err;
+
+hlo_status fail(hlo_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+hlo_status ok() {
+  g_err.clear();
+  return HLO_OK;
+}
+
+hlo_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return ok();
+  return fail(HLO_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool is_float(int dt) { return dt == F32 || dt == BF16 || dt == F16; }
+
+// ---- arrays --------------------------------------------------------------------------------------
+hlo_status check_array(const hlo_array* a, const char* what) {
+  if (!a) return fail(HLO_ERR_INVALID_ARG, "%s: array descriptor is NULL", what);
+  if (a->rank < 0 || a->rank > HLO_MAX_RANK)
+    return fail(HLO_ERR_INVALID_ARG, "%s: rank %d outside 0..%d", what, a->rank, HLO_MAX_RANK);
+  if (dt_bytes(a->dtype) == 0) return fail(HLO_ERR_INVALID_ARG, "%s: unknown element type %d", what, a->dtype);
+  bool seen[HLO_MAX_RANK] = {false};
+  for (int k = 0; k < a->rank; ++k) {
+    if (a->dims[k] < 0) return fail(HLO_ERR_INVALID_ARG, "%s: dimension %d has negative size", what, k);
+    const int64_t d = a->minor_to_major[k];
+    if (d < 0 || d >= a->rank || seen[d])
+      return fail(HLO_ERR_INVALID_ARG, "%s: minor_to_major is not a permutation of 0..%d", what, a->rank - 1);
+    seen[d] = true;
+  }
+  // element count must fit comfortably in 62 bits of bytes
+  long double n = 1;
+  for (int k = 0; k < a->rank; ++k) n *= (long double)a->dims[k];
+  if (n * dt_bytes(a->dtype) > 4.0e18L) return fail(HLO_ERR_INVALID_ARG, "%s: array too large", what);
+  return HLO_OK;
+}
+
+int64_t numel(const hlo_array& a) {
+  int64_t n = 1;
+  for (int k = 0; k < a.rank; ++k) n *= a.dims[k];
+  return n;
+}
+
+// stride[d] of logical dimension d in elements, from minor_to_major.
+void strides_of(const hlo_array& a, int64_t* stride) {
+  int64_t s = 1;
+  for (int k = 0; k < a.rank; ++k) {
+    stride[a.minor_to_major[k]] = s;
+    s *= a.dims[a.minor_to_major[k]];
+  }
+}
+
+bool ranges_overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
+  if (abytes <= 0 || bbytes <= 0) return false;
+  const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+  return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+// ---- chains --------------------------------------------------------------------------------------
+// Validates a chain attached to array `arr` and builds the kernel descriptor.
+hlo_status make_chain(const hlo_ew_chain* c, const hlo_array& arr, bool allow_bcast, const char* what, Chain* out,
+                      int force_dt = -1) {
+  std::memset(out, 0, sizeof *out);
+  out->dt = force_dt >= 0 ? force_dt : arr.dtype;
+  if (!c || c->n_ops == 0) return HLO_OK;
+  if (c->n_ops < 0 || c->n_ops > HLO_MAX_EW_OPS)
+    return fail(HLO_ERR_INVALID_ARG, "%s: n_ops %d outside 0..%d", what, c->n_ops, HLO_MAX_EW_OPS);
+  if (!is_float(out->dt))
+    return fail(HLO_ERR_INVALID_ARG, "%s: elementwise ops need a floating-point element type (exponential/log C1)", what);
+  out->n = c->n_ops;
+  out->round16 = c->round_intermediates ? 1 : 0;
+  for (int k = 0; k < c->n_ops; ++k) {
+    const int op = c->ops[k];
+    if (op < HLO_EW_EXP || op > HLO_EW_ADD_BCAST) return fail(HLO_ERR_INVALID_ARG, "%s: unknown op %d", what, op);
+    out->op[k] = op;
+    if (op != HLO_EW_ADD_BCAST) continue;
+    if (!allow_bcast) return fail(HLO_ERR_UNSUPPORTED, "%s: add of a broadcast operand is not supported here", what);
+    hlo_status st = check_array(&c->bcast, "broadcast operand");
+    if (st != HLO_OK) return st;
+    const hlo_array& b = c->bcast;
+    if (b.dtype != out->dt)
+      return fail(HLO_ERR_INVALID_ARG, "%s: add (C1): broadcast operand type %d differs from %d", what, b.dtype, out->dt);
+    bool used[HLO_MAX_RANK] = {false};
+    int64_t bstr[HLO_MAX_RANK];
+    strides_of(b, bstr);
+    for (int d = 0; d < b.rank; ++d) {
+      const int64_t bd = c->bcast_dimensions[d];
+      if (bd < 0 || bd >= arr.rank)
+        return fail(HLO_ERR_INVALID_ARG, "%s: broadcast_in_dim (C3): broadcast_dimensions[%d] = %lld out of range",
+                    what, d, (long long)bd);
+      if (used[bd]) return fail(HLO_ERR_INVALID_ARG, "%s: broadcast_in_dim (C4): broadcast_dimensions not unique", what);
+      used[bd] = true;
+      if (b.dims[d] != 1 && b.dims[d] != arr.dims[bd])
+        return fail(HLO_ERR_INVALID_ARG, "%s: broadcast_in_dim (C5): operand dim %d has size %lld, result dim %lld has %lld",
+                    what, d, (long long)b.dims[d], (long long)bd, (long long)arr.dims[bd]);
+      if (b.dims[d] != 1) out->bstride[bd] += bstr[d];
+    }
+    if (!c->bcast_ptr && numel(b) > 0) return fail(HLO_ERR_INVALID_ARG, "%s: broadcast operand pointer is NULL", what);
+    out->bptr = c->bcast_ptr;
+    out->bdt = b.dtype;
+  }
+  return HLO_OK;
+}
+
+bool chain_has_bcast(const Chain& c) {
+  for (int k = 0; k < c.n; ++k)
+    if (c.op[k] == OP_ADD_BCAST) return true;
+  return false;
+}
+
+// Builds an IndexMap over axes (major first) with the given sizes and target strides, merging axes
+// that are contiguous in the target.
+IndexMap make_map(const std::vector<int64_t>& size, const std::vector<int64_t>& stride) {
+  std::vector<int64_t> sz, st;
+  for (size_t j = 0; j < size.size(); ++j) {
+    if (size[j] == 1) continue;
+    if (!sz.empty() && st.back() == stride[j] * size[j]) {
+      sz.back() *= size[j];
+      st.back() = stride[j];
+    } else {
+      sz.push_back(size[j]);
+      st.push_back(stride[j]);
+    }
+  }
+  IndexMap m;
+  std::memset(&m, 0, sizeof m);
+  m.n = (int)sz.size();
+  for (int j = 0; j < m.n; ++j) {
+    m.size[j] = sz[j];
+    m.stride[j] = st[j];
+  }
+  m.identity = (m.n == 0 || (m.n == 1 && st[0] == 1)) ? 1 : 0;
+  return m;
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---- quantization parameters ---------------------------------------------------------------------
+hlo_status check_quant(const hlo_quant* q, const hlo_array& a, const char* what, QuantParams* out) {
+  std::memset(out, 0, sizeof *out);
+  if (!q) return fail(HLO_ERR_INVALID_ARG, "%s: quantization parameters are NULL", what);
+  const int qd = q->quantization_dimension;
+  if (qd < -1 || qd >= a.rank)
+    return fail(HLO_ERR_INVALID_ARG, "%s: quantized type (C12): quantization_dimension %d out of range", what, qd);
+  if (qd < 0 && q->n != 1)
+    return fail(HLO_ERR_INVALID_ARG, "%s: quantized type (C11): per-tensor quantization needs exactly 1 scale", what);
+  if (qd >= 0 && q->n != a.dims[qd])
+    return fail(HLO_ERR_INVALID_ARG, "%s: quantized type (C13): %lld scales for a dimension of size %lld", what,
+                (long long)q->n, (long long)a.dims[qd]);
+  if (!(-128 <= q->storage_min && q->storage_min < q->storage_max && q->storage_max <= 127))
+    return fail(HLO_ERR_INVALID_ARG, "%s: quantized type (C4): storage range [%d, %d] invalid for i8", what,
+                q->storage_min, q->storage_max);
+  if (q->host_scales) {
+    for (int64_t i = 0; i < q->n; ++i) {
+      const float s = q->host_scales[i];
+      if (!(s > 0.0f)) return fail(HLO_ERR_INVALID_ARG, "%s: quantized type (C6): scale[%lld] is not > 0", what, (long long)i);
+      if (!std::isfinite(s)) return fail(HLO_ERR_INVALID_ARG, "%s: quantized type (C7): scale[%lld] is not finite", what, (long long)i);
+    }
+  }
+  if (q->host_zero_points) {
+    for (int64_t i = 0; i < q->n; ++i) {
+      const int32_t z = q->host_zero_points[i];
+      if (z < q->storage_min || z > q->storage_max)
+        return fail(HLO_ERR_INVALID_ARG, "%s: quantized type (C8): zero_point[%lld] = %d outside [%d, %d]", what,
+                    (long long)i, z, q->storage_min, q->storage_max);
+    }
+  }
+  out->axis = qd;
+  out->smin = q->storage_min;
+  out->smax = q->storage_max;
+  if (qd < 0) {
+    if (!q->host_scales || !q->host_zero_points)
+      return fail(HLO_ERR_INVALID_ARG, "%s: per-tensor parameters need host_scales and host_zero_points", what);
+    out->scale = q->host_scales[0];
+    out->zp = q->host_zero_points[0];
+    volatile float one = 1.0f;
+    out->inv_scale = one / out->scale;  // IEEE division on the host: RN(1/scale)
+  } else {
+    if ((!q->scales || !q->zero_points) && q->n > 0)
+      return fail(HLO_ERR_INVALID_ARG, "%s: per-axis parameters need device scales and zero_points", what);
+    out->scales = q->scales;
+    out->zps = q->zero_points;
+  }
+  return HLO_OK;
+}
+
+// ---- physical canonicalization of a permutation ---------------------------------------------------
+// Input logical dims in input physical order (major first) and, for the output, the input logical dim
+// each output physical axis reads. Unit dims are dropped; runs adjacent in both orders are merged.
+struct Canon {
+  int k = 0;
+  int64_t size[HLO_MAX_RANK];
+  int out_pos[HLO_MAX_RANK];  // position of canonical axis j in the output physical order (major first)
+};
+
+Canon canonicalize(const hlo_array& in, const int64_t* perm, const int64_t* out_m2m) {
+  const int rank = in.rank;
+  std::vector<int> pin, pout;  // input logical dims, major first
+  for (int k = rank - 1; k >= 0; --k)
+    if (in.dims[in.minor_to_major[k]] != 1) pin.push_back((int)in.minor_to_major[k]);
+  for (int k = rank - 1; k >= 0; --k) {
+    const int od = (int)out_m2m[k];
+    const int idim = (int)perm[od];
+    if (in.dims[idim] != 1) pout.push_back(idim);
+  }
+  // groups: maximal runs of pin that also appear consecutively, in the same order, in pout
+  std::vector<std::vector<int>> groups;
+  for (size_t i = 0; i < pin.size(); ++i) {
+    if (!groups.empty()) {
+      const int prev = groups.back().back();
+      const auto itp = std::find(pout.begin(), pout.end(), prev);
+      if (itp + 1 != pout.end() && *(itp + 1) == pin[i]) {
+        groups.back().push_back(pin[i]);
+        continue;
+      }
+    }
+    groups.push_back({pin[i]});
+  }
+  Canon c;
+  c.k = (int)groups.size();
+  for (int j = 0; j < c.k; ++j) {
+    int64_t s = 1;
+    for (int d : groups[j]) s *= in.dims[d];
+    c.size[j] = s;
+    const int first = groups[j].front();
+    int pos = 0;
+    for (int g = 0; g < c.k; ++g) {
+      // rank of group j among groups by the output position of their first dims
+      const int fg = groups[g].front();
+      const auto pj = std::find(pout.begin(), pout.end(), first) - pout.begin();
+      const auto pg = std::find(pout.begin(), pout.end(), fg) - pout.begin();
+      if (pg < pj) ++pos;
+    }
+    c.out_pos[j] = pos;
+  }
+  return c;
+}
+
+// ---- planners --------------------------------------------------------------------------------------
+hlo_status plan_gather_plain(const hlo_array& in, const void* in_ptr, const hlo_array& out, void* out_ptr,
+                             const int64_t* perm, int self_add, const Chain& pro, const Chain& epi, cudaStream_t s) {
+  GatherPlan g;
+  std::memset(&g, 0, sizeof g);
+  g.in = in_ptr;
+  g.out = out_ptr;
+  g.kind = G_PLAIN;
+  g.rank = out.rank;
+  g.n = numel(out);
+  int64_t istr[HLO_MAX_RANK];
+  strides_of(in, istr);
+  for (int j = 0; j < out.rank; ++j) {
+    const int od = (int)out.minor_to_major[out.rank - 1 - j];
+    g.out_size[j] = out.dims[od];
+    g.out_logical[j] = od;
+  }
+  for (int k = 0; k < out.rank; ++k) {
+    g.perm[k] = (int)perm[k];
+    g.in_stride_of_out[k] = istr[perm[k]];
+    g.self_stride_of_out[k] = istr[k];
+  }
+  g.self_add = self_add;
+  g.in_dt = in.dtype;
+  g.out_dt = out.dtype;
+  g.elem_bytes = dt_bytes(in.dtype);
+  g.pro = pro;
+  g.epi = epi;
+  return cuda_status(launch_gather(g, s), "gather kernel launch");
+}
+
+}  // namespace
+
+int hlo::device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+extern "C" {
+
+const char* hlo_last_error(void) { return g_err.c_str(); }
+
+const char* hlo_version(void) { return "hlofusion 0.1 (sm_103a)"; }
+
+size_t hlo_reduce_workspace_size(const hlo_array* in, const int64_t* dimensions, int32_t n_dimensions,
+                                 int32_t accum_dtype) {
+  (void)in;
+  (void)dimensions;
+  (void)n_dimensions;
+  (void)accum_dtype;
+  return 0;
+}
+
+hlo_status hlo_reduce_fusion(const hlo_array* in, const void* in_ptr, const hlo_ew_chain* prologue,
+                             const int64_t* dimensions, int32_t n_dimensions, int32_t kind, double init_value,
+                             int32_t accum_dtype, const hlo_array* out, void* out_ptr, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  hlo_status st = check_array(in, "reduce input");
+  if (st != HLO_OK) return st;
+  st = check_array(out, "reduce output");
+  if (st != HLO_OK) return st;
+  if (kind != HLO_RED_ADD && kind != HLO_RED_MAX) return fail(HLO_ERR_INVALID_ARG, "reduce: unknown body %d", kind);
+  if (accum_dtype != HLO_F32) return fail(HLO_ERR_UNSUPPORTED, "reduce: only f32 accumulation is implemented");
+  if (!is_float(in->dtype)) return fail(HLO_ERR_UNSUPPORTED, "reduce: input element type %d not supported", in->dtype);
+  if (!is_float(out->dtype)) return fail(HLO_ERR_UNSUPPORTED, "reduce: output element type %d not supported", out->dtype);
+  if (n_dimensions < 0 || n_dimensions > in->rank)
+    return fail(HLO_ERR_INVALID_ARG, "reduce (C4): %d dimensions for rank %d", n_dimensions, in->rank);
+  if (n_dimensions > 0 && !dimensions) return fail(HLO_ERR_INVALID_ARG, "reduce: dimensions is NULL");
+  bool red[HLO_MAX_RANK] = {false};
+  for (int i = 0; i < n_dimensions; ++i) {
+    const int64_t d = dimensions[i];
+    if (d < 0 || d >= in->rank)
+      return fail(HLO_ERR_INVALID_ARG, "reduce (C4): dimension %lld outside [0, %d)", (long long)d, in->rank);
+    if (red[d]) return fail(HLO_ERR_INVALID_ARG, "reduce (C5): dimension %lld repeated", (long long)d);
+    red[d] = true;
+  }
+  std::vector<int> kept;
+  for (int d = 0; d < in->rank; ++d)
+    if (!red[d]) kept.push_back(d);
+  if (out->rank != (int)kept.size())
+    return fail(HLO_ERR_INVALID_ARG, "reduce (C7): output rank %d, expected %d", out->rank, (int)kept.size());
+  for (size_t k = 0; k < kept.size(); ++k)
+    if (out->dims[k] != in->dims[kept[k]])
+      return fail(HLO_ERR_INVALID_ARG, "reduce (C7): output dim %d is %lld, expected %lld", (int)k,
+                  (long long)out->dims[k], (long long)in->dims[kept[k]]);
+  Chain chain;
+  st = make_chain(prologue, *in, true, "reduce prologue", &chain);
+  if (st != HLO_OK) return st;
+  const int64_t n_in = numel(*in), n_out = numel(*out);
+  if (n_in > 0 && !in_ptr) return fail(HLO_ERR_INVALID_ARG, "reduce: input pointer is NULL");
+  if (n_out > 0 && !out_ptr) return fail(HLO_ERR_INVALID_ARG, "reduce: output pointer is NULL");
+  if (ranges_overlap(in_ptr, n_in * dt_bytes(in->dtype), out_ptr, n_out * dt_bytes(out->dtype)))
+    return fail(HLO_ERR_INVALID_ARG, "reduce: input and output overlap");
+  const cudaStream_t s = as_stream(stream);
+  const float init = (float)init_value;
+  if (n_out == 0) return ok();
+  int64_t n_red = 1;
+  for (int d = 0; d < in->rank; ++d)
+    if (red[d]) n_red *= in->dims[d];
+  if (n_red == 0) return cuda_status(launch_fill(out_ptr, out->dtype, n_out, init, s), "fill kernel launch");
+
+  int64_t istr[HLO_MAX_RANK], ostr_out[HLO_MAX_RANK];
+  strides_of(*in, istr);
+  strides_of(*out, ostr_out);
+  int64_t ostr_in[HLO_MAX_RANK] = {0};  // output stride of each kept INPUT logical dim
+  for (size_t k = 0; k < kept.size(); ++k) ostr_in[kept[k]] = ostr_out[k];
+
+  // physical axes of the input, major first, unit dims dropped; runs of reduced / kept dims
+  struct Run {
+    bool reduced;
+    int64_t size;
+    std::vector<int> dims;
+  };
+  std::vector<Run> runs;
+  for (int k = in->rank - 1; k >= 0; --k) {
+    const int d = (int)in->minor_to_major[k];
+    if (in->dims[d] == 1) continue;
+    if (!runs.empty() && runs.back().reduced == red[d]) {
+      runs.back().size *= in->dims[d];
+      runs.back().dims.push_back(d);
+    } else {
+      runs.push_back({red[d], in->dims[d], {d}});
+    }
+  }
+  int n_red_runs = 0;
+  for (auto& r : runs) n_red_runs += r.reduced ? 1 : 0;
+  // kept dims in input physical order (major first), for the row -> output / broadcast maps
+  std::vector<int> kept_phys;
+  for (auto& r : runs)
+    if (!r.reduced)
+      for (int d : r.dims) kept_phys.push_back(d);
+  auto kept_map = [&](const int64_t* target_stride_by_dim) {
+    std::vector<int64_t> sz, st2;
+    for (int d : kept_phys) {
+      sz.push_back(in->dims[d]);
+      st2.push_back(target_stride_by_dim[d]);
+    }
+    return make_map(sz, st2);
+  };
+
+  const bool has_bcast = chain_has_bcast(chain);
+  const bool row_pattern = n_red_runs == 0 || (n_red_runs == 1 && runs.back().reduced);
+  const bool col_pattern = n_red_runs == 1 && !runs.back().reduced;
+
+  if (row_pattern) {
+    RowReducePlan p;
+    std::memset(&p, 0, sizeof p);
+    p.in = in_ptr;
+    p.out = out_ptr;
+    p.len = n_red_runs ? runs.back().size : 1;
+    p.rows = n_in / p.len;
+    p.in_dt = in->dtype;
+    p.out_dt = out->dtype;
+    p.kind = kind;
+    p.init = init;
+    p.chain = chain;
+    p.omap = kept_map(ostr_in);
+    p.bmode = BC_NONE;
+    bool ok_plan = true;
+    if (has_bcast) {
+      bool kept_zero = true, red_match = true, red_zero = true;
+      for (int d = 0; d < in->rank; ++d) {
+        if (in->dims[d] == 1) continue;
+        if (red[d]) {
+          if (chain.bstride[d] != istr[d]) red_match = false;
+          if (chain.bstride[d] != 0) red_zero = false;
+        } else if (chain.bstride[d] != 0) {
+          kept_zero = false;
+        }
+      }
+      if (kept_zero && red_match && n_red_runs == 1) {
+        p.bmode = BC_ROWVEC;
+      } else if (red_zero) {
+        p.bmode = BC_PERROW;
+        p.bmap = kept_map(chain.bstride);
+      } else {
+        ok_plan = false;
+      }
+    }
+    if (ok_plan) return cuda_status(launch_row_reduce(p, s), "row reduce launch");
+  } else if (col_pattern && !has_bcast) {
+    ColReducePlan p;
+    std::memset(&p, 0, sizeof p);
+    p.in = in_ptr;
+    p.out = out_ptr;
+    p.a = 1;
+    p.b = 1;
+    bool before = true;
+    for (auto& r : runs) {
+      if (r.reduced) {
+        p.r = r.size;
+        before = false;
+      } else if (before) {
+        p.a *= r.size;
+      } else {
+        p.b *= r.size;
+      }
+    }
+    p.in_dt = in->dtype;
+    p.out_dt = out->dtype;
+    p.kind = kind;
+    p.init = init;
+    p.chain = chain;
+    p.omap = kept_map(ostr_in);
+    if (p.a <= 65535) return cuda_status(launch_col_reduce(p, s), "column reduce launch");
+  }
+
+  // general plan
+  GenReducePlan g;
+  std::memset(&g, 0, sizeof g);
+  g.in = in_ptr;
+  g.out = out_ptr;
+  g.in_dt = in->dtype;
+  g.out_dt = out->dtype;
+  g.kind = kind;
+  g.init = init;
+  g.chain = chain;
+  g.n_out = n_out;
+  g.n_red = n_red;
+  g.rank = in->rank;
+  g.nk = out->rank;
+  for (int j = 0; j < out->rank; ++j) {
+    const int od = (int)out->minor_to_major[out->rank - 1 - j];
+    g.kdim_size[j] = out->dims[od];
+    g.kdim_logical[j] = kept[od];
+    g.kdim_in_stride[j] = istr[kept[od]];
+  }
+  for (int k = in->rank - 1; k >= 0; --k) {
+    const int d = (int)in->minor_to_major[k];
+    if (!red[d]) continue;
+    g.rdim_size[g.nr] = in->dims[d];
+    g.rdim_in_stride[g.nr] = istr[d];
+    g.rdim_logical[g.nr] = d;
+    ++g.nr;
+  }
+  return cuda_status(launch_gen_reduce(g, s), "general reduce launch");
+}
+
+hlo_status hlo_transpose_fusion(const hlo_array* in, const void* in_ptr, const hlo_ew_chain* prologue,
+                                const int64_t* permutation, int32_t self_add_epilogue, const hlo_ew_chain* epilogue,
+                                const hlo_array* out, void* out_ptr, void* stream) {
+  hlo_status st = check_array(in, "transpose input");
+  if (st != HLO_OK) return st;
+  st = check_array(out, "transpose output");
+  if (st != HLO_OK) return st;
+  if (out->rank != in->rank) return fail(HLO_ERR_INVALID_ARG, "transpose: output rank differs from input rank");
+  if (out->dtype != in->dtype) return fail(HLO_ERR_INVALID_ARG, "transpose: output element type differs from input");
+  if (in->rank > 0 && !permutation) return fail(HLO_ERR_INVALID_ARG, "transpose: permutation is NULL");
+  bool seen[HLO_MAX_RANK] = {false};
+  for (int k = 0; k < in->rank; ++k) {
+    const int64_t p = permutation[k];
+    if (p < 0 || p >= in->rank || seen[p])
+      return fail(HLO_ERR_INVALID_ARG, "transpose: permutation is not a permutation of 0..%d", in->rank - 1);
+    seen[p] = true;
+    if (out->dims[k] != in->dims[p])
+      return fail(HLO_ERR_INVALID_ARG, "transpose: output dim %d is %lld, expected dims(in)[%lld] = %lld", k,
+                  (long long)out->dims[k], (long long)p, (long long)in->dims[p]);
+    if (self_add_epilogue && out->dims[k] != in->dims[k])
+      return fail(HLO_ERR_INVALID_ARG, "transpose: the self-add form needs dims(out) == dims(in) (add C1)");
+  }
+  Chain pro, epi;
+  st = make_chain(prologue, *in, true, "transpose prologue", &pro);
+  if (st != HLO_OK) return st;
+  st = make_chain(epilogue, *out, false, "transpose epilogue", &epi);
+  if (st != HLO_OK) return st;
+  const int64_t n = numel(*in);
+  const int64_t bytes = n * dt_bytes(in->dtype);
+  if (n > 0 && (!in_ptr || !out_ptr)) return fail(HLO_ERR_INVALID_ARG, "transpose: NULL data pointer");
+  if (ranges_overlap(in_ptr, bytes, out_ptr, bytes)) return fail(HLO_ERR_INVALID_ARG, "transpose: input and output overlap");
+  if (n == 0) return ok();
+  const cudaStream_t s = as_stream(stream);
+  const bool bcast = chain_has_bcast(pro);
+
+  if (self_add_epilogue) {
+    // fast pair-tile path: a square matrix once unit dims are dropped, transposed, same memory order
+    std::vector<int> nonunit;
+    for (int d = 0; d < in->rank; ++d)
+      if (in->dims[d] != 1) nonunit.push_back(d);
+    bool pair = in->dtype == F32 && !bcast && nonunit.size() == 2;
+    if (pair) {
+      const int da = nonunit[0], db = nonunit[1];
+      pair = in->dims[da] == in->dims[db] && permutation[da] == db && permutation[db] == da;
+      auto minor_of = [&](const hlo_array& a) {
+        for (int k = 0; k < a.rank; ++k)
+          if (a.dims[a.minor_to_major[k]] != 1) return (int)a.minor_to_major[k];
+        return -1;
+      };
+      pair = pair && minor_of(*in) == minor_of(*out);
+    }
+    if (pair) {
+      SelfAddPlan p;
+      std::memset(&p, 0, sizeof p);
+      p.in = in_ptr;
+      p.out = out_ptr;
+      p.n = in->dims[nonunit[0]];
+      p.dt = in->dtype;
+      p.pro = pro;
+      p.epi = epi;
+      return cuda_status(launch_selfadd_transpose(p, s), "self-add transpose launch");
+    }
+    return plan_gather_plain(*in, in_ptr, *out, out_ptr, permutation, 1, pro, epi, s);
+  }
+  if (bcast) return plan_gather_plain(*in, in_ptr, *out, out_ptr, permutation, 0, pro, epi, s);
+
+  Canon c = canonicalize(*in, permutation, out->minor_to_major);
+  bool identity = true;
+  for (int j = 0; j < c.k; ++j)
+    if (c.out_pos[j] != j) identity = false;
+  if (identity) return cuda_status(launch_elementwise(in_ptr, out_ptr, n, in->dtype, pro, epi, s), "elementwise launch");
+  const int ax_a = c.k - 1;
+  int ax_b = -1;
+  for (int j = 0; j < c.k; ++j)
+    if (c.out_pos[j] == c.k - 1) ax_b = j;
+  if (ax_b == ax_a || ax_b < 0) return plan_gather_plain(*in, in_ptr, *out, out_ptr, permutation, 0, pro, epi, s);
+  TilePlan t;
+  std::memset(&t, 0, sizeof t);
+  t.in = in_ptr;
+  t.out = out_ptr;
+  t.k = c.k;
+  int64_t sacc = 1;
+  for (int j = c.k - 1; j >= 0; --j) {
+    t.size[j] = c.size[j];
+    t.in_stride[j] = sacc;
+    sacc *= c.size[j];
+  }
+  // output strides: axes ordered by out_pos, minor (largest position) first
+  std::vector<int> by_pos(c.k);
+  for (int j = 0; j < c.k; ++j) by_pos[c.out_pos[j]] = j;
+  sacc = 1;
+  for (int q = c.k - 1; q >= 0; --q) {
+    t.out_stride[by_pos[q]] = sacc;
+    sacc *= c.size[by_pos[q]];
+  }
+  t.ax_a = ax_a;
+  t.ax_b = ax_b;
+  t.n_batch = 1;
+  for (int j = 0; j < c.k; ++j) {
+    if (j == ax_a || j == ax_b) continue;
+    t.batch_axis[t.nbatch_axes++] = j;
+    t.n_batch *= c.size[j];
+  }
+  t.dt = in->dtype;
+  t.pro = pro;
+  t.epi = epi;
+  return cuda_status(launch_tile_transpose(t, s), "tiled transpose launch");
+}
+
+hlo_status hlo_layout_convert(const hlo_array* in, const void* in_ptr, const int64_t* out_minor_to_major,
+                              void* out_ptr, void* stream) {
+  hlo_status st = check_array(in, "layout_convert input");
+  if (st != HLO_OK) return st;
+  if (in->rank > 0 && !out_minor_to_major) return fail(HLO_ERR_INVALID_ARG, "layout_convert: out_minor_to_major is NULL");
+  hlo_array out = *in;
+  for (int k = 0; k < in->rank; ++k) out.minor_to_major[k] = out_minor_to_major[k];
+  st = check_array(&out, "layout_convert output");
+  if (st != HLO_OK) return st;
+  int64_t perm[HLO_MAX_RANK];
+  for (int k = 0; k < in->rank; ++k) perm[k] = k;
+  return hlo_transpose_fusion(in, in_ptr, nullptr, perm, 0, nullptr, &out, out_ptr, stream);
+}
+
+hlo_status hlo_quant_fusion(const hlo_array* in, const void* in_ptr, const hlo_quant* in_q,
+                            const hlo_ew_chain* float_ops, const int64_t* out_minor_to_major, const hlo_array* out,
+                            void* out_ptr, const hlo_quant* out_q, void* stream) {
+  hlo_status st = check_array(in, "quant input");
+  if (st != HLO_OK) return st;
+  st = check_array(out, "quant output");
+  if (st != HLO_OK) return st;
+  if (in->dtype != S8) return fail(HLO_ERR_UNSUPPORTED, "quant: storage type must be s8");
+  if (out->rank != in->rank) return fail(HLO_ERR_INVALID_ARG, "quant: output rank differs from input rank");
+  for (int d = 0; d < in->rank; ++d)
+    if (out->dims[d] != in->dims[d]) return fail(HLO_ERR_INVALID_ARG, "quant: a layout change keeps the shape; dim %d differs", d);
+  if (in->rank > 0 && out_minor_to_major)
+    for (int k = 0; k < in->rank; ++k)
+      if (out->minor_to_major[k] != out_minor_to_major[k])
+        return fail(HLO_ERR_INVALID_ARG, "quant: out_minor_to_major differs from out->minor_to_major");
+  QuantParams qin, qout;
+  std::memset(&qout, 0, sizeof qout);
+  st = check_quant(in_q, *in, "quant input parameters", &qin);
+  if (st != HLO_OK) return st;
+  const bool out_float = out_q == nullptr;
+  if (out_float) {
+    if (out->dtype != F32) return fail(HLO_ERR_INVALID_ARG, "quant: without output parameters the output must be f32");
+  } else {
+    if (out->dtype != S8) return fail(HLO_ERR_UNSUPPORTED, "quant: quantized output storage must be s8");
+    st = check_quant(out_q, *out, "quant output parameters", &qout);
+    if (st != HLO_OK) return st;
+  }
+  Chain ops;
+  st = make_chain(float_ops, *in, true, "quant float ops", &ops, F32);
+  if (st != HLO_OK) return st;
+  const int64_t n = numel(*in);
+  if (n > 0 && (!in_ptr || !out_ptr)) return fail(HLO_ERR_INVALID_ARG, "quant: NULL data pointer");
+  if (ranges_overlap(in_ptr, n, out_ptr, n * dt_bytes(out->dtype)))
+    return fail(HLO_ERR_INVALID_ARG, "quant: input and output overlap");
+  if (n == 0) return ok();
+  const cudaStream_t s = as_stream(stream);
+
+  // fast path: two non-unit dims (i major, j minor in the input), output with i minor
+  std::vector<int> nonunit;
+  for (int d = 0; d < in->rank; ++d)
+    if (in->dims[d] != 1) nonunit.push_back(d);
+  auto minor_of = [&](const hlo_array& a) {
+    for (int k = 0; k < a.rank; ++k)
+      if (a.dims[a.minor_to_major[k]] != 1) return (int)a.minor_to_major[k];
+    return -1;
+  };
+  if (!out_float && nonunit.size() == 2 && !chain_has_bcast(ops)) {
+    const int jd = minor_of(*in);
+    const int id = nonunit[0] == jd ? nonunit[1] : nonunit[0];
+    if (minor_of(*out) == id) {
+      auto axis_of = [&](int qd) { return qd < 0 ? -1 : qd == id ? 0 : qd == jd ? 1 : -2; };
+      const int ain = axis_of(qin.axis), aout = axis_of(qout.axis);
+      if (ain != -2 && aout != -2) {
+        QuantTilePlan p;
+        std::memset(&p, 0, sizeof p);
+        p.in = reinterpret_cast<const int8_t*>(in_ptr);
+        p.out = reinterpret_cast<int8_t*>(out_ptr);
+        p.n0 = in->dims[id];
+        p.n1 = in->dims[jd];
+        p.qin = qin;
+        p.qin.axis = ain;
+        p.qout = qout;
+        p.qout.axis = aout;
+        p.ops = ops;
+        return cuda_status(launch_quant_tile(p, s), "quantized tile launch");
+      }
+    }
+  }
+  GatherPlan g;
+  std::memset(&g, 0, sizeof g);
+  g.in = in_ptr;
+  g.out = out_ptr;
+  g.kind = G_QUANT;
+  g.rank = in->rank;
+  g.n = n;
+  int64_t istr[HLO_MAX_RANK];
+  strides_of(*in, istr);
+  for (int j = 0; j < out->rank; ++j) {
+    const int od = (int)out->minor_to_major[out->rank - 1 - j];
+    g.out_size[j] = out->dims[od];
+    g.out_logical[j] = od;
+  }
+  for (int k = 0; k < in->rank; ++k) {
+    g.perm[k] = k;
+    g.in_stride_of_out[k] = istr[k];
+  }
+  g.in_dt = S8;
+  g.out_dt = out->dtype;
+  g.elem_bytes = 1;
+  g.pro = ops;
+  g.qin = qin;
+  g.qout = qout;
+  g.qin_axis_out = qin.axis;
+  g.qout_axis_out = out_float ? -1 : qout.axis;
+  g.out_float = out_float ? 1 : 0;
+  return cuda_status(launch_gather(g, s), "quantized gather launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,191 @@
+// Internal plan structures shared by the host planner (hlo_api.cu) and the kernel translation units.
+// Every structure here is plain data passed to kernels by value.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace hlo {
+
+enum Dt : int { F32 = 0, BF16 = 1, S8 = 2, F16 = 3, S32 = 4 };
+enum Op : int { OP_NONE = 0, OP_EXP = 1, OP_LOG = 2, OP_ABS = 3, OP_NEG = 4, OP_ADD_BCAST = 5 };
+enum Red : int { RED_ADD = 0, RED_MAX = 1 };
+
+constexpr int kMaxRank = 8;
+constexpr int kMaxOps = 4;
+
+inline __host__ __device__ int dt_bytes(int dt) {
+  return dt == F32 || dt == S32 ? 4 : dt == BF16 || dt == F16 ? 2 : dt == S8 ? 1 : 0;
+}
+
+// A linear index decomposed over up to kMaxRank axes (major first) and re-composed with other
+// strides: offset(k) = sum_j ((k / inner_j) % size_j) * stride_j. Used for "row k -> output offset"
+// and "row k -> broadcast offset" maps. identity != 0 means offset(k) == k.
+struct IndexMap {
+  int n;
+  int identity;
+  int64_t size[kMaxRank];
+  int64_t stride[kMaxRank];
+};
+
+__host__ __device__ inline int64_t map_index(const IndexMap& m, int64_t k) {
+  if (m.identity) return k;
+  int64_t off = 0;
+  for (int j = m.n - 1; j >= 0; --j) {
+    int64_t s = m.size[j];
+    off += (k % s) * m.stride[j];
+    k /= s;
+  }
+  return off;
+}
+
+// Elementwise chain as the kernels see it. dt is the element type of the array the chain is
+// attached to; round16 = round every op result to dt (16-bit float types only).
+// Broadcast operand: bptr/bdt and, for the general kernels, bstride[d] = offset contribution of the
+// fused array's logical index in dimension d (0 where the operand is broadcast).
+struct Chain {
+  int n;
+  int op[kMaxOps];
+  int round16;
+  int dt;
+  const void* bptr;
+  int bdt;
+  int64_t bstride[kMaxRank];
+};
+
+// Broadcast addressing in the fast row-reduce kernel.
+enum BcastMode : int { BC_NONE = 0, BC_ROWVEC = 1, BC_PERROW = 2 };
+
+struct RowReducePlan {
+  const void* in;
+  void* out;
+  int64_t rows;     // K
+  int64_t len;      // R, elements per row (contiguous)
+  int in_dt, out_dt, kind;
+  float init;
+  Chain chain;
+  int bmode;        // BcastMode
+  IndexMap bmap;    // BC_PERROW: row -> broadcast offset
+  IndexMap omap;    // row -> output offset
+};
+
+struct ColReducePlan {
+  const void* in;
+  void* out;
+  int64_t a, r, b;  // [A, R, B] in physical order, B contiguous
+  int in_dt, out_dt, kind;
+  float init;
+  Chain chain;      // no broadcast in this kernel
+  IndexMap omap;    // (a * B + b) -> output offset
+};
+
+// General reduce: one thread per output element.
+struct GenReducePlan {
+  const void* in;
+  void* out;
+  int in_dt, out_dt, kind;
+  float init;
+  Chain chain;
+  int64_t n_out, n_red;
+  // output element (linear index in output physical order) -> logical kept index
+  int nk;
+  int64_t kdim_size[kMaxRank];     // kept axes in output physical order (major first)
+  int64_t kdim_in_stride[kMaxRank];
+  int kdim_logical[kMaxRank];      // logical dimension of the input
+  int nr;
+  int64_t rdim_size[kMaxRank];     // reduced axes in input physical order (major first)
+  int64_t rdim_in_stride[kMaxRank];
+  int rdim_logical[kMaxRank];
+  int rank;
+};
+
+// Pair-tile transpose with self add: out = f(in) + f(in)^T for a square 2-D array (after removing
+// unit dimensions) with identical input/output layouts; physically [n, n] row-major.
+struct SelfAddPlan {
+  const void* in;
+  void* out;
+  int64_t n;
+  int dt;
+  Chain pro, epi;
+};
+
+// Tiled transpose of canonical physical axes: input axes 0..k-1 (major..minor, contiguous strides),
+// output written with out_stride per axis. Axis a_in = k-1 (input-minor), axis b = output-minor.
+struct TilePlan {
+  const void* in;
+  void* out;
+  int k;
+  int64_t size[kMaxRank];
+  int64_t in_stride[kMaxRank];
+  int64_t out_stride[kMaxRank];
+  int ax_a;           // input-minor axis (stride 1 in input)
+  int ax_b;           // output-minor axis (stride 1 in output)
+  int64_t n_batch;    // product of the other axes
+  int nbatch_axes;
+  int batch_axis[kMaxRank];
+  int dt;             // element type
+  Chain pro, epi;     // f32 chains only (no broadcast)
+};
+
+// Quantized relayout of a 2-D s8 array: logical [n0, n1], input row-major (dim 1 minor), output
+// column-major (dim 0 minor); per-axis or per-tensor dequantize, quantize per-tensor or per-axis.
+struct QuantParams {
+  int axis;                 // quantization dimension in the 2-D canonical view: 0, 1 or -1
+  const float* scales;      // device, when per-axis
+  const int32_t* zps;       // device, when per-axis
+  float scale;              // per-tensor
+  int32_t zp;               // per-tensor
+  float inv_scale;          // per-tensor: RN(1 / scale), used by the division shortcut
+  int32_t smin, smax;
+};
+
+struct QuantTilePlan {
+  const int8_t* in;
+  int8_t* out;
+  int64_t n0, n1;
+  QuantParams qin, qout;
+  Chain ops;                // f32 chain on the dequantized value (no broadcast)
+};
+
+// General elementwise gather: one thread per output element (output physical order).
+// Covers transposes, layout changes and quantized relayouts the fast kernels do not.
+enum GatherKind : int { G_PLAIN = 0, G_QUANT = 1 };
+struct GatherPlan {
+  const void* in;
+  void* out;
+  int kind;
+  int rank;
+  int64_t n;
+  int64_t out_size[kMaxRank];       // output logical dims in output physical order (major first)
+  int out_logical[kMaxRank];        // output logical dimension of each physical axis
+  int64_t in_stride_of_out[kMaxRank];   // input stride for each output logical dim (via permutation)
+  int64_t self_stride_of_out[kMaxRank]; // self-add: input stride of the same logical index
+  int self_add;
+  int in_dt, out_dt;
+  int elem_bytes;
+  Chain pro, epi;                   // pro.bstride is per INPUT logical dim, epi has no broadcast
+  int perm[kMaxRank];               // out logical dim k reads input logical dim perm[k]
+  // quant
+  int qin_axis_out;                 // output logical dim of the input quantization axis (-1)
+  int qout_axis_out;                // output logical dim of the output quantization axis (-1)
+  QuantParams qin, qout;
+  int out_float;                    // quant with float output
+};
+
+// Kernel launchers (defined in the k_*.cu translation units). Return the launch status.
+cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s);
+cudaError_t launch_col_reduce(const ColReducePlan& p, cudaStream_t s);
+cudaError_t launch_gen_reduce(const GenReducePlan& p, cudaStream_t s);
+cudaError_t launch_fill(void* out, int dt, int64_t n, float value, cudaStream_t s);
+cudaError_t launch_selfadd_transpose(const SelfAddPlan& p, cudaStream_t s);
+cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s);
+cudaError_t launch_quant_tile(const QuantTilePlan& p, cudaStream_t s);
+cudaError_t launch_gather(const GatherPlan& p, cudaStream_t s);
+cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, const Chain& pro, const Chain& epi,
+                               cudaStream_t s);
+
+// Device properties cached per device (SM count, cluster support).
+int device_sm_count();
+
+}  // namespace hlo

@@ -1,0 +1,487 @@
+// Reduce-hero kernels ("StableHLO Specification", section "reduce"; "XLA:GPU Emitters": the reduction
+// emitter reduces with warp shuffles and shared memory).
+//
+//  row_reduce_kernel  -- reduced dimensions are the minor-most physical ones: the input is [K, R] with
+//                        rows contiguous. Persistent blocks walk rows; every thread streams 16-byte
+//                        vectors of the row, applies the prologue in registers and accumulates in f32;
+//                        the block combines through warp shuffles and shared memory.
+//  col_reduce_kernel  -- kept dimensions on both sides: the input is [A, R, B] with B contiguous.
+//                        A thread owns one 16-byte column vector; the 8 warps of a block split the rows
+//                        of a slab; a thread-block cluster of kColCluster blocks splits R into slabs and
+//                        block rank 0 combines the slab partials read from the others' shared memory
+//                        (distributed shared memory), so one launch produces the output, no workspace.
+//  gen_reduce_kernel  -- any other pattern: one thread per output element.
+#include <cooperative_groups.h>
+
+#include "device_common.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace hlo {
+
+// Compiled prologue chains of the row kernel.
+enum RowChain : int { RC_NONE = 0, RC_EXP = 1, RC_EXP_BCAST_BF16 = 2, RC_RT = 3 };
+
+constexpr int kRowThreads = 512;
+constexpr int kRowUnroll = 4;
+
+template <int KIND>
+__device__ __forceinline__ float block_reduce(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = combine<KIND>(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  if (warp == 0) {
+    v = lane < nw ? red[lane] : identity<KIND>();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = combine<KIND>(v, __shfl_xor_sync(0xffffffffu, v, o));
+  }
+  __syncthreads();
+  return v;  // valid in thread 0
+}
+
+__device__ __forceinline__ void store_result(void* out, int dt, int64_t off, float v) {
+  store_from_f32(out, dt, off, v);
+}
+
+// ---- element kernels of the row reduce --------------------------------------------------------
+// Processes one 16-byte vector: f32 x4 or 16-bit x8.
+template <int IN_DT, int CH, int KIND>
+__device__ __forceinline__ float row_vec(uint4 x, uint4 b, float acc, const Chain& ch, const LogTab& lt) {
+  if (IN_DT == F32) {
+    float v[4] = {__uint_as_float(x.x), __uint_as_float(x.y), __uint_as_float(x.z), __uint_as_float(x.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float t = v[i];
+      if (CH == RC_EXP) t = fast_exp(t);
+      if (CH == RC_RT) t = apply_chain_rt<true>(ch, t, 0, lt);
+      acc = combine<KIND>(acc, t);
+    }
+    return acc;
+  } else {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    float part = identity<KIND>();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      if (IN_DT == BF16) {
+        lo = bf16_bits_to_f32(w[i] & 0xFFFFu);
+        hi = __uint_as_float(w[i] & 0xFFFF0000u);
+      } else {
+        lo = f16_bits_to_f32((uint16_t)(w[i] & 0xFFFFu));
+        hi = f16_bits_to_f32((uint16_t)(w[i] >> 16));
+      }
+      if (CH == RC_EXP_BCAST_BF16) {
+        // bf16(exp(x)) then the bf16 add with the broadcast pair, rounded once (add.rn.bf16x2)
+        float elo = fast_exp(lo), ehi = fast_exp(hi);
+        uint32_t e2, s2;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(e2) : "f"(ehi), "f"(elo));
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(s2) : "r"(e2), "r"(bw[i]));
+        lo = __uint_as_float(s2 << 16);
+        hi = __uint_as_float(s2 & 0xFFFF0000u);
+      } else {
+        if (CH == RC_EXP) {
+          lo = fast_exp(lo);
+          hi = fast_exp(hi);
+          if (ch.round16) {
+            lo = round_to_dt(lo, IN_DT);
+            hi = round_to_dt(hi, IN_DT);
+          }
+        }
+        if (CH == RC_RT) {
+          lo = apply_chain_rt<true>(ch, lo, 0, lt);
+          hi = apply_chain_rt<true>(ch, hi, 0, lt);
+        }
+      }
+      part = combine<KIND>(part, combine<KIND>(lo, hi));
+    }
+    return combine<KIND>(acc, part);
+  }
+}
+
+// VEC = elements per 16-byte vector (4 for f32, 8 for 16-bit) or 1 for the scalar variant.
+template <int IN_DT, int VEC, int CH, int KIND>
+__global__ void __launch_bounds__(kRowThreads) row_reduce_kernel(RowReducePlan p) {
+  __shared__ float red[32];
+  __shared__ float4 s_lc[HLO_LOG_NC];
+  __shared__ float2 s_le[HLO_LOG_NE];
+  LogTab lt = global_log_tables();
+  if (CH == RC_RT && chain_has_log(p.chain)) {
+    load_log_tables(s_lc, s_le);
+    __syncthreads();
+    lt = {s_lc, s_le};
+  }
+  const int eb = IN_DT == F32 ? 4 : 2;
+  const int64_t len = p.len;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    const char* base = reinterpret_cast<const char*>(p.in) + row * len * eb;
+    float acc = identity<KIND>();
+    int64_t tail_start = 0;
+    if (VEC > 1) {
+      const int64_t nvec = len / VEC;
+      const uint4* xv = reinterpret_cast<const uint4*>(base);
+      const uint4* bv = reinterpret_cast<const uint4*>(p.chain.bptr);
+      int64_t v = tid;
+      for (; v + (kRowUnroll - 1) * (int64_t)nt < nvec; v += kRowUnroll * (int64_t)nt) {
+        uint4 x[kRowUnroll], b[kRowUnroll];
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) {
+          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(x[u].x), "=r"(x[u].y), "=r"(x[u].z), "=r"(x[u].w)
+                       : "l"(xv + v + u * nt));
+        }
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) {
+          if (CH == RC_EXP_BCAST_BF16) b[u] = __ldg(bv + v + u * nt);
+          else b[u] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) acc = row_vec<IN_DT, CH, KIND>(x[u], b[u], acc, p.chain, lt);
+      }
+      for (; v < nvec; v += nt) {
+        uint4 x = __ldg(xv + v);
+        uint4 b = CH == RC_EXP_BCAST_BF16 ? __ldg(bv + v) : make_uint4(0, 0, 0, 0);
+        acc = row_vec<IN_DT, CH, KIND>(x, b, acc, p.chain, lt);
+      }
+      tail_start = nvec * VEC;
+    }
+    // scalar elements (all of them for VEC == 1, the ragged tail otherwise)
+    for (int64_t e = tail_start + tid; e < len; e += nt) {
+      float t = load_as_f32(base, IN_DT, e);
+      if (CH == RC_EXP) {
+        t = fast_exp(t);
+        if (p.chain.round16) t = round_to_dt(t, IN_DT);
+      } else if (CH == RC_EXP_BCAST_BF16) {
+        t = round_to_dt(fast_exp(t), BF16);
+        t = round_to_dt(__fadd_rn(t, load_as_f32(p.chain.bptr, BF16, e)), BF16);
+      } else if (CH == RC_RT) {
+        int64_t boff = p.bmode == BC_ROWVEC ? e : p.bmode == BC_PERROW ? map_index(p.bmap, row) : 0;
+        t = apply_chain_rt<true>(p.chain, t, boff, lt);
+      }
+      acc = combine<KIND>(acc, t);
+    }
+    acc = block_reduce<KIND>(acc, red);
+    if (tid == 0) store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+  }
+}
+
+// Row kernel for the runtime chain when the broadcast operand is per row or the vector path does
+// not apply: scalar loads, any chain.
+template <int IN_DT, int KIND>
+__global__ void __launch_bounds__(kRowThreads) row_reduce_rt_kernel(RowReducePlan p) {
+  __shared__ float red[32];
+  __shared__ float4 s_lc[HLO_LOG_NC];
+  __shared__ float2 s_le[HLO_LOG_NE];
+  LogTab lt = global_log_tables();
+  if (chain_has_log(p.chain)) {
+    load_log_tables(s_lc, s_le);
+    __syncthreads();
+    lt = {s_lc, s_le};
+  }
+  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    const char* base = reinterpret_cast<const char*>(p.in) + row * p.len * dt_bytes(IN_DT);
+    const int64_t rowb = p.bmode == BC_PERROW ? map_index(p.bmap, row) : 0;
+    float acc = identity<KIND>();
+    for (int64_t e = threadIdx.x; e < p.len; e += blockDim.x) {
+      float t = load_as_f32(base, IN_DT, e);
+      int64_t boff = p.bmode == BC_ROWVEC ? e : rowb;
+      t = apply_chain_rt<true>(p.chain, t, boff, lt);
+      acc = combine<KIND>(acc, t);
+    }
+    acc = block_reduce<KIND>(acc, red);
+    if (threadIdx.x == 0) store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+  }
+}
+
+template <typename K>
+static int occupancy_blocks(K kernel, int threads) {
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess || nb < 1) nb = 1;
+  return nb;
+}
+
+template <int IN_DT, int KIND>
+static cudaError_t row_dispatch(const RowReducePlan& p, cudaStream_t s, int ch, bool vec) {
+  auto launch = [&](auto kernel) -> cudaError_t {
+    static int nb = -1;
+    if (nb < 0) nb = occupancy_blocks(kernel, kRowThreads);
+    int64_t grid = (int64_t)device_sm_count() * nb;
+    if (grid > p.rows) grid = p.rows;
+    if (grid < 1) grid = 1;
+    int threads = kRowThreads;
+    // short rows: fewer threads so that lanes are not idle
+    int64_t work = vec ? (p.len / (IN_DT == F32 ? 4 : 8)) : p.len;
+    while (threads > 64 && work <= threads / 2) threads >>= 1;
+    kernel<<<(unsigned)grid, threads, 0, s>>>(p);
+    return cudaGetLastError();
+  };
+  constexpr int V = IN_DT == F32 ? 4 : 8;
+  if (ch == RC_RT && p.bmode == BC_PERROW) return launch(row_reduce_rt_kernel<IN_DT, KIND>);
+  if (vec) {
+    switch (ch) {
+      case RC_NONE: return launch(row_reduce_kernel<IN_DT, V, RC_NONE, KIND>);
+      case RC_EXP: return launch(row_reduce_kernel<IN_DT, V, RC_EXP, KIND>);
+      case RC_EXP_BCAST_BF16:
+        if (IN_DT == BF16) return launch(row_reduce_kernel<BF16, 8, RC_EXP_BCAST_BF16, KIND>);
+        break;
+      default: break;
+    }
+    return launch(row_reduce_rt_kernel<IN_DT, KIND>);
+  }
+  switch (ch) {
+    case RC_NONE: return launch(row_reduce_kernel<IN_DT, 1, RC_NONE, KIND>);
+    case RC_EXP: return launch(row_reduce_kernel<IN_DT, 1, RC_EXP, KIND>);
+    default: return launch(row_reduce_rt_kernel<IN_DT, KIND>);
+  }
+}
+
+static int classify_row_chain(const RowReducePlan& p) {
+  const Chain& c = p.chain;
+  if (c.n == 0) return RC_NONE;
+  if (c.n == 1 && c.op[0] == OP_EXP) return RC_EXP;
+  if (c.n == 2 && c.op[0] == OP_EXP && c.op[1] == OP_ADD_BCAST && c.dt == BF16 && c.bdt == BF16 &&
+      c.round16 && p.bmode == BC_ROWVEC)
+    return RC_EXP_BCAST_BF16;
+  return RC_RT;
+}
+
+cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s) {
+  const int eb = dt_bytes(p.in_dt);
+  const int ch = classify_row_chain(p);
+  // 16-byte vectors need 16-byte aligned rows (and broadcast vector, when streamed alongside)
+  bool vec = ((uintptr_t)p.in % 16 == 0) && ((p.len * eb) % 16 == 0);
+  if (ch == RC_EXP_BCAST_BF16) vec = vec && ((uintptr_t)p.chain.bptr % 16 == 0);
+  if (ch == RC_RT) vec = false;
+  if (p.in_dt == F32)
+    return p.kind == RED_ADD ? row_dispatch<F32, RED_ADD>(p, s, ch, vec) : row_dispatch<F32, RED_MAX>(p, s, ch, vec);
+  if (p.in_dt == BF16)
+    return p.kind == RED_ADD ? row_dispatch<BF16, RED_ADD>(p, s, ch, vec) : row_dispatch<BF16, RED_MAX>(p, s, ch, vec);
+  return p.kind == RED_ADD ? row_dispatch<F16, RED_ADD>(p, s, ch, vec) : row_dispatch<F16, RED_MAX>(p, s, ch, vec);
+}
+
+// ---- column reduce --------------------------------------------------------------------------------
+constexpr int kColCluster = 8;
+constexpr int kColWarps = 8;
+constexpr int kColUnroll = 4;
+
+// Block (x = column block * kColCluster + slab, y = a). Each lane owns VEC consecutive columns.
+template <int IN_DT, int VEC, int KIND, bool RT>
+__global__ void __launch_bounds__(kColWarps * 32) col_reduce_kernel(ColReducePlan p, int64_t rows_per_slab) {
+  __shared__ float part[kColWarps][32 * VEC];
+  __shared__ float4 s_lc[HLO_LOG_NC];
+  __shared__ float2 s_le[HLO_LOG_NE];
+  cg::cluster_group cluster = cg::this_cluster();
+  LogTab lt = global_log_tables();
+  if (RT && chain_has_log(p.chain)) {
+    load_log_tables(s_lc, s_le);
+    __syncthreads();
+    lt = {s_lc, s_le};
+  }
+  const int slab = (int)cluster.block_rank();
+  const int64_t colblock = blockIdx.x / kColCluster;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t col0 = (colblock * 32 + lane) * VEC;  // first column of this lane
+  const int eb = dt_bytes(IN_DT);
+  const int64_t B = p.b;
+  const char* base = reinterpret_cast<const char*>(p.in) + (int64_t)blockIdx.y * p.r * B * eb;
+  float acc[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) acc[i] = identity<KIND>();
+  const int64_t r0 = slab * rows_per_slab;
+  const int64_t r1 = min(r0 + rows_per_slab, p.r);
+  const bool active = col0 < B;
+  if (active) {
+    if (VEC > 1) {
+      int64_t r = r0 + warp;
+      for (; r + (kColUnroll - 1) * kColWarps < r1; r += kColUnroll * kColWarps) {
+        uint4 x[kColUnroll];
+#pragma unroll
+        for (int u = 0; u < kColUnroll; ++u) {
+          const uint4* ptr = reinterpret_cast<const uint4*>(base + ((r + u * kColWarps) * B + col0) * eb);
+          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(x[u].x), "=r"(x[u].y), "=r"(x[u].z), "=r"(x[u].w)
+                       : "l"(ptr));
+        }
+#pragma unroll
+        for (int u = 0; u < kColUnroll; ++u) {
+          const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (IN_DT == F32) {
+              float t = __uint_as_float(w[i]);
+              if (RT) t = apply_chain_rt<true>(p.chain, t, 0, lt);
+              acc[i] = combine<KIND>(acc[i], t);
+            } else {
+              float lo = IN_DT == BF16 ? bf16_bits_to_f32(w[i] & 0xFFFFu) : f16_bits_to_f32((uint16_t)(w[i] & 0xFFFFu));
+              float hi = IN_DT == BF16 ? __uint_as_float(w[i] & 0xFFFF0000u) : f16_bits_to_f32((uint16_t)(w[i] >> 16));
+              if (RT) {
+                lo = apply_chain_rt<true>(p.chain, lo, 0, lt);
+                hi = apply_chain_rt<true>(p.chain, hi, 0, lt);
+              }
+              acc[2 * i] = combine<KIND>(acc[2 * i], lo);
+              acc[2 * i + 1] = combine<KIND>(acc[2 * i + 1], hi);
+            }
+          }
+        }
+      }
+      for (; r < r1; r += kColWarps) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(base + (r * B + col0) * eb));
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (IN_DT == F32) {
+            float t = __uint_as_float(w[i]);
+            if (RT) t = apply_chain_rt<true>(p.chain, t, 0, lt);
+            acc[i] = combine<KIND>(acc[i], t);
+          } else {
+            float lo = IN_DT == BF16 ? bf16_bits_to_f32(w[i] & 0xFFFFu) : f16_bits_to_f32((uint16_t)(w[i] & 0xFFFFu));
+            float hi = IN_DT == BF16 ? __uint_as_float(w[i] & 0xFFFF0000u) : f16_bits_to_f32((uint16_t)(w[i] >> 16));
+            if (RT) {
+              lo = apply_chain_rt<true>(p.chain, lo, 0, lt);
+              hi = apply_chain_rt<true>(p.chain, hi, 0, lt);
+            }
+            acc[2 * i] = combine<KIND>(acc[2 * i], lo);
+            acc[2 * i + 1] = combine<KIND>(acc[2 * i + 1], hi);
+          }
+        }
+      }
+    } else {
+      for (int64_t r = r0 + warp; r < r1; r += kColWarps) {
+        float t = load_as_f32(base, IN_DT, r * B + col0);
+        if (RT) t = apply_chain_rt<true>(p.chain, t, 0, lt);
+        acc[0] = combine<KIND>(acc[0], t);
+      }
+    }
+  }
+  // combine the warps of this block
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) part[warp][lane * VEC + i] = acc[i];
+  __syncthreads();
+  for (int c = threadIdx.x; c < 32 * VEC; c += blockDim.x) {
+    float v = part[0][c];
+    for (int w = 1; w < kColWarps; ++w) v = combine<KIND>(v, part[w][c]);
+    part[0][c] = v;
+  }
+  // combine the slabs of the cluster in rank order (deterministic), in block rank 0
+  cluster.sync();
+  if (slab == 0) {
+    for (int c = threadIdx.x; c < 32 * VEC; c += blockDim.x) {
+      float v = part[0][c];
+      for (int q = 1; q < kColCluster; ++q) {
+        const float* peer = cluster.map_shared_rank(&part[0][0], q);
+        v = combine<KIND>(v, peer[c]);
+      }
+      const int64_t col = colblock * 32 * VEC + c;
+      if (col < B) {
+        const int64_t k = (int64_t)blockIdx.y * B + col;
+        store_result(p.out, p.out_dt, map_index(p.omap, k), combine<KIND>(p.init, v));
+      }
+    }
+  }
+  cluster.sync();  // peers keep their shared memory until rank 0 has read it
+}
+
+template <int IN_DT, int VEC, int KIND, bool RT>
+static cudaError_t col_launch(const ColReducePlan& p, cudaStream_t s) {
+  const int64_t ncb = (p.b + 32 * VEC - 1) / (32 * VEC);
+  const int64_t rows_per_slab = (p.r + kColCluster - 1) / kColCluster;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(ncb * kColCluster), (unsigned)p.a, 1);
+  cfg.blockDim = dim3(kColWarps * 32, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kColCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, col_reduce_kernel<IN_DT, VEC, KIND, RT>, p, rows_per_slab);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int IN_DT, int KIND>
+static cudaError_t col_dispatch(const ColReducePlan& p, cudaStream_t s) {
+  constexpr int V = IN_DT == F32 ? 4 : 8;
+  const bool rt = p.chain.n > 0;
+  const bool vec = ((uintptr_t)p.in % 16 == 0) && ((p.b * dt_bytes(IN_DT)) % 16 == 0);
+  if (vec) return rt ? col_launch<IN_DT, V, KIND, true>(p, s) : col_launch<IN_DT, V, KIND, false>(p, s);
+  return rt ? col_launch<IN_DT, 1, KIND, true>(p, s) : col_launch<IN_DT, 1, KIND, false>(p, s);
+}
+
+cudaError_t launch_col_reduce(const ColReducePlan& p, cudaStream_t s) {
+  if (p.in_dt == F32) return p.kind == RED_ADD ? col_dispatch<F32, RED_ADD>(p, s) : col_dispatch<F32, RED_MAX>(p, s);
+  if (p.in_dt == BF16) return p.kind == RED_ADD ? col_dispatch<BF16, RED_ADD>(p, s) : col_dispatch<BF16, RED_MAX>(p, s);
+  return p.kind == RED_ADD ? col_dispatch<F16, RED_ADD>(p, s) : col_dispatch<F16, RED_MAX>(p, s);
+}
+
+// ---- general reduce -------------------------------------------------------------------------------
+// Sums are formed in chunks of 256 terms so that the f32 error stays near (256 + n/256) ulp.
+__global__ void __launch_bounds__(256) gen_reduce_kernel(GenReducePlan p) {
+  const int64_t o = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (o >= p.n_out) return;
+  const LogTab lt = global_log_tables();
+  // decompose o over the kept axes in output physical order
+  int64_t idx[kMaxRank];
+  for (int d = 0; d < kMaxRank; ++d) idx[d] = 0;
+  int64_t rem = o, base = 0, bbase = 0;
+  for (int j = p.nk - 1; j >= 0; --j) {
+    int64_t i = rem % p.kdim_size[j];
+    rem /= p.kdim_size[j];
+    idx[p.kdim_logical[j]] = i;
+    base += i * p.kdim_in_stride[j];
+    bbase += i * p.chain.bstride[p.kdim_logical[j]];
+  }
+  float total = p.kind == RED_ADD ? 0.f : __int_as_float(0xFF800000);
+  float chunk = total;
+  int64_t ridx[kMaxRank];
+  for (int j = 0; j < p.nr; ++j) ridx[j] = 0;
+  for (int64_t t = 0; t < p.n_red; ++t) {
+    int64_t off = base, boff = bbase;
+    for (int j = 0; j < p.nr; ++j) {
+      off += ridx[j] * p.rdim_in_stride[j];
+      boff += ridx[j] * p.chain.bstride[p.rdim_logical[j]];
+    }
+    float v = apply_chain_rt<true>(p.chain, load_as_f32(p.in, p.in_dt, off), boff, lt);
+    chunk = combine_rt(p.kind, chunk, v);
+    if ((t & 255) == 255) {
+      total = combine_rt(p.kind, total, chunk);
+      chunk = p.kind == RED_ADD ? 0.f : __int_as_float(0xFF800000);
+    }
+    for (int j = p.nr - 1; j >= 0; --j) {  // odometer over the reduced axes, minor fastest
+      if (++ridx[j] < p.rdim_size[j]) break;
+      ridx[j] = 0;
+    }
+  }
+  total = combine_rt(p.kind, total, chunk);
+  store_result(p.out, p.out_dt, o, combine_rt(p.kind, p.init, total));
+  (void)idx;
+}
+
+cudaError_t launch_gen_reduce(const GenReducePlan& p, cudaStream_t s) {
+  if (p.n_out == 0) return cudaSuccess;
+  const int64_t blocks = (p.n_out + 255) / 256;
+  gen_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+__global__ void fill_kernel(void* out, int dt, int64_t n, float value) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    store_from_f32(out, dt, i, value);
+}
+
+cudaError_t launch_fill(void* out, int dt, int64_t n, float value, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  fill_kernel<<<(unsigned)blocks, 256, 0, s>>>(out, dt, n, value);
+  return cudaGetLastError();
+}
+
+}  // namespace hlo

@@ -1,0 +1,478 @@
+// Transpose / layout-change hero kernels ("XLA:GPU Emitters", section "Transpose emitter": coalesced
+// reads into a shared-memory tile, a barrier, coalesced writes out of it).
+//
+//  selfadd_pair_kernel  -- out = f(p) + transpose(f(p)) for an n x n array. A block owns the tile
+//                          pair (I,J), (J,I): it loads both once, applies the prologue f once per
+//                          element while staging into padded shared memory, and writes both output
+//                          tiles; so p is read once, f is evaluated once per element (the
+//                          partitioning concern of "XLA:GPU Emitters", section "Partitioning") and the
+//                          output is written once. Persistent blocks walk the pairs.
+//  tile_transpose_kernel -- any physical permutation whose input-minor and output-minor axes
+//                          differ: a 32 x 32 tile over those two axes, other axes batched.
+//  quant_tile_kernel    -- s8 [n0, n1] row-major -> column-major with dequantize / quantize fused:
+//                          128 x 128-byte tiles, 16-byte loads, an XOR-swizzled shared tile read back
+//                          4 bytes at a time, 4x4 byte transposes in registers, 16-byte stores.
+//  gather_kernel        -- everything else: one thread per output element.
+#include "device_common.cuh"
+
+namespace hlo {
+
+// ---------------------------------------------------------------------------------------------
+// pair-tile self-add transpose
+// ---------------------------------------------------------------------------------------------
+constexpr int kT = 64;        // tile edge (elements)
+constexpr int kTP = kT + 1;   // padded row pitch: column reads hit 32 distinct banks
+constexpr int kPairThreads = 256;
+
+enum PairChain : int { PC_NONE = 0, PC_LOG = 1, PC_RT = 2 };
+
+// Maps a pair index to (I, J), I < J, enumerating row by row.
+__device__ __forceinline__ void pair_of(int64_t item, int64_t nt, int64_t& I, int64_t& J) {
+  const double b = 2.0 * (double)nt - 1.0;
+  int64_t i = (int64_t)((b - sqrt(b * b - 8.0 * (double)item)) * 0.5);
+  if (i < 0) i = 0;
+  auto start = [nt](int64_t r) { return r * (nt - 1) - r * (r - 1) / 2; };
+  while (i > 0 && start(i) > item) --i;
+  while (start(i + 1) <= item) ++i;
+  I = i;
+  J = i + 1 + (item - start(i));
+}
+
+template <int CH>
+__device__ __forceinline__ float pair_pro(float v, const Chain& c, const LogTab& lt) {
+  if (CH == PC_LOG) return cr_logf(v, lt.c, lt.e);
+  if (CH == PC_RT) return apply_chain_rt<false>(c, v, 0, lt);
+  return v;
+}
+
+// Loads tile (TI, TJ) of the n x n input into dst (padded), applying the prologue.
+template <int CH, bool VEC>
+__device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t n, int64_t TI, int64_t TJ,
+                                          float* dst, const Chain& c, const LogTab& lt) {
+  const int t = threadIdx.x;
+  if (VEC) {
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = (t >> 4) + 16 * k, col = (t & 15) * 4;
+      const int64_t gr = TI * kT + r, gc = TJ * kT + col;
+      if (gr < n && gc < n) {
+        const float4* src = reinterpret_cast<const float4*>(in + gr * n + gc);
+        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(v[k].x), "=f"(v[k].y), "=f"(v[k].z), "=f"(v[k].w)
+                     : "l"(src));
+      } else {
+        v[k] = make_float4(1.f, 1.f, 1.f, 1.f);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = (t >> 4) + 16 * k, col = (t & 15) * 4;
+      float* d = dst + r * kTP + col;
+      d[0] = pair_pro<CH>(v[k].x, c, lt);
+      d[1] = pair_pro<CH>(v[k].y, c, lt);
+      d[2] = pair_pro<CH>(v[k].z, c, lt);
+      d[3] = pair_pro<CH>(v[k].w, c, lt);
+    }
+  } else {
+    for (int e = t; e < kT * kT; e += kPairThreads) {
+      const int r = e / kT, col = e % kT;
+      const int64_t gr = TI * kT + r, gc = TJ * kT + col;
+      float x = (gr < n && gc < n) ? in[gr * n + gc] : 1.f;
+      dst[r * kTP + col] = pair_pro<CH>(x, c, lt);
+    }
+  }
+}
+
+// Writes out tile (TI, TJ) = own[r][c] + other[c][r], then the epilogue.
+__device__ __forceinline__ void pair_store(float* __restrict__ out, int64_t n, int64_t TI, int64_t TJ,
+                                           const float* own, const float* other, const Chain& epi,
+                                           const LogTab& lt) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll 4
+  for (int rr = 0; rr < kT / (kPairThreads / 32); ++rr) {
+    const int r = warp + rr * (kPairThreads / 32);
+    const int64_t gr = TI * kT + r;
+#pragma unroll
+    for (int h = 0; h < kT / 32; ++h) {
+      const int c = lane + 32 * h;
+      const int64_t gc = TJ * kT + c;
+      float v = __fadd_rn(own[r * kTP + c], other[c * kTP + r]);
+      if (epi.n) v = apply_chain_rt<false>(epi, v, 0, lt);
+      if (gr < n && gc < n) out[gr * n + gc] = v;
+    }
+  }
+}
+
+template <int CH, bool VEC>
+__global__ void __launch_bounds__(kPairThreads, 4)
+    selfadd_pair_kernel(SelfAddPlan p, int64_t nt, int64_t n_off, int64_t n_items) {
+  extern __shared__ float4 smem_f4[];
+  float4* s_lc = smem_f4;
+  float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
+  float* ta = reinterpret_cast<float*>(s_le + HLO_LOG_NE);
+  float* tb = ta + kT * kTP;
+  load_log_tables(s_lc, s_le);
+  __syncthreads();
+  const LogTab lt = {s_lc, s_le};
+  const float* in = reinterpret_cast<const float*>(p.in);
+  float* out = reinterpret_cast<float*>(p.out);
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    int64_t I, J;
+    if (item < n_off) {
+      pair_of(item, nt, I, J);
+    } else {
+      I = J = item - n_off;
+    }
+    pair_load<CH, VEC>(in, p.n, I, J, ta, p.pro, lt);
+    if (I != J) pair_load<CH, VEC>(in, p.n, J, I, tb, p.pro, lt);
+    __syncthreads();
+    if (I != J) {
+      pair_store(out, p.n, I, J, ta, tb, p.epi, lt);
+      pair_store(out, p.n, J, I, tb, ta, p.epi, lt);
+    } else {
+      pair_store(out, p.n, I, I, ta, ta, p.epi, lt);
+    }
+    __syncthreads();
+  }
+}
+
+static size_t pair_smem_bytes() {
+  return HLO_LOG_NC * sizeof(float4) + HLO_LOG_NE * sizeof(float2) + 2 * kT * kTP * sizeof(float);
+}
+
+template <int CH, bool VEC>
+static cudaError_t pair_launch(const SelfAddPlan& p, cudaStream_t s) {
+  auto kernel = selfadd_pair_kernel<CH, VEC>;
+  const size_t smem = pair_smem_bytes();
+  static int nb = -1;
+  if (nb < 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kPairThreads, smem) != cudaSuccess || nb < 1)
+      nb = 1;
+  }
+  const int64_t nt = (p.n + kT - 1) / kT;
+  const int64_t n_off = nt * (nt - 1) / 2;
+  const int64_t n_items = n_off + nt;
+  int64_t grid = (int64_t)device_sm_count() * nb;
+  if (grid > n_items) grid = n_items;
+  if (grid < 1) grid = 1;
+  kernel<<<(unsigned)grid, kPairThreads, smem, s>>>(p, nt, n_off, n_items);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selfadd_transpose(const SelfAddPlan& p, cudaStream_t s) {
+  if (p.n == 0) return cudaSuccess;
+  const bool vec = (p.n % 4 == 0) && ((uintptr_t)p.in % 16 == 0);
+  int ch = PC_RT;
+  if (p.pro.n == 0) ch = PC_NONE;
+  else if (p.pro.n == 1 && p.pro.op[0] == OP_LOG) ch = PC_LOG;
+  if (ch == PC_LOG) return vec ? pair_launch<PC_LOG, true>(p, s) : pair_launch<PC_LOG, false>(p, s);
+  if (ch == PC_NONE) return vec ? pair_launch<PC_NONE, true>(p, s) : pair_launch<PC_NONE, false>(p, s);
+  return vec ? pair_launch<PC_RT, true>(p, s) : pair_launch<PC_RT, false>(p, s);
+}
+
+// ---------------------------------------------------------------------------------------------
+// generic tiled transpose over canonical axes
+// ---------------------------------------------------------------------------------------------
+constexpr int kTT = 32;
+
+template <typename T, bool CHAINS>
+__global__ void __launch_bounds__(256) tile_transpose_kernel(TilePlan p, int64_t nta, int64_t ntb) {
+  __shared__ T tile[kTT][kTT + 1];
+  __shared__ float ftile[CHAINS ? kTT : 1][CHAINS ? kTT + 1 : 1];
+  int64_t bid = blockIdx.x;
+  const int64_t tA = bid % nta;
+  bid /= nta;
+  const int64_t tB = bid % ntb;
+  const int64_t batch = bid / ntb;
+  int64_t in_base = 0, out_base = 0, rem = batch;
+  for (int j = p.nbatch_axes - 1; j >= 0; --j) {
+    const int ax = p.batch_axis[j];
+    const int64_t i = rem % p.size[ax];
+    rem /= p.size[ax];
+    in_base += i * p.in_stride[ax];
+    out_base += i * p.out_stride[ax];
+  }
+  const int64_t a0 = tA * kTT, b0 = tB * kTT;
+  const int64_t na = p.size[p.ax_a], nbb = p.size[p.ax_b];
+  const int64_t sib = p.in_stride[p.ax_b], soa = p.out_stride[p.ax_a];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const T* in = reinterpret_cast<const T*>(p.in);
+  T* out = reinterpret_cast<T*>(p.out);
+  const LogTab lt = global_log_tables();
+#pragma unroll
+  for (int k = 0; k < kTT / 8; ++k) {
+    const int r = ty + 8 * k;
+    const int64_t a = a0 + tx, b = b0 + r;
+    if (a < na && b < nbb) {
+      if (CHAINS) {
+        float v = load_as_f32(p.in, p.dt, in_base + b * sib + a);
+        ftile[r][tx] = apply_chain_rt<false>(p.pro, v, 0, lt);
+      } else {
+        tile[r][tx] = in[in_base + b * sib + a];
+      }
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kTT / 8; ++k) {
+    const int r = ty + 8 * k;  // a within tile
+    const int64_t a = a0 + r, b = b0 + tx;
+    if (a < na && b < nbb) {
+      if (CHAINS) {
+        float v = apply_chain_rt<false>(p.epi, ftile[tx][r], 0, lt);
+        store_from_f32(p.out, p.dt, out_base + a * soa + b, round_to_dt(v, p.dt));
+      } else {
+        out[out_base + a * soa + b] = tile[tx][r];
+      }
+    }
+  }
+}
+
+cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s) {
+  const int64_t nta = (p.size[p.ax_a] + kTT - 1) / kTT;
+  const int64_t ntb = (p.size[p.ax_b] + kTT - 1) / kTT;
+  const int64_t blocks = nta * ntb * p.n_batch;
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  const bool chains = p.pro.n > 0 || p.epi.n > 0;
+  if (chains) {
+    tile_transpose_kernel<uint32_t, true><<<(unsigned)blocks, 256, 0, s>>>(p, nta, ntb);
+  } else {
+    switch (dt_bytes(p.dt)) {
+      case 1: tile_transpose_kernel<uint8_t, false><<<(unsigned)blocks, 256, 0, s>>>(p, nta, ntb); break;
+      case 2: tile_transpose_kernel<uint16_t, false><<<(unsigned)blocks, 256, 0, s>>>(p, nta, ntb); break;
+      default: tile_transpose_kernel<uint32_t, false><<<(unsigned)blocks, 256, 0, s>>>(p, nta, ntb); break;
+    }
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// quantization
+// ---------------------------------------------------------------------------------------------
+// real = scale * (q - zero_point): exact integer difference, one f32 multiply.
+__device__ __forceinline__ float dequant(int code, float scale, int zp) {
+  return __fmul_rn(scale, (float)(code - zp));
+}
+
+// clamp(round_nearest_even(real / scale) + zero_point, smin, smax). The division is the IEEE f32
+// division; with inv = RN(1/scale) the product real*inv is within 2^-23 relative of real/scale, so
+// when it is farther than 2^-22 (relative) from a half-integer both round to the same integer and the
+// product decides. Otherwise the correctly rounded quotient decides.
+__device__ __forceinline__ int quant_code(float real, float scale, float inv, int zp, int smin, int smax) {
+  if (real != real) return zp;
+  float y = __fmul_rn(real, inv);
+  const float f = __fsub_rn(y, floorf(y));
+  if (fabsf(__fsub_rn(f, 0.5f)) <= __fmul_rn(fabsf(y), 0x1p-22f)) y = __fdiv_rn(real, scale);
+  float q = __fadd_rn(rintf(y), (float)zp);
+  q = fminf(fmaxf(q, (float)smin), (float)smax);
+  return (int)q;
+}
+
+struct QTileParams {
+  float sc_in, sc_out, inv_out;
+  int zp_in, zp_out;
+};
+
+// i, j: logical indices; qs_*: per-axis params staged in shared memory for this tile.
+__device__ __forceinline__ int quant_elem(int code, int il, int jl, const QuantTilePlan& p,
+                                          const float* s_sin_i, const int* s_zin_i, const float* s_sin_j,
+                                          const int* s_zin_j, const float* s_sout_i, const int* s_zout_i,
+                                          const float* s_sout_j, const int* s_zout_j, const LogTab& lt) {
+  float sin = p.qin.scale;
+  int zin = p.qin.zp;
+  if (p.qin.axis == 0) { sin = s_sin_i[il]; zin = s_zin_i[il]; }
+  else if (p.qin.axis == 1) { sin = s_sin_j[jl]; zin = s_zin_j[jl]; }
+  float real = dequant(code, sin, zin);
+  if (p.ops.n) real = apply_chain_rt<false>(p.ops, real, 0, lt);
+  float sout = p.qout.scale, inv = p.qout.inv_scale;
+  int zout = p.qout.zp;
+  if (p.qout.axis == 0) { sout = s_sout_i[il]; zout = s_zout_i[il]; inv = __frcp_rn(sout); }
+  else if (p.qout.axis == 1) { sout = s_sout_j[jl]; zout = s_zout_j[jl]; inv = __frcp_rn(sout); }
+  return quant_code(real, sout, inv, zout, p.qout.smin, p.qout.smax);
+}
+
+constexpr int kQT = 128;  // tile edge in bytes
+
+__global__ void __launch_bounds__(256) quant_tile_kernel(QuantTilePlan p, int64_t ntj) {
+  __shared__ __align__(16) uint32_t tile[kQT * kQT / 4];  // 128 rows x 32 words, word column swizzled
+  __shared__ float s_sin_i[kQT], s_sin_j[kQT], s_sout_i[kQT], s_sout_j[kQT];
+  __shared__ int s_zin_i[kQT], s_zin_j[kQT], s_zout_i[kQT], s_zout_j[kQT];
+  const int t = threadIdx.x;
+  const int64_t ti = blockIdx.x / ntj, tj = blockIdx.x % ntj;
+  const int64_t i0 = ti * kQT, j0 = tj * kQT;
+  const int64_t n0 = p.n0, n1 = p.n1;
+  const LogTab lt = global_log_tables();
+  // stage the per-axis parameters of this tile
+  if (t < kQT) {
+    const int64_t i = i0 + t, j = j0 + t;
+    if (p.qin.axis == 0 && i < n0) { s_sin_i[t] = p.qin.scales[i]; s_zin_i[t] = p.qin.zps[i]; }
+    if (p.qin.axis == 1 && j < n1) { s_sin_j[t] = p.qin.scales[j]; s_zin_j[t] = p.qin.zps[j]; }
+    if (p.qout.axis == 0 && i < n0) { s_sout_i[t] = p.qout.scales[i]; s_zout_i[t] = p.qout.zps[i]; }
+    if (p.qout.axis == 1 && j < n1) { s_sout_j[t] = p.qout.scales[j]; s_zout_j[t] = p.qout.zps[j]; }
+  }
+  __syncthreads();
+  const bool full = (i0 + kQT <= n0) && (j0 + kQT <= n1) && (n0 % 16 == 0) && (n1 % 16 == 0) &&
+                    ((uintptr_t)p.in % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
+  if (full) {
+    // 128 rows x 8 chunks of 16 bytes; chunk (row, c) stored at word column 4 * (c ^ ((row >> 4) & 7))
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = t + 256 * k, row = q >> 3, c = q & 7;
+      const uint4* src = reinterpret_cast<const uint4*>(p.in + (i0 + row) * n1 + j0 + 16 * c);
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
+                   : "l"(src));
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int q = t + 256 * k, row = q >> 3, c = q & 7;
+      uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int code = (int)(int8_t)((w[m] >> (8 * b)) & 0xFFu);
+          const int jl = 16 * c + 4 * m + b;
+          const int r = quant_elem(code, row, jl, p, s_sin_i, s_zin_i, s_sin_j, s_zin_j, s_sout_i, s_zout_i,
+                                   s_sout_j, s_zout_j, lt);
+          packed |= ((uint32_t)r & 0xFFu) << (8 * b);
+        }
+        o[m] = packed;
+      }
+      const int wc = 4 * (c ^ ((row >> 4) & 7));
+      *reinterpret_cast<uint4*>(&tile[row * 32 + wc]) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    __syncthreads();
+    // unit: word column jg (output rows 4jg..4jg+3), 16-row chunk ic
+    const int jg = t >> 3, ic = t & 7;
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int row = 16 * ic + k;
+      w[k] = tile[row * 32 + (jg ^ (4 * ic))];
+    }
+    uint32_t outw[4][4];  // [q][m]
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t a = w[4 * m], b = w[4 * m + 1], c = w[4 * m + 2], d = w[4 * m + 3];
+      const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+      const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
+      outw[0][m] = __byte_perm(t0, t2, 0x5410);
+      outw[1][m] = __byte_perm(t0, t2, 0x7632);
+      outw[2][m] = __byte_perm(t1, t3, 0x5410);
+      outw[3][m] = __byte_perm(t1, t3, 0x7632);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (j0 + 4 * jg + q) * n0 + i0 + 16 * ic);
+      *dst = make_uint4(outw[q][0], outw[q][1], outw[q][2], outw[q][3]);
+    }
+  } else {
+    // ragged or unaligned tile: byte by byte through shared memory (unswizzled)
+    uint8_t* bt = reinterpret_cast<uint8_t*>(tile);
+    for (int e = t; e < kQT * kQT; e += 256) {
+      const int row = e / kQT, col = e % kQT;
+      const int64_t i = i0 + row, j = j0 + col;
+      if (i < n0 && j < n1) {
+        const int code = (int)p.in[i * n1 + j];
+        bt[col * kQT + row] = (uint8_t)quant_elem(code, row, col, p, s_sin_i, s_zin_i, s_sin_j, s_zin_j,
+                                                  s_sout_i, s_zout_i, s_sout_j, s_zout_j, lt);
+      }
+    }
+    __syncthreads();
+    for (int e = t; e < kQT * kQT; e += 256) {
+      const int col = e / kQT, row = e % kQT;
+      const int64_t i = i0 + row, j = j0 + col;
+      if (i < n0 && j < n1) p.out[j * n0 + i] = (int8_t)bt[col * kQT + row];
+    }
+  }
+}
+
+cudaError_t launch_quant_tile(const QuantTilePlan& p, cudaStream_t s) {
+  const int64_t nti = (p.n0 + kQT - 1) / kQT, ntj = (p.n1 + kQT - 1) / kQT;
+  const int64_t blocks = nti * ntj;
+  if (blocks == 0) return cudaSuccess;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  quant_tile_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, ntj);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// general gather
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_kernel(GatherPlan p) {
+  const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= p.n) return;
+  const LogTab lt = global_log_tables();
+  int64_t r[kMaxRank];
+  int64_t rem = e;
+  for (int j = p.rank - 1; j >= 0; --j) {
+    const int64_t sz = p.out_size[j];
+    r[p.out_logical[j]] = rem % sz;
+    rem /= sz;
+  }
+  int64_t off = 0, self_off = 0, boff = 0, self_boff = 0;
+  for (int k = 0; k < p.rank; ++k) {
+    off += r[k] * p.in_stride_of_out[k];
+    self_off += r[k] * p.self_stride_of_out[k];
+    boff += r[k] * p.pro.bstride[p.perm[k]];
+    self_boff += r[k] * p.pro.bstride[k];
+  }
+  if (p.kind == G_PLAIN) {
+    if (p.pro.n == 0 && p.epi.n == 0 && !p.self_add) {
+      const char* src = reinterpret_cast<const char*>(p.in) + off * p.elem_bytes;
+      char* dst = reinterpret_cast<char*>(p.out) + e * p.elem_bytes;
+      for (int b = 0; b < p.elem_bytes; ++b) dst[b] = src[b];
+      return;
+    }
+    float v = apply_chain_rt<false>(p.pro, load_as_f32(p.in, p.in_dt, off), boff, lt);
+    if (p.self_add) {
+      const float s = apply_chain_rt<false>(p.pro, load_as_f32(p.in, p.in_dt, self_off), self_boff, lt);
+      v = round_to_dt(__fadd_rn(s, v), p.pro.round16 ? p.in_dt : F32);
+    }
+    v = apply_chain_rt<false>(p.epi, v, 0, lt);
+    store_from_f32(p.out, p.out_dt, e, round_to_dt(v, p.out_dt));
+    return;
+  }
+  // quantized: dequantize (input axis), float chain, quantize or f32 output
+  const int code = (int)reinterpret_cast<const int8_t*>(p.in)[off];
+  float sin = p.qin.scale;
+  int zin = p.qin.zp;
+  if (p.qin_axis_out >= 0) {
+    const int64_t j = r[p.qin_axis_out];
+    sin = p.qin.scales[j];
+    zin = p.qin.zps[j];
+  }
+  float real = dequant(code, sin, zin);
+  real = apply_chain_rt<false>(p.pro, real, boff, lt);
+  if (p.out_float) {
+    reinterpret_cast<float*>(p.out)[e] = real;
+    return;
+  }
+  float sout = p.qout.scale, inv = p.qout.inv_scale;
+  int zout = p.qout.zp;
+  if (p.qout_axis_out >= 0) {
+    const int64_t j = r[p.qout_axis_out];
+    sout = p.qout.scales[j];
+    zout = p.qout.zps[j];
+    inv = __frcp_rn(sout);
+  }
+  reinterpret_cast<int8_t*>(p.out)[e] = (int8_t)quant_code(real, sout, inv, zout, p.qout.smin, p.qout.smax);
+}
+
+cudaError_t launch_gather(const GatherPlan& p, cudaStream_t s) {
+  if (p.n == 0) return cudaSuccess;
+  const int64_t blocks = (p.n + 255) / 256;
+  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+  gather_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace hlo
