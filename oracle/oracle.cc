@@ -194,8 +194,13 @@ static int prec_of(int dt) { return dt == ORC_BF16 ? 8 : dt == ORC_F16 ? 11 : dt
 static int emin_of(int dt) { return dt == ORC_F16 ? -14 : dt == ORC_F64 ? -1022 : -126; }
 static int emax_of(int dt) { return dt == ORC_F16 ? 15 : dt == ORC_F64 ? 1023 : 127; }
 
+static bool is_float_type(int dt) { return dt == ORC_F32 || dt == ORC_BF16 || dt == ORC_F16 || dt == ORC_F64; }
+
+// Rounds v into element type dt. Integer types hold their values exactly (a transpose or layout change
+// moves elements; it does not convert them), so nothing is rounded for them.
 template <typename T>
 static T round_to(T v, int dt) {
+  if (!is_float_type(dt)) return v;
   if (dt == ORC_F64) return (T)(double)v;
   return round_to_format<T>(v, prec_of(dt), emin_of(dt), emax_of(dt));
 }

@@ -152,6 +152,16 @@ def test_transpose_all_permutations_vs_numpy(orc, rank):
         assert np.array_equal(from_physical(out, out_dims, out_m2m), want)
 
 
+def test_transpose_moves_integers_exactly(orc):
+    """A transpose is a pure index map: 32-bit integers keep all their bits (no float rounding)."""
+    rng = np.random.default_rng(19)
+    dims = [3, 5, 7]
+    logical = rng.integers(-2 ** 31, 2 ** 31 - 1, size=dims).astype(np.int32)
+    for perm in itertools.permutations(range(3)):
+        out = orc.transpose(logical.ravel(), dims, "s32", list(perm))
+        assert np.array_equal(out.reshape([dims[p] for p in perm]), np.transpose(logical, perm))
+
+
 def test_transpose_self_add(orc):
     rng = np.random.default_rng(7)
     n = 9
