@@ -579,7 +579,10 @@ hlo_status hlo_transpose_fusion(const hlo_array* in, const void* in_ptr, const h
   bool identity = true;
   for (int j = 0; j < c.k; ++j)
     if (c.out_pos[j] != j) identity = false;
-  if (identity) return cuda_status(launch_elementwise(in_ptr, out_ptr, n, in->dtype, pro, epi, s), "elementwise launch");
+  if (identity) {
+    if (pro.n == 0 && epi.n == 0) return cuda_status(launch_copy(in_ptr, out_ptr, bytes, s), "copy launch");
+    return cuda_status(launch_elementwise(in_ptr, out_ptr, n, in->dtype, pro, epi, s), "elementwise launch");
+  }
   const int ax_a = c.k - 1;
   int ax_b = -1;
   for (int j = 0; j < c.k; ++j)

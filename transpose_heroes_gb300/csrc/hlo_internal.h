@@ -182,6 +182,7 @@ cudaError_t launch_selfadd_transpose(const SelfAddPlan& p, cudaStream_t s);
 cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s);
 cudaError_t launch_quant_tile(const QuantTilePlan& p, cudaStream_t s);
 cudaError_t launch_gather(const GatherPlan& p, cudaStream_t s);
+cudaError_t launch_copy(const void* in, void* out, int64_t nbytes, cudaStream_t s);
 cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, const Chain& pro, const Chain& epi,
                                cudaStream_t s);
 
