@@ -142,48 +142,55 @@ static __device__ __noinline__ float cr_logf_accurate(float x) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Stage 1. ctab/etab may point to shared or global copies of kLogCTab / kLogETab.
+// Stage 1. ctab/etab may point to shared or global copies of kLogCTab / kLogETab. Returns the
+// correctly rounded log when ok is set; ok is cleared for special operands and for results whose
+// rounding the error bound cannot decide (stage 2 must then be used).
 // ------------------------------------------------------------------------------------------------
-__device__ __forceinline__ float cr_logf(float x, const float4* __restrict__ ctab,
-                                         const float2* __restrict__ etab) {
-  uint32_t ix = __float_as_uint(x);
-  if (ix - 0x00800000u >= 0x7F000000u) return cr_logf_accurate(x);  // not a positive normal
-  uint32_t tmp = ix - HLO_LOG_OFF;
-  int e = (int)tmp >> 23;
-  uint32_t i = (tmp >> HLO_LOG_SHIFT) & (HLO_LOG_NC - 1);
-  float m = __uint_as_float(ix - (tmp & 0xFF800000u));
-  float4 c = ctab[i];                       // inv_c, log c hi, log c lo
-  float2 E = etab[e - HLO_LOG_EMIN];        // e*ln2 hi, lo
-  float r = __fmaf_rn(m, c.x, -1.0f);       // exact by table construction
+__device__ __forceinline__ float cr_logf_fast(float x, const float4* __restrict__ ctab,
+                                              const float2* __restrict__ etab, bool& ok) {
+  const uint32_t ix = __float_as_uint(x);
+  const bool normal = ix - 0x00800000u < 0x7F000000u;  // positive normal
+  const uint32_t tmp = ix - HLO_LOG_OFF;
+  const int e = normal ? (int)tmp >> 23 : 0;
+  const uint32_t i = (tmp >> HLO_LOG_SHIFT) & (HLO_LOG_NC - 1);
+  const float m = __uint_as_float(ix - (tmp & 0xFF800000u));
+  const float4 c = ctab[i];                       // inv_c, log c hi, log c lo
+  const float2 E = etab[e - HLO_LOG_EMIN];        // e*ln2 hi, lo
+  const float r = __fmaf_rn(m, c.x, -1.0f);       // exact by table construction
   // s1 = E_hi + logc_hi: E_hi is 0 or dominates, so Fast2Sum is exact
-  float s1 = __fadd_rn(E.x, c.y);
-  float e1 = __fsub_rn(c.y, __fsub_rn(s1, E.x));
+  const float s1 = __fadd_rn(E.x, c.y);
+  const float e1 = __fsub_rn(c.y, __fsub_rn(s1, E.x));
   // s2 = s1 + r: s1 is 0 or |s1| >= |r| (table check / |e*ln2| - |log c| > |r|)
-  float s2 = __fadd_rn(s1, r);
-  float e2 = __fsub_rn(r, __fsub_rn(s2, s1));
+  const float s2 = __fadd_rn(s1, r);
+  const float e2 = __fsub_rn(r, __fsub_rn(s2, s1));
   // -r^2/2 split exactly into qh + ql
-  float hr = -0.5f * r;
-  float qh = __fmul_rn(hr, r);
-  float ql = __fmaf_rn(hr, r, -qh);
-  float s3 = __fadd_rn(s2, qh);
-  float e3 = __fsub_rn(qh, __fsub_rn(s3, s2));
+  const float hr = -0.5f * r;
+  const float qh = __fmul_rn(hr, r);
+  const float ql = __fmaf_rn(hr, r, -qh);
+  const float s3 = __fadd_rn(s2, qh);
+  const float e3 = __fsub_rn(qh, __fsub_rn(s3, s2));
   // r^3 (1/3 - r/4 + r^2/5 - r^3/6)
   float p = __fmaf_rn(r, -0.16666667f, 0.2f);
   p = __fmaf_rn(r, p, -0.25f);
   p = __fmaf_rn(r, p, 0.33333334f);
-  float r3 = __fmul_rn(__fmul_rn(r, r), r);
+  const float r3 = __fmul_rn(__fmul_rn(r, r), r);
   float lo = __fmaf_rn(r3, p, ql);
   lo = __fadd_rn(lo, __fadd_rn(E.y, c.z));
   lo = __fadd_rn(lo, __fadd_rn(__fadd_rn(e1, e2), e3));
-  float yh = __fadd_rn(s3, lo);
-  float yl = __fsub_rn(lo, __fsub_rn(yh, s3));
-  // rounding test: boundary at half an ulp of yh; powers of two and y = 0 go to stage 2
-  float err = __fmaf_rn(fabsf(yh), 0x1p-42f, __fmul_rn(fabsf(r3), 0x1p-23f));
-  uint32_t yb = __float_as_uint(yh);
-  float half_ulp = __uint_as_float((yb & 0x7F800000u) - (24u << 23));
-  bool ambiguous = (__fadd_rn(fabsf(yl), err) >= half_ulp) | ((yb & 0x007FFFFFu) == 0u);
-  if (ambiguous) return cr_logf_accurate(x);
+  const float yh = __fadd_rn(s3, lo);
+  const float yl = __fsub_rn(lo, __fsub_rn(yh, s3));
+  // rounding test: boundary at half an ulp of yh; powers of two and y = 0 are left to stage 2
+  const float err = __fmaf_rn(fabsf(yh), 0x1p-42f, __fmul_rn(fabsf(r3), 0x1p-23f));
+  const uint32_t yb = __float_as_uint(yh);
+  const float half_ulp = __uint_as_float((yb & 0x7F800000u) - (24u << 23));
+  ok = normal & (__fadd_rn(fabsf(yl), err) < half_ulp) & ((yb & 0x007FFFFFu) != 0u);
   return yh;
+}
+
+__device__ __forceinline__ float cr_logf(float x, const float4* __restrict__ ctab, const float2* __restrict__ etab) {
+  bool ok;
+  const float y = cr_logf_fast(x, ctab, etab, ok);
+  return ok ? y : cr_logf_accurate(x);
 }
 
 // Loads the tables into shared memory (called by all threads of a block, followed by a barrier).

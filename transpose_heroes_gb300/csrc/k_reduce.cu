@@ -266,7 +266,7 @@ cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s) {
 // ---- column reduce --------------------------------------------------------------------------------
 constexpr int kColCluster = 8;
 constexpr int kColWarps = 8;
-constexpr int kColUnroll = 4;
+constexpr int kColUnroll = 8;
 
 // Block (x = column block * kColCluster + slab, y = a). Each lane owns VEC consecutive columns.
 template <int IN_DT, int VEC, int KIND, bool RT>

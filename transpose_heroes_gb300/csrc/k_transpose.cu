@@ -21,16 +21,18 @@ namespace hlo {
 // pair-tile self-add transpose
 // ---------------------------------------------------------------------------------------------
 constexpr int kT = 64;        // tile edge (elements)
-constexpr int kTP = kT + 1;   // padded row pitch: column reads hit 32 distinct banks
+constexpr int kTP = kT + 1;   // padded pitch: transposed stores and row reads hit 32 distinct banks
 constexpr int kPairThreads = 256;
 
 enum PairChain : int { PC_NONE = 0, PC_LOG = 1, PC_RT = 2 };
 
-// Maps a pair index to (I, J), I < J, enumerating row by row.
+// Maps a pair index to (I, J), I < J, enumerating row by row (single-precision estimate, then exact
+// integer correction; FP64 is a slow pipe on this part).
 __device__ __forceinline__ void pair_of(int64_t item, int64_t nt, int64_t& I, int64_t& J) {
-  const double b = 2.0 * (double)nt - 1.0;
-  int64_t i = (int64_t)((b - sqrt(b * b - 8.0 * (double)item)) * 0.5);
-  if (i < 0) i = 0;
+  const float b = 2.0f * (float)nt - 1.0f;
+  const float disc = fmaxf(b * b - 8.0f * (float)item, 0.0f);
+  int64_t i = (int64_t)((b - sqrtf(disc)) * 0.5f);
+  i = i < 0 ? 0 : (i > nt - 2 ? nt - 2 : i);
   auto start = [nt](int64_t r) { return r * (nt - 1) - r * (r - 1) / 2; };
   while (i > 0 && start(i) > item) --i;
   while (start(i + 1) <= item) ++i;
@@ -45,17 +47,30 @@ __device__ __forceinline__ float pair_pro(float v, const Chain& c, const LogTab&
   return v;
 }
 
-// Loads tile (TI, TJ) of the n x n input into dst (padded), applying the prologue.
+// Thread mapping inside a 64 x 64 tile: slot k (0..3) of warp w covers rows 4*rg .. 4*rg+3, columns
+// 32*h .. 32*h+31, with 8 lanes (16 bytes each) per 128-byte row segment. A lane owns row
+// r = 4*rg + lane/8 and columns c .. c+3, c = 32*h + 4*(lane%8).
+__device__ __forceinline__ void pair_slot(int k, int& r, int& c) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int s = warp * 4 + k;
+  r = 4 * (s >> 1) + (lane >> 3);
+  c = 32 * (s & 1) + 4 * (lane & 7);
+}
+
+// Loads this thread's 16 elements of tile (TI, TJ), applies the prologue and stores the results
+// transposed: dst[col * kTP + row]. With kTP = 65 the 32 lanes of a store hit 32 distinct banks.
+// For log, the rare elements whose rounding the fast path cannot decide are redone afterwards from
+// the input value parked in their slot, so no register array lives across the slow calls.
 template <int CH, bool VEC>
 __device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t n, int64_t TI, int64_t TJ,
                                           float* dst, const Chain& c, const LogTab& lt) {
-  const int t = threadIdx.x;
-  if (VEC) {
-    float4 v[4];
+  float4 v[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = (t >> 4) + 16 * k, col = (t & 15) * 4;
-      const int64_t gr = TI * kT + r, gc = TJ * kT + col;
+  for (int k = 0; k < 4; ++k) {
+    int r, col;
+    pair_slot(k, r, col);
+    const int64_t gr = TI * kT + r, gc = TJ * kT + col;
+    if (VEC) {
       if (gr < n && gc < n) {
         const float4* src = reinterpret_cast<const float4*>(in + gr * n + gc);
         asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -64,42 +79,78 @@ __device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t 
       } else {
         v[k] = make_float4(1.f, 1.f, 1.f, 1.f);
       }
-    }
+    } else {
+      float* o = &v[k].x;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = (t >> 4) + 16 * k, col = (t & 15) * 4;
-      float* d = dst + r * kTP + col;
-      d[0] = pair_pro<CH>(v[k].x, c, lt);
-      d[1] = pair_pro<CH>(v[k].y, c, lt);
-      d[2] = pair_pro<CH>(v[k].z, c, lt);
-      d[3] = pair_pro<CH>(v[k].w, c, lt);
+      for (int q = 0; q < 4; ++q) o[q] = (gr < n && gc + q < n) ? in[gr * n + gc + q] : 1.f;
     }
-  } else {
-    for (int e = t; e < kT * kT; e += kPairThreads) {
-      const int r = e / kT, col = e % kT;
-      const int64_t gr = TI * kT + r, gc = TJ * kT + col;
-      float x = (gr < n && gc < n) ? in[gr * n + gc] : 1.f;
-      dst[r * kTP + col] = pair_pro<CH>(x, c, lt);
+  }
+  uint32_t redo = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    int r, col;
+    pair_slot(k, r, col);
+    const float* o = &v[k].x;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float y;
+      if (CH == PC_LOG) {
+        bool ok;
+        y = cr_logf_fast(o[q], lt.c, lt.e, ok);
+        if (!ok) {
+          redo |= 1u << (4 * k + q);
+          y = o[q];  // park the input
+        }
+      } else {
+        y = pair_pro<CH>(o[q], c, lt);
+      }
+      dst[(col + q) * kTP + r] = y;
+    }
+  }
+  if (CH == PC_LOG && redo) {
+#pragma unroll 1
+    for (int e = 0; e < 16; ++e) {
+      if (!((redo >> e) & 1u)) continue;
+      int r, col;
+      pair_slot(e >> 2, r, col);
+      float* slot = dst + (col + (e & 3)) * kTP + r;
+      *slot = cr_logf_accurate(*slot);
     }
   }
 }
 
-// Writes out tile (TI, TJ) = own[r][c] + other[c][r], then the epilogue.
+// Writes this thread's 16 elements of output tile (TI, TJ) = own[r][c] + other[c][r], where ownT and
+// otherT hold the two tiles transposed (so own[r][c] = ownT[c][r], other[c][r] = otherT[r][c]), then
+// the epilogue. Both reads hit 32 distinct banks per warp.
+template <bool VEC>
 __device__ __forceinline__ void pair_store(float* __restrict__ out, int64_t n, int64_t TI, int64_t TJ,
-                                           const float* own, const float* other, const Chain& epi,
+                                           const float* ownT, const float* otherT, const Chain& epi,
                                            const LogTab& lt) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll 4
-  for (int rr = 0; rr < kT / (kPairThreads / 32); ++rr) {
-    const int r = warp + rr * (kPairThreads / 32);
-    const int64_t gr = TI * kT + r;
 #pragma unroll
-    for (int h = 0; h < kT / 32; ++h) {
-      const int c = lane + 32 * h;
-      const int64_t gc = TJ * kT + c;
-      float v = __fadd_rn(own[r * kTP + c], other[c * kTP + r]);
-      if (epi.n) v = apply_chain_rt<false>(epi, v, 0, lt);
-      if (gr < n && gc < n) out[gr * n + gc] = v;
+  for (int k = 0; k < 4; ++k) {
+    int r, col;
+    pair_slot(k, r, col);
+    const float* t = otherT + r * kTP + col;
+    const float* o = ownT + col * kTP + r;
+    float4 v;
+    v.x = __fadd_rn(o[0 * kTP], t[0]);
+    v.y = __fadd_rn(o[1 * kTP], t[1]);
+    v.z = __fadd_rn(o[2 * kTP], t[2]);
+    v.w = __fadd_rn(o[3 * kTP], t[3]);
+    if (epi.n) {
+      v.x = apply_chain_rt<false>(epi, v.x, 0, lt);
+      v.y = apply_chain_rt<false>(epi, v.y, 0, lt);
+      v.z = apply_chain_rt<false>(epi, v.z, 0, lt);
+      v.w = apply_chain_rt<false>(epi, v.w, 0, lt);
+    }
+    const int64_t gr = TI * kT + r, gc = TJ * kT + col;
+    if (VEC) {
+      if (gr < n && gc < n) *reinterpret_cast<float4*>(out + gr * n + gc) = v;
+    } else {
+      const float* pv = &v.x;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (gr < n && gc + q < n) out[gr * n + gc + q] = pv[q];
     }
   }
 }
@@ -110,8 +161,8 @@ __global__ void __launch_bounds__(kPairThreads, 4)
   extern __shared__ float4 smem_f4[];
   float4* s_lc = smem_f4;
   float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
-  float* ta = reinterpret_cast<float*>(s_le + HLO_LOG_NE);
-  float* tb = ta + kT * kTP;
+  float* ta = reinterpret_cast<float*>(s_le + HLO_LOG_NE);  // tile (I,J) after the prologue, transposed
+  float* tb = ta + kT * kTP;                                 // tile (J,I) after the prologue, transposed
   load_log_tables(s_lc, s_le);
   __syncthreads();
   const LogTab lt = {s_lc, s_le};
@@ -128,10 +179,10 @@ __global__ void __launch_bounds__(kPairThreads, 4)
     if (I != J) pair_load<CH, VEC>(in, p.n, J, I, tb, p.pro, lt);
     __syncthreads();
     if (I != J) {
-      pair_store(out, p.n, I, J, ta, tb, p.epi, lt);
-      pair_store(out, p.n, J, I, tb, ta, p.epi, lt);
+      pair_store<VEC>(out, p.n, I, J, ta, tb, p.epi, lt);  // out(I,J) = A + B^T
+      pair_store<VEC>(out, p.n, J, I, tb, ta, p.epi, lt);  // out(J,I) = B + A^T
     } else {
-      pair_store(out, p.n, I, I, ta, ta, p.epi, lt);
+      pair_store<VEC>(out, p.n, I, I, ta, ta, p.epi, lt);
     }
     __syncthreads();
   }
@@ -164,7 +215,7 @@ static cudaError_t pair_launch(const SelfAddPlan& p, cudaStream_t s) {
 
 cudaError_t launch_selfadd_transpose(const SelfAddPlan& p, cudaStream_t s) {
   if (p.n == 0) return cudaSuccess;
-  const bool vec = (p.n % 4 == 0) && ((uintptr_t)p.in % 16 == 0);
+  const bool vec = (p.n % 4 == 0) && ((uintptr_t)p.in % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
   int ch = PC_RT;
   if (p.pro.n == 0) ch = PC_NONE;
   else if (p.pro.n == 1 && p.pro.op[0] == OP_LOG) ch = PC_LOG;
@@ -253,146 +304,230 @@ cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s) {
 // ---------------------------------------------------------------------------------------------
 // quantization
 // ---------------------------------------------------------------------------------------------
-// real = scale * (q - zero_point): exact integer difference, one f32 multiply.
+constexpr float kMagic = 12582912.0f;      // 1.5 * 2^23: x + kMagic rounds x to an integer (|x| < 2^22)
+constexpr int kMagicBits = 0x4B400000;     // bit pattern of kMagic
+
+// real = scale * (q - zero_point): exact integer difference, exact int -> float (|d| <= 255 < 2^22
+// through the magic constant), one f32 multiply.
 __device__ __forceinline__ float dequant(int code, float scale, int zp) {
-  return __fmul_rn(scale, (float)(code - zp));
+  const int d = code - zp;
+  const float df = __fsub_rn(__int_as_float(kMagicBits + d), kMagic);
+  return __fmul_rn(scale, df);
 }
 
-// clamp(round_nearest_even(real / scale) + zero_point, smin, smax). The division is the IEEE f32
-// division; with inv = RN(1/scale) the product real*inv is within 2^-23 relative of real/scale, so
-// when it is farther than 2^-22 (relative) from a half-integer both round to the same integer and the
-// product decides. Otherwise the correctly rounded quotient decides.
-__device__ __forceinline__ int quant_code(float real, float scale, float inv, int zp, int smin, int smax) {
+// The exact definition: clamp(rint(real / scale) + zp), IEEE f32 division, NaN -> zero point.
+__device__ __noinline__ int quant_code_exact(float real, float scale, int zp, int smin, int smax) {
   if (real != real) return zp;
-  float y = __fmul_rn(real, inv);
-  const float f = __fsub_rn(y, floorf(y));
-  if (fabsf(__fsub_rn(f, 0.5f)) <= __fmul_rn(fabsf(y), 0x1p-22f)) y = __fdiv_rn(real, scale);
+  const float y = __fdiv_rn(real, scale);
   float q = __fadd_rn(rintf(y), (float)zp);
   q = fminf(fmaxf(q, (float)smin), (float)smax);
   return (int)q;
 }
 
-struct QTileParams {
-  float sc_in, sc_out, inv_out;
-  int zp_in, zp_out;
-};
-
-// i, j: logical indices; qs_*: per-axis params staged in shared memory for this tile.
-__device__ __forceinline__ int quant_elem(int code, int il, int jl, const QuantTilePlan& p,
-                                          const float* s_sin_i, const int* s_zin_i, const float* s_sin_j,
-                                          const int* s_zin_j, const float* s_sout_i, const int* s_zout_i,
-                                          const float* s_sout_j, const int* s_zout_j, const LogTab& lt) {
-  float sin = p.qin.scale;
-  int zin = p.qin.zp;
-  if (p.qin.axis == 0) { sin = s_sin_i[il]; zin = s_zin_i[il]; }
-  else if (p.qin.axis == 1) { sin = s_sin_j[jl]; zin = s_zin_j[jl]; }
-  float real = dequant(code, sin, zin);
-  if (p.ops.n) real = apply_chain_rt<false>(p.ops, real, 0, lt);
-  float sout = p.qout.scale, inv = p.qout.inv_scale;
-  int zout = p.qout.zp;
-  if (p.qout.axis == 0) { sout = s_sout_i[il]; zout = s_zout_i[il]; inv = __frcp_rn(sout); }
-  else if (p.qout.axis == 1) { sout = s_sout_j[jl]; zout = s_zout_j[jl]; inv = __frcp_rn(sout); }
-  return quant_code(real, sout, inv, zout, p.qout.smin, p.qout.smax);
+// Same result, fast: with inv = RN(1/scale) the product real*inv is within 2^-23 relative of
+// real/scale, and the IEEE quotient within 2^-24; when the product is farther than 2^-22 (relative)
+// from the nearest half-integer, all three round to the same integer, which the magic-constant add
+// produces (ties to even). Otherwise, or out of range / NaN, the exact definition decides.
+__device__ __forceinline__ int quant_code(float real, float scale, float inv, int zp, int smin, int smax) {
+  const float y = __fmul_rn(real, inv);
+  const float t = __fadd_rn(y, kMagic);
+  const float f = __fsub_rn(y, __fsub_rn(t, kMagic));
+  const float ay = fabsf(y);
+  if (!(ay < 4194304.0f) || fabsf(__fsub_rn(fabsf(f), 0.5f)) <= __fmul_rn(ay, 0x1p-22f))
+    return quant_code_exact(real, scale, zp, smin, smax);
+  const int q = (__float_as_int(t) - kMagicBits) + zp;
+  return min(max(q, smin), smax);
 }
 
 constexpr int kQT = 128;  // tile edge in bytes
 
-__global__ void __launch_bounds__(256) quant_tile_kernel(QuantTilePlan p, int64_t ntj) {
+struct QuantSmem {
+  float sin_[kQT];   // input scale per tile row (axis 0) or column (axis 1)
+  int zin[kQT];
+  float sout[kQT];   // output scale per tile row or column
+  float inv[kQT];    // RN(1 / output scale)
+  int zout[kQT];
+};
+
+// Ragged or unaligned tile, byte by byte (kept out of line: it is rare and large).
+__device__ __noinline__ void quant_tile_ragged(const QuantTilePlan& p, int64_t i0, int64_t j0, uint8_t* bt,
+                                               const QuantSmem& q) {
+  const int t = threadIdx.x;
+  for (int e = t; e < kQT * kQT; e += blockDim.x) {
+    const int row = e / kQT, col = e % kQT;
+    const int64_t i = i0 + row, j = j0 + col;
+    if (i < p.n0 && j < p.n1) {
+      const int code = (int)p.in[i * p.n1 + j];
+      float sin = p.qin.scale;
+      int zin = p.qin.zp;
+      if (p.qin.axis == 0) { sin = q.sin_[row]; zin = q.zin[row]; }
+      if (p.qin.axis == 1) { sin = q.sin_[col]; zin = q.zin[col]; }
+      float real = dequant(code, sin, zin);
+      if (p.ops.n) real = apply_chain_rt<false>(p.ops, real, 0, global_log_tables());
+      float sout = p.qout.scale, inv = p.qout.inv_scale;
+      int zout = p.qout.zp;
+      if (p.qout.axis == 0) { sout = q.sout[row]; inv = q.inv[row]; zout = q.zout[row]; }
+      if (p.qout.axis == 1) { sout = q.sout[col]; inv = q.inv[col]; zout = q.zout[col]; }
+      bt[col * kQT + row] = (uint8_t)quant_code(real, sout, inv, zout, p.qout.smin, p.qout.smax);
+    }
+  }
+  __syncthreads();
+  for (int e = t; e < kQT * kQT; e += blockDim.x) {
+    const int col = e / kQT, row = e % kQT;
+    const int64_t i = i0 + row, j = j0 + col;
+    if (i < p.n0 && j < p.n1) p.out[j * p.n0 + i] = (int8_t)bt[col * kQT + row];
+  }
+}
+
+// Fast path of quant_code: returns false (leaving q undefined) when the exact definition must decide.
+__device__ __forceinline__ bool quant_code_fast(float real, float inv, int zp, int smin, int smax, int& q) {
+  const float y = __fmul_rn(real, inv);
+  const float t = __fadd_rn(y, kMagic);
+  const float f = __fsub_rn(y, __fsub_rn(t, kMagic));
+  const float ay = fabsf(y);
+  const bool ok = (ay < 4194304.0f) & (fabsf(__fsub_rn(fabsf(f), 0.5f)) > __fmul_rn(ay, 0x1p-22f));
+  q = min(max((__float_as_int(t) - kMagicBits) + zp, smin), smax);
+  return ok;
+}
+
+template <int QIN, int QOUT, bool OPS>
+__device__ __forceinline__ void quant_params(int row, int jl, const QuantTilePlan& p, const QuantSmem& q, float& sin,
+                                             int& zin, float& sout, float& inv, int& zout) {
+  sin = QIN == 0 ? q.sin_[row] : QIN == 1 ? q.sin_[jl] : p.qin.scale;
+  zin = QIN == 0 ? q.zin[row] : QIN == 1 ? q.zin[jl] : p.qin.zp;
+  sout = QOUT == 0 ? q.sout[row] : QOUT == 1 ? q.sout[jl] : p.qout.scale;
+  inv = QOUT == 0 ? q.inv[row] : QOUT == 1 ? q.inv[jl] : p.qout.inv_scale;
+  zout = QOUT == 0 ? q.zout[row] : QOUT == 1 ? q.zout[jl] : p.qout.zp;
+}
+
+// 16 codes of one tile row (local row `row`, local columns 16c .. 16c+15) -> 16 output codes. The
+// fast path runs for all 16; the rare ones it cannot decide are recomputed exactly afterwards.
+template <int QIN, int QOUT, bool OPS>
+__device__ __forceinline__ uint4 quant_chunk(uint4 x, int row, int c, const QuantTilePlan& p, const QuantSmem& q) {
+  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  uint32_t o[4];
+  uint32_t redo = 0;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    uint32_t packed = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int jl = 16 * c + 4 * m + b;
+      const int code = (int)(int8_t)(w[m] >> (8 * b));
+      float sin, sout, inv;
+      int zin, zout;
+      quant_params<QIN, QOUT, OPS>(row, jl, p, q, sin, zin, sout, inv, zout);
+      float real = dequant(code, sin, zin);
+      if (OPS) real = apply_chain_rt<false>(p.ops, real, 0, global_log_tables());
+      int r;
+      if (!quant_code_fast(real, inv, zout, p.qout.smin, p.qout.smax, r)) redo |= 1u << (4 * m + b);
+      packed |= ((uint32_t)r & 0xFFu) << (8 * b);
+    }
+    o[m] = packed;
+  }
+  if (redo) {
+    uint4 res = make_uint4(o[0], o[1], o[2], o[3]);
+    uint32_t* ro = reinterpret_cast<uint32_t*>(&res);
+#pragma unroll 1
+    for (int e = 0; e < 16; ++e) {
+      if (!((redo >> e) & 1u)) continue;
+      const int m = e >> 2, b = e & 3, jl = 16 * c + e;
+      const uint32_t word = m == 0 ? x.x : m == 1 ? x.y : m == 2 ? x.z : x.w;
+      const int code = (int)(int8_t)(word >> (8 * b));
+      float sin, sout, inv;
+      int zin, zout;
+      quant_params<QIN, QOUT, OPS>(row, jl, p, q, sin, zin, sout, inv, zout);
+      float real = dequant(code, sin, zin);
+      if (OPS) real = apply_chain_rt<false>(p.ops, real, 0, global_log_tables());
+      const int r = quant_code_exact(real, sout, zout, p.qout.smin, p.qout.smax);
+      ro[m] = (ro[m] & ~(0xFFu << (8 * b))) | (((uint32_t)r & 0xFFu) << (8 * b));
+    }
+    return res;
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int QIN, int QOUT, bool OPS>
+__global__ void __launch_bounds__(256, 3) quant_tile_kernel(QuantTilePlan p, int64_t ntj) {
   __shared__ __align__(16) uint32_t tile[kQT * kQT / 4];  // 128 rows x 32 words, word column swizzled
-  __shared__ float s_sin_i[kQT], s_sin_j[kQT], s_sout_i[kQT], s_sout_j[kQT];
-  __shared__ int s_zin_i[kQT], s_zin_j[kQT], s_zout_i[kQT], s_zout_j[kQT];
+  __shared__ QuantSmem q;
   const int t = threadIdx.x;
   const int64_t ti = blockIdx.x / ntj, tj = blockIdx.x % ntj;
   const int64_t i0 = ti * kQT, j0 = tj * kQT;
   const int64_t n0 = p.n0, n1 = p.n1;
-  const LogTab lt = global_log_tables();
   // stage the per-axis parameters of this tile
   if (t < kQT) {
     const int64_t i = i0 + t, j = j0 + t;
-    if (p.qin.axis == 0 && i < n0) { s_sin_i[t] = p.qin.scales[i]; s_zin_i[t] = p.qin.zps[i]; }
-    if (p.qin.axis == 1 && j < n1) { s_sin_j[t] = p.qin.scales[j]; s_zin_j[t] = p.qin.zps[j]; }
-    if (p.qout.axis == 0 && i < n0) { s_sout_i[t] = p.qout.scales[i]; s_zout_i[t] = p.qout.zps[i]; }
-    if (p.qout.axis == 1 && j < n1) { s_sout_j[t] = p.qout.scales[j]; s_zout_j[t] = p.qout.zps[j]; }
+    if (p.qin.axis == 0 && i < n0) { q.sin_[t] = p.qin.scales[i]; q.zin[t] = p.qin.zps[i]; }
+    if (p.qin.axis == 1 && j < n1) { q.sin_[t] = p.qin.scales[j]; q.zin[t] = p.qin.zps[j]; }
+    const int64_t k = p.qout.axis == 0 ? i : j;
+    if (p.qout.axis >= 0 && k < (p.qout.axis == 0 ? n0 : n1)) {
+      const float s = p.qout.scales[k];
+      q.sout[t] = s;
+      q.inv[t] = __frcp_rn(s);
+      q.zout[t] = p.qout.zps[k];
+    }
   }
   __syncthreads();
   const bool full = (i0 + kQT <= n0) && (j0 + kQT <= n1) && (n0 % 16 == 0) && (n1 % 16 == 0) &&
                     ((uintptr_t)p.in % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
-  if (full) {
-    // 128 rows x 8 chunks of 16 bytes; chunk (row, c) stored at word column 4 * (c ^ ((row >> 4) & 7))
-    uint4 v[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int q = t + 256 * k, row = q >> 3, c = q & 7;
-      const uint4* src = reinterpret_cast<const uint4*>(p.in + (i0 + row) * n1 + j0 + 16 * c);
-      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
-                   : "l"(src));
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int q = t + 256 * k, row = q >> 3, c = q & 7;
-      uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-      uint32_t o[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint32_t packed = 0;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int code = (int)(int8_t)((w[m] >> (8 * b)) & 0xFFu);
-          const int jl = 16 * c + 4 * m + b;
-          const int r = quant_elem(code, row, jl, p, s_sin_i, s_zin_i, s_sin_j, s_zin_j, s_sout_i, s_zout_i,
-                                   s_sout_j, s_zout_j, lt);
-          packed |= ((uint32_t)r & 0xFFu) << (8 * b);
-        }
-        o[m] = packed;
-      }
-      const int wc = 4 * (c ^ ((row >> 4) & 7));
-      *reinterpret_cast<uint4*>(&tile[row * 32 + wc]) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    __syncthreads();
-    // unit: word column jg (output rows 4jg..4jg+3), 16-row chunk ic
-    const int jg = t >> 3, ic = t & 7;
-    uint32_t w[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int row = 16 * ic + k;
-      w[k] = tile[row * 32 + (jg ^ (4 * ic))];
-    }
-    uint32_t outw[4][4];  // [q][m]
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const uint32_t a = w[4 * m], b = w[4 * m + 1], c = w[4 * m + 2], d = w[4 * m + 3];
-      const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
-      const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
-      outw[0][m] = __byte_perm(t0, t2, 0x5410);
-      outw[1][m] = __byte_perm(t0, t2, 0x7632);
-      outw[2][m] = __byte_perm(t1, t3, 0x5410);
-      outw[3][m] = __byte_perm(t1, t3, 0x7632);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (j0 + 4 * jg + q) * n0 + i0 + 16 * ic);
-      *dst = make_uint4(outw[q][0], outw[q][1], outw[q][2], outw[q][3]);
-    }
-  } else {
-    // ragged or unaligned tile: byte by byte through shared memory (unswizzled)
-    uint8_t* bt = reinterpret_cast<uint8_t*>(tile);
-    for (int e = t; e < kQT * kQT; e += 256) {
-      const int row = e / kQT, col = e % kQT;
-      const int64_t i = i0 + row, j = j0 + col;
-      if (i < n0 && j < n1) {
-        const int code = (int)p.in[i * n1 + j];
-        bt[col * kQT + row] = (uint8_t)quant_elem(code, row, col, p, s_sin_i, s_zin_i, s_sin_j, s_zin_j,
-                                                  s_sout_i, s_zout_i, s_sout_j, s_zout_j, lt);
-      }
-    }
-    __syncthreads();
-    for (int e = t; e < kQT * kQT; e += 256) {
-      const int col = e / kQT, row = e % kQT;
-      const int64_t i = i0 + row, j = j0 + col;
-      if (i < n0 && j < n1) p.out[j * n0 + i] = (int8_t)bt[col * kQT + row];
-    }
+  if (!full) {
+    quant_tile_ragged(p, i0, j0, reinterpret_cast<uint8_t*>(tile), q);
+    return;
   }
+  // 128 rows x 8 chunks of 16 bytes; chunk (row, c) stored at word column 4 * (c ^ ((row >> 4) & 7))
+  uint4 v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int qd = t + 256 * k, row = qd >> 3, c = qd & 7;
+    const uint4* src = reinterpret_cast<const uint4*>(p.in + (i0 + row) * n1 + j0 + 16 * c);
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
+                 : "l"(src));
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int qd = t + 256 * k, row = qd >> 3, c = qd & 7;
+    const uint4 o = quant_chunk<QIN, QOUT, OPS>(v[k], row, c, p, q);
+    const int wc = 4 * (c ^ ((row >> 4) & 7));
+    *reinterpret_cast<uint4*>(&tile[row * 32 + wc]) = o;
+  }
+  __syncthreads();
+  // unit: word column jg (output rows 4jg..4jg+3), 16-row chunk ic
+  const int jg = t >> 3, ic = t & 7;
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] = tile[(16 * ic + k) * 32 + (jg ^ (4 * ic))];
+  uint32_t outw[4][4];  // [q][m]
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t a = w[4 * m], b = w[4 * m + 1], c = w[4 * m + 2], d = w[4 * m + 3];
+    const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+    const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
+    outw[0][m] = __byte_perm(t0, t2, 0x5410);
+    outw[1][m] = __byte_perm(t0, t2, 0x7632);
+    outw[2][m] = __byte_perm(t1, t3, 0x5410);
+    outw[3][m] = __byte_perm(t1, t3, 0x7632);
+  }
+#pragma unroll
+  for (int qq = 0; qq < 4; ++qq) {
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (j0 + 4 * jg + qq) * n0 + i0 + 16 * ic);
+    *dst = make_uint4(outw[qq][0], outw[qq][1], outw[qq][2], outw[qq][3]);
+  }
+}
+
+template <int QIN, int QOUT>
+static cudaError_t quant_launch2(const QuantTilePlan& p, int64_t blocks, int64_t ntj, cudaStream_t s) {
+  if (p.ops.n) quant_tile_kernel<QIN, QOUT, true><<<(unsigned)blocks, 256, 0, s>>>(p, ntj);
+  else quant_tile_kernel<QIN, QOUT, false><<<(unsigned)blocks, 256, 0, s>>>(p, ntj);
+  return cudaGetLastError();
+}
+
+template <int QIN>
+static cudaError_t quant_launch1(const QuantTilePlan& p, int64_t blocks, int64_t ntj, cudaStream_t s) {
+  if (p.qout.axis == 0) return quant_launch2<QIN, 0>(p, blocks, ntj, s);
+  if (p.qout.axis == 1) return quant_launch2<QIN, 1>(p, blocks, ntj, s);
+  return quant_launch2<QIN, -1>(p, blocks, ntj, s);
 }
 
 cudaError_t launch_quant_tile(const QuantTilePlan& p, cudaStream_t s) {
@@ -400,8 +535,9 @@ cudaError_t launch_quant_tile(const QuantTilePlan& p, cudaStream_t s) {
   const int64_t blocks = nti * ntj;
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  quant_tile_kernel<<<(unsigned)blocks, 256, 0, s>>>(p, ntj);
-  return cudaGetLastError();
+  if (p.qin.axis == 0) return quant_launch1<0>(p, blocks, ntj, s);
+  if (p.qin.axis == 1) return quant_launch1<1>(p, blocks, ntj, s);
+  return quant_launch1<-1>(p, blocks, ntj, s);
 }
 
 // ---------------------------------------------------------------------------------------------
