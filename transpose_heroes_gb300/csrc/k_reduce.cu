@@ -169,6 +169,131 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_kernel(RowReducePlan p
   }
 }
 
+// ---- streaming row reduce (bulk asynchronous copies into a shared-memory ring) --------------------
+// Rows are cut into chunks of up to kChunkBytes. Thread 0 keeps kStages chunks in flight with 1-D bulk
+// copies (cp.async.bulk, completion counted on one mbarrier per stage); all threads consume a chunk
+// from shared memory with 16-byte reads, then a barrier frees its stage for the next copy. Bytes in
+// flight therefore do not depend on registers: up to kStages * kChunkBytes per block.
+constexpr int kStreamThreads = 256;
+constexpr int kChunkBytes = 16384;
+constexpr int kStages = 4;
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: far beyond any legitimate wait
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Waits for phase `parity` of the mbarrier; returns false if the bound ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+
+template <int IN_DT, int CH, int KIND>
+__global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePlan p, int cpr) {
+  extern __shared__ __align__(128) uint8_t ring[];  // kStages x kChunkBytes
+  __shared__ __align__(8) uint64_t bar[kStages];
+  __shared__ float red[32];
+  __shared__ int abort_flag;
+  const int tid = threadIdx.x;
+  constexpr int eb = IN_DT == F32 ? 4 : 2;
+  const int64_t row_bytes = p.len * eb;
+  const int64_t my_rows = p.rows > blockIdx.x ? (p.rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t n_chunks = my_rows * cpr;
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    abort_flag = 0;
+  }
+  __syncthreads();
+  auto chunk_src = [&](int64_t g, uint32_t& bytes) {
+    const int64_t row = blockIdx.x + (g / cpr) * (int64_t)gridDim.x;
+    const int64_t off = (g % cpr) * (int64_t)kChunkBytes;
+    const int64_t rem = row_bytes - off;
+    bytes = (uint32_t)(rem < kChunkBytes ? rem : kChunkBytes);
+    return reinterpret_cast<const uint8_t*>(p.in) + row * row_bytes + off;
+  };
+  auto issue = [&](int64_t g) {
+    uint32_t bytes;
+    const uint8_t* src = chunk_src(g, bytes);
+    const int s = (int)(g % kStages);
+    const uint32_t b = smem_addr(&bar[s]);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(ring + s * kChunkBytes)), "l"(src), "r"(bytes), "r"(b)
+                 : "memory");
+  };
+  if (tid == 0)
+    for (int64_t g = 0; g < kStages && g < n_chunks; ++g) issue(g);
+  const uint4* bv = reinterpret_cast<const uint4*>(p.chain.bptr);
+  const LogTab lt = global_log_tables();
+  float acc = identity<KIND>();
+  int64_t issued = n_chunks < kStages ? n_chunks : kStages;
+  for (int64_t g = 0; g < n_chunks; ++g) {
+    const int s = (int)(g % kStages);
+    const uint32_t parity = (uint32_t)((g / kStages) & 1);
+    if (!mbar_wait(smem_addr(&bar[s]), parity)) abort_flag = 1;
+    uint32_t bytes;
+    chunk_src(g, bytes);
+    const int64_t part = g % cpr;
+    const uint4* xv = reinterpret_cast<const uint4*>(ring + s * kChunkBytes);
+    const int nv = (int)(bytes / 16);
+    const int64_t vbase = part * (kChunkBytes / 16);  // vector index of the chunk within the row
+#pragma unroll 4
+    for (int v = tid; v < nv; v += kStreamThreads) {
+      const uint4 x = xv[v];
+      const uint4 b = CH == RC_EXP_BCAST_BF16 ? __ldg(bv + vbase + v) : make_uint4(0, 0, 0, 0);
+      acc = row_vec<IN_DT, CH, KIND>(x, b, acc, p.chain, lt);
+    }
+    __syncthreads();  // every thread is done with stage s
+    if (abort_flag) break;
+    if (tid == 0 && issued < n_chunks) issue(issued++);
+    if (part == cpr - 1) {
+      const int64_t row = blockIdx.x + (g / cpr) * (int64_t)gridDim.x;
+      acc = block_reduce<KIND>(acc, red);
+      if (tid == 0) store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+      acc = identity<KIND>();
+    }
+  }
+  if (abort_flag && tid == 0) {
+    // a copy did not complete in time: wait (bounded) for the copies still in flight, then leave
+    for (int64_t g = 0; g < issued; ++g) mbar_wait(smem_addr(&bar[g % kStages]), (uint32_t)((g / kStages) & 1));
+  }
+}
+
+template <int IN_DT, int KIND>
+static cudaError_t stream_dispatch(const RowReducePlan& p, cudaStream_t s, int ch) {
+  auto launch = [&](auto kernel) -> cudaError_t {
+    const size_t smem = (size_t)kStages * kChunkBytes;
+    static int nb = -1;
+    if (nb < 0) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kStreamThreads, smem) != cudaSuccess || nb < 1)
+        nb = 1;
+    }
+    int64_t grid = (int64_t)device_sm_count() * nb;
+    if (grid > p.rows) grid = p.rows;
+    const int cpr = (int)((p.len * dt_bytes(IN_DT) + kChunkBytes - 1) / kChunkBytes);
+    kernel<<<(unsigned)grid, kStreamThreads, smem, s>>>(p, cpr);
+    return cudaGetLastError();
+  };
+  if (ch == RC_EXP_BCAST_BF16 && IN_DT == BF16) return launch(row_stream_kernel<BF16, RC_EXP_BCAST_BF16, KIND>);
+  if (ch == RC_EXP) return launch(row_stream_kernel<IN_DT, RC_EXP, KIND>);
+  return launch(row_stream_kernel<IN_DT, RC_NONE, KIND>);
+}
+
 // Row kernel for the runtime chain when the broadcast operand is per row or the vector path does
 // not apply: scalar loads, any chain.
 template <int IN_DT, int KIND>
@@ -256,6 +381,15 @@ cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s) {
   bool vec = ((uintptr_t)p.in % 16 == 0) && ((p.len * eb) % 16 == 0);
   if (ch == RC_EXP_BCAST_BF16) vec = vec && ((uintptr_t)p.chain.bptr % 16 == 0);
   if (ch == RC_RT) vec = false;
+  // long rows on the vector path stream through the bulk-copy ring
+  const bool stream = vec && ch != RC_RT && p.len * eb >= 8192 && p.rows >= 64;
+  if (stream) {
+    if (p.in_dt == F32)
+      return p.kind == RED_ADD ? stream_dispatch<F32, RED_ADD>(p, s, ch) : stream_dispatch<F32, RED_MAX>(p, s, ch);
+    if (p.in_dt == BF16)
+      return p.kind == RED_ADD ? stream_dispatch<BF16, RED_ADD>(p, s, ch) : stream_dispatch<BF16, RED_MAX>(p, s, ch);
+    return p.kind == RED_ADD ? stream_dispatch<F16, RED_ADD>(p, s, ch) : stream_dispatch<F16, RED_MAX>(p, s, ch);
+  }
   if (p.in_dt == F32)
     return p.kind == RED_ADD ? row_dispatch<F32, RED_ADD>(p, s, ch, vec) : row_dispatch<F32, RED_MAX>(p, s, ch, vec);
   if (p.in_dt == BF16)
