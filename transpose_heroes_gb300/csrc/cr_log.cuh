@@ -193,6 +193,104 @@ __device__ __forceinline__ float cr_logf(float x, const float4* __restrict__ cta
   return ok ? y : cr_logf_accurate(x);
 }
 
+// ------------------------------------------------------------------------------------------------
+// Packed f32x2 arithmetic (two lanes of f32 in one 64-bit register; one instruction per pair).
+// ------------------------------------------------------------------------------------------------
+namespace f2 {
+__device__ __forceinline__ uint64_t pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t splat(float a) { return pk(a, a); }
+__device__ __forceinline__ uint64_t add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+}  // namespace f2
+
+// ------------------------------------------------------------------------------------------------
+// First pass, two elements at a time: 32-interval table (three 32-float arrays, so a warp's lookups
+// hit distinct banks), e*ln2 from exact products, error below ~2^-32 |y|:
+//   log x = A + r - r^2/2 + r^3 P(r) + (e*LN2_B + log(c)_lo),  A = e*LN2_A + log(c)_hi (exact),
+// with A + r and the -r^2/2 head added by Fast2Sum and -r^2/2 split exactly by FMA. Rounding test
+// (Ziv): yh + yl*(1 + 2^-6) rounds back to yh only if |yl| stays 2^-6 below the half gap to the
+// neighbouring float, which is more than the error bound; then yh is the correctly rounded log.
+// ok = false (about 1.6% of inputs, and every special operand) leaves the decision to cr_logf.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* __restrict__ tinv,
+                                               const float* __restrict__ thi, const float* __restrict__ tlo,
+                                               float& y0, float& y1, bool& ok0, bool& ok1) {
+  const uint32_t ix0 = __float_as_uint(x0), ix1 = __float_as_uint(x1);
+  const bool n0 = ix0 - 0x00800000u < 0x7F000000u, n1 = ix1 - 0x00800000u < 0x7F000000u;
+  const uint32_t t0 = ix0 - HLO_LOG1_OFF, t1 = ix1 - HLO_LOG1_OFF;
+  const uint32_t i0 = (t0 >> HLO_LOG1_SHIFT) & 31u, i1 = (t1 >> HLO_LOG1_SHIFT) & 31u;
+  const float m0 = __uint_as_float(ix0 - (t0 & 0xFF800000u)), m1 = __uint_as_float(ix1 - (t1 & 0xFF800000u));
+  // e as a float through the 1.5*2^23 constant (|e| < 2^22): bits 0x4B400000 + e, minus 1.5*2^23
+  const float eb0 = __int_as_float(0x4B400000 + ((int)t0 >> 23));
+  const float eb1 = __int_as_float(0x4B400000 + ((int)t1 >> 23));
+  const uint64_t EF = f2::sub(f2::pk(eb0, eb1), f2::splat(12582912.0f));
+  const uint64_t M = f2::pk(m0, m1);
+  const uint64_t INV = f2::pk(tinv[i0], tinv[i1]);
+  const uint64_t LCH = f2::pk(thi[i0], thi[i1]);
+  const uint64_t LCL = f2::pk(tlo[i0], tlo[i1]);
+  const uint64_t R = f2::fma(M, INV, f2::splat(-1.0f));            // exact
+  const uint64_t A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), LCH);   // exact (16-bit grid)
+  const uint64_t S = f2::add(A, R);                                 // Fast2Sum: A = 0 or |A| >= |r|
+  const uint64_t ERR = f2::sub(R, f2::sub(S, A));
+  const uint64_t HR = f2::mul(R, f2::splat(-0.5f));
+  const uint64_t QH = f2::mul(HR, R);                               // -r^2/2 rounded
+  const uint64_t QL = f2::fma(HR, R, f2::sub(f2::splat(0.0f), QH)); // its exact remainder
+  const uint64_t S2 = f2::add(S, QH);                               // Fast2Sum: |S| >> r^2/2
+  const uint64_t ERR2 = f2::sub(QH, f2::sub(S2, S));
+  const uint64_t RR = f2::mul(R, R);
+  const uint64_t R3 = f2::mul(RR, R);
+  uint64_t P = f2::fma(R, f2::splat(-0.125f), f2::splat(0.14285715f));
+  P = f2::fma(R, P, f2::splat(-0.16666667f));
+  P = f2::fma(R, P, f2::splat(0.2f));
+  P = f2::fma(R, P, f2::splat(-0.25f));
+  P = f2::fma(R, P, f2::splat(0.33333334f));
+  uint64_t REST = f2::fma(R3, P, QL);
+  REST = f2::add(REST, f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), LCL));
+  const uint64_t LO = f2::add(REST, f2::add(ERR, ERR2));
+  const uint64_t YH = f2::add(S2, LO);
+  const uint64_t YL = f2::sub(LO, f2::sub(YH, S2));
+  const uint64_t T = f2::fma(YL, f2::splat(1.015625f), YH);         // 1 + 2^-6
+  float z0, z1;
+  f2::upk(YH, y0, y1);
+  f2::upk(T, z0, z1);
+  ok0 = n0 & (z0 == y0);
+  ok1 = n1 & (z1 == y1);
+}
+
+// Loads the 32-entry first-pass table into shared memory (three arrays of 32 floats).
+__device__ __forceinline__ void load_log1_tables(float* s_inv, float* s_hi, float* s_lo) {
+  for (int i = threadIdx.x; i < 32; i += blockDim.x) {
+    s_inv[i] = kLog1Inv[i];
+    s_hi[i] = kLog1Hi[i];
+    s_lo[i] = kLog1Lo[i];
+  }
+}
+
 // Loads the tables into shared memory (called by all threads of a block, followed by a barrier).
 __device__ __forceinline__ void load_log_tables(float4* sc, float2* se) {
   for (int i = threadIdx.x; i < HLO_LOG_NC; i += blockDim.x) sc[i] = kLogCTab[i];

@@ -14,6 +14,12 @@ inv_c = 1, so log x = log1p(x - 1) near 1 with no cancellation. For the interval
 generator also checks |log c_hi| >= max |r| over the interval, which the kernel's Fast2Sum relies on.
 
 All values are computed with Python's decimal module at 60 digits and rounded to f32 exactly.
+A second, 32-entry table serves a cheap first pass (error ~2^-32, see cr_log.cuh): its interval holding
+1.0 is centred on 1.0 as well, and log(c) hi is rounded to a multiple of 2^-16 so that
+e*LN2_A + log(c)_hi is exact in f32 for every exponent (LN2_A = ln2 rounded to 16 bits; Tang's device);
+log(c)_lo = log(c) - log(c)_hi and LN2_B = ln2 - LN2_A are single floats. The generator checks that
+r is exact and that |log(c)_hi| >= max |r| wherever c != 1 (Fast2Sum precondition).
+
 Run:  python gen_log_table.py  (writes log_table.inc next to this file).
 """
 
@@ -107,6 +113,55 @@ def build():
     return ctab, etab, max_r
 
 
+# cheap first-pass table: 32 intervals
+OFF1_TARGET = 0x3F3504F3
+INDEX_BITS1 = 5
+SHIFT1 = 23 - INDEX_BITS1
+
+
+def off1():
+    half = 1 << (SHIFT1 - 1)
+    cands = [o for o in range(0x3F300000, 0x3F3A0000) if (0x3F800000 - o) % (1 << SHIFT1) == half]
+    return min(cands, key=lambda o: abs(o - OFF1_TARGET))
+
+
+def build1():
+    ln2 = Decimal(2).ln()
+    ln2_a = Decimal(round(ln2 * 2 ** 16)) / 2 ** 16
+    ln2_b = round_f32(ln2 - ln2_a)
+    off = off1()
+    rows = []
+    max_r = 0.0
+    for i in range(1 << INDEX_BITS1):
+        lo = off + (i << SHIFT1)
+        bits = np.arange(lo, lo + (1 << SHIFT1), dtype=np.uint64).astype(np.uint32)
+        m = bits.view(np.float32).astype(np.float64)
+        if m[0] <= 1.0 <= m[-1]:
+            inv_c = 1.0
+            ok, mr = residual_exact(m, inv_c)
+            assert ok
+        else:
+            target = 2.0 / (m[0] + m[-1])
+            chosen = None
+            for q in range(14, 0, -1):
+                cand = round(target * 2 ** q) / 2 ** q
+                ok, mr = residual_exact(m, cand)
+                if ok:
+                    chosen = (cand, mr)
+                    break
+            assert chosen is not None
+            inv_c, mr = chosen
+        logc = -Decimal(inv_c).ln()
+        hi = Decimal(round(logc * 2 ** 16)) / 2 ** 16
+        assert float(hi) == round_f32(hi)  # 16-bit grid value is an exact f32
+        lo_ = round_f32(logc - hi)
+        if inv_c != 1.0:
+            assert abs(float(hi)) >= mr, (i, hi, mr)
+        max_r = max(max_r, mr)
+        rows.append((inv_c, float(hi), lo_))
+    return off, float(ln2_a), ln2_b, rows, max_r
+
+
 def fmt(v: float) -> str:
     return f"{float(v).hex()}f" if v != 0 else "0.0f"
 
@@ -133,7 +188,15 @@ def main():
         for row in etab:
             f.write("  {" + ", ".join(fmt(v) for v in row) + "},\n")
         f.write("};\n")
-    print(f"wrote {out}; max |r| = {max_r} (2^{np.log2(max_r):.2f})")
+        off, ln2_a, ln2_b, rows, max_r1 = build1()
+        f.write(f"// First-pass table: 32 intervals (index = bits {SHIFT1}..22 of bits(x) - 0x{off:08X}); max |r| = {max_r1!r}\n")
+        f.write(f"#define HLO_LOG1_OFF 0x{off:08X}u\n")
+        f.write(f"#define HLO_LOG1_SHIFT {SHIFT1}\n")
+        f.write(f"#define HLO_LOG1_LN2_A {fmt(ln2_a)}\n")
+        f.write(f"#define HLO_LOG1_LN2_B {fmt(ln2_b)}\n")
+        for name, col in (("kLog1Inv", 0), ("kLog1Hi", 1), ("kLog1Lo", 2)):
+            f.write(f"static __device__ const float {name}[32] = {{" + ", ".join(fmt(r[col]) for r in rows) + "};\n")
+    print(f"wrote {out}; max |r| = {max_r} (2^{np.log2(max_r):.2f}); first pass max |r| = 2^{np.log2(max_r1):.2f}")
 
 
 if __name__ == "__main__":

@@ -18,13 +18,27 @@ __device__ __forceinline__ float ew_apply(const EwPlan& p, float v, const LogTab
   return apply_chain_rt<false>(p.epi, v, 0, lt);
 }
 
+// Two elements of log through the first pass, the rest of the correctly rounded log where it
+// leaves the rounding open (same result as cr_logf).
+__device__ __forceinline__ void log2x(float& a, float& b, const float* l1i, const float* l1h, const float* l1l,
+                                      const LogTab& lt) {
+  float ya, yb;
+  bool oa, ob;
+  cr_logf_first2(a, b, l1i, l1h, l1l, ya, yb, oa, ob);
+  a = oa ? ya : cr_logf(a, lt.c, lt.e);
+  b = ob ? yb : cr_logf(b, lt.c, lt.e);
+}
+
 template <bool VEC>
 __global__ void __launch_bounds__(256) elementwise_f32_kernel(EwPlan p) {
   __shared__ float4 s_lc[HLO_LOG_NC];
   __shared__ float2 s_le[HLO_LOG_NE];
+  __shared__ float s_l1[3][32];
   load_log_tables(s_lc, s_le);
+  load_log1_tables(s_l1[0], s_l1[1], s_l1[2]);
   __syncthreads();
   const LogTab lt = {s_lc, s_le};
+  const bool pure_log = p.pro.n == 1 && p.pro.op[0] == OP_LOG && p.epi.n == 0;
   const float* in = reinterpret_cast<const float*>(p.in);
   float* out = reinterpret_cast<float*>(p.out);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -34,10 +48,15 @@ __global__ void __launch_bounds__(256) elementwise_f32_kernel(EwPlan p) {
     const int64_t nv = p.n / 4;
     for (int64_t v = tid; v < nv; v += stride) {
       float4 x = __ldg(reinterpret_cast<const float4*>(in) + v);
-      x.x = ew_apply(p, x.x, lt);
-      x.y = ew_apply(p, x.y, lt);
-      x.z = ew_apply(p, x.z, lt);
-      x.w = ew_apply(p, x.w, lt);
+      if (pure_log) {
+        log2x(x.x, x.y, s_l1[0], s_l1[1], s_l1[2], lt);
+        log2x(x.z, x.w, s_l1[0], s_l1[1], s_l1[2], lt);
+      } else {
+        x.x = ew_apply(p, x.x, lt);
+        x.y = ew_apply(p, x.y, lt);
+        x.z = ew_apply(p, x.z, lt);
+        x.w = ew_apply(p, x.w, lt);
+      }
       reinterpret_cast<float4*>(out)[v] = x;
     }
     done = nv * 4;
