@@ -88,7 +88,10 @@ def check(f, gpu, ref, asum):
         else:
             same = gpu == ref
         nbad = int((~same).sum())
-        assert nbad == 0, f"{nbad} of {same.size} outputs differ; first at {np.argmax(~same)}"
+        if nbad:
+            where = np.flatnonzero(~same)[:4]
+            detail = [(int(w), gpu.flat[w].item(), ref.flat[w].item()) for w in where]
+            raise AssertionError(f"{nbad} of {same.size} outputs differ; (index, gpu, oracle): {detail}")
 
 
 NAMES = list(inp.FULL)
@@ -222,6 +225,26 @@ def test_selfadd_log_sizes(n):
     f = inp.transpose_log(seed=n, n=n)
     ref, _ = run_oracle(f)
     check(f, run_gpu(f), ref, None)
+
+
+@pytest.mark.parametrize("value", [1.015741229057312, 1.0, 0.5, 2.0 ** -130])
+def test_selfadd_every_element_open(value):
+    """Inputs whose log the first pass cannot round: the per-block list overflows and the per-thread
+    spill path settles the rest (and exactly 1.0 / a subnormal take the special-operand route)."""
+    n = 192
+    data = np.full(n * n, value, dtype=np.float32)
+    data[::7] = np.float32(1.3)  # a mix of open and settled elements
+    f = inp.Fusion(name="open", kind="transpose", dims=[n, n], m2m=[1, 0], dtype="f32", data=data,
+                   permutation=[1, 0], self_add=True, prologue={"ops": ["log"]}, out_dims=[n, n], out_m2m=[1, 0],
+                   out_dtype="f32")
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+    # the same value through the identity-layout log kernel
+    x = torch.full((1024,), value, dtype=torch.float32, device="cuda")
+    y = torch.empty_like(x)
+    hf.transpose_fusion(x, [1024], "f32", [0], y, prologue={"ops": ["log"]})
+    torch.cuda.synchronize()
+    assert np.all(y.cpu().numpy() == np.float32(oracle.log(float(np.float32(value)), "f32")))
 
 
 def test_selfadd_other_forms():
