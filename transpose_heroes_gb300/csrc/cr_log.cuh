@@ -194,38 +194,20 @@ __device__ __forceinline__ float cr_logf(float x, const float4* __restrict__ cta
 }
 
 // ------------------------------------------------------------------------------------------------
-// Packed f32x2 arithmetic (two lanes of f32 in one 64-bit register; one instruction per pair).
+// Packed f32x2 arithmetic through CUDA's float2 intrinsics (one instruction per pair of lanes, each
+// lane rounded to nearest even, never contracted).
 // ------------------------------------------------------------------------------------------------
 namespace f2 {
-__device__ __forceinline__ uint64_t pk(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
+__device__ __forceinline__ float2 pk(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ void upk(float2 r, float& a, float& b) {
+  a = r.x;
+  b = r.y;
 }
-__device__ __forceinline__ void upk(uint64_t r, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ uint64_t splat(float a) { return pk(a, a); }
-__device__ __forceinline__ uint64_t add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
+__device__ __forceinline__ float2 splat(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+__device__ __forceinline__ float2 mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 }  // namespace f2
 
 // ------------------------------------------------------------------------------------------------
@@ -248,33 +230,33 @@ __device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* 
   // e as a float through the 1.5*2^23 constant (|e| < 2^22): bits 0x4B400000 + e, minus 1.5*2^23
   const float eb0 = __int_as_float(0x4B400000 + ((int)t0 >> 23));
   const float eb1 = __int_as_float(0x4B400000 + ((int)t1 >> 23));
-  const uint64_t EF = f2::sub(f2::pk(eb0, eb1), f2::splat(12582912.0f));
-  const uint64_t M = f2::pk(m0, m1);
-  const uint64_t INV = f2::pk(tinv[i0], tinv[i1]);
-  const uint64_t LCH = f2::pk(thi[i0], thi[i1]);
-  const uint64_t LCL = f2::pk(tlo[i0], tlo[i1]);
-  const uint64_t R = f2::fma(M, INV, f2::splat(-1.0f));            // exact
-  const uint64_t A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), LCH);   // exact (16-bit grid)
-  const uint64_t S = f2::add(A, R);                                 // Fast2Sum: A = 0 or |A| >= |r|
-  const uint64_t ERR = f2::sub(R, f2::sub(S, A));
-  const uint64_t HR = f2::mul(R, f2::splat(-0.5f));
-  const uint64_t QH = f2::mul(HR, R);                               // -r^2/2 rounded
-  const uint64_t QL = f2::fma(HR, R, f2::sub(f2::splat(0.0f), QH)); // its exact remainder
-  const uint64_t S2 = f2::add(S, QH);                               // Fast2Sum: |S| >> r^2/2
-  const uint64_t ERR2 = f2::sub(QH, f2::sub(S2, S));
-  const uint64_t RR = f2::mul(R, R);
-  const uint64_t R3 = f2::mul(RR, R);
-  uint64_t P = f2::fma(R, f2::splat(-0.125f), f2::splat(0.14285715f));
+  const float2 EF = f2::sub(f2::pk(eb0, eb1), f2::splat(12582912.0f));
+  const float2 M = f2::pk(m0, m1);
+  const float2 INV = f2::pk(tinv[i0], tinv[i1]);
+  const float2 LCH = f2::pk(thi[i0], thi[i1]);
+  const float2 LCL = f2::pk(tlo[i0], tlo[i1]);
+  const float2 R = f2::fma(M, INV, f2::splat(-1.0f));            // exact
+  const float2 A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), LCH);   // exact (16-bit grid)
+  const float2 S = f2::add(A, R);                                 // Fast2Sum: A = 0 or |A| >= |r|
+  const float2 ERR = f2::sub(R, f2::sub(S, A));
+  const float2 HR = f2::mul(R, f2::splat(-0.5f));
+  const float2 QH = f2::mul(HR, R);                               // -r^2/2 rounded
+  const float2 QL = f2::fma(HR, R, f2::sub(f2::splat(0.0f), QH)); // its exact remainder
+  const float2 S2 = f2::add(S, QH);                               // Fast2Sum: |S| >> r^2/2
+  const float2 ERR2 = f2::sub(QH, f2::sub(S2, S));
+  const float2 RR = f2::mul(R, R);
+  const float2 R3 = f2::mul(RR, R);
+  float2 P = f2::fma(R, f2::splat(-0.125f), f2::splat(0.14285715f));
   P = f2::fma(R, P, f2::splat(-0.16666667f));
   P = f2::fma(R, P, f2::splat(0.2f));
   P = f2::fma(R, P, f2::splat(-0.25f));
   P = f2::fma(R, P, f2::splat(0.33333334f));
-  uint64_t REST = f2::fma(R3, P, QL);
+  float2 REST = f2::fma(R3, P, QL);
   REST = f2::add(REST, f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), LCL));
-  const uint64_t LO = f2::add(REST, f2::add(ERR, ERR2));
-  const uint64_t YH = f2::add(S2, LO);
-  const uint64_t YL = f2::sub(LO, f2::sub(YH, S2));
-  const uint64_t T = f2::fma(YL, f2::splat(1.015625f), YH);         // 1 + 2^-6
+  const float2 LO = f2::add(REST, f2::add(ERR, ERR2));
+  const float2 YH = f2::add(S2, LO);
+  const float2 YL = f2::sub(LO, f2::sub(YH, S2));
+  const float2 T = f2::fma(YL, f2::splat(1.015625f), YH);         // 1 + 2^-6
   float z0, z1;
   f2::upk(YH, y0, y1);
   f2::upk(T, z0, z1);
