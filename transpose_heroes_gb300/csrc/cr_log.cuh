@@ -212,12 +212,14 @@ __device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) { return __f
 
 // ------------------------------------------------------------------------------------------------
 // First pass, two elements at a time: 32-interval table (three 32-float arrays, so a warp's lookups
-// hit distinct banks), e*ln2 from exact products, error below ~2^-32 |y|:
-//   log x = A + r - r^2/2 + r^3 P(r) + (e*LN2_B + log(c)_lo),  A = e*LN2_A + log(c)_hi (exact),
-// with A + r and the -r^2/2 head added by Fast2Sum and -r^2/2 split exactly by FMA. Rounding test
-// (Ziv): yh + yl*(1 + 2^-6) rounds back to yh only if |yl| stays 2^-6 below the half gap to the
-// neighbouring float, which is more than the error bound; then yh is the correctly rounded log.
-// ok = false (about 1.6% of inputs, and every special operand) leaves the decision to cr_logf.
+// hit distinct banks), e*ln2 from exact products:
+//   log x = S + err + rest,  S + err = A + r exactly (Fast2Sum),  A = e*LN2_A + log(c)_hi (exact),
+//   rest = r^2 (-1/2 + r/3 - r^2/4 + r^3/5 - r^4/6 + r^5/7) + (e*LN2_B + log(c)_lo)   in f32.
+// Every error (rest's rounding ~2^-35.3, the lo sum ~2^-36.3, table and LN2_B terms below 2^-36 for
+// all exponents, truncation 2^-48) stays under the absolute bound 2^-33.5. Rounding test: yh is the
+// correctly rounded log when yh + (yl +- 2^-33.5), the error interval's end nearer a boundary, still
+// rounds to yh. About 2% of inputs in [0.5, 2) (most of those near 1) and every special operand are
+// left open (ok = false) for cr_logf.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* __restrict__ tinv,
                                                const float* __restrict__ thi, const float* __restrict__ tlo,
@@ -230,38 +232,27 @@ __device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* 
   // e as a float through the 1.5*2^23 constant (|e| < 2^22): bits 0x4B400000 + e, minus 1.5*2^23
   const float eb0 = __int_as_float(0x4B400000 + ((int)t0 >> 23));
   const float eb1 = __int_as_float(0x4B400000 + ((int)t1 >> 23));
-  const float2 EF = f2::sub(f2::pk(eb0, eb1), f2::splat(12582912.0f));
-  const float2 M = f2::pk(m0, m1);
-  const float2 INV = f2::pk(tinv[i0], tinv[i1]);
-  const float2 LCH = f2::pk(thi[i0], thi[i1]);
-  const float2 LCL = f2::pk(tlo[i0], tlo[i1]);
-  const float2 R = f2::fma(M, INV, f2::splat(-1.0f));            // exact
-  const float2 A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), LCH);   // exact (16-bit grid)
-  const float2 S = f2::add(A, R);                                 // Fast2Sum: A = 0 or |A| >= |r|
+  const float2 EF = f2::add(f2::pk(eb0, eb1), f2::splat(-12582912.0f));
+  const float2 R = f2::fma(f2::pk(m0, m1), f2::pk(tinv[i0], tinv[i1]), f2::splat(-1.0f));  // exact
+  const float2 A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), f2::pk(thi[i0], thi[i1]));        // exact
+  const float2 S = f2::add(A, R);                       // Fast2Sum: A = 0 or |A| >= |r|
   const float2 ERR = f2::sub(R, f2::sub(S, A));
-  const float2 HR = f2::mul(R, f2::splat(-0.5f));
-  const float2 QH = f2::mul(HR, R);                               // -r^2/2 rounded
-  const float2 QL = f2::fma(HR, R, f2::sub(f2::splat(0.0f), QH)); // its exact remainder
-  const float2 S2 = f2::add(S, QH);                               // Fast2Sum: |S| >> r^2/2
-  const float2 ERR2 = f2::sub(QH, f2::sub(S2, S));
-  const float2 RR = f2::mul(R, R);
-  const float2 R3 = f2::mul(RR, R);
-  float2 P = f2::fma(R, f2::splat(-0.125f), f2::splat(0.14285715f));
-  P = f2::fma(R, P, f2::splat(-0.16666667f));
+  float2 P = f2::fma(R, f2::splat(0.14285715f), f2::splat(-0.16666667f));
   P = f2::fma(R, P, f2::splat(0.2f));
   P = f2::fma(R, P, f2::splat(-0.25f));
   P = f2::fma(R, P, f2::splat(0.33333334f));
-  float2 REST = f2::fma(R3, P, QL);
-  REST = f2::add(REST, f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), LCL));
-  const float2 LO = f2::add(REST, f2::add(ERR, ERR2));
-  const float2 YH = f2::add(S2, LO);
-  const float2 YL = f2::sub(LO, f2::sub(YH, S2));
-  const float2 T = f2::fma(YL, f2::splat(1.015625f), YH);         // 1 + 2^-6
-  float z0, z1;
-  f2::upk(YH, y0, y1);
-  f2::upk(T, z0, z1);
-  ok0 = n0 & (z0 == y0);
-  ok1 = n1 & (z1 == y1);
+  P = f2::fma(R, P, f2::splat(-0.5f));
+  const float2 B = f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), f2::pk(tlo[i0], tlo[i1]));
+  const float2 REST = f2::fma(f2::mul(R, R), P, B);
+  const float2 LO = f2::add(ERR, REST);
+  const float2 YH = f2::add(S, LO);
+  const float2 YL = f2::sub(LO, f2::sub(YH, S));
+  const float bound = 0x1.6a09e6p-34f;                  // 2^-33.5
+  const float2 T = f2::add(YH, f2::add(YL, f2::pk(copysignf(bound, YL.x), copysignf(bound, YL.y))));
+  y0 = YH.x;
+  y1 = YH.y;
+  ok0 = n0 & (T.x == YH.x);
+  ok1 = n1 & (T.y == YH.y);
 }
 
 // Loads the 32-entry first-pass table into shared memory (three arrays of 32 floats).

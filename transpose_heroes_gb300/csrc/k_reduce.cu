@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_kernel(RowReducePlan p
 // flight therefore do not depend on registers: up to kStages * kChunkBytes per block.
 constexpr int kStreamThreads = 256;
 constexpr int kChunkBytes = 16384;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: far beyond any legitimate wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -195,6 +195,48 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     if (done) return true;
     if (clock64() - t0 > kWaitCycles) return false;
+  }
+}
+
+// Packed (float2) element work of the streaming row reduce for the add body: two independent
+// f32 partial sums per thread, combined at the end of the row.
+__device__ __forceinline__ float ex2_approx(float t) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(t));
+  return y;
+}
+
+template <int IN_DT, int CH>
+__device__ __forceinline__ float2 row_vec2_add(uint4 x, uint4 b, float2 acc) {
+  const float2 l2e = make_float2(1.4426950408889634f, 1.4426950408889634f);
+  if (IN_DT == F32) {
+    float2 v0 = make_float2(__uint_as_float(x.x), __uint_as_float(x.y));
+    float2 v1 = make_float2(__uint_as_float(x.z), __uint_as_float(x.w));
+    if (CH == RC_EXP) {
+      const float2 t0 = __fmul2_rn(v0, l2e), t1 = __fmul2_rn(v1, l2e);
+      v0 = make_float2(ex2_approx(t0.x), ex2_approx(t0.y));
+      v1 = make_float2(ex2_approx(t1.x), ex2_approx(t1.y));
+    }
+    return __fadd2_rn(__fadd2_rn(acc, v0), v1);
+  } else {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 v = IN_DT == BF16 ? make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u))
+                               : make_float2(f16_bits_to_f32((uint16_t)(w[i] & 0xFFFFu)),
+                                             f16_bits_to_f32((uint16_t)(w[i] >> 16)));
+      if (CH == RC_EXP_BCAST_BF16) {
+        // bf16(exp(x)), then the bf16 add with the broadcast pair rounded once (add.rn.bf16x2)
+        const float2 t = __fmul2_rn(v, l2e);
+        uint32_t e2, s2;
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(e2) : "f"(ex2_approx(t.y)), "f"(ex2_approx(t.x)));
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(s2) : "r"(e2), "r"(bw[i]));
+        v = make_float2(__uint_as_float(s2 << 16), __uint_as_float(s2 & 0xFFFF0000u));
+      }
+      acc = __fadd2_rn(acc, v);
+    }
+    return acc;
   }
 }
 
@@ -250,11 +292,22 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
     const uint4* xv = reinterpret_cast<const uint4*>(ring + s * kChunkBytes);
     const int nv = (int)(bytes / 16);
     const int64_t vbase = part * (kChunkBytes / 16);  // vector index of the chunk within the row
+    if (KIND == RED_ADD && CH != RC_RT && !(CH == RC_EXP && IN_DT != F32 && p.chain.round16)) {
+      float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll 4
-    for (int v = tid; v < nv; v += kStreamThreads) {
-      const uint4 x = xv[v];
-      const uint4 b = CH == RC_EXP_BCAST_BF16 ? __ldg(bv + vbase + v) : make_uint4(0, 0, 0, 0);
-      acc = row_vec<IN_DT, CH, KIND>(x, b, acc, p.chain, lt);
+      for (int v = tid; v < nv; v += kStreamThreads) {
+        const uint4 x = xv[v];
+        const uint4 b = CH == RC_EXP_BCAST_BF16 ? __ldg(bv + vbase + v) : make_uint4(0, 0, 0, 0);
+        acc2 = row_vec2_add<IN_DT, CH>(x, b, acc2);
+      }
+      acc = __fadd_rn(acc, __fadd_rn(acc2.x, acc2.y));
+    } else {
+#pragma unroll 4
+      for (int v = tid; v < nv; v += kStreamThreads) {
+        const uint4 x = xv[v];
+        const uint4 b = CH == RC_EXP_BCAST_BF16 ? __ldg(bv + vbase + v) : make_uint4(0, 0, 0, 0);
+        acc = row_vec<IN_DT, CH, KIND>(x, b, acc, p.chain, lt);
+      }
     }
     __syncthreads();  // every thread is done with stage s
     if (abort_flag) break;

@@ -442,15 +442,29 @@ __device__ __noinline__ void quant_tile_ragged(const QuantTilePlan& p, int64_t i
   }
 }
 
-// Fast path of quant_code: returns false (leaving q undefined) when the exact definition must decide.
-__device__ __forceinline__ bool quant_code_fast(float real, float inv, int zp, int smin, int smax, int& q) {
-  const float y = __fmul_rn(real, inv);
-  const float t = __fadd_rn(y, kMagic);
-  const float f = __fsub_rn(y, __fsub_rn(t, kMagic));
-  const float ay = fabsf(y);
-  const bool ok = (ay < 4194304.0f) & (fabsf(__fsub_rn(fabsf(f), 0.5f)) > __fmul_rn(ay, 0x1p-22f));
-  q = min(max((__float_as_int(t) - kMagicBits) + zp, smin), smax);
-  return ok;
+// Two codes at a time: dequantize, optional float chain, then the fast path of quant_code with
+// float2 arithmetic. okmask bit 0/1 is cleared when the exact definition must decide that lane.
+template <bool OPS>
+__device__ __forceinline__ void quant_pair(int c0, int c1, float2 sin, int2 zin, float2 inv, int2 zout, int smin,
+                                           int smax, const QuantTilePlan& p, int& q0, int& q1, uint32_t& okmask) {
+  const float2 magic = make_float2(kMagic, kMagic);
+  const float2 df = __fadd2_rn(make_float2(__int_as_float(kMagicBits + c0 - zin.x), __int_as_float(kMagicBits + c1 - zin.y)),
+                               make_float2(-kMagic, -kMagic));  // exact q - zero_point
+  float2 real = __fmul2_rn(sin, df);
+  if (OPS) {
+    real.x = apply_chain_rt<false>(p.ops, real.x, 0, global_log_tables());
+    real.y = apply_chain_rt<false>(p.ops, real.y, 0, global_log_tables());
+  }
+  const float2 y = __fmul2_rn(real, inv);
+  const float2 t = __fadd2_rn(y, magic);
+  const float2 f = __fadd2_rn(y, __fadd2_rn(make_float2(-t.x, -t.y), magic));  // y - rint(y)
+  const float2 g = __fadd2_rn(make_float2(fabsf(f.x), fabsf(f.y)), make_float2(-0.5f, -0.5f));
+  const float2 lim = __fmul2_rn(make_float2(fabsf(y.x), fabsf(y.y)), make_float2(0x1p-22f, 0x1p-22f));
+  const bool ok0 = (fabsf(y.x) < 4194304.0f) & (fabsf(g.x) > lim.x);
+  const bool ok1 = (fabsf(y.y) < 4194304.0f) & (fabsf(g.y) > lim.y);
+  q0 = min(max((__float_as_int(t.x) - kMagicBits) + zout.x, smin), smax);
+  q1 = min(max((__float_as_int(t.y) - kMagicBits) + zout.y, smin), smax);
+  okmask = (ok0 ? 1u : 0u) | (ok1 ? 2u : 0u);
 }
 
 template <int QIN, int QOUT, bool OPS>
@@ -464,7 +478,8 @@ __device__ __forceinline__ void quant_params(int row, int jl, const QuantTilePla
 }
 
 // 16 codes of one tile row (local row `row`, local columns 16c .. 16c+15) -> 16 output codes. The
-// fast path runs for all 16; the rare ones it cannot decide are recomputed exactly afterwards.
+// fast path runs for all 16 (two per float2 instruction); the rare ones it cannot decide are
+// recomputed exactly afterwards.
 template <int QIN, int QOUT, bool OPS>
 __device__ __forceinline__ uint4 quant_chunk(uint4 x, int row, int c, const QuantTilePlan& p, const QuantSmem& q) {
   const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -474,17 +489,19 @@ __device__ __forceinline__ uint4 quant_chunk(uint4 x, int row, int c, const Quan
   for (int m = 0; m < 4; ++m) {
     uint32_t packed = 0;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < 4; b += 2) {
       const int jl = 16 * c + 4 * m + b;
-      const int code = (int)(int8_t)(w[m] >> (8 * b));
-      float sin, sout, inv;
-      int zin, zout;
-      quant_params<QIN, QOUT, OPS>(row, jl, p, q, sin, zin, sout, inv, zout);
-      float real = dequant(code, sin, zin);
-      if (OPS) real = apply_chain_rt<false>(p.ops, real, 0, global_log_tables());
-      int r;
-      if (!quant_code_fast(real, inv, zout, p.qout.smin, p.qout.smax, r)) redo |= 1u << (4 * m + b);
-      packed |= ((uint32_t)r & 0xFFu) << (8 * b);
+      const int c0 = (int)(int8_t)(w[m] >> (8 * b)), c1 = (int)(int8_t)(w[m] >> (8 * b + 8));
+      float s0, s1, so0, so1, i0, i1;
+      int z0, z1, zo0, zo1;
+      quant_params<QIN, QOUT, OPS>(row, jl, p, q, s0, z0, so0, i0, zo0);
+      quant_params<QIN, QOUT, OPS>(row, jl + 1, p, q, s1, z1, so1, i1, zo1);
+      int r0, r1;
+      uint32_t okm;
+      quant_pair<OPS>(c0, c1, make_float2(s0, s1), make_int2(z0, z1), make_float2(i0, i1), make_int2(zo0, zo1),
+                      p.qout.smin, p.qout.smax, p, r0, r1, okm);
+      redo |= ((~okm) & 3u) << (4 * m + b);
+      packed |= (((uint32_t)r0 & 0xFFu) << (8 * b)) | (((uint32_t)r1 & 0xFFu) << (8 * b + 8));
     }
     o[m] = packed;
   }
