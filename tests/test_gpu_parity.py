@@ -195,6 +195,21 @@ def test_max_nan_and_signed_zero():
         assert np.isnan(gpu[0]) and gpu[1] == 0 and not np.signbit(gpu[1]) and np.signbit(gpu[2])
 
 
+@pytest.mark.parametrize("d3", [8192 + 8, 20000, 16384])
+def test_streaming_row_reduce_chunking(d3):
+    """Rows long enough for the bulk-copy ring: a second chunk of 16 bytes, three chunks (broadcast read
+    from memory), and exactly two full chunks (broadcast held in registers)."""
+    f = inp.bcast_exp_reduce(seed=9, d0=2, d2=37, d3=d3)
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+    g = inp.rng(d3)
+    x = inp.normal_bf16(g, 70 * d3)
+    f = inp.Fusion(name="maxrow", kind="reduce", dims=[70, d3], m2m=[1, 0], dtype="bf16", data=x, dimensions=[1],
+                   reduce_kind="max", init=-math.inf, out_dims=[70], out_m2m=[0], out_dtype="bf16")
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+
+
 def test_bcast_row_reduce_variants():
     g = inp.rng(5)
     d0, d2, d3 = 2, 7, 515

@@ -240,7 +240,7 @@ __device__ __forceinline__ float2 row_vec2_add(uint4 x, uint4 b, float2 acc) {
   }
 }
 
-template <int IN_DT, int CH, int KIND>
+template <int IN_DT, int CH, int KIND, bool BREG>
 __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePlan p, int cpr) {
   extern __shared__ __align__(128) uint8_t ring[];  // kStages x kChunkBytes
   __shared__ __align__(8) uint64_t bar[kStages];
@@ -280,6 +280,19 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
     for (int64_t g = 0; g < kStages && g < n_chunks; ++g) issue(g);
   const uint4* bv = reinterpret_cast<const uint4*>(p.chain.bptr);
   const LogTab lt = global_log_tables();
+  // BREG: rows of at most two chunks; this thread's slice of the broadcast vector (the same for every
+  // row) stays in registers: vectors tid + 256 k of each chunk.
+  constexpr int kVecPerThread = kChunkBytes / 16 / kStreamThreads;
+  uint4 breg[2][kVecPerThread];
+  if (BREG) {
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int k = 0; k < kVecPerThread; ++k) {
+        const int64_t vi = (int64_t)part * (kChunkBytes / 16) + tid + k * kStreamThreads;
+        breg[part][k] = (part < cpr && vi * 16 < row_bytes) ? __ldg(bv + vi) : make_uint4(0, 0, 0, 0);
+      }
+  }
   float acc = identity<KIND>();
   int64_t issued = n_chunks < kStages ? n_chunks : kStages;
   for (int64_t g = 0; g < n_chunks; ++g) {
@@ -292,7 +305,15 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
     const uint4* xv = reinterpret_cast<const uint4*>(ring + s * kChunkBytes);
     const int nv = (int)(bytes / 16);
     const int64_t vbase = part * (kChunkBytes / 16);  // vector index of the chunk within the row
-    if (KIND == RED_ADD && CH != RC_RT && !(CH == RC_EXP && IN_DT != F32 && p.chain.round16)) {
+    if (BREG) {
+      float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < kVecPerThread; ++k) {
+        const int v = tid + k * kStreamThreads;
+        if (v < nv) acc2 = row_vec2_add<IN_DT, CH>(xv[v], part == 0 ? breg[0][k] : breg[1][k], acc2);
+      }
+      acc = __fadd_rn(acc, __fadd_rn(acc2.x, acc2.y));
+    } else if (KIND == RED_ADD && CH != RC_RT && !(CH == RC_EXP && IN_DT != F32 && p.chain.round16)) {
       float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll 4
       for (int v = tid; v < nv; v += kStreamThreads) {
@@ -342,9 +363,13 @@ static cudaError_t stream_dispatch(const RowReducePlan& p, cudaStream_t s, int c
     kernel<<<(unsigned)grid, kStreamThreads, smem, s>>>(p, cpr);
     return cudaGetLastError();
   };
-  if (ch == RC_EXP_BCAST_BF16 && IN_DT == BF16) return launch(row_stream_kernel<BF16, RC_EXP_BCAST_BF16, KIND>);
-  if (ch == RC_EXP) return launch(row_stream_kernel<IN_DT, RC_EXP, KIND>);
-  return launch(row_stream_kernel<IN_DT, RC_NONE, KIND>);
+  const bool two_chunks = p.len * dt_bytes(IN_DT) <= 2 * (int64_t)kChunkBytes;
+  if (ch == RC_EXP_BCAST_BF16 && IN_DT == BF16) {
+    if (two_chunks && KIND == RED_ADD) return launch(row_stream_kernel<BF16, RC_EXP_BCAST_BF16, KIND, true>);
+    return launch(row_stream_kernel<BF16, RC_EXP_BCAST_BF16, KIND, false>);
+  }
+  if (ch == RC_EXP) return launch(row_stream_kernel<IN_DT, RC_EXP, KIND, false>);
+  return launch(row_stream_kernel<IN_DT, RC_NONE, KIND, false>);
 }
 
 // Row kernel for the runtime chain when the broadcast operand is per row or the vector path does

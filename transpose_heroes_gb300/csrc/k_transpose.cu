@@ -106,14 +106,8 @@ __device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t 
       bool ok[4];
       cr_logf_first2(v[k].x, v[k].y, ps.l1_inv, ps.l1_hi, ps.l1_lo, y[0], y[1], ok[0], ok[1]);
       cr_logf_first2(v[k].z, v[k].w, ps.l1_inv, ps.l1_hi, ps.l1_lo, y[2], y[3], ok[2], ok[3]);
-      const float* xi = &v[k].x;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (!ok[q]) {
-          redo |= 1u << (4 * k + q);
-          y[q] = xi[q];  // park the input
-        }
-      }
+      for (int q = 0; q < 4; ++q) redo |= (ok[q] ? 0u : 1u) << (4 * k + q);
     } else {
       const float* xi = &v[k].x;
 #pragma unroll
@@ -153,20 +147,30 @@ __device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t 
   }
 }
 
-// Settles the elements the first pass left open: the block's list, then this thread's spills.
-__device__ __forceinline__ void pair_settle(float* tiles, PairShared& ps, uint32_t spill, const LogTab& lt) {
+// Settles the elements the first pass left open -- the block's list, then this thread's spills --
+// recomputing each from its input, re-read from global memory (slot offset -> tile, row, column).
+__device__ __forceinline__ float pair_input(const float* __restrict__ in, int64_t n, int64_t I, int64_t J, int off) {
+  const bool second = off >= kT * kTP;
+  const int o = second ? off - kT * kTP : off;
+  const int col = o / kTP, r = o % kTP;  // slots hold tile element (r, col) at col * kTP + r
+  const int64_t gr = (second ? J : I) * kT + r, gc = (second ? I : J) * kT + col;
+  return (gr < n && gc < n) ? in[gr * n + gc] : 1.f;
+}
+
+__device__ __forceinline__ void pair_settle(float* tiles, const float* __restrict__ in, int64_t n, int64_t I,
+                                            int64_t J, PairShared& ps, uint32_t spill, const LogTab& lt) {
   const int cnt = min(ps.redo_count, kRedoCap);
   for (int j = threadIdx.x; j < cnt; j += kPairThreads) {
-    float* slot = tiles + ps.redo[j];
-    *slot = cr_logf(*slot, lt.c, lt.e);
+    const int off = ps.redo[j];
+    tiles[off] = cr_logf(pair_input(in, n, I, J, off), lt.c, lt.e);
   }
   while (spill) {
     const int e = __ffs(spill) - 1;
     spill &= spill - 1;
     int r, col;
     pair_slot((e & 15) >> 2, r, col);
-    float* slot = tiles + ((e >= 16) ? kT * kTP : 0) + (col + (e & 3)) * kTP + r;
-    *slot = cr_logf(*slot, lt.c, lt.e);
+    const int off = ((e >= 16) ? kT * kTP : 0) + (col + (e & 3)) * kTP + r;
+    tiles[off] = cr_logf(pair_input(in, n, I, J, off), lt.c, lt.e);
   }
 }
 
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kPairThreads, 4)
     __syncthreads();
     if (CH == PC_LOG) {
       if (ps.redo_count) {  // uniform: every thread reads the same count after the barrier
-        pair_settle(ta, ps, spill, lt);
+        pair_settle(ta, in, p.n, I, J, ps, spill, lt);
         __syncthreads();
       }
     }
