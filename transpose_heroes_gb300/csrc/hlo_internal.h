@@ -189,4 +189,8 @@ cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, con
 // Device properties cached per device (SM count, cluster support).
 int device_sm_count();
 
+// Resident blocks per SM of `kernel` at this block size and dynamic shared memory, cached per kernel
+// and device; on first use also raises the kernel's dynamic shared-memory limit to `smem`.
+int kernel_blocks_per_sm(const void* kernel, int threads, size_t smem);
+
 }  // namespace hlo

@@ -350,13 +350,7 @@ template <int IN_DT, int KIND>
 static cudaError_t stream_dispatch(const RowReducePlan& p, cudaStream_t s, int ch) {
   auto launch = [&](auto kernel) -> cudaError_t {
     const size_t smem = (size_t)kStages * kChunkBytes;
-    static int nb = -1;
-    if (nb < 0) {
-      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kStreamThreads, smem) != cudaSuccess || nb < 1)
-        nb = 1;
-    }
+    const int nb = kernel_blocks_per_sm((const void*)kernel, kStreamThreads, smem);
     int64_t grid = (int64_t)device_sm_count() * nb;
     if (grid > p.rows) grid = p.rows;
     const int cpr = (int)((p.len * dt_bytes(IN_DT) + kChunkBytes - 1) / kChunkBytes);
@@ -400,18 +394,10 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_rt_kernel(RowReducePla
   }
 }
 
-template <typename K>
-static int occupancy_blocks(K kernel, int threads) {
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, 0) != cudaSuccess || nb < 1) nb = 1;
-  return nb;
-}
-
 template <int IN_DT, int KIND>
 static cudaError_t row_dispatch(const RowReducePlan& p, cudaStream_t s, int ch, bool vec) {
   auto launch = [&](auto kernel) -> cudaError_t {
-    static int nb = -1;
-    if (nb < 0) nb = occupancy_blocks(kernel, kRowThreads);
+    const int nb = kernel_blocks_per_sm((const void*)kernel, kRowThreads, 0);
     int64_t grid = (int64_t)device_sm_count() * nb;
     if (grid > p.rows) grid = p.rows;
     if (grid < 1) grid = 1;

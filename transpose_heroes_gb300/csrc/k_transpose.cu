@@ -263,13 +263,7 @@ template <int CH, bool VEC>
 static cudaError_t pair_launch(const SelfAddPlan& p, cudaStream_t s) {
   auto kernel = selfadd_pair_kernel<CH, VEC>;
   const size_t smem = pair_smem_bytes();
-  static int nb = -1;
-  if (nb < 0) {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, kPairThreads, smem) != cudaSuccess || nb < 1)
-      nb = 1;
-  }
+  const int nb = kernel_blocks_per_sm((const void*)kernel, kPairThreads, smem);
   const int64_t nt = (p.n + kT - 1) / kT;
   const int64_t n_off = nt * (nt - 1) / 2;
   const int64_t n_items = n_off + nt;
