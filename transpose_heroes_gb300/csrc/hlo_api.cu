@@ -319,7 +319,7 @@ int hlo::kernel_blocks_per_sm(const void* kernel, int threads, size_t smem) {
   auto key = std::make_pair(kernel, dev * 4096 + threads);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
-  if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem > 0) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int nb = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess || nb < 1) nb = 1;
   cudaGetLastError();  // clear any error from the queries above
