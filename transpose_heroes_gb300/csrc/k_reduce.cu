@@ -185,7 +185,7 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
 
 // Waits for phase `parity` of the mbarrier; returns false if the bound ran out.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
+  long long t0 = -1;
   while (true) {
     uint32_t done;
     asm volatile(
@@ -194,7 +194,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     if (done) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+    const long long now = clock64();
+    if (t0 < 0) t0 = now;
+    else if (now - t0 > kWaitCycles) return false;
   }
 }
 
@@ -258,26 +260,32 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
     abort_flag = 0;
   }
   __syncthreads();
-  auto chunk_src = [&](int64_t g, uint32_t& bytes) {
-    const int64_t row = blockIdx.x + (g / cpr) * (int64_t)gridDim.x;
-    const int64_t off = (g % cpr) * (int64_t)kChunkBytes;
-    const int64_t rem = row_bytes - off;
-    bytes = (uint32_t)(rem < kChunkBytes ? rem : kChunkBytes);
-    return reinterpret_cast<const uint8_t*>(p.in) + row * row_bytes + off;
+  // chunk g of this block is part (g mod cpr) of its row (g div cpr); producer and consumers walk the
+  // chunks in order with incremental counters (no 64-bit division per chunk)
+  auto chunk_bytes = [&](int part) {
+    const int64_t rem = row_bytes - (int64_t)part * kChunkBytes;
+    return (uint32_t)(rem < kChunkBytes ? rem : kChunkBytes);
   };
-  auto issue = [&](int64_t g) {
-    uint32_t bytes;
-    const uint8_t* src = chunk_src(g, bytes);
-    const int s = (int)(g % kStages);
+  int64_t prod_row = blockIdx.x;
+  int prod_part = 0, prod_stage = 0;
+  auto issue = [&]() {
+    const uint32_t bytes = chunk_bytes(prod_part);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.in) + prod_row * row_bytes + (int64_t)prod_part * kChunkBytes;
+    const int s = prod_stage;
     const uint32_t b = smem_addr(&bar[s]);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_addr(ring + s * kChunkBytes)), "l"(src), "r"(bytes), "r"(b)
                  : "memory");
+    if (++prod_part == cpr) {
+      prod_part = 0;
+      prod_row += gridDim.x;
+    }
+    prod_stage = prod_stage + 1 == kStages ? 0 : prod_stage + 1;
   };
   if (tid == 0)
-    for (int64_t g = 0; g < kStages && g < n_chunks; ++g) issue(g);
+    for (int64_t g = 0; g < kStages && g < n_chunks; ++g) issue();
   const uint4* bv = reinterpret_cast<const uint4*>(p.chain.bptr);
   const LogTab lt = global_log_tables();
   // BREG: rows of at most two chunks; this thread's slice of the broadcast vector (the same for every
@@ -295,13 +303,14 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
   }
   float acc = identity<KIND>();
   int64_t issued = n_chunks < kStages ? n_chunks : kStages;
+  int cons_part = 0, cons_stage = 0;
+  uint32_t cons_parity = 0;
+  int64_t cons_row = blockIdx.x;
   for (int64_t g = 0; g < n_chunks; ++g) {
-    const int s = (int)(g % kStages);
-    const uint32_t parity = (uint32_t)((g / kStages) & 1);
-    if (!mbar_wait(smem_addr(&bar[s]), parity)) abort_flag = 1;
-    uint32_t bytes;
-    chunk_src(g, bytes);
-    const int64_t part = g % cpr;
+    const int s = cons_stage;
+    if (!mbar_wait(smem_addr(&bar[s]), cons_parity)) abort_flag = 1;
+    const uint32_t bytes = chunk_bytes(cons_part);
+    const int part = cons_part;
     const uint4* xv = reinterpret_cast<const uint4*>(ring + s * kChunkBytes);
     const int nv = (int)(bytes / 16);
     const int64_t vbase = part * (kChunkBytes / 16);  // vector index of the chunk within the row
@@ -332,12 +341,20 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
     }
     __syncthreads();  // every thread is done with stage s
     if (abort_flag) break;
-    if (tid == 0 && issued < n_chunks) issue(issued++);
+    if (tid == 0 && issued < n_chunks) {
+      issue();
+      ++issued;
+    }
     if (part == cpr - 1) {
-      const int64_t row = blockIdx.x + (g / cpr) * (int64_t)gridDim.x;
       acc = block_reduce<KIND>(acc, red);
-      if (tid == 0) store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+      if (tid == 0) store_result(p.out, p.out_dt, map_index(p.omap, cons_row), combine<KIND>(p.init, acc));
       acc = identity<KIND>();
+      cons_row += gridDim.x;
+    }
+    if (++cons_part == cpr) cons_part = 0;
+    if (++cons_stage == kStages) {
+      cons_stage = 0;
+      cons_parity ^= 1u;
     }
   }
   if (abort_flag && tid == 0) {
@@ -626,13 +643,10 @@ __global__ void __launch_bounds__(256) gen_reduce_kernel(GenReducePlan p) {
   if (o >= p.n_out) return;
   const LogTab lt = global_log_tables();
   // decompose o over the kept axes in output physical order
-  int64_t idx[kMaxRank];
-  for (int d = 0; d < kMaxRank; ++d) idx[d] = 0;
   int64_t rem = o, base = 0, bbase = 0;
   for (int j = p.nk - 1; j >= 0; --j) {
     int64_t i = rem % p.kdim_size[j];
     rem /= p.kdim_size[j];
-    idx[p.kdim_logical[j]] = i;
     base += i * p.kdim_in_stride[j];
     bbase += i * p.chain.bstride[p.kdim_logical[j]];
   }
@@ -659,7 +673,6 @@ __global__ void __launch_bounds__(256) gen_reduce_kernel(GenReducePlan p) {
   }
   total = combine_rt(p.kind, total, chunk);
   store_result(p.out, p.out_dt, o, combine_rt(p.kind, p.init, total));
-  (void)idx;
 }
 
 cudaError_t launch_gen_reduce(const GenReducePlan& p, cudaStream_t s) {

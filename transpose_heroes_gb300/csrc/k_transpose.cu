@@ -73,17 +73,19 @@ struct PairShared {
 // spill mask if the list is full, and settled after the barrier.
 template <int CH, bool VEC>
 __device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t n, int64_t TI, int64_t TJ,
-                                          float* dst, int dst_base, const Chain& c, const LogTab& lt,
-                                          PairShared& ps, uint32_t& spill) {
+                                          const int (&toff)[4], float* dst, int dst_base, const Chain& c,
+                                          const LogTab& lt, PairShared& ps, uint32_t& spill) {
   float4 v[4];
+  const float* tile = in + TI * kT * n + TJ * kT;          // element (0, 0) of the tile
+  const bool full = (TI + 1) * kT <= n && (TJ + 1) * kT <= n;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     int r, col;
     pair_slot(k, r, col);
     const int64_t gr = TI * kT + r, gc = TJ * kT + col;
     if (VEC) {
-      if (gr < n && gc < n) {
-        const float4* src = reinterpret_cast<const float4*>(in + gr * n + gc);
+      if (full || (gr < n && gc < n)) {
+        const float4* src = reinterpret_cast<const float4*>(tile + toff[k]);
         asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
                      : "=f"(v[k].x), "=f"(v[k].y), "=f"(v[k].z), "=f"(v[k].w)
                      : "l"(src));
@@ -106,8 +108,12 @@ __device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t 
       bool ok[4];
       cr_logf_first2(v[k].x, v[k].y, ps.l1_inv, ps.l1_hi, ps.l1_lo, y[0], y[1], ok[0], ok[1]);
       cr_logf_first2(v[k].z, v[k].w, ps.l1_inv, ps.l1_hi, ps.l1_lo, y[2], y[3], ok[2], ok[3]);
+      const float* xi = &v[k].x;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) redo |= (ok[q] ? 0u : 1u) << (4 * k + q);
+      for (int q = 0; q < 4; ++q) {
+        redo |= (ok[q] ? 0u : 1u) << (4 * k + q);
+        y[q] = ok[q] ? y[q] : xi[q];  // park the input of an open element in its slot
+      }
     } else {
       const float* xi = &v[k].x;
 #pragma unroll
@@ -148,29 +154,20 @@ __device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t 
 }
 
 // Settles the elements the first pass left open -- the block's list, then this thread's spills --
-// recomputing each from its input, re-read from global memory (slot offset -> tile, row, column).
-__device__ __forceinline__ float pair_input(const float* __restrict__ in, int64_t n, int64_t I, int64_t J, int off) {
-  const bool second = off >= kT * kTP;
-  const int o = second ? off - kT * kTP : off;
-  const int col = o / kTP, r = o % kTP;  // slots hold tile element (r, col) at col * kTP + r
-  const int64_t gr = (second ? J : I) * kT + r, gc = (second ? I : J) * kT + col;
-  return (gr < n && gc < n) ? in[gr * n + gc] : 1.f;
-}
-
-__device__ __forceinline__ void pair_settle(float* tiles, const float* __restrict__ in, int64_t n, int64_t I,
-                                            int64_t J, PairShared& ps, uint32_t spill, const LogTab& lt) {
+// from the input parked in their slot.
+__device__ __forceinline__ void pair_settle(float* tiles, PairShared& ps, uint32_t spill, const LogTab& lt) {
   const int cnt = min(ps.redo_count, kRedoCap);
   for (int j = threadIdx.x; j < cnt; j += kPairThreads) {
-    const int off = ps.redo[j];
-    tiles[off] = cr_logf(pair_input(in, n, I, J, off), lt.c, lt.e);
+    float* slot = tiles + ps.redo[j];
+    *slot = cr_logf(*slot, lt.c, lt.e);
   }
   while (spill) {
     const int e = __ffs(spill) - 1;
     spill &= spill - 1;
     int r, col;
     pair_slot((e & 15) >> 2, r, col);
-    const int off = ((e >= 16) ? kT * kTP : 0) + (col + (e & 3)) * kTP + r;
-    tiles[off] = cr_logf(pair_input(in, n, I, J, off), lt.c, lt.e);
+    float* slot = tiles + ((e >= 16) ? kT * kTP : 0) + (col + (e & 3)) * kTP + r;
+    *slot = cr_logf(*slot, lt.c, lt.e);
   }
 }
 
@@ -179,8 +176,10 @@ __device__ __forceinline__ void pair_settle(float* tiles, const float* __restric
 // the epilogue. Both reads hit 32 distinct banks per warp.
 template <bool VEC>
 __device__ __forceinline__ void pair_store(float* __restrict__ out, int64_t n, int64_t TI, int64_t TJ,
-                                           const float* ownT, const float* otherT, const Chain& epi,
-                                           const LogTab& lt) {
+                                           const int (&toff)[4], const float* ownT, const float* otherT,
+                                           const Chain& epi, const LogTab& lt) {
+  float* tile = out + TI * kT * n + TJ * kT;
+  const bool full = (TI + 1) * kT <= n && (TJ + 1) * kT <= n;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     int r, col;
@@ -200,7 +199,7 @@ __device__ __forceinline__ void pair_store(float* __restrict__ out, int64_t n, i
     }
     const int64_t gr = TI * kT + r, gc = TJ * kT + col;
     if (VEC) {
-      if (gr < n && gc < n) *reinterpret_cast<float4*>(out + gr * n + gc) = v;
+      if (full || (gr < n && gc < n)) *reinterpret_cast<float4*>(tile + toff[k]) = v;
     } else {
       const float* pv = &v.x;
 #pragma unroll
@@ -226,6 +225,13 @@ __global__ void __launch_bounds__(kPairThreads, 4)
   const LogTab lt = {s_lc, s_le};
   const float* in = reinterpret_cast<const float*>(p.in);
   float* out = reinterpret_cast<float*>(p.out);
+  int toff[4];  // this thread's in-tile element offsets (row * n + column); 64 * n < 2^31 always holds
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    int r, col;
+    pair_slot(k, r, col);
+    toff[k] = r * (int)p.n + col;
+  }
   for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
     int64_t I, J;
     if (item < n_off) {
@@ -234,20 +240,20 @@ __global__ void __launch_bounds__(kPairThreads, 4)
       I = J = item - n_off;
     }
     uint32_t spill = 0;
-    pair_load<CH, VEC>(in, p.n, I, J, ta, 0, p.pro, lt, ps, spill);
-    if (I != J) pair_load<CH, VEC>(in, p.n, J, I, tb, kT * kTP, p.pro, lt, ps, spill);
+    pair_load<CH, VEC>(in, p.n, I, J, toff, ta, 0, p.pro, lt, ps, spill);
+    if (I != J) pair_load<CH, VEC>(in, p.n, J, I, toff, tb, kT * kTP, p.pro, lt, ps, spill);
     __syncthreads();
     if (CH == PC_LOG) {
       if (ps.redo_count) {  // uniform: every thread reads the same count after the barrier
-        pair_settle(ta, in, p.n, I, J, ps, spill, lt);
+        pair_settle(ta, ps, spill, lt);
         __syncthreads();
       }
     }
     if (I != J) {
-      pair_store<VEC>(out, p.n, I, J, ta, tb, p.epi, lt);  // out(I,J) = A + B^T
-      pair_store<VEC>(out, p.n, J, I, tb, ta, p.epi, lt);  // out(J,I) = B + A^T
+      pair_store<VEC>(out, p.n, I, J, toff, ta, tb, p.epi, lt);  // out(I,J) = A + B^T
+      pair_store<VEC>(out, p.n, J, I, toff, tb, ta, p.epi, lt);  // out(J,I) = B + A^T
     } else {
-      pair_store<VEC>(out, p.n, I, I, ta, ta, p.epi, lt);
+      pair_store<VEC>(out, p.n, I, I, toff, ta, ta, p.epi, lt);
     }
     if (threadIdx.x == 0) ps.redo_count = 0;  // nobody reads it again before the barrier below
     __syncthreads();
