@@ -235,18 +235,18 @@ def test_bcast_row_reduce_variants():
 
 
 # ---- transposes -----------------------------------------------------------------------------------------
-@pytest.mark.parametrize("n", [1, 2, 63, 64, 65, 130, 257])
+@pytest.mark.parametrize("n", [1, 2, 4, 63, 64, 65, 68, 130, 132, 257, 1028])
 def test_selfadd_log_sizes(n):
     f = inp.transpose_log(seed=n, n=n)
     ref, _ = run_oracle(f)
     check(f, run_gpu(f), ref, None)
 
 
+@pytest.mark.parametrize("n", [192, 196])
 @pytest.mark.parametrize("value", [1.015741229057312, 1.0, 0.5, 2.0 ** -130])
-def test_selfadd_every_element_open(value):
+def test_selfadd_every_element_open(value, n):
     """Inputs whose log the first pass cannot round: the per-block list overflows and the per-thread
     spill path settles the rest (and exactly 1.0 / a subnormal take the special-operand route)."""
-    n = 192
     data = np.full(n * n, value, dtype=np.float32)
     data[::7] = np.float32(1.3)  # a mix of open and settled elements
     f = inp.Fusion(name="open", kind="transpose", dims=[n, n], m2m=[1, 0], dtype="f32", data=data,
@@ -262,9 +262,9 @@ def test_selfadd_every_element_open(value):
     assert np.all(y.cpu().numpy() == np.float32(oracle.log(float(np.float32(value)), "f32")))
 
 
-def test_selfadd_other_forms():
+@pytest.mark.parametrize("n", [70, 72])
+def test_selfadd_other_forms(n):
     g = inp.rng(8)
-    n = 70
     data = inp.uniform_f32(g, n * n, 0.1, 3.0)
     for m2m in ([1, 0], [0, 1]):
         for pro, epi in ((None, None), ({"ops": ["log", "neg"]}, {"ops": ["abs"]})):

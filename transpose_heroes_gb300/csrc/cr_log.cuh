@@ -214,12 +214,14 @@ __device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) { return __f
 // First pass, two elements at a time: 32-interval table (three 32-float arrays, so a warp's lookups
 // hit distinct banks), e*ln2 from exact products:
 //   log x = S + err + rest,  S + err = A + r exactly (Fast2Sum),  A = e*LN2_A + log(c)_hi (exact),
-//   rest = r^2 (-1/2 + r/3 - r^2/4 + r^3/5 - r^4/6 + r^5/7) + (e*LN2_B + log(c)_lo)   in f32.
-// Every error (rest's rounding ~2^-35.3, the lo sum ~2^-36.3, table and LN2_B terms below 2^-36 for
-// all exponents, truncation 2^-48) stays under the absolute bound 2^-33.5. Rounding test: yh is the
-// correctly rounded log when yh + (yl +- 2^-33.5), the error interval's end nearer a boundary, still
-// rounds to yh. About 2% of inputs in [0.5, 2) (most of those near 1) and every special operand are
-// left open (ok = false) for cr_logf.
+//   rest = r^2 (-1/2 + r/3 - r^2/4 + r^3/5 - r^4/6) + (e*LN2_B + log(c)_lo)   in f32.
+// With lo = RN(err + rest), every error (truncation r^7/7 < 2^-42, the roundings of r^2, of the
+// polynomial and of rest ~2^-36.3 each, the table and LN2_B terms below 2^-36 for all exponents, lo's
+// rounding ~2^-36.2) sums to under 2^-33.8, so |log x - (S + lo)| < b = 2^-33.5 with room for the
+// rounding of lo +- b (< 2^-37). Rounding test by monotonicity of round-to-nearest: if S + (lo - b)
+// and S + (lo + b) round to the same float, every value between them, the exact log among them,
+// rounds to it. About 2% of inputs in [0.5, 2) (most of those near 1) and every special operand
+// are left open (ok = false) for cr_logf.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* __restrict__ tinv,
                                                const float* __restrict__ thi, const float* __restrict__ tlo,
@@ -237,22 +239,20 @@ __device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* 
   const float2 A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), f2::pk(thi[i0], thi[i1]));        // exact
   const float2 S = f2::add(A, R);                       // Fast2Sum: A = 0 or |A| >= |r|
   const float2 ERR = f2::sub(R, f2::sub(S, A));
-  float2 P = f2::fma(R, f2::splat(0.14285715f), f2::splat(-0.16666667f));
-  P = f2::fma(R, P, f2::splat(0.2f));
+  float2 P = f2::fma(R, f2::splat(-0.16666667f), f2::splat(0.2f));
   P = f2::fma(R, P, f2::splat(-0.25f));
   P = f2::fma(R, P, f2::splat(0.33333334f));
   P = f2::fma(R, P, f2::splat(-0.5f));
   const float2 B = f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), f2::pk(tlo[i0], tlo[i1]));
   const float2 REST = f2::fma(f2::mul(R, R), P, B);
   const float2 LO = f2::add(ERR, REST);
-  const float2 YH = f2::add(S, LO);
-  const float2 YL = f2::sub(LO, f2::sub(YH, S));
   const float bound = 0x1.6a09e6p-34f;                  // 2^-33.5
-  const float2 T = f2::add(YH, f2::add(YL, f2::pk(copysignf(bound, YL.x), copysignf(bound, YL.y))));
-  y0 = YH.x;
-  y1 = YH.y;
-  ok0 = n0 & (T.x == YH.x);
-  ok1 = n1 & (T.y == YH.y);
+  const float2 YP = f2::add(S, f2::add(LO, f2::splat(bound)));
+  const float2 YM = f2::add(S, f2::sub(LO, f2::splat(bound)));
+  y0 = YP.x;
+  y1 = YP.y;
+  ok0 = n0 & (YP.x == YM.x);
+  ok1 = n1 & (YP.y == YM.y);
 }
 
 // Loads the 32-entry first-pass table into shared memory (three arrays of 32 floats).

@@ -580,6 +580,8 @@ hlo_status hlo_transpose_fusion(const hlo_array* in, const void* in_ptr, const h
       };
       pair = pair && minor_of(*in) == minor_of(*out);
     }
+    // the pair kernels index tile pairs with 31-bit counts: n < 64 * 65536 (far beyond any device's memory)
+    if (pair && in->dims[nonunit[0]] >= (int64_t)64 * 65536) pair = false;
     if (pair) {
       SelfAddPlan p;
       std::memset(&p, 0, sizeof p);

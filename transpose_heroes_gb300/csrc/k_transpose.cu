@@ -26,14 +26,16 @@ constexpr int kPairThreads = 256;
 
 enum PairChain : int { PC_NONE = 0, PC_LOG = 1, PC_RT = 2 };
 
-// Maps a pair index to (I, J), I < J, enumerating row by row (single-precision estimate, then exact
-// integer correction; FP64 is a slow pipe on this part).
+// Maps a pair index to (I, J), I < J, enumerating row by row: a single-precision estimate from the
+// quadratic formula, then exact integer correction. Only 32-bit integer <-> float conversions are used
+// (64-bit ones run on the FP64 pipe, a slow unit on this part); the launcher guarantees that the pair
+// count fits in 31 bits.
 __device__ __forceinline__ void pair_of(int64_t item, int64_t nt, int64_t& I, int64_t& J) {
-  const float b = 2.0f * (float)nt - 1.0f;
-  const float disc = fmaxf(b * b - 8.0f * (float)item, 0.0f);
-  int64_t i = (int64_t)((b - sqrtf(disc)) * 0.5f);
+  const float b = 2.0f * (float)(int)nt - 1.0f;
+  const float disc = fmaxf(b * b - 8.0f * (float)(int)item, 0.0f);
+  int64_t i = (int)((b - sqrtf(disc)) * 0.5f);
   i = i < 0 ? 0 : (i > nt - 2 ? nt - 2 : i);
-  auto start = [nt](int64_t r) { return r * (nt - 1) - r * (r - 1) / 2; };
+  auto start = [nt](int64_t r) { return r * (nt - 1) - ((r * (r - 1)) >> 1); };
   while (i > 0 && start(i) > item) --i;
   while (start(i + 1) <= item) ++i;
   I = i;
@@ -260,6 +262,223 @@ __global__ void __launch_bounds__(kPairThreads, 4)
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Register-blocked pair kernel, for rows that start on 16-byte boundaries (n % 4 == 0, aligned
+// pointers). Thread t owns the 4 x 4 block (bi, bj) = (t / 16, t % 16) of each 64 x 64 tile:
+//   1. it loads its block of tile A = (I,J) and of tile B = (J,I) (four 16-byte loads each; a warp
+//      reads two whole 256-byte tile rows per load), applies the prologue in registers and stores the
+//      blocks to shared memory, 16-byte chunk c of row r at chunk c ^ ((r / 4) % 8) of that row;
+//   2. its warp settles the log elements the first pass left open (a per-warp list, so no block-wide
+//      wait stands between the first pass and the settling);
+//   3. after a barrier it reads its block of A and block (bj, bi) of B, both as four 16-byte reads that
+//      hit 32 distinct banks per quarter-warp, transposes the latter in registers and writes block
+//      (bi, bj) of out(I,J) = A + B^T with four 16-byte stores; then out(J,I) = B + A^T alike.
+// Every element is loaded once, goes through the prologue once, is written to and read from shared
+// memory with one 16-byte access each way, and is stored once.
+// ---------------------------------------------------------------------------------------------
+constexpr int kWarpList = 64;
+struct BlockShared {
+  float l1_inv[32], l1_hi[32], l1_lo[32];
+  uint16_t wlist[kPairThreads / 32][kWarpList];
+};
+
+__device__ __forceinline__ float comp(const float4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ void item_pair(int64_t item, int64_t nt, int64_t n_off, int64_t& I, int64_t& J) {
+  if (item < n_off) {
+    pair_of(item, nt, I, J);
+  } else {
+    I = J = item - n_off;
+  }
+}
+
+// Log of a block's four rows in registers: settled elements take their log, open ones keep their input
+// and set bit 4k+q (+ shift) of `open`.
+__device__ __forceinline__ void block_log(float4 (&v)[4], const BlockShared& bs, uint32_t& open, int shift) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float y[4];
+    bool ok[4];
+    cr_logf_first2(v[k].x, v[k].y, bs.l1_inv, bs.l1_hi, bs.l1_lo, y[0], y[1], ok[0], ok[1]);
+    cr_logf_first2(v[k].z, v[k].w, bs.l1_inv, bs.l1_hi, bs.l1_lo, y[2], y[3], ok[2], ok[3]);
+    v[k].x = ok[0] ? y[0] : v[k].x;
+    v[k].y = ok[1] ? y[1] : v[k].y;
+    v[k].z = ok[2] ? y[2] : v[k].z;
+    v[k].w = ok[3] ? y[3] : v[k].w;
+    open |= ((ok[0] ? 0u : 1u) | (ok[1] ? 0u : 2u) | (ok[2] ? 0u : 4u) | (ok[3] ? 0u : 8u)) << (4 * k + shift);
+  }
+}
+
+// Settles the warp's open elements in shared memory (their slots hold the input): the warp gathers
+// their offsets into its list and each lane takes one; a lane whose elements do not fit settles the
+// rest itself.
+__device__ __forceinline__ void warp_settle(uint32_t open, float* tiles, int own, uint16_t* wl, const LogTab& lt) {
+  const int lane = threadIdx.x & 31;
+  const int cnt = __popc(open);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, 31);
+  if (total == 0) return;  // warp-uniform
+  int pos = incl - cnt;
+  while (open && pos < kWarpList) {
+    const int b = __ffs(open) - 1;
+    open &= open - 1;
+    wl[pos++] = (uint16_t)((b >> 4) * (kT * kT) + own + ((b >> 2) & 3) * kT + (b & 3));
+  }
+  __syncwarp();  // the blocks' stores and the list are visible to the whole warp
+  const int listed = total < kWarpList ? total : kWarpList;
+  for (int j = lane; j < listed; j += 32) {
+    float* s = tiles + wl[j];
+    *s = cr_logf(*s, lt.c, lt.e);
+  }
+  while (open) {
+    const int b = __ffs(open) - 1;
+    open &= open - 1;
+    float* s = tiles + (b >> 4) * (kT * kT) + own + ((b >> 2) & 3) * kT + (b & 3);
+    *s = cr_logf(*s, lt.c, lt.e);
+  }
+}
+
+// Writes block (bi, bj) of an output tile: row k = a[k] + column k of b (b holds the other tile's
+// block (bj, bi) row by row), then the epilogue. `rows` = rows of the tile left from row 4*bi.
+template <bool EPI>
+__device__ __forceinline__ void block_store(float* dst, int64_t n, const float4 (&a)[4], const float4 (&b)[4],
+                                            int64_t rows, bool cols_ok, const Chain& epi, const LogTab& lt) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float4 v;
+    v.x = __fadd_rn(a[k].x, comp(b[0], k));
+    v.y = __fadd_rn(a[k].y, comp(b[1], k));
+    v.z = __fadd_rn(a[k].z, comp(b[2], k));
+    v.w = __fadd_rn(a[k].w, comp(b[3], k));
+    if (EPI) {
+      v.x = apply_chain_rt<false>(epi, v.x, 0, lt);
+      v.y = apply_chain_rt<false>(epi, v.y, 0, lt);
+      v.z = apply_chain_rt<false>(epi, v.z, 0, lt);
+      v.w = apply_chain_rt<false>(epi, v.w, 0, lt);
+    }
+    if (cols_ok && k < rows) *reinterpret_cast<float4*>(dst + k * n) = v;
+  }
+}
+
+template <int CH, bool EPI>
+__global__ void __launch_bounds__(kPairThreads, 4)
+    selfadd_block_kernel(SelfAddPlan p, int64_t nt, int64_t n_off, int64_t n_items) {
+  extern __shared__ float4 smem_f4[];
+  float* ta = reinterpret_cast<float*>(smem_f4);  // tile A, then tile B: 64 x 64 floats each
+  float* tb = ta + kT * kT;
+  float4* s_lc = reinterpret_cast<float4*>(ta + 2 * kT * kT);
+  float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
+  BlockShared& bs = *reinterpret_cast<BlockShared*>(s_le + HLO_LOG_NE);
+  load_log_tables(s_lc, s_le);
+  load_log1_tables(bs.l1_inv, bs.l1_hi, bs.l1_lo);
+  __syncthreads();
+  const LogTab lt = {s_lc, s_le};
+  const float* in = reinterpret_cast<const float*>(p.in);
+  float* out = reinterpret_cast<float*>(p.out);
+  const int64_t n = p.n;
+  const int bi = threadIdx.x >> 4, bj = threadIdx.x & 15;
+  const int own = 4 * bi * kT + ((bj ^ (bi & 7)) << 2);  // row 4*bi, chunk bj (swizzled)
+  const int oth = 4 * bj * kT + ((bi ^ (bj & 7)) << 2);  // row 4*bj, chunk bi (swizzled)
+  const int64_t goff = 4 * bi * n + 4 * bj;
+  uint16_t* wl = bs.wlist[threadIdx.x >> 5];
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    int64_t I, J;
+    item_pair(item, nt, n_off, I, J);
+    const bool two = I != J;
+    // rows of tile A left from this thread's first row (A's columns are B's rows and vice versa);
+    // n % 4 == 0, so a 4-column chunk is wholly inside or outside
+    const int64_t ra = n - I * kT - 4 * bi, rb = n - J * kT - 4 * bi;
+    const bool ca = J * kT + 4 * bj < n, cb = I * kT + 4 * bj < n;
+    const float* pa = in + (I * kT) * n + J * kT + goff;
+    const float* pb = in + (J * kT) * n + I * kT + goff;
+    float4 va[4], vb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      va[k] = make_float4(2.f, 2.f, 2.f, 2.f);
+      vb[k] = va[k];
+      if (ca && k < ra)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(va[k].x), "=f"(va[k].y), "=f"(va[k].z), "=f"(va[k].w)
+                     : "l"(pa + k * n));
+      if (two && cb && k < rb)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(vb[k].x), "=f"(vb[k].y), "=f"(vb[k].z), "=f"(vb[k].w)
+                     : "l"(pb + k * n));
+    }
+    uint32_t open = 0;
+    if (CH == PC_LOG) {
+      block_log(va, bs, open, 0);
+      if (two) block_log(vb, bs, open, 16);
+    } else if (CH == PC_RT) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        va[k].x = pair_pro<CH>(va[k].x, p.pro, lt);
+        va[k].y = pair_pro<CH>(va[k].y, p.pro, lt);
+        va[k].z = pair_pro<CH>(va[k].z, p.pro, lt);
+        va[k].w = pair_pro<CH>(va[k].w, p.pro, lt);
+        vb[k].x = pair_pro<CH>(vb[k].x, p.pro, lt);
+        vb[k].y = pair_pro<CH>(vb[k].y, p.pro, lt);
+        vb[k].z = pair_pro<CH>(vb[k].z, p.pro, lt);
+        vb[k].w = pair_pro<CH>(vb[k].w, p.pro, lt);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      *reinterpret_cast<float4*>(ta + own + k * kT) = va[k];
+      if (two) *reinterpret_cast<float4*>(tb + own + k * kT) = vb[k];
+    }
+    if (CH == PC_LOG) warp_settle(open, ta, own, wl, lt);
+    __syncthreads();
+    {
+      float4 a[4], b[4];
+      const float* other = two ? tb : ta;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[k] = *reinterpret_cast<const float4*>(ta + own + k * kT);
+        b[k] = *reinterpret_cast<const float4*>(other + oth + k * kT);
+      }
+      block_store<EPI>(out + (I * kT) * n + J * kT + goff, n, a, b, ra, ca, p.epi, lt);  // out(I,J) = A + B^T
+    }
+    if (two) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[k] = *reinterpret_cast<const float4*>(tb + own + k * kT);
+        b[k] = *reinterpret_cast<const float4*>(ta + oth + k * kT);
+      }
+      block_store<EPI>(out + (J * kT) * n + I * kT + goff, n, a, b, rb, cb, p.epi, lt);  // out(J,I) = B + A^T
+    }
+    __syncthreads();  // the tiles are rewritten by the next item
+  }
+}
+
+static size_t block_smem_bytes() {
+  return 2 * kT * kT * sizeof(float) + HLO_LOG_NC * sizeof(float4) + HLO_LOG_NE * sizeof(float2) +
+         sizeof(BlockShared);
+}
+
+template <int CH, bool EPI>
+static cudaError_t block_launch(const SelfAddPlan& p, cudaStream_t s) {
+  auto kernel = selfadd_block_kernel<CH, EPI>;
+  const size_t smem = block_smem_bytes();
+  const int nb = kernel_blocks_per_sm((const void*)kernel, kPairThreads, smem);
+  const int64_t nt = (p.n + kT - 1) / kT;
+  const int64_t n_off = nt * (nt - 1) / 2;
+  const int64_t n_items = n_off + nt;
+  int64_t grid = (int64_t)device_sm_count() * nb;
+  if (grid > n_items) grid = n_items;
+  if (grid < 1) grid = 1;
+  kernel<<<(unsigned)grid, kPairThreads, smem, s>>>(p, nt, n_off, n_items);
+  return cudaGetLastError();
+}
+
 static size_t pair_smem_bytes() {
   return HLO_LOG_NC * sizeof(float4) + HLO_LOG_NE * sizeof(float2) + 2 * kT * kTP * sizeof(float) +
          sizeof(PairShared);
@@ -286,6 +505,16 @@ cudaError_t launch_selfadd_transpose(const SelfAddPlan& p, cudaStream_t s) {
   int ch = PC_RT;
   if (p.pro.n == 0) ch = PC_NONE;
   else if (p.pro.n == 1 && p.pro.op[0] == OP_LOG) ch = PC_LOG;
+  if (vec) {  // rows on 16-byte boundaries: the register-blocked kernel
+    if (p.epi.n) {
+      if (ch == PC_LOG) return block_launch<PC_LOG, true>(p, s);
+      if (ch == PC_NONE) return block_launch<PC_NONE, true>(p, s);
+      return block_launch<PC_RT, true>(p, s);
+    }
+    if (ch == PC_LOG) return block_launch<PC_LOG, false>(p, s);
+    if (ch == PC_NONE) return block_launch<PC_NONE, false>(p, s);
+    return block_launch<PC_RT, false>(p, s);
+  }
   if (ch == PC_LOG) return vec ? pair_launch<PC_LOG, true>(p, s) : pair_launch<PC_LOG, false>(p, s);
   if (ch == PC_NONE) return vec ? pair_launch<PC_NONE, true>(p, s) : pair_launch<PC_NONE, false>(p, s);
   return vec ? pair_launch<PC_RT, true>(p, s) : pair_launch<PC_RT, false>(p, s);
