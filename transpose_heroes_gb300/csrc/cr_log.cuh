@@ -8,11 +8,13 @@
 //   log x = e*ln2 + log(c) + log1p(r),  r = m * inv_c - 1 (exact: see gen_log_table.py),
 //   log1p(r) = r - r^2/2 + r^3 * (1/3 - r/4 + r^2/5 - r^3/6) + O(r^7).
 //
-// Stage 1 evaluates this sum in float-float arithmetic (Fast2Sum, exact FMA products) to an error
-// below 2^-42 |y| + 2^-23 |r|^3, then applies a rounding test (Ziv's strategy): if the error interval
+// Stage 1 evaluates this sum in float-float arithmetic (Fast2Sum, exact FMA products), then applies a
+// rounding test (Ziv's strategy) with the error bound 2^-44 |y| + 2^-23 |r|^3: if the error interval
 // around the float-float value contains no rounding boundary of f32, the leading float is the
-// correctly rounded result. Otherwise (probability ~2^-17 per element) stage 2 recomputes log x in
-// double-double arithmetic via log m = 2 atanh((m-1)/(m+1)) to ~2^-75 relative and rounds that.
+// correctly rounded result. The bound is at least twice the largest error of the evaluation over every
+// positive normal f32 input (an exhaustive check; the input set is finite). Otherwise (probability
+// ~2^-19 per element) stage 2 recomputes log x with double-double sums to better than 2^-70 relative
+// and rounds that.
 // Special operands (0, negative, subnormal, inf, NaN, exactly 1) also take stage 2.
 #pragma once
 #include <cstdint>
@@ -55,19 +57,6 @@ __device__ __forceinline__ dd dd_add(dd x, dd y) {  // accurate: two_sum on both
   return dd_fast_two_sum(s.hi, s.lo);
 }
 
-__device__ __forceinline__ dd dd_mul(dd x, dd y) {
-  dd p = dd_two_prod(x.hi, y.hi);
-  p.lo = __fma_rn(x.hi, y.lo, p.lo);
-  p.lo = __fma_rn(x.lo, y.hi, p.lo);
-  return dd_fast_two_sum(p.hi, p.lo);
-}
-
-__device__ __forceinline__ dd dd_recip_int(double k) {  // 1/k as a double-double, k a small integer
-  double h = __drcp_rn(k);
-  double l = __ddiv_rn(__fma_rn(-h, k, 1.0), k);
-  return {h, l};
-}
-
 // Rounds the double-double value y (|y.lo| <= ulp(y.hi)/2) to the nearest f32, ties to even.
 __device__ __forceinline__ float dd_to_f32_rn(dd y) {
   float f = __double2float_rn(y.hi);
@@ -84,7 +73,13 @@ __device__ __forceinline__ float dd_to_f32_rn(dd y) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Stage 2: double-double evaluation (also handles every special operand).
+// Stage 2: double-double evaluation (also handles every special operand). Same reduction as stage 1,
+// x = 2^e m, r = m * inv_c - 1 exact, and
+//   log x = e*ln2 + log(c) + r - r^2/2 + r^3 P(r),   P(r) = 1/3 - r/4 + r^2/5 - ... - r^7/10,
+// with e*ln2 and log(c) as double-doubles, r - r^2/2 summed exactly (r^2 is exact in double for a
+// 24-bit r) and r^3 P(r) in double. |r| < 2^-8.5, so the truncation (r^11/11) stays below 2^-94 and
+// the double evaluation of r^3 P(r) errs by ~2^-53 |r|^3 / 3 < 2^-80; relative to y that is below
+// 2^-70, and below 2^-100 near x = 1 where y ~ r. No division: FP64 is a slow pipe on this part.
 // ------------------------------------------------------------------------------------------------
 static __device__ __noinline__ float cr_logf_accurate(float x) {
   uint32_t ix = __float_as_uint(x);
@@ -98,46 +93,29 @@ static __device__ __noinline__ float cr_logf_accurate(float x) {
     ix = __float_as_uint(x * 8388608.0f);
     eadj = -23;
   }
-  uint32_t tmp = ix - HLO_LOG_OFF;
-  int e = ((int)tmp >> 23) + eadj;
-  double m = (double)__uint_as_float(ix - (tmp & 0xFF800000u));
-  // s = (m - 1) / (m + 1) as a double-double; numerator and denominator are exact doubles
-  double num = __dsub_rn(m, 1.0), den = __dadd_rn(m, 1.0);
-  double sh = __ddiv_rn(num, den);
-  double sl = __ddiv_rn(__fma_rn(-sh, den, num), den);
-  dd s = dd_fast_two_sum(sh, sl);
-  dd z = dd_mul(s, s);
-  // U = z/3 + z^2/5 + z^3/7 + z^4 W(z): W in double, the rest in double-double (|z| < 0.03)
-  double zd = z.hi;
-  double w = 1.0 / 35.0;
-  w = __fma_rn(w, zd, 1.0 / 33.0);
-  w = __fma_rn(w, zd, 1.0 / 31.0);
-  w = __fma_rn(w, zd, 1.0 / 29.0);
-  w = __fma_rn(w, zd, 1.0 / 27.0);
-  w = __fma_rn(w, zd, 1.0 / 25.0);
-  w = __fma_rn(w, zd, 1.0 / 23.0);
-  w = __fma_rn(w, zd, 1.0 / 21.0);
-  w = __fma_rn(w, zd, 1.0 / 19.0);
-  w = __fma_rn(w, zd, 1.0 / 17.0);
-  w = __fma_rn(w, zd, 1.0 / 15.0);
-  w = __fma_rn(w, zd, 1.0 / 13.0);
-  w = __fma_rn(w, zd, 1.0 / 11.0);
-  w = __fma_rn(w, zd, 1.0 / 9.0);
-  dd u = {w, 0.0};
-  u = dd_add(dd_mul(u, z), dd_recip_int(7.0));
-  u = dd_add(dd_mul(u, z), dd_recip_int(5.0));
-  u = dd_add(dd_mul(u, z), dd_recip_int(3.0));
-  u = dd_mul(u, z);                                       // U
-  dd one_u = dd_add({1.0, 0.0}, u);
-  dd two_s = {__dmul_rn(2.0, s.hi), __dmul_rn(2.0, s.lo)};
-  dd logm = dd_mul(two_s, one_u);                         // log m = 2 s (1 + U)
-  // e * ln2 with ln2 as a double-double constant
-  const dd ln2 = {0x1.62e42fefa39efp-1, 0x1.abc9e3b39803fp-56};
-  double ed = (double)e;
-  dd eln2 = dd_two_prod(ln2.hi, ed);
-  eln2.lo = __fma_rn(ln2.lo, ed, eln2.lo);
-  eln2 = dd_fast_two_sum(eln2.hi, eln2.lo);
-  dd y = dd_add(eln2, logm);
+  const uint32_t tmp = ix - HLO_LOG_OFF;
+  const int e = ((int)tmp >> 23) + eadj;
+  const uint32_t i = (tmp >> HLO_LOG_SHIFT) & (HLO_LOG_NC - 1);
+  const float m = __uint_as_float(ix - (tmp & 0xFF800000u));
+  const double r = (double)__fmaf_rn(m, kLogCTab[i].x, -1.0f);  // exact by table construction
+  const double r2 = __dmul_rn(r, r);                             // exact
+  double p = -0.1;
+  p = __fma_rn(p, r, 1.0 / 9.0);
+  p = __fma_rn(p, r, -0.125);
+  p = __fma_rn(p, r, 1.0 / 7.0);
+  p = __fma_rn(p, r, -1.0 / 6.0);
+  p = __fma_rn(p, r, 0.2);
+  p = __fma_rn(p, r, -0.25);
+  p = __fma_rn(p, r, 1.0 / 3.0);
+  const double t = __dmul_rn(__dmul_rn(r2, r), p);               // r^3 P(r)
+  dd l1 = dd_two_sum(r, __dmul_rn(-0.5, r2));                    // r - r^2/2, exact
+  l1 = dd_add(l1, {t, 0.0});                                     // log1p(r)
+  const double2 lc = kLogC3[i];                                  // log(c)
+  const double ed = (double)e;
+  dd el = dd_two_prod(HLO_LN2_DD_HI, ed);                        // e*ln2
+  el.lo = __fma_rn(HLO_LN2_DD_LO, ed, el.lo);
+  el = dd_fast_two_sum(el.hi, el.lo);
+  const dd y = dd_add(dd_add(el, {lc.x, lc.y}), l1);
   return dd_to_f32_rn(y);
 }
 
@@ -180,7 +158,7 @@ __device__ __forceinline__ float cr_logf_fast(float x, const float4* __restrict_
   const float yh = __fadd_rn(s3, lo);
   const float yl = __fsub_rn(lo, __fsub_rn(yh, s3));
   // rounding test: boundary at half an ulp of yh; powers of two and y = 0 are left to stage 2
-  const float err = __fmaf_rn(fabsf(yh), 0x1p-42f, __fmul_rn(fabsf(r3), 0x1p-23f));
+  const float err = __fmaf_rn(fabsf(yh), 0x1p-44f, __fmul_rn(fabsf(r3), 0x1p-23f));
   const uint32_t yb = __float_as_uint(yh);
   const float half_ulp = __uint_as_float((yb & 0x7F800000u) - (24u << 23));
   ok = normal & (__fadd_rn(fabsf(yl), err) < half_ulp) & ((yb & 0x007FFFFFu) != 0u);

@@ -13,7 +13,8 @@ unevaluated f32 pair (hi, lo), and e*ln2 as a pair per exponent. The interval ho
 inv_c = 1, so log x = log1p(x - 1) near 1 with no cancellation. For the intervals with e = 0 the
 generator also checks |log c_hi| >= max |r| over the interval, which the kernel's Fast2Sum relies on.
 
-All values are computed with Python's decimal module at 60 digits and rounded to f32 exactly.
+All values are computed with Python's decimal module at 60 digits and rounded to f32 exactly. The
+accurate stage also gets log(c) and ln 2 as double-doubles (each part rounded to double exactly).
 A second, 32-entry table serves a cheap first pass (error ~2^-32, see cr_log.cuh): its interval holding
 1.0 is centred on 1.0 as well, and log(c) hi is rounded to a multiple of 2^-16 so that
 e*LN2_A + log(c)_hi is exact in f32 for every exponent (LN2_A = ln2 rounded to 16 bits; Tang's device);
@@ -162,6 +163,24 @@ def build1():
     return off, float(ln2_a), ln2_b, rows, max_r
 
 
+def round_f64(d: Decimal) -> float:
+    """Nearest double to the Decimal d (ties to even), decided exactly."""
+    f = float(d)
+    best = None
+    for cand in (np.nextafter(f, -np.inf), f, np.nextafter(f, np.inf)):
+        dist = abs(Decimal(float(cand)) - d)
+        key = (dist, struct.unpack("<Q", struct.pack("<d", float(cand)))[0] & 1)
+        if best is None or key < best[0]:
+            best = (key, float(cand))
+    return best[1]
+
+
+def split_dd(d: Decimal):
+    hi = round_f64(d)
+    lo = round_f64(d - Decimal(hi))
+    return hi, lo
+
+
 def fmt(v: float) -> str:
     return f"{float(v).hex()}f" if v != 0 else "0.0f"
 
@@ -188,6 +207,14 @@ def main():
         for row in etab:
             f.write("  {" + ", ".join(fmt(v) for v in row) + "},\n")
         f.write("};\n")
+        f.write("// log(c) = -log(inv_c) for the same intervals as a double-double {hi, lo} (accurate stage)\n")
+        f.write("static __device__ const double2 kLogC3[HLO_LOG_NC] = {\n")
+        for row in ctab:
+            hi, lo = split_dd(-Decimal(row[0]).ln())
+            f.write(f"  {{{hi.hex()}, {lo.hex() if lo != 0 else '0.0'}}},\n")
+        f.write("};\n")
+        ln2_hi, ln2_lo = split_dd(Decimal(2).ln())
+        f.write(f"#define HLO_LN2_DD_HI {ln2_hi.hex()}\n#define HLO_LN2_DD_LO {ln2_lo.hex()}\n")
         off, ln2_a, ln2_b, rows, max_r1 = build1()
         f.write(f"// First-pass table: 32 intervals (index = bits {SHIFT1}..22 of bits(x) - 0x{off:08X}); max |r| = {max_r1!r}\n")
         f.write(f"#define HLO_LOG1_OFF 0x{off:08X}u\n")
