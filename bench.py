@@ -44,8 +44,8 @@ WORKLOAD = ("HLO hero fusions, one launch each per step: row_reduce_exp f32[256,
             "quant_relayout s8[4096,4096]{1,0}->{0,1}")
 L2_NOTE = "L2 flushed by a 256 MiB device write before every timed step (outside the timed interval)"
 # kernel each fusion launches (for the launch list / roofline)
-KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_pair_kernel",
-           "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_reduce_kernel",
+KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_block_kernel",
+           "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",
            "quant_relayout": "quant_tile_kernel"}
 
 

@@ -296,13 +296,14 @@ __device__ __forceinline__ void item_pair(int64_t item, int64_t nt, int64_t n_of
 
 // Log of a block's four rows in registers: settled elements take their log, open ones keep their input
 // and set bit 4k+q (+ shift) of `open`.
-__device__ __forceinline__ void block_log(float4 (&v)[4], const BlockShared& bs, uint32_t& open, int shift) {
+__device__ __forceinline__ void block_log(float4 (&v)[4], const float* tinv, const float* thi, const float* tlo,
+                                          uint32_t& open, int shift) {
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     float y[4];
     bool ok[4];
-    cr_logf_first2(v[k].x, v[k].y, bs.l1_inv, bs.l1_hi, bs.l1_lo, y[0], y[1], ok[0], ok[1]);
-    cr_logf_first2(v[k].z, v[k].w, bs.l1_inv, bs.l1_hi, bs.l1_lo, y[2], y[3], ok[2], ok[3]);
+    cr_logf_first2(v[k].x, v[k].y, tinv, thi, tlo, y[0], y[1], ok[0], ok[1]);
+    cr_logf_first2(v[k].z, v[k].w, tinv, thi, tlo, y[2], y[3], ok[2], ok[3]);
     v[k].x = ok[0] ? y[0] : v[k].x;
     v[k].y = ok[1] ? y[1] : v[k].y;
     v[k].z = ok[2] ? y[2] : v[k].z;
@@ -414,8 +415,8 @@ __global__ void __launch_bounds__(kPairThreads, 4)
     }
     uint32_t open = 0;
     if (CH == PC_LOG) {
-      block_log(va, bs, open, 0);
-      if (two) block_log(vb, bs, open, 16);
+      block_log(va, bs.l1_inv, bs.l1_hi, bs.l1_lo, open, 0);
+      if (two) block_log(vb, bs.l1_inv, bs.l1_hi, bs.l1_lo, open, 16);
     } else if (CH == PC_RT) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
