@@ -73,14 +73,42 @@ __device__ __forceinline__ float dd_to_f32_rn(dd y) {
 }
 
 // ------------------------------------------------------------------------------------------------
-// Stage 2: double-double evaluation (also handles every special operand). Same reduction as stage 1,
+// Stage 2 (inputs stage 1 cannot round, and every special operand). Same reduction as stage 1,
 // x = 2^e m, r = m * inv_c - 1 exact, and
 //   log x = e*ln2 + log(c) + r - r^2/2 + r^3 P(r),   P(r) = 1/3 - r/4 + r^2/5 - ... - r^7/10,
-// with e*ln2 and log(c) as double-doubles, r - r^2/2 summed exactly (r^2 is exact in double for a
-// 24-bit r) and r^3 P(r) in double. |r| < 2^-8.5, so the truncation (r^11/11) stays below 2^-94 and
-// the double evaluation of r^3 P(r) errs by ~2^-53 |r|^3 / 3 < 2^-80; relative to y that is below
-// 2^-70, and below 2^-100 near x = 1 where y ~ r. No division: FP64 is a slow pipe on this part.
+// |r| < 2^-8.5, so the truncation (r^11/11) stays below 2^-94. FP64 is a slow pipe on this part (one
+// warp instruction per 64 cycles), so the common case takes ~30 double operations:
+//   A = e*LN2_HI + LOGC_HI is exact (ln 2 on the 2^-44 grid, log(c) on the 2^-45 grid, |e*ln2| < 2^7);
+//   S + E = A + r exactly (Fast2Sum: A = 0 or |A| > |r|);
+//   M = -r^2/2 + r^3 P(r) + e*LN2_LO + LOGC_LO in double (error < 2^-70.9 absolute, and relative to r^2
+//   when A = 0); yh + yl = S + (E + M) exactly.
+// The total error is below 2^-61.5 |y|; when no f32 rounding boundary lies within 2^-60 |y| of
+// yh + yl, the nearer float is the answer. Otherwise (about 2^-16 of these calls) the double-double
+// evaluation below, accurate to better than 2^-100, decides.
 // ------------------------------------------------------------------------------------------------
+static __device__ __noinline__ float cr_logf_dd(int e, double r, int i) {
+  const double r2 = __dmul_rn(r, r);                             // exact
+  double p = -0.1;
+  p = __fma_rn(p, r, 1.0 / 9.0);
+  p = __fma_rn(p, r, -0.125);
+  p = __fma_rn(p, r, 1.0 / 7.0);
+  p = __fma_rn(p, r, -1.0 / 6.0);
+  p = __fma_rn(p, r, 0.2);
+  p = __fma_rn(p, r, -0.25);
+  p = __fma_rn(p, r, 1.0 / 3.0);
+  const double t = __dmul_rn(__dmul_rn(r2, r), p);               // r^3 P(r)
+  dd l1 = dd_two_sum(r, __dmul_rn(-0.5, r2));                    // r - r^2/2, exact
+  l1 = dd_add(l1, {t, 0.0});                                     // log1p(r)
+  const double2 lct = kLogC3[i];
+  const dd lc = dd_fast_two_sum(lct.x, lct.y);                   // log(c), normalised
+  const double ed = (double)e;
+  dd el = dd_two_prod(HLO_LN2_DD_HI, ed);                        // e*ln2
+  el.lo = __fma_rn(HLO_LN2_DD_LO, ed, el.lo);
+  el = dd_fast_two_sum(el.hi, el.lo);
+  const dd y = dd_add(dd_add(el, lc), l1);
+  return dd_to_f32_rn(y);
+}
+
 static __device__ __noinline__ float cr_logf_accurate(float x) {
   uint32_t ix = __float_as_uint(x);
   if (x != x) return x;                                   // NaN stays NaN
@@ -95,7 +123,7 @@ static __device__ __noinline__ float cr_logf_accurate(float x) {
   }
   const uint32_t tmp = ix - HLO_LOG_OFF;
   const int e = ((int)tmp >> 23) + eadj;
-  const uint32_t i = (tmp >> HLO_LOG_SHIFT) & (HLO_LOG_NC - 1);
+  const int i = (int)((tmp >> HLO_LOG_SHIFT) & (HLO_LOG_NC - 1));
   const float m = __uint_as_float(ix - (tmp & 0xFF800000u));
   const double r = (double)__fmaf_rn(m, kLogCTab[i].x, -1.0f);  // exact by table construction
   const double r2 = __dmul_rn(r, r);                             // exact
@@ -108,15 +136,27 @@ static __device__ __noinline__ float cr_logf_accurate(float x) {
   p = __fma_rn(p, r, -0.25);
   p = __fma_rn(p, r, 1.0 / 3.0);
   const double t = __dmul_rn(__dmul_rn(r2, r), p);               // r^3 P(r)
-  dd l1 = dd_two_sum(r, __dmul_rn(-0.5, r2));                    // r - r^2/2, exact
-  l1 = dd_add(l1, {t, 0.0});                                     // log1p(r)
-  const double2 lc = kLogC3[i];                                  // log(c)
+  const double2 lc = kLogC3[i];
   const double ed = (double)e;
-  dd el = dd_two_prod(HLO_LN2_DD_HI, ed);                        // e*ln2
-  el.lo = __fma_rn(HLO_LN2_DD_LO, ed, el.lo);
-  el = dd_fast_two_sum(el.hi, el.lo);
-  const dd y = dd_add(dd_add(el, {lc.x, lc.y}), l1);
-  return dd_to_f32_rn(y);
+  const double A = __fma_rn(ed, HLO_LN2_DD_HI, lc.x);            // exact
+  const double S = __dadd_rn(A, r);
+  const double E = __dsub_rn(r, __dsub_rn(S, A));
+  const double M = __fma_rn(-0.5, r2, __dadd_rn(t, __fma_rn(ed, HLO_LN2_DD_LO, lc.y)));
+  const double L = __dadd_rn(E, M);
+  const double yh = __dadd_rn(S, L);
+  const double yl = __dsub_rn(L, __dsub_rn(yh, S));
+  // f = nearest float to yh; d = (yh + yl) - f; h = half the gap from f to its neighbour towards d
+  const float f = __double2float_rn(yh);
+  const double d = __dadd_rn(__dsub_rn(yh, (double)f), yl);
+  if (d == 0.0) return f;
+  const uint32_t fb = __float_as_uint(f);
+  const float nb = __uint_as_float((d > 0.0) == (f > 0.0f) ? fb + 1u : fb - 1u);
+  const double h = __dmul_rn(__dsub_rn((double)nb, (double)f), 0.5);
+  const double margin = __dmul_rn(fabs(yh), 0x1p-60);
+  const double ad = fabs(d), ah = fabs(h);
+  if (ad < __dsub_rn(ah, margin)) return f;
+  if (ad > __dadd_rn(ah, margin)) return nb;
+  return cr_logf_dd(e, r, i);
 }
 
 // ------------------------------------------------------------------------------------------------

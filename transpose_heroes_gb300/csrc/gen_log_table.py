@@ -207,14 +207,23 @@ def main():
         for row in etab:
             f.write("  {" + ", ".join(fmt(v) for v in row) + "},\n")
         f.write("};\n")
-        f.write("// log(c) = -log(inv_c) for the same intervals as a double-double {hi, lo} (accurate stage)\n")
+        # accurate stage: log(c) = hi + lo with hi on the 2^-45 grid, ln 2 = hi + lo with hi on the 2^-44
+        # grid, so that e*LN2_HI + LOGC_HI is exact in double for every |e| <= 149 (a multiple of 2^-45
+        # below 2^7: 52 bits)
+        f.write("// log(c) = -log(inv_c) as {hi on the 2^-45 grid, lo = RN(log(c) - hi)} (accurate stage)\n")
         f.write("static __device__ const double2 kLogC3[HLO_LOG_NC] = {\n")
         for row in ctab:
-            hi, lo = split_dd(-Decimal(row[0]).ln())
-            f.write(f"  {{{hi.hex()}, {lo.hex() if lo != 0 else '0.0'}}},\n")
+            logc = -Decimal(row[0]).ln()
+            hi = Decimal(round(logc * 2 ** 45)) / 2 ** 45
+            assert float(hi) == hi
+            lo = round_f64(logc - hi)
+            f.write(f"  {{{float(hi).hex()}, {lo.hex() if lo != 0 else '0.0'}}},\n")
         f.write("};\n")
-        ln2_hi, ln2_lo = split_dd(Decimal(2).ln())
-        f.write(f"#define HLO_LN2_DD_HI {ln2_hi.hex()}\n#define HLO_LN2_DD_LO {ln2_lo.hex()}\n")
+        ln2 = Decimal(2).ln()
+        ln2_hi = Decimal(round(ln2 * 2 ** 44)) / 2 ** 44
+        assert float(ln2_hi) == ln2_hi
+        ln2_lo = round_f64(ln2 - ln2_hi)
+        f.write(f"#define HLO_LN2_DD_HI {float(ln2_hi).hex()}\n#define HLO_LN2_DD_LO {ln2_lo.hex()}\n")
         off, ln2_a, ln2_b, rows, max_r1 = build1()
         f.write(f"// First-pass table: 32 intervals (index = bits {SHIFT1}..22 of bits(x) - 0x{off:08X}); max |r| = {max_r1!r}\n")
         f.write(f"#define HLO_LOG1_OFF 0x{off:08X}u\n")
