@@ -638,12 +638,13 @@ __device__ __forceinline__ int quant_code(float real, float scale, float inv, in
 
 constexpr int kQT = 128;  // tile edge in bytes
 
-struct QuantSmem {
+struct __align__(16) QuantSmem {
   float sin_[kQT];   // input scale per tile row (axis 0) or column (axis 1)
   int zin[kQT];
   float sout[kQT];   // output scale per tile row or column
   float inv[kQT];    // RN(1 / output scale)
   int zout[kQT];
+  int zinm[kQT];     // kMagicBits - input zero point: code + zinm = bits of (1.5*2^23 + code - zp)
 };
 
 // Ragged or unaligned tile, byte by byte (kept out of line: it is rare and large).
@@ -676,31 +677,6 @@ __device__ __noinline__ void quant_tile_ragged(const QuantTilePlan& p, int64_t i
   }
 }
 
-// Two codes at a time: dequantize, optional float chain, then the fast path of quant_code with
-// float2 arithmetic. okmask bit 0/1 is cleared when the exact definition must decide that lane.
-template <bool OPS>
-__device__ __forceinline__ void quant_pair(int c0, int c1, float2 sin, int2 zin, float2 inv, int2 zout, int smin,
-                                           int smax, const QuantTilePlan& p, int& q0, int& q1, uint32_t& okmask) {
-  const float2 magic = make_float2(kMagic, kMagic);
-  const float2 df = __fadd2_rn(make_float2(__int_as_float(kMagicBits + c0 - zin.x), __int_as_float(kMagicBits + c1 - zin.y)),
-                               make_float2(-kMagic, -kMagic));  // exact q - zero_point
-  float2 real = __fmul2_rn(sin, df);
-  if (OPS) {
-    real.x = apply_chain_rt<false>(p.ops, real.x, 0, global_log_tables());
-    real.y = apply_chain_rt<false>(p.ops, real.y, 0, global_log_tables());
-  }
-  const float2 y = __fmul2_rn(real, inv);
-  const float2 t = __fadd2_rn(y, magic);
-  const float2 f = __fadd2_rn(y, __fadd2_rn(make_float2(-t.x, -t.y), magic));  // y - rint(y)
-  const float2 g = __fadd2_rn(make_float2(fabsf(f.x), fabsf(f.y)), make_float2(-0.5f, -0.5f));
-  const float2 lim = __fmul2_rn(make_float2(fabsf(y.x), fabsf(y.y)), make_float2(0x1p-22f, 0x1p-22f));
-  const bool ok0 = (fabsf(y.x) < 4194304.0f) & (fabsf(g.x) > lim.x);
-  const bool ok1 = (fabsf(y.y) < 4194304.0f) & (fabsf(g.y) > lim.y);
-  q0 = min(max((__float_as_int(t.x) - kMagicBits) + zout.x, smin), smax);
-  q1 = min(max((__float_as_int(t.y) - kMagicBits) + zout.y, smin), smax);
-  okmask = (ok0 ? 1u : 0u) | (ok1 ? 2u : 0u);
-}
-
 template <int QIN, int QOUT, bool OPS>
 __device__ __forceinline__ void quant_params(int row, int jl, const QuantTilePlan& p, const QuantSmem& q, float& sin,
                                              int& zin, float& sout, float& inv, int& zout) {
@@ -711,58 +687,119 @@ __device__ __forceinline__ void quant_params(int row, int jl, const QuantTilePla
   zout = QOUT == 0 ? q.zout[row] : QOUT == 1 ? q.zout[jl] : p.qout.zp;
 }
 
-// 16 codes of one tile row (local row `row`, local columns 16c .. 16c+15) -> 16 output codes. The
-// fast path runs for all 16 (two per float2 instruction); the rare ones it cannot decide are
-// recomputed exactly afterwards.
+// Dequantize -> [float chain] -> quantize for two codes with float2 arithmetic. The fast path of
+// quant_code: y = real * RN(1/scale) is within 2^-22 |y| of the IEEE quotient, so both round to the
+// same integer when 0.5 - |y - rint(y)| > 2^-22 |y|. With f = y - rint(y), 0.5 - |f| >= 1/4 - f^2 and
+// 2^-22 |y| <= 2^-31 y^2 + 2^-15 (|y| <= (y^2/a + a)/2 with a = 2^8), so it suffices that
+// f^2 + 2^-31 y^2 < 1/4 - 2^-15 - 2^-24 (the last term absorbs the roundings of the test). NaN,
+// infinities and |y| >= 2^14.5 fail the test as well. Lanes that fail are settled exactly later.
+template <bool OPS>
+__device__ __forceinline__ void quant_two(int c0, int c1, float2 sin, int zm0, int zm1, float2 inv, int zo0, int zo1,
+                                          int smin, int smax, const QuantTilePlan& p, int& q0, int& q1, bool& ok0,
+                                          bool& ok1) {
+  const float2 magic = make_float2(kMagic, kMagic);
+  const float2 df = __fadd2_rn(make_float2(__int_as_float(c0 + zm0), __int_as_float(c1 + zm1)),
+                               make_float2(-kMagic, -kMagic));  // exact code - zero point
+  float2 real = __fmul2_rn(sin, df);
+  if (OPS) {
+    real.x = apply_chain_rt<false>(p.ops, real.x, 0, global_log_tables());
+    real.y = apply_chain_rt<false>(p.ops, real.y, 0, global_log_tables());
+  }
+  const float2 y = __fmul2_rn(real, inv);
+  const float2 t = __fadd2_rn(y, magic);
+  const float2 f = __ffma2_rn(__fadd2_rn(t, make_float2(-kMagic, -kMagic)), make_float2(-1.0f, -1.0f), y);
+  const float2 yy = __fmul2_rn(y, __fmul2_rn(y, make_float2(0x1p-31f, 0x1p-31f)));
+  const float2 lhs = __ffma2_rn(f, f, yy);
+  constexpr float kLim = 0.25f - 0x1p-15f - 0x1p-24f;  // exact in f32
+  ok0 = lhs.x < kLim;
+  ok1 = lhs.y < kLim;
+  q0 = min(max((__float_as_int(t.x) - kMagicBits) + zo0, smin), smax);
+  q1 = min(max((__float_as_int(t.y) - kMagicBits) + zo1, smin), smax);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
+  return m == 0 ? v.x : (m == 1 ? v.y : (m == 2 ? v.z : v.w));
+}
+
+// Four 16-byte row chunks (tile rows r0 + 32k, k = 0..3; local columns 16c .. 16c+15) -> their output
+// codes, in place. Column parameters are loaded once for the four rows, row parameters once per row.
 template <int QIN, int QOUT, bool OPS>
-__device__ __forceinline__ uint4 quant_chunk(uint4 x, int row, int c, const QuantTilePlan& p, const QuantSmem& q) {
-  const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-  uint32_t o[4];
-  uint32_t redo = 0;
+__device__ __forceinline__ void quant_rows(uint4 (&v)[4], int r0, int c, const QuantTilePlan& p, const QuantSmem& q) {
+  float rs[4], ri[4];
+  int rzm[4], rzo[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int row = r0 + 32 * k;
+    rs[k] = QIN == 0 ? q.sin_[row] : p.qin.scale;
+    rzm[k] = QIN == 0 ? q.zinm[row] : kMagicBits - p.qin.zp;
+    ri[k] = QOUT == 0 ? q.inv[row] : p.qout.inv_scale;
+    rzo[k] = QOUT == 0 ? q.zout[row] : p.qout.zp;
+  }
+  const int smin = p.qout.smin, smax = p.qout.smax;
+  uint32_t o[4][4];
+  uint32_t redo[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    uint32_t packed = 0;
+    int r[4][4];
 #pragma unroll
     for (int b = 0; b < 4; b += 2) {
       const int jl = 16 * c + 4 * m + b;
-      const int c0 = (int)(int8_t)(w[m] >> (8 * b)), c1 = (int)(int8_t)(w[m] >> (8 * b + 8));
-      float s0, s1, so0, so1, i0, i1;
-      int z0, z1, zo0, zo1;
-      quant_params<QIN, QOUT, OPS>(row, jl, p, q, s0, z0, so0, i0, zo0);
-      quant_params<QIN, QOUT, OPS>(row, jl + 1, p, q, s1, z1, so1, i1, zo1);
-      int r0, r1;
-      uint32_t okm;
-      quant_pair<OPS>(c0, c1, make_float2(s0, s1), make_int2(z0, z1), make_float2(i0, i1), make_int2(zo0, zo1),
-                      p.qout.smin, p.qout.smax, p, r0, r1, okm);
-      redo |= ((~okm) & 3u) << (4 * m + b);
-      packed |= (((uint32_t)r0 & 0xFFu) << (8 * b)) | (((uint32_t)r1 & 0xFFu) << (8 * b + 8));
+      float2 cs = make_float2(0.f, 0.f), ci = make_float2(0.f, 0.f);
+      int czm0 = 0, czm1 = 0, czo0 = 0, czo1 = 0;
+      if (QIN == 1) {
+        cs = *reinterpret_cast<const float2*>(&q.sin_[jl]);
+        czm0 = q.zinm[jl];
+        czm1 = q.zinm[jl + 1];
+      }
+      if (QOUT == 1) {
+        ci = *reinterpret_cast<const float2*>(&q.inv[jl]);
+        czo0 = q.zout[jl];
+        czo1 = q.zout[jl + 1];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w = word_of(v[k], m);
+        const int c0 = (int)(int8_t)(w >> (8 * b)), c1 = (int)(int8_t)(w >> (8 * b + 8));
+        const float2 s2 = QIN == 1 ? cs : make_float2(rs[k], rs[k]);
+        const float2 i2 = QOUT == 1 ? ci : make_float2(ri[k], ri[k]);
+        bool ok0, ok1;
+        quant_two<OPS>(c0, c1, s2, QIN == 1 ? czm0 : rzm[k], QIN == 1 ? czm1 : rzm[k], i2,
+                       QOUT == 1 ? czo0 : rzo[k], QOUT == 1 ? czo1 : rzo[k], smin, smax, p, r[k][b], r[k][b + 1],
+                       ok0, ok1);
+        redo[k] |= ((ok0 ? 0u : 1u) | (ok1 ? 0u : 2u)) << (4 * m + b);
+      }
     }
-    o[m] = packed;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      o[k][m] = __byte_perm(__byte_perm(r[k][0], r[k][1], 0x0040), __byte_perm(r[k][2], r[k][3], 0x0040), 0x5410);
   }
-  if (redo) {
-    uint4 res = make_uint4(o[0], o[1], o[2], o[3]);
-    uint32_t* ro = reinterpret_cast<uint32_t*>(&res);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t rk = redo[k];
+    const int row = r0 + 32 * k;
 #pragma unroll 1
-    for (int e = 0; e < 16; ++e) {
-      if (!((redo >> e) & 1u)) continue;
+    while (rk) {  // rare: the exact definition decides
+      const int e = __ffs(rk) - 1;
+      rk &= rk - 1;
       const int m = e >> 2, b = e & 3, jl = 16 * c + e;
-      const uint32_t word = m == 0 ? x.x : m == 1 ? x.y : m == 2 ? x.z : x.w;
-      const int code = (int)(int8_t)(word >> (8 * b));
+      const int code = (int)(int8_t)(word_of(v[k], m) >> (8 * b));
       float sin, sout, inv;
       int zin, zout;
       quant_params<QIN, QOUT, OPS>(row, jl, p, q, sin, zin, sout, inv, zout);
       float real = dequant(code, sin, zin);
       if (OPS) real = apply_chain_rt<false>(p.ops, real, 0, global_log_tables());
-      const int r = quant_code_exact(real, sout, zout, p.qout.smin, p.qout.smax);
-      ro[m] = (ro[m] & ~(0xFFu << (8 * b))) | (((uint32_t)r & 0xFFu) << (8 * b));
+      const int res = quant_code_exact(real, sout, zout, smin, smax);
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm)  // static indices keep o in registers
+        if (mm == m) o[k][mm] = (o[k][mm] & ~(0xFFu << (8 * b))) | (((uint32_t)res & 0xFFu) << (8 * b));
     }
-    return res;
   }
-  return make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
 }
 
 template <int QIN, int QOUT, bool OPS>
-__global__ void __launch_bounds__(256, 3) quant_tile_kernel(QuantTilePlan p, int64_t ntj) {
+__global__ void __launch_bounds__(256, 4) quant_tile_kernel(QuantTilePlan p, int64_t ntj) {
   __shared__ __align__(16) uint32_t tile[kQT * kQT / 4];  // 128 rows x 32 words, word column swizzled
   __shared__ QuantSmem q;
   const int t = threadIdx.x;
@@ -774,6 +811,7 @@ __global__ void __launch_bounds__(256, 3) quant_tile_kernel(QuantTilePlan p, int
     const int64_t i = i0 + t, j = j0 + t;
     if (p.qin.axis == 0 && i < n0) { q.sin_[t] = p.qin.scales[i]; q.zin[t] = p.qin.zps[i]; }
     if (p.qin.axis == 1 && j < n1) { q.sin_[t] = p.qin.scales[j]; q.zin[t] = p.qin.zps[j]; }
+    if (p.qin.axis >= 0 && (p.qin.axis == 0 ? i < n0 : j < n1)) q.zinm[t] = kMagicBits - q.zin[t];
     const int64_t k = p.qout.axis == 0 ? i : j;
     if (p.qout.axis >= 0 && k < (p.qout.axis == 0 ? n0 : n1)) {
       const float s = p.qout.scales[k];
@@ -799,12 +837,12 @@ __global__ void __launch_bounds__(256, 3) quant_tile_kernel(QuantTilePlan p, int
                  : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
                  : "l"(src));
   }
+  quant_rows<QIN, QOUT, OPS>(v, t >> 3, t & 7, p, q);  // rows t/8 + 32k, chunk t%8
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int qd = t + 256 * k, row = qd >> 3, c = qd & 7;
-    const uint4 o = quant_chunk<QIN, QOUT, OPS>(v[k], row, c, p, q);
     const int wc = 4 * (c ^ ((row >> 4) & 7));
-    *reinterpret_cast<uint4*>(&tile[row * 32 + wc]) = o;
+    *reinterpret_cast<uint4*>(&tile[row * 32 + wc]) = v[k];
   }
   __syncthreads();
   // unit: word column jg (output rows 4jg..4jg+3), 16-row chunk ic
