@@ -170,13 +170,19 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_kernel(RowReducePlan p
 }
 
 // ---- streaming row reduce (bulk asynchronous copies into a shared-memory ring) --------------------
-// Rows are cut into chunks of up to kChunkBytes. Thread 0 keeps kStages chunks in flight with 1-D bulk
-// copies (cp.async.bulk, completion counted on one mbarrier per stage); all threads consume a chunk
-// from shared memory with 16-byte reads, then a barrier frees its stage for the next copy. Bytes in
-// flight therefore do not depend on registers: up to kStages * kChunkBytes per block.
+// Rows are cut into chunks of up to kChunkBytes, kept in flight kStages at a time with 1-D bulk copies
+// (cp.async.bulk, completion counted on one mbarrier per stage). Every warp consumes its share of a
+// chunk from shared memory with 16-byte reads and then releases the stage on a shared counter; the
+// warp whose release completes the count issues the copy of the chunk kStages ahead into that stage.
+// At the end of a row each warp leaves its partial in a slot, and the warp that completes the slot
+// combines the partials in warp order and stores the row. So no block-wide barrier stands in the
+// stream: warps drift apart by at most kStages chunks. Bytes in flight do not depend on registers:
+// up to kStages * kChunkBytes per block.
 constexpr int kStreamThreads = 256;
+constexpr int kStreamWarps = kStreamThreads / 32;
 constexpr int kChunkBytes = 16384;
 constexpr int kStages = 3;
+constexpr int kRowSlots = 8;  // > the rows kStages chunks can span, so a slot is free when reused
 constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: far beyond any legitimate wait
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -229,12 +235,16 @@ __device__ __forceinline__ float2 row_vec2_add(uint4 x, uint4 b, float2 acc) {
                                : make_float2(f16_bits_to_f32((uint16_t)(w[i] & 0xFFFFu)),
                                              f16_bits_to_f32((uint16_t)(w[i] >> 16)));
       if (CH == RC_EXP_BCAST_BF16) {
-        // bf16(exp(x)), then the bf16 add with the broadcast pair rounded once (add.rn.bf16x2)
+        // bf16(exp(x)), then the bf16 add with the broadcast pair rounded once (add.rn.bf16x2), then
+        // each bf16 sum added to its f32 partial in one instruction (the bf16 -> f32 widening is exact)
         const float2 t = __fmul2_rn(v, l2e);
         uint32_t e2, s2;
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(e2) : "f"(ex2_approx(t.y)), "f"(ex2_approx(t.x)));
         asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(s2) : "r"(e2), "r"(bw[i]));
-        v = make_float2(__uint_as_float(s2 << 16), __uint_as_float(s2 & 0xFFFF0000u));
+        asm("{ .reg .b16 l, h; mov.b32 {l, h}, %2; add.rn.f32.bf16 %0, l, %0; add.rn.f32.bf16 %1, h, %1; }"
+            : "+f"(acc.x), "+f"(acc.y)
+            : "r"(s2));
+        continue;
       }
       acc = __fadd2_rn(acc, v);
     }
@@ -246,46 +256,55 @@ template <int IN_DT, int CH, int KIND, bool BREG>
 __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePlan p, int cpr) {
   extern __shared__ __align__(128) uint8_t ring[];  // kStages x kChunkBytes
   __shared__ __align__(8) uint64_t bar[kStages];
-  __shared__ float red[32];
-  __shared__ int abort_flag;
-  const int tid = threadIdx.x;
+  __shared__ int stage_cnt[kStages];                 // warps done with the stage's current chunk
+  __shared__ long long last_issued[kStages];         // last chunk copied into each stage
+  __shared__ int row_cnt[kRowSlots];                 // warps done with the slot's row
+  __shared__ float partial[kRowSlots][kStreamWarps];
+  __shared__ volatile int abort_flag;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int eb = IN_DT == F32 ? 4 : 2;
   const int64_t row_bytes = p.len * eb;
   const int64_t my_rows = p.rows > blockIdx.x ? (p.rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   const int64_t n_chunks = my_rows * cpr;
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s)
+    for (int s = 0; s < kStages; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])));
+      stage_cnt[s] = 0;
+      last_issued[s] = -1;
+    }
+    for (int r = 0; r < kRowSlots; ++r) row_cnt[r] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     abort_flag = 0;
   }
   __syncthreads();
-  // chunk g of this block is part (g mod cpr) of its row (g div cpr); producer and consumers walk the
-  // chunks in order with incremental counters (no 64-bit division per chunk)
   auto chunk_bytes = [&](int part) {
     const int64_t rem = row_bytes - (int64_t)part * kChunkBytes;
     return (uint32_t)(rem < kChunkBytes ? rem : kChunkBytes);
   };
-  int64_t prod_row = blockIdx.x;
-  int prod_part = 0, prod_stage = 0;
-  auto issue = [&]() {
-    const uint32_t bytes = chunk_bytes(prod_part);
-    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.in) + prod_row * row_bytes + (int64_t)prod_part * kChunkBytes;
-    const int s = prod_stage;
+  // copies chunk g (row `row`, part `part`) into stage g mod kStages
+  auto issue = [&](int64_t g, int64_t row, int part) {
+    const uint32_t bytes = chunk_bytes(part);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.in) + row * row_bytes + (int64_t)part * kChunkBytes;
+    const int s = (int)(g % kStages);
     const uint32_t b = smem_addr(&bar[s]);
+    last_issued[s] = g;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_addr(ring + s * kChunkBytes)), "l"(src), "r"(bytes), "r"(b)
                  : "memory");
-    if (++prod_part == cpr) {
-      prod_part = 0;
-      prod_row += gridDim.x;
-    }
-    prod_stage = prod_stage + 1 == kStages ? 0 : prod_stage + 1;
   };
-  if (tid == 0)
-    for (int64_t g = 0; g < kStages && g < n_chunks; ++g) issue();
+  if (tid == 0) {
+    int64_t row = blockIdx.x;
+    int part = 0;
+    for (int64_t g = 0; g < kStages && g < n_chunks; ++g) {
+      issue(g, row, part);
+      if (++part == cpr) {
+        part = 0;
+        row += gridDim.x;
+      }
+    }
+  }
   const uint4* bv = reinterpret_cast<const uint4*>(p.chain.bptr);
   const LogTab lt = global_log_tables();
   // BREG: rows of at most two chunks; this thread's slice of the broadcast vector (the same for every
@@ -302,13 +321,19 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
       }
   }
   float acc = identity<KIND>();
-  int64_t issued = n_chunks < kStages ? n_chunks : kStages;
-  int cons_part = 0, cons_stage = 0;
+  int cons_part = 0, cons_stage = 0, row_slot = 0;
   uint32_t cons_parity = 0;
   int64_t cons_row = blockIdx.x;
+  // the chunk kStages ahead of the one being consumed: its row and part
+  int64_t nxt_row = blockIdx.x + (int64_t)(kStages / cpr) * gridDim.x;
+  int nxt_part = kStages % cpr;
   for (int64_t g = 0; g < n_chunks; ++g) {
     const int s = cons_stage;
-    if (!mbar_wait(smem_addr(&bar[s]), cons_parity)) abort_flag = 1;
+    if (abort_flag) break;
+    if (!mbar_wait(smem_addr(&bar[s]), cons_parity)) {
+      abort_flag = 1;
+      break;
+    }
     const uint32_t bytes = chunk_bytes(cons_part);
     const int part = cons_part;
     const uint4* xv = reinterpret_cast<const uint4*>(ring + s * kChunkBytes);
@@ -339,27 +364,54 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
         acc = row_vec<IN_DT, CH, KIND>(x, b, acc, p.chain, lt);
       }
     }
-    __syncthreads();  // every thread is done with stage s
-    if (abort_flag) break;
-    if (tid == 0 && issued < n_chunks) {
-      issue();
-      ++issued;
+    __syncwarp();  // the warp's reads of stage s are done
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&stage_cnt[s], 1) == kStreamWarps - 1) {  // the last warp out refills the stage
+        __threadfence_block();
+        stage_cnt[s] = 0;
+        if (g + kStages < n_chunks && !abort_flag) issue(g + kStages, nxt_row, nxt_part);
+      }
     }
-    if (part == cpr - 1) {
-      acc = block_reduce<KIND>(acc, red);
-      if (tid == 0) store_result(p.out, p.out_dt, map_index(p.omap, cons_row), combine<KIND>(p.init, acc));
+    if (part == cpr - 1) {  // end of the row: partial per warp; the warp completing the slot stores
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc = combine<KIND>(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+      if (lane == 0) {
+        partial[row_slot][warp] = acc;
+        __threadfence_block();
+        if (atomicAdd(&row_cnt[row_slot], 1) == kStreamWarps - 1) {
+          row_cnt[row_slot] = 0;
+          __threadfence_block();
+          float r = partial[row_slot][0];
+#pragma unroll
+          for (int w = 1; w < kStreamWarps; ++w) r = combine<KIND>(r, partial[row_slot][w]);
+          store_result(p.out, p.out_dt, map_index(p.omap, cons_row), combine<KIND>(p.init, r));
+        }
+      }
       acc = identity<KIND>();
       cons_row += gridDim.x;
+      row_slot = row_slot + 1 == kRowSlots ? 0 : row_slot + 1;
     }
     if (++cons_part == cpr) cons_part = 0;
     if (++cons_stage == kStages) {
       cons_stage = 0;
       cons_parity ^= 1u;
     }
+    if (++nxt_part == cpr) {
+      nxt_part = 0;
+      nxt_row += gridDim.x;
+    }
   }
-  if (abort_flag && tid == 0) {
-    // a copy did not complete in time: wait (bounded) for the copies still in flight, then leave
-    for (int64_t g = 0; g < issued; ++g) mbar_wait(smem_addr(&bar[g % kStages]), (uint32_t)((g / kStages) & 1));
+  __syncthreads();  // every warp has left the loop (finished, or given up after a bounded wait)
+  if (abort_flag) {
+    // a copy did not complete in time: wait (bounded) for each stage's last copy, then mark this
+    // block's rows NaN so the failure shows in the output
+    if (tid == 0)
+      for (int st = 0; st < kStages; ++st)
+        if (last_issued[st] >= 0)
+          mbar_wait(smem_addr(&bar[st]), (uint32_t)((last_issued[st] / kStages) & 1));
+    for (int64_t r = tid; r < my_rows; r += kStreamThreads)
+      store_result(p.out, p.out_dt, map_index(p.omap, blockIdx.x + r * gridDim.x), __int_as_float(0x7FC00000));
   }
 }
 
