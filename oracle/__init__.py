@@ -24,11 +24,12 @@ _SRC = os.path.join(_HERE, "oracle.cc")
 _SO = os.path.join(_HERE, "liboracle.so")
 
 MAX_RANK = 8
-MAX_OPS = 4
+MAX_OPS = 16
 DTYPES = {"f32": 0, "bf16": 1, "s8": 2, "f16": 3, "s32": 4, "f64": 5, "u8": 6}
 NP_DTYPES = {"f32": np.float32, "bf16": np.uint16, "s8": np.int8, "f16": np.uint16,
              "s32": np.int32, "f64": np.float64, "u8": np.uint8}
-OPS = {"exp": 1, "log": 2, "abs": 3, "neg": 4, "add_bcast": 5}
+OPS = {"exp": 1, "log": 2, "abs": 3, "neg": 4, "add_bcast": 5, "tanh": 6, "add_const": 7, "mul_const": 8,
+       "add_input": 9, "mul_input": 10}
 REDUCE_KINDS = {"add": 0, "max": 1}
 
 # Compiler flags: no fast-math and no FMA contraction, so every source operation rounds exactly once.
@@ -53,7 +54,7 @@ class Chain(ctypes.Structure):
     _fields_ = [("n_ops", ctypes.c_int32), ("ops", ctypes.c_int32 * MAX_OPS),
                 ("round_each", ctypes.c_int32), ("has_bcast", ctypes.c_int32),
                 ("bcast", Arr), ("bcast_dimensions", ctypes.c_int64 * MAX_RANK),
-                ("bcast_data", ctypes.c_void_p)]
+                ("bcast_data", ctypes.c_void_p), ("imm", ctypes.c_double * MAX_OPS)]
 
 
 class Quant(ctypes.Structure):
@@ -146,6 +147,8 @@ class _ChainKeep:
             raise ValueError("too many ops")
         self.c.n_ops = len(ops)
         for i, op in enumerate(ops):
+            if isinstance(op, (tuple, list)):  # (name, constant) for add_const / mul_const
+                op, self.c.imm[i] = op[0], float(op[1])
             self.c.ops[i] = OPS[op]
         self.c.round_each = 1 if spec.get("round_each", True) else 0
         if "bcast" in spec and spec["bcast"] is not None:

@@ -50,9 +50,12 @@
 // ----------------------------------------------------------------------------------------------
 // Descriptors (the oracle's own; plain C layout, mirrored by oracle/__init__.py with ctypes).
 // ----------------------------------------------------------------------------------------------
-enum { ORC_MAX_RANK = 8, ORC_MAX_OPS = 4 };
+enum { ORC_MAX_RANK = 8, ORC_MAX_OPS = 16 };
 enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_S8 = 2, ORC_F16 = 3, ORC_S32 = 4, ORC_F64 = 5, ORC_U8 = 6 };
-enum { ORC_OP_EXP = 1, ORC_OP_LOG = 2, ORC_OP_ABS = 3, ORC_OP_NEG = 4, ORC_OP_ADD_BCAST = 5 };
+enum {
+  ORC_OP_EXP = 1, ORC_OP_LOG = 2, ORC_OP_ABS = 3, ORC_OP_NEG = 4, ORC_OP_ADD_BCAST = 5, ORC_OP_TANH = 6,
+  ORC_OP_ADD_CONST = 7, ORC_OP_MUL_CONST = 8, ORC_OP_ADD_INPUT = 9, ORC_OP_MUL_INPUT = 10
+};
 enum { ORC_RED_ADD = 0, ORC_RED_MAX = 1 };
 enum { ORC_OK = 0, ORC_EINVAL = 1, ORC_EUNRESOLVED = 2 };
 
@@ -73,6 +76,10 @@ typedef struct {
   orc_arr bcast;                            // the broadcast operand of ORC_OP_ADD_BCAST
   int64_t bcast_dimensions[ORC_MAX_RANK];   // broadcast_in_dim's broadcast_dimensions
   const void* bcast_data;
+  // ORC_OP_ADD_CONST / ORC_OP_MUL_CONST: the constant, taken as a value of the element type
+  // ("StableHLO Specification", "constant"); ORC_OP_ADD_INPUT / MUL_INPUT combine the running value
+  // with the element that entered the chain.
+  double imm[ORC_MAX_OPS];
 } orc_chain;
 
 typedef struct {
@@ -236,6 +243,20 @@ static double cr_log(double x, int dt) {
   return (double)round_to<long double>(l, dt);
 }
 
+// Correctly rounded tanh ("StableHLO Specification", "tanh": IEEE-754 tanh of the element type), the
+// same way: libm's double tanh, rechecked in long double next to a rounding boundary.
+static double cr_tanh(double x, int dt) {
+  if (std::isnan(x)) return x;
+  double d = std::tanh(x);
+  if (!near_boundary<double>(d, prec_of(dt), emin_of(dt), std::ldexp(1.0, -50))) return round_to<double>(d, dt);
+  long double l = std::tanh((long double)x);
+  if (near_boundary<long double>(l, prec_of(dt), emin_of(dt), std::ldexp(1.0L, -60))) {
+#pragma omp atomic
+    g_unresolved++;
+  }
+  return (double)round_to<long double>(l, dt);
+}
+
 extern "C" int orc_unresolved_count(void) { return g_unresolved; }
 extern "C" void orc_reset_unresolved(void) { g_unresolved = 0; }
 
@@ -351,10 +372,20 @@ static int working_type(const orc_chain* c, int dt) {
 static double apply_chain(const orc_chain* c, double v, int dt, const int64_t* index) {
   if (!c) return v;
   int wt = working_type(c, dt);
+  const double x = v;  // the element entering the chain
   for (int k = 0; k < c->n_ops; ++k) {
+    // products and sums of two values of at most 24 significand bits: exact in double for the
+    // product; a sum rounded in double first is still rounded correctly into f32/bf16/f16
+    // (53 >= 2 * 24 + 2)
+    const double cst = round_to<double>(c->imm[k], dt);
     switch (c->ops[k]) {
       case ORC_OP_EXP: v = cr_exp(v, wt); break;
       case ORC_OP_LOG: v = cr_log(v, wt); break;
+      case ORC_OP_TANH: v = cr_tanh(v, wt); break;
+      case ORC_OP_ADD_CONST: v = round_to<double>(v + cst, wt); break;
+      case ORC_OP_MUL_CONST: v = round_to<double>(v * cst, wt); break;
+      case ORC_OP_ADD_INPUT: v = round_to<double>(v + x, wt); break;
+      case ORC_OP_MUL_INPUT: v = round_to<double>(v * x, wt); break;
       case ORC_OP_ABS: v = std::fabs(v); break;
       case ORC_OP_NEG: v = -v; break;
       case ORC_OP_ADD_BCAST: {
@@ -374,7 +405,7 @@ static bool valid_chain(const orc_chain* c, const orc_arr* fused) {
   if (c->n_ops < 0 || c->n_ops > ORC_MAX_OPS) return false;
   for (int k = 0; k < c->n_ops; ++k) {
     int op = c->ops[k];
-    if (op < ORC_OP_EXP || op > ORC_OP_ADD_BCAST) return false;
+    if (op < ORC_OP_EXP || op > ORC_OP_MUL_INPUT) return false;
     if (op == ORC_OP_ADD_BCAST) {
       if (!c->has_bcast || !valid_arr(&c->bcast) || !c->bcast_data) return false;
       for (int d = 0; d < c->bcast.rank; ++d) {

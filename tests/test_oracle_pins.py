@@ -478,3 +478,163 @@ def test_quant_fusion_relayout_vs_numpy(orc):
     ratio = (real / np.float32(0.05)).astype(np.float32)                               # f32 divide
     want = np.clip(np.rint(ratio), -128, 127).astype(np.int8)                          # ties to even
     assert np.array_equal(from_physical(out, f.dims, f.out_m2m), want)
+
+
+# ---------------------------------------------------------------------------------------------
+# tanh, constants and the loop fusion (XLA:GPU Emitters, "Loop emitter": the GELU function)
+# ---------------------------------------------------------------------------------------------
+FORMATS = {"bf16": (8, -126, 127), "f16": (11, -14, 15), "f32": (24, -126, 127)}
+
+
+def round_fraction(q: Fraction, fmt: str) -> float:
+    """Nearest value of the binary format to the exact rational q, ties to even, gradual underflow,
+    overflow to infinity (test-side, written independently of the oracle)."""
+    prec, emin, emax = FORMATS[fmt]
+    if q == 0:
+        return 0.0
+    sign, a = (-1, -q) if q < 0 else (1, q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    lead = max(e, emin)
+    quantum = Fraction(2) ** (lead - prec + 1)
+    n = a / quantum
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    r = fl * quantum
+    if r > Fraction(2) ** emax * (2 - Fraction(2) ** (1 - prec)):
+        return sign * math.inf
+    return sign * float(r)
+
+
+def decimal_tanh(x: float) -> Fraction:
+    """tanh(x) to ~60 significant digits as an exact rational (series near 0, exp form elsewhere)."""
+    d = Decimal(x)
+    if abs(d) < Decimal("1e-6"):
+        t = d - d ** 3 / 3 + 2 * d ** 5 / 15 - 17 * d ** 7 / 315
+    else:
+        em = (-2 * abs(d)).exp()  # e^{-2|x|}: no overflow for large |x|
+        t = (1 - em) / (1 + em)
+        t = t if d > 0 else -t
+    return Fraction(t)
+
+
+def bf16_values():
+    bits = np.arange(1 << 16, dtype=np.uint32) << 16
+    return bits.view(np.float32)
+
+
+def f16_values():
+    return np.arange(1 << 16, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def chain_1d(orc, data, dtype, ops):
+    n = len(data)
+    return orc.transpose(data, [n], dtype, [0], prologue={"ops": ops, "round_each": True})
+
+
+def test_gelu_constants_match_the_printed_mlir(orc):
+    g = load_golden("gelu_loop_fusion.txt")
+    for c, printed in zip(g["hlo_constants"], g["printed_bf16"]):
+        # the MLIR prints a bf16 constant with a short decimal that reads back as the same bf16 value
+        v = orc.round_to(c, "bf16")
+        assert v == orc.round_to(float(printed), "bf16") == round_fraction(Fraction(printed), "bf16")
+        assert v == round_fraction(Fraction(c), "bf16")
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_tanh_every_16bit_input_correctly_rounded(orc, fmt):
+    vals = bf16_values() if fmt == "bf16" else f16_values()
+    if fmt == "bf16":
+        got = chain_1d(orc, (vals.view(np.uint32) >> 16).astype(np.uint16), "bf16", ["tanh"])
+        got = (got.astype(np.uint32) << 16).view(np.float32)
+    else:  # f16 travels as its bit pattern
+        got = chain_1d(orc, np.arange(1 << 16, dtype=np.uint16), "f16", ["tanh"])
+        got = np.asarray(got, dtype=np.uint16).view(np.float16).astype(np.float32)
+    bad = 0
+    for x, y in zip(vals, got):
+        x = float(x)
+        if math.isnan(x):
+            bad += not math.isnan(float(y))
+            continue
+        if math.isinf(x):
+            bad += float(y) != math.copysign(1.0, x)
+            continue
+        want = x if x == 0 else round_fraction(decimal_tanh(x), fmt)  # tanh(+-0) = +-0
+        bad += (float(y) != want) or (math.copysign(1.0, float(y)) != math.copysign(1.0, want))
+    assert bad == 0
+
+
+def test_tanh_f32_sample_correctly_rounded(orc):
+    g = np.random.default_rng(5)
+    x = np.concatenate([g.uniform(-6, 6, 1500), g.uniform(-1e-3, 1e-3, 300), [0.5, -2.0, 1e-20, 9.0]])
+    x = x.astype(np.float32)
+    got = chain_1d(orc, x, "f32", ["tanh"])
+    for xi, yi in zip(x, got):
+        assert float(yi) == round_fraction(decimal_tanh(float(xi)), "f32"), float(xi)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f32"])
+def test_constant_and_input_ops_exact(orc, fmt):
+    """v <- x*x + c, * d, + x, * x: each step the exact rational result rounded to the format."""
+    g = np.random.default_rng(6)
+    x = g.standard_normal(500).astype(np.float32) * np.float32(3)
+    c, d = 0.1, -1.7
+    if fmt == "bf16":
+        xb = (x.view(np.uint32) >> 16).astype(np.uint16)  # truncation makes valid bf16 values
+        xs = (xb.astype(np.uint32) << 16).view(np.float32)
+        got = chain_1d(orc, xb, "bf16", ["mul_input", ["add_const", c], ["mul_const", d], "add_input", "mul_input"])
+        got = (got.astype(np.uint32) << 16).view(np.float32)
+    else:
+        xs = x
+        got = chain_1d(orc, x, "f32", ["mul_input", ["add_const", c], ["mul_const", d], "add_input", "mul_input"])
+    cq, dq = Fraction(round_fraction(Fraction(c), fmt)), Fraction(round_fraction(Fraction(d), fmt))
+    for xi, yi in zip(xs, got):
+        xq = Fraction(float(xi))
+        v = Fraction(round_fraction(xq * xq, fmt))
+        v = Fraction(round_fraction(v + cq, fmt))
+        v = Fraction(round_fraction(v * dq, fmt))
+        v = Fraction(round_fraction(v + xq, fmt))
+        want = round_fraction(v * xq, fmt)
+        assert float(yi) == want
+
+
+def gelu_reference(x: float) -> float:
+    """The HLO's ops on exact rationals, each rounded to bf16 (test-side)."""
+    def r(q):
+        return Fraction(round_fraction(q, "bf16"))
+    c3, c2, c1, c0 = (r(Fraction(v)) for v in (0.044708, 0.79785, 1.0, 0.5))
+    xq = Fraction(x)
+    sq = r(xq * xq)
+    cube = r(sq * xq)
+    m3 = r(cube * c3)
+    a1 = r(xq + m3)
+    m2 = r(a1 * c2)
+    th = r(decimal_tanh(float(m2)))
+    a0 = r(th + c1)
+    m1 = r(a0 * c0)
+    out = round_fraction(xq * m1, "bf16")
+    # m1 >= 0 (tanh >= -1), so an IEEE zero product carries the sign of x
+    return math.copysign(0.0, x) if out == 0 else out
+
+
+def test_gelu_chain_against_exact_evaluation(orc):
+    g = load_golden("gelu_loop_fusion.txt")
+    ops = [tuple(o) if isinstance(o, list) else o for o in g["ops"]]
+    vals = bf16_values()
+    finite = vals[np.isfinite(vals) & (np.abs(vals) < 1e4)]
+    sample = np.concatenate([finite[::13], np.float32([0.0, -0.0, 1.0, -1.0, 8.0, -8.0, 0.5])])
+    xb = (sample.view(np.uint32) >> 16).astype(np.uint16)
+    got = (chain_1d(orc, xb, "bf16", ops).astype(np.uint32) << 16).view(np.float32)
+    for xi, yi in zip(sample, got):
+        want = gelu_reference(float(xi))
+        assert float(yi) == want and math.copysign(1.0, float(yi)) == math.copysign(1.0, want), float(xi)
+    # closed forms: gelu(x) = x once tanh rounds to 1; gelu(-x) = -0 once it rounds to -1
+    big = (np.float32([4.0, 8.0, 100.0]).view(np.uint32) >> 16).astype(np.uint16)
+    out = (chain_1d(orc, big, "bf16", ops).astype(np.uint32) << 16).view(np.float32)
+    assert list(out) == [4.0, 8.0, 100.0]
+    neg = (np.float32([-8.0, -100.0]).view(np.uint32) >> 16).astype(np.uint16)
+    out = (chain_1d(orc, neg, "bf16", ops).astype(np.uint32) << 16).view(np.float32)
+    assert all(v == 0 and math.copysign(1.0, float(v)) < 0 for v in out)
