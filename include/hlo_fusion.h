@@ -40,7 +40,7 @@ extern "C" {
 #endif
 
 #define HLO_MAX_RANK 8
-#define HLO_MAX_EW_OPS 4
+#define HLO_MAX_EW_OPS 16
 
 typedef enum {
   HLO_OK = 0,
@@ -68,14 +68,33 @@ typedef struct {
 } hlo_array;
 
 /* Elementwise ops of a prologue/epilogue chain. Each is the IEEE-754 operation on the element type
- * ("StableHLO Specification", sections "exponential", "log", "abs", "negate", "add"); the result type
- * equals the operand type (constraint C1 of each op). */
+ * ("StableHLO Specification", sections "exponential", "log", "tanh", "abs", "negate", "add",
+ * "multiply", "constant"); the result type equals the operand type (constraint C1 of each op). The
+ * chain carries one running value v, which starts as the element x entering the chain:
+ *   HLO_EW_EXP/LOG/TANH/ABS/NEG  v = op(v)
+ *   HLO_EW_ADD_BCAST             v = v + broadcast_in_dim(bcast, bcast_dimensions)[i]
+ *   HLO_EW_ADD_CONST/MUL_CONST   v = v + c, v * c, with c = imm[k] as a constant of the element type
+ *                                (the double is rounded to the element type, nearest even)
+ *   HLO_EW_ADD_INPUT/MUL_INPUT   v = v + x, v * x (x: the element that entered the chain)
+ * So any expression that folds the input into one running value with constants is a chain; the GELU
+ * loop fusion of "XLA:GPU Emitters" (section "Loop emitter") is
+ *   MUL_INPUT, MUL_INPUT, MUL_CONST 0.044708, ADD_INPUT, MUL_CONST 0.79785, TANH, ADD_CONST 1,
+ *   MUL_CONST 0.5, MUL_INPUT.
+ * Rounding: log is correctly rounded; exp and tanh are correctly rounded for bf16/f16 results and
+ * within 2 ulp for f32 results (CUDA's expf, tanhf), except that a reduce prologue's exp of bf16 may
+ * use a faster exp whose rare one-ulp differences stay inside the reduction's tolerance; the other
+ * ops are exact IEEE operations. */
 typedef enum {
   HLO_EW_EXP = 1,
   HLO_EW_LOG = 2,
   HLO_EW_ABS = 3,
   HLO_EW_NEG = 4,
-  HLO_EW_ADD_BCAST = 5 /* x + broadcast_in_dim(bcast, bcast_dimensions) */
+  HLO_EW_ADD_BCAST = 5, /* v + broadcast_in_dim(bcast, bcast_dimensions) */
+  HLO_EW_TANH = 6,
+  HLO_EW_ADD_CONST = 7,
+  HLO_EW_MUL_CONST = 8,
+  HLO_EW_ADD_INPUT = 9,
+  HLO_EW_MUL_INPUT = 10
 } hlo_ew_kind;
 
 /* A chain of up to HLO_MAX_EW_OPS elementwise ops applied in order to every element of the array
@@ -98,6 +117,7 @@ typedef struct {
   const void* bcast_ptr;                   /* device pointer; used by HLO_EW_ADD_BCAST only */
   hlo_array bcast;
   int64_t bcast_dimensions[HLO_MAX_RANK];
+  double imm[HLO_MAX_EW_OPS];              /* the constant of op k (HLO_EW_ADD_CONST/MUL_CONST) */
 } hlo_ew_chain;
 
 typedef enum { HLO_RED_ADD = 0, HLO_RED_MAX = 1 } hlo_reduce_kind;

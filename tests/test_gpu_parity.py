@@ -450,3 +450,68 @@ def test_log_exhaustive_all_floats():
     assert total_bad == 0, [hex(v) for v in examples[:16]]
     bad, ex = oracle.check_log_f32(0x80000000, _gpu_log_bits(0x80000000 - (1 << 32), 1 << 20))
     assert bad == 0
+
+
+# ---- loop fusions: chains with tanh, constants and the input as operands (XLA:GPU Emitters, "Loop
+# emitter"); 16-bit results correctly rounded, so bit-exact -------------------------------------------------
+def _chain_fusion(data, dtype, ops, name="chain"):
+    n = len(data)
+    return inp.Fusion(name=name, kind="transpose", dims=[n], m2m=[0], dtype=dtype, data=data, permutation=[0],
+                      prologue={"ops": ops, "round_each": True}, out_dims=[n], out_m2m=[0], out_dtype=dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("op", ["tanh", "exp", "log"])
+def test_16bit_exp_log_tanh_every_input(dtype, op):
+    """All 65536 bit patterns through the packed 16-bit kernel, then through the scalar kernel (an
+    unaligned view), both against the oracle's correctly rounded values."""
+    data = np.arange(1 << 16, dtype=np.uint16)
+    f = _chain_fusion(data, dtype, [op])
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+    base = torch.from_numpy(np.concatenate([[0], data]).astype(np.uint16).view(np.int16)).cuda()
+    x = base[1:]
+    y = torch.empty(len(data) + 1, dtype=torch.int16, device="cuda")[1:]
+    hf.transpose_fusion(x, [len(data)], dtype, [0], y, prologue={"ops": [op], "round_each": True})
+    torch.cuda.synchronize()
+    check(f, y.cpu().numpy().view(np.uint16), ref, None)
+
+
+def test_gelu_every_bf16_input():
+    data = np.arange(1 << 16, dtype=np.uint16)
+    f = inp.gelu_bf16(dims=[1 << 16], data=data)
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
+@pytest.mark.parametrize("dims", [[6, 512, 4096], [3, 7, 1001]])
+def test_gelu_loop_fusion_sizes(dims):
+    """The emitter's GELU at its size (the benchmark's launch), and a ragged one (tail elements)."""
+    f = inp.gelu_bf16(seed=3, dims=dims)
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
+def test_f32_tanh_within_two_ulp():
+    g = np.random.default_rng(11)
+    x = np.concatenate([g.uniform(-10, 10, 200000), g.uniform(-1e-3, 1e-3, 1000)]).astype(np.float32)
+    f = _chain_fusion(x, "f32", ["tanh"])
+    ref, _ = run_oracle(f)
+    got = run_gpu(f)
+    ulp = np.abs(np.spacing(ref.astype(np.float32)))
+    # within 2 ulp of the exact tanh, so within 2.5 ulp of its correct rounding
+    assert np.all(np.abs(got.astype(np.float64) - ref.astype(np.float64)) <= 2.5 * ulp)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_longest_chain_of_exact_ops(dtype):
+    """Sixteen ops (the most a chain holds) of IEEE add/multiply/negate/abs: bit-exact."""
+    g = np.random.default_rng(12)
+    x = g.standard_normal(50001).astype(np.float32)
+    data = x if dtype == "f32" else inp.f32_to_bf16_bits(x)
+    ops = ["mul_input", ("add_const", 0.25), ("mul_const", -1.5), "add_input", "abs", ("mul_const", 0.1),
+           "mul_input", "neg", ("add_const", 3.0), "mul_input", ("mul_const", 0.7), "add_input", "abs",
+           ("add_const", -2.0), "mul_input", "neg"]
+    f = _chain_fusion(data, dtype, ops)
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)

@@ -23,9 +23,10 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libhlofusion.so")
 
 MAX_RANK = 8
-MAX_EW_OPS = 4
+MAX_EW_OPS = 16
 DTYPES = {"f32": 0, "bf16": 1, "s8": 2, "f16": 3, "s32": 4}
-OPS = {"exp": 1, "log": 2, "abs": 3, "neg": 4, "add_bcast": 5}
+OPS = {"exp": 1, "log": 2, "abs": 3, "neg": 4, "add_bcast": 5, "tanh": 6, "add_const": 7, "mul_const": 8,
+       "add_input": 9, "mul_input": 10}
 REDUCE_KINDS = {"add": 0, "max": 1}
 STATUS = {0: "HLO_OK", 1: "HLO_ERR_INVALID_ARG", 2: "HLO_ERR_UNSUPPORTED", 3: "HLO_ERR_CUDA", 4: "HLO_ERR_WORKSPACE"}
 
@@ -48,7 +49,8 @@ class Array(ctypes.Structure):
 class EwChain(ctypes.Structure):
     _fields_ = [("n_ops", ctypes.c_int32), ("ops", ctypes.c_int32 * MAX_EW_OPS),
                 ("round_intermediates", ctypes.c_int32), ("bcast_ptr", ctypes.c_void_p),
-                ("bcast", Array), ("bcast_dimensions", ctypes.c_int64 * MAX_RANK)]
+                ("bcast", Array), ("bcast_dimensions", ctypes.c_int64 * MAX_RANK),
+                ("imm", ctypes.c_double * MAX_EW_OPS)]
 
 
 class Quant(ctypes.Structure):
@@ -144,13 +146,17 @@ def _stream(stream) -> int:
 
 def make_chain(spec) -> Optional[EwChain]:
     """spec: {"ops": [...], "round_each": bool, "bcast": {"tensor", "dims", "m2m", "dtype",
-    "broadcast_dimensions"}} or None."""
+    "broadcast_dimensions"}} or None. An op is a name, or (name, constant) for add_const/mul_const."""
     if spec is None or not spec.get("ops"):
         return None
     c = EwChain()
     ops = list(spec["ops"])
+    if len(ops) > MAX_EW_OPS:
+        raise HloError(f"a chain holds at most {MAX_EW_OPS} ops")
     c.n_ops = len(ops)
     for i, op in enumerate(ops):
+        if isinstance(op, (tuple, list)):
+            op, c.imm[i] = op[0], float(op[1])
         c.ops[i] = OPS[op]
     c.round_intermediates = 1 if spec.get("round_each", True) else 0
     b = spec.get("bcast")

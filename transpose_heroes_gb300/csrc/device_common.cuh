@@ -85,26 +85,78 @@ struct LogTab {
 __device__ __forceinline__ LogTab global_log_tables() { return {kLogCTab, kLogETab}; }
 
 // One elementwise op. FAST_EXP selects the SFU exp (reductions) or CUDA's expf (elsewhere).
+// Correct rounding into a 16-bit float type from an f32 approximation y of f(x) with an error of at
+// most 2 f32 ulps: if y - 2 ulp and y + 2 ulp round alike, so does f(x) (rounding is monotone).
+// Returns false (and leaves r unset) when they do not, or when y sits next to 0, the subnormals or
+// the top of the range, where the ulp test is not valid.
+__device__ __forceinline__ bool round16_settled(float y, int dt, float& r) {
+  const uint32_t b = __float_as_uint(y), a = b & 0x7FFFFFFFu;
+  if (a >= 0x7F800000u) {  // inf, NaN
+    r = y;
+    return true;
+  }
+  if (a < 0x00800002u || a > 0x7F7FFFFDu) return false;
+  const float v = round_to_dt(y, dt);
+  if (round_to_dt(__uint_as_float(b - 2u), dt) != v || round_to_dt(__uint_as_float(b + 2u), dt) != v) return false;
+  r = v;
+  return true;
+}
+
+// A double rounded once into a 16-bit float type: round to odd into f32 (truncate, then set the last
+// bit if anything was cut off), then to nearest even; f32 keeps at least 2 bits more than the 16-bit
+// significand, so the second rounding cannot go wrong.
+__device__ __forceinline__ float round16_from_double(double d, int dt) {
+  float t = __double2float_rz(d);
+  if ((double)t != d && !isinf(t)) t = __uint_as_float(__float_as_uint(t) | 1u);
+  return round_to_dt(t, dt);
+}
+
+// exp / tanh / log correctly rounded into bf16 or f16 for a 16-bit input: the f32 result (CUDA's expf
+// and tanhf are within 2 ulp, cr_logf within half an ulp) settles almost every element; the rest
+// (about 2^-14 of them) take CUDA's double exp/tanh/log (within 1 double ulp), rounded once.
+static __device__ __noinline__ float exp_round16_slow(float x, int dt) { return round16_from_double(exp((double)x), dt); }
+static __device__ __noinline__ float tanh_round16_slow(float x, int dt) { return round16_from_double(tanh((double)x), dt); }
+static __device__ __noinline__ float log_round16_slow(float x, int dt) { return round16_from_double(log((double)x), dt); }
+
 template <bool FAST_EXP>
-__device__ __forceinline__ float apply_op(int op, float v, float b, const LogTab& lt) {
+__device__ __forceinline__ float apply_op(int op, float v, float b, float x, float imm, bool r16, int dt,
+                                          const LogTab& lt) {
+  float r;
   switch (op) {
-    case OP_EXP: return FAST_EXP ? fast_exp(v) : expf(v);
-    case OP_LOG: return cr_logf(v, lt.c, lt.e);
+    case OP_EXP:
+      if (FAST_EXP) return fast_exp(v);
+      if (!r16) return expf(v);
+      return round16_settled(expf(v), dt, r) ? r : exp_round16_slow(v, dt);
+    case OP_LOG:
+      if (!r16) return cr_logf(v, lt.c, lt.e);
+      return round16_settled(cr_logf(v, lt.c, lt.e), dt, r) ? r : log_round16_slow(v, dt);
+    case OP_TANH:
+      if (!r16) return tanhf(v);
+      return round16_settled(tanhf(v), dt, r) ? r : tanh_round16_slow(v, dt);
     case OP_ABS: return fabsf(v);
     case OP_NEG: return -v;
     case OP_ADD_BCAST: return __fadd_rn(v, b);
+    case OP_ADD_CONST: return __fadd_rn(v, imm);
+    case OP_MUL_CONST: return __fmul_rn(v, imm);
+    case OP_ADD_IN: return __fadd_rn(v, x);
+    case OP_MUL_IN: return __fmul_rn(v, x);
   }
   return v;
 }
 
 // Runtime-interpreted chain (used by the general kernels). boff = offset of the broadcast element.
+// With round16 every op result is rounded to the 16-bit element type: f32 arithmetic on two 16-bit
+// values followed by one rounding equals the correctly rounded 16-bit operation (f32 has at least
+// 2p + 2 significand bits for p = 8 and 11).
 template <bool FAST_EXP>
 __device__ __forceinline__ float apply_chain_rt(const Chain& c, float v, int64_t boff, const LogTab& lt) {
+  const float x = v;
+  const bool r16 = c.round16 && (c.dt == BF16 || c.dt == F16);
   for (int k = 0; k < c.n; ++k) {
-    int op = c.op[k];
+    const int op = c.op[k];
     float b = 0.f;
     if (op == OP_ADD_BCAST) b = load_as_f32(c.bptr, c.bdt, boff);
-    v = apply_op<FAST_EXP>(op, v, b, lt);
+    v = apply_op<FAST_EXP>(op, v, b, x, c.imm[k], r16, c.dt, lt);
     if (c.round16) v = round_to_dt(v, c.dt);
   }
   return v;

@@ -86,6 +86,24 @@ bool ranges_overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes
 }
 
 // ---- chains --------------------------------------------------------------------------------------
+// A constant of the chain as a value of float element type dt: round to nearest, ties to even, at the
+// type's precision (8 significand bits for bf16, 11 for f16, 24 for f32), with gradual underflow and
+// overflow to infinity ("StableHLO Specification", section "constant": the literal is a value of the
+// element type).
+static float constant_of_type(double v, int dt) {
+  if (v == 0 || std::isnan(v) || std::isinf(v)) return (float)v;
+  const int prec = dt == BF16 ? 8 : dt == F16 ? 11 : 24;
+  const int emin = dt == F16 ? -14 : -126, emax = dt == F16 ? 15 : 127;
+  int e;
+  std::frexp(v, &e);
+  const int lead = std::max(e - 1, emin);
+  const double quantum = std::ldexp(1.0, lead - prec + 1);
+  const double r = std::nearbyint(v / quantum) * quantum;  // v / quantum is exact
+  const double maxv = std::ldexp(1.0, emax) * (2.0 - std::ldexp(1.0, 1 - prec));
+  if (std::fabs(r) > maxv) return v > 0 ? INFINITY : -INFINITY;
+  return (float)r;  // exact: r has at most prec <= 24 significand bits
+}
+
 // Validates a chain attached to array `arr` and builds the kernel descriptor.
 hlo_status make_chain(const hlo_ew_chain* c, const hlo_array& arr, bool allow_bcast, const char* what, Chain* out,
                       int force_dt = -1) {
@@ -100,8 +118,9 @@ hlo_status make_chain(const hlo_ew_chain* c, const hlo_array& arr, bool allow_bc
   out->round16 = c->round_intermediates ? 1 : 0;
   for (int k = 0; k < c->n_ops; ++k) {
     const int op = c->ops[k];
-    if (op < HLO_EW_EXP || op > HLO_EW_ADD_BCAST) return fail(HLO_ERR_INVALID_ARG, "%s: unknown op %d", what, op);
+    if (op < HLO_EW_EXP || op > HLO_EW_MUL_INPUT) return fail(HLO_ERR_INVALID_ARG, "%s: unknown op %d", what, op);
     out->op[k] = op;
+    if (op == HLO_EW_ADD_CONST || op == HLO_EW_MUL_CONST) out->imm[k] = constant_of_type(c->imm[k], out->dt);
     if (op != HLO_EW_ADD_BCAST) continue;
     if (!allow_bcast) return fail(HLO_ERR_UNSUPPORTED, "%s: add of a broadcast operand is not supported here", what);
     hlo_status st = check_array(&c->bcast, "broadcast operand");

@@ -9,11 +9,14 @@
 namespace hlo {
 
 enum Dt : int { F32 = 0, BF16 = 1, S8 = 2, F16 = 3, S32 = 4 };
-enum Op : int { OP_NONE = 0, OP_EXP = 1, OP_LOG = 2, OP_ABS = 3, OP_NEG = 4, OP_ADD_BCAST = 5 };
+enum Op : int {
+  OP_NONE = 0, OP_EXP = 1, OP_LOG = 2, OP_ABS = 3, OP_NEG = 4, OP_ADD_BCAST = 5, OP_TANH = 6,
+  OP_ADD_CONST = 7, OP_MUL_CONST = 8, OP_ADD_IN = 9, OP_MUL_IN = 10
+};
 enum Red : int { RED_ADD = 0, RED_MAX = 1 };
 
 constexpr int kMaxRank = 8;
-constexpr int kMaxOps = 4;
+constexpr int kMaxOps = 16;
 
 inline __host__ __device__ int dt_bytes(int dt) {
   return dt == F32 || dt == S32 ? 4 : dt == BF16 || dt == F16 ? 2 : dt == S8 ? 1 : 0;
@@ -47,6 +50,7 @@ __host__ __device__ inline int64_t map_index(const IndexMap& m, int64_t k) {
 struct Chain {
   int n;
   int op[kMaxOps];
+  float imm[kMaxOps];  // constants of OP_ADD_CONST / OP_MUL_CONST, already values of the element type
   int round16;
   int dt;
   const void* bptr;

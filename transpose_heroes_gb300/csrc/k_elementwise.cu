@@ -73,6 +73,117 @@ __global__ void __launch_bounds__(256) elementwise_any_kernel(EwPlan p) {
   }
 }
 
+// ---- 16-bit float chains, every op rounded to the element type ----------------------------------
+// Eight elements per 16-byte vector, held as four packed pairs. Adds and multiplies (by the input or
+// by a constant) run as packed bf16x2 / f16x2 instructions, which round each lane's exact result once:
+// the spec's per-op semantics. exp, log and tanh unpack a pair to f32 and use the correctly rounded
+// 16-bit versions. The ops are walked once per vector, so their dispatch is shared by eight elements.
+template <int DT>
+__device__ __forceinline__ uint32_t pk_add(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if (DT == BF16) asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  else asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pk_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  if (DT == BF16) asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  else asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+template <int DT>
+__device__ __forceinline__ float pk_lo(uint32_t w) {
+  return DT == BF16 ? __uint_as_float(w << 16) : f16_bits_to_f32((uint16_t)(w & 0xFFFFu));
+}
+
+template <int DT>
+__device__ __forceinline__ float pk_hi(uint32_t w) {
+  return DT == BF16 ? __uint_as_float(w & 0xFFFF0000u) : f16_bits_to_f32((uint16_t)(w >> 16));
+}
+
+// Two f32 values that are already values of the 16-bit type, packed (exactly).
+template <int DT>
+__device__ __forceinline__ uint32_t pk_pack(float lo, float hi) {
+  uint32_t r;
+  if (DT == BF16) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t pk_splat(float c) {
+  const uint32_t b = DT == BF16 ? (__float_as_uint(c) >> 16) : (uint32_t)f32_to_f16_bits(c);
+  return b | (b << 16);
+}
+
+template <int DT>
+__device__ __forceinline__ void chain16x2(const Chain& c, uint32_t (&v)[4], const uint32_t (&x)[4], const LogTab& lt) {
+  for (int k = 0; k < c.n; ++k) {
+    const int op = c.op[k];
+    if (op == OP_MUL_IN) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = pk_mul<DT>(v[j], x[j]);
+    } else if (op == OP_ADD_IN) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = pk_add<DT>(v[j], x[j]);
+    } else if (op == OP_MUL_CONST) {
+      const uint32_t c2 = pk_splat<DT>(c.imm[k]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = pk_mul<DT>(v[j], c2);
+    } else if (op == OP_ADD_CONST) {
+      const uint32_t c2 = pk_splat<DT>(c.imm[k]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = pk_add<DT>(v[j], c2);
+    } else if (op == OP_NEG) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] ^= 0x80008000u;
+    } else if (op == OP_ABS) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] &= 0x7FFF7FFFu;
+    } else {  // exp, log, tanh
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = apply_op<false>(op, pk_lo<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt);
+        const float b = apply_op<false>(op, pk_hi<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt);
+        v[j] = pk_pack<DT>(a, b);
+      }
+    }
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) elementwise_16x2_kernel(EwPlan p) {
+  const LogTab lt = global_log_tables();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nv = p.n / 8;
+  const uint4* in = reinterpret_cast<const uint4*>(p.in);
+  uint4* out = reinterpret_cast<uint4*>(p.out);
+  for (int64_t i = tid; i < nv; i += stride) {
+    const uint4 w = __ldg(in + i);
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+    uint32_t v[4] = {w.x, w.y, w.z, w.w};
+    chain16x2<DT>(p.pro, v, x, lt);
+    out[i] = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+  for (int64_t e = nv * 8 + tid; e < p.n; e += stride) {
+    const float r = apply_chain_rt<false>(p.pro, load_as_f32(p.in, DT, e), 0, lt);
+    store_from_f32(p.out, DT, e, r);
+  }
+}
+
+// True when the 16-bit vector kernel applies: every op rounded to the 16-bit type, no broadcast
+// operand, no epilogue.
+static bool chain16x2_ok(const Chain& pro, const Chain& epi, int dt) {
+  if ((dt != BF16 && dt != F16) || epi.n != 0 || !pro.round16) return false;
+  for (int k = 0; k < pro.n; ++k)
+    if (pro.op[k] == OP_ADD_BCAST) return false;
+  return true;
+}
+
 // Pure data movement with identical memory order: raw bytes, 16 at a time where aligned.
 __global__ void __launch_bounds__(256) copy_bytes_kernel(const uint8_t* in, uint8_t* out, int64_t nbytes, bool vec) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -111,6 +222,13 @@ cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, con
     const bool vec = ((uintptr_t)in % 16 == 0) && ((uintptr_t)out % 16 == 0);
     if (vec) elementwise_f32_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(p);
     else elementwise_f32_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(p);
+  } else if (chain16x2_ok(pro, epi, dt) && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0) {
+    int64_t vblocks = (n / 8 + 255) / 256;
+    const int64_t vcap = (int64_t)device_sm_count() * 8;
+    if (vblocks > vcap) vblocks = vcap;
+    if (vblocks < 1) vblocks = 1;
+    if (dt == BF16) elementwise_16x2_kernel<BF16><<<(unsigned)vblocks, 256, 0, s>>>(p);
+    else elementwise_16x2_kernel<F16><<<(unsigned)vblocks, 256, 0, s>>>(p);
   } else {
     elementwise_any_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
   }

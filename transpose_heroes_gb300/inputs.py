@@ -173,6 +173,37 @@ def quant_relayout(seed: int = 1, n0: int = 4096, n1: int = 4096) -> Fusion:
         description="per-axis (dim 1) dequantize of q s8[n0,n1]{1,0}, relayout to {0,1}, quantize per-tensor 0.05:0")
 
 
+# The loop fusion of "XLA:GPU Emitters", section "Loop emitter" (the GELU function and its HLO module
+# in "Reproducer"): bf16 multiply/add/tanh with the HLO's constants, every op rounded to bf16, as one
+# chain that folds the parameter into a running value.
+GELU_CHAIN = [
+    "mul_input",                # square = x * x
+    "mul_input",                # cube = square * x
+    ("mul_const", 0.044708),    # * constant(0.044708)
+    "add_input",                # x + ...
+    ("mul_const", 0.79785),     # * constant(0.79785)
+    "tanh",
+    ("add_const", 1.0),         # + constant(1)
+    ("mul_const", 0.5),         # * constant(0.5)
+    "mul_input",                # x * ...
+]
+
+
+def gelu_bf16(seed: int = 1, dims=(6, 512, 4096), data=None) -> Fusion:
+    """x bf16[6,512,4096]{2,1,0} ~ N(0,1) (activations; the pages give no distribution), out bf16 same
+    shape and layout = gelu(x) with the per-op bf16 rounding of the HLO."""
+    dims = list(dims)
+    n = int(np.prod(dims))
+    if data is None:
+        data = normal_bf16(rng(seed), n)
+    m2m = _default_m2m(len(dims))
+    return Fusion(
+        name="gelu_bf16_" + "x".join(str(d) for d in dims), kind="transpose", dims=dims, m2m=m2m, dtype="bf16",
+        data=data, permutation=list(range(len(dims))), self_add=False,
+        prologue={"ops": list(GELU_CHAIN), "round_each": True}, out_dims=dims, out_m2m=m2m, out_dtype="bf16",
+        description="loop fusion: gelu(x) (tanh form) on x bf16[6,512,4096] ~ N(0,1), bf16 per op")
+
+
 # The five full-size workloads, in a fixed order.
 FULL = {
     "row_reduce_exp": row_reduce_exp,
