@@ -119,36 +119,103 @@ __device__ __forceinline__ uint32_t pk_splat(float c) {
   return b | (b << 16);
 }
 
-template <int DT>
-__device__ __forceinline__ void chain16x2(const Chain& c, uint32_t (&v)[4], const uint32_t (&x)[4], const LogTab& lt) {
+// tanh in f32 for the bf16 path, two lanes per f32x2 instruction, within 16 f32 ulps of tanh(x) for
+// every bf16 x (checked over all of them): |x| < 0.55: x P(x^2), P a degree-5 fit of tanh(x)/x;
+// otherwise (1 - e)/(1 + e), e = e^{-2|x|} from the SFU exponential and reciprocal.
+__device__ __forceinline__ float2 tanh_fast2(float2 x) {
+  const float2 ax = make_float2(fabsf(x.x), fabsf(x.y));
+  const float2 s = __fmul2_rn(x, x);
+  float2 p = __ffma2_rn(s, make_float2(-0.006230350583791733f, -0.006230350583791733f),
+                        make_float2(0.02103571780025959f, 0.02103571780025959f));
+  p = __ffma2_rn(p, s, make_float2(-0.05384165421128273f, -0.05384165421128273f));
+  p = __ffma2_rn(p, s, make_float2(0.1333244889974594f, 0.1333244889974594f));
+  p = __ffma2_rn(p, s, make_float2(-0.3333331048488617f, -0.3333331048488617f));
+  p = __ffma2_rn(p, s, make_float2(1.0f, 1.0f));
+  const float2 small = __fmul2_rn(x, p);
+  const float2 t = __fmul2_rn(ax, make_float2(-2.885390081777927f, -2.885390081777927f));
+  float2 e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.x) : "f"(t.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e.y) : "f"(t.y));
+  const float2 d = __fadd2_rn(e, make_float2(1.0f, 1.0f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(d.y));
+  const float2 big = __fmul2_rn(__ffma2_rn(e, make_float2(-1.0f, -1.0f), make_float2(1.0f, 1.0f)), r);
+  return make_float2(ax.x < 0.55f ? small.x : copysignf(big.x, x.x), ax.y < 0.55f ? small.y : copysignf(big.y, x.y));
+}
+
+// True when every f32 value within `ulps` ulps of y rounds to bf16 the way y does: the 16 bits bf16
+// drops are not within `ulps` of the midpoint 0x8000 (ulps are uniform inside a binade and through
+// the subnormals; inf and NaN pass).
+__device__ __forceinline__ bool bf16_clear_of_midpoint(float y, int ulps) {
+  const uint32_t b = __float_as_uint(y);
+  const int d = (int)(b & 0xFFFFu) - 0x8000;
+  return (d > ulps || d < -ulps) || ((b & 0x7F800000u) == 0x7F800000u);
+}
+
+// exp, log or tanh of one packed bf16 pair, correctly rounded to bf16.
+__device__ __forceinline__ uint32_t bf16_fn2(int op, uint32_t w, const LogTab& lt) {
+  const float a = pk_lo<BF16>(w), b = pk_hi<BF16>(w);
+  float2 f;
+  int ulps = 2;  // expf is within 2 ulps; cr_logf is correctly rounded
+  if (op == OP_TANH) {
+    f = tanh_fast2(make_float2(a, b));
+    ulps = 16;
+  } else if (op == OP_EXP) {
+    f = make_float2(expf(a), expf(b));
+  } else {
+    f = make_float2(cr_logf(a, lt.c, lt.e), cr_logf(b, lt.c, lt.e));
+  }
+  // the f32 value's bf16 rounding is the correct one unless the bits it drops lie within `ulps`
+  // of the midpoint; then the correctly rounded 16-bit path decides
+  if (bf16_clear_of_midpoint(f.x, ulps) && bf16_clear_of_midpoint(f.y, ulps)) return pk_pack<BF16>(f.x, f.y);
+  return pk_pack<BF16>(apply_op<false>(op, a, 0.f, 0.f, 0.f, true, BF16, lt),
+                       apply_op<false>(op, b, 0.f, 0.f, 0.f, true, BF16, lt));
+}
+
+// The chain on kV packed pairs (2 kV elements); the op dispatch is shared by all of them.
+template <int DT, int kV>
+__device__ __forceinline__ void chain16x2(const Chain& c, uint32_t (&v)[kV], const uint32_t (&x)[kV], const LogTab& lt) {
   for (int k = 0; k < c.n; ++k) {
-    const int op = c.op[k];
-    if (op == OP_MUL_IN) {
+    switch (c.op[k]) {
+      case OP_MUL_IN:
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = pk_mul<DT>(v[j], x[j]);
-    } else if (op == OP_ADD_IN) {
+        for (int j = 0; j < kV; ++j) v[j] = pk_mul<DT>(v[j], x[j]);
+        break;
+      case OP_ADD_IN:
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = pk_add<DT>(v[j], x[j]);
-    } else if (op == OP_MUL_CONST) {
-      const uint32_t c2 = pk_splat<DT>(c.imm[k]);
+        for (int j = 0; j < kV; ++j) v[j] = pk_add<DT>(v[j], x[j]);
+        break;
+      case OP_MUL_CONST: {
+        const uint32_t c2 = pk_splat<DT>(c.imm[k]);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = pk_mul<DT>(v[j], c2);
-    } else if (op == OP_ADD_CONST) {
-      const uint32_t c2 = pk_splat<DT>(c.imm[k]);
+        for (int j = 0; j < kV; ++j) v[j] = pk_mul<DT>(v[j], c2);
+        break;
+      }
+      case OP_ADD_CONST: {
+        const uint32_t c2 = pk_splat<DT>(c.imm[k]);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] = pk_add<DT>(v[j], c2);
-    } else if (op == OP_NEG) {
+        for (int j = 0; j < kV; ++j) v[j] = pk_add<DT>(v[j], c2);
+        break;
+      }
+      case OP_NEG:
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] ^= 0x80008000u;
-    } else if (op == OP_ABS) {
+        for (int j = 0; j < kV; ++j) v[j] ^= 0x80008000u;
+        break;
+      case OP_ABS:
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] &= 0x7FFF7FFFu;
-    } else {  // exp, log, tanh
+        for (int j = 0; j < kV; ++j) v[j] &= 0x7FFF7FFFu;
+        break;
+      default: {  // exp, log, tanh
+        const int op = c.op[k];
+        if (DT == BF16) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = apply_op<false>(op, pk_lo<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt);
-        const float b = apply_op<false>(op, pk_hi<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt);
-        v[j] = pk_pack<DT>(a, b);
+          for (int j = 0; j < kV; ++j) v[j] = bf16_fn2(op, v[j], lt);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kV; ++j)
+            v[j] = pk_pack<DT>(apply_op<false>(op, pk_lo<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt),
+                               apply_op<false>(op, pk_hi<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt));
+        }
       }
     }
   }
@@ -159,17 +226,18 @@ __global__ void __launch_bounds__(256) elementwise_16x2_kernel(EwPlan p) {
   const LogTab lt = global_log_tables();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t nv = p.n / 8;
+  const int64_t nv = p.n / 16;  // two 16-byte vectors per step
   const uint4* in = reinterpret_cast<const uint4*>(p.in);
   uint4* out = reinterpret_cast<uint4*>(p.out);
   for (int64_t i = tid; i < nv; i += stride) {
-    const uint4 w = __ldg(in + i);
-    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
-    uint32_t v[4] = {w.x, w.y, w.z, w.w};
-    chain16x2<DT>(p.pro, v, x, lt);
-    out[i] = make_uint4(v[0], v[1], v[2], v[3]);
+    const uint4 w0 = __ldg(in + 2 * i), w1 = __ldg(in + 2 * i + 1);
+    const uint32_t x[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    uint32_t v[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    chain16x2<DT, 8>(p.pro, v, x, lt);
+    out[2 * i] = make_uint4(v[0], v[1], v[2], v[3]);
+    out[2 * i + 1] = make_uint4(v[4], v[5], v[6], v[7]);
   }
-  for (int64_t e = nv * 8 + tid; e < p.n; e += stride) {
+  for (int64_t e = nv * 16 + tid; e < p.n; e += stride) {
     const float r = apply_chain_rt<false>(p.pro, load_as_f32(p.in, DT, e), 0, lt);
     store_from_f32(p.out, DT, e, r);
   }
@@ -223,7 +291,7 @@ cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, con
     if (vec) elementwise_f32_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(p);
     else elementwise_f32_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(p);
   } else if (chain16x2_ok(pro, epi, dt) && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0) {
-    int64_t vblocks = (n / 8 + 255) / 256;
+    int64_t vblocks = (n / 16 + 255) / 256;
     const int64_t vcap = (int64_t)device_sm_count() * 8;
     if (vblocks > vcap) vblocks = vcap;
     if (vblocks < 1) vblocks = 1;
