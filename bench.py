@@ -43,6 +43,8 @@ WORKLOAD = ("HLO hero fusions, one launch each per step: row_reduce_exp f32[256,
             "bcast_exp_row_reduce bf16[8,1,1280,16384]{3,2,0,1}+bf16[16384]; "
             "quant_relayout s8[4096,4096]{1,0}->{0,1}")
 L2_NOTE = "L2 flushed by a 256 MiB device write before every timed step (outside the timed interval)"
+# the loop fusion of "XLA:GPU Emitters" (section "Loop emitter"), measured beside the step
+NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed)}
 # kernel each fusion launches (for the launch list / roofline)
 KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_block_kernel",
            "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",
@@ -344,6 +346,29 @@ def ours(args):
     e2e = {"value": e2e_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": e2e_steps}
 
+    # fusions beyond the five workloads (the loop fusions and the rest of the path's next steps), each
+    # timed alone the same way (L2 flushed before every launch, CUDA events), not part of `value`
+    next_rows = {}
+    reps = max(3, min(args.steps, 200))
+    for name, make in NEXT_ROWS.items():
+        f = make(args.seed)
+        d = DeviceFusion(f, device=dev, pin_host=False)
+        for _ in range(3):
+            d.run(stream=stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in evs:
+            flush.fill_(3)
+            a.record(stream)
+            d.run(stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs)
+        gbs = f.algorithmic_bytes / (us / 1e6) / 1e9
+        next_rows[name] = {"workload": f.description, "us": us, "algorithmic_bytes": f.algorithmic_bytes,
+                           "gbs": gbs, "frac_of_" + peak_src: gbs / hbm, "elements_per_s": f.elements / (us / 1e6),
+                           "launches": reps}
+        del d
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -353,7 +378,7 @@ def ours(args):
                        "parallelism": f"replicas{world}"},
             "elements_per_s": aggregate(float(step_elems * args.steps), "sum") / total_s,
             "per_fusion": per, "roofline": roofline, "clocks": clocks, "e2e": e2e,
-            "gpu_launches": len(devs) * args.steps,
+            "gpu_launches": len(devs) * args.steps, "next_rows": next_rows,
         }
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
