@@ -82,6 +82,9 @@ def lib():
             h.orc_transpose.argtypes = [P(Arr), ctypes.c_void_p, P(Chain), P(ctypes.c_int64), ctypes.c_int,
                                         P(Chain), P(Arr), ctypes.c_void_p]
             h.orc_layout_convert.argtypes = [P(Arr), ctypes.c_void_p, P(ctypes.c_int64), ctypes.c_void_p]
+            h.orc_reduce_max_argmax.argtypes = [P(Arr), ctypes.c_void_p, P(Arr), ctypes.c_void_p, P(ctypes.c_int64),
+                                                ctypes.c_int, ctypes.c_double, ctypes.c_int64, P(Arr),
+                                                ctypes.c_void_p, P(Arr), ctypes.c_void_p]
             h.orc_quant_fusion.argtypes = [P(Arr), ctypes.c_void_p, P(Quant), P(Chain), P(Arr),
                                            ctypes.c_void_p, P(Quant)]
             for name in ("orc_round_to", "orc_exp", "orc_log"):
@@ -269,6 +272,32 @@ def quantize(spec, real, idx=()):
 def dequantize(spec, code, idx=()):
     q = _QuantKeep(spec)
     return lib().orc_dequantize(q.ptr, int(code), _i64(idx or [0]))
+
+
+def reduce_max_argmax(data, dims, dtype, dimensions, init_value, init_index, m2m=None, out_m2m=None,
+                      indices=None, idx_m2m=None, out_idx_m2m=None):
+    """Variadic max/argmax reduce: returns (values, indices); indices None means the position along
+    the single reduced dimension."""
+    a = make_arr(dims, m2m, dtype)
+    kept = [d for d in range(len(dims)) if d not in dimensions]
+    out_dims = [dims[d] for d in kept]
+    o = make_arr(out_dims, out_m2m, dtype)
+    oi = make_arr(out_dims, out_idx_m2m, "s32")
+    src, sp = _buf(data, dtype)
+    if indices is not None:
+        ka = make_arr(dims, idx_m2m if idx_m2m is not None else m2m, "s32")
+        kbuf, kp = _buf(indices, "s32")
+    else:
+        ka, kbuf, kp = make_arr(dims, m2m, "s32"), None, None
+    vals = np.zeros(max(1, int(np.prod(out_dims))), dtype=NP_DTYPES[dtype])
+    idx = np.zeros(max(1, int(np.prod(out_dims))), dtype=np.int32)
+    rc = lib().orc_reduce_max_argmax(ctypes.byref(a), sp, ctypes.byref(ka), kp, _i64(dimensions), len(dimensions),
+                                     ctypes.c_double(init_value), ctypes.c_int64(init_index), ctypes.byref(o),
+                                     vals.ctypes.data_as(ctypes.c_void_p), ctypes.byref(oi),
+                                     idx.ctypes.data_as(ctypes.c_void_p))
+    _check(rc, "reduce_max_argmax")
+    n = int(np.prod(out_dims))
+    return vals[:n], idx[:n]
 
 
 def round_to(x, dtype):

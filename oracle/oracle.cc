@@ -483,6 +483,82 @@ extern "C" int orc_reduce(const orc_arr* in, const void* in_data, const orc_chai
 }
 
 // ----------------------------------------------------------------------------------------------
+// Variadic reduce with the max/argmax body (XLA Operation Semantics, "Variadic Reduce"): inputs V
+// (float) and K (s32, or the position along the single reduced dimension when k_data is NULL), init
+// (I_V, I_K). For every output, the reduced indices are visited in lexicographic order and
+//   f(max, argmax, value, index) = (value, index) if value >= max else (max, argmax)
+// is applied from f(I_V, I_K, V_0, K_0) on, exactly as the recursion f_0, f_1, ..., f_(N-1) of the
+// pages. The value is stored in V's element type (a member of V or I_V: exact), the index as s32.
+// ----------------------------------------------------------------------------------------------
+extern "C" int orc_reduce_max_argmax(const orc_arr* in, const void* in_data, const orc_arr* kin, const void* k_data,
+                                     const int64_t* dimensions, int n_dimensions, double init_value,
+                                     int64_t init_index, const orc_arr* out, void* out_data,
+                                     const orc_arr* out_idx, void* out_idx_data) {
+  if (!valid_arr(in) || !valid_arr(out) || !valid_arr(out_idx)) return ORC_EINVAL;
+  if (!is_float_type(in->dtype) || out->dtype != in->dtype || out_idx->dtype != ORC_S32) return ORC_EINVAL;
+  if (n_dimensions < 0 || n_dimensions > in->rank) return ORC_EINVAL;
+  if (k_data) {
+    if (!valid_arr(kin) || kin->dtype != ORC_S32 || kin->rank != in->rank) return ORC_EINVAL;
+    for (int d = 0; d < in->rank; ++d) if (kin->dims[d] != in->dims[d]) return ORC_EINVAL;
+  } else if (n_dimensions != 1) {
+    return ORC_EINVAL;  // the implicit index runs along one dimension
+  }
+  bool reduced[ORC_MAX_RANK] = {false};
+  for (int i = 0; i < n_dimensions; ++i) {
+    int64_t d = dimensions[i];
+    if (d < 0 || d >= in->rank || reduced[d]) return ORC_EINVAL;
+    reduced[d] = true;
+  }
+  int kept[ORC_MAX_RANK], nk = 0, red[ORC_MAX_RANK], nr = 0;
+  for (int d = 0; d < in->rank; ++d) (reduced[d] ? red[nr++] : kept[nk++]) = d;
+  if (out->rank != nk || out_idx->rank != nk) return ORC_EINVAL;
+  for (int k = 0; k < nk; ++k)
+    if (out->dims[k] != in->dims[kept[k]] || out_idx->dims[k] != in->dims[kept[k]]) return ORC_EINVAL;
+  int64_t kdims[ORC_MAX_RANK], rdims[ORC_MAX_RANK];
+  for (int k = 0; k < nk; ++k) kdims[k] = in->dims[kept[k]];
+  for (int k = 0; k < nr; ++k) rdims[k] = in->dims[red[k]];
+  int64_t n_out = 1, n_red = 1;
+  for (int k = 0; k < nk; ++k) n_out *= kdims[k];
+  for (int k = 0; k < nr; ++k) n_red *= rdims[k];
+  int64_t istride[ORC_MAX_RANK], kstride[ORC_MAX_RANK], ostride[ORC_MAX_RANK], oistride[ORC_MAX_RANK];
+  strides_of(in, istride);
+  if (k_data) strides_of(kin, kstride);
+  strides_of(out, ostride);
+  strides_of(out_idx, oistride);
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t o = 0; o < n_out; ++o) {
+    int64_t kidx[ORC_MAX_RANK], ridx[ORC_MAX_RANK], full[ORC_MAX_RANK];
+    lex_index(nk, kdims, o, kidx);
+    for (int k = 0; k < nk; ++k) full[kept[k]] = kidx[k];
+    double mx = round_to<double>(init_value, in->dtype);
+    int64_t am = init_index;
+    for (int64_t t = 0; t < n_red; ++t) {
+      lex_index(nr, rdims, t, ridx);
+      for (int k = 0; k < nr; ++k) full[red[k]] = ridx[k];
+      int64_t off = 0, koff = 0;
+      for (int d = 0; d < in->rank; ++d) {
+        off += full[d] * istride[d];
+        if (k_data) koff += full[d] * kstride[d];
+      }
+      const double value = load_elem(in_data, in->dtype, off);
+      const int64_t index = k_data ? (int64_t)((const int32_t*)k_data)[koff] : ridx[0];
+      if (value >= mx) {  // f: (value, index) if value >= max else (max, argmax)
+        mx = value;
+        am = index;
+      }
+    }
+    int64_t ooff = 0, oioff = 0;
+    for (int k = 0; k < nk; ++k) {
+      ooff += kidx[k] * ostride[k];
+      oioff += kidx[k] * oistride[k];
+    }
+    store_elem(out_data, out->dtype, ooff, mx);
+    ((int32_t*)out_idx_data)[oioff] = (int32_t)am;
+  }
+  return ORC_OK;
+}
+
+// ----------------------------------------------------------------------------------------------
 // Transpose fusion: out = epilogue(T(prologue(in))) or, with self_add,
 // out = epilogue(prologue(in) + T(prologue(in))) where T permutes dimensions:
 // dims(out)[k] = dims(in)[perm[k]] and T(x)[r] = x[i] with i[perm[k]] = r[k].

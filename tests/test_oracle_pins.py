@@ -638,3 +638,51 @@ def test_gelu_chain_against_exact_evaluation(orc):
     neg = (np.float32([-8.0, -100.0]).view(np.uint32) >> 16).astype(np.uint16)
     out = (chain_1d(orc, neg, "bf16", ops).astype(np.uint32) << 16).view(np.float32)
     assert all(v == 0 and math.copysign(1.0, float(v)) < 0 for v in out)
+
+
+# ---------------------------------------------------------------------------------------------
+# variadic reduce with the max/argmax body (XLA Operation Semantics, "Variadic Reduce")
+# ---------------------------------------------------------------------------------------------
+def test_argmax_closed_forms(orc):
+    ninf = -math.inf
+    # equal maxima keep the last index (value >= max replaces)
+    v, i = orc.reduce_max_argmax(np.float32([1, 3, 2, 3, 0]), [5], "f32", [0], ninf, -1)
+    assert (v[0], i[0]) == (3.0, 3)
+    # NaN never compares >= max, so it is never selected
+    v, i = orc.reduce_max_argmax(np.float32([np.nan, 2, np.nan, 1]), [4], "f32", [0], ninf, -1)
+    assert (v[0], i[0]) == (2.0, 1)
+    # an init above every value survives with its index; an init equal to the max is replaced
+    v, i = orc.reduce_max_argmax(np.float32([1, 2, 3]), [3], "f32", [0], 7.0, 42)
+    assert (v[0], i[0]) == (7.0, 42)
+    v, i = orc.reduce_max_argmax(np.float32([1, 3, 2]), [3], "f32", [0], 3.0, 42)
+    assert (v[0], i[0]) == (3.0, 1)
+    # an empty reduced dimension yields the init values
+    v, i = orc.reduce_max_argmax(np.zeros(0, np.float32), [4, 0], "f32", [1], ninf, -5)
+    assert list(v) == [ninf] * 4 and list(i) == [-5] * 4
+    # a ramp: the last position
+    v, i = orc.reduce_max_argmax(np.arange(10, dtype=np.float32), [10], "f32", [0], ninf, -1)
+    assert (v[0], i[0]) == (9.0, 9)
+
+
+@pytest.mark.parametrize("dimsred", [[1], [0], [0, 2], [2, 1]])
+def test_argmax_against_numpy_last_maximum(orc, dimsred):
+    """Random small integers (many ties), explicit K = a random permutation: the answer is K at the
+    last position, in the lexicographic walk of the reduced dims, that holds the maximum."""
+    g = np.random.default_rng(21)
+    dims = [5, 7, 6]
+    v = g.integers(-3, 4, size=dims).astype(np.float32)
+    k = g.permutation(int(np.prod(dims))).astype(np.int32).reshape(dims)
+    for m2m in ([2, 1, 0], [0, 2, 1]):
+        vals, idx = orc.reduce_max_argmax(to_physical(v, m2m), dims, "f32", dimsred, -math.inf, -1, m2m=m2m,
+                                          indices=to_physical(k, m2m), idx_m2m=m2m)
+        kept = [d for d in range(3) if d not in dimsred]
+        order = kept + sorted(dimsred)  # reduced dims in increasing order: the lexicographic walk
+        vv = np.transpose(v, order).reshape([dims[d] for d in kept] + [-1])
+        kk = np.transpose(k, order).reshape([dims[d] for d in kept] + [-1])
+        n = vv.shape[-1]
+        last = n - 1 - np.argmax(vv[..., ::-1], axis=-1)
+        want_v = np.take_along_axis(vv, last[..., None], -1)[..., 0]
+        want_k = np.take_along_axis(kk, last[..., None], -1)[..., 0]
+        # outputs in the default layout: row-major over the kept dims in their logical order
+        assert np.array_equal(vals, want_v.ravel())
+        assert np.array_equal(idx, want_k.ravel())
