@@ -43,8 +43,9 @@ WORKLOAD = ("HLO hero fusions, one launch each per step: row_reduce_exp f32[256,
             "bcast_exp_row_reduce bf16[8,1,1280,16384]{3,2,0,1}+bf16[16384]; "
             "quant_relayout s8[4096,4096]{1,0}->{0,1}")
 L2_NOTE = "L2 flushed by a 256 MiB device write before every timed step (outside the timed interval)"
-# the loop fusion of "XLA:GPU Emitters" (section "Loop emitter"), measured beside the step
-NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed)}
+# fusions beyond the five workloads, measured beside the step: the loop fusion of "XLA:GPU Emitters"
+# (section "Loop emitter") and the max/argmax variadic reduce of "XLA Operation Semantics"
+NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed), "argmax_f32": lambda seed: inp.argmax_f32(seed=seed)}
 # kernel each fusion launches (for the launch list / roofline)
 KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_block_kernel",
            "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",

@@ -234,6 +234,31 @@ hlo_status hlo_quant_fusion(const hlo_array* in, const void* in_ptr, const hlo_q
                             const hlo_ew_chain* float_ops, const int64_t* out_minor_to_major,
                             const hlo_array* out, void* out_ptr, const hlo_quant* out_q, void* stream);
 
+/* ------------------------------------------------------------------------------------------------
+ * Variadic reduce with the max/argmax body ("XLA Operation Semantics", section "Variadic Reduce"):
+ * inputs V and K, init values I_V, I_K, and the body
+ *     f(max, argmax, value, index) = (value, index) if value >= max else (max, argmax)
+ * applied from f(I_V, I_K, V_0, K_0) on, along the lexicographic walk of the reduced dimensions (in
+ * increasing dimension order). So equal maxima keep the last index walked, and NaN values are never
+ * selected (a comparison with NaN is false). The result is exact: a member of V (or I_V) and of K
+ * (or I_K).
+ *
+ *   in, in_ptr          V: float element type (HLO_F32, HLO_BF16, HLO_F16), any layout
+ *   idx, idx_ptr        K: HLO_S32, same dims as V, any layout; or idx_ptr == NULL, then K is the
+ *                       position along the reduced dimension (n_dimensions must be 1: the iota of
+ *                       the pages' example)
+ *   dimensions          n_dimensions distinct dimensions of V to reduce (may be 0)
+ *   init_value          I_V, rounded to V's element type (nearest even)
+ *   init_index          I_K, in the s32 range
+ *   out, out_ptr        the maxima: V's element type, dims = V's kept dims in order, any layout
+ *   out_idx, out_idx_ptr the indices: HLO_S32, same dims as out, any layout
+ * Errors as for hlo_reduce_fusion (C4, C5, C7 of "reduce"); buffers must not overlap the outputs.
+ * ---------------------------------------------------------------------------------------------- */
+hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const hlo_array* idx,
+                                 const void* idx_ptr, const int64_t* dimensions, int32_t n_dimensions,
+                                 double init_value, int64_t init_index, const hlo_array* out, void* out_ptr,
+                                 const hlo_array* out_idx, void* out_idx_ptr, void* stream);
+
 /* Thread-local description of the last error returned on this thread ("" if none). */
 const char* hlo_last_error(void);
 

@@ -515,3 +515,80 @@ def test_longest_chain_of_exact_ops(dtype):
     f = _chain_fusion(data, dtype, ops)
     ref, _ = run_oracle(f)
     check(f, run_gpu(f), ref, None)
+
+
+# ---- variadic reduce with the max/argmax body (XLA Operation Semantics, "Variadic Reduce") ----------------
+def _torch_buf(np_arr):
+    a = np.ascontiguousarray(np_arr)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+def _argmax_case(data, dims, dtype, dimensions, m2m=None, indices=None, idx_m2m=None, out_m2m=None, out_idx_m2m=None,
+                 init_value=-math.inf, init_index=-1):
+    ref_v, ref_i = oracle.reduce_max_argmax(data, dims, dtype, dimensions, init_value, init_index, m2m=m2m,
+                                            out_m2m=out_m2m, indices=indices, idx_m2m=idx_m2m, out_idx_m2m=out_idx_m2m)
+    n_out = ref_v.size
+    x = _torch_buf(data)
+    k = _torch_buf(indices) if indices is not None else None
+    tdt = torch.float32 if dtype == "f32" else torch.int16
+    ov = torch.empty(max(1, n_out), dtype=tdt, device="cuda")
+    oi = torch.empty(max(1, n_out), dtype=torch.int32, device="cuda")
+    hf.reduce_max_argmax(x, dims, dtype, dimensions, ov, oi, init_value=init_value, init_index=init_index, indices=k,
+                         in_m2m=m2m, idx_m2m=idx_m2m, out_m2m=out_m2m, out_idx_m2m=out_idx_m2m)
+    torch.cuda.synchronize()
+    gv = ov.cpu().numpy()[:n_out]
+    gi = oi.cpu().numpy()[:n_out]
+    if dtype == "f32":
+        same_v = (gv.view(np.uint32) == ref_v.view(np.uint32)) | (np.isnan(gv) & np.isnan(ref_v))
+    else:
+        same_v = gv.view(np.uint16) == np.asarray(ref_v, np.uint16)
+    assert same_v.all(), f"{int((~same_v).sum())} values differ"
+    assert np.array_equal(gi, ref_i), f"{int((gi != ref_i).sum())} indices differ, first at {np.flatnonzero(gi != ref_i)[:4]}"
+
+
+def _values(g, n, dtype, ties=True):
+    x = (g.integers(-4, 5, n) if ties else g.standard_normal(n)).astype(np.float32)
+    x[g.integers(0, n, max(1, n // 97))] = np.nan
+    x[g.integers(0, n, max(1, n // 89))] = -0.0
+    if dtype == "bf16":
+        return inp.f32_to_bf16_bits(x)
+    if dtype == "f16":
+        return x.astype(np.float16).view(np.uint16)
+    return x
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("shape", [[37, 1000], [64, 1024], [5, 4096], [300, 7]])
+def test_argmax_rows(dtype, shape):
+    g = np.random.default_rng(shape[0] * 7 + shape[1])
+    _argmax_case(_values(g, shape[0] * shape[1], dtype), shape, dtype, [1])
+    _argmax_case(_values(g, shape[0] * shape[1], dtype, ties=False), shape, dtype, [1], init_value=0.5, init_index=-7)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_argmax_columns_layouts_and_given_indices(dtype):
+    g = np.random.default_rng(31)
+    dims = [6, 50, 33]
+    n = int(np.prod(dims))
+    data = _values(g, n, dtype)
+    k = g.permutation(n).astype(np.int32)
+    _argmax_case(data, [50, 33], dtype, [0], m2m=[1, 0])                       # reduce the major dim
+    for dimsred, m2m, km2m, om2m in (([0, 2], [2, 1, 0], [0, 1, 2], [0]), ([1], [0, 2, 1], [2, 1, 0], [0, 1]),
+                                     ([2, 0], [1, 0, 2], [1, 2, 0], [0]), ([0, 1, 2], [2, 1, 0], [2, 0, 1], [])):
+        kept = [d for d in range(3) if d not in dimsred]
+        _argmax_case(data, dims, dtype, dimsred, m2m=m2m, indices=k, idx_m2m=km2m, out_m2m=om2m,
+                     out_idx_m2m=list(reversed(om2m)) if len(kept) == 2 else om2m)
+
+
+def test_argmax_empty_and_degenerate():
+    _argmax_case(np.zeros(0, np.float32), [4, 0], "f32", [1], init_index=-3)          # empty reduced dim
+    _argmax_case(np.float32([np.nan] * 12), [3, 4], "f32", [1], init_value=1.0)        # all NaN: init stays
+    _argmax_case(np.float32([2.0] * 12), [3, 4], "f32", [1], init_value=2.0, init_index=9)  # ties with init
+
+
+def test_argmax_full_size_logits():
+    """argmax over f32[4096, 32768] rows (the next-rows benchmark workload)."""
+    f = inp.argmax_f32(seed=4)
+    _argmax_case(f.data, f.dims, f.dtype, f.dimensions)

@@ -142,3 +142,25 @@ def test_quant_validation(lib):
 
 def test_workspace_size_is_zero(lib):
     assert hf.reduce_workspace_size([8192, 16384], "bf16", [0]) == 0
+
+
+def test_argmax_validation(lib):
+    x, out = FAKE_IN, FAKE_OUT
+    out_idx = FAKE_OUT + 4096
+    # without an index input exactly one dimension is reduced
+    st, msg = _status(lambda: hf.reduce_max_argmax(x, [4, 5], "f32", [0, 1], out, out_idx, stream=0))
+    assert st == 1 and "one dimension" in msg
+    # repeated dimension (C5) and out-of-range dimension (C4)
+    idx = FAKE_IN + 8192
+    st, msg = _status(lambda: hf.reduce_max_argmax(x, [4, 5], "f32", [1, 1], out, out_idx, indices=idx, stream=0))
+    assert st == 1 and "C5" in msg
+    st, msg = _status(lambda: hf.reduce_max_argmax(x, [4, 5], "f32", [3], out, out_idx, stream=0))
+    assert st == 1 and "C4" in msg
+    # integer values are not supported; the values output overlapping the input is rejected
+    st, _ = _status(lambda: hf.reduce_max_argmax(x, [4, 5], "s32", [1], out, out_idx, stream=0))
+    assert st == 2
+    st, msg = _status(lambda: hf.reduce_max_argmax(x, [4, 5], "f32", [1], x + 8, out_idx, stream=0))
+    assert st == 1 and "overlap" in msg
+    # init_index outside s32
+    st, msg = _status(lambda: hf.reduce_max_argmax(x, [4, 5], "f32", [1], out, out_idx, init_index=1 << 40, stream=0))
+    assert st == 1 and "s32" in msg

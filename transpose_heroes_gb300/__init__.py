@@ -32,7 +32,7 @@ STATUS = {0: "HLO_OK", 1: "HLO_ERR_INVALID_ARG", 2: "HLO_ERR_UNSUPPORTED", 3: "H
 
 # Every function the header declares; the library must export all of them.
 EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_workspace_size", "hlo_transpose_fusion", "hlo_layout_convert",
-           "hlo_quant_fusion", "hlo_last_error", "hlo_version")
+           "hlo_quant_fusion", "hlo_reduce_max_argmax", "hlo_last_error", "hlo_version")
 
 
 class HloError(RuntimeError):
@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
             h.hlo_layout_convert.restype = ctypes.c_int
             h.hlo_quant_fusion.argtypes = [P(Array), vp, P(Quant), P(EwChain), P(i64), P(Array), vp, P(Quant), vp]
             h.hlo_quant_fusion.restype = ctypes.c_int
+            h.hlo_reduce_max_argmax.argtypes = [P(Array), vp, P(Array), vp, P(i64), i32, ctypes.c_double, i64,
+                                                P(Array), vp, P(Array), vp, vp]
+            h.hlo_reduce_max_argmax.restype = ctypes.c_int
             h.hlo_last_error.restype = ctypes.c_char_p
             h.hlo_version.restype = ctypes.c_char_p
             _lib = h
@@ -221,6 +224,22 @@ def reduce_fusion(inp, in_dims, in_dtype, dimensions, kind, init, out, out_dtype
                                    REDUCE_KINDS[kind], float(init), DTYPES["f32"], ctypes.byref(o), _ptr(out),
                                    _ptr(workspace), int(workspace_bytes), _stream(stream)))
     return out
+
+
+def reduce_max_argmax(inp, in_dims, in_dtype, dimensions, out, out_idx, init_value=float("-inf"), init_index=-1,
+                      indices=None, in_m2m=None, idx_m2m=None, out_m2m=None, out_idx_m2m=None, stream=None):
+    """hlo_reduce_max_argmax: (out, out_idx) = variadic reduce of (inp, indices or the position along the
+    single reduced dimension) with the max/argmax body; equal maxima keep the last index."""
+    a = make_array(in_dims, in_m2m, in_dtype)
+    red = set(int(d) for d in dimensions)
+    out_dims = [d for i, d in enumerate(in_dims) if i not in red]
+    o = make_array(out_dims, out_m2m, in_dtype)
+    oi = make_array(out_dims, out_idx_m2m, "s32")
+    k = make_array(in_dims, idx_m2m if idx_m2m is not None else in_m2m, "s32") if indices is not None else None
+    _check(lib().hlo_reduce_max_argmax(ctypes.byref(a), _ptr(inp), _ref(k), _ptr(indices), _i64(dimensions),
+                                       len(list(dimensions)), float(init_value), int(init_index), ctypes.byref(o),
+                                       _ptr(out), ctypes.byref(oi), _ptr(out_idx), _stream(stream)))
+    return out, out_idx
 
 
 def reduce_workspace_size(in_dims, in_dtype, dimensions, in_m2m=None) -> int:

@@ -348,6 +348,100 @@ int hlo::kernel_blocks_per_sm(const void* kernel, int threads, size_t smem) {
 
 extern "C" {
 
+// ---- variadic reduce: max / argmax ------------------------------------------------------------------
+hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const hlo_array* idx, const void* idx_ptr,
+                                 const int64_t* dimensions, int32_t n_dimensions, double init_value,
+                                 int64_t init_index, const hlo_array* out, void* out_ptr, const hlo_array* out_idx,
+                                 void* out_idx_ptr, void* stream) {
+  hlo_status st = check_array(in, "argmax input");
+  if (st != HLO_OK) return st;
+  if ((st = check_array(out, "argmax values")) != HLO_OK) return st;
+  if ((st = check_array(out_idx, "argmax indices")) != HLO_OK) return st;
+  if (!is_float(in->dtype)) return fail(HLO_ERR_UNSUPPORTED, "argmax: input element type %d not supported", in->dtype);
+  if (out->dtype != in->dtype)
+    return fail(HLO_ERR_INVALID_ARG, "variadic reduce (C7): values type %d differs from input %d", out->dtype, in->dtype);
+  if (out_idx->dtype != HLO_S32) return fail(HLO_ERR_UNSUPPORTED, "argmax: indices must be s32");
+  if (init_index < INT32_MIN || init_index > INT32_MAX) return fail(HLO_ERR_INVALID_ARG, "argmax: init_index outside s32");
+  if (n_dimensions < 0 || n_dimensions > in->rank)
+    return fail(HLO_ERR_INVALID_ARG, "reduce (C4): %d dimensions for rank %d", n_dimensions, in->rank);
+  if (n_dimensions > 0 && !dimensions) return fail(HLO_ERR_INVALID_ARG, "argmax: dimensions is NULL");
+  bool red[HLO_MAX_RANK] = {false};
+  for (int i = 0; i < n_dimensions; ++i) {
+    const int64_t d = dimensions[i];
+    if (d < 0 || d >= in->rank)
+      return fail(HLO_ERR_INVALID_ARG, "reduce (C4): dimension %lld outside [0, %d)", (long long)d, in->rank);
+    if (red[d]) return fail(HLO_ERR_INVALID_ARG, "reduce (C5): dimension %lld repeated", (long long)d);
+    red[d] = true;
+  }
+  if (idx_ptr) {
+    if (!idx) return fail(HLO_ERR_INVALID_ARG, "argmax: index array descriptor is NULL");
+    if ((st = check_array(idx, "argmax index input")) != HLO_OK) return st;
+    if (idx->dtype != HLO_S32) return fail(HLO_ERR_UNSUPPORTED, "argmax: index input must be s32");
+    if (idx->rank != in->rank) return fail(HLO_ERR_INVALID_ARG, "variadic reduce (C2): index input rank differs");
+    for (int d = 0; d < in->rank; ++d)
+      if (idx->dims[d] != in->dims[d]) return fail(HLO_ERR_INVALID_ARG, "variadic reduce (C2): index input shape differs");
+  } else if (n_dimensions != 1) {
+    return fail(HLO_ERR_INVALID_ARG, "argmax: without an index input exactly one dimension is reduced");
+  }
+  std::vector<int> kept, redd;
+  for (int d = 0; d < in->rank; ++d) (red[d] ? redd : kept).push_back(d);
+  for (const hlo_array* o : {out, out_idx}) {
+    if (o->rank != (int)kept.size())
+      return fail(HLO_ERR_INVALID_ARG, "reduce (C7): output rank %d, expected %d", o->rank, (int)kept.size());
+    for (size_t k = 0; k < kept.size(); ++k)
+      if (o->dims[k] != in->dims[kept[k]])
+        return fail(HLO_ERR_INVALID_ARG, "reduce (C7): output dim %d is %lld, expected %lld", (int)k,
+                    (long long)o->dims[k], (long long)in->dims[kept[k]]);
+  }
+  const int64_t n_in = numel(*in), n_out = numel(*out);
+  if (n_in > 0 && !in_ptr) return fail(HLO_ERR_INVALID_ARG, "argmax: input pointer is NULL");
+  if (n_out > 0 && (!out_ptr || !out_idx_ptr)) return fail(HLO_ERR_INVALID_ARG, "argmax: output pointer is NULL");
+  const int64_t vb = n_out * dt_bytes(out->dtype), ib = n_out * 4;
+  if (ranges_overlap(in_ptr, n_in * dt_bytes(in->dtype), out_ptr, vb) ||
+      ranges_overlap(in_ptr, n_in * dt_bytes(in->dtype), out_idx_ptr, ib) || ranges_overlap(out_ptr, vb, out_idx_ptr, ib) ||
+      (idx_ptr && (ranges_overlap(idx_ptr, n_in * 4, out_ptr, vb) || ranges_overlap(idx_ptr, n_in * 4, out_idx_ptr, ib))))
+    return fail(HLO_ERR_INVALID_ARG, "argmax: an output overlaps another buffer");
+  if (n_out == 0) return ok();
+  int64_t vstr[HLO_MAX_RANK], kstr[HLO_MAX_RANK] = {0}, ostr[HLO_MAX_RANK], istr[HLO_MAX_RANK];
+  strides_of(*in, vstr);
+  if (idx_ptr) strides_of(*idx, kstr);
+  strides_of(*out, ostr);
+  strides_of(*out_idx, istr);
+  // kept dims walked lexicographically (output linear index), reduced dims likewise (walk position)
+  std::vector<int64_t> ksz, kv, kk, ko, ki, rsz, rv, rk;
+  for (size_t k = 0; k < kept.size(); ++k) {
+    ksz.push_back(in->dims[kept[k]]);
+    kv.push_back(vstr[kept[k]]);
+    kk.push_back(kstr[kept[k]]);
+    ko.push_back(ostr[k]);
+    ki.push_back(istr[k]);
+  }
+  for (int d : redd) {
+    rsz.push_back(in->dims[d]);
+    rv.push_back(vstr[d]);
+    rk.push_back(kstr[d]);
+  }
+  ArgmaxPlan p;
+  std::memset(&p, 0, sizeof p);
+  p.v = in_ptr;
+  p.k = static_cast<const int32_t*>(idx_ptr);
+  p.out = out_ptr;
+  p.out_idx = static_cast<int32_t*>(out_idx_ptr);
+  p.dt = in->dtype;
+  p.n_out = n_out;
+  p.n_red = 1;
+  for (int64_t r : rsz) p.n_red *= r;
+  p.vkept = make_map(ksz, kv);
+  p.kkept = make_map(ksz, kk);
+  p.okept = make_map(ksz, ko);
+  p.ikept = make_map(ksz, ki);
+  p.vred = make_map(rsz, rv);
+  p.kred = make_map(rsz, rk);
+  p.init_value = constant_of_type(init_value, in->dtype);
+  p.init_index = (int32_t)init_index;
+  return cuda_status(launch_argmax(p, as_stream(stream)), "argmax launch");
+}
+
 const char* hlo_last_error(void) { return g_err.c_str(); }
 
 const char* hlo_version(void) { return "hlofusion 0.1 (sm_103a)"; }

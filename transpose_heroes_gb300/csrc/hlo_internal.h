@@ -178,6 +178,21 @@ struct GatherPlan {
 };
 
 // Kernel launchers (defined in the k_*.cu translation units). Return the launch status.
+// Max/argmax variadic reduce. Output o (lexicographic over the kept dims): V at
+// map_index(vkept, o) + map_index(vred, t) for walk position t; K (if any) likewise with kkept/kred;
+// results at map_index(okept, o) and map_index(ikept, o).
+struct ArgmaxPlan {
+  const void* v;
+  const int32_t* k;  // NULL: the index is the walk position
+  void* out;
+  int32_t* out_idx;
+  int dt;
+  int64_t n_out, n_red;
+  IndexMap vkept, vred, kkept, kred, okept, ikept;
+  float init_value;
+  int32_t init_index;
+};
+cudaError_t launch_argmax(const ArgmaxPlan& p, cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s);
 cudaError_t launch_col_reduce(const ColReducePlan& p, cudaStream_t s);
 cudaError_t launch_gen_reduce(const GenReducePlan& p, cudaStream_t s);

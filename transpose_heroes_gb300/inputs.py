@@ -67,7 +67,7 @@ class Fusion:
     """Plain description of one fusion instance and its input buffers (physical order)."""
 
     name: str
-    kind: str                      # "reduce" | "transpose" | "quant"
+    kind: str                      # "reduce" | "transpose" | "quant" | "argmax"
     dims: list
     m2m: list
     dtype: str
@@ -108,6 +108,8 @@ class Fusion:
         if self.in_q is not None:
             # scales f32 + zero points stored in the storage type
             b += len(np.atleast_1d(self.in_q["scales"])) * (4 + ELEM_BYTES[self.dtype])
+        if self.kind == "argmax":  # the s32 index output beside the values
+            b += int(np.prod(self.out_dims)) * 4
         return int(b)
 
 
@@ -202,6 +204,18 @@ def gelu_bf16(seed: int = 1, dims=(6, 512, 4096), data=None) -> Fusion:
         data=data, permutation=list(range(len(dims))), self_add=False,
         prologue={"ops": list(GELU_CHAIN), "round_each": True}, out_dims=dims, out_m2m=m2m, out_dtype="bf16",
         description="loop fusion: gelu(x) (tanh form) on x bf16[6,512,4096] ~ N(0,1), bf16 per op")
+
+
+def argmax_f32(seed: int = 1, rows: int = 4096, cols: int = 32768) -> Fusion:
+    """Variadic max/argmax reduce (XLA Operation Semantics, "Variadic Reduce") over the last dim of
+    f32[rows, cols]{1,0} ~ N(0,1) with the position as index (a logits-like row argmax; the pages give
+    no size); out f32[rows] values and s32[rows] indices."""
+    g = rng(seed)
+    return Fusion(
+        name=f"argmax_f32_{rows}x{cols}", kind="argmax", dims=[rows, cols], m2m=[1, 0], dtype="f32",
+        data=g.standard_normal(rows * cols, dtype=np.float32), dimensions=[1], reduce_kind="max_argmax",
+        init=float("-inf"), out_dims=[rows], out_m2m=[0], out_dtype="f32",
+        description=f"max/argmax over dim 1 of x f32[{rows},{cols}]{{1,0}} ~ N(0,1), index = position")
 
 
 # The five full-size workloads, in a fixed order.
