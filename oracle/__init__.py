@@ -264,6 +264,22 @@ def quant_fusion(data, dims, in_dtype, in_q, out_m2m, out_dtype, out_q=None, m2m
     return out
 
 
+QUANT_BINARY_OPS = {"add": 0, "divide": 1, "maximum": 2, "minimum": 3, "multiply": 4}
+
+
+def quant_binary(op, lhs, rhs, dims, lhs_q, rhs_q, out_q, lhs_m2m=None, rhs_m2m=None, out_m2m=None):
+    """quantize(op(dequantize(lhs), dequantize(rhs))) with per-tensor s8 operands."""
+    a, b, o = make_arr(dims, lhs_m2m, "s8"), make_arr(dims, rhs_m2m, "s8"), make_arr(dims, out_m2m, "s8")
+    lb, lp = _buf(lhs, "s8")
+    rb, rp = _buf(rhs, "s8")
+    out = np.zeros(max(1, int(np.prod(dims))), dtype=np.int8)
+    ql, qr, qo = _QuantKeep(lhs_q), _QuantKeep(rhs_q), _QuantKeep(out_q)
+    rc = lib().orc_quant_binary(QUANT_BINARY_OPS[op], ctypes.byref(a), lp, ql.ptr, ctypes.byref(b), rp, qr.ptr,
+                                ctypes.byref(o), out.ctypes.data_as(ctypes.c_void_p), qo.ptr)
+    _check(rc, "quant_binary")
+    return out[:int(np.prod(dims))]
+
+
 def quantize(spec, real, idx=()):
     q = _QuantKeep(spec)
     return lib().orc_quantize(q.ptr, float(real), _i64(idx or [0]))

@@ -703,6 +703,59 @@ extern "C" int orc_quant_fusion(const orc_arr* in, const void* in_data, const or
 }
 
 // ----------------------------------------------------------------------------------------------
+// Quantized elementwise binary ops ("StableHLO Specification", sections add, divide, maximum,
+// minimum, multiply: dequantize_op_quantize(op, lhs, rhs, type(result))): both operands dequantized,
+// the op in IEEE f32 (maximum / minimum: NaN propagates, -0 < +0), the result quantized with the
+// result's parameters. Operands and result share dims; each has its own layout. op: 0 add, 1 divide,
+// 2 maximum, 3 minimum, 4 multiply.
+// ----------------------------------------------------------------------------------------------
+static float ieee_binary(int op, float a, float b) {
+  switch (op) {
+    case 0: return a + b;
+    case 1: return a / b;
+    case 2:
+    case 3: {
+      if (std::isnan(a) || std::isnan(b)) return NAN;
+      if (a == b) {  // equal values, possibly zeros of different sign: maximum(-0, +0) = +0
+        bool neg_a = std::signbit(a), neg_b = std::signbit(b);
+        if (op == 2) return neg_a ? b : a;
+        return neg_a ? a : b;
+      }
+      return op == 2 ? (a > b ? a : b) : (a < b ? a : b);
+    }
+    default: return a * b;
+  }
+}
+
+extern "C" int orc_quant_binary(int op, const orc_arr* lhs, const void* l_data, const orc_quant* lq,
+                                const orc_arr* rhs, const void* r_data, const orc_quant* rq, const orc_arr* out,
+                                void* out_data, const orc_quant* oq) {
+  if (op < 0 || op > 4) return ORC_EINVAL;
+  if (!valid_arr(lhs) || !valid_arr(rhs) || !valid_arr(out)) return ORC_EINVAL;
+  if (rhs->rank != lhs->rank || out->rank != lhs->rank) return ORC_EINVAL;
+  for (int d = 0; d < lhs->rank; ++d)
+    if (rhs->dims[d] != lhs->dims[d] || out->dims[d] != lhs->dims[d]) return ORC_EINVAL;
+  if (!valid_quant(lq, lhs) || !valid_quant(rq, rhs) || !valid_quant(oq, out)) return ORC_EINVAL;
+  if (lq->per_axis || rq->per_axis || oq->per_axis) return ORC_EINVAL;  // per-tensor operands (I1, I2)
+  int64_t ls[ORC_MAX_RANK], rs[ORC_MAX_RANK], os[ORC_MAX_RANK];
+  strides_of(lhs, ls);
+  strides_of(rhs, rs);
+  strides_of(out, os);
+  const int64_t n = num_elements(lhs);
+#pragma omp parallel for schedule(static)
+  for (int64_t e = 0; e < n; ++e) {
+    int64_t idx[ORC_MAX_RANK];
+    lex_index(lhs->rank, lhs->dims, e, idx);
+    int64_t lo = 0, ro = 0, oo = 0;
+    for (int d = 0; d < lhs->rank; ++d) { lo += idx[d] * ls[d]; ro += idx[d] * rs[d]; oo += idx[d] * os[d]; }
+    const float a = dequantize_one(lq, (int32_t)load_elem(l_data, lhs->dtype, lo), idx);
+    const float b = dequantize_one(rq, (int32_t)load_elem(r_data, rhs->dtype, ro), idx);
+    store_elem(out_data, out->dtype, oo, (double)quantize_one(oq, ieee_binary(op, a, b), idx));
+  }
+  return ORC_OK;
+}
+
+// ----------------------------------------------------------------------------------------------
 // Scalar entry points used to pin the elementwise rules.
 // ----------------------------------------------------------------------------------------------
 extern "C" double orc_round_to(double v, int dtype) { return round_to<double>(v, dtype); }

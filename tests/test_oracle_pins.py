@@ -686,3 +686,78 @@ def test_argmax_against_numpy_last_maximum(orc, dimsred):
         # outputs in the default layout: row-major over the kept dims in their logical order
         assert np.array_equal(vals, want_v.ravel())
         assert np.array_equal(idx, want_k.ravel())
+
+
+# ---------------------------------------------------------------------------------------------
+# quantized elementwise binary ops (StableHLO Specification, add/divide/maximum/minimum/multiply on
+# quantized types: dequantize_op_quantize)
+# ---------------------------------------------------------------------------------------------
+def _pt(scale, zp):
+    return {"scales": np.float32([scale]), "zero_points": np.int32([zp]), "quantization_dimension": None}
+
+
+ALL_CODES = np.arange(-128, 128, dtype=np.int8)
+
+
+def test_quant_binary_invariants(orc):
+    q = _pt(0.3, 0)  # the pages' quantized-add test type !quant.uniform<i8:f32, 0.3>
+    a = np.repeat(ALL_CODES, 256)
+    b = np.tile(ALL_CODES, 256)
+    dims = [a.size]
+    zero = np.zeros_like(a)
+    # x + 0 and max(x, x) requantized with the same parameters give x back
+    assert np.array_equal(orc.quant_binary("add", a, zero, dims, q, q, q), a)
+    assert np.array_equal(orc.quant_binary("maximum", a, a, dims, q, q, q), a)
+    assert np.array_equal(orc.quant_binary("minimum", a, a, dims, q, q, q), a)
+    # commutative ops
+    for op in ("add", "multiply", "maximum", "minimum"):
+        assert np.array_equal(orc.quant_binary(op, a, b, dims, q, _pt(0.7, 3), _pt(0.2, -5)),
+                              orc.quant_binary(op, b, a, dims, _pt(0.7, 3), q, _pt(0.2, -5)))
+    # max/min of equal parameters pick one operand's code
+    mx = orc.quant_binary("maximum", a, b, dims, q, q, q)
+    assert np.array_equal(mx, np.maximum(a, b))
+    assert np.array_equal(orc.quant_binary("minimum", a, b, dims, q, q, q), np.minimum(a, b))
+    # x / x = 1 exactly (for x != zero point); 1 / 0.25 = 4
+    nz = a[a != 0]
+    assert np.all(orc.quant_binary("divide", nz, nz, [nz.size], q, q, _pt(0.25, 0)) == 4)
+    # saturation: 127 * 0.3 * 127 * 0.3 / 0.01 is far above the storage range
+    assert orc.quant_binary("multiply", np.int8([127]), np.int8([127]), [1], q, q, _pt(0.01, 0))[0] == 127
+    # 0 / 0 is NaN, which quantizes to the zero point
+    assert orc.quant_binary("divide", np.int8([0]), np.int8([0]), [1], q, q, _pt(0.5, 7))[0] == 7
+
+
+@pytest.mark.parametrize("op", ["add", "divide", "maximum", "minimum", "multiply"])
+def test_quant_binary_exact_steps(orc, op):
+    """Each step on exact rationals with the rounding the definition prescribes: the f32 product
+    scale * (q - zp), the f32 op, the f32 quotient by the result scale, ties to even, clamp."""
+    g = np.random.default_rng(7 + len(op))
+    a = g.integers(-128, 128, 400).astype(np.int8)
+    b = g.integers(-128, 128, 400).astype(np.int8)
+    sl, zl, sr, zr, so, zo = 0.0371, 4, 0.113, -9, 0.09, 2
+    got = orc.quant_binary(op, a, b, [400], _pt(sl, zl), _pt(sr, zr), _pt(so, zo))
+    f = lambda v: Fraction(round_fraction(Fraction(float(np.float32(v))), "f32"))
+    S = {k: f(v) for k, v in dict(sl=sl, sr=sr, so=so).items()}
+    for x, y, r in zip(a, b, got):
+        dl = Fraction(round_fraction(S["sl"] * (int(x) - zl), "f32"))
+        dr = Fraction(round_fraction(S["sr"] * (int(y) - zr), "f32"))
+        if op == "add":
+            v = dl + dr
+        elif op == "multiply":
+            v = dl * dr
+        elif op == "maximum":
+            v = max(dl, dr)
+        elif op == "minimum":
+            v = min(dl, dr)
+        else:
+            if dr == 0:
+                want = zo if dl == 0 else (127 if dl > 0 else -128)
+                assert r == want
+                continue
+            v = dl / dr
+        v = Fraction(round_fraction(v, "f32"))
+        ratio = Fraction(round_fraction(v / S["so"], "f32"))
+        fl = ratio.numerator // ratio.denominator
+        rem = ratio - fl
+        if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+            fl += 1
+        assert r == max(-128, min(127, fl + zo))
