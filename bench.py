@@ -44,8 +44,10 @@ WORKLOAD = ("HLO hero fusions, one launch each per step: row_reduce_exp f32[256,
             "quant_relayout s8[4096,4096]{1,0}->{0,1}")
 L2_NOTE = "L2 flushed by a 256 MiB device write before every timed step (outside the timed interval)"
 # fusions beyond the five workloads, measured beside the step: the loop fusion of "XLA:GPU Emitters"
-# (section "Loop emitter") and the max/argmax variadic reduce of "XLA Operation Semantics"
-NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed), "argmax_f32": lambda seed: inp.argmax_f32(seed=seed)}
+# (section "Loop emitter"), the max/argmax variadic reduce of "XLA Operation Semantics" and a
+# quantized add (dequantize_op_quantize)
+NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed), "argmax_f32": lambda seed: inp.argmax_f32(seed=seed),
+             "quant_add_s8": lambda seed: inp.quant_add_s8(seed=seed)}
 # kernel each fusion launches (for the launch list / roofline)
 KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_block_kernel",
            "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",

@@ -235,6 +235,32 @@ hlo_status hlo_quant_fusion(const hlo_array* in, const void* in_ptr, const hlo_q
                             const hlo_array* out, void* out_ptr, const hlo_quant* out_q, void* stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * Elementwise binary op on per-tensor quantized operands ("StableHLO Specification", sections "add",
+ * "divide", "maximum", "minimum", "multiply": for quantized types each performs
+ * dequantize_op_quantize(op, lhs, rhs, type(result))):
+ *     out[i] = clamp(round_nearest_even(op(dl, dr) / s_out) + zp_out, storage_min, storage_max)
+ *     dl = s_l * (lhs[i] - zp_l),  dr = s_r * (rhs[i] - zp_r)
+ * with every float step a single IEEE f32 operation (maximum/minimum propagate NaN; a NaN result
+ * quantizes to zp_out), so the result is bit-exact.
+ *   op                    HLO_QOP_ADD, HLO_QOP_DIVIDE, HLO_QOP_MAXIMUM, HLO_QOP_MINIMUM, HLO_QOP_MULTIPLY
+ *   lhs, rhs, out         HLO_S8 arrays with equal dims, any layouts (element i is the same logical
+ *                         index in each)
+ *   lhs_q, rhs_q, out_q   per-tensor parameters (quantization_dimension -1, host_scales and
+ *                         host_zero_points set); per-axis operands are rejected (I1, I2 of each op)
+ * ---------------------------------------------------------------------------------------------- */
+typedef enum {
+  HLO_QOP_ADD = 0,
+  HLO_QOP_DIVIDE = 1,
+  HLO_QOP_MAXIMUM = 2,
+  HLO_QOP_MINIMUM = 3,
+  HLO_QOP_MULTIPLY = 4
+} hlo_quant_binary_op;
+
+hlo_status hlo_quant_binary(int32_t op, const hlo_array* lhs, const void* lhs_ptr, const hlo_quant* lhs_q,
+                            const hlo_array* rhs, const void* rhs_ptr, const hlo_quant* rhs_q, const hlo_array* out,
+                            void* out_ptr, const hlo_quant* out_q, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
  * Variadic reduce with the max/argmax body ("XLA Operation Semantics", section "Variadic Reduce"):
  * inputs V and K, init values I_V, I_K, and the body
  *     f(max, argmax, value, index) = (value, index) if value >= max else (max, argmax)

@@ -592,3 +592,49 @@ def test_argmax_full_size_logits():
     """argmax over f32[4096, 32768] rows (the next-rows benchmark workload)."""
     f = inp.argmax_f32(seed=4)
     _argmax_case(f.data, f.dims, f.dtype, f.dimensions)
+
+
+# ---- quantized elementwise binary ops (dequantize_op_quantize) ---------------------------------------------
+def _qpt(scale, zp, smin=-128, smax=127):
+    return {"scales": np.float32([scale]), "zero_points": np.int32([zp]), "quantization_dimension": None,
+            "host_scales": np.float32([scale]), "host_zero_points": np.int32([zp]), "storage_min": smin,
+            "storage_max": smax}
+
+
+@pytest.mark.parametrize("op", ["add", "divide", "maximum", "minimum", "multiply"])
+def test_quant_binary_every_code_pair(op):
+    """All 65536 code pairs, aligned (vector kernel) and through unaligned views (per-element kernel)."""
+    codes = np.arange(-128, 128, dtype=np.int8)
+    a, b = np.repeat(codes, 256), np.tile(codes, 256)
+    ql, qr, qo = _qpt(0.0371, 4), _qpt(0.113, -9), _qpt(0.09, 2, -100, 120)
+    ref = oracle.quant_binary(op, a, b, [a.size], ql, qr, qo)
+    for shift in (0, 1):
+        base_a = torch.from_numpy(np.concatenate([np.zeros(shift, np.int8), a])).cuda()
+        base_b = torch.from_numpy(np.concatenate([np.zeros(shift, np.int8), b])).cuda()
+        out = torch.empty(a.size + shift, dtype=torch.int8, device="cuda")
+        hf.quant_binary(op, base_a[shift:], base_b[shift:], [a.size], ql, qr, out[shift:], qo)
+        torch.cuda.synchronize()
+        got = out[shift:].cpu().numpy()
+        assert np.array_equal(got, ref), f"{int((got != ref).sum())} codes differ (shift {shift})"
+
+
+def test_quant_binary_layouts_and_sizes():
+    g = np.random.default_rng(41)
+    dims = [37, 53, 5]
+    n = int(np.prod(dims))
+    a = g.integers(-128, 128, n).astype(np.int8)
+    b = g.integers(-128, 128, n).astype(np.int8)
+    q = _qpt(0.3, 0)
+    for lm, rm, om in (([2, 1, 0], [0, 1, 2], [1, 2, 0]), ([0, 2, 1], [0, 2, 1], [0, 2, 1])):
+        ref = oracle.quant_binary("add", a, b, dims, q, q, q, lhs_m2m=lm, rhs_m2m=rm, out_m2m=om)
+        out = torch.empty(n, dtype=torch.int8, device="cuda")
+        hf.quant_binary("add", torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), dims, q, q, out, q,
+                        lhs_m2m=lm, rhs_m2m=rm, out_m2m=om)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), ref)
+
+
+def test_quant_add_full_size():
+    f = inp.quant_add_s8(seed=2)
+    ref = oracle.quant_binary(f.op, f.data, f.rhs, f.dims, f.in_q, f.in_q, f.out_q)
+    assert np.array_equal(run_gpu(f), ref)

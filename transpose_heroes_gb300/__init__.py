@@ -32,7 +32,8 @@ STATUS = {0: "HLO_OK", 1: "HLO_ERR_INVALID_ARG", 2: "HLO_ERR_UNSUPPORTED", 3: "H
 
 # Every function the header declares; the library must export all of them.
 EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_workspace_size", "hlo_transpose_fusion", "hlo_layout_convert",
-           "hlo_quant_fusion", "hlo_reduce_max_argmax", "hlo_last_error", "hlo_version")
+           "hlo_quant_fusion", "hlo_quant_binary", "hlo_reduce_max_argmax", "hlo_last_error", "hlo_version")
+QUANT_BINARY_OPS = {"add": 0, "divide": 1, "maximum": 2, "minimum": 3, "multiply": 4}
 
 
 class HloError(RuntimeError):
@@ -89,6 +90,9 @@ def lib() -> ctypes.CDLL:
             h.hlo_layout_convert.restype = ctypes.c_int
             h.hlo_quant_fusion.argtypes = [P(Array), vp, P(Quant), P(EwChain), P(i64), P(Array), vp, P(Quant), vp]
             h.hlo_quant_fusion.restype = ctypes.c_int
+            h.hlo_quant_binary.argtypes = [i32, P(Array), vp, P(Quant), P(Array), vp, P(Quant), P(Array), vp,
+                                           P(Quant), vp]
+            h.hlo_quant_binary.restype = ctypes.c_int
             h.hlo_reduce_max_argmax.argtypes = [P(Array), vp, P(Array), vp, P(i64), i32, ctypes.c_double, i64,
                                                 P(Array), vp, P(Array), vp, vp]
             h.hlo_reduce_max_argmax.restype = ctypes.c_int
@@ -191,8 +195,10 @@ class _QuantKeep:
             q.host_zero_points = hz.ctypes.data
             n = hs.size if n is None else n
         q.n = int(n if n is not None else spec["scales"].numel())
-        q.scales = _ptr(spec.get("scales"))
-        q.zero_points = _ptr(spec.get("zero_points"))
+        # device parameters (per-axis); host arrays under these keys are not device memory
+        dev = lambda t: _ptr(t) if t is not None and not isinstance(t, np.ndarray) else 0
+        q.scales = dev(spec.get("scales"))
+        q.zero_points = dev(spec.get("zero_points"))
         q.storage_min = int(spec.get("storage_min", -128))
         q.storage_max = int(spec.get("storage_max", 127))
         self.q = q
@@ -264,6 +270,17 @@ def layout_convert(inp, dims, dtype, in_m2m, out_m2m, out, stream=None):
     """hlo_layout_convert: the same logical array written with out_m2m."""
     a = make_array(dims, in_m2m, dtype)
     _check(lib().hlo_layout_convert(ctypes.byref(a), _ptr(inp), _i64(out_m2m), _ptr(out), _stream(stream)))
+    return out
+
+
+def quant_binary(op, lhs, rhs, dims, lhs_q, rhs_q, out, out_q, lhs_m2m=None, rhs_m2m=None, out_m2m=None,
+                 stream=None):
+    """hlo_quant_binary: out = quantize(op(dequantize(lhs), dequantize(rhs))), per-tensor s8 operands.
+    The *_q specs carry host_scales / host_zero_points (one each)."""
+    a, b, o = make_array(dims, lhs_m2m, "s8"), make_array(dims, rhs_m2m, "s8"), make_array(dims, out_m2m, "s8")
+    ql, qr, qo = _QuantKeep(lhs_q), _QuantKeep(rhs_q), _QuantKeep(out_q)
+    _check(lib().hlo_quant_binary(QUANT_BINARY_OPS[op], ctypes.byref(a), _ptr(lhs), ql.ref(), ctypes.byref(b), _ptr(rhs),
+                                  qr.ref(), ctypes.byref(o), _ptr(out), qo.ref(), _stream(stream)))
     return out
 
 

@@ -348,6 +348,59 @@ int hlo::kernel_blocks_per_sm(const void* kernel, int threads, size_t smem) {
 
 extern "C" {
 
+// ---- quantized elementwise binary ops ------------------------------------------------------------------
+hlo_status hlo_quant_binary(int32_t op, const hlo_array* lhs, const void* lhs_ptr, const hlo_quant* lhs_q,
+                            const hlo_array* rhs, const void* rhs_ptr, const hlo_quant* rhs_q, const hlo_array* out,
+                            void* out_ptr, const hlo_quant* out_q, void* stream) {
+  if (op < HLO_QOP_ADD || op > HLO_QOP_MULTIPLY) return fail(HLO_ERR_INVALID_ARG, "quantized op: unknown op %d", op);
+  hlo_status st;
+  const hlo_array* arrs[3] = {lhs, rhs, out};
+  const char* names[3] = {"quantized lhs", "quantized rhs", "quantized result"};
+  for (int a = 0; a < 3; ++a) {
+    if ((st = check_array(arrs[a], names[a])) != HLO_OK) return st;
+    if (arrs[a]->dtype != HLO_S8) return fail(HLO_ERR_UNSUPPORTED, "%s: storage type must be s8", names[a]);
+  }
+  for (int a = 1; a < 3; ++a) {
+    if (arrs[a]->rank != lhs->rank) return fail(HLO_ERR_INVALID_ARG, "%s (C1): rank differs from lhs", names[a]);
+    for (int d = 0; d < lhs->rank; ++d)
+      if (arrs[a]->dims[d] != lhs->dims[d]) return fail(HLO_ERR_INVALID_ARG, "%s (C1): shape differs from lhs", names[a]);
+  }
+  QuantBinaryPlan p;
+  std::memset(&p, 0, sizeof p);
+  const hlo_quant* qs[3] = {lhs_q, rhs_q, out_q};
+  QuantParams* qp[3] = {&p.ql, &p.qr, &p.qo};
+  for (int a = 0; a < 3; ++a) {
+    if ((st = check_quant(qs[a], *arrs[a], names[a], qp[a])) != HLO_OK) return st;
+    if (qp[a]->axis >= 0)
+      return fail(HLO_ERR_INVALID_ARG, "%s (I1, I2): per-tensor quantized tensors only", names[a]);
+  }
+  const int64_t n = numel(*lhs);
+  if (n > 0 && (!lhs_ptr || !rhs_ptr || !out_ptr)) return fail(HLO_ERR_INVALID_ARG, "quantized op: NULL pointer");
+  if (ranges_overlap(out_ptr, n, lhs_ptr, n) || ranges_overlap(out_ptr, n, rhs_ptr, n))
+    return fail(HLO_ERR_INVALID_ARG, "quantized op: the result overlaps an operand");
+  if (n == 0) return ok();
+  p.lhs = static_cast<const int8_t*>(lhs_ptr);
+  p.rhs = static_cast<const int8_t*>(rhs_ptr);
+  p.out = static_cast<int8_t*>(out_ptr);
+  p.n = n;
+  p.op = op;
+  bool same_layout = true;
+  for (int a = 1; a < 3; ++a)
+    for (int d = 0; d < lhs->rank; ++d) same_layout = same_layout && arrs[a]->minor_to_major[d] == lhs->minor_to_major[d];
+  if (same_layout) {  // the same physical offset holds the same logical index in all three
+    p.lmap = p.rmap = p.omap = make_map({n}, {1});
+  } else {
+    std::vector<int64_t> sz(lhs->dims, lhs->dims + lhs->rank);
+    IndexMap* maps[3] = {&p.lmap, &p.rmap, &p.omap};
+    for (int a = 0; a < 3; ++a) {
+      int64_t str[HLO_MAX_RANK];
+      strides_of(*arrs[a], str);
+      *maps[a] = make_map(sz, std::vector<int64_t>(str, str + lhs->rank));
+    }
+  }
+  return cuda_status(launch_quant_binary(p, as_stream(stream)), "quantized op launch");
+}
+
 // ---- variadic reduce: max / argmax ------------------------------------------------------------------
 hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const hlo_array* idx, const void* idx_ptr,
                                  const int64_t* dimensions, int32_t n_dimensions, double init_value,

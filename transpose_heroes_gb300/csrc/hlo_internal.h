@@ -193,6 +193,19 @@ struct ArgmaxPlan {
   int32_t init_index;
 };
 cudaError_t launch_argmax(const ArgmaxPlan& p, cudaStream_t s);
+
+// Quantized binary op: out at map_index(omap, i) = q(op(dq(lhs at lmap(i)), dq(rhs at rmap(i)))), i the
+// logical linear index (identity maps when all three share one layout).
+struct QuantBinaryPlan {
+  const int8_t* lhs;
+  const int8_t* rhs;
+  int8_t* out;
+  int64_t n;
+  int op;
+  IndexMap lmap, rmap, omap;
+  QuantParams ql, qr, qo;
+};
+cudaError_t launch_quant_binary(const QuantBinaryPlan& p, cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s);
 cudaError_t launch_col_reduce(const ColReducePlan& p, cudaStream_t s);
 cudaError_t launch_gen_reduce(const GenReducePlan& p, cudaStream_t s);

@@ -82,6 +82,9 @@ class Fusion:
     # quant
     in_q: Optional[dict] = None
     out_q: Optional[dict] = None
+    # quantized binary op: the op name and the second operand (physical order)
+    op: Optional[str] = None
+    rhs: Optional[np.ndarray] = None
     # common
     prologue: Optional[dict] = None
     epilogue: Optional[dict] = None
@@ -110,6 +113,8 @@ class Fusion:
             b += len(np.atleast_1d(self.in_q["scales"])) * (4 + ELEM_BYTES[self.dtype])
         if self.kind == "argmax":  # the s32 index output beside the values
             b += int(np.prod(self.out_dims)) * 4
+        if self.kind == "quant_binary":  # the second operand
+            b += self.elements * ELEM_BYTES[self.dtype]
         return int(b)
 
 
@@ -216,6 +221,25 @@ def argmax_f32(seed: int = 1, rows: int = 4096, cols: int = 32768) -> Fusion:
         data=g.standard_normal(rows * cols, dtype=np.float32), dimensions=[1], reduce_kind="max_argmax",
         init=float("-inf"), out_dims=[rows], out_m2m=[0], out_dtype="f32",
         description=f"max/argmax over dim 1 of x f32[{rows},{cols}]{{1,0}} ~ N(0,1), index = position")
+
+
+def quant_add_s8(seed: int = 1, n0: int = 4096, n1: int = 4096) -> Fusion:
+    """Quantized add (StableHLO Specification, "add" on quantized types; the quantized test case of
+    "StableHLO Quantization" adds two i8:f32 0.3 tensors): lhs, rhs s8[n0,n1]{1,0} ~ U[-128,127],
+    both per-tensor 0.3:0, result per-tensor 0.3:0. `data` holds lhs, `rhs` the second operand."""
+    g = rng(seed)
+    n = n0 * n1
+    f = Fusion(
+        name=f"quant_add_s8_{n0}x{n1}", kind="quant_binary", dims=[n0, n1], m2m=[1, 0], dtype="s8",
+        data=integers(g, n, -128, 127, np.int8),
+        in_q={"scales": np.float32([0.3]), "zero_points": np.int32([0]), "quantization_dimension": None},
+        out_q={"scales": np.float32([0.3]), "zero_points": np.int32([0]), "quantization_dimension": None,
+               "storage_min": -128, "storage_max": 127},
+        out_dims=[n0, n1], out_m2m=[1, 0], out_dtype="s8",
+        description=f"quantized add of s8[{n0},{n1}] i8:f32 0.3 operands, result i8:f32 0.3",
+        op="add")
+    f.rhs = integers(g, n, -128, 127, np.int8)
+    return f
 
 
 # The five full-size workloads, in a fixed order.

@@ -10,7 +10,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import layout_convert, quant_fusion, reduce_fusion, reduce_max_argmax, transpose_fusion
+from . import layout_convert, quant_binary, quant_fusion, reduce_fusion, reduce_max_argmax, transpose_fusion
 from .inputs import ELEM_BYTES, Fusion
 
 # physical buffers as torch tensors of the same element size (16-bit floats carried as int16 bits)
@@ -52,6 +52,12 @@ class DeviceFusion:
         self.out = torch.empty(n_out, dtype=_TORCH[f.out_dtype], device=device)
         self.host_out = torch.empty(n_out, dtype=_TORCH[f.out_dtype], pin_memory=pin_host)
         self.out_idx = torch.empty(n_out, dtype=torch.int32, device=device) if f.kind == "argmax" else None
+        self.rhs = None
+        if f.kind == "quant_binary":
+            self.rhs = host_tensor(f.rhs, f.dtype).to(device)
+            self._qspec = lambda q: {"host_scales": q["scales"], "host_zero_points": q["zero_points"],
+                                     "quantization_dimension": None, "storage_min": q.get("storage_min", -128),
+                                     "storage_max": q.get("storage_max", 127)}
 
     def _quant(self, q):
         scales = np.ascontiguousarray(np.atleast_1d(q["scales"]), dtype=np.float32)
@@ -84,6 +90,9 @@ class DeviceFusion:
         elif f.kind == "quant":
             quant_fusion(self.x, f.dims, self.qin, f.out_m2m, self.out, out_dtype=f.out_dtype, out_q=self.qout,
                          in_m2m=f.m2m, float_ops=self._chain(f.prologue), stream=stream)
+        elif f.kind == "quant_binary":
+            quant_binary(f.op, self.x, self.rhs, f.dims, self._qspec(f.in_q), self._qspec(f.in_q), self.out,
+                         self._qspec(f.out_q), lhs_m2m=f.m2m, rhs_m2m=f.m2m, out_m2m=f.out_m2m, stream=stream)
         elif f.kind == "argmax":
             reduce_max_argmax(self.x, f.dims, f.dtype, f.dimensions, self.out, self.out_idx, init_value=f.init,
                               init_index=-1, in_m2m=f.m2m, out_m2m=f.out_m2m, out_idx_m2m=f.out_m2m, stream=stream)
