@@ -379,7 +379,7 @@ def _qspec(g, n, per_axis_dim, smin=-128, smax=127):
             "quantization_dimension": per_axis_dim, "storage_min": smin, "storage_max": smax}
 
 
-@pytest.mark.parametrize("n0,n1", [(128, 128), (256, 384), (130, 200), (7, 3), (4096, 16)])
+@pytest.mark.parametrize("n0,n1", [(128, 128), (256, 384), (384, 128), (130, 200), (7, 3), (4096, 16)])
 def test_quant_relayout_variants(n0, n1):
     g = inp.rng(n0 + n1)
     q = inp.integers(g, n0 * n1, -128, 127, np.int8)
@@ -419,6 +419,30 @@ def test_quant_division_ties():
                    out_dims=[n0, n1], out_m2m=[0, 1], out_dtype="s8")
     ref, _ = run_oracle(f)
     check(f, run_gpu(f), ref, None)
+
+
+@pytest.mark.parametrize("ratio", [3000.0, 20000.0])
+def test_quant_scale_ratios(ratio):
+    """Input/output scale ratios that push quotients far past the i8 range, so that saturation decides
+    (3000), and beyond the range the bracketed fast test accepts (20000: the exact test decides)."""
+    n0, n1 = 256, 384
+    g = inp.rng(int(ratio))
+    q = inp.integers(g, n0 * n1, -128, 127, np.int8)
+    for qin_dim, qout_dim, smin, smax in ((1, None, -128, 127), (0, 1, -128, 127), (None, None, -7, 9)):
+        dims = [n0, n1]
+        nin = dims[qin_dim] if qin_dim is not None else 1
+        nout = dims[qout_dim] if qout_dim is not None else 1
+        scale_out = inp.uniform_f32(g, nout, 0.5, 1.0) / np.float32(ratio)
+        qin = {"scales": inp.uniform_f32(g, nin, 0.5, 1.0), "zero_points": inp.integers(g, nin, -20, 20, np.int32),
+               "quantization_dimension": qin_dim}
+        qout = {"scales": scale_out.astype(np.float32), "zero_points": inp.integers(g, nout, -3, 3, np.int32),
+                "quantization_dimension": qout_dim, "storage_min": smin, "storage_max": smax}
+        f = inp.Fusion(name="qr", kind="quant", dims=dims, m2m=[1, 0], dtype="s8", data=q, in_q=qin, out_q=qout,
+                       out_dims=dims, out_m2m=[0, 1], out_dtype="s8")
+        ref, _ = run_oracle(f)
+        out = run_gpu(f)
+        check(f, out, ref, None)
+        assert np.count_nonzero(ref == smax) > 0 and np.count_nonzero(ref == smin) > 0
 
 
 # ---- the correctly rounded log ------------------------------------------------------------------------------

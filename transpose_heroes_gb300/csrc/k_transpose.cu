@@ -611,6 +611,8 @@ struct __align__(16) QuantSmem {
   float inv[kQT];    // RN(1 / output scale)
   int zout[kQT];
   int zinm[kQT];     // kMagicBits - input zero point: code + zinm = bits of (1.5*2^23 + code - zp)
+  float nzin[kQT];   // -(1.5*2^23 + 128 + input zero point), exact
+  float mout[kQT];   // 1.5*2^23 + output zero point, exact
 };
 
 // Ragged or unaligned tile, byte by byte (kept out of line: it is rare and large).
@@ -764,6 +766,96 @@ __device__ __forceinline__ void quant_rows(uint4 (&v)[4], int r0, int c, const Q
   for (int k = 0; k < 4; ++k) v[k] = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
 }
 
+// Dequantize -> quantize of four 16-byte row chunks without a float chain, for finite parameters with
+// |scale_in / scale_out| < 2^13 (so |y| < 2^21 below). Per code:
+//  * d = code - zp exactly: after flipping the sign bits, the byte (code + 128) becomes the low byte of
+//    the f32 1.5*2^23, and subtracting 1.5*2^23 + 128 + zp is exact;
+//  * real = RN(scale_in * d), as the definition has it; y = RN(real * RN(1/scale_out)) lies within
+//    1.5*2^-23 (1 + 2^-22) |y| of the IEEE quotient RN(real / scale_out), so y(1 - 2^-22) and
+//    y(1 + 2^-22) bracket it;
+//  * t± = RN(y(1 ± 2^-22) + M) with M = 1.5*2^23 + zp_out (one FMA each) is M + the nearest integer to
+//    y(1 ± 2^-22). When t+ = t-, no half-integer lies in the bracket (an end can be one only for
+//    |y| >= 2^21, where the clamp decides anyway), so rint(quotient) + zp_out = bits(t) - bits(1.5*2^23).
+// cvt.pack.sat saturates to [-128, 127]; CLAMP adds a narrower storage range. Words holding a code whose
+// bracket contained a half-integer (about 1 in 10^4 at |y| ~ 100) are redone with the exact definition.
+template <int QIN, int QOUT, bool CLAMP>
+__device__ __forceinline__ void quant_rows_bracket(uint4 (&v)[4], int r0, int c, const QuantTilePlan& p,
+                                                   const QuantSmem& q) {
+  float rs[4], rz[4], ri[4], rm[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int row = r0 + 32 * k;
+    rs[k] = QIN == 0 ? q.sin_[row] : p.qin.scale;
+    rz[k] = QIN == 0 ? q.nzin[row] : -(kMagic + 128.0f + (float)p.qin.zp);
+    ri[k] = QOUT == 0 ? q.inv[row] : p.qout.inv_scale;
+    rm[k] = QOUT == 0 ? q.mout[row] : kMagic + (float)p.qout.zp;
+  }
+  const int smin = p.qout.smin, smax = p.qout.smax;
+  const float2 kp = make_float2(1.0f + 0x1p-22f, 1.0f + 0x1p-22f), km = make_float2(1.0f - 0x1p-22f, 1.0f - 0x1p-22f);
+  uint32_t o[4][4];
+  uint32_t redo = 0u;  // bit 4k + m: word m of chunk k
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    uint32_t hi[4], dw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int b = 2; b >= 0; b -= 2) {  // codes 2, 3 first: their pack is the upper half of the word
+      const int jl = 16 * c + 4 * m + b;
+      float2 cs = make_float2(0.f, 0.f), cz = cs, ci = cs, cm = cs;
+      if (QIN == 1) {
+        cs = *reinterpret_cast<const float2*>(&q.sin_[jl]);
+        cz = *reinterpret_cast<const float2*>(&q.nzin[jl]);
+      }
+      if (QOUT == 1) {
+        ci = *reinterpret_cast<const float2*>(&q.inv[jl]);
+        cm = *reinterpret_cast<const float2*>(&q.mout[jl]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w = word_of(v[k], m) ^ 0x80808080u;
+        const float2 e = make_float2(__uint_as_float(__byte_perm(w, (uint32_t)kMagicBits, 0x7650u | b)),
+                                     __uint_as_float(__byte_perm(w, (uint32_t)kMagicBits, 0x7650u | (b + 1))));
+        const float2 df = __fadd2_rn(e, QIN == 1 ? cz : make_float2(rz[k], rz[k]));
+        const float2 real = __fmul2_rn(QIN == 1 ? cs : make_float2(rs[k], rs[k]), df);
+        const float2 y = __fmul2_rn(real, QOUT == 1 ? ci : make_float2(ri[k], ri[k]));
+        const float2 mm = QOUT == 1 ? cm : make_float2(rm[k], rm[k]);
+        const float2 tp = __ffma2_rn(y, kp, mm), tm = __ffma2_rn(y, km, mm);
+        dw[k] |= (__float_as_uint(tp.x) ^ __float_as_uint(tm.x)) | (__float_as_uint(tp.y) ^ __float_as_uint(tm.y));
+        int q0 = __float_as_int(tp.x) - kMagicBits, q1 = __float_as_int(tp.y) - kMagicBits;
+        if (CLAMP) {
+          q0 = min(max(q0, smin), smax);
+          q1 = min(max(q1, smin), smax);
+        }
+        if (b == 2) asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi[k]) : "r"(q1), "r"(q0));
+        else asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(o[k][m]) : "r"(q1), "r"(q0), "r"(hi[k]));
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) redo |= (dw[k] != 0u ? 1u : 0u) << (4 * k + m);
+  }
+#pragma unroll 1
+  while (redo) {  // rare: the exact definition decides the word's four codes
+    const int e = __ffs(redo) - 1;
+    redo &= redo - 1;
+    const int k = e >> 2, m = e & 3, row = r0 + 32 * k;
+    const uint32_t w = word_of(v[k], m);
+    uint32_t res = 0u;
+    for (int b = 0; b < 4; ++b) {
+      float sin, sout, inv;
+      int zin, zout;
+      quant_params<QIN, QOUT, false>(row, 16 * c + 4 * m + b, p, q, sin, zin, sout, inv, zout);
+      const int code = (int)(int8_t)(w >> (8 * b));
+      res |= ((uint32_t)quant_code_exact(dequant(code, sin, zin), sout, zout, smin, smax) & 0xFFu) << (8 * b);
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)  // static indices keep o in registers
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm)
+        if (kk == k && mm == m) o[kk][mm] = res;
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
+}
+
 template <int QIN, int QOUT, bool OPS>
 __global__ void __launch_bounds__(256, 4) quant_tile_kernel(QuantTilePlan p, int64_t ntj) {
   __shared__ __align__(16) uint32_t tile[kQT * kQT / 4];  // 128 rows x 32 words, word column swizzled
@@ -773,20 +865,29 @@ __global__ void __launch_bounds__(256, 4) quant_tile_kernel(QuantTilePlan p, int
   const int64_t i0 = ti * kQT, j0 = tj * kQT;
   const int64_t n0 = p.n0, n1 = p.n1;
   // stage the per-axis parameters of this tile
+  bool bad = false;
   if (t < kQT) {
     const int64_t i = i0 + t, j = j0 + t;
     if (p.qin.axis == 0 && i < n0) { q.sin_[t] = p.qin.scales[i]; q.zin[t] = p.qin.zps[i]; }
     if (p.qin.axis == 1 && j < n1) { q.sin_[t] = p.qin.scales[j]; q.zin[t] = p.qin.zps[j]; }
-    if (p.qin.axis >= 0 && (p.qin.axis == 0 ? i < n0 : j < n1)) q.zinm[t] = kMagicBits - q.zin[t];
+    float a = fabsf(p.qin.scale), b = fabsf(p.qout.inv_scale);
+    if (p.qin.axis >= 0 && (p.qin.axis == 0 ? i < n0 : j < n1)) {
+      q.zinm[t] = kMagicBits - q.zin[t];
+      q.nzin[t] = -(kMagic + 128.0f + (float)q.zin[t]);
+      a = fabsf(q.sin_[t]);
+    }
     const int64_t k = p.qout.axis == 0 ? i : j;
     if (p.qout.axis >= 0 && k < (p.qout.axis == 0 ? n0 : n1)) {
       const float s = p.qout.scales[k];
       q.sout[t] = s;
       q.inv[t] = __frcp_rn(s);
       q.zout[t] = p.qout.zps[k];
+      q.mout[t] = kMagic + (float)q.zout[t];
+      b = fabsf(q.inv[t]);
     }
+    bad = !(a < 0x1p60f && b < 0x1p60f && a * b < 8192.0f);  // outside quant_rows_bracket's range
   }
-  __syncthreads();
+  const int slow = __syncthreads_or(bad);
   const bool full = (i0 + kQT <= n0) && (j0 + kQT <= n1) && (n0 % 16 == 0) && (n1 % 16 == 0) &&
                     ((uintptr_t)p.in % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
   if (!full) {
@@ -803,7 +904,12 @@ __global__ void __launch_bounds__(256, 4) quant_tile_kernel(QuantTilePlan p, int
                  : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
                  : "l"(src));
   }
-  quant_rows<QIN, QOUT, OPS>(v, t >> 3, t & 7, p, q);  // rows t/8 + 32k, chunk t%8
+  if (!OPS && !slow) {  // rows t/8 + 32k, chunk t%8
+    if (p.qout.smin > -128 || p.qout.smax < 127) quant_rows_bracket<QIN, QOUT, true>(v, t >> 3, t & 7, p, q);
+    else quant_rows_bracket<QIN, QOUT, false>(v, t >> 3, t & 7, p, q);
+  } else {
+    quant_rows<QIN, QOUT, OPS>(v, t >> 3, t & 7, p, q);
+  }
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int qd = t + 256 * k, row = qd >> 3, c = qd & 7;
