@@ -769,14 +769,17 @@ extern "C" float orc_dequantize(const orc_quant* q, int32_t code, const int64_t*
 // cand[i] (bit pattern of a claimed correctly rounded f32 log) with the oracle's value. NaN results
 // match any NaN pattern. Returns the number of mismatches; the first max_report mismatching input
 // patterns (in ascending order) are written to report.
-extern "C" int64_t orc_check_log_f32(uint32_t first_bits, int64_t count, const uint32_t* cand,
-                          uint32_t* report, int64_t max_report) {
+// Counts the candidates (f32 bit patterns of f(x) for the consecutive inputs x starting at first_bits)
+// that differ from the oracle's correctly rounded f32 value; any NaN matches a NaN.
+template <double (*F)(double, int)>
+static int64_t check_f32(uint32_t first_bits, int64_t count, const uint32_t* cand, uint32_t* report,
+                         int64_t max_report) {
   std::vector<uint8_t> bad_flag((size_t)count, 0);
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < count; ++i) {
     uint32_t b = first_bits + (uint32_t)i;
     float x; std::memcpy(&x, &b, 4);
-    float y = (float)cr_log(x, ORC_F32);
+    float y = (float)F(x, ORC_F32);
     uint32_t yb; std::memcpy(&yb, &y, 4);
     bool cand_nan = (cand[i] & 0x7F800000u) == 0x7F800000u && (cand[i] & 0x7FFFFFu) != 0;
     bool same = std::isnan(y) ? cand_nan : yb == cand[i];
@@ -789,6 +792,16 @@ extern "C" int64_t orc_check_log_f32(uint32_t first_bits, int64_t count, const u
     ++bad;
   }
   return bad;
+}
+
+extern "C" int64_t orc_check_log_f32(uint32_t first_bits, int64_t count, const uint32_t* cand,
+                                     uint32_t* report, int64_t max_report) {
+  return check_f32<cr_log>(first_bits, count, cand, report, max_report);
+}
+
+extern "C" int64_t orc_check_exp_f32(uint32_t first_bits, int64_t count, const uint32_t* cand,
+                                     uint32_t* report, int64_t max_report) {
+  return check_f32<cr_exp>(first_bits, count, cand, report, max_report);
 }
 
 extern "C" void orc_set_num_threads(int n) {

@@ -312,8 +312,8 @@ def test_transpose_rank3_all_perms_and_layouts(dtype):
 
 
 def test_transpose_emitter_example_exp_abs():
-    """The transpose-emitter example: f32[20,160,170] -> exp -> transpose {2,1,0} -> abs. exp here is CUDA's
-    expf (not correctly rounded), so the bar is 2 ulp, not bit equality."""
+    """The transpose-emitter example: f32[20,160,170] -> exp -> transpose {2,1,0} -> abs, bit-exact (exp
+    is correctly rounded on both sides)."""
     g = inp.rng(21)
     dims = [20, 160, 170]
     data = inp.uniform_f32(g, int(np.prod(dims)), -3, 3)
@@ -321,9 +321,35 @@ def test_transpose_emitter_example_exp_abs():
                    permutation=[2, 1, 0], prologue={"ops": ["exp"]}, epilogue={"ops": ["abs"]},
                    out_dims=[170, 160, 20], out_m2m=[2, 1, 0], out_dtype="f32")
     ref, _ = run_oracle(f)
-    gpu = run_gpu(f)
-    ulps = np.abs(gpu.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
-    assert ulps.max() <= 2
+    check(f, run_gpu(f), ref, None)
+
+
+def _gpu_exp_bits(first: int, count: int) -> np.ndarray:
+    x = torch.arange(first, first + count, dtype=torch.int64, device="cuda").to(torch.int32).view(torch.float32)
+    y = torch.empty_like(x)
+    hf.transpose_fusion(x, [count], "f32", [0], y, prologue={"ops": ["exp"]})
+    torch.cuda.synchronize()
+    return y.view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+def test_exp_exhaustive():
+    """Every f32 whose exp is neither 0 nor inf after rounding, both signs (x in [-104, 89]), plus the
+    ends of the range, bit-exact against the oracle's correctly rounded exp."""
+    chunk = 1 << 27
+    total_bad, examples = 0, []
+    for lo, hi in ((0x00000000, 0x42B20000), (0x80000000, 0xC2D00000)):  # +0 .. 89.0, -0 .. -104.0
+        for first in range(lo, hi, chunk):
+            n = min(chunk, hi - first)
+            start = first - (1 << 32) if first >= 1 << 31 else first
+            bad, ex = oracle.check_exp_f32(first, _gpu_exp_bits(start, n))
+            total_bad += bad
+            examples += ex
+    for first in (0x42B20000, 0x7F7F0000, 0x7F800000, 0xC2D00000, 0xFF7F0000, 0xFF800000):  # past the range
+        start = first - (1 << 32) if first >= 1 << 31 else first
+        bad, ex = oracle.check_exp_f32(first, _gpu_exp_bits(start, 1 << 16))
+        total_bad += bad
+        examples += ex
+    assert total_bad == 0, [hex(v) for v in examples[:16]]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "s8"])

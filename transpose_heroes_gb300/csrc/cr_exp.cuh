@@ -1,0 +1,78 @@
+// Correctly rounded f32 exp ("StableHLO Specification", section "exponential": the IEEE-754 exp of
+// the element type; rounding to nearest even of the exact value).
+//
+// Stage 1: CUDA's double exp, documented within 1 double ulp, rounded once to f32. That rounding is
+// the correct one unless the double lies within 3 double ulps of an f32 rounding boundary (a
+// midpoint between two floats), which happens for about 2^-26 of the arguments.
+// Stage 2 (those, and NaN): a double-double evaluation after Tang ("Table-driven implementation of
+// the exponential function in IEEE floating-point arithmetic", ACM TOMS 15(2), 1989):
+//   k = rint(64 x / ln2) = 64 e + j,  r = x - k ln2/64 (as a double-double, exactly up to 2^-94),
+//   exp x = 2^e * 2^(j/64) * exp(r),  exp(r) = 1 + r + r^2/2 + r^3 P(r),
+// P the Taylor polynomial to r^6/7! (|r| < 2^-7.4, so the truncation is below 2^-97), with every
+// rounding error below 2^-74 relative; the nearer float of that value is returned.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "cr_log.cuh"  // double-double helpers
+#include "exp_table.inc"
+
+namespace hlo {
+
+static __device__ __noinline__ float cr_expf_dd(float x) {
+  if (x != x) return x;                      // NaN
+  if (x > 89.0f) return __int_as_float(0x7F800000);  // exp > 2^128: +inf
+  if (x < -104.0f) return 0.0f;              // exp < 2^-150: rounds to +0
+  const double xd = (double)x;
+  const double kd = rint(__dmul_rn(xd, HLO_EXP_INV64_LN2));
+  const int k = (int)kd;
+  const double a = __fma_rn(-kd, HLO_EXP_L1, xd);  // exact: k L1 has at most 53 bits, |a| < 2^-6
+  const dd p2 = dd_two_prod(kd, HLO_EXP_L2);        // k L2 exactly
+  dd r = dd_two_sum(a, -p2.hi);
+  r.lo = __dsub_rn(__dsub_rn(r.lo, p2.lo), __dmul_rn(kd, HLO_EXP_L3));
+  r = dd_fast_two_sum(r.hi, r.lo);
+  const double rh = r.hi, rl = r.lo;
+  // r^3 (1/3! + r/4! + r^2/5! + r^3/6! + r^4/7!) in double (rl's share is below 2^-75)
+  double p = 1.0 / 5040.0;
+  p = __fma_rn(p, rh, 1.0 / 720.0);
+  p = __fma_rn(p, rh, 1.0 / 120.0);
+  p = __fma_rn(p, rh, 1.0 / 24.0);
+  p = __fma_rn(p, rh, 1.0 / 6.0);
+  const double q = __dmul_rn(__dmul_rn(__dmul_rn(rh, rh), rh), p);
+  // 1 + rh + rh^2/2 exactly as three double-doubles, then the small terms
+  const dd sq = dd_two_prod(rh, rh);
+  const dd s1 = dd_fast_two_sum(1.0, rh);
+  const dd s2 = dd_two_sum(s1.hi, __dmul_rn(sq.hi, 0.5));
+  double small = __dadd_rn(s1.lo, s2.lo);
+  small = __dadd_rn(small, rl);
+  small = __dadd_rn(small, __fma_rn(rh, rl, __dmul_rn(sq.lo, 0.5)));
+  small = __dadd_rn(small, q);
+  const dd e = dd_fast_two_sum(s2.hi, small);
+  // times 2^(j/64) (double-double) and 2^(k >> 6)
+  const double2 t = kExpT[k & 63];
+  const dd pr = dd_two_prod(t.x, e.hi);
+  const double lo = __dadd_rn(pr.lo, __fma_rn(t.x, e.lo, __dmul_rn(t.y, e.hi)));
+  dd y = dd_fast_two_sum(pr.hi, lo);
+  const double scale = __hiloint2double((1023 + (k >> 6)) << 20, 0);  // 2^e, e in [-163, 128]
+  y.hi = __dmul_rn(y.hi, scale);
+  y.lo = __dmul_rn(y.lo, scale);
+  const float f = __double2float_rn(y.hi);
+  if (isinf(f)) return f;
+  return dd_to_f32_rn(y);
+}
+
+__device__ __forceinline__ float cr_expf(float x) {
+  const double y = exp((double)x);
+  if (y >= 0x1p-126) {  // normal f32 range (and +inf): the boundary is at 2^28 in the 29 low bits
+    const uint32_t low = (uint32_t)__double_as_longlong(y) & 0x1FFFFFFFu;
+    if (low - (0x10000000u - 3u) > 6u) return __double2float_rn(y);
+  } else if (y >= 0.0) {  // subnormal or zero f32: boundaries at odd multiples of 2^-150
+    const double s = __dmul_rn(y, 0x1p149);  // exact
+    const double fr = __dsub_rn(s, floor(s));
+    if (fabs(__dsub_rn(fr, 0.5)) > __dmul_rn(s, 0x1p-50)) return __double2float_rn(y);
+  }
+  return cr_expf_dd(x);
+}
+
+}  // namespace hlo

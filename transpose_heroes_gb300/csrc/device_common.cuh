@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "cr_exp.cuh"
 #include "cr_log.cuh"
 #include "hlo_internal.h"
 
@@ -84,7 +85,8 @@ struct LogTab {
 };
 __device__ __forceinline__ LogTab global_log_tables() { return {kLogCTab, kLogETab}; }
 
-// One elementwise op. FAST_EXP selects the SFU exp (reductions) or CUDA's expf (elsewhere).
+// One elementwise op. FAST_EXP selects the SFU exp (reductions) or the correctly rounded exp
+// (elsewhere; CUDA's expf settles the 16-bit types).
 // Correct rounding into a 16-bit float type from an f32 approximation y of f(x) with an error of at
 // most 2 f32 ulps: if y - 2 ulp and y + 2 ulp round alike, so does f(x) (rounding is monotone).
 // Returns false (and leaves r unset) when they do not, or when y sits next to 0, the subnormals or
@@ -125,7 +127,7 @@ __device__ __forceinline__ float apply_op(int op, float v, float b, float x, flo
   switch (op) {
     case OP_EXP:
       if (FAST_EXP) return fast_exp(v);
-      if (!r16) return expf(v);
+      if (!r16) return cr_expf(v);
       return round16_settled(expf(v), dt, r) ? r : exp_round16_slow(v, dt);
     case OP_LOG:
       if (!r16) return cr_logf(v, lt.c, lt.e);
