@@ -102,6 +102,9 @@ def lib():
             h.orc_check_exp_f32.argtypes = [ctypes.c_uint32, ctypes.c_int64, ctypes.c_void_p,
                                             ctypes.c_void_p, ctypes.c_int64]
             h.orc_check_exp_f32.restype = ctypes.c_int64
+            h.orc_check_tanh_f32.argtypes = [ctypes.c_uint32, ctypes.c_int64, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_int64]
+            h.orc_check_tanh_f32.restype = ctypes.c_int64
             h.orc_unresolved_count.restype = ctypes.c_int
             h.orc_set_num_threads.argtypes = [ctypes.c_int]
             h.orc_max_threads.restype = ctypes.c_int
@@ -350,6 +353,15 @@ def check_exp_f32(first_bits: int, cand_bits: np.ndarray, max_report: int = 16):
     cand = np.ascontiguousarray(cand_bits, dtype=np.uint32)
     report = np.zeros(max_report, dtype=np.uint32)
     bad = lib().orc_check_exp_f32(first_bits, cand.size, cand.ctypes.data, report.ctypes.data, max_report)
+    return int(bad), report[: min(bad, max_report)].tolist()
+
+
+def check_tanh_f32(first_bits: int, cand_bits: np.ndarray, max_report: int = 16):
+    """Count mismatches between cand_bits (uint32 patterns of f32 tanh results for consecutive inputs
+    starting at first_bits) and the oracle's correctly rounded tanh. Returns (count, examples)."""
+    cand = np.ascontiguousarray(cand_bits, dtype=np.uint32)
+    report = np.zeros(max_report, dtype=np.uint32)
+    bad = lib().orc_check_tanh_f32(first_bits, cand.size, cand.ctypes.data, report.ctypes.data, max_report)
     return int(bad), report[: min(bad, max_report)].tolist()
 
 

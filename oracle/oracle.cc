@@ -799,6 +799,11 @@ extern "C" int64_t orc_check_log_f32(uint32_t first_bits, int64_t count, const u
   return check_f32<cr_log>(first_bits, count, cand, report, max_report);
 }
 
+extern "C" int64_t orc_check_tanh_f32(uint32_t first_bits, int64_t count, const uint32_t* cand,
+                                      uint32_t* report, int64_t max_report) {
+  return check_f32<cr_tanh>(first_bits, count, cand, report, max_report);
+}
+
 extern "C" int64_t orc_check_exp_f32(uint32_t first_bits, int64_t count, const uint32_t* cand,
                                      uint32_t* report, int64_t max_report) {
   return check_f32<cr_exp>(first_bits, count, cand, report, max_report);

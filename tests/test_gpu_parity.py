@@ -542,15 +542,40 @@ def test_gelu_loop_fusion_sizes(dims):
     check(f, run_gpu(f), ref, None)
 
 
-def test_f32_tanh_within_two_ulp():
-    g = np.random.default_rng(11)
-    x = np.concatenate([g.uniform(-10, 10, 200000), g.uniform(-1e-3, 1e-3, 1000)]).astype(np.float32)
-    f = _chain_fusion(x, "f32", ["tanh"])
+def test_gelu_chain_f32_bit_exact():
+    """The same GELU chain on f32 (every op, tanh included, correctly rounded on both sides): bit-exact."""
+    g = np.random.default_rng(13)
+    x = np.concatenate([g.standard_normal(1 << 20), g.uniform(-12, 12, 1 << 16)]).astype(np.float32)
+    f = _chain_fusion(x, "f32", list(inp.GELU_CHAIN))
     ref, _ = run_oracle(f)
-    got = run_gpu(f)
-    ulp = np.abs(np.spacing(ref.astype(np.float32)))
-    # within 2 ulp of the exact tanh, so within 2.5 ulp of its correct rounding
-    assert np.all(np.abs(got.astype(np.float64) - ref.astype(np.float64)) <= 2.5 * ulp)
+    check(f, run_gpu(f), ref, None)
+
+
+def _gpu_unary_bits(op: str, first: int, count: int) -> np.ndarray:
+    x = torch.arange(first, first + count, dtype=torch.int64, device="cuda").to(torch.int32).view(torch.float32)
+    y = torch.empty_like(x)
+    hf.transpose_fusion(x, [count], "f32", [0], y, prologue={"ops": [op]})
+    torch.cuda.synchronize()
+    return y.view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+def test_f32_tanh_exhaustive():
+    """Every f32 in [0, 10] (tanh rounds to 1 beyond 9.02; the GPU evaluates |x| and restores the sign),
+    a run of negative inputs, and the ends of the range, bit-exact against the oracle's correctly
+    rounded tanh."""
+    chunk = 1 << 27
+    total_bad, examples = 0, []
+    hi = 0x41200000  # 10.0
+    for first in range(0, hi, chunk):
+        bad, ex = oracle.check_tanh_f32(first, _gpu_unary_bits("tanh", first, min(chunk, hi - first)))
+        total_bad += bad
+        examples += ex
+    for first in (0xBF000000, 0x80000000, 0x7F7F0000, 0x7F800000, 0xFF7F0000, 0xFF800000):
+        start = first - (1 << 32) if first >= 1 << 31 else first
+        bad, ex = oracle.check_tanh_f32(first, _gpu_unary_bits("tanh", start, 1 << 20))
+        total_bad += bad
+        examples += ex
+    assert total_bad == 0, [hex(v) for v in examples[:16]]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -133,7 +133,7 @@ __device__ __forceinline__ float apply_op(int op, float v, float b, float x, flo
       if (!r16) return cr_logf(v, lt.c, lt.e);
       return round16_settled(cr_logf(v, lt.c, lt.e), dt, r) ? r : log_round16_slow(v, dt);
     case OP_TANH:
-      if (!r16) return tanhf(v);
+      if (!r16) return cr_tanhf(v);
       return round16_settled(tanhf(v), dt, r) ? r : tanh_round16_slow(v, dt);
     case OP_ABS: return fabsf(v);
     case OP_NEG: return -v;
