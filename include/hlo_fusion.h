@@ -26,8 +26,9 @@
  *  - On any error nothing is enqueued, except HLO_ERR_CUDA, which reports a failed launch.
  *    hlo_last_error() returns a thread-local message naming the violated constraint.
  *  - Floating point: reductions accumulate in f32; the order of accumulation is implementation
- *    defined, as the reduce semantics allow ("StableHLO Specification", section "reduce"). log is
- *    correctly rounded in f32; transposes, layout changes and quantization are bit-exact.
+ *    defined, as the reduce semantics allow ("StableHLO Specification", section "reduce"). exp, log
+ *    and tanh are correctly rounded; transposes, layout changes, elementwise chains and quantization
+ *    are bit-exact.
  */
 #ifndef HLO_FUSION_H
 #define HLO_FUSION_H
@@ -80,10 +81,9 @@ typedef struct {
  * loop fusion of "XLA:GPU Emitters" (section "Loop emitter") is
  *   MUL_INPUT, MUL_INPUT, MUL_CONST 0.044708, ADD_INPUT, MUL_CONST 0.79785, TANH, ADD_CONST 1,
  *   MUL_CONST 0.5, MUL_INPUT.
- * Rounding: log is correctly rounded; exp and tanh are correctly rounded for bf16/f16 results and
- * within 2 ulp for f32 results (CUDA's expf, tanhf), except that a reduce prologue's exp of bf16 may
- * use a faster exp whose rare one-ulp differences stay inside the reduction's tolerance; the other
- * ops are exact IEEE operations. */
+ * Rounding: exp, log and tanh are correctly rounded to the element type (f32, bf16, f16), except
+ * that a float reduction's exp prologue uses a faster exp whose rare one-ulp differences stay inside
+ * the reduction's tolerance; the other ops are exact IEEE operations. */
 typedef enum {
   HLO_EW_EXP = 1,
   HLO_EW_LOG = 2,
