@@ -542,6 +542,24 @@ def test_gelu_loop_fusion_sizes(dims):
     check(f, run_gpu(f), ref, None)
 
 
+@pytest.mark.parametrize("dtype,ops", [("bf16", list(inp.GELU_CHAIN)),
+                                       ("f16", ["exp", ("mul_const", 0.5), "tanh", "log"])])
+def test_chain_table_every_16bit_input(dtype, ops):
+    """Inputs large enough for the table kernel (16-bit chains of 2^22 elements or more): every bit
+    pattern 64 times over plus a ragged tail, bit-exact against the oracle."""
+    pats = np.arange(1 << 16, dtype=np.uint16)
+    data = np.concatenate([np.tile(pats, 64), pats[:13]])
+    f = _chain_fusion(data, dtype, ops)
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+    # f32 intermediates (one rounding at the end): the table is built with the per-element code
+    n = len(data)
+    f = inp.Fusion(name="chain_f32mid", kind="transpose", dims=[n], m2m=[0], dtype=dtype, data=data, permutation=[0],
+                   prologue={"ops": ops, "round_each": False}, out_dims=[n], out_m2m=[0], out_dtype=dtype)
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
 def test_gelu_chain_f32_bit_exact():
     """The same GELU chain on f32 (every op, tanh included, correctly rounded on both sides): bit-exact."""
     g = np.random.default_rng(13)

@@ -1,7 +1,11 @@
 // Elementwise kernel for fusions whose transpose is the identity on memory (same physical order in and
 // out): the loop emitter of "XLA:GPU Emitters" (section "Loop emitter": a linear walk over the output
 // so that writes are coalesced, with vectorized loads and stores, section "Vectorization").
+#include <cooperative_groups.h>
+
 #include "device_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace hlo {
 
@@ -252,6 +256,121 @@ static bool chain16x2_ok(const Chain& pro, const Chain& epi, int dt) {
   return true;
 }
 
+// ---- 16-bit chains as a table of all 65536 inputs ------------------------------------------------
+// A chain on a 16-bit input with a 16-bit result (no broadcast operand) is a function of the input's
+// bits alone, so a large input is served from a table of its 65536 results held in shared memory
+// (128 KiB per block, one block of 1024 threads per SM). A cluster of kLutCluster blocks builds the
+// table together: each block evaluates 1/kLutCluster of the entries with the per-element code
+// (ew_apply, every op rounded to the element type) and writes them into the shared memory of every
+// block of its cluster (distributed shared memory); after the cluster barrier each block streams
+// 16-byte vectors and looks every element up locally. The table costs 65536 / kLutCluster
+// evaluations per block, no global memory beyond the input and output.
+constexpr int kLutCluster = 8;
+constexpr int kLutThreads = 1024;
+constexpr int kLutEntries = 1 << 16;
+constexpr int64_t kLutMinElems = int64_t(1) << 22;  // below this the direct kernels are faster
+
+template <int DT>
+__device__ __forceinline__ uint32_t lut_entry(const EwPlan& p, uint32_t bits, const LogTab& lt) {
+  const float x = DT == BF16 ? bf16_bits_to_f32(bits) : f16_bits_to_f32((uint16_t)bits);
+  const float v = round_to_dt(ew_apply(p, x, lt), DT);
+  return DT == BF16 ? f32_to_bf16_bits(v) : f32_to_f16_bits(v);
+}
+
+__device__ __forceinline__ uint32_t lut_pair(const uint16_t* lut, uint32_t w) {
+  return (uint32_t)lut[w & 0xFFFFu] | ((uint32_t)lut[w >> 16] << 16);
+}
+
+// PACKED: the chain qualifies for the packed pair evaluation (chain16x2), used for the table too.
+template <int DT, bool PACKED>
+__global__ void __launch_bounds__(kLutThreads, 1) elementwise_lut16_kernel(EwPlan p) {
+  extern __shared__ __align__(16) uint16_t lut[];  // kLutEntries results
+  cg::cluster_group cluster = cg::this_cluster();
+  const LogTab lt = global_log_tables();
+  {  // this block's share of the table: eight consecutive entries per thread, copied to every block
+    const int first = (int)cluster.block_rank() * (kLutEntries / kLutCluster) + 8 * (int)threadIdx.x;
+    uint32_t w[4];
+    if (PACKED) {
+      uint32_t x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = w[i] = (uint32_t)(first + 2 * i) | ((uint32_t)(first + 2 * i + 1) << 16);
+      chain16x2<DT, 4>(p.pro, w, x, lt);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = lut_entry<DT>(p, first + 2 * i, lt) | (lut_entry<DT>(p, first + 2 * i + 1, lt) << 16);
+    }
+    const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
+#pragma unroll
+    for (int d = 0; d < kLutCluster; ++d)
+      *reinterpret_cast<uint4*>(cluster.map_shared_rank(lut, d) + first) = v;
+  }
+  cluster.sync();  // every block's table is complete; no shared-memory access crosses blocks after this
+  const uint16_t* in = reinterpret_cast<const uint16_t*>(p.in);
+  uint16_t* out = reinterpret_cast<uint16_t*>(p.out);
+  const int64_t nv = p.n / 8;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  constexpr int kU = 4;  // vectors in flight per thread
+  for (int64_t v0 = tid; v0 < nv; v0 += kU * stride) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nv)
+        asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(x[u].x), "=r"(x[u].y), "=r"(x[u].z), "=r"(x[u].w)
+                     : "l"(reinterpret_cast<const uint4*>(in) + v));
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nv)
+        reinterpret_cast<uint4*>(out)[v] =
+            make_uint4(lut_pair(lut, x[u].x), lut_pair(lut, x[u].y), lut_pair(lut, x[u].z), lut_pair(lut, x[u].w));
+    }
+  }
+  for (int64_t e = nv * 8 + tid; e < p.n; e += stride) out[e] = lut[in[e]];
+}
+
+static bool lut16_ok(const Chain& pro, const Chain& epi, int dt, int64_t n) {
+  if ((dt != BF16 && dt != F16) || n < kLutMinElems) return false;
+  bool costly = false;
+  for (const Chain* c : {&pro, &epi})
+    for (int k = 0; k < c->n; ++k) {
+      if (c->op[k] == OP_ADD_BCAST) return false;
+      if (c->op[k] == OP_EXP || c->op[k] == OP_LOG || c->op[k] == OP_TANH) costly = true;
+    }
+  return costly;
+}
+
+template <int DT, bool PACKED>
+static cudaError_t lut16_launch(const EwPlan& p, cudaStream_t s) {
+  const size_t smem = kLutEntries * sizeof(uint16_t);
+  auto kernel = elementwise_lut16_kernel<DT, PACKED>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kLutCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kLutThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  cfg.gridDim = dim3(kLutCluster, 1, 1);
+  if (cudaOccupancyMaxActiveClusters(&clusters, (void*)kernel, &cfg) != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    clusters = 1;
+  }
+  cfg.gridDim = dim3((unsigned)(clusters * kLutCluster), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // Pure data movement with identical memory order: raw bytes, 16 at a time where aligned.
 __global__ void __launch_bounds__(256) copy_bytes_kernel(const uint8_t* in, uint8_t* out, int64_t nbytes, bool vec) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -290,6 +409,9 @@ cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, con
     const bool vec = ((uintptr_t)in % 16 == 0) && ((uintptr_t)out % 16 == 0);
     if (vec) elementwise_f32_kernel<true><<<(unsigned)blocks, 256, 0, s>>>(p);
     else elementwise_f32_kernel<false><<<(unsigned)blocks, 256, 0, s>>>(p);
+  } else if (lut16_ok(pro, epi, dt, n) && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0) {
+    if (chain16x2_ok(pro, epi, dt)) return dt == BF16 ? lut16_launch<BF16, true>(p, s) : lut16_launch<F16, true>(p, s);
+    return dt == BF16 ? lut16_launch<BF16, false>(p, s) : lut16_launch<F16, false>(p, s);
   } else if (chain16x2_ok(pro, epi, dt) && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0) {
     int64_t vblocks = (n / 16 + 255) / 256;
     const int64_t vcap = (int64_t)device_sm_count() * 8;
