@@ -711,6 +711,23 @@ def test_quant_binary_every_code_pair(op):
         assert np.array_equal(got, ref), f"{int((got != ref).sum())} codes differ (shift {shift})"
 
 
+@pytest.mark.parametrize("op", ["add", "divide", "maximum", "minimum", "multiply"])
+def test_quant_binary_table_every_code_pair(op):
+    """Inputs large enough for the pair-table kernel (2^22 elements or more): all 65536 code pairs 64
+    times over plus a ragged tail, bit-exact against the oracle."""
+    codes = np.arange(-128, 128, dtype=np.int8)
+    a0, b0 = np.repeat(codes, 256), np.tile(codes, 256)
+    a = np.concatenate([np.tile(a0, 64), a0[:13]])
+    b = np.concatenate([np.tile(b0, 64), b0[7:20]])
+    ql, qr, qo = _qpt(0.0371, 4), _qpt(0.113, -9), _qpt(0.09, 2, -100, 120)
+    ref = oracle.quant_binary(op, a, b, [a.size], ql, qr, qo)
+    out = torch.empty(a.size, dtype=torch.int8, device="cuda")
+    hf.quant_binary(op, torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), [a.size], ql, qr, out, qo)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} codes differ"
+
+
 def test_quant_binary_layouts_and_sizes():
     g = np.random.default_rng(41)
     dims = [37, 53, 5]

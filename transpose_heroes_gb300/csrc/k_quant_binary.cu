@@ -2,7 +2,11 @@
 // op, quantize ("StableHLO Specification": dequantize_op_quantize(op, lhs, rhs, type(result)) for
 // add, divide, maximum, minimum, multiply). Same layout everywhere: 16 codes per 16-byte vector;
 // otherwise a thread per element with index maps.
+#include <cooperative_groups.h>
+
 #include "quant_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace hlo {
 
@@ -63,10 +67,103 @@ __global__ void __launch_bounds__(256) quant_binary_map_kernel(QuantBinaryPlan p
     p.out[map_index(p.omap, i)] = (int8_t)qbin<OP>(p.lhs[map_index(p.lmap, i)], p.rhs[map_index(p.rmap, i)], p);
 }
 
+// Large same-layout inputs: the result depends on the two codes alone, so it is read from a table of
+// all 256 x 256 code pairs (64 KiB of shared memory per block). A cluster of kQbCluster blocks builds
+// the table together, each block computing 1/kQbCluster of the pairs with qbin and writing them into
+// every block of the cluster through distributed shared memory; after the cluster barrier each block
+// streams 16-byte vectors of both operands and looks every pair up locally. No global memory beyond
+// the operands and the result.
+constexpr int kQbCluster = 8;
+constexpr int kQbThreads = 1024;
+constexpr int kQbEntries = 1 << 16;
+constexpr int64_t kQbTableMinElems = int64_t(1) << 22;
+
+// Four results for the four code pairs of two words; the table index is (lhs byte << 8) | rhs byte.
+__device__ __forceinline__ uint32_t qb_lookup4(const uint8_t* lut, uint32_t a, uint32_t b) {
+  const uint32_t i01 = __byte_perm(b, a, 0x5140), i23 = __byte_perm(b, a, 0x7362);  // [b0 a0 b1 a1], [b2 a2 b3 a3]
+  const uint32_t r0 = lut[i01 & 0xFFFFu], r1 = lut[i01 >> 16], r2 = lut[i23 & 0xFFFFu], r3 = lut[i23 >> 16];
+  return r0 | (r1 << 8) | (r2 << 16) | (r3 << 24);
+}
+
+template <int OP>
+__global__ void __launch_bounds__(kQbThreads, 1) quant_binary_table_kernel(QuantBinaryPlan p) {
+  extern __shared__ __align__(16) uint8_t qlut[];  // kQbEntries results
+  cg::cluster_group cluster = cg::this_cluster();
+  {  // this block's share: eight consecutive entries per thread, copied to every block of the cluster
+    const int first = (int)cluster.block_rank() * (kQbEntries / kQbCluster) + 8 * (int)threadIdx.x;
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = first + i;
+      const int r = qbin<OP>((int)(int8_t)(e >> 8), (int)(int8_t)(e & 0xFF), p);
+      w[i >> 2] |= ((uint32_t)r & 0xFFu) << (8 * (i & 3));
+    }
+#pragma unroll
+    for (int d = 0; d < kQbCluster; ++d)
+      *reinterpret_cast<uint2*>(cluster.map_shared_rank(qlut, d) + first) = make_uint2(w[0], w[1]);
+  }
+  cluster.sync();  // every block's table is complete; no shared-memory access crosses blocks after this
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nv = p.n / 16;
+  const uint4* l = reinterpret_cast<const uint4*>(p.lhs);
+  const uint4* r = reinterpret_cast<const uint4*>(p.rhs);
+  uint4* o = reinterpret_cast<uint4*>(p.out);
+  constexpr int kU = 2;  // vector pairs in flight per thread
+  for (int64_t v0 = tid; v0 < nv; v0 += kU * stride) {
+    uint4 a[kU], b[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nv) {
+        a[u] = __ldg(l + v);
+        b[u] = __ldg(r + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nv)
+        o[v] = make_uint4(qb_lookup4(qlut, a[u].x, b[u].x), qb_lookup4(qlut, a[u].y, b[u].y),
+                          qb_lookup4(qlut, a[u].z, b[u].z), qb_lookup4(qlut, a[u].w, b[u].w));
+    }
+  }
+  for (int64_t e = nv * 16 + tid; e < p.n; e += stride)
+    p.out[e] = (int8_t)qlut[((uint32_t)(uint8_t)p.lhs[e] << 8) | (uint8_t)p.rhs[e]];
+}
+
+template <int OP>
+static cudaError_t qb_table_launch(const QuantBinaryPlan& p, cudaStream_t s) {
+  const size_t smem = kQbEntries;
+  auto kernel = quant_binary_table_kernel<OP>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kQbCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kQbThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(kQbCluster, 1, 1);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, (void*)kernel, &cfg) != cudaSuccess || clusters < 1) {
+    cudaGetLastError();
+    clusters = 1;
+  }
+  cfg.gridDim = dim3((unsigned)(clusters * kQbCluster), 1, 1);
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 template <int OP>
 static cudaError_t qb_launch(const QuantBinaryPlan& p, cudaStream_t s) {
   const bool same = p.lmap.identity && p.rmap.identity && p.omap.identity;
   const bool aligned = ((uintptr_t)p.lhs % 16 == 0) && ((uintptr_t)p.rhs % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
+  if (same && aligned && p.n >= kQbTableMinElems) return qb_table_launch<OP>(p, s);
   const int64_t per = same && aligned ? 16 : 1;
   int64_t blocks = (p.n / per + 255) / 256;
   const int64_t cap = (int64_t)device_sm_count() * 8;
