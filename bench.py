@@ -43,9 +43,9 @@ WORKLOAD = ("HLO hero fusions, one launch each per step: row_reduce_exp f32[256,
             "bcast_exp_row_reduce bf16[8,1,1280,16384]{3,2,0,1}+bf16[16384]; "
             "quant_relayout s8[4096,4096]{1,0}->{0,1}")
 L2_NOTE = ("L2 flushed by a 256 MiB device write before every timed step (outside the timed interval), then a "
-           "~1 ms device-side spin so that the host has queued the whole step before it starts: host issue time "
+           "device-side spin (8M cycles) so that the host has queued the whole step before it starts: host issue time "
            "is outside the device timing (it is inside e2e)")
-HOST_LEAD_CYCLES = 2_000_000  # device clock cycles the stream spins after the flush (~1 ms at 2 GHz)
+HOST_LEAD_CYCLES = 8_000_000  # device clock cycles the stream spins after the flush
 # fusions beyond the five workloads, measured beside the step: the loop fusion of "XLA:GPU Emitters"
 # (section "Loop emitter"), the max/argmax variadic reduce of "XLA Operation Semantics" and a
 # quantized add (dequantize_op_quantize)

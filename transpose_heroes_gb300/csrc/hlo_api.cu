@@ -329,6 +329,43 @@ int hlo::device_sm_count() {
   return cache[dev];
 }
 
+void hlo::table_cluster_shape(const void* kernel, int threads, size_t smem, int* cluster_size, int* clusters) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, std::pair<int, int>> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto key = std::make_pair(kernel, dev);
+  auto it = cache.find(key);
+  if (it == cache.end()) {
+    cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    std::pair<int, int> best(2, 1);
+    for (int cs : {8, 4, 2}) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cs;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(cs, 1, 1);
+      cfg.blockDim = dim3(threads, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+      if (n >= 1) {  // the largest size that fits: building the table costs 65536 / size evaluations per block
+        best = std::make_pair(cs, n);
+        break;
+      }
+    }
+    cudaGetLastError();  // clear any error from the queries above
+    it = cache.emplace(key, best).first;
+  }
+  *cluster_size = it->second.first;
+  *clusters = it->second.second;
+}
+
 int hlo::kernel_blocks_per_sm(const void* kernel, int threads, size_t smem) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, int> cache;

@@ -224,5 +224,10 @@ int device_sm_count();
 // Resident blocks per SM of `kernel` at this block size and dynamic shared memory, cached per kernel
 // and device; on first use also raises the kernel's dynamic shared-memory limit to `smem`.
 int kernel_blocks_per_sm(const void* kernel, int threads, size_t smem);
+// Cluster size (the largest of 8, 4, 2 that fits) and the number of clusters that can be resident at
+// once, for a kernel with one block per SM; sets the kernel's dynamic shared-memory limit. Cached.
+// (On GB300, 15 clusters of 8 fit: 120 SMs. Smaller clusters reach more SMs but each block then
+// builds a larger share of its table, which measured slower for the 16-bit chain tables.)
+void table_cluster_shape(const void* kernel, int threads, size_t smem, int* cluster_size, int* clusters);
 
 }  // namespace hlo

@@ -259,13 +259,11 @@ static bool chain16x2_ok(const Chain& pro, const Chain& epi, int dt) {
 // ---- 16-bit chains as a table of all 65536 inputs ------------------------------------------------
 // A chain on a 16-bit input with a 16-bit result (no broadcast operand) is a function of the input's
 // bits alone, so a large input is served from a table of its 65536 results held in shared memory
-// (128 KiB per block, one block of 1024 threads per SM). A cluster of kLutCluster blocks builds the
-// table together: each block evaluates 1/kLutCluster of the entries with the per-element code
-// (ew_apply, every op rounded to the element type) and writes them into the shared memory of every
-// block of its cluster (distributed shared memory); after the cluster barrier each block streams
-// 16-byte vectors and looks every element up locally. The table costs 65536 / kLutCluster
-// evaluations per block, no global memory beyond the input and output.
-constexpr int kLutCluster = 8;
+// (128 KiB per block, one block of 1024 threads per SM). The blocks of a thread-block cluster (8 where
+// they fit) build the table together: each evaluates its share of the entries with the per-element
+// code and writes them into the shared memory of every block of its cluster (distributed shared
+// memory); after the cluster barrier each block streams 16-byte vectors and looks every element up
+// locally. No global memory beyond input and output.
 constexpr int kLutThreads = 1024;
 constexpr int kLutEntries = 1 << 16;
 constexpr int64_t kLutMinElems = int64_t(1) << 22;  // below this the direct kernels are faster
@@ -287,8 +285,10 @@ __global__ void __launch_bounds__(kLutThreads, 1) elementwise_lut16_kernel(EwPla
   extern __shared__ __align__(16) uint16_t lut[];  // kLutEntries results
   cg::cluster_group cluster = cg::this_cluster();
   const LogTab lt = global_log_tables();
-  {  // this block's share of the table: eight consecutive entries per thread, copied to every block
-    const int first = (int)cluster.block_rank() * (kLutEntries / kLutCluster) + 8 * (int)threadIdx.x;
+  const int nb = (int)cluster.num_blocks(), share = kLutEntries / nb;
+  for (int c = 8 * (int)threadIdx.x; c < share; c += 8 * kLutThreads) {
+    // this block's share of the table, eight consecutive entries at a time, copied to every block
+    const int first = (int)cluster.block_rank() * share + c;
     uint32_t w[4];
     if (PACKED) {
       uint32_t x[4];
@@ -301,9 +301,7 @@ __global__ void __launch_bounds__(kLutThreads, 1) elementwise_lut16_kernel(EwPla
         w[i] = lut_entry<DT>(p, first + 2 * i, lt) | (lut_entry<DT>(p, first + 2 * i + 1, lt) << 16);
     }
     const uint4 v = make_uint4(w[0], w[1], w[2], w[3]);
-#pragma unroll
-    for (int d = 0; d < kLutCluster; ++d)
-      *reinterpret_cast<uint4*>(cluster.map_shared_rank(lut, d) + first) = v;
+    for (int d = 0; d < nb; ++d) *reinterpret_cast<uint4*>(cluster.map_shared_rank(lut, d) + first) = v;
   }
   cluster.sync();  // every block's table is complete; no shared-memory access crosses blocks after this
   const uint16_t* in = reinterpret_cast<const uint16_t*>(p.in);
@@ -348,26 +346,20 @@ template <int DT, bool PACKED>
 static cudaError_t lut16_launch(const EwPlan& p, cudaStream_t s) {
   const size_t smem = kLutEntries * sizeof(uint16_t);
   auto kernel = elementwise_lut16_kernel<DT, PACKED>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  int cs = 0, clusters = 0;
+  table_cluster_shape((const void*)kernel, kLutThreads, smem, &cs, &clusters);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kLutCluster;
+  attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(cs * (clusters > 0 ? clusters : 1)), 1, 1);
   cfg.blockDim = dim3(kLutThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int clusters = 0;
-  cfg.gridDim = dim3(kLutCluster, 1, 1);
-  if (cudaOccupancyMaxActiveClusters(&clusters, (void*)kernel, &cfg) != cudaSuccess || clusters < 1) {
-    cudaGetLastError();
-    clusters = 1;
-  }
-  cfg.gridDim = dim3((unsigned)(clusters * kLutCluster), 1, 1);
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 

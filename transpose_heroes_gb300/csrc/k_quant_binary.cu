@@ -68,12 +68,11 @@ __global__ void __launch_bounds__(256) quant_binary_map_kernel(QuantBinaryPlan p
 }
 
 // Large same-layout inputs: the result depends on the two codes alone, so it is read from a table of
-// all 256 x 256 code pairs (64 KiB of shared memory per block). A cluster of kQbCluster blocks builds
-// the table together, each block computing 1/kQbCluster of the pairs with qbin and writing them into
-// every block of the cluster through distributed shared memory; after the cluster barrier each block
-// streams 16-byte vectors of both operands and looks every pair up locally. No global memory beyond
-// the operands and the result.
-constexpr int kQbCluster = 8;
+// all 256 x 256 code pairs (64 KiB of shared memory per block). The blocks of a thread-block cluster
+// (8 where they fit) build the table together, each computing its share of the pairs with qbin and
+// writing them into every block of the cluster through distributed shared memory; after the cluster
+// barrier each block streams 16-byte vectors of both operands and looks every pair up locally. No
+// global memory beyond the operands and the result.
 constexpr int kQbThreads = 1024;
 constexpr int kQbEntries = 1 << 16;
 constexpr int64_t kQbTableMinElems = int64_t(1) << 22;
@@ -89,8 +88,10 @@ template <int OP>
 __global__ void __launch_bounds__(kQbThreads, 1) quant_binary_table_kernel(QuantBinaryPlan p) {
   extern __shared__ __align__(16) uint8_t qlut[];  // kQbEntries results
   cg::cluster_group cluster = cg::this_cluster();
-  {  // this block's share: eight consecutive entries per thread, copied to every block of the cluster
-    const int first = (int)cluster.block_rank() * (kQbEntries / kQbCluster) + 8 * (int)threadIdx.x;
+  const int nb = (int)cluster.num_blocks(), share = kQbEntries / nb;
+  for (int c = 8 * (int)threadIdx.x; c < share; c += 8 * kQbThreads) {
+    // this block's share, eight consecutive entries at a time, copied to every block of the cluster
+    const int first = (int)cluster.block_rank() * share + c;
     uint32_t w[2] = {0u, 0u};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -98,9 +99,7 @@ __global__ void __launch_bounds__(kQbThreads, 1) quant_binary_table_kernel(Quant
       const int r = qbin<OP>((int)(int8_t)(e >> 8), (int)(int8_t)(e & 0xFF), p);
       w[i >> 2] |= ((uint32_t)r & 0xFFu) << (8 * (i & 3));
     }
-#pragma unroll
-    for (int d = 0; d < kQbCluster; ++d)
-      *reinterpret_cast<uint2*>(cluster.map_shared_rank(qlut, d) + first) = make_uint2(w[0], w[1]);
+    for (int d = 0; d < nb; ++d) *reinterpret_cast<uint2*>(cluster.map_shared_rank(qlut, d) + first) = make_uint2(w[0], w[1]);
   }
   cluster.sync();  // every block's table is complete; no shared-memory access crosses blocks after this
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -136,26 +135,20 @@ template <int OP>
 static cudaError_t qb_table_launch(const QuantBinaryPlan& p, cudaStream_t s) {
   const size_t smem = kQbEntries;
   auto kernel = quant_binary_table_kernel<OP>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  int cs = 0, clusters = 0;
+  table_cluster_shape((const void*)kernel, kQbThreads, smem, &cs, &clusters);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kQbCluster;
+  attr[0].val.clusterDim.x = cs;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(cs * (clusters > 0 ? clusters : 1)), 1, 1);
   cfg.blockDim = dim3(kQbThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(kQbCluster, 1, 1);
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, (void*)kernel, &cfg) != cudaSuccess || clusters < 1) {
-    cudaGetLastError();
-    clusters = 1;
-  }
-  cfg.gridDim = dim3((unsigned)(clusters * kQbCluster), 1, 1);
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
