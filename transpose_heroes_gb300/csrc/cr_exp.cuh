@@ -1,10 +1,11 @@
 // Correctly rounded f32 exp and tanh ("StableHLO Specification", sections "exponential" and "tanh":
 // the IEEE-754 function of the element type; rounding to nearest even of the exact value).
 //
-// Stage 1: CUDA's double exp, documented within 1 double ulp, rounded once to f32. That rounding is
+// Stage 1 (cr_expf): a float-float evaluation in f32 with a rounding test, below.
+// Stage 2: CUDA's double exp, documented within 1 double ulp, rounded once to f32. That rounding is
 // the correct one unless the double lies within 3 double ulps of an f32 rounding boundary (a
 // midpoint between two floats), which happens for about 2^-26 of the arguments.
-// Stage 2 (those, and NaN): a double-double evaluation after Tang ("Table-driven implementation of
+// Stage 3 (those, and NaN): a double-double evaluation after Tang ("Table-driven implementation of
 // the exponential function in IEEE floating-point arithmetic", ACM TOMS 15(2), 1989):
 //   k = rint(64 x / ln2) = 64 e + j,  r = x - k ln2/64 (as a double-double, exactly up to 2^-94),
 //   exp x = 2^e * 2^(j/64) * exp(r),  exp(r) = 1 + r + r^2/2 + r^3 P(r),
@@ -84,9 +85,56 @@ __device__ __forceinline__ bool f32_rounding_settled(double y) {
   return false;  // NaN
 }
 
-__device__ __forceinline__ float cr_expf(float x) {
+static __device__ __noinline__ float cr_expf_double(float x) {
   const double y = exp((double)x);
   return f32_rounding_settled(y) ? __double2float_rn(y) : cr_expf_dd(x);
+}
+
+// First pass in f32 for arguments with a normal, finite result (about 1 in 2^11 of them stays open):
+//   k = rint(64 x / ln2) through the 1.5*2^23 constant, r1 = x - k L1f exactly (k L1f is exact and the
+//   difference fits 24 bits for every f32 in range, checked exhaustively), r = rh + rl = r1 - k L2f -
+//   k L3f (the k L2f product split exactly by FMA, the sum by TwoSum),
+//   exp(r) - 1 = rh + pe,  pe = rh^2 (1/2 + rh/6 + rh^2/24) + rl (1 + rh)   (truncation < 2^-44),
+//   y = yh + yl = 2^(j/64) (1 + rh + pe), with 2^(j/64) = Th + Tl and Th rh split exactly by FMA,
+//   exp x = 2^(k >> 6) y.
+// Every rounding error sums to under 2^-36.5 absolute (y < 2.02; 2^-37.2 in an emulation over 4.2 M
+// arguments); with b = 2^-35 the rounding is decided by monotonicity: if yh + (yl - b) and
+// yh + (yl + b) round to the same float, so does y. Scaling by 2^e is exact in the normal range.
+__device__ __forceinline__ void expf_ff(float x, float& yh, float& yl, int& e) {
+  const float t = __fmaf_rn(x, HLO_EXPF_INV64_LN2, 12582912.0f);
+  const int k = __float_as_int(t) - 0x4B400000;
+  const float kf = __fsub_rn(t, 12582912.0f);
+  const float r1 = __fmaf_rn(-kf, HLO_EXPF_L1, x);  // exact
+  const float p2h = __fmul_rn(kf, HLO_EXPF_L2);
+  const float p2l = __fmaf_rn(kf, HLO_EXPF_L2, -p2h);  // k L2f = p2h + p2l exactly
+  const float rh = __fsub_rn(r1, p2h);                   // TwoSum(r1, -p2h)
+  const float bb = __fsub_rn(rh, r1);
+  float rl = __fadd_rn(__fsub_rn(r1, __fsub_rn(rh, bb)), __fsub_rn(-p2h, bb));
+  rl = __fmaf_rn(-kf, HLO_EXPF_L3, __fsub_rn(rl, p2l));
+  float q = __fmaf_rn(rh, 0x1.555556p-5f, 0x1.555556p-3f);  // 1/24, 1/6
+  q = __fmaf_rn(rh, q, 0.5f);
+  float pe = __fmaf_rn(__fmul_rn(rh, rh), q, rl);
+  pe = __fmaf_rn(rl, rh, pe);
+  const float2 T = __ldg(&kExpTf[k & 63]);
+  const float ah = __fmul_rn(T.x, rh);
+  const float al = __fmaf_rn(T.x, rh, -ah);
+  float lo = __fmaf_rn(T.x, pe, T.y);
+  lo = __fadd_rn(__fmaf_rn(T.y, rh, lo), al);
+  yh = __fadd_rn(T.x, ah);  // Fast2Sum: Th >= 1 > |ah|
+  yl = __fadd_rn(__fsub_rn(ah, __fsub_rn(yh, T.x)), lo);
+  e = k >> 6;
+}
+
+__device__ __forceinline__ float cr_expf(float x) {
+  if (x > -87.0f && x < 88.5f) {
+    float yh, yl;
+    int e;
+    expf_ff(x, yh, yl, e);
+    const float yp = __fadd_rn(yh, __fadd_rn(yl, 0x1p-35f));
+    const float ym = __fadd_rn(yh, __fsub_rn(yl, 0x1p-35f));
+    if (yp == ym) return __fmul_rn(yp, __int_as_float((127 + e) << 23));
+  }
+  return cr_expf_double(x);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -134,10 +182,58 @@ static __device__ __noinline__ float cr_tanhf_dd(float x) {
   return x < 0.0f ? -f : f;
 }
 
-__device__ __forceinline__ float cr_tanhf(float x) {
-  if (fabsf(x) < 0x1p-126f) return x;  // zero and subnormals: |tanh x - x| is far below half an ulp
+static __device__ __noinline__ float cr_tanhf_double(float x) {
   const double y = tanh((double)x);
   return f32_rounding_settled(y) ? __double2float_rn(y) : cr_tanhf_dd(x);
+}
+
+// First pass in f32 (a = |x|, sign restored at the end), then the rounding test of cr_expf:
+//   a < 2^-4:  tanh a = a - a^3/3 + a^5 P(a^2), P = 2/15 - 17 a^2/315 + 62 a^4/2835 - 1382 a^6/155925
+//              (truncation below 2^-45 a); a^3/3 as an f32 pair (a^2, a^3 split by FMA, 1/3 as an
+//              f32 pair), the a^5 P term in f32: error below 2^-40 a; test bound a 2^-37.
+//   2^-4 <= a < 9.05: tanh a = 1 - 2/(t + 1), t = exp(2a) as an f32 pair from expf_ff (error below
+//              2^-36.5 t); 2/(t + 1) = q0 + q1 with q0 the IEEE quotient of the high parts and q1 from
+//              its exact remainder; 1 - q0 split exactly. Error below 2^-37.3 absolute; bound 2^-35.5.
+//   a >= 9.05: 1 - tanh a < 2^-25.1, so tanh rounds to 1.
+__device__ __forceinline__ float cr_tanhf(float x) {
+  const float a = fabsf(x);
+  if (a < 0x1p-126f) return x;  // zero and subnormals: |tanh x - x| is far below half an ulp
+  if (a >= 9.05f) return a == a ? copysignf(1.0f, x) : x;
+  float th, tl, b;
+  if (a < 0x1p-4f) {
+    const float a2h = __fmul_rn(a, a), a2l = __fmaf_rn(a, a, -a2h);
+    const float a3h = __fmul_rn(a, a2h);
+    const float a3l = __fmaf_rn(a, a2l, __fmaf_rn(a, a2h, -a3h));
+    const float ch = __fmul_rn(a3h, 0x1.555556p-2f);
+    const float cl = __fmaf_rn(a3l, 0x1.555556p-2f, __fmaf_rn(a3h, -0x1.555556p-27f, __fmaf_rn(a3h, 0x1.555556p-2f, -ch)));
+    float p = __fmaf_rn(a2h, -0x1.226e36p-7f, 0x1.664f48p-6f);
+    p = __fmaf_rn(a2h, p, -0x1.ba1ba2p-5f);
+    p = __fmaf_rn(a2h, p, 0x1.111112p-3f);
+    const float t5 = __fmul_rn(__fmul_rn(a3h, a2h), p);
+    th = __fsub_rn(a, ch);  // Fast2Sum: a > a^3/3
+    tl = __fadd_rn(__fsub_rn(__fsub_rn(a, th), ch), __fsub_rn(t5, cl));
+    b = __fmul_rn(a, 0x1p-37f);
+  } else {
+    float yh, yl;
+    int e;
+    expf_ff(__fmul_rn(2.0f, a), yh, yl, e);
+    const float sc = __int_as_float((127 + e) << 23);  // 2^e, e in [0, 26]
+    const float eh = __fmul_rn(yh, sc), el = __fmul_rn(yl, sc);
+    const float d1 = __fadd_rn(eh, 1.0f);  // Fast2Sum: eh >= 1
+    const float d2 = __fadd_rn(__fsub_rn(1.0f, __fsub_rn(d1, eh)), el);
+    const float dh = __fadd_rn(d1, d2);  // renormalised (el is not below half an ulp of eh)
+    const float dl = __fsub_rn(d2, __fsub_rn(dh, d1));
+    const float q0 = __fdiv_rn(2.0f, dh);
+    const float r = __fmaf_rn(-q0, dl, __fmaf_rn(-q0, dh, 2.0f));  // 2 - q0 dh is exact
+    const float q1 = __fmul_rn(r, __fmul_rn(q0, 0.5f));
+    th = __fsub_rn(1.0f, q0);  // Fast2Sum: 1 > q0
+    tl = __fsub_rn(__fsub_rn(__fsub_rn(1.0f, th), q0), q1);
+    b = 0x1.6a09e6p-36f;  // 2^-35.5
+  }
+  const float yp = __fadd_rn(th, __fadd_rn(tl, b));
+  const float ym = __fadd_rn(th, __fsub_rn(tl, b));
+  if (yp == ym) return x < 0.0f ? -yp : yp;
+  return cr_tanhf_double(x);
 }
 
 }  // namespace hlo
