@@ -164,3 +164,34 @@ def test_argmax_validation(lib):
     # init_index outside s32
     st, msg = _status(lambda: hf.reduce_max_argmax(x, [4, 5], "f32", [1], out, out_idx, init_index=1 << 40, stream=0))
     assert st == 1 and "s32" in msg
+
+
+# ---- constants of the correctly rounded f32 exp ------------------------------------------------------------
+def test_exp_table_matches_its_generator(tmp_path):
+    """exp_table.inc is what gen_exp_table.py writes (Python decimal, exact conversions)."""
+    import importlib.util
+    csrc = os.path.join(ROOT, "transpose_heroes_gb300", "csrc")
+    spec = importlib.util.spec_from_file_location("gen_exp_table", os.path.join(csrc, "gen_exp_table.py"))
+    gen = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(gen)
+    out = tmp_path / "exp_table.inc"
+    gen.main(str(out))
+    with open(os.path.join(csrc, "exp_table.inc")) as f:
+        assert out.read_text() == f.read()
+
+
+def test_exp_first_reduction_step_is_exact():
+    """The f32 exp pass relies on r1 = x - k*L1f being exact (k = rint(64 x / ln2) from the f32 constant):
+    check it on a million f32 arguments spread over the range and on the range ends."""
+    import re
+    with open(os.path.join(ROOT, "transpose_heroes_gb300", "csrc", "exp_table.inc")) as f:
+        text = f.read()
+    inv = float.fromhex(re.search(r"HLO_EXPF_INV64_LN2 (\S+)f", text).group(1))
+    l1 = float.fromhex(re.search(r"HLO_EXPF_L1 (\S+)f", text).group(1))
+    g = np.random.default_rng(5)
+    x = np.concatenate([g.uniform(-87, 88.5, 1_000_000), [-87.0, 88.4999, 1e-30, -1e-30, 0.0054, -0.0054]])
+    x = x.astype(np.float32).astype(np.float64)
+    k = np.rint(x * np.float32(inv).astype(np.float64))  # x * INV is exact in f64; fma rounds it to an integer
+    r1 = x - k * l1
+    assert np.array_equal(r1.astype(np.float32).astype(np.float64), r1)
+    assert np.abs(r1).max() < 0.04
