@@ -339,13 +339,33 @@ def ours(args):
         d.run(stream=stream)
         d.d2h()
     torch.cuda.synchronize()
+    # three streams so that copies in, fusions and copies out overlap (the copy engines run both
+    # directions at once); per-fusion events keep each buffer's reads and writes in order across steps
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in devs]
+    ev_ran = [torch.cuda.Event() for _ in devs]
+    ev_out = [torch.cuda.Event() for _ in devs]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        for d in devs:
-            d.h2d()
+    s_in.wait_event(e0)
+    for k in range(e2e_steps):
+        for i, d in enumerate(devs):
+            with torch.cuda.stream(s_in):
+                if k:
+                    s_in.wait_event(ev_ran[i])  # the previous step's fusion has read d's input
+                d.h2d()
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if k:
+                stream.wait_event(ev_out[i])  # the previous step's output has been copied out
             d.run(stream=stream)
-            d.d2h()
+            ev_ran[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_ran[i])
+                d.d2h()
+                ev_out[i].record(s_out)
+    for ev in ev_out:
+        stream.wait_event(ev)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_s = aggregate(e0.elapsed_time(e1) / 1e3, "max")
