@@ -195,3 +195,56 @@ def test_exp_first_reduction_step_is_exact():
     r1 = x - k * l1
     assert np.array_equal(r1.astype(np.float32).astype(np.float64), r1)
     assert np.abs(r1).max() < 0.04
+
+
+def _expf_first_pass_emulated(x):
+    """The f32 exp first pass of cr_exp.cuh, step for step in numpy (an FMA is emulated in f64: the
+    product is exact there and the sum rounds once, twice only in rare ties, which a sampled bound
+    tolerates). Returns (yh, yl, e) with exp(x) ~ (yh + yl) 2^e."""
+    import re
+    with open(os.path.join(ROOT, "transpose_heroes_gb300", "csrc", "exp_table.inc")) as f:
+        text = f.read()
+    c = {k: np.float32(float.fromhex(re.search(r"HLO_EXPF_%s (\S+)f" % k, text).group(1)))
+         for k in ("INV64_LN2", "L1", "L2", "L3")}
+    tab = re.findall(r"\{(\S+)f, (\S+)f\}", text.split("kExpTf")[1].split("};")[0])
+    th = np.array([float.fromhex(a) for a, _ in tab], np.float32)
+    tl = np.array([float.fromhex(b) for _, b in tab], np.float32)
+    f32 = np.float32
+
+    def fma(a, b, cc):
+        return (np.asarray(a, np.float64) * np.asarray(b, np.float64) + np.asarray(cc, np.float64)).astype(f32)
+
+    m = f32(12582912.0)
+    t = fma(x, c["INV64_LN2"], m)
+    k = t.view(np.int32) - 0x4B400000
+    kf = (t - m).astype(f32)
+    r1 = fma(-kf, c["L1"], x)
+    p2h = (kf * c["L2"]).astype(f32)
+    p2l = fma(kf, c["L2"], -p2h)
+    rh = (r1 - p2h).astype(f32)
+    bb = (rh - r1).astype(f32)
+    rl = ((r1 - (rh - bb).astype(f32)).astype(f32) + (-p2h - bb).astype(f32)).astype(f32)
+    rl = fma(-kf, c["L3"], (rl - p2l).astype(f32))
+    q = fma(rh, f32(float.fromhex("0x1.555556p-5")), f32(float.fromhex("0x1.555556p-3")))
+    q = fma(rh, q, f32(0.5))
+    pe = fma((rh * rh).astype(f32), q, rl)
+    pe = fma(rl, rh, pe)
+    j = k & 63
+    ah = (th[j] * rh).astype(f32)
+    al = fma(th[j], rh, -ah)
+    lo = fma(th[j], pe, tl[j])
+    lo = (fma(tl[j], rh, lo) + al).astype(f32)
+    yh = (th[j] + ah).astype(f32)
+    yl = ((ah - (yh - th[j]).astype(f32)).astype(f32) + lo).astype(f32)
+    return yh, yl, k >> 6
+
+
+def test_expf_first_pass_error_below_its_rounding_bound():
+    """The bound the kernel's rounding test uses (2^-35 on yh + yl, which lies in [1, 2.02)) holds with
+    a margin: the emulated first pass stays within 2^-36.5 of exp(x) 2^-e (long double reference)."""
+    g = np.random.default_rng(7)
+    x = np.concatenate([g.uniform(-87, 88.5, 200_000), g.uniform(-0.01, 0.01, 50_000)]).astype(np.float32)
+    yh, yl, e = _expf_first_pass_emulated(x)
+    ref = np.exp(x.astype(np.longdouble)) / np.ldexp(np.longdouble(1), e)
+    err = np.abs(yh.astype(np.longdouble) + yl.astype(np.longdouble) - ref)
+    assert float(err.max()) < 2.0 ** -36.5
