@@ -248,3 +248,48 @@ def test_expf_first_pass_error_below_its_rounding_bound():
     ref = np.exp(x.astype(np.longdouble)) / np.ldexp(np.longdouble(1), e)
     err = np.abs(yh.astype(np.longdouble) + yl.astype(np.longdouble) - ref)
     assert float(err.max()) < 2.0 ** -36.5
+
+
+def test_tanhf_first_pass_errors_below_their_rounding_bounds():
+    """Both branches of the f32 tanh first pass (cr_exp.cuh), emulated step for step: the Taylor branch
+    (a < 2^-4) within 2^-39 a of tanh a (the test uses a 2^-37), the 1 - 2/(exp(2a) + 1) branch within
+    2^-37.5 absolute (the test uses 2^-35.5)."""
+    f32 = np.float32
+
+    def fma(a, b, c):
+        return (np.asarray(a, np.float64) * np.asarray(b, np.float64) + np.asarray(c, np.float64)).astype(f32)
+
+    h = lambda s: f32(float.fromhex(s))
+    g = np.random.default_rng(8)
+    a = np.concatenate([g.uniform(2.0 ** -20, 0.0625, 100_000), np.geomspace(1e-30, 0.0624, 20_000)]).astype(f32)
+    a = a[a < f32(0.0625)]
+    a2h = (a * a).astype(f32)
+    a2l = fma(a, a, -a2h)
+    a3h = (a * a2h).astype(f32)
+    a3l = fma(a, a2l, fma(a, a2h, -a3h))
+    ch = (a3h * h("0x1.555556p-2")).astype(f32)
+    cl = fma(a3l, h("0x1.555556p-2"), fma(a3h, h("-0x1.555556p-27"), fma(a3h, h("0x1.555556p-2"), -ch)))
+    p = fma(a2h, h("-0x1.226e36p-7"), h("0x1.664f48p-6"))
+    p = fma(a2h, p, h("-0x1.ba1ba2p-5"))
+    p = fma(a2h, p, h("0x1.111112p-3"))
+    t5 = ((a3h * a2h).astype(f32) * p).astype(f32)
+    th = (a - ch).astype(f32)
+    tl = (((a - th).astype(f32) - ch).astype(f32) + (t5 - cl).astype(f32)).astype(f32)
+    err = np.abs(th.astype(np.longdouble) + tl.astype(np.longdouble) - np.tanh(a.astype(np.longdouble)))
+    assert float((err / a.astype(np.longdouble)).max()) < 2.0 ** -39
+
+    a = g.uniform(0.0625, 9.05, 200_000).astype(f32)
+    yh, yl, e = _expf_first_pass_emulated((2 * a).astype(f32))
+    sc = np.ldexp(f32(1), e).astype(f32)
+    eh, el = (yh * sc).astype(f32), (yl * sc).astype(f32)
+    d1 = (eh + f32(1)).astype(f32)
+    d2 = ((f32(1) - (d1 - eh).astype(f32)).astype(f32) + el).astype(f32)
+    dh = (d1 + d2).astype(f32)
+    dl = (d2 - (dh - d1).astype(f32)).astype(f32)
+    q0 = (f32(2) / dh).astype(f32)
+    r = fma(-q0, dl, fma(-q0, dh, f32(2)))
+    q1 = (r * (q0 * f32(0.5)).astype(f32)).astype(f32)
+    th = (f32(1) - q0).astype(f32)
+    tl = (((f32(1) - th).astype(f32) - q0).astype(f32) - q1).astype(f32)
+    err = np.abs(th.astype(np.longdouble) + tl.astype(np.longdouble) - np.tanh(a.astype(np.longdouble)))
+    assert float(err.max()) < 2.0 ** -37.5
