@@ -463,7 +463,8 @@ extern "C" int orc_reduce(const orc_arr* in, const void* in_data, const orc_chai
     int64_t kidx[ORC_MAX_RANK], ridx[ORC_MAX_RANK], full[ORC_MAX_RANK];
     lex_index(nk, kdims, o, kidx);
     for (int k = 0; k < nk; ++k) full[kept[k]] = kidx[k];
-    double acc = init, asum = 0;
+    // init_values has the inputs' element type ("reduce" C2): the init literal is a value of it
+    double acc = round_to<double>(init, in->dtype), asum = 0;
     for (int64_t t = 0; t < n_red; ++t) {
       lex_index(nr, rdims, t, ridx);
       for (int k = 0; k < nr; ++k) full[red[k]] = ridx[k];

@@ -761,3 +761,183 @@ def test_quant_binary_exact_steps(orc, op):
         if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
             fl += 1
         assert r == max(-128, min(127, fl + zo))
+
+
+# ---------------------------------------------------------------------------------------------
+# f32 intermediates for 16-bit chains (round_intermediates = 0). This is the emitter's lowering of a
+# bf16/f16 op through f32 (XLA:GPU Emitters, "Loop emitter": fpext -> f32 op -> fptrunc) with the
+# fptrunc/fpext pair between two fused ops left out: every op is the correctly rounded f32 operation,
+# the value is rounded to the element type once, where the chain's result is stored. A constant keeps
+# the type of its HLO constant instruction, the element type (StableHLO Specification, "constant"):
+# constant(0.1) of bf16 is the bf16 value 0.10009765625 whichever precision the ops run in.
+# ---------------------------------------------------------------------------------------------
+def _exact_unary(name: str, v: Fraction) -> Fraction:
+    """The exact value (to ~80 digits) of op(v) for an f32 value v, as a rational."""
+    if name == "exp":
+        return Fraction(Decimal(float(v)).exp())
+    if name == "log":
+        return Fraction(Decimal(float(v)).ln())
+    if name == "tanh":
+        return decimal_tanh(float(v))
+    raise ValueError(name)
+
+
+def _chain_f32_mode(ops, x: float, fmt: str, const_fmt: str) -> float:
+    """Test-side evaluation of a chain with f32 intermediates: each op's exact result rounded to f32,
+    constants rounded to const_fmt, one final rounding to fmt."""
+    xq = Fraction(x)
+    v = xq
+    for op in ops:
+        if isinstance(op, (tuple, list)):
+            name, c = op
+            cq = Fraction(round_fraction(Fraction(c), const_fmt))
+            v = v + cq if name == "add_const" else v * cq
+        elif op in ("exp", "log", "tanh"):
+            v = _exact_unary(op, v)
+        elif op == "abs":
+            v = abs(v)
+        elif op == "neg":
+            v = -v
+        elif op == "add_input":
+            v = v + xq
+        elif op == "mul_input":
+            v = v * xq
+        v = Fraction(round_fraction(v, "f32"))
+    return round_fraction(v, fmt)
+
+
+def _bits_of(vals, fmt):
+    if fmt == "bf16":
+        return (vals.view(np.uint32) >> 16).astype(np.uint16)
+    return vals.astype(np.float16).view(np.uint16)
+
+
+def _vals_of(bits, fmt):
+    if fmt == "bf16":
+        return (np.asarray(bits, np.uint32) << 16).view(np.float32)
+    return np.asarray(bits, np.uint16).view(np.float16).astype(np.float32)
+
+
+F32_MODE_CHAINS = [
+    ["exp", ("add_const", 0.1), ("mul_const", -1.7), "tanh"],
+    ["abs", ("add_const", 0.01), "log", "mul_input", "neg"],
+]
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("ops", F32_MODE_CHAINS, ids=["exp-const-tanh", "abs-log-input"])
+def test_chain_with_f32_intermediates_exact(orc, fmt, ops):
+    g = np.random.default_rng(29)
+    x = g.uniform(-6, 6, 400).astype(np.float32)
+    bits = _bits_of(x, fmt)  # bf16 by truncation, f16 by numpy's nearest: both valid 16-bit values
+    xs = _vals_of(bits, fmt)
+    got = orc.transpose(bits, [len(bits)], fmt, [0], prologue={"ops": ops, "round_each": False})
+    got = _vals_of(got, fmt)
+    differs_from_spec_types = differs_from_f32_consts = 0
+    spec = _vals_of(orc.transpose(bits, [len(bits)], fmt, [0], prologue={"ops": ops, "round_each": True}), fmt)
+    for xi, yi, si in zip(xs, got, spec):
+        want = _chain_f32_mode(ops, float(xi), fmt, const_fmt=fmt)
+        assert float(yi) == want, (float(xi), float(yi), want)
+        differs_from_spec_types += float(si) != want
+        differs_from_f32_consts += _chain_f32_mode(ops, float(xi), fmt, const_fmt="f32") != want
+    # the pin discriminates: per-op rounding to the element type, and f32 constants, each change results
+    assert differs_from_spec_types > 0
+    assert differs_from_f32_consts > 0
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+def test_reduce_terms_with_f32_intermediates_exact(orc, fmt):
+    """exp then add of a broadcast operand with f32 intermediates: each term is f32(f32(exp x) + b),
+    never rounded to the 16-bit type, and the terms are summed (the f64 oracle sum is exact here)."""
+    import transpose_heroes_gb300.inputs as inp
+
+    rng = inp.rng(43)
+    n = 300
+    if fmt == "bf16":
+        x = inp.normal_bf16(rng, n)
+        b = inp.uniform_bf16(rng, n, -1, 1)
+    else:
+        x = rng.standard_normal(n).astype(np.float16).view(np.uint16)
+        b = rng.uniform(-1, 1, n).astype(np.float16).view(np.uint16)
+    chain = {"ops": ["exp", "add_bcast"], "round_each": False,
+             "bcast": {"data": b, "dims": [n], "dtype": fmt, "broadcast_dimensions": [1]}}
+    out = orc.reduce(x, [1, n], fmt, [1], "add", 0.0, "f64", prologue=chain)
+    total = total_spec = Fraction(0)
+    for xi, bi in zip(_vals_of(x, fmt), _vals_of(b, fmt)):
+        e = Fraction(round_fraction(Fraction(Decimal(float(xi)).exp()), "f32"))
+        total += Fraction(round_fraction(e + Fraction(float(bi)), "f32"))
+        e16 = Fraction(round_fraction(Fraction(Decimal(float(xi)).exp()), fmt))
+        total_spec += Fraction(round_fraction(e16 + Fraction(float(bi)), fmt))
+    assert out[0] == float(total)
+    assert float(total) != float(total_spec)  # the two readings give different sums
+
+
+def test_reduce_init_is_a_value_of_the_input_type(orc):
+    """reduce (C2): init_values has the inputs' element type, so init 0.1 on bf16 inputs is the bf16
+    value 0.10009765625 (on f16 0.0999755859375, on f32 the f32 nearest 0.1)."""
+    for fmt, want in [("bf16", 0.10009765625), ("f16", 0.0999755859375), ("f32", float(np.float32(0.1)))]:
+        zeros = np.zeros(4, dtype=np.float32 if fmt == "f32" else np.uint16)
+        out = orc.reduce(zeros, [1, 4], fmt, [1], "add", 0.1, "f64")
+        assert out[0] == want == round_fraction(Fraction(0.1), fmt)
+        empty = orc.reduce(np.zeros(0, np.float32 if fmt == "f32" else np.uint16), [3, 0], fmt, [1], "max", 0.1,
+                           "f64")
+        assert list(empty) == [want] * 3
+
+
+# ---------------------------------------------------------------------------------------------
+# quantize: round, then add the zero point, then clamp (the reading of the missing uniform_quantize
+# section; the other order, adding the zero point before rounding, changes exact ties when the zero
+# point is odd). And the float ops between dequantize and quantize, pinned step by step.
+# ---------------------------------------------------------------------------------------------
+def test_quantize_adds_the_zero_point_after_rounding(orc):
+    odd = {"scales": [1.0], "zero_points": [1]}
+    assert orc.quantize(odd, 2.5) == 3    # RNE(2.5) = 2, + 1; zero point first: RNE(3.5) = 4
+    assert orc.quantize(odd, 3.5) == 5    # RNE(3.5) = 4, + 1; zero point first: RNE(4.5) = 4
+    assert orc.quantize(odd, -0.5) == 1   # RNE(-0.5) = -0, + 1; zero point first: RNE(0.5) = 0
+    neg = {"scales": [1.0], "zero_points": [-3]}
+    assert orc.quantize(neg, 0.5) == -3   # RNE(0.5) = 0, - 3; zero point first: RNE(-2.5) = -2
+    # the clamp comes last: 126.5 -> 126 + 1 = 127; 127.5 -> 128 + 1 -> clamped to 127
+    assert orc.quantize(odd, 126.5) == 127 and orc.quantize(odd, 127.5) == 127
+    assert orc.quantize({"scales": [0.5], "zero_points": [1]}, 1.25) == 3  # 1.25/0.5 = 2.5 -> 2, + 1
+
+
+def _rne_int(q: Fraction) -> int:
+    fl = q.numerator // q.denominator
+    rem = q - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return fl
+
+
+@pytest.mark.parametrize("out_kind", ["s8", "f32"])
+def test_quant_fusion_float_ops_chain_exact(orc, out_kind):
+    """dequantize (per-axis on dim 1) -> abs, neg, exp, *1.5, +(-0.25) in f32 -> relayout {1,0} -> {0,1}
+    -> quantize (0.01, zero point 3) or the f32 value, each step on exact rationals rounded to f32."""
+    g = np.random.default_rng(23)
+    n0, n1 = 12, 20
+    q = g.integers(-128, 128, size=(n0, n1)).astype(np.int8)
+    scales = g.uniform(0.001, 0.01, n1).astype(np.float32)
+    zps = g.integers(-20, 21, n1).astype(np.int32)
+    in_q = {"scales": scales, "zero_points": zps, "quantization_dimension": 1}
+    out_q = {"scales": [0.01], "zero_points": [3]} if out_kind == "s8" else None
+    ops = ["abs", "neg", "exp", ("mul_const", 1.5), ("add_const", -0.25)]
+    out = orc.quant_fusion(q.ravel(), [n0, n1], "s8", in_q, [0, 1], out_kind, out_q=out_q,
+                           float_ops={"ops": ops})
+    s_out = Fraction(float(np.float32(0.01)))
+
+    def f32(v):
+        return Fraction(round_fraction(v, "f32"))
+
+    for i in range(n0):
+        for j in range(n1):
+            v = f32(Fraction(float(scales[j])) * (int(q[i, j]) - int(zps[j])))
+            v = -abs(v)
+            v = f32(Fraction(Decimal(float(v)).exp()))
+            v = f32(v * f32(Fraction(1.5)))
+            v = f32(v + f32(Fraction(-0.25)))
+            got = out[j * n0 + i]  # layout {0,1}: dimension 0 is minor
+            if out_kind == "f32":
+                assert Fraction(float(got)) == v
+            else:
+                code = min(127, max(-128, _rne_int(f32(v / s_out)) + 3))
+                assert int(got) == code, (i, j)
