@@ -50,7 +50,8 @@ HOST_LEAD_CYCLES = 8_000_000  # device clock cycles the stream spins after the f
 # (section "Loop emitter"), the max/argmax variadic reduce of "XLA Operation Semantics" and a
 # quantized add (dequantize_op_quantize)
 NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed), "argmax_f32": lambda seed: inp.argmax_f32(seed=seed),
-             "quant_add_s8": lambda seed: inp.quant_add_s8(seed=seed)}
+             "quant_add_s8": lambda seed: inp.quant_add_s8(seed=seed),
+             "transpose3_exp_abs_f32": lambda seed: inp.transpose3_exp_abs(seed=seed)}
 # kernel each fusion launches (for the launch list / roofline)
 KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_block_kernel",
            "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",
@@ -198,26 +199,39 @@ def run_oracle_once(fusions):
     return nbytes, time.perf_counter() - t0
 
 
-def cpu_baseline(min_seconds=10.0):
-    """The oracle, as it stands, on the host cores: whole passes of the full workload until at least
-    min_seconds of CPU time have run (the first pass is a warm-up and not counted)."""
-    import oracle
-
-    oracle.build()
-    cores = len(os.sched_getaffinity(0))
-    oracle.set_num_threads(cores)
-    fusions = cpu_sample_fusions(1.0)
-    run_oracle_once(fusions)
+def _timed_passes(fusions, min_seconds):
+    run_oracle_once(fusions)  # warm-up, not counted
     total_bytes, total_t, passes = 0, 0.0, 0
     while total_t < min_seconds:
         b, dt = run_oracle_once(fusions)
         total_bytes += b
         total_t += dt
         passes += 1
+    return total_bytes, total_t, passes
+
+
+def cpu_baseline(min_seconds=10.0):
+    """The oracle, as it stands, on the host cores: whole passes of the full workload on all cores until
+    at least min_seconds have run (the first pass is a warm-up and not counted); then the same on one
+    thread, on a 1/32 row sample of the workload."""
+    import oracle
+
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_num_threads(cores)
+    fusions = cpu_sample_fusions(1.0)
+    total_bytes, total_t, passes = _timed_passes(fusions, min_seconds)
     sample = (f"{passes} timed passes (after one warm-up pass) of the five fusions at full size: " +
               "; ".join(f"{f.name}" for f in fusions))
+    oracle.set_num_threads(1)
+    small = cpu_sample_fusions(1.0 / 32)
+    b1, t1, p1 = _timed_passes(small, min_seconds)
+    oracle.set_num_threads(cores)
+    one = {"value": b1 / t1 / 1e9, "unit": "GB/s", "cores": 1, "seconds": t1,
+           "sample": f"{p1} timed passes (after one warm-up pass) of the leading 1/32 of each fusion's rows "
+                     "(row_reduce_exp in full): " + "; ".join(f.name for f in small)}
     return {"value": total_bytes / total_t / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
-            "seconds": total_t}
+            "seconds": total_t, "one_thread": one}
 
 
 def reference_arm(args):
@@ -268,6 +282,12 @@ def ours(args):
     from transpose_heroes_gb300.runner import DeviceFusion
 
     rank, world, local = dist_env()
+    if args.gpus != world:
+        # one process per GPU: N > 1 is launched by torchrun, which sets WORLD_SIZE = N
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N > 1 with "
+              f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus}",
+              file=sys.stderr)
+        return 2
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)

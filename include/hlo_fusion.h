@@ -81,9 +81,13 @@ typedef struct {
  * loop fusion of "XLA:GPU Emitters" (section "Loop emitter") is
  *   MUL_INPUT, MUL_INPUT, MUL_CONST 0.044708, ADD_INPUT, MUL_CONST 0.79785, TANH, ADD_CONST 1,
  *   MUL_CONST 0.5, MUL_INPUT.
- * Rounding: exp, log and tanh are correctly rounded to the element type (f32, bf16, f16), except
- * that a float reduction's exp prologue uses a faster exp whose rare one-ulp differences stay inside
- * the reduction's tolerance; the other ops are exact IEEE operations. */
+ * Rounding: exp, log and tanh are correctly rounded to the element type (f32, bf16, f16) and the other
+ * ops are exact IEEE operations, with one exception: a reduce with the add body whose prologue is
+ * exactly (exp) or (exp, add of a bf16 vector broadcast along the reduced dimension) evaluates that
+ * exp with a faster approximation (relative error below about 2^-17). For f32 terms this stays inside
+ * the reduction's tolerance for any input; a 16-bit term can come out one unit of its type away from
+ * the correctly rounded one when exp lies that close to a rounding boundary (rare for spread-out
+ * inputs; the tolerance holds for them, not for inputs made only of such values). */
 typedef enum {
   HLO_EW_EXP = 1,
   HLO_EW_LOG = 2,
@@ -284,6 +288,27 @@ hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const 
                                  const void* idx_ptr, const int64_t* dimensions, int32_t n_dimensions,
                                  double init_value, int64_t init_index, const hlo_array* out, void* out_ptr,
                                  const hlo_array* out_idx, void* out_idx_ptr, void* stream);
+
+/* ------------------------------------------------------------------------------------------------
+ * Device-side faults. A kernel that gives up on a bounded wait records a fault bit in a word the
+ * library keeps on each device (no counterpart in the pages: this is the library's own diagnostics).
+ *   HLO_FAULT_COPY_TIMEOUT  the streaming row reduce waited about one second for an asynchronous
+ *                           global -> shared copy without seeing it complete; that block stopped,
+ *                           waited (again with a bound) for its copies in flight, wrote NaN to its
+ *                           output rows and returned, so the launch itself still reports success.
+ *
+ * hlo_device_faults waits for all work on the current device (cudaDeviceSynchronize), then stores the
+ * fault bits recorded there since the last clear in *faults (0: none) and, if clear != 0, resets them.
+ * HLO_ERR_CUDA if the device reports an error.
+ *
+ * hlo_selftest_bounded_wait enqueues one block that waits, bounded to about a millisecond, on a barrier
+ * nothing completes, and records HLO_FAULT_COPY_TIMEOUT as the streaming kernel would: it checks the
+ * reporting path without a failing copy.
+ * ---------------------------------------------------------------------------------------------- */
+#define HLO_FAULT_COPY_TIMEOUT 1u
+
+hlo_status hlo_device_faults(uint32_t* faults, int32_t clear);
+hlo_status hlo_selftest_bounded_wait(void* stream);
 
 /* Thread-local description of the last error returned on this thread ("" if none). */
 const char* hlo_last_error(void);

@@ -48,3 +48,16 @@ def test_single_process_aggregate_is_identity():
 
     assert bench.aggregate(3.5, "max") == 3.5
     assert bench.aggregate(7.0, "sum") == 7.0
+
+
+def test_gpus_flag_needs_one_process_per_gpu():
+    """--gpus N > 1 without torchrun (WORLD_SIZE unset) is refused instead of silently running one replica."""
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2
+    assert "torch.distributed.run" in r.stderr

@@ -210,6 +210,64 @@ def test_streaming_row_reduce_chunking(d3):
     check(f, run_gpu(f), ref, asum)
 
 
+def _reduce_case(name, data, dims, dtype, dimensions, kind, ops, init=0.0, round_each=True, out_dtype="f32"):
+    kept = [d for d in range(len(dims)) if d not in dimensions]
+    out_dims = [dims[d] for d in kept]
+    return inp.Fusion(name=name, kind="reduce", dims=dims, m2m=list(range(len(dims) - 1, -1, -1)), dtype=dtype,
+                      data=data, dimensions=dimensions, reduce_kind=kind, init=init,
+                      prologue={"ops": ops, "round_each": round_each} if ops else None,
+                      out_dims=out_dims, out_m2m=list(range(len(out_dims) - 1, -1, -1)), out_dtype=out_dtype)
+
+
+# row (short rows), row (bulk-copy stream), column, general
+REDUCE_PATTERNS = [([64, 1000], [1]), ([64, 8192], [1]), ([300, 64], [0]), ([4, 5, 6], [0, 2])]
+
+
+@pytest.mark.parametrize("dims,dimensions", REDUCE_PATTERNS)
+@pytest.mark.parametrize("dtype,round_each", [("f32", True), ("bf16", True), ("bf16", False)])
+def test_max_of_exp_chains_bit_exact(dims, dimensions, dtype, round_each):
+    """A max body keeps every term exact, so exp in the prologue is correctly rounded there (to the
+    element type, or to f32 for f32 intermediates) and the result is bit-exact."""
+    g = inp.rng(31)
+    n = int(np.prod(dims))
+    x = g.uniform(-20, 20, n).astype(np.float32)
+    data = x if dtype == "f32" else inp.f32_to_bf16_bits(x)
+    for ops in (["exp"], ["neg", "exp"]):
+        f = _reduce_case("maxexp", data, dims, dtype, dimensions, "max", ops, init=-math.inf, round_each=round_each)
+        ref, asum = run_oracle(f)
+        check(f, run_gpu(f), ref, asum)
+
+
+@pytest.mark.parametrize("dims,dimensions", REDUCE_PATTERNS)
+def test_exp_inside_longer_chains_of_add_reductions(dims, dimensions):
+    """exp followed by more ops is correctly rounded: exp -> log keeps tiny results (x down to -100, where
+    exp is subnormal), and exp -> add_const(-1) near 0 cancels to about x, both within the tolerance."""
+    g = inp.rng(37)
+    n = int(np.prod(dims))
+    deep = g.uniform(-100, -88, n).astype(np.float32)
+    f = _reduce_case("explog", deep, dims, "f32", dimensions, "add", ["exp", "log"])
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+    near0 = g.uniform(-1e-3, 1e-3, n).astype(np.float32)
+    f = _reduce_case("expm1", near0, dims, "f32", dimensions, "add", ["exp", ("add_const", -1.0)])
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_reduce_init_rounded_to_the_input_type(dtype):
+    """reduce (C2): init 0.1 is a value of the input element type."""
+    g = inp.rng(3)
+    x = g.uniform(-1, 1, 40 * 33).astype(np.float32)
+    data = {"f32": x, "bf16": inp.f32_to_bf16_bits(x), "f16": x.astype(np.float16).view(np.uint16)}[dtype]
+    for dims, dimensions in [([40, 33], [1]), ([40, 33], [0]), ([40, 0], [1])]:
+        d = data[: int(np.prod(dims))]
+        for kind in ("add", "max"):
+            f = _reduce_case("init01", d, dims, dtype, dimensions, kind, None, init=0.1)
+            ref, asum = run_oracle(f)
+            check(f, run_gpu(f), ref, asum)
+
+
 def test_bcast_row_reduce_variants():
     g = inp.rng(5)
     d0, d2, d3 = 2, 7, 515
@@ -320,6 +378,14 @@ def test_transpose_emitter_example_exp_abs():
     f = inp.Fusion(name="emit", kind="transpose", dims=dims, m2m=[2, 1, 0], dtype="f32", data=data,
                    permutation=[2, 1, 0], prologue={"ops": ["exp"]}, epilogue={"ops": ["abs"]},
                    out_dims=[170, 160, 20], out_m2m=[2, 1, 0], out_dtype="f32")
+    ref, _ = run_oracle(f)
+    check(f, run_gpu(f), ref, None)
+
+
+def test_transpose3_exp_abs_full_size():
+    """The transpose-emitter fusion scaled up (f32[512,640,680] -> [680,640,512]) as the benchmark runs
+    it, on every output."""
+    f = inp.transpose3_exp_abs(seed=1)
     ref, _ = run_oracle(f)
     check(f, run_gpu(f), ref, None)
 
@@ -748,3 +814,18 @@ def test_quant_add_full_size():
     f = inp.quant_add_s8(seed=2)
     ref = oracle.quant_binary(f.op, f.data, f.rhs, f.dims, f.in_q, f.in_q, f.out_q)
     assert np.array_equal(run_gpu(f), ref)
+
+
+# ---- device faults ---------------------------------------------------------------------------------------
+def test_bounded_wait_reports_a_fault():
+    """A bounded wait that runs out (one block waits about a millisecond on a barrier nothing completes)
+    records HLO_FAULT_COPY_TIMEOUT; the context stays usable and the bit clears."""
+    hf.device_faults(clear=True)
+    assert hf.device_faults() == 0
+    hf.selftest_bounded_wait()
+    assert hf.device_faults(clear=True) == hf.FAULT_COPY_TIMEOUT
+    assert hf.device_faults() == 0
+    f = inp.small("row_reduce_exp", seed=1)  # the device still runs fusions afterwards
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+    assert hf.device_faults() == 0

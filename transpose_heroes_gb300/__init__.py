@@ -28,11 +28,13 @@ DTYPES = {"f32": 0, "bf16": 1, "s8": 2, "f16": 3, "s32": 4}
 OPS = {"exp": 1, "log": 2, "abs": 3, "neg": 4, "add_bcast": 5, "tanh": 6, "add_const": 7, "mul_const": 8,
        "add_input": 9, "mul_input": 10}
 REDUCE_KINDS = {"add": 0, "max": 1}
+STATUS_INVALID_ARG = 1
 STATUS = {0: "HLO_OK", 1: "HLO_ERR_INVALID_ARG", 2: "HLO_ERR_UNSUPPORTED", 3: "HLO_ERR_CUDA", 4: "HLO_ERR_WORKSPACE"}
 
 # Every function the header declares; the library must export all of them.
 EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_workspace_size", "hlo_transpose_fusion", "hlo_layout_convert",
-           "hlo_quant_fusion", "hlo_quant_binary", "hlo_reduce_max_argmax", "hlo_last_error", "hlo_version")
+           "hlo_quant_fusion", "hlo_quant_binary", "hlo_reduce_max_argmax", "hlo_device_faults",
+           "hlo_selftest_bounded_wait", "hlo_last_error", "hlo_version")
 QUANT_BINARY_OPS = {"add": 0, "divide": 1, "maximum": 2, "minimum": 3, "multiply": 4}
 
 
@@ -96,6 +98,10 @@ def lib() -> ctypes.CDLL:
             h.hlo_reduce_max_argmax.argtypes = [P(Array), vp, P(Array), vp, P(i64), i32, ctypes.c_double, i64,
                                                 P(Array), vp, P(Array), vp, vp]
             h.hlo_reduce_max_argmax.restype = ctypes.c_int
+            h.hlo_device_faults.argtypes = [P(ctypes.c_uint32), i32]
+            h.hlo_device_faults.restype = ctypes.c_int
+            h.hlo_selftest_bounded_wait.argtypes = [vp]
+            h.hlo_selftest_bounded_wait.restype = ctypes.c_int
             h.hlo_last_error.restype = ctypes.c_char_p
             h.hlo_version.restype = ctypes.c_char_p
             _lib = h
@@ -159,7 +165,7 @@ def make_chain(spec) -> Optional[EwChain]:
     c = EwChain()
     ops = list(spec["ops"])
     if len(ops) > MAX_EW_OPS:
-        raise HloError(f"a chain holds at most {MAX_EW_OPS} ops")
+        raise HloError(STATUS_INVALID_ARG, f"a chain holds at most {MAX_EW_OPS} ops")
     c.n_ops = len(ops)
     for i, op in enumerate(ops):
         if isinstance(op, (tuple, list)):
@@ -246,6 +252,21 @@ def reduce_max_argmax(inp, in_dims, in_dtype, dimensions, out, out_idx, init_val
                                        len(list(dimensions)), float(init_value), int(init_index), ctypes.byref(o),
                                        _ptr(out), ctypes.byref(oi), _ptr(out_idx), _stream(stream)))
     return out, out_idx
+
+
+FAULT_COPY_TIMEOUT = 1
+
+
+def device_faults(clear: bool = False) -> int:
+    """hlo_device_faults: the fault bits kernels recorded on the current device (waits for the device)."""
+    f = ctypes.c_uint32(0)
+    _check(lib().hlo_device_faults(ctypes.byref(f), 1 if clear else 0))
+    return int(f.value)
+
+
+def selftest_bounded_wait(stream=None) -> None:
+    """hlo_selftest_bounded_wait: one block's bounded wait runs out and records FAULT_COPY_TIMEOUT."""
+    _check(lib().hlo_selftest_bounded_wait(_stream(stream)))
 
 
 def reduce_workspace_size(in_dims, in_dtype, dimensions, in_m2m=None) -> int:

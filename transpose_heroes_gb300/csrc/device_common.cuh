@@ -48,8 +48,12 @@ __device__ __forceinline__ float round_to_dt(float v, int dt) {
   return v;
 }
 
-// exp(x) = 2^(x log2 e) on the SFU: relative error ~2^-21, used where the hero is a float reduction
-// whose tolerance absorbs it.
+// exp(x) = 2^(x log2 e) on the SFU. Used only as the last op before an add-combine of a float
+// reduction: RN(x log2 e) carries a relative error of at most 2^-24 |x log2 e| <= 2^-17 for the finite
+// range |x| < 89, so a term's relative error stays below about 2^-17 (plus the SFU's own ~2^-22) --
+// inside the add reduction's tolerance of 1e-5 sum|terms|. Results below 2^-126 are flushed to zero
+// (an absolute error under 2^-126 per term). Never used where a value is rounded afterwards for a
+// bit-exact result (max bodies, transposes, elementwise chains).
 __device__ __forceinline__ float fast_exp(float x) {
   float t = __fmul_rn(x, 1.4426950408889634f);
   float y;
@@ -85,8 +89,6 @@ struct LogTab {
 };
 __device__ __forceinline__ LogTab global_log_tables() { return {kLogCTab, kLogETab}; }
 
-// One elementwise op. FAST_EXP selects the SFU exp (reductions) or the correctly rounded exp
-// (elsewhere; CUDA's expf settles the 16-bit types).
 // Correct rounding into a 16-bit float type from an f32 approximation y of f(x) with an error of at
 // most 2 f32 ulps: if y - 2 ulp and y + 2 ulp round alike, so does f(x) (rounding is monotone).
 // Returns false (and leaves r unset) when they do not, or when y sits next to 0, the subnormals or
@@ -120,15 +122,20 @@ static __device__ __noinline__ float exp_round16_slow(float x, int dt) { return 
 static __device__ __noinline__ float tanh_round16_slow(float x, int dt) { return round16_from_double(tanh((double)x), dt); }
 static __device__ __noinline__ float log_round16_slow(float x, int dt) { return round16_from_double(log((double)x), dt); }
 
-template <bool FAST_EXP>
+// exp as a chain op: correctly rounded to f32, or (r16) to the 16-bit element type dt, where CUDA's
+// expf settles almost every element.
+__device__ __forceinline__ float chain_exp(float v, bool r16, int dt) {
+  float r;
+  if (!r16) return cr_expf(v);
+  return round16_settled(expf(v), dt, r) ? r : exp_round16_slow(v, dt);
+}
+
+// One elementwise op of a chain, every result correctly rounded (exp, log, tanh) or exact.
 __device__ __forceinline__ float apply_op(int op, float v, float b, float x, float imm, bool r16, int dt,
                                           const LogTab& lt) {
   float r;
   switch (op) {
-    case OP_EXP:
-      if (FAST_EXP) return fast_exp(v);
-      if (!r16) return cr_expf(v);
-      return round16_settled(expf(v), dt, r) ? r : exp_round16_slow(v, dt);
+    case OP_EXP: return chain_exp(v, r16, dt);
     case OP_LOG:
       if (!r16) return cr_logf(v, lt.c, lt.e);
       return round16_settled(cr_logf(v, lt.c, lt.e), dt, r) ? r : log_round16_slow(v, dt);
@@ -150,7 +157,6 @@ __device__ __forceinline__ float apply_op(int op, float v, float b, float x, flo
 // With round16 every op result is rounded to the 16-bit element type: f32 arithmetic on two 16-bit
 // values followed by one rounding equals the correctly rounded 16-bit operation (f32 has at least
 // 2p + 2 significand bits for p = 8 and 11).
-template <bool FAST_EXP>
 __device__ __forceinline__ float apply_chain_rt(const Chain& c, float v, int64_t boff, const LogTab& lt) {
   const float x = v;
   const bool r16 = c.round16 && (c.dt == BF16 || c.dt == F16);
@@ -158,7 +164,7 @@ __device__ __forceinline__ float apply_chain_rt(const Chain& c, float v, int64_t
     const int op = c.op[k];
     float b = 0.f;
     if (op == OP_ADD_BCAST) b = load_as_f32(c.bptr, c.bdt, boff);
-    v = apply_op<FAST_EXP>(op, v, b, x, c.imm[k], r16, c.dt, lt);
+    v = apply_op(op, v, b, x, c.imm[k], r16, c.dt, lt);
     if (c.round16) v = round_to_dt(v, c.dt);
   }
   return v;

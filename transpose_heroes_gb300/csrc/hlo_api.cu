@@ -317,6 +317,13 @@ hlo_status plan_gather_plain(const hlo_array& in, const void* in_ptr, const hlo_
 
 }  // namespace
 
+// The occupancy queries below may leave an error of their own in CUDA's sticky last-error slot; that
+// one is cleared so the next launch check does not report it. An error that was already pending when
+// the query began (from the caller's earlier asynchronous work) is left in place.
+static void clear_query_error(cudaError_t pending) {
+  if (pending == cudaSuccess) cudaGetLastError();
+}
+
 int hlo::device_sm_count() {
   static int cache[64] = {0};
   int dev = 0;
@@ -338,6 +345,7 @@ void hlo::table_cluster_shape(const void* kernel, int threads, size_t smem, int*
   auto key = std::make_pair(kernel, dev);
   auto it = cache.find(key);
   if (it == cache.end()) {
+    const cudaError_t pending = cudaPeekAtLastError();
     cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     std::pair<int, int> best(2, 1);
     for (int cs : {8, 4, 2}) {
@@ -359,7 +367,7 @@ void hlo::table_cluster_shape(const void* kernel, int threads, size_t smem, int*
         break;
       }
     }
-    cudaGetLastError();  // clear any error from the queries above
+    clear_query_error(pending);
     it = cache.emplace(key, best).first;
   }
   *cluster_size = it->second.first;
@@ -375,10 +383,11 @@ int hlo::kernel_blocks_per_sm(const void* kernel, int threads, size_t smem) {
   auto key = std::make_pair(kernel, dev * 4096 + threads);
   auto it = cache.find(key);
   if (it != cache.end()) return it->second;
+  const cudaError_t pending = cudaPeekAtLastError();
   if (smem > 0) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int nb = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel, threads, smem) != cudaSuccess || nb < 1) nb = 1;
-  cudaGetLastError();  // clear any error from the queries above
+  clear_query_error(pending);
   cache[key] = nb;
   return nb;
 }
@@ -532,6 +541,22 @@ hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const 
   return cuda_status(launch_argmax(p, as_stream(stream)), "argmax launch");
 }
 
+hlo_status hlo_device_faults(uint32_t* faults, int32_t clear) {
+  if (!faults) return fail(HLO_ERR_INVALID_ARG, "device_faults: faults is NULL");
+  *faults = 0;
+  unsigned int fr = 0, ft = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = read_faults_reduce(&fr, clear != 0);
+  if (e == cudaSuccess) e = read_faults_transpose(&ft, clear != 0);
+  hlo_status st = cuda_status(e, "device_faults");
+  if (st == HLO_OK) *faults = fr | ft;
+  return st;
+}
+
+hlo_status hlo_selftest_bounded_wait(void* stream) {
+  return cuda_status(launch_wait_selftest(as_stream(stream)), "bounded-wait self test launch");
+}
+
 const char* hlo_last_error(void) { return g_err.c_str(); }
 
 const char* hlo_version(void) { return "hlofusion 0.1 (sm_103a)"; }
@@ -588,7 +613,8 @@ hlo_status hlo_reduce_fusion(const hlo_array* in, const void* in_ptr, const hlo_
   if (ranges_overlap(in_ptr, n_in * dt_bytes(in->dtype), out_ptr, n_out * dt_bytes(out->dtype)))
     return fail(HLO_ERR_INVALID_ARG, "reduce: input and output overlap");
   const cudaStream_t s = as_stream(stream);
-  const float init = (float)init_value;
+  // init_values has the inputs' element type ("reduce" C2): the literal is rounded to it
+  const float init = constant_of_type(init_value, in->dtype);
   if (n_out == 0) return ok();
   int64_t n_red = 1;
   for (int d = 0; d < in->rank; ++d)

@@ -206,6 +206,14 @@ struct QuantBinaryPlan {
   QuantParams ql, qr, qo;
 };
 cudaError_t launch_quant_binary(const QuantBinaryPlan& p, cudaStream_t s);
+// Device-side faults (bit mask, the same values as HLO_FAULT_* of the C ABI).
+constexpr unsigned int kFaultCopyTimeout = 1u;
+// Copy the fault word of a translation unit out (and clear it when asked); the caller has waited for
+// the device.
+cudaError_t read_faults_reduce(unsigned int* faults, bool clear);
+cudaError_t read_faults_transpose(unsigned int* faults, bool clear);
+// Launches the bounded-wait self test (sets kFaultCopyTimeout after about a millisecond).
+cudaError_t launch_wait_selftest(cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s);
 cudaError_t launch_col_reduce(const ColReducePlan& p, cudaStream_t s);
 cudaError_t launch_gen_reduce(const GenReducePlan& p, cudaStream_t s);

@@ -18,8 +18,8 @@ struct EwPlan {
 };
 
 __device__ __forceinline__ float ew_apply(const EwPlan& p, float v, const LogTab& lt) {
-  v = apply_chain_rt<false>(p.pro, v, 0, lt);
-  return apply_chain_rt<false>(p.epi, v, 0, lt);
+  v = apply_chain_rt(p.pro, v, 0, lt);
+  return apply_chain_rt(p.epi, v, 0, lt);
 }
 
 // Two elements of log through the first pass, the rest of the correctly rounded log where it
@@ -172,8 +172,8 @@ __device__ __forceinline__ uint32_t bf16_fn2(int op, uint32_t w, const LogTab& l
   // the f32 value's bf16 rounding is the correct one unless the bits it drops lie within `ulps`
   // of the midpoint; then the correctly rounded 16-bit path decides
   if (bf16_clear_of_midpoint(f.x, ulps) && bf16_clear_of_midpoint(f.y, ulps)) return pk_pack<BF16>(f.x, f.y);
-  return pk_pack<BF16>(apply_op<false>(op, a, 0.f, 0.f, 0.f, true, BF16, lt),
-                       apply_op<false>(op, b, 0.f, 0.f, 0.f, true, BF16, lt));
+  return pk_pack<BF16>(apply_op(op, a, 0.f, 0.f, 0.f, true, BF16, lt),
+                       apply_op(op, b, 0.f, 0.f, 0.f, true, BF16, lt));
 }
 
 // The chain on kV packed pairs (2 kV elements); the op dispatch is shared by all of them.
@@ -217,8 +217,8 @@ __device__ __forceinline__ void chain16x2(const Chain& c, uint32_t (&v)[kV], con
         } else {
 #pragma unroll
           for (int j = 0; j < kV; ++j)
-            v[j] = pk_pack<DT>(apply_op<false>(op, pk_lo<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt),
-                               apply_op<false>(op, pk_hi<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt));
+            v[j] = pk_pack<DT>(apply_op(op, pk_lo<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt),
+                               apply_op(op, pk_hi<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt));
         }
       }
     }
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(256) elementwise_16x2_kernel(EwPlan p) {
     out[2 * i + 1] = make_uint4(v[4], v[5], v[6], v[7]);
   }
   for (int64_t e = nv * 16 + tid; e < p.n; e += stride) {
-    const float r = apply_chain_rt<false>(p.pro, load_as_f32(p.in, DT, e), 0, lt);
+    const float r = apply_chain_rt(p.pro, load_as_f32(p.in, DT, e), 0, lt);
     store_from_f32(p.out, DT, e, r);
   }
 }

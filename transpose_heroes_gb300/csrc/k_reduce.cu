@@ -13,6 +13,7 @@
 //  gen_reduce_kernel  -- any other pattern: one thread per output element.
 #include <cooperative_groups.h>
 
+#include "async_copy.cuh"
 #include "device_common.cuh"
 
 namespace cg = cooperative_groups;
@@ -55,8 +56,8 @@ __device__ __forceinline__ float row_vec(uint4 x, uint4 b, float acc, const Chai
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float t = v[i];
-      if (CH == RC_EXP) t = fast_exp(t);
-      if (CH == RC_RT) t = apply_chain_rt<true>(ch, t, 0, lt);
+      if (CH == RC_EXP) t = KIND == RED_ADD ? fast_exp(t) : cr_expf(t);
+      if (CH == RC_RT) t = apply_chain_rt(ch, t, 0, lt);
       acc = combine<KIND>(acc, t);
     }
     return acc;
@@ -75,8 +76,16 @@ __device__ __forceinline__ float row_vec(uint4 x, uint4 b, float acc, const Chai
         hi = f16_bits_to_f32((uint16_t)(w[i] >> 16));
       }
       if (CH == RC_EXP_BCAST_BF16) {
-        // bf16(exp(x)) then the bf16 add with the broadcast pair, rounded once (add.rn.bf16x2)
-        float elo = fast_exp(lo), ehi = fast_exp(hi);
+        // bf16(exp(x)) then the bf16 add with the broadcast pair, rounded once (add.rn.bf16x2); a max
+        // body keeps every term exact, so it takes the correctly rounded bf16 exp
+        float elo, ehi;
+        if (KIND == RED_ADD) {
+          elo = fast_exp(lo);
+          ehi = fast_exp(hi);
+        } else {
+          elo = chain_exp(lo, true, BF16);
+          ehi = chain_exp(hi, true, BF16);
+        }
         uint32_t e2, s2;
         asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(e2) : "f"(ehi), "f"(elo));
         asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(s2) : "r"(e2), "r"(bw[i]));
@@ -84,16 +93,21 @@ __device__ __forceinline__ float row_vec(uint4 x, uint4 b, float acc, const Chai
         hi = __uint_as_float(s2 & 0xFFFF0000u);
       } else {
         if (CH == RC_EXP) {
-          lo = fast_exp(lo);
-          hi = fast_exp(hi);
-          if (ch.round16) {
-            lo = round_to_dt(lo, IN_DT);
-            hi = round_to_dt(hi, IN_DT);
+          if (KIND == RED_ADD) {
+            lo = fast_exp(lo);
+            hi = fast_exp(hi);
+            if (ch.round16) {
+              lo = round_to_dt(lo, IN_DT);
+              hi = round_to_dt(hi, IN_DT);
+            }
+          } else {
+            lo = chain_exp(lo, ch.round16, IN_DT);
+            hi = chain_exp(hi, ch.round16, IN_DT);
           }
         }
         if (CH == RC_RT) {
-          lo = apply_chain_rt<true>(ch, lo, 0, lt);
-          hi = apply_chain_rt<true>(ch, hi, 0, lt);
+          lo = apply_chain_rt(ch, lo, 0, lt);
+          hi = apply_chain_rt(ch, hi, 0, lt);
         }
       }
       part = combine<KIND>(part, combine<KIND>(lo, hi));
@@ -153,14 +167,18 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_kernel(RowReducePlan p
     for (int64_t e = tail_start + tid; e < len; e += nt) {
       float t = load_as_f32(base, IN_DT, e);
       if (CH == RC_EXP) {
-        t = fast_exp(t);
-        if (p.chain.round16) t = round_to_dt(t, IN_DT);
+        if (KIND == RED_ADD) {
+          t = fast_exp(t);
+          if (p.chain.round16) t = round_to_dt(t, IN_DT);
+        } else {
+          t = chain_exp(t, p.chain.round16 && IN_DT != F32, IN_DT);
+        }
       } else if (CH == RC_EXP_BCAST_BF16) {
-        t = round_to_dt(fast_exp(t), BF16);
+        t = KIND == RED_ADD ? round_to_dt(fast_exp(t), BF16) : chain_exp(t, true, BF16);
         t = round_to_dt(__fadd_rn(t, load_as_f32(p.chain.bptr, BF16, e)), BF16);
       } else if (CH == RC_RT) {
         int64_t boff = p.bmode == BC_ROWVEC ? e : p.bmode == BC_PERROW ? map_index(p.bmap, row) : 0;
-        t = apply_chain_rt<true>(p.chain, t, boff, lt);
+        t = apply_chain_rt(p.chain, t, boff, lt);
       }
       acc = combine<KIND>(acc, t);
     }
@@ -183,29 +201,6 @@ constexpr int kStreamWarps = kStreamThreads / 32;
 constexpr int kChunkBytes = 16384;
 constexpr int kStages = 3;
 constexpr int kRowSlots = 8;  // > the rows kStages chunks can span, so a slot is free when reused
-constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz: far beyond any legitimate wait
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Waits for phase `parity` of the mbarrier; returns false if the bound ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  long long t0 = -1;
-  while (true) {
-    uint32_t done;
-    asm volatile(
-        "{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-    const long long now = clock64();
-    if (t0 < 0) t0 = now;
-    else if (now - t0 > kWaitCycles) return false;
-  }
-}
-
 // Packed (float2) element work of the streaming row reduce for the add body: two independent
 // f32 partial sums per thread, combined at the end of the row.
 __device__ __forceinline__ float ex2_approx(float t) {
@@ -268,12 +263,12 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
   const int64_t n_chunks = my_rows * cpr;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[s])));
+      mbar_init(smem_addr(&bar[s]), 1);
       stage_cnt[s] = 0;
       last_issued[s] = -1;
     }
     for (int r = 0; r < kRowSlots; ++r) row_cnt[r] = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_mbar_init();
     abort_flag = 0;
   }
   __syncthreads();
@@ -288,11 +283,9 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
     const int s = (int)(g % kStages);
     const uint32_t b = smem_addr(&bar[s]);
     last_issued[s] = g;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_addr(ring + s * kChunkBytes)), "l"(src), "r"(bytes), "r"(b)
-                 : "memory");
+    fence_proxy_async();
+    mbar_arrive_expect_tx(b, bytes);
+    bulk_load(ring + s * kChunkBytes, src, bytes, b);
   };
   if (tid == 0) {
     int64_t row = blockIdx.x;
@@ -404,8 +397,9 @@ __global__ void __launch_bounds__(kStreamThreads) row_stream_kernel(RowReducePla
   }
   __syncthreads();  // every warp has left the loop (finished, or given up after a bounded wait)
   if (abort_flag) {
-    // a copy did not complete in time: wait (bounded) for each stage's last copy, then mark this
-    // block's rows NaN so the failure shows in the output
+    // a copy did not complete in time: record the fault for hlo_device_faults(), wait (bounded) for
+    // each stage's last copy, then mark this block's rows NaN so the failure also shows in the output
+    if (tid == 0) record_fault(kFaultCopyTimeout);
     if (tid == 0)
       for (int st = 0; st < kStages; ++st)
         if (last_issued[st] >= 0)
@@ -455,7 +449,7 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_rt_kernel(RowReducePla
     for (int64_t e = threadIdx.x; e < p.len; e += blockDim.x) {
       float t = load_as_f32(base, IN_DT, e);
       int64_t boff = p.bmode == BC_ROWVEC ? e : rowb;
-      t = apply_chain_rt<true>(p.chain, t, boff, lt);
+      t = apply_chain_rt(p.chain, t, boff, lt);
       acc = combine<KIND>(acc, t);
     }
     acc = block_reduce<KIND>(acc, red);
@@ -530,6 +524,25 @@ cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s) {
   return p.kind == RED_ADD ? row_dispatch<F16, RED_ADD>(p, s, ch, vec) : row_dispatch<F16, RED_MAX>(p, s, ch, vec);
 }
 
+// ---- device faults -------------------------------------------------------------------------------
+// One block waits, with a short bound, on an mbarrier that nothing completes: the bounded wait of the
+// streaming kernels runs out and records the same fault bit they record, so that the reporting path
+// can be checked without a failing copy.
+__global__ void wait_selftest_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_addr(&bar), 1);
+  fence_mbar_init();
+  if (!mbar_wait(smem_addr(&bar), 0, limit)) record_fault(kFaultCopyTimeout);
+}
+
+cudaError_t launch_wait_selftest(cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(2000000LL);  // ~1 ms
+  return cudaGetLastError();
+}
+
+cudaError_t read_faults_reduce(unsigned int* faults, bool clear) { return read_tu_faults(faults, clear); }
+
 // ---- column reduce --------------------------------------------------------------------------------
 constexpr int kColCluster = 8;
 constexpr int kColWarps = 8;
@@ -580,14 +593,14 @@ __global__ void __launch_bounds__(kColWarps * 32) col_reduce_kernel(ColReducePla
           for (int i = 0; i < 4; ++i) {
             if (IN_DT == F32) {
               float t = __uint_as_float(w[i]);
-              if (RT) t = apply_chain_rt<true>(p.chain, t, 0, lt);
+              if (RT) t = apply_chain_rt(p.chain, t, 0, lt);
               acc[i] = combine<KIND>(acc[i], t);
             } else {
               float lo = IN_DT == BF16 ? bf16_bits_to_f32(w[i] & 0xFFFFu) : f16_bits_to_f32((uint16_t)(w[i] & 0xFFFFu));
               float hi = IN_DT == BF16 ? __uint_as_float(w[i] & 0xFFFF0000u) : f16_bits_to_f32((uint16_t)(w[i] >> 16));
               if (RT) {
-                lo = apply_chain_rt<true>(p.chain, lo, 0, lt);
-                hi = apply_chain_rt<true>(p.chain, hi, 0, lt);
+                lo = apply_chain_rt(p.chain, lo, 0, lt);
+                hi = apply_chain_rt(p.chain, hi, 0, lt);
               }
               acc[2 * i] = combine<KIND>(acc[2 * i], lo);
               acc[2 * i + 1] = combine<KIND>(acc[2 * i + 1], hi);
@@ -602,14 +615,14 @@ __global__ void __launch_bounds__(kColWarps * 32) col_reduce_kernel(ColReducePla
         for (int i = 0; i < 4; ++i) {
           if (IN_DT == F32) {
             float t = __uint_as_float(w[i]);
-            if (RT) t = apply_chain_rt<true>(p.chain, t, 0, lt);
+            if (RT) t = apply_chain_rt(p.chain, t, 0, lt);
             acc[i] = combine<KIND>(acc[i], t);
           } else {
             float lo = IN_DT == BF16 ? bf16_bits_to_f32(w[i] & 0xFFFFu) : f16_bits_to_f32((uint16_t)(w[i] & 0xFFFFu));
             float hi = IN_DT == BF16 ? __uint_as_float(w[i] & 0xFFFF0000u) : f16_bits_to_f32((uint16_t)(w[i] >> 16));
             if (RT) {
-              lo = apply_chain_rt<true>(p.chain, lo, 0, lt);
-              hi = apply_chain_rt<true>(p.chain, hi, 0, lt);
+              lo = apply_chain_rt(p.chain, lo, 0, lt);
+              hi = apply_chain_rt(p.chain, hi, 0, lt);
             }
             acc[2 * i] = combine<KIND>(acc[2 * i], lo);
             acc[2 * i + 1] = combine<KIND>(acc[2 * i + 1], hi);
@@ -619,7 +632,7 @@ __global__ void __launch_bounds__(kColWarps * 32) col_reduce_kernel(ColReducePla
     } else {
       for (int64_t r = r0 + warp; r < r1; r += kColWarps) {
         float t = load_as_f32(base, IN_DT, r * B + col0);
-        if (RT) t = apply_chain_rt<true>(p.chain, t, 0, lt);
+        if (RT) t = apply_chain_rt(p.chain, t, 0, lt);
         acc[0] = combine<KIND>(acc[0], t);
       }
     }
@@ -712,7 +725,7 @@ __global__ void __launch_bounds__(256) gen_reduce_kernel(GenReducePlan p) {
       off += ridx[j] * p.rdim_in_stride[j];
       boff += ridx[j] * p.chain.bstride[p.rdim_logical[j]];
     }
-    float v = apply_chain_rt<true>(p.chain, load_as_f32(p.in, p.in_dt, off), boff, lt);
+    float v = apply_chain_rt(p.chain, load_as_f32(p.in, p.in_dt, off), boff, lt);
     chunk = combine_rt(p.kind, chunk, v);
     if ((t & 255) == 255) {
       total = combine_rt(p.kind, total, chunk);

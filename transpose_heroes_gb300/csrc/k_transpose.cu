@@ -14,6 +14,11 @@
 //                          4 bytes at a time, 4x4 byte transposes in registers, 16-byte stores.
 //  gather_kernel        -- everything else: one thread per output element.
 #include "device_common.cuh"
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "async_copy.cuh"
 #include "quant_common.cuh"
 
 namespace hlo {
@@ -46,7 +51,7 @@ __device__ __forceinline__ void pair_of(int64_t item, int64_t nt, int64_t& I, in
 template <int CH>
 __device__ __forceinline__ float pair_pro(float v, const Chain& c, const LogTab& lt) {
   if (CH == PC_LOG) return cr_logf(v, lt.c, lt.e);
-  if (CH == PC_RT) return apply_chain_rt<false>(c, v, 0, lt);
+  if (CH == PC_RT) return apply_chain_rt(c, v, 0, lt);
   return v;
 }
 
@@ -195,10 +200,10 @@ __device__ __forceinline__ void pair_store(float* __restrict__ out, int64_t n, i
     v.z = __fadd_rn(o[2 * kTP], t[2]);
     v.w = __fadd_rn(o[3 * kTP], t[3]);
     if (epi.n) {
-      v.x = apply_chain_rt<false>(epi, v.x, 0, lt);
-      v.y = apply_chain_rt<false>(epi, v.y, 0, lt);
-      v.z = apply_chain_rt<false>(epi, v.z, 0, lt);
-      v.w = apply_chain_rt<false>(epi, v.w, 0, lt);
+      v.x = apply_chain_rt(epi, v.x, 0, lt);
+      v.y = apply_chain_rt(epi, v.y, 0, lt);
+      v.z = apply_chain_rt(epi, v.z, 0, lt);
+      v.w = apply_chain_rt(epi, v.w, 0, lt);
     }
     const int64_t gr = TI * kT + r, gc = TJ * kT + col;
     if (VEC) {
@@ -360,10 +365,10 @@ __device__ __forceinline__ void block_store(float* dst, int64_t n, const float4 
     v.z = __fadd_rn(a[k].z, comp(b[2], k));
     v.w = __fadd_rn(a[k].w, comp(b[3], k));
     if (EPI) {
-      v.x = apply_chain_rt<false>(epi, v.x, 0, lt);
-      v.y = apply_chain_rt<false>(epi, v.y, 0, lt);
-      v.z = apply_chain_rt<false>(epi, v.z, 0, lt);
-      v.w = apply_chain_rt<false>(epi, v.w, 0, lt);
+      v.x = apply_chain_rt(epi, v.x, 0, lt);
+      v.y = apply_chain_rt(epi, v.y, 0, lt);
+      v.z = apply_chain_rt(epi, v.z, 0, lt);
+      v.w = apply_chain_rt(epi, v.w, 0, lt);
     }
     if (cols_ok && k < rows) *reinterpret_cast<float4*>(dst + k * n) = v;
   }
@@ -461,6 +466,213 @@ __global__ void __launch_bounds__(kPairThreads, 4)
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Tensor-copy pair kernel (the path for rows on 16-byte boundaries when the driver's tensor-map
+// encoder is available). The same thread mapping, prologue, swizzle and transposed stores as
+// selfadd_block_kernel, but the raw input arrives by 2-D tensor copies (cp.async.bulk.tensor, one
+// 64 x 64 box per tile) into a ring of NS shared-memory stages, and the prologue's results are
+// written back into the stage they were read from:
+//   wait for the stage's mbarrier; then per tile: 16-byte reads of the raw rows (a quarter warp reads
+//   128 contiguous bytes), the prologue in registers, __syncwarp, 16-byte writes of the results to
+//   the swizzled positions. A thread's swizzled chunk lies in its own four rows, which only its own
+//   half warp reads, so the warp-level sync orders the in-place rewrite; then the warp settles its
+//   open log elements; block barrier; transposed reads, add, 16-byte stores.
+// The barrier of item j also tells thread 0 that every thread is done with item j-1, so the stage
+// item j-1 used is refilled there with item j + NS - 1: the copies run NS - 1.5 items ahead of use
+// and one barrier per item suffices.
+// A bounded wait that runs out makes the whole block stop (the decision is made block-wide at the
+// barrier), record kFaultCopyTimeout, wait (bounded) for its copies in flight and return.
+// ---------------------------------------------------------------------------------------------
+template <int NS>
+struct TmaShared {
+  float l1_inv[32], l1_hi[32], l1_lo[32];
+  uint16_t wlist[kPairThreads / 32][kWarpList];
+  uint64_t full[NS];
+};
+
+template <int NS>
+static size_t tma_smem_bytes() {
+  return 128 /* alignment slack */ + (size_t)NS * 2 * kT * kT * sizeof(float) + HLO_LOG_NC * sizeof(float4) +
+         HLO_LOG_NE * sizeof(float2) + sizeof(TmaShared<NS>);
+}
+
+// Prologue of one raw tile of the stage, written back in place (swizzled); open log elements keep
+// their input and set their bits in `open` (from bit `shift`).
+template <int CH>
+__device__ __forceinline__ void tma_tile_prologue(float* tile, int raw, int own, const SelfAddPlan& p, const LogTab& lt,
+                                                  const float* tinv, const float* thi, const float* tlo, uint32_t& open,
+                                                  int shift) {
+  float4 v[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const float4*>(tile + raw + k * kT);
+  if (CH == PC_LOG) {
+    block_log(v, tinv, thi, tlo, open, shift);
+  } else if (CH == PC_RT) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k].x = pair_pro<CH>(v[k].x, p.pro, lt);
+      v[k].y = pair_pro<CH>(v[k].y, p.pro, lt);
+      v[k].z = pair_pro<CH>(v[k].z, p.pro, lt);
+      v[k].w = pair_pro<CH>(v[k].w, p.pro, lt);
+    }
+  }
+  __syncwarp();  // the half warp owning these rows has read them
+#pragma unroll
+  for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(tile + own + k * kT) = v[k];
+}
+
+template <int CH, bool EPI, int NS>
+__global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
+    selfadd_tma_kernel(const __grid_constant__ CUtensorMap tmap, SelfAddPlan p, int64_t nt, int64_t n_off,
+                       int64_t n_items) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  float* stage = reinterpret_cast<float*>(base);              // [NS][2][64 * 64]: tile (I,J), tile (J,I)
+  float4* s_lc = reinterpret_cast<float4*>(stage + NS * 2 * kT * kT);
+  float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
+  TmaShared<NS>& ts = *reinterpret_cast<TmaShared<NS>*>(s_le + HLO_LOG_NE);
+  const int tid = threadIdx.x;
+  // copies item `it` (walk position j) into stage j % NS
+  auto issue = [&](int64_t it, int64_t j) {
+    int64_t I, J;
+    item_pair(it, nt, n_off, I, J);
+    const int st = (int)(j % NS);
+    const uint32_t bar = smem_addr(&ts.full[st]);
+    float* dst = stage + st * 2 * kT * kT;
+    mbar_arrive_expect_tx(bar, (I != J ? 2u : 1u) * kT * kT * (uint32_t)sizeof(float));
+    tma_load_2d(dst, &tmap, (int32_t)(J * kT), (int32_t)(I * kT), bar);                      // tile (I, J)
+    if (I != J) tma_load_2d(dst + kT * kT, &tmap, (int32_t)(I * kT), (int32_t)(J * kT), bar);  // tile (J, I)
+  };
+  if (tid == 0) {
+    prefetch_tensor_map(&tmap);
+    for (int st = 0; st < NS; ++st) mbar_init(smem_addr(&ts.full[st]), 1);
+    fence_mbar_init();
+    for (int64_t j = 0; j < NS; ++j) {
+      const int64_t it = blockIdx.x + j * gridDim.x;
+      if (it < n_items) issue(it, j);
+    }
+  }
+  load_log_tables(s_lc, s_le);
+  load_log1_tables(ts.l1_inv, ts.l1_hi, ts.l1_lo);
+  __syncthreads();
+  const LogTab lt = {s_lc, s_le};
+  float* out = reinterpret_cast<float*>(p.out);
+  const int64_t n = p.n;
+  const int bi = tid >> 4, bj = tid & 15;
+  const int own = 4 * bi * kT + ((bj ^ (bi & 7)) << 2);  // row 4*bi, chunk bj (swizzled)
+  const int oth = 4 * bj * kT + ((bi ^ (bj & 7)) << 2);  // row 4*bj, chunk bi (swizzled)
+  const int raw = 4 * bi * kT + 4 * bj;                  // row 4*bi, columns 4*bj.. of a raw tile
+  const int64_t goff = 4 * bi * n + 4 * bj;
+  uint16_t* wl = ts.wlist[tid >> 5];
+  int64_t j = 0;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+    int64_t I, J;
+    item_pair(item, nt, n_off, I, J);
+    const bool two = I != J;
+    const int st = (int)(j % NS);
+    const bool arrived = mbar_wait(smem_addr(&ts.full[st]), (uint32_t)((j / NS) & 1));
+    float* ta = stage + st * 2 * kT * kT;
+    float* tb = ta + kT * kT;
+    uint32_t open = 0;
+    tma_tile_prologue<CH>(ta, raw, own, p, lt, ts.l1_inv, ts.l1_hi, ts.l1_lo, open, 0);
+    if (two) tma_tile_prologue<CH>(tb, raw, own, p, lt, ts.l1_inv, ts.l1_hi, ts.l1_lo, open, 16);
+    if (CH == PC_LOG) warp_settle(open, ta, own, wl, lt);
+    // every tile of item j is complete, and every thread is done with item j - 1
+    if (__syncthreads_or(arrived ? 0 : 1)) {
+      // a copy did not arrive in time: record the fault, wait (bounded) for this block's copies still
+      // in flight (items j .. j + NS - 2, plus j + NS - 1 if it was issued), leave the rest of its
+      // outputs unwritten and return
+      if (tid == 0) {
+        record_fault(kFaultCopyTimeout);
+        for (int64_t q = j; q < j + NS && blockIdx.x + q * gridDim.x < n_items; ++q)
+          if (q < j + NS - 1 || j == 0) mbar_wait(smem_addr(&ts.full[q % NS]), (uint32_t)((q / NS) & 1));
+      }
+      return;
+    }
+    if (tid == 0 && j > 0) {  // refill the stage of item j - 1 with item j + NS - 1
+      const int64_t nxt = item + (int64_t)(NS - 1) * gridDim.x;
+      if (nxt < n_items) {
+        fence_proxy_async();
+        issue(nxt, j + NS - 1);
+      }
+    }
+    const int64_t rows_a = n - I * kT - 4 * bi, rows_b = n - J * kT - 4 * bi;
+    const bool ca = J * kT + 4 * bj < n, cb = I * kT + 4 * bj < n;
+    {
+      float4 a[4], b[4];
+      const float* other = two ? tb : ta;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[k] = *reinterpret_cast<const float4*>(ta + own + k * kT);
+        b[k] = *reinterpret_cast<const float4*>(other + oth + k * kT);
+      }
+      block_store<EPI>(out + (I * kT) * n + J * kT + goff, n, a, b, rows_a, ca, p.epi, lt);  // out(I,J) = A + B^T
+    }
+    if (two) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[k] = *reinterpret_cast<const float4*>(tb + own + k * kT);
+        b[k] = *reinterpret_cast<const float4*>(ta + oth + k * kT);
+      }
+      block_store<EPI>(out + (J * kT) * n + I * kT + goff, n, a, b, rows_b, cb, p.epi, lt);  // out(J,I) = B + A^T
+    }
+  }
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link against libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool looked = false;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!looked) {
+    looked = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else
+      cudaGetLastError();  // the lookup's own error, if any: the caller falls back to plain loads
+  }
+  return fn;
+}
+
+// A 2-D f32 tensor map over the n x n row-major input with 64 x 64 boxes; false if it cannot be made.
+static bool make_pair_tensor_map(const SelfAddPlan& p, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || p.n > (int64_t)INT32_MAX) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)p.n, (cuuint64_t)p.n};
+  const cuuint64_t strides[1] = {(cuuint64_t)p.n * sizeof(float)};
+  const cuuint32_t box[2] = {kT, kT};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(p.in), dims, strides, box, elem_strides,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#ifndef HLO_SELFADD_STAGES
+#define HLO_SELFADD_STAGES 3
+#endif
+template <int CH, bool EPI>
+static cudaError_t tma_launch(const SelfAddPlan& p, const CUtensorMap& map, cudaStream_t s) {
+  constexpr int NS = HLO_SELFADD_STAGES;
+  auto kernel = selfadd_tma_kernel<CH, EPI, NS>;
+  const size_t smem = tma_smem_bytes<NS>();
+  const int nb = kernel_blocks_per_sm((const void*)kernel, kPairThreads, smem);
+  const int64_t nt = (p.n + kT - 1) / kT;
+  const int64_t n_off = nt * (nt - 1) / 2;
+  const int64_t n_items = n_off + nt;
+  int64_t grid = (int64_t)device_sm_count() * nb;
+  if (grid > n_items) grid = n_items;
+  if (grid < 1) grid = 1;
+  kernel<<<(unsigned)grid, kPairThreads, smem, s>>>(map, p, nt, n_off, n_items);
+  return cudaGetLastError();
+}
+
+cudaError_t read_faults_transpose(unsigned int* faults, bool clear) { return read_tu_faults(faults, clear); }
+
 static size_t block_smem_bytes() {
   return 2 * kT * kT * sizeof(float) + HLO_LOG_NC * sizeof(float4) + HLO_LOG_NE * sizeof(float2) +
          sizeof(BlockShared);
@@ -507,6 +719,17 @@ cudaError_t launch_selfadd_transpose(const SelfAddPlan& p, cudaStream_t s) {
   int ch = PC_RT;
   if (p.pro.n == 0) ch = PC_NONE;
   else if (p.pro.n == 1 && p.pro.op[0] == OP_LOG) ch = PC_LOG;
+  CUtensorMap map;
+  if (vec && make_pair_tensor_map(p, &map)) {  // rows on 16-byte boundaries: tensor copies into a stage ring
+    if (p.epi.n) {
+      if (ch == PC_LOG) return tma_launch<PC_LOG, true>(p, map, s);
+      if (ch == PC_NONE) return tma_launch<PC_NONE, true>(p, map, s);
+      return tma_launch<PC_RT, true>(p, map, s);
+    }
+    if (ch == PC_LOG) return tma_launch<PC_LOG, false>(p, map, s);
+    if (ch == PC_NONE) return tma_launch<PC_NONE, false>(p, map, s);
+    return tma_launch<PC_RT, false>(p, map, s);
+  }
   if (vec) {  // rows on 16-byte boundaries: the register-blocked kernel
     if (p.epi.n) {
       if (ch == PC_LOG) return block_launch<PC_LOG, true>(p, s);
@@ -558,7 +781,7 @@ __global__ void __launch_bounds__(256) tile_transpose_kernel(TilePlan p, int64_t
     if (a < na && b < nbb) {
       if (CHAINS) {
         float v = load_as_f32(p.in, p.dt, in_base + b * sib + a);
-        ftile[r][tx] = apply_chain_rt<false>(p.pro, v, 0, lt);
+        ftile[r][tx] = apply_chain_rt(p.pro, v, 0, lt);
       } else {
         tile[r][tx] = in[in_base + b * sib + a];
       }
@@ -571,7 +794,7 @@ __global__ void __launch_bounds__(256) tile_transpose_kernel(TilePlan p, int64_t
     const int64_t a = a0 + r, b = b0 + tx;
     if (a < na && b < nbb) {
       if (CHAINS) {
-        float v = apply_chain_rt<false>(p.epi, ftile[tx][r], 0, lt);
+        float v = apply_chain_rt(p.epi, ftile[tx][r], 0, lt);
         store_from_f32(p.out, p.dt, out_base + a * soa + b, round_to_dt(v, p.dt));
       } else {
         out[out_base + a * soa + b] = tile[tx][r];
@@ -629,7 +852,7 @@ __device__ __noinline__ void quant_tile_ragged(const QuantTilePlan& p, int64_t i
       if (p.qin.axis == 0) { sin = q.sin_[row]; zin = q.zin[row]; }
       if (p.qin.axis == 1) { sin = q.sin_[col]; zin = q.zin[col]; }
       float real = dequant(code, sin, zin);
-      if (p.ops.n) real = apply_chain_rt<false>(p.ops, real, 0, global_log_tables());
+      if (p.ops.n) real = apply_chain_rt(p.ops, real, 0, global_log_tables());
       float sout = p.qout.scale, inv = p.qout.inv_scale;
       int zout = p.qout.zp;
       if (p.qout.axis == 0) { sout = q.sout[row]; inv = q.inv[row]; zout = q.zout[row]; }
@@ -670,8 +893,8 @@ __device__ __forceinline__ void quant_two(int c0, int c1, float2 sin, int zm0, i
                                make_float2(-kMagic, -kMagic));  // exact code - zero point
   float2 real = __fmul2_rn(sin, df);
   if (OPS) {
-    real.x = apply_chain_rt<false>(p.ops, real.x, 0, global_log_tables());
-    real.y = apply_chain_rt<false>(p.ops, real.y, 0, global_log_tables());
+    real.x = apply_chain_rt(p.ops, real.x, 0, global_log_tables());
+    real.y = apply_chain_rt(p.ops, real.y, 0, global_log_tables());
   }
   const float2 y = __fmul2_rn(real, inv);
   const float2 t = __fadd2_rn(y, magic);
@@ -755,7 +978,7 @@ __device__ __forceinline__ void quant_rows(uint4 (&v)[4], int r0, int c, const Q
       int zin, zout;
       quant_params<QIN, QOUT, OPS>(row, jl, p, q, sin, zin, sout, inv, zout);
       float real = dequant(code, sin, zin);
-      if (OPS) real = apply_chain_rt<false>(p.ops, real, 0, global_log_tables());
+      if (OPS) real = apply_chain_rt(p.ops, real, 0, global_log_tables());
       const int res = quant_code_exact(real, sout, zout, smin, smax);
 #pragma unroll
       for (int mm = 0; mm < 4; ++mm)  // static indices keep o in registers
@@ -992,12 +1215,12 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherPlan p) {
       for (int b = 0; b < p.elem_bytes; ++b) dst[b] = src[b];
       return;
     }
-    float v = apply_chain_rt<false>(p.pro, load_as_f32(p.in, p.in_dt, off), boff, lt);
+    float v = apply_chain_rt(p.pro, load_as_f32(p.in, p.in_dt, off), boff, lt);
     if (p.self_add) {
-      const float s = apply_chain_rt<false>(p.pro, load_as_f32(p.in, p.in_dt, self_off), self_boff, lt);
+      const float s = apply_chain_rt(p.pro, load_as_f32(p.in, p.in_dt, self_off), self_boff, lt);
       v = round_to_dt(__fadd_rn(s, v), p.pro.round16 ? p.in_dt : F32);
     }
-    v = apply_chain_rt<false>(p.epi, v, 0, lt);
+    v = apply_chain_rt(p.epi, v, 0, lt);
     store_from_f32(p.out, p.out_dt, e, round_to_dt(v, p.out_dt));
     return;
   }
@@ -1011,7 +1234,7 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherPlan p) {
     zin = p.qin.zps[j];
   }
   float real = dequant(code, sin, zin);
-  real = apply_chain_rt<false>(p.pro, real, boff, lt);
+  real = apply_chain_rt(p.pro, real, boff, lt);
   if (p.out_float) {
     reinterpret_cast<float*>(p.out)[e] = real;
     return;

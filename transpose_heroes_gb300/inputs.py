@@ -242,6 +242,21 @@ def quant_add_s8(seed: int = 1, n0: int = 4096, n1: int = 4096) -> Fusion:
     return f
 
 
+def transpose3_exp_abs(seed: int = 1, dims=(512, 640, 680)) -> Fusion:
+    """The transpose fusion of "XLA:GPU Emitters", section "Transpose emitter" (exp -> transpose with
+    permutation {2,1,0} -> abs, printed on f32[20,160,170]), scaled up so that it streams HBM: x
+    f32[d0,d1,d2]{2,1,0} ~ U(-3,3) (the pages give no distribution), out f32[d2,d1,d0]{2,1,0}."""
+    dims = list(dims)
+    n = int(np.prod(dims))
+    out_dims = [dims[2], dims[1], dims[0]]
+    return Fusion(
+        name="transpose3_exp_abs_f32_" + "x".join(str(d) for d in dims), kind="transpose", dims=dims,
+        m2m=[2, 1, 0], dtype="f32", data=uniform_f32(rng(seed), n, -3.0, 3.0), permutation=[2, 1, 0],
+        self_add=False, prologue={"ops": ["exp"], "round_each": True}, epilogue={"ops": ["abs"], "round_each": True},
+        out_dims=out_dims, out_m2m=[2, 1, 0], out_dtype="f32",
+        description=f"abs(transpose(exp(x), {{2,1,0}})), x f32[{dims[0]},{dims[1]},{dims[2]}]{{2,1,0}} ~ U(-3,3)")
+
+
 # The five full-size workloads, in a fixed order.
 FULL = {
     "row_reduce_exp": row_reduce_exp,
