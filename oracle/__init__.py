@@ -87,6 +87,11 @@ def lib():
                                                 ctypes.c_void_p, P(Arr), ctypes.c_void_p]
             h.orc_quant_fusion.argtypes = [P(Arr), ctypes.c_void_p, P(Quant), P(Chain), P(Arr),
                                            ctypes.c_void_p, P(Quant)]
+            h.orc_quant_broadcast_in_dim.argtypes = [P(Arr), ctypes.c_void_p, P(Quant), P(ctypes.c_int64), P(Arr),
+                                                     ctypes.c_void_p, P(ctypes.c_float), P(ctypes.c_int32),
+                                                     P(ctypes.c_int32), P(ctypes.c_int64)]
+            h.orc_quant_reshape.argtypes = [P(Arr), ctypes.c_void_p, P(Quant), P(Arr), ctypes.c_int32,
+                                            ctypes.c_void_p]
             for name in ("orc_round_to", "orc_exp", "orc_log"):
                 getattr(h, name).argtypes = [ctypes.c_double, ctypes.c_int]
                 getattr(h, name).restype = ctypes.c_double
@@ -268,6 +273,41 @@ def quant_fusion(data, dims, in_dtype, in_q, out_m2m, out_dtype, out_q=None, m2m
                                 out.ctypes.data_as(ctypes.c_void_p), qo.ptr)
     _check(rc, "quant_fusion")
     return out
+
+
+def quant_broadcast_in_dim(data, dims, q, broadcast_dimensions, out_dims, m2m=None, out_m2m=None, dtype="s8"):
+    """broadcast_in_dim of a quantized tensor: returns (codes in the result layout, result parameters
+    {"scales", "zero_points", "quantization_dimension"})."""
+    a, o = make_arr(dims, m2m, dtype), make_arr(out_dims, out_m2m, dtype)
+    src, sp = _buf(data, dtype)
+    out = np.zeros(max(1, int(np.prod(out_dims))), dtype=NP_DTYPES[dtype])
+    cap = max([1] + [int(d) for d in out_dims])
+    rs = np.zeros(cap, np.float32)
+    rz = np.zeros(cap, np.int32)
+    rqd, rn = ctypes.c_int32(), ctypes.c_int64()
+    qk = _QuantKeep(q)
+    rc = lib().orc_quant_broadcast_in_dim(ctypes.byref(a), sp, qk.ptr, _i64(broadcast_dimensions), ctypes.byref(o),
+                                          out.ctypes.data_as(ctypes.c_void_p),
+                                          rs.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                          rz.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), ctypes.byref(rqd),
+                                          ctypes.byref(rn))
+    _check(rc, "quant_broadcast_in_dim")
+    params = {"scales": rs[:rn.value].copy(), "zero_points": rz[:rn.value].copy(),
+              "quantization_dimension": None if rqd.value < 0 else rqd.value}
+    return out[:int(np.prod(out_dims))], params
+
+
+def reshape(data, dims, out_dims, dtype, m2m=None, out_m2m=None, q=None, result_qdim=-1):
+    """reshape (lexicographic order kept); q: the operand's quantization (None for plain arrays) and
+    result_qdim the result type's quantization dimension (-1 per-tensor)."""
+    a, o = make_arr(dims, m2m, dtype), make_arr(out_dims, out_m2m, dtype)
+    src, sp = _buf(data, dtype)
+    out = np.zeros(max(1, int(np.prod(out_dims))), dtype=NP_DTYPES[dtype])
+    qk = _QuantKeep(q)
+    rc = lib().orc_quant_reshape(ctypes.byref(a), sp, qk.ptr, ctypes.byref(o), int(result_qdim),
+                                 out.ctypes.data_as(ctypes.c_void_p))
+    _check(rc, "reshape")
+    return out[:int(np.prod(out_dims))]
 
 
 QUANT_BINARY_OPS = {"add": 0, "divide": 1, "maximum": 2, "minimum": 3, "multiply": 4}

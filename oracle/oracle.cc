@@ -704,6 +704,89 @@ extern "C" int orc_quant_fusion(const orc_arr* in, const void* in_data, const or
 }
 
 // ----------------------------------------------------------------------------------------------
+// Data movement of quantized tensors: broadcast_in_dim and reshape ("StableHLO Specification",
+// sections "broadcast_in_dim" and "reshape"). Both copy stored values (result[result_index] =
+// operand[operand_index]); the quantization parameters of the result follow from the constraints:
+//   broadcast_in_dim (C1, C6): a per-tensor operand gives a per-tensor result with the same
+//     (scale, zero_point); a per-axis operand along qd gives a per-axis result along
+//     broadcast_dimensions[qd], whose parameters are the operand's, or, when dim(operand, qd) = 1,
+//     the operand's single pair repeated dim(result, broadcast_dimensions[qd]) times;
+//   reshape (C1, C3): the parameters are unchanged; for a per-axis operand the result's quantization
+//     dimension must keep the quantized axis intact -- the same size, the same product of the
+//     dimensions before it and the same product of the dimensions after it.
+// ----------------------------------------------------------------------------------------------
+extern "C" int orc_quant_broadcast_in_dim(const orc_arr* operand, const void* operand_data, const orc_quant* q,
+                                          const int64_t* broadcast_dimensions, const orc_arr* result,
+                                          void* result_data, float* result_scales, int32_t* result_zero_points,
+                                          int32_t* result_quantization_dimension, int64_t* result_n) {
+  if (!valid_quant(q, operand)) return ORC_EINVAL;
+  int rc = orc_broadcast_in_dim(operand, operand_data, broadcast_dimensions, result, result_data);
+  if (rc != ORC_OK) return rc;
+  if (!q->per_axis) {
+    *result_quantization_dimension = -1;
+    *result_n = 1;
+    result_scales[0] = q->scales[0];
+    result_zero_points[0] = q->zero_points[0];
+    return ORC_OK;
+  }
+  const int qd = q->quantization_dimension;
+  const int rqd = (int)broadcast_dimensions[qd];  // C6
+  const int64_t n = result->dims[rqd];
+  const bool single = operand->dims[qd] == 1;
+  for (int64_t i = 0; i < n; ++i) {
+    result_scales[i] = q->scales[single ? 0 : i];
+    result_zero_points[i] = q->zero_points[single ? 0 : i];
+  }
+  *result_quantization_dimension = rqd;
+  *result_n = n;
+  return ORC_OK;
+}
+
+static int64_t prod_dims(const orc_arr* a, int from, int to) {  // dims[from .. to-1]
+  int64_t p = 1;
+  for (int d = from; d < to; ++d) p *= a->dims[d];
+  return p;
+}
+
+// reshape: the element at lexicographic position p of the operand goes to lexicographic position p
+// of the result (both arrays in their own layouts). result_qdim is the result type's quantization
+// dimension (-1 for a per-tensor or unquantized tensor); q may be NULL for an unquantized reshape.
+extern "C" int orc_quant_reshape(const orc_arr* operand, const void* operand_data, const orc_quant* q,
+                                 const orc_arr* result, int32_t result_qdim, void* result_data) {
+  if (!valid_arr(operand) || !valid_arr(result) || operand->dtype != result->dtype) return ORC_EINVAL;
+  if (num_elements(operand) != num_elements(result)) return ORC_EINVAL;  // C2
+  if (q) {
+    if (!valid_quant(q, operand)) return ORC_EINVAL;
+    if (q->per_axis) {  // C3
+      const int qd = q->quantization_dimension;
+      if (result_qdim < 0 || result_qdim >= result->rank) return ORC_EINVAL;
+      if (prod_dims(operand, 0, qd) != prod_dims(result, 0, result_qdim)) return ORC_EINVAL;
+      if (operand->dims[qd] != result->dims[result_qdim]) return ORC_EINVAL;
+      if (prod_dims(operand, qd + 1, operand->rank) != prod_dims(result, result_qdim + 1, result->rank))
+        return ORC_EINVAL;
+    } else if (result_qdim != -1) {
+      return ORC_EINVAL;  // C1: a per-tensor operand stays per-tensor
+    }
+  }
+  int64_t ostride[ORC_MAX_RANK], rstride[ORC_MAX_RANK];
+  strides_of(operand, ostride);
+  strides_of(result, rstride);
+  const int eb = elem_bytes(operand->dtype);
+  const int64_t n = num_elements(operand);
+#pragma omp parallel for schedule(static)
+  for (int64_t p = 0; p < n; ++p) {
+    int64_t oi[ORC_MAX_RANK], ri[ORC_MAX_RANK];
+    lex_index(operand->rank, operand->dims, p, oi);
+    lex_index(result->rank, result->dims, p, ri);
+    int64_t oo = 0, ro = 0;
+    for (int d = 0; d < operand->rank; ++d) oo += oi[d] * ostride[d];
+    for (int d = 0; d < result->rank; ++d) ro += ri[d] * rstride[d];
+    std::memcpy((char*)result_data + ro * eb, (const char*)operand_data + oo * eb, eb);
+  }
+  return ORC_OK;
+}
+
+// ----------------------------------------------------------------------------------------------
 // Quantized elementwise binary ops ("StableHLO Specification", sections add, divide, maximum,
 // minimum, multiply: dequantize_op_quantize(op, lhs, rhs, type(result))): both operands dequantized,
 // the op in IEEE f32 (maximum / minimum: NaN propagates, -0 < +0), the result quantized with the

@@ -941,3 +941,128 @@ def test_quant_fusion_float_ops_chain_exact(orc, out_kind):
             else:
                 code = min(127, max(-128, _rne_int(f32(v / s_out)) + 3))
                 assert int(got) == code, (i, j)
+
+
+# ---------------------------------------------------------------------------------------------
+# quantized broadcast_in_dim and reshape (StableHLO Specification, "broadcast_in_dim" C1, C6;
+# "reshape" C1-C3): stored codes move like plain elements, the parameters follow the constraints
+# ---------------------------------------------------------------------------------------------
+def _dequant_logical(codes, dims, params):
+    """Test-side dequantize of a logical (row-major) code array with numpy f32 arithmetic."""
+    c = np.asarray(codes, np.int32).reshape(dims)
+    s = np.asarray(params["scales"], np.float32)
+    z = np.asarray(params["zero_points"], np.int32)
+    qd = params.get("quantization_dimension")
+    if qd is None:
+        return (s[0] * (c - z[0]).astype(np.float32)).astype(np.float32)
+    shape = [1] * len(dims)
+    shape[qd] = dims[qd]
+    return (s.reshape(shape) * (c - z.reshape(shape)).astype(np.float32)).astype(np.float32)
+
+
+def test_quant_broadcast_in_dim_example_per_axis(orc):
+    """The spec's example [[1, 2, 3]] -> tensor<2x3x2> with broadcast_dimensions [2, 1], quantized per
+    axis along operand dimension 1 with the quantization page's {0.2:20, 0.1:10, 0.3:30}: the codes are
+    the printed result and the result is per-axis along broadcast_dimensions[1] = 1 (C6) with the same
+    parameters."""
+    g = load_golden("broadcast_example.txt")
+    qa = load_golden("quant_examples.txt")["per_axis"]
+    q = {"scales": np.float32(qa["scales"]), "zero_points": np.int32(qa["zero_points"]), "quantization_dimension": 1}
+    codes, params = orc.quant_broadcast_in_dim(np.int8(g["operand"]).ravel(), g["operand_dims"], q,
+                                               g["broadcast_dimensions"], g["result_dims"])
+    assert codes.reshape(g["result_dims"]).tolist() == g["result"]
+    assert params["quantization_dimension"] == 1
+    assert params["scales"].tolist() == np.float32(qa["scales"]).tolist()
+    assert params["zero_points"].tolist() == qa["zero_points"]
+    # the real values are broadcast: result[i, j, k] = real(operand[0, j])
+    real_in = _dequant_logical(np.int8(g["operand"]).ravel(), g["operand_dims"], q)
+    real_out = _dequant_logical(codes, g["result_dims"], params)
+    for i in range(2):
+        for j in range(3):
+            for k in range(2):
+                assert real_out[i, j, k] == real_in[0, j]
+
+
+def test_quant_broadcast_in_dim_unit_quantized_dimension(orc):
+    """C6: when dim(operand, qd) = 1, the single (scale, zero_point) is repeated along the result's
+    quantization dimension; a per-tensor operand stays per-tensor (C1)."""
+    q = {"scales": np.float32([0.5]), "zero_points": np.int32([2]), "quantization_dimension": 0}
+    codes, params = orc.quant_broadcast_in_dim(np.int8([7, -3, 1]), [1, 3], q, [2, 1], [4, 3, 5])
+    assert params["quantization_dimension"] == 2
+    assert params["scales"].tolist() == [0.5] * 5 and params["zero_points"].tolist() == [2] * 5
+    assert np.array_equal(codes.reshape(4, 3, 5), np.broadcast_to(np.int8([7, -3, 1])[None, :, None], (4, 3, 5)))
+    pt = {"scales": np.float32([0.25]), "zero_points": np.int32([-1])}
+    _, params = orc.quant_broadcast_in_dim(np.int8([7, -3, 1]), [1, 3], pt, [2, 1], [4, 3, 5])
+    assert params["quantization_dimension"] is None and params["scales"].tolist() == [0.25]
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_quant_broadcast_in_dim_commutes_with_dequantize(orc, seed):
+    """dequantize(broadcast_in_dim(q)) = broadcast_in_dim(dequantize(q)) exactly, on random shapes,
+    broadcast dimensions, layouts and per-axis dimensions (brute force against numpy)."""
+    g = np.random.default_rng(seed)
+    rank_in = int(g.integers(1, 4))
+    rank_out = rank_in + int(g.integers(0, 3))
+    bdims = sorted(g.choice(rank_out, size=rank_in, replace=False).tolist())
+    if seed == 3:
+        bdims = bdims[::-1]  # broadcast_dimensions need not be increasing
+    out_dims = [int(v) for v in g.integers(1, 5, size=rank_out)]
+    dims = [1 if g.random() < 0.3 else out_dims[b] for b in bdims]
+    qd = int(g.integers(0, rank_in))
+    q = {"scales": g.uniform(0.01, 0.5, dims[qd]).astype(np.float32),
+         "zero_points": g.integers(-20, 21, dims[qd]).astype(np.int32), "quantization_dimension": qd}
+    codes = g.integers(-128, 128, size=dims).astype(np.int8)
+    in_m2m = g.permutation(rank_in).tolist()
+    out_m2m = g.permutation(rank_out).tolist()
+    out, params = orc.quant_broadcast_in_dim(to_physical(codes, in_m2m), dims, q, bdims, out_dims, m2m=in_m2m,
+                                             out_m2m=out_m2m)
+    out_logical = from_physical(out, out_dims, out_m2m)
+    assert params["quantization_dimension"] == bdims[qd]
+    real_in = _dequant_logical(codes.ravel(), dims, q)
+    real_out = _dequant_logical(out_logical.ravel(), out_dims, params)
+    # numpy broadcast of the dequantized operand: move operand dim d to result dim bdims[d]
+    expand = np.zeros([1] * rank_out, np.float32) + 0
+    shape = [1] * rank_out
+    order = np.argsort(bdims)
+    moved = np.transpose(real_in, order).reshape([dims[d] for d in order])
+    for d in range(rank_in):
+        shape[bdims[d]] = dims[d]
+    want = np.broadcast_to(moved.reshape(shape) + expand, out_dims)
+    assert np.array_equal(real_out, want)
+
+
+def test_reshape_example(orc):
+    g = load_golden("reshape_example.txt")
+    out = orc.reshape(np.int32(g["operand"]).ravel(), g["operand_dims"], g["result_dims"], "s32")
+    assert out.reshape(g["result_dims"]).tolist() == g["result"]
+
+
+def test_quant_reshape_per_axis_rules(orc):
+    """C3 on the quantization page's t[4, 3, 2] (per-axis along 1): [2, 2, 3, 2] keeps the axis (before 4,
+    size 3, after 2) as dimension 2; [12, 2] and [4, 6] do not; a per-tensor operand has no axis."""
+    qa = load_golden("quant_examples.txt")["per_axis"]
+    q = {"scales": np.float32(qa["scales"]), "zero_points": np.int32(qa["zero_points"]), "quantization_dimension": 1}
+    g = np.random.default_rng(7)
+    codes = g.integers(-128, 128, size=qa["dims"]).astype(np.int8)
+    out = orc.reshape(codes.ravel(), qa["dims"], [2, 2, 3, 2], "s8", q=q, result_qdim=2)
+    assert np.array_equal(out, codes.ravel())  # default layouts: the same bytes
+    rq = dict(q, quantization_dimension=2)
+    assert np.array_equal(_dequant_logical(out, [2, 2, 3, 2], rq).ravel(), _dequant_logical(codes.ravel(), qa["dims"], q).ravel())
+    for bad_dims, bad_qd in [([12, 2], 0), ([4, 6], 1), ([2, 2, 3, 2], 1), ([4, 3, 2], 2)]:
+        with pytest.raises(ValueError):
+            orc.reshape(codes.ravel(), qa["dims"], bad_dims, "s8", q=q, result_qdim=bad_qd)
+    with pytest.raises(ValueError):  # C2: the element count is kept
+        orc.reshape(codes.ravel(), qa["dims"], [5, 5], "s8")
+    pt = {"scales": np.float32([0.1]), "zero_points": np.int32([0])}
+    assert np.array_equal(orc.reshape(codes.ravel(), qa["dims"], [24], "s8", q=pt, result_qdim=-1), codes.ravel())
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_reshape_with_layouts_vs_numpy(orc, seed):
+    g = np.random.default_rng(seed)
+    dims, out_dims = [3, 4, 5], [6, 10]
+    x = g.integers(-1000, 1000, size=dims).astype(np.int32)
+    for in_m2m in all_layouts(3):
+        for out_m2m in ([1, 0], [0, 1]):
+            out = orc.reshape(to_physical(x, in_m2m), dims, out_dims, "s32", m2m=in_m2m, out_m2m=out_m2m)
+            assert np.array_equal(from_physical(out, out_dims, out_m2m), x.reshape(out_dims))
