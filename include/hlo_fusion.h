@@ -265,6 +265,42 @@ hlo_status hlo_quant_binary(int32_t op, const hlo_array* lhs, const void* lhs_pt
                             void* out_ptr, const hlo_quant* out_q, void* stream);
 
 /* ------------------------------------------------------------------------------------------------
+ * Data movement of quantized tensors. Stored codes move like plain elements (result[result_index] =
+ * operand[operand_index]); the result's quantization parameters follow the ops' quantized constraints.
+ * Note: add, divide, maximum, minimum and multiply take per-tensor quantized operands only (inputs I1,
+ * I2 of each op), which is why hlo_quant_binary rejects per-axis ones; per-axis tensors are moved by the
+ * two entry points below.
+ *
+ * hlo_quant_broadcast_in_dim ("StableHLO Specification", section "broadcast_in_dim", constraints C1-C6):
+ *   operand, operand_ptr, operand_q   HLO_S8 operand and its parameters (per-tensor or per-axis)
+ *   broadcast_dimensions              operand->rank entries: result dimension of each operand dimension
+ *                                     (C3 in range, C4 unique, C5 size 1 or equal)
+ *   result, result_ptr                HLO_S8 result (any layout)
+ *   result_quantization_dimension     (host, out) -1 for a per-tensor operand; otherwise
+ *                                     broadcast_dimensions[quantization_dimension(operand)] (C6)
+ *   result_scales, result_zero_points (device, out) the result's pairs: 1 for per-tensor; otherwise
+ *                                     dim(result, *result_quantization_dimension) pairs, the operand's,
+ *                                     or its single pair repeated when dim(operand, qd) = 1 (C6)
+ *
+ * hlo_quant_reshape ("StableHLO Specification", section "reshape", constraints C1-C3): the element at
+ * lexicographic position p of the operand becomes the element at position p of the result, in each
+ * array's own layout (bit-exact, any element type).
+ *   operand_q                       NULL for an unquantized array; else the operand's parameters (HLO_S8)
+ *   result_quantization_dimension   the result type's quantization dimension: -1 for unquantized and
+ *                                   per-tensor operands; for a per-axis operand a result dimension with
+ *                                   the same size and the same products of the dimensions before and
+ *                                   after it (C3), HLO_ERR_INVALID_ARG otherwise. The (scale,
+ *                                   zero_point) pairs are the operand's, unchanged (C1).
+ * ---------------------------------------------------------------------------------------------- */
+hlo_status hlo_quant_broadcast_in_dim(const hlo_array* operand, const void* operand_ptr, const hlo_quant* operand_q,
+                                      const int64_t* broadcast_dimensions, const hlo_array* result, void* result_ptr,
+                                      float* result_scales, int32_t* result_zero_points,
+                                      int32_t* result_quantization_dimension, void* stream);
+hlo_status hlo_quant_reshape(const hlo_array* operand, const void* operand_ptr, const hlo_quant* operand_q,
+                             const hlo_array* result, int32_t result_quantization_dimension, void* result_ptr,
+                             void* stream);
+
+/* ------------------------------------------------------------------------------------------------
  * Variadic reduce with the max/argmax body ("XLA Operation Semantics", section "Variadic Reduce"):
  * inputs V and K, init values I_V, I_K, and the body
  *     f(max, argmax, value, index) = (value, index) if value >= max else (max, argmax)

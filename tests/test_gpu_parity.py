@@ -829,3 +829,106 @@ def test_bounded_wait_reports_a_fault():
     ref, asum = run_oracle(f)
     check(f, run_gpu(f), ref, asum)
     assert hf.device_faults() == 0
+
+
+# ---- quantized data movement: broadcast_in_dim and reshape -------------------------------------------------
+def _to_physical(arr, m2m):
+    return np.ascontiguousarray(np.transpose(arr, list(reversed(m2m)))).ravel()
+
+
+def _qdev(q):
+    """Device copies of per-axis parameters (host copies kept for the library's value checks)."""
+    out = {"host_scales": np.float32(q["scales"]), "host_zero_points": np.int32(q["zero_points"]),
+           "quantization_dimension": q.get("quantization_dimension")}
+    if q.get("quantization_dimension") is not None:
+        out["scales"] = torch.from_numpy(np.float32(q["scales"])).cuda()
+        out["zero_points"] = torch.from_numpy(np.int32(q["zero_points"])).cuda()
+    return out
+
+
+def _gpu_quant_broadcast(codes_phys, dims, q, bdims, out_dims, in_m2m, out_m2m):
+    x = torch.from_numpy(np.ascontiguousarray(codes_phys, np.int8)).cuda()
+    out = torch.empty(max(1, int(np.prod(out_dims))), dtype=torch.int8, device="cuda")
+    cap = max([1] + list(out_dims))
+    rs = torch.empty(cap, dtype=torch.float32, device="cuda")
+    rz = torch.empty(cap, dtype=torch.int32, device="cuda")
+    rqd = hf.quant_broadcast_in_dim(x, dims, _qdev(q), bdims, out, out_dims, rs, rz, in_m2m=in_m2m, out_m2m=out_m2m)
+    torch.cuda.synchronize()
+    n = 1 if rqd < 0 else out_dims[rqd]
+    return out.cpu().numpy()[: int(np.prod(out_dims))], rqd, rs.cpu().numpy()[:n], rz.cpu().numpy()[:n]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_quant_broadcast_in_dim_vs_oracle(seed):
+    """Random ranks, broadcast dimensions (some of size 1), layouts and quantization axes, per-axis and
+    per-tensor: codes bit-exact, parameters equal to the oracle's (constraints C1, C6)."""
+    g = np.random.default_rng(100 + seed)
+    rank_in = int(g.integers(1, 4))
+    rank_out = rank_in + int(g.integers(0, 3))
+    bdims = g.choice(rank_out, size=rank_in, replace=False).tolist()
+    out_dims = [int(v) for v in g.integers(1, 40, size=rank_out)]
+    dims = [1 if g.random() < 0.3 else out_dims[b] for b in bdims]
+    qd = int(g.integers(0, rank_in))
+    if seed % 3 == 2:
+        q = {"scales": np.float32([0.07]), "zero_points": np.int32([-5]), "quantization_dimension": None}
+    else:
+        q = {"scales": g.uniform(0.01, 0.5, dims[qd]).astype(np.float32),
+             "zero_points": g.integers(-20, 21, dims[qd]).astype(np.int32), "quantization_dimension": qd}
+    codes = g.integers(-128, 128, size=dims).astype(np.int8)
+    in_m2m, out_m2m = g.permutation(rank_in).tolist(), g.permutation(rank_out).tolist()
+    phys = _to_physical(codes, in_m2m)
+    ref, params = oracle.quant_broadcast_in_dim(phys, dims, q, bdims, out_dims, m2m=in_m2m, out_m2m=out_m2m)
+    got, rqd, rs, rz = _gpu_quant_broadcast(phys, dims, q, bdims, out_dims, in_m2m, out_m2m)
+    assert np.array_equal(got, ref)
+    assert rqd == (-1 if params["quantization_dimension"] is None else params["quantization_dimension"])
+    assert np.array_equal(rs.view(np.uint32), params["scales"].view(np.uint32))
+    assert np.array_equal(rz, params["zero_points"])
+
+
+def test_quant_broadcast_in_dim_large_per_axis():
+    """A per-axis vector s8[4096] (axis 0) broadcast to s8[4096, 4096] along dimension 1, column-major."""
+    g = np.random.default_rng(5)
+    n = 4096
+    q = {"scales": g.uniform(0.001, 0.1, n).astype(np.float32), "zero_points": g.integers(-20, 21, n).astype(np.int32),
+         "quantization_dimension": 0}
+    codes = g.integers(-128, 128, size=n).astype(np.int8)
+    ref, params = oracle.quant_broadcast_in_dim(codes, [n], q, [1], [n, n], out_m2m=[0, 1])
+    got, rqd, rs, rz = _gpu_quant_broadcast(codes, [n], q, [1], [n, n], [0], [0, 1])
+    assert np.array_equal(got, ref) and rqd == 1
+    assert np.array_equal(rs, params["scales"]) and np.array_equal(rz, params["zero_points"])
+
+
+@pytest.mark.parametrize("dtype", ["s8", "bf16", "f32"])
+def test_reshape_layouts_vs_oracle(dtype):
+    g = np.random.default_rng(11)
+    cases = [([3, 4, 5], [6, 10]), ([8, 9, 10], [2, 4, 90]), ([1000, 33], [33, 1000]), ([7], [7, 1, 1])]
+    npt = {"s8": np.int8, "bf16": np.uint16, "f32": np.float32}[dtype]
+    for dims, out_dims in cases:
+        x = g.integers(-100, 100, size=dims).astype(npt)
+        for in_m2m in [list(range(len(dims) - 1, -1, -1)), list(range(len(dims)))]:
+            for out_m2m in [list(range(len(out_dims) - 1, -1, -1)), list(range(len(out_dims)))]:
+                phys = _to_physical(x, in_m2m)
+                ref = oracle.reshape(phys, dims, out_dims, dtype, m2m=in_m2m, out_m2m=out_m2m)
+                xt = torch.from_numpy(np.ascontiguousarray(phys).view({"s8": np.int8, "bf16": np.int16,
+                                                                       "f32": np.float32}[dtype])).cuda()
+                out = torch.empty_like(xt)
+                hf.reshape(xt, dims, out, out_dims, dtype, in_m2m=in_m2m, out_m2m=out_m2m)
+                torch.cuda.synchronize()
+                got = out.cpu().numpy().view(npt)
+                assert np.array_equal(got, ref), (dims, out_dims, in_m2m, out_m2m)
+
+
+def test_quant_reshape_per_axis_keeps_parameters():
+    """t[4, 3, 2] per-axis along 1 (the quantization page's example) reshaped to [2, 2, 3, 2] along 2: the
+    codes move as the oracle moves them, in a non-default layout too."""
+    g = np.random.default_rng(12)
+    q = {"scales": np.float32([0.2, 0.1, 0.3]), "zero_points": np.int32([20, 10, 30]), "quantization_dimension": 1}
+    codes = g.integers(-128, 128, size=[4, 3, 2]).astype(np.int8)
+    for in_m2m, out_m2m in [([2, 1, 0], [3, 2, 1, 0]), ([0, 2, 1], [1, 3, 0, 2])]:
+        phys = _to_physical(codes, in_m2m)
+        ref = oracle.reshape(phys, [4, 3, 2], [2, 2, 3, 2], "s8", m2m=in_m2m, out_m2m=out_m2m, q=q, result_qdim=2)
+        xt = torch.from_numpy(phys).cuda()
+        out = torch.empty_like(xt)
+        hf.reshape(xt, [4, 3, 2], out, [2, 2, 3, 2], "s8", q=_qdev(q), result_qdim=2, in_m2m=in_m2m, out_m2m=out_m2m)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), ref)

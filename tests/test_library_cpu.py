@@ -293,3 +293,27 @@ def test_tanhf_first_pass_errors_below_their_rounding_bounds():
     tl = (((f32(1) - th).astype(f32) - q0).astype(f32) - q1).astype(f32)
     err = np.abs(th.astype(np.longdouble) + tl.astype(np.longdouble) - np.tanh(a.astype(np.longdouble)))
     assert float(err.max()) < 2.0 ** -37.5
+
+
+def test_quantized_data_movement_validation(lib):
+    """broadcast_in_dim C3-C5 and reshape C1-C3 are checked before anything is enqueued."""
+    # per-axis operands need device parameter pointers: fake ones, never dereferenced
+    q = {"scales": 0x300000, "zero_points": 0x310000, "host_scales": np.float32([0.2, 0.1, 0.3]),
+         "host_zero_points": np.int32([20, 10, 30]), "quantization_dimension": 1}
+    sc, zp = FAKE_OUT + (1 << 20), FAKE_OUT + (2 << 20)
+    # C3: broadcast dimension out of range; C4: repeated; C5: size mismatch
+    for bdims, out_dims, tag in [([0, 3], [2, 3, 2], "C3"), ([2, 2], [2, 3, 2], "C4"), ([0, 2], [2, 3, 4], "C5")]:
+        st, msg = _status(lambda: hf.quant_broadcast_in_dim(FAKE_IN, [2, 3], q, bdims, FAKE_OUT, out_dims, sc, zp,
+                                                            stream=0))
+        assert st == 1 and tag in msg, msg
+    # reshape C2 (element count), C3 (quantized axis kept), C1 (per-tensor stays per-tensor)
+    st, msg = _status(lambda: hf.reshape(FAKE_IN, [4, 3, 2], FAKE_OUT, [5, 5], "s8", q=None, stream=0))
+    assert st == 1 and "C2" in msg
+    q3 = q
+    for out_dims, rqd in [([12, 2], 0), ([4, 6], 1), ([2, 2, 3, 2], 1)]:
+        st, msg = _status(lambda: hf.reshape(FAKE_IN, [4, 3, 2], FAKE_OUT, out_dims, "s8", q=q3, result_qdim=rqd,
+                                             stream=0))
+        assert st == 1 and "C3" in msg, msg
+    pt = {"host_scales": np.float32([0.1]), "host_zero_points": np.int32([0]), "quantization_dimension": None}
+    st, msg = _status(lambda: hf.reshape(FAKE_IN, [4, 3, 2], FAKE_OUT, [24], "s8", q=pt, result_qdim=0, stream=0))
+    assert st == 1 and "C1" in msg

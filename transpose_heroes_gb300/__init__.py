@@ -33,7 +33,8 @@ STATUS = {0: "HLO_OK", 1: "HLO_ERR_INVALID_ARG", 2: "HLO_ERR_UNSUPPORTED", 3: "H
 
 # Every function the header declares; the library must export all of them.
 EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_workspace_size", "hlo_transpose_fusion", "hlo_layout_convert",
-           "hlo_quant_fusion", "hlo_quant_binary", "hlo_reduce_max_argmax", "hlo_device_faults",
+           "hlo_quant_fusion", "hlo_quant_binary", "hlo_quant_broadcast_in_dim", "hlo_quant_reshape",
+           "hlo_reduce_max_argmax", "hlo_device_faults",
            "hlo_selftest_bounded_wait", "hlo_last_error", "hlo_version")
 QUANT_BINARY_OPS = {"add": 0, "divide": 1, "maximum": 2, "minimum": 3, "multiply": 4}
 
@@ -98,6 +99,11 @@ def lib() -> ctypes.CDLL:
             h.hlo_reduce_max_argmax.argtypes = [P(Array), vp, P(Array), vp, P(i64), i32, ctypes.c_double, i64,
                                                 P(Array), vp, P(Array), vp, vp]
             h.hlo_reduce_max_argmax.restype = ctypes.c_int
+            h.hlo_quant_broadcast_in_dim.argtypes = [P(Array), vp, P(Quant), P(i64), P(Array), vp, vp, vp,
+                                                     P(ctypes.c_int32), vp]
+            h.hlo_quant_broadcast_in_dim.restype = ctypes.c_int
+            h.hlo_quant_reshape.argtypes = [P(Array), vp, P(Quant), P(Array), i32, vp, vp]
+            h.hlo_quant_reshape.restype = ctypes.c_int
             h.hlo_device_faults.argtypes = [P(ctypes.c_uint32), i32]
             h.hlo_device_faults.restype = ctypes.c_int
             h.hlo_selftest_bounded_wait.argtypes = [vp]
@@ -252,6 +258,28 @@ def reduce_max_argmax(inp, in_dims, in_dtype, dimensions, out, out_idx, init_val
                                        len(list(dimensions)), float(init_value), int(init_index), ctypes.byref(o),
                                        _ptr(out), ctypes.byref(oi), _ptr(out_idx), _stream(stream)))
     return out, out_idx
+
+
+def quant_broadcast_in_dim(inp, dims, q, broadcast_dimensions, out, out_dims, out_scales, out_zero_points,
+                           in_m2m=None, out_m2m=None, stream=None) -> int:
+    """hlo_quant_broadcast_in_dim on s8 codes; writes the result's parameters into out_scales /
+    out_zero_points (device tensors) and returns the result's quantization dimension (-1 per-tensor)."""
+    a, o = make_array(dims, in_m2m, "s8"), make_array(out_dims, out_m2m, "s8")
+    qk = _QuantKeep(q)
+    rqd = ctypes.c_int32(0)
+    _check(lib().hlo_quant_broadcast_in_dim(ctypes.byref(a), _ptr(inp), qk.ref(), _i64(broadcast_dimensions),
+                                            ctypes.byref(o), _ptr(out), _ptr(out_scales), _ptr(out_zero_points),
+                                            ctypes.byref(rqd), _stream(stream)))
+    return int(rqd.value)
+
+
+def reshape(inp, dims, out, out_dims, dtype, q=None, result_qdim=-1, in_m2m=None, out_m2m=None, stream=None):
+    """hlo_quant_reshape: the lexicographic order is kept; q / result_qdim for quantized (s8) operands."""
+    a, o = make_array(dims, in_m2m, dtype), make_array(out_dims, out_m2m, dtype)
+    qk = _QuantKeep(q)
+    _check(lib().hlo_quant_reshape(ctypes.byref(a), _ptr(inp), qk.ref(), ctypes.byref(o), int(result_qdim), _ptr(out),
+                                   _stream(stream)))
+    return out
 
 
 FAULT_COPY_TIMEOUT = 1

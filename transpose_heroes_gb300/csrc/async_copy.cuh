@@ -5,7 +5,10 @@
 #include <cstdint>
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "hlo_internal.h"
 
@@ -86,6 +89,26 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 
 __device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link against libcuda).
+static inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool looked = false;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!looked) {
+    looked = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t pending = cudaPeekAtLastError();
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    else if (pending == cudaSuccess)
+      cudaGetLastError();  // the lookup's own error: the caller falls back to plain loads
+  }
+  return fn;
 }
 
 }  // namespace hlo

@@ -130,18 +130,33 @@ __device__ __forceinline__ float chain_exp(float v, bool r16, int dt) {
   return round16_settled(expf(v), dt, r) ? r : exp_round16_slow(v, dt);
 }
 
+__device__ __forceinline__ float chain_log(float v, bool r16, int dt, const float4* c, const float2* e) {
+  float r;
+  if (!r16) return cr_logf(v, c, e);
+  return round16_settled(cr_logf(v, c, e), dt, r) ? r : log_round16_slow(v, dt);
+}
+
+__device__ __forceinline__ float chain_tanh(float v, bool r16, int dt) {
+  float r;
+  if (!r16) return cr_tanhf(v);
+  return round16_settled(tanhf(v), dt, r) ? r : tanh_round16_slow(v, dt);
+}
+
+// The same three, out of line: the kernels that interpret chains at run time call one shared copy
+// instead of inlining all three evaluations at every use (which multiplies code size and build time).
+static __device__ __noinline__ float chain_exp_call(float v, bool r16, int dt) { return chain_exp(v, r16, dt); }
+static __device__ __noinline__ float chain_log_call(float v, bool r16, int dt, const float4* c, const float2* e) {
+  return chain_log(v, r16, dt, c, e);
+}
+static __device__ __noinline__ float chain_tanh_call(float v, bool r16, int dt) { return chain_tanh(v, r16, dt); }
+
 // One elementwise op of a chain, every result correctly rounded (exp, log, tanh) or exact.
 __device__ __forceinline__ float apply_op(int op, float v, float b, float x, float imm, bool r16, int dt,
                                           const LogTab& lt) {
-  float r;
   switch (op) {
-    case OP_EXP: return chain_exp(v, r16, dt);
-    case OP_LOG:
-      if (!r16) return cr_logf(v, lt.c, lt.e);
-      return round16_settled(cr_logf(v, lt.c, lt.e), dt, r) ? r : log_round16_slow(v, dt);
-    case OP_TANH:
-      if (!r16) return cr_tanhf(v);
-      return round16_settled(tanhf(v), dt, r) ? r : tanh_round16_slow(v, dt);
+    case OP_EXP: return chain_exp_call(v, r16, dt);
+    case OP_LOG: return chain_log_call(v, r16, dt, lt.c, lt.e);
+    case OP_TANH: return chain_tanh_call(v, r16, dt);
     case OP_ABS: return fabsf(v);
     case OP_NEG: return -v;
     case OP_ADD_BCAST: return __fadd_rn(v, b);

@@ -541,6 +541,149 @@ hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const 
   return cuda_status(launch_argmax(p, as_stream(stream)), "argmax launch");
 }
 
+// ---- quantized data movement: broadcast_in_dim and reshape -------------------------------------------
+hlo_status hlo_quant_broadcast_in_dim(const hlo_array* operand, const void* operand_ptr, const hlo_quant* operand_q,
+                                      const int64_t* broadcast_dimensions, const hlo_array* result, void* result_ptr,
+                                      float* result_scales, int32_t* result_zero_points,
+                                      int32_t* result_quantization_dimension, void* stream) {
+  hlo_status st = check_array(operand, "broadcast_in_dim operand");
+  if (st != HLO_OK) return st;
+  if ((st = check_array(result, "broadcast_in_dim result")) != HLO_OK) return st;
+  if (operand->dtype != S8 || result->dtype != S8)
+    return fail(HLO_ERR_UNSUPPORTED, "quantized broadcast_in_dim: storage type must be s8 for operand and result");
+  QuantParams qp;
+  if ((st = check_quant(operand_q, *operand, "broadcast_in_dim operand", &qp)) != HLO_OK) return st;
+  if (operand->rank > 0 && !broadcast_dimensions)
+    return fail(HLO_ERR_INVALID_ARG, "broadcast_in_dim (C2): broadcast_dimensions is NULL");
+  bool used[HLO_MAX_RANK] = {false};
+  for (int d = 0; d < operand->rank; ++d) {
+    const int64_t bd = broadcast_dimensions[d];
+    if (bd < 0 || bd >= result->rank)
+      return fail(HLO_ERR_INVALID_ARG, "broadcast_in_dim (C3): broadcast_dimensions[%d] = %lld out of range", d,
+                  (long long)bd);
+    if (used[bd]) return fail(HLO_ERR_INVALID_ARG, "broadcast_in_dim (C4): broadcast_dimensions not unique");
+    used[bd] = true;
+    if (operand->dims[d] != 1 && operand->dims[d] != result->dims[bd])
+      return fail(HLO_ERR_INVALID_ARG, "broadcast_in_dim (C5): operand dim %d has size %lld, result dim %lld has %lld", d,
+                  (long long)operand->dims[d], (long long)bd, (long long)result->dims[bd]);
+  }
+  if (!result_quantization_dimension)
+    return fail(HLO_ERR_INVALID_ARG, "quantized broadcast_in_dim: result_quantization_dimension is NULL");
+  // C1, C6: the result's quantization dimension and the number of its (scale, zero_point) pairs
+  const int rqd = qp.axis < 0 ? -1 : (int)broadcast_dimensions[qp.axis];
+  const int64_t n_params = rqd < 0 ? 1 : result->dims[rqd];
+  if (n_params > 0 && (!result_scales || !result_zero_points))
+    return fail(HLO_ERR_INVALID_ARG, "quantized broadcast_in_dim: result parameter buffers are NULL");
+  const int64_t n_in = numel(*operand), n_out = numel(*result);
+  if (n_out > 0 && (!result_ptr || (n_in > 0 && !operand_ptr)))
+    return fail(HLO_ERR_INVALID_ARG, "quantized broadcast_in_dim: NULL data pointer");
+  if (ranges_overlap(operand_ptr, n_in, result_ptr, n_out) ||
+      ranges_overlap(result_scales, n_params * 4, result_ptr, n_out) ||
+      ranges_overlap(result_zero_points, n_params * 4, result_ptr, n_out) ||
+      ranges_overlap(result_scales, n_params * 4, result_zero_points, n_params * 4))
+    return fail(HLO_ERR_INVALID_ARG, "quantized broadcast_in_dim: output buffers overlap an input or each other");
+  const cudaStream_t s = as_stream(stream);
+  *result_quantization_dimension = rqd;
+  cudaError_t e = rqd < 0 ? launch_quant_params(nullptr, nullptr, qp.scale, qp.zp, 1, result_scales,
+                                                result_zero_points, 1, s)
+                          : launch_quant_params(qp.scales, qp.zps, 0.f, 0, operand->dims[qp.axis] == 1 ? 1 : 0,
+                                                result_scales, result_zero_points, n_params, s);
+  if (e != cudaSuccess) return cuda_status(e, "quantized parameter kernel launch");
+  if (n_out == 0) return ok();
+  // the codes: result element r reads operand index i[d] = dim(operand, d) == 1 ? 0 : r[bdims[d]]
+  GatherPlan g;
+  std::memset(&g, 0, sizeof g);
+  g.in = operand_ptr;
+  g.out = result_ptr;
+  g.kind = G_PLAIN;
+  g.rank = result->rank;
+  g.n = n_out;
+  int64_t istr[HLO_MAX_RANK];
+  strides_of(*operand, istr);
+  for (int j = 0; j < result->rank; ++j) {
+    const int od = (int)result->minor_to_major[result->rank - 1 - j];
+    g.out_size[j] = result->dims[od];
+    g.out_logical[j] = od;
+  }
+  for (int d = 0; d < operand->rank; ++d)
+    if (operand->dims[d] != 1) g.in_stride_of_out[broadcast_dimensions[d]] = istr[d];
+  for (int k = 0; k < result->rank; ++k) g.perm[k] = k;
+  g.in_dt = g.out_dt = S8;
+  g.elem_bytes = 1;
+  return cuda_status(launch_gather(g, s), "broadcast gather launch");
+}
+
+hlo_status hlo_quant_reshape(const hlo_array* operand, const void* operand_ptr, const hlo_quant* operand_q,
+                             const hlo_array* result, int32_t result_quantization_dimension, void* result_ptr,
+                             void* stream) {
+  hlo_status st = check_array(operand, "reshape operand");
+  if (st != HLO_OK) return st;
+  if ((st = check_array(result, "reshape result")) != HLO_OK) return st;
+  if (operand->dtype != result->dtype)
+    return fail(HLO_ERR_INVALID_ARG, "reshape (C1): result element type differs from the operand's");
+  const int64_t n = numel(*operand);
+  if (numel(*result) != n) return fail(HLO_ERR_INVALID_ARG, "reshape (C2): %lld elements into %lld", (long long)n,
+                                       (long long)numel(*result));
+  if (operand_q) {
+    QuantParams qp;
+    if (operand->dtype != S8) return fail(HLO_ERR_UNSUPPORTED, "quantized reshape: storage type must be s8");
+    if ((st = check_quant(operand_q, *operand, "reshape operand", &qp)) != HLO_OK) return st;
+    if (qp.axis < 0) {
+      if (result_quantization_dimension != -1)
+        return fail(HLO_ERR_INVALID_ARG, "reshape (C1): a per-tensor operand gives a per-tensor result");
+    } else {
+      const int qd = qp.axis, rqd = result_quantization_dimension;
+      if (rqd < 0 || rqd >= result->rank)
+        return fail(HLO_ERR_INVALID_ARG, "reshape (C3): result quantization dimension %d out of range", rqd);
+      int64_t before_o = 1, after_o = 1, before_r = 1, after_r = 1;
+      for (int d = 0; d < qd; ++d) before_o *= operand->dims[d];
+      for (int d = qd + 1; d < operand->rank; ++d) after_o *= operand->dims[d];
+      for (int d = 0; d < rqd; ++d) before_r *= result->dims[d];
+      for (int d = rqd + 1; d < result->rank; ++d) after_r *= result->dims[d];
+      if (before_o != before_r || operand->dims[qd] != result->dims[rqd] || after_o != after_r)
+        return fail(HLO_ERR_INVALID_ARG, "reshape (C3): result dimension %d does not keep the quantized axis intact", rqd);
+    }
+  } else if (result_quantization_dimension != -1) {
+    return fail(HLO_ERR_INVALID_ARG, "reshape: a quantization dimension without operand parameters");
+  }
+  const int eb = dt_bytes(operand->dtype);
+  if (n > 0 && (!operand_ptr || !result_ptr)) return fail(HLO_ERR_INVALID_ARG, "reshape: NULL data pointer");
+  if (ranges_overlap(operand_ptr, n * eb, result_ptr, n * eb))
+    return fail(HLO_ERR_INVALID_ARG, "reshape: operand and result overlap");
+  if (n == 0) return ok();
+  ReshapePlan p;
+  std::memset(&p, 0, sizeof p);
+  p.in = operand_ptr;
+  p.out = result_ptr;
+  p.n = n;
+  p.elem_bytes = eb;
+  int64_t ostr[HLO_MAX_RANK], lex_r[HLO_MAX_RANK];
+  strides_of(*operand, ostr);
+  int64_t acc = 1;
+  for (int d = result->rank - 1; d >= 0; --d) {
+    lex_r[d] = acc;
+    acc *= result->dims[d];
+  }
+  std::vector<int64_t> sz, st2;
+  for (int k = result->rank - 1; k >= 0; --k) {  // result physical axes, major first
+    const int d = (int)result->minor_to_major[k];
+    sz.push_back(result->dims[d]);
+    st2.push_back(lex_r[d]);
+  }
+  p.out_to_lex = make_map(sz, st2);
+  sz.clear();
+  st2.clear();
+  for (int d = 0; d < operand->rank; ++d) {  // lexicographic axes of the operand, major first
+    sz.push_back(operand->dims[d]);
+    st2.push_back(ostr[d]);
+  }
+  p.lex_to_in = make_map(sz, st2);
+  const cudaStream_t s = as_stream(stream);
+  if (p.out_to_lex.identity && p.lex_to_in.identity)
+    return cuda_status(launch_copy(operand_ptr, result_ptr, n * eb, s), "copy launch");
+  return cuda_status(launch_reshape(p, s), "reshape launch");
+}
+
 hlo_status hlo_device_faults(uint32_t* faults, int32_t clear) {
   if (!faults) return fail(HLO_ERR_INVALID_ARG, "device_faults: faults is NULL");
   *faults = 0;

@@ -206,6 +206,21 @@ struct QuantBinaryPlan {
   QuantParams ql, qr, qo;
 };
 cudaError_t launch_quant_binary(const QuantBinaryPlan& p, cudaStream_t s);
+
+// Reshape: output element e (physical order) is the element at lexicographic position
+// p = map_index(out_to_lex, e) of the operand, found at map_index(lex_to_in, p).
+struct ReshapePlan {
+  const void* in;
+  void* out;
+  int64_t n;
+  int elem_bytes;
+  IndexMap out_to_lex, lex_to_in;
+};
+cudaError_t launch_reshape(const ReshapePlan& p, cudaStream_t s);
+// Quantization parameters of a result: n pairs, each copied from (src_s, src_z)[single ? 0 : i], or, with
+// src_s == NULL, the pair (s0, z0) repeated.
+cudaError_t launch_quant_params(const float* src_s, const int32_t* src_z, float s0, int32_t z0, int single, float* dst_s,
+                                int32_t* dst_z, int64_t n, cudaStream_t s);
 // Device-side faults (bit mask, the same values as HLO_FAULT_* of the C ABI).
 constexpr unsigned int kFaultCopyTimeout = 1u;
 // Copy the fault word of a translation unit out (and clear it when asked); the caller has waited for

@@ -1,749 +1,17 @@
 // Transpose / layout-change hero kernels ("XLA:GPU Emitters", section "Transpose emitter": coalesced
-// reads into a shared-memory tile, a barrier, coalesced writes out of it).
+// reads into a shared-memory tile, a barrier, coalesced writes out of it), and the element gathers.
 //
-//  selfadd_pair_kernel  -- out = f(p) + transpose(f(p)) for an n x n array. A block owns the tile
-//                          pair (I,J), (J,I): it loads both once, applies the prologue f once per
-//                          element while staging into padded shared memory, and writes both output
-//                          tiles; so p is read once, f is evaluated once per element (the
-//                          partitioning concern of "XLA:GPU Emitters", section "Partitioning") and the
-//                          output is written once. Persistent blocks walk the pairs.
 //  tile_transpose_kernel -- any physical permutation whose input-minor and output-minor axes
 //                          differ: a 32 x 32 tile over those two axes, other axes batched.
-//  quant_tile_kernel    -- s8 [n0, n1] row-major -> column-major with dequantize / quantize fused:
-//                          128 x 128-byte tiles, 16-byte loads, an XOR-swizzled shared tile read back
-//                          4 bytes at a time, 4x4 byte transposes in registers, 16-byte stores.
-//  gather_kernel        -- everything else: one thread per output element.
+//  gather_kernel        -- everything else: one thread per output element (also the quantized
+//                          relayouts the tile kernel does not take, and broadcast_in_dim).
+//  reshape_kernel       -- reshape with layouts: lexicographic position -> physical offsets.
+#include <type_traits>
+
 #include "device_common.cuh"
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "async_copy.cuh"
 #include "quant_common.cuh"
 
 namespace hlo {
-
-// ---------------------------------------------------------------------------------------------
-// pair-tile self-add transpose
-// ---------------------------------------------------------------------------------------------
-constexpr int kT = 64;        // tile edge (elements)
-constexpr int kTP = kT + 1;   // padded pitch: transposed stores and row reads hit 32 distinct banks
-constexpr int kPairThreads = 256;
-
-enum PairChain : int { PC_NONE = 0, PC_LOG = 1, PC_RT = 2 };
-
-// Maps a pair index to (I, J), I < J, enumerating row by row: a single-precision estimate from the
-// quadratic formula, then exact integer correction. Only 32-bit integer <-> float conversions are used
-// (64-bit ones run on the FP64 pipe, a slow unit on this part); the launcher guarantees that the pair
-// count fits in 31 bits.
-__device__ __forceinline__ void pair_of(int64_t item, int64_t nt, int64_t& I, int64_t& J) {
-  const float b = 2.0f * (float)(int)nt - 1.0f;
-  const float disc = fmaxf(b * b - 8.0f * (float)(int)item, 0.0f);
-  int64_t i = (int)((b - sqrtf(disc)) * 0.5f);
-  i = i < 0 ? 0 : (i > nt - 2 ? nt - 2 : i);
-  auto start = [nt](int64_t r) { return r * (nt - 1) - ((r * (r - 1)) >> 1); };
-  while (i > 0 && start(i) > item) --i;
-  while (start(i + 1) <= item) ++i;
-  I = i;
-  J = i + 1 + (item - start(i));
-}
-
-template <int CH>
-__device__ __forceinline__ float pair_pro(float v, const Chain& c, const LogTab& lt) {
-  if (CH == PC_LOG) return cr_logf(v, lt.c, lt.e);
-  if (CH == PC_RT) return apply_chain_rt(c, v, 0, lt);
-  return v;
-}
-
-// Thread mapping inside a 64 x 64 tile: slot k (0..3) of warp w covers rows 4*rg .. 4*rg+3, columns
-// 32*h .. 32*h+31, with 8 lanes (16 bytes each) per 128-byte row segment. A lane owns row
-// r = 4*rg + lane/8 and columns c .. c+3, c = 32*h + 4*(lane%8).
-__device__ __forceinline__ void pair_slot(int k, int& r, int& c) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int s = warp * 4 + k;
-  r = 4 * (s >> 1) + (lane >> 3);
-  c = 32 * (s & 1) + 4 * (lane & 7);
-}
-
-// Shared state of the pair kernel's log: the two-pass tables and the list of elements whose rounding
-// the first pass left open (their slot offsets; the slot holds the input meanwhile).
-constexpr int kRedoCap = 2048;
-struct PairShared {
-  float l1_inv[32], l1_hi[32], l1_lo[32];
-  int redo_count;
-  uint16_t redo[kRedoCap];
-};
-
-// Loads this thread's 16 elements of tile (TI, TJ), applies the prologue and stores the results
-// transposed: dst[col * kTP + row]. With kTP = 65 the 32 lanes of a store hit 32 distinct banks.
-// For log, the first pass (two elements per f32x2 instruction) settles ~98% of the elements; the
-// others are parked (input value in the slot) on the block's redo list, or in the thread's own
-// spill mask if the list is full, and settled after the barrier.
-template <int CH, bool VEC>
-__device__ __forceinline__ void pair_load(const float* __restrict__ in, int64_t n, int64_t TI, int64_t TJ,
-                                          const int (&toff)[4], float* dst, int dst_base, const Chain& c,
-                                          const LogTab& lt, PairShared& ps, uint32_t& spill) {
-  float4 v[4];
-  const float* tile = in + TI * kT * n + TJ * kT;          // element (0, 0) of the tile
-  const bool full = (TI + 1) * kT <= n && (TJ + 1) * kT <= n;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int r, col;
-    pair_slot(k, r, col);
-    const int64_t gr = TI * kT + r, gc = TJ * kT + col;
-    if (VEC) {
-      if (full || (gr < n && gc < n)) {
-        const float4* src = reinterpret_cast<const float4*>(tile + toff[k]);
-        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                     : "=f"(v[k].x), "=f"(v[k].y), "=f"(v[k].z), "=f"(v[k].w)
-                     : "l"(src));
-      } else {
-        v[k] = make_float4(1.f, 1.f, 1.f, 1.f);
-      }
-    } else {
-      float* o = &v[k].x;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) o[q] = (gr < n && gc + q < n) ? in[gr * n + gc + q] : 1.f;
-    }
-  }
-  uint32_t redo = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int r, col;
-    pair_slot(k, r, col);
-    float y[4];
-    if (CH == PC_LOG) {
-      bool ok[4];
-      cr_logf_first2(v[k].x, v[k].y, ps.l1_inv, ps.l1_hi, ps.l1_lo, y[0], y[1], ok[0], ok[1]);
-      cr_logf_first2(v[k].z, v[k].w, ps.l1_inv, ps.l1_hi, ps.l1_lo, y[2], y[3], ok[2], ok[3]);
-      const float* xi = &v[k].x;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        redo |= (ok[q] ? 0u : 1u) << (4 * k + q);
-        y[q] = ok[q] ? y[q] : xi[q];  // park the input of an open element in its slot
-      }
-    } else {
-      const float* xi = &v[k].x;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) y[q] = pair_pro<CH>(xi[q], c, lt);
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) dst[(col + q) * kTP + r] = y[q];
-  }
-  if (CH == PC_LOG) {
-    // append the open elements to the block list: one atomic per warp
-    const int lane = threadIdx.x & 31;
-    const int cnt = __popc(redo);
-    int incl = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (total) {
-      int base = 0;
-      if (lane == 31) base = atomicAdd(&ps.redo_count, total);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      int pos = base + incl - cnt;
-      uint32_t m = redo;
-      while (m) {
-        const int e = __ffs(m) - 1;
-        m &= m - 1;
-        int r, col;
-        pair_slot(e >> 2, r, col);
-        const int off = dst_base + (col + (e & 3)) * kTP + r;
-        if (pos < kRedoCap) ps.redo[pos] = (uint16_t)off;
-        else spill |= 1u << (e + (dst_base ? 16 : 0));
-        ++pos;
-      }
-    }
-  }
-}
-
-// Settles the elements the first pass left open -- the block's list, then this thread's spills --
-// from the input parked in their slot.
-__device__ __forceinline__ void pair_settle(float* tiles, PairShared& ps, uint32_t spill, const LogTab& lt) {
-  const int cnt = min(ps.redo_count, kRedoCap);
-  for (int j = threadIdx.x; j < cnt; j += kPairThreads) {
-    float* slot = tiles + ps.redo[j];
-    *slot = cr_logf(*slot, lt.c, lt.e);
-  }
-  while (spill) {
-    const int e = __ffs(spill) - 1;
-    spill &= spill - 1;
-    int r, col;
-    pair_slot((e & 15) >> 2, r, col);
-    float* slot = tiles + ((e >= 16) ? kT * kTP : 0) + (col + (e & 3)) * kTP + r;
-    *slot = cr_logf(*slot, lt.c, lt.e);
-  }
-}
-
-// Writes this thread's 16 elements of output tile (TI, TJ) = own[r][c] + other[c][r], where ownT and
-// otherT hold the two tiles transposed (so own[r][c] = ownT[c][r], other[c][r] = otherT[r][c]), then
-// the epilogue. Both reads hit 32 distinct banks per warp.
-template <bool VEC>
-__device__ __forceinline__ void pair_store(float* __restrict__ out, int64_t n, int64_t TI, int64_t TJ,
-                                           const int (&toff)[4], const float* ownT, const float* otherT,
-                                           const Chain& epi, const LogTab& lt) {
-  float* tile = out + TI * kT * n + TJ * kT;
-  const bool full = (TI + 1) * kT <= n && (TJ + 1) * kT <= n;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int r, col;
-    pair_slot(k, r, col);
-    const float* t = otherT + r * kTP + col;
-    const float* o = ownT + col * kTP + r;
-    float4 v;
-    v.x = __fadd_rn(o[0 * kTP], t[0]);
-    v.y = __fadd_rn(o[1 * kTP], t[1]);
-    v.z = __fadd_rn(o[2 * kTP], t[2]);
-    v.w = __fadd_rn(o[3 * kTP], t[3]);
-    if (epi.n) {
-      v.x = apply_chain_rt(epi, v.x, 0, lt);
-      v.y = apply_chain_rt(epi, v.y, 0, lt);
-      v.z = apply_chain_rt(epi, v.z, 0, lt);
-      v.w = apply_chain_rt(epi, v.w, 0, lt);
-    }
-    const int64_t gr = TI * kT + r, gc = TJ * kT + col;
-    if (VEC) {
-      if (full || (gr < n && gc < n)) *reinterpret_cast<float4*>(tile + toff[k]) = v;
-    } else {
-      const float* pv = &v.x;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (gr < n && gc + q < n) out[gr * n + gc + q] = pv[q];
-    }
-  }
-}
-
-template <int CH, bool VEC>
-__global__ void __launch_bounds__(kPairThreads, 4)
-    selfadd_pair_kernel(SelfAddPlan p, int64_t nt, int64_t n_off, int64_t n_items) {
-  extern __shared__ float4 smem_f4[];
-  float4* s_lc = smem_f4;
-  float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
-  float* ta = reinterpret_cast<float*>(s_le + HLO_LOG_NE);  // tile (I,J) after the prologue, transposed
-  float* tb = ta + kT * kTP;                                 // tile (J,I) after the prologue, transposed
-  PairShared& ps = *reinterpret_cast<PairShared*>(tb + kT * kTP);
-  load_log_tables(s_lc, s_le);
-  load_log1_tables(ps.l1_inv, ps.l1_hi, ps.l1_lo);
-  if (threadIdx.x == 0) ps.redo_count = 0;
-  __syncthreads();
-  const LogTab lt = {s_lc, s_le};
-  const float* in = reinterpret_cast<const float*>(p.in);
-  float* out = reinterpret_cast<float*>(p.out);
-  int toff[4];  // this thread's in-tile element offsets (row * n + column); 64 * n < 2^31 always holds
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    int r, col;
-    pair_slot(k, r, col);
-    toff[k] = r * (int)p.n + col;
-  }
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    int64_t I, J;
-    if (item < n_off) {
-      pair_of(item, nt, I, J);
-    } else {
-      I = J = item - n_off;
-    }
-    uint32_t spill = 0;
-    pair_load<CH, VEC>(in, p.n, I, J, toff, ta, 0, p.pro, lt, ps, spill);
-    if (I != J) pair_load<CH, VEC>(in, p.n, J, I, toff, tb, kT * kTP, p.pro, lt, ps, spill);
-    __syncthreads();
-    if (CH == PC_LOG) {
-      if (ps.redo_count) {  // uniform: every thread reads the same count after the barrier
-        pair_settle(ta, ps, spill, lt);
-        __syncthreads();
-      }
-    }
-    if (I != J) {
-      pair_store<VEC>(out, p.n, I, J, toff, ta, tb, p.epi, lt);  // out(I,J) = A + B^T
-      pair_store<VEC>(out, p.n, J, I, toff, tb, ta, p.epi, lt);  // out(J,I) = B + A^T
-    } else {
-      pair_store<VEC>(out, p.n, I, I, toff, ta, ta, p.epi, lt);
-    }
-    if (threadIdx.x == 0) ps.redo_count = 0;  // nobody reads it again before the barrier below
-    __syncthreads();
-  }
-}
-
-// ---------------------------------------------------------------------------------------------
-// Register-blocked pair kernel, for rows that start on 16-byte boundaries (n % 4 == 0, aligned
-// pointers). Thread t owns the 4 x 4 block (bi, bj) = (t / 16, t % 16) of each 64 x 64 tile:
-//   1. it loads its block of tile A = (I,J) and of tile B = (J,I) (four 16-byte loads each; a warp
-//      reads two whole 256-byte tile rows per load), applies the prologue in registers and stores the
-//      blocks to shared memory, 16-byte chunk c of row r at chunk c ^ ((r / 4) % 8) of that row;
-//   2. its warp settles the log elements the first pass left open (a per-warp list, so no block-wide
-//      wait stands between the first pass and the settling);
-//   3. after a barrier it reads its block of A and block (bj, bi) of B, both as four 16-byte reads that
-//      hit 32 distinct banks per quarter-warp, transposes the latter in registers and writes block
-//      (bi, bj) of out(I,J) = A + B^T with four 16-byte stores; then out(J,I) = B + A^T alike.
-// Every element is loaded once, goes through the prologue once, is written to and read from shared
-// memory with one 16-byte access each way, and is stored once.
-// ---------------------------------------------------------------------------------------------
-constexpr int kWarpList = 64;
-struct BlockShared {
-  float l1_inv[32], l1_hi[32], l1_lo[32];
-  uint16_t wlist[kPairThreads / 32][kWarpList];
-};
-
-__device__ __forceinline__ float comp(const float4& v, int k) {
-  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
-}
-
-__device__ __forceinline__ void item_pair(int64_t item, int64_t nt, int64_t n_off, int64_t& I, int64_t& J) {
-  if (item < n_off) {
-    pair_of(item, nt, I, J);
-  } else {
-    I = J = item - n_off;
-  }
-}
-
-// Log of a block's four rows in registers: settled elements take their log, open ones keep their input
-// and set bit 4k+q (+ shift) of `open`.
-__device__ __forceinline__ void block_log(float4 (&v)[4], const float* tinv, const float* thi, const float* tlo,
-                                          uint32_t& open, int shift) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float y[4];
-    bool ok[4];
-    cr_logf_first2(v[k].x, v[k].y, tinv, thi, tlo, y[0], y[1], ok[0], ok[1]);
-    cr_logf_first2(v[k].z, v[k].w, tinv, thi, tlo, y[2], y[3], ok[2], ok[3]);
-    v[k].x = ok[0] ? y[0] : v[k].x;
-    v[k].y = ok[1] ? y[1] : v[k].y;
-    v[k].z = ok[2] ? y[2] : v[k].z;
-    v[k].w = ok[3] ? y[3] : v[k].w;
-    open |= ((ok[0] ? 0u : 1u) | (ok[1] ? 0u : 2u) | (ok[2] ? 0u : 4u) | (ok[3] ? 0u : 8u)) << (4 * k + shift);
-  }
-}
-
-// Settles the warp's open elements in shared memory (their slots hold the input): the warp gathers
-// their offsets into its list and each lane takes one; a lane whose elements do not fit settles the
-// rest itself.
-__device__ __forceinline__ void warp_settle(uint32_t open, float* tiles, int own, uint16_t* wl, const LogTab& lt) {
-  const int lane = threadIdx.x & 31;
-  const int cnt = __popc(open);
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  const int total = __shfl_sync(0xffffffffu, incl, 31);
-  if (total == 0) return;  // warp-uniform
-  int pos = incl - cnt;
-  while (open && pos < kWarpList) {
-    const int b = __ffs(open) - 1;
-    open &= open - 1;
-    wl[pos++] = (uint16_t)((b >> 4) * (kT * kT) + own + ((b >> 2) & 3) * kT + (b & 3));
-  }
-  __syncwarp();  // the blocks' stores and the list are visible to the whole warp
-  const int listed = total < kWarpList ? total : kWarpList;
-  for (int j = lane; j < listed; j += 32) {
-    float* s = tiles + wl[j];
-    *s = cr_logf(*s, lt.c, lt.e);
-  }
-  while (open) {
-    const int b = __ffs(open) - 1;
-    open &= open - 1;
-    float* s = tiles + (b >> 4) * (kT * kT) + own + ((b >> 2) & 3) * kT + (b & 3);
-    *s = cr_logf(*s, lt.c, lt.e);
-  }
-}
-
-// Writes block (bi, bj) of an output tile: row k = a[k] + column k of b (b holds the other tile's
-// block (bj, bi) row by row), then the epilogue. `rows` = rows of the tile left from row 4*bi.
-template <bool EPI>
-__device__ __forceinline__ void block_store(float* dst, int64_t n, const float4 (&a)[4], const float4 (&b)[4],
-                                            int64_t rows, bool cols_ok, const Chain& epi, const LogTab& lt) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float4 v;
-    v.x = __fadd_rn(a[k].x, comp(b[0], k));
-    v.y = __fadd_rn(a[k].y, comp(b[1], k));
-    v.z = __fadd_rn(a[k].z, comp(b[2], k));
-    v.w = __fadd_rn(a[k].w, comp(b[3], k));
-    if (EPI) {
-      v.x = apply_chain_rt(epi, v.x, 0, lt);
-      v.y = apply_chain_rt(epi, v.y, 0, lt);
-      v.z = apply_chain_rt(epi, v.z, 0, lt);
-      v.w = apply_chain_rt(epi, v.w, 0, lt);
-    }
-    if (cols_ok && k < rows) *reinterpret_cast<float4*>(dst + k * n) = v;
-  }
-}
-
-template <int CH, bool EPI>
-__global__ void __launch_bounds__(kPairThreads, 4)
-    selfadd_block_kernel(SelfAddPlan p, int64_t nt, int64_t n_off, int64_t n_items) {
-  extern __shared__ float4 smem_f4[];
-  float* ta = reinterpret_cast<float*>(smem_f4);  // tile A, then tile B: 64 x 64 floats each
-  float* tb = ta + kT * kT;
-  float4* s_lc = reinterpret_cast<float4*>(ta + 2 * kT * kT);
-  float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
-  BlockShared& bs = *reinterpret_cast<BlockShared*>(s_le + HLO_LOG_NE);
-  load_log_tables(s_lc, s_le);
-  load_log1_tables(bs.l1_inv, bs.l1_hi, bs.l1_lo);
-  __syncthreads();
-  const LogTab lt = {s_lc, s_le};
-  const float* in = reinterpret_cast<const float*>(p.in);
-  float* out = reinterpret_cast<float*>(p.out);
-  const int64_t n = p.n;
-  const int bi = threadIdx.x >> 4, bj = threadIdx.x & 15;
-  const int own = 4 * bi * kT + ((bj ^ (bi & 7)) << 2);  // row 4*bi, chunk bj (swizzled)
-  const int oth = 4 * bj * kT + ((bi ^ (bj & 7)) << 2);  // row 4*bj, chunk bi (swizzled)
-  const int64_t goff = 4 * bi * n + 4 * bj;
-  uint16_t* wl = bs.wlist[threadIdx.x >> 5];
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    int64_t I, J;
-    item_pair(item, nt, n_off, I, J);
-    const bool two = I != J;
-    // rows of tile A left from this thread's first row (A's columns are B's rows and vice versa);
-    // n % 4 == 0, so a 4-column chunk is wholly inside or outside
-    const int64_t ra = n - I * kT - 4 * bi, rb = n - J * kT - 4 * bi;
-    const bool ca = J * kT + 4 * bj < n, cb = I * kT + 4 * bj < n;
-    const float* pa = in + (I * kT) * n + J * kT + goff;
-    const float* pb = in + (J * kT) * n + I * kT + goff;
-    float4 va[4], vb[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      va[k] = make_float4(2.f, 2.f, 2.f, 2.f);
-      vb[k] = va[k];
-      if (ca && k < ra)
-        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                     : "=f"(va[k].x), "=f"(va[k].y), "=f"(va[k].z), "=f"(va[k].w)
-                     : "l"(pa + k * n));
-      if (two && cb && k < rb)
-        asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                     : "=f"(vb[k].x), "=f"(vb[k].y), "=f"(vb[k].z), "=f"(vb[k].w)
-                     : "l"(pb + k * n));
-    }
-    uint32_t open = 0;
-    if (CH == PC_LOG) {
-      block_log(va, bs.l1_inv, bs.l1_hi, bs.l1_lo, open, 0);
-      if (two) block_log(vb, bs.l1_inv, bs.l1_hi, bs.l1_lo, open, 16);
-    } else if (CH == PC_RT) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        va[k].x = pair_pro<CH>(va[k].x, p.pro, lt);
-        va[k].y = pair_pro<CH>(va[k].y, p.pro, lt);
-        va[k].z = pair_pro<CH>(va[k].z, p.pro, lt);
-        va[k].w = pair_pro<CH>(va[k].w, p.pro, lt);
-        vb[k].x = pair_pro<CH>(vb[k].x, p.pro, lt);
-        vb[k].y = pair_pro<CH>(vb[k].y, p.pro, lt);
-        vb[k].z = pair_pro<CH>(vb[k].z, p.pro, lt);
-        vb[k].w = pair_pro<CH>(vb[k].w, p.pro, lt);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      *reinterpret_cast<float4*>(ta + own + k * kT) = va[k];
-      if (two) *reinterpret_cast<float4*>(tb + own + k * kT) = vb[k];
-    }
-    if (CH == PC_LOG) warp_settle(open, ta, own, wl, lt);
-    __syncthreads();
-    {
-      float4 a[4], b[4];
-      const float* other = two ? tb : ta;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        a[k] = *reinterpret_cast<const float4*>(ta + own + k * kT);
-        b[k] = *reinterpret_cast<const float4*>(other + oth + k * kT);
-      }
-      block_store<EPI>(out + (I * kT) * n + J * kT + goff, n, a, b, ra, ca, p.epi, lt);  // out(I,J) = A + B^T
-    }
-    if (two) {
-      float4 a[4], b[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        a[k] = *reinterpret_cast<const float4*>(tb + own + k * kT);
-        b[k] = *reinterpret_cast<const float4*>(ta + oth + k * kT);
-      }
-      block_store<EPI>(out + (J * kT) * n + I * kT + goff, n, a, b, rb, cb, p.epi, lt);  // out(J,I) = B + A^T
-    }
-    __syncthreads();  // the tiles are rewritten by the next item
-  }
-}
-
-// ---------------------------------------------------------------------------------------------
-// Tensor-copy pair kernel (the path for rows on 16-byte boundaries when the driver's tensor-map
-// encoder is available). The same thread mapping, prologue, swizzle and transposed stores as
-// selfadd_block_kernel, but the raw input arrives by 2-D tensor copies (cp.async.bulk.tensor, one
-// 64 x 64 box per tile) into a ring of NS shared-memory stages, and the prologue's results are
-// written back into the stage they were read from:
-//   wait for the stage's mbarrier; then per tile: 16-byte reads of the raw rows (a quarter warp reads
-//   128 contiguous bytes), the prologue in registers, __syncwarp, 16-byte writes of the results to
-//   the swizzled positions. A thread's swizzled chunk lies in its own four rows, which only its own
-//   half warp reads, so the warp-level sync orders the in-place rewrite; then the warp settles its
-//   open log elements; block barrier; transposed reads, add, 16-byte stores.
-// The barrier of item j also tells thread 0 that every thread is done with item j-1, so the stage
-// item j-1 used is refilled there with item j + NS - 1: the copies run NS - 1.5 items ahead of use
-// and one barrier per item suffices.
-// A bounded wait that runs out makes the whole block stop (the decision is made block-wide at the
-// barrier), record kFaultCopyTimeout, wait (bounded) for its copies in flight and return.
-// ---------------------------------------------------------------------------------------------
-template <int NS>
-struct TmaShared {
-  float l1_inv[32], l1_hi[32], l1_lo[32];
-  uint16_t wlist[kPairThreads / 32][kWarpList];
-  uint64_t full[NS];
-};
-
-template <int NS>
-static size_t tma_smem_bytes() {
-  return 128 /* alignment slack */ + (size_t)NS * 2 * kT * kT * sizeof(float) + HLO_LOG_NC * sizeof(float4) +
-         HLO_LOG_NE * sizeof(float2) + sizeof(TmaShared<NS>);
-}
-
-// Prologue of one raw tile of the stage, written back in place (swizzled); open log elements keep
-// their input and set their bits in `open` (from bit `shift`).
-template <int CH>
-__device__ __forceinline__ void tma_tile_prologue(float* tile, int raw, int own, const SelfAddPlan& p, const LogTab& lt,
-                                                  const float* tinv, const float* thi, const float* tlo, uint32_t& open,
-                                                  int shift) {
-  float4 v[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const float4*>(tile + raw + k * kT);
-  if (CH == PC_LOG) {
-    block_log(v, tinv, thi, tlo, open, shift);
-  } else if (CH == PC_RT) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      v[k].x = pair_pro<CH>(v[k].x, p.pro, lt);
-      v[k].y = pair_pro<CH>(v[k].y, p.pro, lt);
-      v[k].z = pair_pro<CH>(v[k].z, p.pro, lt);
-      v[k].w = pair_pro<CH>(v[k].w, p.pro, lt);
-    }
-  }
-  __syncwarp();  // the half warp owning these rows has read them
-#pragma unroll
-  for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(tile + own + k * kT) = v[k];
-}
-
-template <int CH, bool EPI, int NS>
-__global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
-    selfadd_tma_kernel(const __grid_constant__ CUtensorMap tmap, SelfAddPlan p, int64_t nt, int64_t n_off,
-                       int64_t n_items) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  float* stage = reinterpret_cast<float*>(base);              // [NS][2][64 * 64]: tile (I,J), tile (J,I)
-  float4* s_lc = reinterpret_cast<float4*>(stage + NS * 2 * kT * kT);
-  float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
-  TmaShared<NS>& ts = *reinterpret_cast<TmaShared<NS>*>(s_le + HLO_LOG_NE);
-  const int tid = threadIdx.x;
-  // copies item `it` (walk position j) into stage j % NS
-  auto issue = [&](int64_t it, int64_t j) {
-    int64_t I, J;
-    item_pair(it, nt, n_off, I, J);
-    const int st = (int)(j % NS);
-    const uint32_t bar = smem_addr(&ts.full[st]);
-    float* dst = stage + st * 2 * kT * kT;
-    mbar_arrive_expect_tx(bar, (I != J ? 2u : 1u) * kT * kT * (uint32_t)sizeof(float));
-    tma_load_2d(dst, &tmap, (int32_t)(J * kT), (int32_t)(I * kT), bar);                      // tile (I, J)
-    if (I != J) tma_load_2d(dst + kT * kT, &tmap, (int32_t)(I * kT), (int32_t)(J * kT), bar);  // tile (J, I)
-  };
-  if (tid == 0) {
-    prefetch_tensor_map(&tmap);
-    for (int st = 0; st < NS; ++st) mbar_init(smem_addr(&ts.full[st]), 1);
-    fence_mbar_init();
-    for (int64_t j = 0; j < NS; ++j) {
-      const int64_t it = blockIdx.x + j * gridDim.x;
-      if (it < n_items) issue(it, j);
-    }
-  }
-  load_log_tables(s_lc, s_le);
-  load_log1_tables(ts.l1_inv, ts.l1_hi, ts.l1_lo);
-  __syncthreads();
-  const LogTab lt = {s_lc, s_le};
-  float* out = reinterpret_cast<float*>(p.out);
-  const int64_t n = p.n;
-  const int bi = tid >> 4, bj = tid & 15;
-  const int own = 4 * bi * kT + ((bj ^ (bi & 7)) << 2);  // row 4*bi, chunk bj (swizzled)
-  const int oth = 4 * bj * kT + ((bi ^ (bj & 7)) << 2);  // row 4*bj, chunk bi (swizzled)
-  const int raw = 4 * bi * kT + 4 * bj;                  // row 4*bi, columns 4*bj.. of a raw tile
-  const int64_t goff = 4 * bi * n + 4 * bj;
-  uint16_t* wl = ts.wlist[tid >> 5];
-  int64_t j = 0;
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
-    int64_t I, J;
-    item_pair(item, nt, n_off, I, J);
-    const bool two = I != J;
-    const int st = (int)(j % NS);
-    const bool arrived = mbar_wait(smem_addr(&ts.full[st]), (uint32_t)((j / NS) & 1));
-    float* ta = stage + st * 2 * kT * kT;
-    float* tb = ta + kT * kT;
-    uint32_t open = 0;
-    tma_tile_prologue<CH>(ta, raw, own, p, lt, ts.l1_inv, ts.l1_hi, ts.l1_lo, open, 0);
-    if (two) tma_tile_prologue<CH>(tb, raw, own, p, lt, ts.l1_inv, ts.l1_hi, ts.l1_lo, open, 16);
-    if (CH == PC_LOG) warp_settle(open, ta, own, wl, lt);
-    // every tile of item j is complete, and every thread is done with item j - 1
-    if (__syncthreads_or(arrived ? 0 : 1)) {
-      // a copy did not arrive in time: record the fault, wait (bounded) for this block's copies still
-      // in flight (items j .. j + NS - 2, plus j + NS - 1 if it was issued), leave the rest of its
-      // outputs unwritten and return
-      if (tid == 0) {
-        record_fault(kFaultCopyTimeout);
-        for (int64_t q = j; q < j + NS && blockIdx.x + q * gridDim.x < n_items; ++q)
-          if (q < j + NS - 1 || j == 0) mbar_wait(smem_addr(&ts.full[q % NS]), (uint32_t)((q / NS) & 1));
-      }
-      return;
-    }
-    if (tid == 0 && j > 0) {  // refill the stage of item j - 1 with item j + NS - 1
-      const int64_t nxt = item + (int64_t)(NS - 1) * gridDim.x;
-      if (nxt < n_items) {
-        fence_proxy_async();
-        issue(nxt, j + NS - 1);
-      }
-    }
-    const int64_t rows_a = n - I * kT - 4 * bi, rows_b = n - J * kT - 4 * bi;
-    const bool ca = J * kT + 4 * bj < n, cb = I * kT + 4 * bj < n;
-    {
-      float4 a[4], b[4];
-      const float* other = two ? tb : ta;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        a[k] = *reinterpret_cast<const float4*>(ta + own + k * kT);
-        b[k] = *reinterpret_cast<const float4*>(other + oth + k * kT);
-      }
-      block_store<EPI>(out + (I * kT) * n + J * kT + goff, n, a, b, rows_a, ca, p.epi, lt);  // out(I,J) = A + B^T
-    }
-    if (two) {
-      float4 a[4], b[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        a[k] = *reinterpret_cast<const float4*>(tb + own + k * kT);
-        b[k] = *reinterpret_cast<const float4*>(ta + oth + k * kT);
-      }
-      block_store<EPI>(out + (J * kT) * n + I * kT + goff, n, a, b, rows_b, cb, p.epi, lt);  // out(J,I) = B + A^T
-    }
-  }
-}
-
-// The driver's tensor-map encoder, looked up once through the runtime (no link against libcuda).
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool looked = false;
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!looked) {
-    looked = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    else
-      cudaGetLastError();  // the lookup's own error, if any: the caller falls back to plain loads
-  }
-  return fn;
-}
-
-// A 2-D f32 tensor map over the n x n row-major input with 64 x 64 boxes; false if it cannot be made.
-static bool make_pair_tensor_map(const SelfAddPlan& p, CUtensorMap* map) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc || p.n > (int64_t)INT32_MAX) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)p.n, (cuuint64_t)p.n};
-  const cuuint64_t strides[1] = {(cuuint64_t)p.n * sizeof(float)};
-  const cuuint32_t box[2] = {kT, kT};
-  const cuuint32_t elem_strides[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(p.in), dims, strides, box, elem_strides,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-#ifndef HLO_SELFADD_STAGES
-#define HLO_SELFADD_STAGES 3
-#endif
-template <int CH, bool EPI>
-static cudaError_t tma_launch(const SelfAddPlan& p, const CUtensorMap& map, cudaStream_t s) {
-  constexpr int NS = HLO_SELFADD_STAGES;
-  auto kernel = selfadd_tma_kernel<CH, EPI, NS>;
-  const size_t smem = tma_smem_bytes<NS>();
-  const int nb = kernel_blocks_per_sm((const void*)kernel, kPairThreads, smem);
-  const int64_t nt = (p.n + kT - 1) / kT;
-  const int64_t n_off = nt * (nt - 1) / 2;
-  const int64_t n_items = n_off + nt;
-  int64_t grid = (int64_t)device_sm_count() * nb;
-  if (grid > n_items) grid = n_items;
-  if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, kPairThreads, smem, s>>>(map, p, nt, n_off, n_items);
-  return cudaGetLastError();
-}
-
-cudaError_t read_faults_transpose(unsigned int* faults, bool clear) { return read_tu_faults(faults, clear); }
-
-static size_t block_smem_bytes() {
-  return 2 * kT * kT * sizeof(float) + HLO_LOG_NC * sizeof(float4) + HLO_LOG_NE * sizeof(float2) +
-         sizeof(BlockShared);
-}
-
-template <int CH, bool EPI>
-static cudaError_t block_launch(const SelfAddPlan& p, cudaStream_t s) {
-  auto kernel = selfadd_block_kernel<CH, EPI>;
-  const size_t smem = block_smem_bytes();
-  const int nb = kernel_blocks_per_sm((const void*)kernel, kPairThreads, smem);
-  const int64_t nt = (p.n + kT - 1) / kT;
-  const int64_t n_off = nt * (nt - 1) / 2;
-  const int64_t n_items = n_off + nt;
-  int64_t grid = (int64_t)device_sm_count() * nb;
-  if (grid > n_items) grid = n_items;
-  if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, kPairThreads, smem, s>>>(p, nt, n_off, n_items);
-  return cudaGetLastError();
-}
-
-static size_t pair_smem_bytes() {
-  return HLO_LOG_NC * sizeof(float4) + HLO_LOG_NE * sizeof(float2) + 2 * kT * kTP * sizeof(float) +
-         sizeof(PairShared);
-}
-
-template <int CH, bool VEC>
-static cudaError_t pair_launch(const SelfAddPlan& p, cudaStream_t s) {
-  auto kernel = selfadd_pair_kernel<CH, VEC>;
-  const size_t smem = pair_smem_bytes();
-  const int nb = kernel_blocks_per_sm((const void*)kernel, kPairThreads, smem);
-  const int64_t nt = (p.n + kT - 1) / kT;
-  const int64_t n_off = nt * (nt - 1) / 2;
-  const int64_t n_items = n_off + nt;
-  int64_t grid = (int64_t)device_sm_count() * nb;
-  if (grid > n_items) grid = n_items;
-  if (grid < 1) grid = 1;
-  kernel<<<(unsigned)grid, kPairThreads, smem, s>>>(p, nt, n_off, n_items);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_selfadd_transpose(const SelfAddPlan& p, cudaStream_t s) {
-  if (p.n == 0) return cudaSuccess;
-  const bool vec = (p.n % 4 == 0) && ((uintptr_t)p.in % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
-  int ch = PC_RT;
-  if (p.pro.n == 0) ch = PC_NONE;
-  else if (p.pro.n == 1 && p.pro.op[0] == OP_LOG) ch = PC_LOG;
-  CUtensorMap map;
-  if (vec && make_pair_tensor_map(p, &map)) {  // rows on 16-byte boundaries: tensor copies into a stage ring
-    if (p.epi.n) {
-      if (ch == PC_LOG) return tma_launch<PC_LOG, true>(p, map, s);
-      if (ch == PC_NONE) return tma_launch<PC_NONE, true>(p, map, s);
-      return tma_launch<PC_RT, true>(p, map, s);
-    }
-    if (ch == PC_LOG) return tma_launch<PC_LOG, false>(p, map, s);
-    if (ch == PC_NONE) return tma_launch<PC_NONE, false>(p, map, s);
-    return tma_launch<PC_RT, false>(p, map, s);
-  }
-  if (vec) {  // rows on 16-byte boundaries: the register-blocked kernel
-    if (p.epi.n) {
-      if (ch == PC_LOG) return block_launch<PC_LOG, true>(p, s);
-      if (ch == PC_NONE) return block_launch<PC_NONE, true>(p, s);
-      return block_launch<PC_RT, true>(p, s);
-    }
-    if (ch == PC_LOG) return block_launch<PC_LOG, false>(p, s);
-    if (ch == PC_NONE) return block_launch<PC_NONE, false>(p, s);
-    return block_launch<PC_RT, false>(p, s);
-  }
-  if (ch == PC_LOG) return vec ? pair_launch<PC_LOG, true>(p, s) : pair_launch<PC_LOG, false>(p, s);
-  if (ch == PC_NONE) return vec ? pair_launch<PC_NONE, true>(p, s) : pair_launch<PC_NONE, false>(p, s);
-  return vec ? pair_launch<PC_RT, true>(p, s) : pair_launch<PC_RT, false>(p, s);
-}
 
 // ---------------------------------------------------------------------------------------------
 // generic tiled transpose over canonical axes
@@ -823,371 +91,6 @@ cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------------------------
-// quantization
-// ---------------------------------------------------------------------------------------------
-constexpr int kQT = 128;  // tile edge in bytes
-
-struct __align__(16) QuantSmem {
-  float sin_[kQT];   // input scale per tile row (axis 0) or column (axis 1)
-  int zin[kQT];
-  float sout[kQT];   // output scale per tile row or column
-  float inv[kQT];    // RN(1 / output scale)
-  int zout[kQT];
-  int zinm[kQT];     // kMagicBits - input zero point: code + zinm = bits of (1.5*2^23 + code - zp)
-  float nzin[kQT];   // -(1.5*2^23 + 128 + input zero point), exact
-  float mout[kQT];   // 1.5*2^23 + output zero point, exact
-};
-
-// Ragged or unaligned tile, byte by byte (kept out of line: it is rare and large).
-__device__ __noinline__ void quant_tile_ragged(const QuantTilePlan& p, int64_t i0, int64_t j0, uint8_t* bt,
-                                               const QuantSmem& q) {
-  const int t = threadIdx.x;
-  for (int e = t; e < kQT * kQT; e += blockDim.x) {
-    const int row = e / kQT, col = e % kQT;
-    const int64_t i = i0 + row, j = j0 + col;
-    if (i < p.n0 && j < p.n1) {
-      const int code = (int)p.in[i * p.n1 + j];
-      float sin = p.qin.scale;
-      int zin = p.qin.zp;
-      if (p.qin.axis == 0) { sin = q.sin_[row]; zin = q.zin[row]; }
-      if (p.qin.axis == 1) { sin = q.sin_[col]; zin = q.zin[col]; }
-      float real = dequant(code, sin, zin);
-      if (p.ops.n) real = apply_chain_rt(p.ops, real, 0, global_log_tables());
-      float sout = p.qout.scale, inv = p.qout.inv_scale;
-      int zout = p.qout.zp;
-      if (p.qout.axis == 0) { sout = q.sout[row]; inv = q.inv[row]; zout = q.zout[row]; }
-      if (p.qout.axis == 1) { sout = q.sout[col]; inv = q.inv[col]; zout = q.zout[col]; }
-      bt[col * kQT + row] = (uint8_t)quant_code(real, sout, inv, zout, p.qout.smin, p.qout.smax);
-    }
-  }
-  __syncthreads();
-  for (int e = t; e < kQT * kQT; e += blockDim.x) {
-    const int col = e / kQT, row = e % kQT;
-    const int64_t i = i0 + row, j = j0 + col;
-    if (i < p.n0 && j < p.n1) p.out[j * p.n0 + i] = (int8_t)bt[col * kQT + row];
-  }
-}
-
-template <int QIN, int QOUT, bool OPS>
-__device__ __forceinline__ void quant_params(int row, int jl, const QuantTilePlan& p, const QuantSmem& q, float& sin,
-                                             int& zin, float& sout, float& inv, int& zout) {
-  sin = QIN == 0 ? q.sin_[row] : QIN == 1 ? q.sin_[jl] : p.qin.scale;
-  zin = QIN == 0 ? q.zin[row] : QIN == 1 ? q.zin[jl] : p.qin.zp;
-  sout = QOUT == 0 ? q.sout[row] : QOUT == 1 ? q.sout[jl] : p.qout.scale;
-  inv = QOUT == 0 ? q.inv[row] : QOUT == 1 ? q.inv[jl] : p.qout.inv_scale;
-  zout = QOUT == 0 ? q.zout[row] : QOUT == 1 ? q.zout[jl] : p.qout.zp;
-}
-
-// Dequantize -> [float chain] -> quantize for two codes with float2 arithmetic. The fast path of
-// quant_code: y = real * RN(1/scale) is within 2^-22 |y| of the IEEE quotient, so both round to the
-// same integer when 0.5 - |y - rint(y)| > 2^-22 |y|. With f = y - rint(y), 0.5 - |f| >= 1/4 - f^2 and
-// 2^-22 |y| <= 2^-31 y^2 + 2^-15 (|y| <= (y^2/a + a)/2 with a = 2^8), so it suffices that
-// f^2 + 2^-31 y^2 < 1/4 - 2^-15 - 2^-24 (the last term absorbs the roundings of the test). NaN,
-// infinities and |y| >= 2^14.5 fail the test as well. Lanes that fail are settled exactly later.
-template <bool OPS>
-__device__ __forceinline__ void quant_two(int c0, int c1, float2 sin, int zm0, int zm1, float2 inv, int zo0, int zo1,
-                                          int smin, int smax, const QuantTilePlan& p, int& q0, int& q1, bool& ok0,
-                                          bool& ok1) {
-  const float2 magic = make_float2(kMagic, kMagic);
-  const float2 df = __fadd2_rn(make_float2(__int_as_float(c0 + zm0), __int_as_float(c1 + zm1)),
-                               make_float2(-kMagic, -kMagic));  // exact code - zero point
-  float2 real = __fmul2_rn(sin, df);
-  if (OPS) {
-    real.x = apply_chain_rt(p.ops, real.x, 0, global_log_tables());
-    real.y = apply_chain_rt(p.ops, real.y, 0, global_log_tables());
-  }
-  const float2 y = __fmul2_rn(real, inv);
-  const float2 t = __fadd2_rn(y, magic);
-  const float2 f = __ffma2_rn(__fadd2_rn(t, make_float2(-kMagic, -kMagic)), make_float2(-1.0f, -1.0f), y);
-  const float2 yy = __fmul2_rn(y, __fmul2_rn(y, make_float2(0x1p-31f, 0x1p-31f)));
-  const float2 lhs = __ffma2_rn(f, f, yy);
-  constexpr float kLim = 0.25f - 0x1p-15f - 0x1p-24f;  // exact in f32
-  ok0 = lhs.x < kLim;
-  ok1 = lhs.y < kLim;
-  q0 = min(max((__float_as_int(t.x) - kMagicBits) + zo0, smin), smax);
-  q1 = min(max((__float_as_int(t.y) - kMagicBits) + zo1, smin), smax);
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int m) {
-  return m == 0 ? v.x : (m == 1 ? v.y : (m == 2 ? v.z : v.w));
-}
-
-// Four 16-byte row chunks (tile rows r0 + 32k, k = 0..3; local columns 16c .. 16c+15) -> their output
-// codes, in place. Column parameters are loaded once for the four rows, row parameters once per row.
-template <int QIN, int QOUT, bool OPS>
-__device__ __forceinline__ void quant_rows(uint4 (&v)[4], int r0, int c, const QuantTilePlan& p, const QuantSmem& q) {
-  float rs[4], ri[4];
-  int rzm[4], rzo[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int row = r0 + 32 * k;
-    rs[k] = QIN == 0 ? q.sin_[row] : p.qin.scale;
-    rzm[k] = QIN == 0 ? q.zinm[row] : kMagicBits - p.qin.zp;
-    ri[k] = QOUT == 0 ? q.inv[row] : p.qout.inv_scale;
-    rzo[k] = QOUT == 0 ? q.zout[row] : p.qout.zp;
-  }
-  const int smin = p.qout.smin, smax = p.qout.smax;
-  uint32_t o[4][4];
-  uint32_t redo[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    int r[4][4];
-#pragma unroll
-    for (int b = 0; b < 4; b += 2) {
-      const int jl = 16 * c + 4 * m + b;
-      float2 cs = make_float2(0.f, 0.f), ci = make_float2(0.f, 0.f);
-      int czm0 = 0, czm1 = 0, czo0 = 0, czo1 = 0;
-      if (QIN == 1) {
-        cs = *reinterpret_cast<const float2*>(&q.sin_[jl]);
-        czm0 = q.zinm[jl];
-        czm1 = q.zinm[jl + 1];
-      }
-      if (QOUT == 1) {
-        ci = *reinterpret_cast<const float2*>(&q.inv[jl]);
-        czo0 = q.zout[jl];
-        czo1 = q.zout[jl + 1];
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t w = word_of(v[k], m);
-        const int c0 = (int)(int8_t)(w >> (8 * b)), c1 = (int)(int8_t)(w >> (8 * b + 8));
-        const float2 s2 = QIN == 1 ? cs : make_float2(rs[k], rs[k]);
-        const float2 i2 = QOUT == 1 ? ci : make_float2(ri[k], ri[k]);
-        bool ok0, ok1;
-        quant_two<OPS>(c0, c1, s2, QIN == 1 ? czm0 : rzm[k], QIN == 1 ? czm1 : rzm[k], i2,
-                       QOUT == 1 ? czo0 : rzo[k], QOUT == 1 ? czo1 : rzo[k], smin, smax, p, r[k][b], r[k][b + 1],
-                       ok0, ok1);
-        redo[k] |= ((ok0 ? 0u : 1u) | (ok1 ? 0u : 2u)) << (4 * m + b);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      o[k][m] = __byte_perm(__byte_perm(r[k][0], r[k][1], 0x0040), __byte_perm(r[k][2], r[k][3], 0x0040), 0x5410);
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t rk = redo[k];
-    const int row = r0 + 32 * k;
-#pragma unroll 1
-    while (rk) {  // rare: the exact definition decides
-      const int e = __ffs(rk) - 1;
-      rk &= rk - 1;
-      const int m = e >> 2, b = e & 3, jl = 16 * c + e;
-      const int code = (int)(int8_t)(word_of(v[k], m) >> (8 * b));
-      float sin, sout, inv;
-      int zin, zout;
-      quant_params<QIN, QOUT, OPS>(row, jl, p, q, sin, zin, sout, inv, zout);
-      float real = dequant(code, sin, zin);
-      if (OPS) real = apply_chain_rt(p.ops, real, 0, global_log_tables());
-      const int res = quant_code_exact(real, sout, zout, smin, smax);
-#pragma unroll
-      for (int mm = 0; mm < 4; ++mm)  // static indices keep o in registers
-        if (mm == m) o[k][mm] = (o[k][mm] & ~(0xFFu << (8 * b))) | (((uint32_t)res & 0xFFu) << (8 * b));
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) v[k] = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
-}
-
-// Dequantize -> quantize of four 16-byte row chunks without a float chain, for finite parameters with
-// |scale_in / scale_out| < 2^13 (so |y| < 2^21 below). Per code:
-//  * d = code - zp exactly: after flipping the sign bits, the byte (code + 128) becomes the low byte of
-//    the f32 1.5*2^23, and subtracting 1.5*2^23 + 128 + zp is exact;
-//  * real = RN(scale_in * d), as the definition has it; y = RN(real * RN(1/scale_out)) lies within
-//    1.5*2^-23 (1 + 2^-22) |y| of the IEEE quotient RN(real / scale_out), so y(1 - 2^-22) and
-//    y(1 + 2^-22) bracket it;
-//  * t± = RN(y(1 ± 2^-22) + M) with M = 1.5*2^23 + zp_out (one FMA each) is M + the nearest integer to
-//    y(1 ± 2^-22). When t+ = t-, no half-integer lies in the bracket (an end can be one only for
-//    |y| >= 2^21, where the clamp decides anyway), so rint(quotient) + zp_out = bits(t) - bits(1.5*2^23).
-// cvt.pack.sat saturates to [-128, 127]; CLAMP adds a narrower storage range. Words holding a code whose
-// bracket contained a half-integer (about 1 in 10^4 at |y| ~ 100) are redone with the exact definition.
-template <int QIN, int QOUT, bool CLAMP>
-__device__ __forceinline__ void quant_rows_bracket(uint4 (&v)[4], int r0, int c, const QuantTilePlan& p,
-                                                   const QuantSmem& q) {
-  float rs[4], rz[4], ri[4], rm[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int row = r0 + 32 * k;
-    rs[k] = QIN == 0 ? q.sin_[row] : p.qin.scale;
-    rz[k] = QIN == 0 ? q.nzin[row] : -(kMagic + 128.0f + (float)p.qin.zp);
-    ri[k] = QOUT == 0 ? q.inv[row] : p.qout.inv_scale;
-    rm[k] = QOUT == 0 ? q.mout[row] : kMagic + (float)p.qout.zp;
-  }
-  const int smin = p.qout.smin, smax = p.qout.smax;
-  const float2 kp = make_float2(1.0f + 0x1p-22f, 1.0f + 0x1p-22f), km = make_float2(1.0f - 0x1p-22f, 1.0f - 0x1p-22f);
-  uint32_t o[4][4];
-  uint32_t redo = 0u;  // bit 4k + m: word m of chunk k
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    uint32_t hi[4], dw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int b = 2; b >= 0; b -= 2) {  // codes 2, 3 first: their pack is the upper half of the word
-      const int jl = 16 * c + 4 * m + b;
-      float2 cs = make_float2(0.f, 0.f), cz = cs, ci = cs, cm = cs;
-      if (QIN == 1) {
-        cs = *reinterpret_cast<const float2*>(&q.sin_[jl]);
-        cz = *reinterpret_cast<const float2*>(&q.nzin[jl]);
-      }
-      if (QOUT == 1) {
-        ci = *reinterpret_cast<const float2*>(&q.inv[jl]);
-        cm = *reinterpret_cast<const float2*>(&q.mout[jl]);
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t w = word_of(v[k], m) ^ 0x80808080u;
-        const float2 e = make_float2(__uint_as_float(__byte_perm(w, (uint32_t)kMagicBits, 0x7650u | b)),
-                                     __uint_as_float(__byte_perm(w, (uint32_t)kMagicBits, 0x7650u | (b + 1))));
-        const float2 df = __fadd2_rn(e, QIN == 1 ? cz : make_float2(rz[k], rz[k]));
-        const float2 real = __fmul2_rn(QIN == 1 ? cs : make_float2(rs[k], rs[k]), df);
-        const float2 y = __fmul2_rn(real, QOUT == 1 ? ci : make_float2(ri[k], ri[k]));
-        const float2 mm = QOUT == 1 ? cm : make_float2(rm[k], rm[k]);
-        const float2 tp = __ffma2_rn(y, kp, mm), tm = __ffma2_rn(y, km, mm);
-        dw[k] |= (__float_as_uint(tp.x) ^ __float_as_uint(tm.x)) | (__float_as_uint(tp.y) ^ __float_as_uint(tm.y));
-        int q0 = __float_as_int(tp.x) - kMagicBits, q1 = __float_as_int(tp.y) - kMagicBits;
-        if (CLAMP) {
-          q0 = min(max(q0, smin), smax);
-          q1 = min(max(q1, smin), smax);
-        }
-        if (b == 2) asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi[k]) : "r"(q1), "r"(q0));
-        else asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(o[k][m]) : "r"(q1), "r"(q0), "r"(hi[k]));
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) redo |= (dw[k] != 0u ? 1u : 0u) << (4 * k + m);
-  }
-#pragma unroll 1
-  while (redo) {  // rare: the exact definition decides the word's four codes
-    const int e = __ffs(redo) - 1;
-    redo &= redo - 1;
-    const int k = e >> 2, m = e & 3, row = r0 + 32 * k;
-    const uint32_t w = word_of(v[k], m);
-    uint32_t res = 0u;
-    for (int b = 0; b < 4; ++b) {
-      float sin, sout, inv;
-      int zin, zout;
-      quant_params<QIN, QOUT, false>(row, 16 * c + 4 * m + b, p, q, sin, zin, sout, inv, zout);
-      const int code = (int)(int8_t)(w >> (8 * b));
-      res |= ((uint32_t)quant_code_exact(dequant(code, sin, zin), sout, zout, smin, smax) & 0xFFu) << (8 * b);
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)  // static indices keep o in registers
-#pragma unroll
-      for (int mm = 0; mm < 4; ++mm)
-        if (kk == k && mm == m) o[kk][mm] = res;
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) v[k] = make_uint4(o[k][0], o[k][1], o[k][2], o[k][3]);
-}
-
-template <int QIN, int QOUT, bool OPS>
-__global__ void __launch_bounds__(256, 4) quant_tile_kernel(QuantTilePlan p, int64_t ntj) {
-  __shared__ __align__(16) uint32_t tile[kQT * kQT / 4];  // 128 rows x 32 words, word column swizzled
-  __shared__ QuantSmem q;
-  const int t = threadIdx.x;
-  const int64_t ti = blockIdx.x / ntj, tj = blockIdx.x % ntj;
-  const int64_t i0 = ti * kQT, j0 = tj * kQT;
-  const int64_t n0 = p.n0, n1 = p.n1;
-  // stage the per-axis parameters of this tile
-  bool bad = false;
-  if (t < kQT) {
-    const int64_t i = i0 + t, j = j0 + t;
-    if (p.qin.axis == 0 && i < n0) { q.sin_[t] = p.qin.scales[i]; q.zin[t] = p.qin.zps[i]; }
-    if (p.qin.axis == 1 && j < n1) { q.sin_[t] = p.qin.scales[j]; q.zin[t] = p.qin.zps[j]; }
-    float a = fabsf(p.qin.scale), b = fabsf(p.qout.inv_scale);
-    if (p.qin.axis >= 0 && (p.qin.axis == 0 ? i < n0 : j < n1)) {
-      q.zinm[t] = kMagicBits - q.zin[t];
-      q.nzin[t] = -(kMagic + 128.0f + (float)q.zin[t]);
-      a = fabsf(q.sin_[t]);
-    }
-    const int64_t k = p.qout.axis == 0 ? i : j;
-    if (p.qout.axis >= 0 && k < (p.qout.axis == 0 ? n0 : n1)) {
-      const float s = p.qout.scales[k];
-      q.sout[t] = s;
-      q.inv[t] = __frcp_rn(s);
-      q.zout[t] = p.qout.zps[k];
-      q.mout[t] = kMagic + (float)q.zout[t];
-      b = fabsf(q.inv[t]);
-    }
-    bad = !(a < 0x1p60f && b < 0x1p60f && a * b < 8192.0f);  // outside quant_rows_bracket's range
-  }
-  const int slow = __syncthreads_or(bad);
-  const bool full = (i0 + kQT <= n0) && (j0 + kQT <= n1) && (n0 % 16 == 0) && (n1 % 16 == 0) &&
-                    ((uintptr_t)p.in % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
-  if (!full) {
-    quant_tile_ragged(p, i0, j0, reinterpret_cast<uint8_t*>(tile), q);
-    return;
-  }
-  // 128 rows x 8 chunks of 16 bytes; chunk (row, c) stored at word column 4 * (c ^ ((row >> 4) & 7))
-  uint4 v[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int qd = t + 256 * k, row = qd >> 3, c = qd & 7;
-    const uint4* src = reinterpret_cast<const uint4*>(p.in + (i0 + row) * n1 + j0 + 16 * c);
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v[k].x), "=r"(v[k].y), "=r"(v[k].z), "=r"(v[k].w)
-                 : "l"(src));
-  }
-  if (!OPS && !slow) {  // rows t/8 + 32k, chunk t%8
-    if (p.qout.smin > -128 || p.qout.smax < 127) quant_rows_bracket<QIN, QOUT, true>(v, t >> 3, t & 7, p, q);
-    else quant_rows_bracket<QIN, QOUT, false>(v, t >> 3, t & 7, p, q);
-  } else {
-    quant_rows<QIN, QOUT, OPS>(v, t >> 3, t & 7, p, q);
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int qd = t + 256 * k, row = qd >> 3, c = qd & 7;
-    const int wc = 4 * (c ^ ((row >> 4) & 7));
-    *reinterpret_cast<uint4*>(&tile[row * 32 + wc]) = v[k];
-  }
-  __syncthreads();
-  // unit: word column jg (output rows 4jg..4jg+3), 16-row chunk ic
-  const int jg = t >> 3, ic = t & 7;
-  uint32_t w[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) w[k] = tile[(16 * ic + k) * 32 + (jg ^ (4 * ic))];
-  uint32_t outw[4][4];  // [q][m]
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const uint32_t a = w[4 * m], b = w[4 * m + 1], c = w[4 * m + 2], d = w[4 * m + 3];
-    const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
-    const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
-    outw[0][m] = __byte_perm(t0, t2, 0x5410);
-    outw[1][m] = __byte_perm(t0, t2, 0x7632);
-    outw[2][m] = __byte_perm(t1, t3, 0x5410);
-    outw[3][m] = __byte_perm(t1, t3, 0x7632);
-  }
-#pragma unroll
-  for (int qq = 0; qq < 4; ++qq) {
-    uint4* dst = reinterpret_cast<uint4*>(p.out + (j0 + 4 * jg + qq) * n0 + i0 + 16 * ic);
-    *dst = make_uint4(outw[qq][0], outw[qq][1], outw[qq][2], outw[qq][3]);
-  }
-}
-
-template <int QIN, int QOUT>
-static cudaError_t quant_launch2(const QuantTilePlan& p, int64_t blocks, int64_t ntj, cudaStream_t s) {
-  if (p.ops.n) quant_tile_kernel<QIN, QOUT, true><<<(unsigned)blocks, 256, 0, s>>>(p, ntj);
-  else quant_tile_kernel<QIN, QOUT, false><<<(unsigned)blocks, 256, 0, s>>>(p, ntj);
-  return cudaGetLastError();
-}
-
-template <int QIN>
-static cudaError_t quant_launch1(const QuantTilePlan& p, int64_t blocks, int64_t ntj, cudaStream_t s) {
-  if (p.qout.axis == 0) return quant_launch2<QIN, 0>(p, blocks, ntj, s);
-  if (p.qout.axis == 1) return quant_launch2<QIN, 1>(p, blocks, ntj, s);
-  return quant_launch2<QIN, -1>(p, blocks, ntj, s);
-}
-
-cudaError_t launch_quant_tile(const QuantTilePlan& p, cudaStream_t s) {
-  const int64_t nti = (p.n0 + kQT - 1) / kQT, ntj = (p.n1 + kQT - 1) / kQT;
-  const int64_t blocks = nti * ntj;
-  if (blocks == 0) return cudaSuccess;
-  if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-  if (p.qin.axis == 0) return quant_launch1<0>(p, blocks, ntj, s);
-  if (p.qin.axis == 1) return quant_launch1<1>(p, blocks, ntj, s);
-  return quant_launch1<-1>(p, blocks, ntj, s);
-}
-
-// ---------------------------------------------------------------------------------------------
 // general gather
 // ---------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) gather_kernel(GatherPlan p) {
@@ -1248,6 +151,47 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherPlan p) {
     inv = __frcp_rn(sout);
   }
   reinterpret_cast<int8_t*>(p.out)[e] = (int8_t)quant_code(real, sout, inv, zout, p.qout.smin, p.qout.smax);
+}
+
+// ---------------------------------------------------------------------------------------------
+// reshape and the parameters of quantized data movement
+// ---------------------------------------------------------------------------------------------
+template <int EB>
+__global__ void __launch_bounds__(256) reshape_kernel(ReshapePlan p) {
+  using T = typename std::conditional<EB == 4, uint32_t, typename std::conditional<EB == 2, uint16_t, uint8_t>::type>::type;
+  const T* in = reinterpret_cast<const T*>(p.in);
+  T* out = reinterpret_cast<T*>(p.out);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < p.n; e += (int64_t)gridDim.x * blockDim.x)
+    out[e] = in[map_index(p.lex_to_in, map_index(p.out_to_lex, e))];
+}
+
+cudaError_t launch_reshape(const ReshapePlan& p, cudaStream_t s) {
+  if (p.n == 0) return cudaSuccess;
+  int64_t blocks = (p.n + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (p.elem_bytes == 4) reshape_kernel<4><<<(unsigned)blocks, 256, 0, s>>>(p);
+  else if (p.elem_bytes == 2) reshape_kernel<2><<<(unsigned)blocks, 256, 0, s>>>(p);
+  else reshape_kernel<1><<<(unsigned)blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+__global__ void quant_params_kernel(const float* src_s, const int32_t* src_z, float s0, int32_t z0, int single,
+                                    float* dst_s, int32_t* dst_z, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t k = single ? 0 : i;
+    dst_s[i] = src_s ? src_s[k] : s0;
+    dst_z[i] = src_s ? src_z[k] : z0;
+  }
+}
+
+cudaError_t launch_quant_params(const float* src_s, const int32_t* src_z, float s0, int32_t z0, int single, float* dst_s,
+                                int32_t* dst_z, int64_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > 1024) blocks = 1024;
+  quant_params_kernel<<<(unsigned)blocks, 256, 0, s>>>(src_s, src_z, s0, z0, single, dst_s, dst_z, n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const GatherPlan& p, cudaStream_t s) {
