@@ -164,7 +164,15 @@ typedef struct {
  *   init_value       the init value, converted to the accumulation type
  *   accum_dtype      must be HLO_F32 (the body's element type; inputs are promoted to it, C6)
  *   out, out_ptr     output array (f32, bf16 or f16); the f32 result is rounded to nearest even
- *   workspace        device scratch of at least hlo_reduce_workspace_size() bytes (NULL if 0)
+ *   workspace        device scratch of at least hlo_reduce_workspace_size() bytes, or NULL with
+ *                    workspace_bytes == 0. The library only uses it for row reductions with too few
+ *                    rows to occupy the device (for example a reduction of a whole array to one
+ *                    value): each row is cut into segments that separate blocks reduce into the
+ *                    workspace, and a second kernel combines every row's partials in segment order.
+ *                    Without a workspace such reductions still run, unsplit, on as many blocks as there
+ *                    are rows. A non-NULL workspace smaller than needed is HLO_ERR_WORKSPACE; one that
+ *                    overlaps the input or output is HLO_ERR_INVALID_ARG. Its contents on entry do not
+ *                    matter, and calls that share one workspace must not overlap in time.
  *
  * A reduced dimension of size 0 yields init_value. Reductions whose reduced dimensions are the
  * minor-most physical dimensions run as row reductions, those with kept dimensions on both sides
@@ -176,8 +184,9 @@ hlo_status hlo_reduce_fusion(const hlo_array* in, const void* in_ptr, const hlo_
                              double init_value, int32_t accum_dtype, const hlo_array* out,
                              void* out_ptr, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Device scratch bytes hlo_reduce_fusion needs for this input and reduction (0 for every plan this
- * library currently selects). Returns 0 for invalid arguments as well. */
+/* Device scratch bytes hlo_reduce_fusion can use for this input and reduction on the current device:
+ * 4 bytes per (row, segment) partial when the rows are split (see workspace above), else 0. Returns 0
+ * for invalid arguments as well. */
 size_t hlo_reduce_workspace_size(const hlo_array* in, const int64_t* dimensions, int32_t n_dimensions,
                                  int32_t accum_dtype);
 

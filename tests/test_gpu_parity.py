@@ -135,6 +135,50 @@ def test_row_reduce_shapes(rows, cols, dtype):
         check(f, run_gpu(f), ref, asum)
 
 
+@pytest.mark.parametrize("rows,cols,dtype", [(1, 1 << 22, "f32"), (3, 1000003, "f32"), (10, 1 << 20, "bf16"),
+                                             (1, 65536 * 3 + 5, "bf16"), (150, 40000, "f32")])
+def test_split_row_reduce(rows, cols, dtype):
+    """Few long rows: the rows are cut into segments reduced by separate blocks into the workspace,
+    then combined per row in segment order (with and without a prologue, add and max); the same results
+    without a workspace (unsplit)."""
+    g = inp.rng(rows + cols)
+    n = rows * cols
+    data = inp.uniform_f32(g, n, -1, 1) if dtype == "f32" else inp.normal_bf16(g, n)
+    assert hf.reduce_workspace_size([rows, cols], dtype, [1]) > 0
+    for kind, init, ops in (("add", 0.0, ["exp"]), ("max", -math.inf, None), ("add", 2.5, None),
+                            ("max", -math.inf, ["neg", "exp"])):
+        f = inp.Fusion(name="split", kind="reduce", dims=[rows, cols], m2m=[1, 0], dtype=dtype, data=data,
+                       dimensions=[1], reduce_kind=kind, init=init,
+                       prologue={"ops": ops, "round_each": True} if ops else None,
+                       out_dims=[rows], out_m2m=[0], out_dtype="f32")
+        ref, asum = run_oracle(f)
+        d = DeviceFusion(f)
+        assert d.workspace is not None
+        d.run()
+        torch.cuda.synchronize()
+        check(f, d.output_numpy(), ref, asum)
+        d.workspace = None  # unsplit
+        d.run()
+        torch.cuda.synchronize()
+        check(f, d.output_numpy(), ref, asum)
+
+
+def test_split_row_reduce_with_broadcast_and_layout():
+    """A split reduce of add(exp(x), broadcast(b)) over the minor dims of a {0,1,2} layout array."""
+    g = inp.rng(71)
+    d0, d1 = 2, 300001
+    x = inp.normal_bf16(g, d0 * d1)
+    b = inp.uniform_bf16(g, d1, -1, 1)
+    f = inp.Fusion(name="splitb", kind="reduce", dims=[d1, 1, d0], m2m=[0, 1, 2], dtype="bf16", data=x,
+                   dimensions=[0, 1], reduce_kind="add", init=0.0,
+                   prologue={"ops": ["exp", "add_bcast"], "round_each": True,
+                             "bcast": {"data": b, "dims": [d1], "m2m": [0], "dtype": "bf16",
+                                       "broadcast_dimensions": [0]}},
+                   out_dims=[d0], out_m2m=[0], out_dtype="f32")
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+
+
 @pytest.mark.parametrize("a,r,b", [(1, 1, 1), (1, 9, 5), (3, 33, 264), (2, 1000, 7), (1, 4097, 2048)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_col_reduce_shapes(a, r, b, dtype):

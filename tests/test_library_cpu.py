@@ -317,3 +317,16 @@ def test_quantized_data_movement_validation(lib):
     pt = {"host_scales": np.float32([0.1]), "host_zero_points": np.int32([0]), "quantization_dimension": None}
     st, msg = _status(lambda: hf.reshape(FAKE_IN, [4, 3, 2], FAKE_OUT, [24], "s8", q=pt, result_qdim=0, stream=0))
     assert st == 1 and "C1" in msg
+
+
+def test_reduce_workspace_rules(lib):
+    """Few long rows ask for a workspace (one f32 partial per row segment); a non-NULL workspace that is
+    too small is HLO_ERR_WORKSPACE; many rows, or a column reduce, need none."""
+    need = hf.reduce_workspace_size([1, 1 << 24], "f32", [1])
+    assert need > 0 and need % 4 == 0
+    assert hf.reduce_workspace_size([4096, 4096], "f32", [1]) == 0
+    assert hf.reduce_workspace_size([1 << 20, 8], "f32", [0]) == 0
+    big_in, big_out, ws = 1 << 32, 1 << 34, 1 << 36  # never dereferenced, and far apart
+    st, msg = _status(lambda: hf.reduce_fusion(big_in, [1, 1 << 24], "f32", [1], "add", 0.0, big_out, "f32",
+                                               workspace=ws, workspace_bytes=4, stream=0))
+    assert st == 4 and "workspace" in msg

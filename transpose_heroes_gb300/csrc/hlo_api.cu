@@ -183,6 +183,27 @@ IndexMap make_map(const std::vector<int64_t>& size, const std::vector<int64_t>& 
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Rows and row length of a reduce whose reduced dimensions are the minor-most physical ones (unit
+// dimensions dropped); false for any other pattern.
+bool row_geometry(const hlo_array& in, const bool* red, int64_t* rows, int64_t* len) {
+  int64_t r = 1, l = 1;
+  bool in_reduced_tail = true;  // walking from the minor end
+  for (int k = 0; k < in.rank; ++k) {
+    const int d = (int)in.minor_to_major[k];
+    if (in.dims[d] == 1) continue;
+    if (red[d]) {
+      if (!in_reduced_tail) return false;
+      l *= in.dims[d];
+    } else {
+      in_reduced_tail = false;
+      r *= in.dims[d];
+    }
+  }
+  *rows = r;
+  *len = l;
+  return true;
+}
+
 // ---- quantization parameters ---------------------------------------------------------------------
 hlo_status check_quant(const hlo_quant* q, const hlo_array& a, const char* what, QuantParams* out) {
   std::memset(out, 0, sizeof *out);
@@ -706,19 +727,23 @@ const char* hlo_version(void) { return "hlofusion 0.1 (sm_103a)"; }
 
 size_t hlo_reduce_workspace_size(const hlo_array* in, const int64_t* dimensions, int32_t n_dimensions,
                                  int32_t accum_dtype) {
-  (void)in;
-  (void)dimensions;
-  (void)n_dimensions;
-  (void)accum_dtype;
-  return 0;
+  if (accum_dtype != HLO_F32 || check_array(in, "reduce input") != HLO_OK || !is_float(in->dtype)) return 0;
+  if (n_dimensions < 0 || n_dimensions > in->rank || (n_dimensions > 0 && !dimensions)) return 0;
+  bool red[HLO_MAX_RANK] = {false};
+  for (int i = 0; i < n_dimensions; ++i) {
+    const int64_t d = dimensions[i];
+    if (d < 0 || d >= in->rank || red[d]) return 0;
+    red[d] = true;
+  }
+  int64_t rows, len;
+  if (numel(*in) == 0 || !row_geometry(*in, red, &rows, &len)) return 0;
+  return (size_t)row_split_workspace(rows, row_split_factor(rows, len, dt_bytes(in->dtype)));
 }
 
 hlo_status hlo_reduce_fusion(const hlo_array* in, const void* in_ptr, const hlo_ew_chain* prologue,
                              const int64_t* dimensions, int32_t n_dimensions, int32_t kind, double init_value,
                              int32_t accum_dtype, const hlo_array* out, void* out_ptr, void* workspace,
                              size_t workspace_bytes, void* stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   hlo_status st = check_array(in, "reduce input");
   if (st != HLO_OK) return st;
   st = check_array(out, "reduce output");
@@ -821,6 +846,28 @@ hlo_status hlo_reduce_fusion(const hlo_array* in, const void* in_ptr, const hlo_
     p.chain = chain;
     p.omap = kept_map(ostr_in);
     p.bmode = BC_NONE;
+    p.split = 1;
+    p.seg = p.len;
+    // few long rows: split them into segments reduced by separate blocks (partials in the workspace)
+    const int64_t split = row_split_factor(p.rows, p.len, dt_bytes(in->dtype));
+    if (split > 1) {
+      int64_t seg = (p.len + split - 1) / split;
+      seg = (seg + 511) / 512 * 512;  // whole 16-byte vectors in every segment
+      const int64_t nsplit = (p.len + seg - 1) / seg;
+      const int64_t need = row_split_workspace(p.rows, nsplit);
+      if (workspace && (int64_t)workspace_bytes < need)
+        return fail(HLO_ERR_WORKSPACE, "reduce: workspace of %zu bytes, %lld needed (hlo_reduce_workspace_size)",
+                    workspace_bytes, (long long)need);
+      if (workspace && nsplit > 1) {
+        if ((uintptr_t)workspace % 4 != 0) return fail(HLO_ERR_INVALID_ARG, "reduce: workspace is not 4-byte aligned");
+        if (ranges_overlap(workspace, need, in_ptr, n_in * dt_bytes(in->dtype)) ||
+            ranges_overlap(workspace, need, out_ptr, n_out * dt_bytes(out->dtype)))
+          return fail(HLO_ERR_INVALID_ARG, "reduce: workspace overlaps the input or the output");
+        p.split = nsplit;
+        p.seg = seg;
+        p.ws = static_cast<float*>(workspace);
+      }
+    }
     bool ok_plan = true;
     if (has_bcast) {
       bool kept_zero = true, red_match = true, red_zero = true;

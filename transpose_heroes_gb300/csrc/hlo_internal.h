@@ -72,7 +72,19 @@ struct RowReducePlan {
   int bmode;        // BcastMode
   IndexMap bmap;    // BC_PERROW: row -> broadcast offset
   IndexMap omap;    // row -> output offset
+  // split rows: with split > 1 every row is cut into `split` segments of `seg` elements (the last one
+  // shorter); the blocks reduce segments into ws[row * split + segment], and a second kernel combines
+  // each row's partials in segment order
+  int64_t split;
+  int64_t seg;
+  float* ws;
 };
+
+// Segments per row for a row reduce of `rows` rows of `len` elements of `eb` bytes on this device:
+// 1 (no split) unless the rows are too few to occupy the device and long enough to share out.
+int64_t row_split_factor(int64_t rows, int64_t len, int eb);
+// Workspace bytes a split row reduce needs (0 without a split).
+inline int64_t row_split_workspace(int64_t rows, int64_t split) { return split > 1 ? rows * split * 4 : 0; }
 
 struct ColReducePlan {
   const void* in;

@@ -129,16 +129,20 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_kernel(RowReducePlan p
     lt = {s_lc, s_le};
   }
   const int eb = IN_DT == F32 ? 4 : 2;
-  const int64_t len = p.len;
   const int tid = threadIdx.x, nt = blockDim.x;
-  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-    const char* base = reinterpret_cast<const char*>(p.in) + row * len * eb;
+  const int64_t n_items = p.rows * p.split;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    // item = (row, segment): elements [e0, e0 + len) of the row; e0 is a multiple of VEC
+    const int64_t row = item / p.split, sg = item - row * p.split;
+    const int64_t e0 = sg * p.seg;
+    const int64_t len = min(p.seg, p.len - e0);
+    const char* base = reinterpret_cast<const char*>(p.in) + (row * p.len + e0) * eb;
     float acc = identity<KIND>();
     int64_t tail_start = 0;
     if (VEC > 1) {
       const int64_t nvec = len / VEC;
       const uint4* xv = reinterpret_cast<const uint4*>(base);
-      const uint4* bv = reinterpret_cast<const uint4*>(p.chain.bptr);
+      const uint4* bv = reinterpret_cast<const uint4*>(p.chain.bptr) + (CH == RC_EXP_BCAST_BF16 ? e0 / VEC : 0);
       int64_t v = tid;
       for (; v + (kRowUnroll - 1) * (int64_t)nt < nvec; v += kRowUnroll * (int64_t)nt) {
         uint4 x[kRowUnroll], b[kRowUnroll];
@@ -175,15 +179,31 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_kernel(RowReducePlan p
         }
       } else if (CH == RC_EXP_BCAST_BF16) {
         t = KIND == RED_ADD ? round_to_dt(fast_exp(t), BF16) : chain_exp(t, true, BF16);
-        t = round_to_dt(__fadd_rn(t, load_as_f32(p.chain.bptr, BF16, e)), BF16);
+        t = round_to_dt(__fadd_rn(t, load_as_f32(p.chain.bptr, BF16, e0 + e)), BF16);
       } else if (CH == RC_RT) {
-        int64_t boff = p.bmode == BC_ROWVEC ? e : p.bmode == BC_PERROW ? map_index(p.bmap, row) : 0;
+        int64_t boff = p.bmode == BC_ROWVEC ? e0 + e : p.bmode == BC_PERROW ? map_index(p.bmap, row) : 0;
         t = apply_chain_rt(p.chain, t, boff, lt);
       }
       acc = combine<KIND>(acc, t);
     }
     acc = block_reduce<KIND>(acc, red);
-    if (tid == 0) store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+    if (tid == 0) {
+      if (p.split > 1) p.ws[item] = acc;  // the segment's partial, combined by row_split_combine_kernel
+      else store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+    }
+  }
+}
+
+// Second pass of a split row reduce: one thread per row combines the row's segment partials in segment
+// order (deterministic), then applies init once.
+template <int KIND>
+__global__ void row_split_combine_kernel(RowReducePlan p) {
+  for (int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; row < p.rows;
+       row += (int64_t)gridDim.x * blockDim.x) {
+    const float* part = p.ws + row * p.split;
+    float acc = part[0];
+    for (int64_t sg = 1; sg < p.split; ++sg) acc = combine<KIND>(acc, part[sg]);
+    store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
   }
 }
 
@@ -442,18 +462,24 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_rt_kernel(RowReducePla
     __syncthreads();
     lt = {s_lc, s_le};
   }
-  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+  const int64_t n_items = p.rows * p.split;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int64_t row = item / p.split, sg = item - row * p.split;
+    const int64_t e0 = sg * p.seg, e1 = min(p.len, e0 + p.seg);
     const char* base = reinterpret_cast<const char*>(p.in) + row * p.len * dt_bytes(IN_DT);
     const int64_t rowb = p.bmode == BC_PERROW ? map_index(p.bmap, row) : 0;
     float acc = identity<KIND>();
-    for (int64_t e = threadIdx.x; e < p.len; e += blockDim.x) {
+    for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
       float t = load_as_f32(base, IN_DT, e);
       int64_t boff = p.bmode == BC_ROWVEC ? e : rowb;
       t = apply_chain_rt(p.chain, t, boff, lt);
       acc = combine<KIND>(acc, t);
     }
     acc = block_reduce<KIND>(acc, red);
-    if (threadIdx.x == 0) store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+    if (threadIdx.x == 0) {
+      if (p.split > 1) p.ws[item] = acc;
+      else store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+    }
   }
 }
 
@@ -462,13 +488,20 @@ static cudaError_t row_dispatch(const RowReducePlan& p, cudaStream_t s, int ch, 
   auto launch = [&](auto kernel) -> cudaError_t {
     const int nb = kernel_blocks_per_sm((const void*)kernel, kRowThreads, 0);
     int64_t grid = (int64_t)device_sm_count() * nb;
-    if (grid > p.rows) grid = p.rows;
+    const int64_t items = p.rows * p.split;
+    if (grid > items) grid = items;
     if (grid < 1) grid = 1;
     int threads = kRowThreads;
-    // short rows: fewer threads so that lanes are not idle
-    int64_t work = vec ? (p.len / (IN_DT == F32 ? 4 : 8)) : p.len;
+    // short rows (segments): fewer threads so that lanes are not idle
+    const int64_t seg_len = p.split > 1 ? p.seg : p.len;
+    int64_t work = vec ? (seg_len / (IN_DT == F32 ? 4 : 8)) : seg_len;
     while (threads > 64 && work <= threads / 2) threads >>= 1;
     kernel<<<(unsigned)grid, threads, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || p.split <= 1) return e;
+    int64_t cb = (p.rows + 255) / 256;
+    if (cb > 1024) cb = 1024;
+    row_split_combine_kernel<KIND><<<(unsigned)cb, 256, 0, s>>>(p);
     return cudaGetLastError();
   };
   constexpr int V = IN_DT == F32 ? 4 : 8;
@@ -501,6 +534,18 @@ static int classify_row_chain(const RowReducePlan& p) {
   return RC_RT;
 }
 
+int64_t row_split_factor(int64_t rows, int64_t len, int eb) {
+  // 512-thread blocks, four per SM: split while the rows fill less than half of those slots, into
+  // segments of at least 32 KiB
+  const int64_t slots = (int64_t)device_sm_count() * 4;
+  if (rows <= 0 || rows * 2 > slots) return 1;
+  const int64_t min_seg = 32768 / eb;
+  int64_t split = (slots + rows - 1) / rows;
+  const int64_t by_len = len / min_seg;
+  if (split > by_len) split = by_len;
+  return split > 1 ? split : 1;
+}
+
 cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s) {
   const int eb = dt_bytes(p.in_dt);
   const int ch = classify_row_chain(p);
@@ -509,7 +554,7 @@ cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s) {
   if (ch == RC_EXP_BCAST_BF16) vec = vec && ((uintptr_t)p.chain.bptr % 16 == 0);
   if (ch == RC_RT) vec = false;
   // long rows on the vector path stream through the bulk-copy ring
-  const bool stream = vec && ch != RC_RT && p.len * eb >= 8192 && p.rows >= 64;
+  const bool stream = vec && ch != RC_RT && p.len * eb >= 8192 && p.rows >= 64 && p.split <= 1;
   if (stream) {
     if (p.in_dt == F32)
       return p.kind == RED_ADD ? stream_dispatch<F32, RED_ADD>(p, s, ch) : stream_dispatch<F32, RED_MAX>(p, s, ch);

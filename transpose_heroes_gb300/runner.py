@@ -10,7 +10,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import layout_convert, quant_binary, quant_fusion, reduce_fusion, reduce_max_argmax, transpose_fusion
+from . import (layout_convert, quant_binary, quant_fusion, reduce_fusion, reduce_max_argmax, reduce_workspace_size,
+               transpose_fusion)
 from .inputs import ELEM_BYTES, Fusion
 
 # physical buffers as torch tensors of the same element size (16-bit floats carried as int16 bits)
@@ -52,6 +53,12 @@ class DeviceFusion:
         self.out = torch.empty(n_out, dtype=_TORCH[f.out_dtype], device=device)
         self.host_out = torch.empty(n_out, dtype=_TORCH[f.out_dtype], pin_memory=pin_host)
         self.out_idx = torch.empty(n_out, dtype=torch.int32, device=device) if f.kind == "argmax" else None
+        # the reduce's scratch (row partials when few long rows are split), allocated once
+        self.workspace = None
+        if f.kind == "reduce":
+            nbytes = reduce_workspace_size(f.dims, f.dtype, f.dimensions, in_m2m=f.m2m)
+            if nbytes:
+                self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
         self.rhs = None
         if f.kind == "quant_binary":
             self.rhs = host_tensor(f.rhs, f.dtype).to(device)
@@ -79,8 +86,10 @@ class DeviceFusion:
     def run(self, stream=None):
         f = self.f
         if f.kind == "reduce":
+            ws = self.workspace
             reduce_fusion(self.x, f.dims, f.dtype, f.dimensions, f.reduce_kind, f.init, self.out, f.out_dtype,
-                          in_m2m=f.m2m, out_m2m=f.out_m2m, prologue=self._chain(f.prologue), stream=stream)
+                          in_m2m=f.m2m, out_m2m=f.out_m2m, prologue=self._chain(f.prologue), workspace=ws,
+                          workspace_bytes=0 if ws is None else ws.numel(), stream=stream)
         elif f.kind == "transpose":
             transpose_fusion(self.x, f.dims, f.dtype, f.permutation, self.out, in_m2m=f.m2m, out_m2m=f.out_m2m,
                              prologue=self._chain(f.prologue), self_add=f.self_add,
