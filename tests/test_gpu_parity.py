@@ -426,6 +426,31 @@ def test_transpose_emitter_example_exp_abs():
     check(f, run_gpu(f), ref, None)
 
 
+@pytest.mark.parametrize("dims,perm", [([36, 20, 68], [2, 1, 0]), ([132, 72], [1, 0]), ([4, 12, 8, 132], [3, 0, 2, 1]),
+                                       ([8, 4, 12, 4, 68], [4, 2, 0, 3, 1]), ([200, 3, 76], [2, 0, 1])])
+def test_transpose_tensor_copy_tiles(dims, perm):
+    """Shapes whose strides allow the tensor-copy tile kernel (4-byte elements, strides multiples of four):
+    ragged 64 x 64 tiles and one to three batch axes; f32 with prologue / epilogue chains and s32 without,
+    bit-exact against the oracle."""
+    g = inp.rng(sum(dims))
+    n = int(np.prod(dims))
+    out_dims = [dims[q] for q in perm]
+    m2m, out_m2m = list(range(len(dims) - 1, -1, -1)), list(range(len(dims) - 1, -1, -1))
+    x = inp.uniform_f32(g, n, -3, 3)
+    for pro, epi in ((["exp"], ["abs"]), (None, None), (["neg", ("mul_const", 0.37), "tanh"], [("add_const", 1.5)])):
+        f = inp.Fusion(name="tt", kind="transpose", dims=dims, m2m=m2m, dtype="f32", data=x, permutation=perm,
+                       prologue={"ops": pro, "round_each": True} if pro else None,
+                       epilogue={"ops": epi, "round_each": True} if epi else None,
+                       out_dims=out_dims, out_m2m=out_m2m, out_dtype="f32")
+        ref, asum = run_oracle(f)
+        check(f, run_gpu(f), ref, asum)
+    xi = g.integers(-2 ** 31, 2 ** 31 - 1, size=n, dtype=np.int64).astype(np.int32)
+    f = inp.Fusion(name="tti", kind="transpose", dims=dims, m2m=m2m, dtype="s32", data=xi, permutation=perm,
+                   out_dims=out_dims, out_m2m=out_m2m, out_dtype="s32")
+    ref, asum = run_oracle(f)
+    check(f, run_gpu(f), ref, asum)
+
+
 def test_transpose3_exp_abs_full_size():
     """The transpose-emitter fusion scaled up (f32[512,640,680] -> [680,640,512]) as the benchmark runs
     it, on every output."""

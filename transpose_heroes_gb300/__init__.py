@@ -32,7 +32,8 @@ STATUS_INVALID_ARG = 1
 STATUS = {0: "HLO_OK", 1: "HLO_ERR_INVALID_ARG", 2: "HLO_ERR_UNSUPPORTED", 3: "HLO_ERR_CUDA", 4: "HLO_ERR_WORKSPACE"}
 
 # Every function the header declares; the library must export all of them.
-EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_workspace_size", "hlo_transpose_fusion", "hlo_layout_convert",
+EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_workspace_size", "hlo_transpose_fusion",
+           "hlo_layout_convert",
            "hlo_quant_fusion", "hlo_quant_binary", "hlo_quant_broadcast_in_dim", "hlo_quant_reshape",
            "hlo_reduce_max_argmax", "hlo_device_faults",
            "hlo_selftest_bounded_wait", "hlo_last_error", "hlo_version")

@@ -273,6 +273,54 @@ __device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* 
   ok1 = n1 & (YP.y == YM.y);
 }
 
+// The same first pass for four values, with the tables' addresses known at compile time (static shared
+// memory: `tab` holds the 32 inv_c, then the 32 log(c)_hi, then the 32 log(c)_lo) and the test for
+// positive normal operands made once for all four: the table offset is read straight from the bits,
+// (t >> (HLO_LOG1_SHIFT - 2)) & (31 << 2), and a block with any special operand leaves all four open.
+// Returns the four candidates in y and the settled ones as bits 0..3 of the result.
+__device__ __forceinline__ uint32_t cr_logf_first4(const float4 x, const float (&tab)[96], float4& y) {
+  const uint32_t ix[4] = {__float_as_uint(x.x), __float_as_uint(x.y), __float_as_uint(x.z), __float_as_uint(x.w)};
+  const int mn = min(min((int)ix[0], (int)ix[1]), min((int)ix[2], (int)ix[3]));
+  const int mx = max(max((int)ix[0], (int)ix[1]), max((int)ix[2], (int)ix[3]));
+  const bool normal = (mn >= 0x00800000) & (mx < 0x7F800000);
+  float ym[4], yp[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t t0 = ix[2 * h] - HLO_LOG1_OFF, t1 = ix[2 * h + 1] - HLO_LOG1_OFF;
+    const uint32_t b0 = (t0 >> (HLO_LOG1_SHIFT - 2)) & (31u << 2), b1 = (t1 >> (HLO_LOG1_SHIFT - 2)) & (31u << 2);
+    const char* tb = reinterpret_cast<const char*>(tab);
+    const float m0 = __uint_as_float(ix[2 * h] - (t0 & 0xFF800000u)), m1 = __uint_as_float(ix[2 * h + 1] - (t1 & 0xFF800000u));
+    const float eb0 = __int_as_float(0x4B400000 + ((int)t0 >> 23));
+    const float eb1 = __int_as_float(0x4B400000 + ((int)t1 >> 23));
+    const float2 EF = f2::add(f2::pk(eb0, eb1), f2::splat(-12582912.0f));
+    const float2 INV = f2::pk(*reinterpret_cast<const float*>(tb + b0), *reinterpret_cast<const float*>(tb + b1));
+    const float2 HI = f2::pk(*reinterpret_cast<const float*>(tb + 128 + b0), *reinterpret_cast<const float*>(tb + 128 + b1));
+    const float2 LOT = f2::pk(*reinterpret_cast<const float*>(tb + 256 + b0), *reinterpret_cast<const float*>(tb + 256 + b1));
+    const float2 R = f2::fma(f2::pk(m0, m1), INV, f2::splat(-1.0f));  // exact
+    const float2 A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), HI);       // exact
+    const float2 S = f2::add(A, R);                                     // Fast2Sum: A = 0 or |A| >= |r|
+    const float2 ERR = f2::sub(R, f2::sub(S, A));
+    float2 P = f2::fma(R, f2::splat(-0.16666667f), f2::splat(0.2f));
+    P = f2::fma(R, P, f2::splat(-0.25f));
+    P = f2::fma(R, P, f2::splat(0.33333334f));
+    P = f2::fma(R, P, f2::splat(-0.5f));
+    const float2 B = f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), LOT);
+    const float2 REST = f2::fma(f2::mul(R, R), P, B);
+    const float2 LO = f2::add(ERR, REST);
+    const float bound = 0x1.6a09e6p-34f;  // 2^-33.5, as in cr_logf_first2
+    const float2 YP = f2::add(S, f2::add(LO, f2::splat(bound)));
+    const float2 YM = f2::add(S, f2::sub(LO, f2::splat(bound)));
+    yp[2 * h] = YP.x;
+    yp[2 * h + 1] = YP.y;
+    ym[2 * h] = YM.x;
+    ym[2 * h + 1] = YM.y;
+  }
+  y = make_float4(yp[0], yp[1], yp[2], yp[3]);
+  if (!normal) return 0u;
+  return (yp[0] == ym[0] ? 1u : 0u) | (yp[1] == ym[1] ? 2u : 0u) | (yp[2] == ym[2] ? 4u : 0u) |
+         (yp[3] == ym[3] ? 8u : 0u);
+}
+
 // Loads the 32-entry first-pass table into shared memory (three arrays of 32 floats).
 __device__ __forceinline__ void load_log1_tables(float* s_inv, float* s_hi, float* s_lo) {
   for (int i = threadIdx.x; i < 32; i += blockDim.x) {

@@ -185,6 +185,12 @@ __device__ __forceinline__ float apply_chain_rt(const Chain& c, float v, int64_t
   return v;
 }
 
+__host__ __device__ inline bool chain_has_bcast_dev(const Chain& c) {
+  for (int k = 0; k < c.n; ++k)
+    if (c.op[k] == OP_ADD_BCAST) return true;
+  return false;
+}
+
 __device__ __forceinline__ bool chain_has_log(const Chain& c) {
   for (int k = 0; k < c.n; ++k)
     if (c.op[k] == OP_LOG) return true;

@@ -237,6 +237,12 @@ hlo_status check_quant(const hlo_quant* q, const hlo_array& a, const char* what,
   out->axis = qd;
   out->smin = q->storage_min;
   out->smax = q->storage_max;
+  out->max_abs_scale = -1.0f;
+  if (q->host_scales) {
+    float m = 0.0f;
+    for (int64_t i = 0; i < q->n; ++i) m = std::max(m, std::fabs(q->host_scales[i]));
+    out->max_abs_scale = m;
+  }
   if (qd < 0) {
     if (!q->host_scales || !q->host_zero_points)
       return fail(HLO_ERR_INVALID_ARG, "%s: per-tensor parameters need host_scales and host_zero_points", what);

@@ -154,6 +154,7 @@ struct QuantParams {
   int32_t zp;               // per-tensor
   float inv_scale;          // per-tensor: RN(1 / scale), used by the division shortcut
   int32_t smin, smax;
+  float max_abs_scale;      // largest |scale| when the host copy was given, else -1 (unknown)
 };
 
 struct QuantTilePlan {

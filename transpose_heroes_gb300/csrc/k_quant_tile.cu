@@ -455,22 +455,32 @@ __global__ void __launch_bounds__(256, 4)
       const int r = lane + 32 * k;
       v[k] = *reinterpret_cast<const uint4*>(rt + r * kQT + 16 * (w ^ (r & 7)));
     }
-    // parameters: per row (QIN 0), per column (QIN 1, the same for the whole warp) or per tensor
+    // parameters: per row (QIN 0), per column (QIN 1, the same for the whole warp) or per tensor. With
+    // the zero point z, -(1.5*2^23 + 128 + z) has the bits of 1.5*2^23 plus 128 + z (in [0, 255]) and the
+    // sign bit: df = e + that = code - z exactly.
     float rs[4], rz[4];
-    bool bad = !(fabsf(io) < 0x1p60f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float sc = QIN == 0 ? ps[lane + 32 * k] : p.qin.scale;
       const int zz = QIN == 0 ? pz[lane + 32 * k] : p.qin.zp;
-      rs[k] = sc;
-      rz[k] = -(kMagic + 128.0f + (float)zz);
-      if (QIN != 1) bad |= !(fabsf(sc) < 0x1p60f && fabsf(sc) * fabsf(io) < 8192.0f);
+      rs[k] = QIN == 0 ? ps[lane + 32 * k] : p.qin.scale;
+      rz[k] = __int_as_float((kMagicBits + 128 + zz) | (int)0x80000000u);
     }
-    if (QIN == 1) {
+    // the bracket needs finite parameters with |scale_in / scale_out| < 2^13: known from the host copies
+    // when they were given, else checked on this thread's parameters
+    bool bad;
+    if (p.qin.max_abs_scale >= 0.0f) {
+      bad = !(fabsf(io) < 0x1p60f && p.qin.max_abs_scale < 0x1p60f && p.qin.max_abs_scale * fabsf(io) < 8192.0f);
+    } else {
+      bad = !(fabsf(io) < 0x1p60f);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float sc = ps[16 * w + c];
-        bad |= !(fabsf(sc) < 0x1p60f && fabsf(sc) * fabsf(io) < 8192.0f);
+      for (int k = 0; k < 4; ++k)
+        if (QIN != 1) bad |= !(fabsf(rs[k]) < 0x1p60f && fabsf(rs[k]) * fabsf(io) < 8192.0f);
+      if (QIN == 1) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float sc = ps[16 * w + c];
+          bad |= !(fabsf(sc) < 0x1p60f && fabsf(sc) * fabsf(io) < 8192.0f);
+        }
       }
     }
     uint32_t o[4][4];
@@ -486,7 +496,8 @@ __global__ void __launch_bounds__(256, 4)
             const int jl = 16 * w + 4 * m + b;
             cs = *reinterpret_cast<const float2*>(&ps[jl]);
             const int2 zz = *reinterpret_cast<const int2*>(&pz[jl]);
-            cz = make_float2(-(kMagic + 128.0f + (float)zz.x), -(kMagic + 128.0f + (float)zz.y));
+            cz = make_float2(__int_as_float((kMagicBits + 128 + zz.x) | (int)0x80000000u),
+                             __int_as_float((kMagicBits + 128 + zz.y) | (int)0x80000000u));
           }
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -627,10 +638,10 @@ static cudaError_t quant_tma_launch(const QuantTilePlan& p, const CUtensorMap& m
   const void* kernel = clamp ? (const void*)quant_tma_kernel<QIN, true> : (const void*)quant_tma_kernel<QIN, false>;
   const size_t smem = quant_tma_smem_bytes();
   const int nb = kernel_blocks_per_sm(kernel, 256, smem);
-  // every block takes kQStages tiles up front when the grid allows it, so all loads start at once
-  int64_t grid = (n_tiles + kQStages - 1) / kQStages;
-  const int64_t slots = (int64_t)device_sm_count() * nb;
-  if (grid > slots) grid = slots;
+  // one wave of every resident block: tiles dealt round-robin, the first kQStages of each block's
+  // requested at once
+  int64_t grid = (int64_t)device_sm_count() * nb;
+  if (grid > n_tiles) grid = n_tiles;
   if (grid < 1) grid = 1;
   if (clamp) quant_tma_kernel<QIN, true><<<(unsigned)grid, 256, smem, s>>>(map, p, ntj, n_tiles);
   else quant_tma_kernel<QIN, false><<<(unsigned)grid, 256, smem, s>>>(map, p, ntj, n_tiles);

@@ -483,6 +483,39 @@ __global__ void __launch_bounds__(kRowThreads) row_reduce_rt_kernel(RowReducePla
   }
 }
 
+// Short rows (at most 512 16-byte vectors): one warp per row, eight rows per block. Every lane requests
+// its vectors before using any, and the warp combines with shuffles only: no block barrier, no shared
+// memory, one wave for a few hundred rows.
+constexpr int kWarpRowMaxVec = 512;
+template <int IN_DT, int CH, int KIND>
+__global__ void __launch_bounds__(256) row_warp_kernel(RowReducePlan p) {
+  constexpr int V = IN_DT == F32 ? 4 : 8;
+  constexpr int kU = 4;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= p.rows) return;
+  const int64_t nvec = p.len / V;  // the row is whole 16-byte vectors
+  const uint4* xv = reinterpret_cast<const uint4*>(p.in) + row * nvec;
+  const LogTab lt = global_log_tables();
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  float acc = identity<KIND>();
+  int64_t v = lane;
+  for (; v + 32 * (kU - 1) < nvec; v += 32 * kU) {
+    uint4 x[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(x[u].x), "=r"(x[u].y), "=r"(x[u].z), "=r"(x[u].w)
+                   : "l"(xv + v + 32 * u));
+#pragma unroll
+    for (int u = 0; u < kU; ++u) acc = row_vec<IN_DT, CH, KIND>(x[u], zero, acc, p.chain, lt);
+  }
+  for (; v < nvec; v += 32) acc = row_vec<IN_DT, CH, KIND>(__ldg(xv + v), zero, acc, p.chain, lt);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc = combine<KIND>(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+  if (lane == 0) store_result(p.out, p.out_dt, map_index(p.omap, row), combine<KIND>(p.init, acc));
+}
+
 template <int IN_DT, int KIND>
 static cudaError_t row_dispatch(const RowReducePlan& p, cudaStream_t s, int ch, bool vec) {
   auto launch = [&](auto kernel) -> cudaError_t {
@@ -506,6 +539,14 @@ static cudaError_t row_dispatch(const RowReducePlan& p, cudaStream_t s, int ch, 
   };
   constexpr int V = IN_DT == F32 ? 4 : 8;
   if (ch == RC_RT && p.bmode == BC_PERROW) return launch(row_reduce_rt_kernel<IN_DT, KIND>);
+  if (vec && p.split <= 1 && (ch == RC_NONE || ch == RC_EXP) && p.len / V <= kWarpRowMaxVec) {
+    const int64_t blocks = (p.rows + 7) / 8;
+    if (blocks <= 0x7FFFFFFF) {
+      if (ch == RC_NONE) row_warp_kernel<IN_DT, RC_NONE, KIND><<<(unsigned)blocks, 256, 0, s>>>(p);
+      else row_warp_kernel<IN_DT, RC_EXP, KIND><<<(unsigned)blocks, 256, 0, s>>>(p);
+      return cudaGetLastError();
+    }
+  }
   if (vec) {
     switch (ch) {
       case RC_NONE: return launch(row_reduce_kernel<IN_DT, V, RC_NONE, KIND>);

@@ -346,7 +346,6 @@ __device__ __forceinline__ void block_store(float* dst, int64_t n, const float4 
 constexpr int kPairWarps = kPairThreads / 32;
 template <int NS>
 struct TmaShared {
-  float l1_inv[32], l1_hi[32], l1_lo[32];
   uint16_t wlist[kPairWarps][kWarpList];
   int wcount[kPairWarps];  // fill of each warp's settle list
   int done[NS];            // warps done with the stage's current item
@@ -361,16 +360,25 @@ static size_t tma_smem_bytes() {
 }
 
 // Prologue of one raw tile of the stage, written back in place (swizzled); open log elements keep
-// their input and set their bits in `open` (from bit `shift`).
+// their input and set their bits in `open` (from bit `shift`). `l1` is the first-pass log table in
+// static shared memory.
 template <int CH>
 __device__ __forceinline__ void tma_tile_prologue(float* tile, int raw, int own, const SelfAddPlan& p, const LogTab& lt,
-                                                  const float* tinv, const float* thi, const float* tlo, uint32_t& open,
-                                                  int shift) {
+                                                  const float (&l1)[96], uint32_t& open, int shift) {
   float4 v[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const float4*>(tile + raw + k * kT);
   if (CH == PC_LOG) {
-    block_log(v, tinv, thi, tlo, open, shift);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float4 y;
+      const uint32_t ok = cr_logf_first4(v[k], l1, y);
+      v[k].x = (ok & 1u) ? y.x : v[k].x;  // an open element keeps its input in its slot
+      v[k].y = (ok & 2u) ? y.y : v[k].y;
+      v[k].z = (ok & 4u) ? y.z : v[k].z;
+      v[k].w = (ok & 8u) ? y.w : v[k].w;
+      open |= (~ok & 15u) << (4 * k + shift);
+    }
   } else if (CH == PC_RT) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -426,6 +434,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
   float4* s_lc = reinterpret_cast<float4*>(stage + NS * 2 * kT * kT);
   float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
   TmaShared<NS>& ts = *reinterpret_cast<TmaShared<NS>*>(s_le + HLO_LOG_NE);
+  __shared__ float l1[96];  // first-pass log table (inv_c, log(c)_hi, log(c)_lo), at a static address
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // copies item `it` (walk position j) into stage j % NS and records its tile pair there
   auto issue = [&](int64_t it, int64_t j) {
@@ -453,7 +462,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
     }
   }
   load_log_tables(s_lc, s_le);
-  load_log1_tables(ts.l1_inv, ts.l1_hi, ts.l1_lo);
+  load_log1_tables(l1, l1 + 32, l1 + 64);
   __syncthreads();
   const LogTab lt = {s_lc, s_le};
   float* out = reinterpret_cast<float*>(p.out);
@@ -474,8 +483,8 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
     float* ta = stage + st * 2 * kT * kT;
     float* tb = ta + kT * kT;
     uint32_t open = 0;
-    tma_tile_prologue<CH>(ta, raw, own, p, lt, ts.l1_inv, ts.l1_hi, ts.l1_lo, open, 0);
-    if (two) tma_tile_prologue<CH>(tb, raw, own, p, lt, ts.l1_inv, ts.l1_hi, ts.l1_lo, open, 16);
+    tma_tile_prologue<CH>(ta, raw, own, p, lt, l1, open, 0);
+    if (two) tma_tile_prologue<CH>(tb, raw, own, p, lt, l1, open, 16);
     if (CH == PC_LOG) warp_settle_list(open, ta, own, wl, &ts.wcount[warp], lt);
     // every tile of item j is complete
     if (__syncthreads_or(arrived ? 0 : 1)) {

@@ -1,6 +1,9 @@
 // Transpose / layout-change hero kernels ("XLA:GPU Emitters", section "Transpose emitter": coalesced
 // reads into a shared-memory tile, a barrier, coalesced writes out of it), and the element gathers.
 //
+//  tile_tma_kernel      -- the same for 4-byte elements when every stride allows 16-byte accesses:
+//                          64 x 64 tiles by 2-D..5-D tensor copies into a ring of shared-memory
+//                          stages, the prologue in place, 4 x 4 register transposes, 16-byte stores.
 //  tile_transpose_kernel -- any physical permutation whose input-minor and output-minor axes
 //                          differ: a 32 x 32 tile over those two axes, other axes batched.
 //  gather_kernel        -- everything else: one thread per output element (also the quantized
@@ -8,6 +11,7 @@
 //  reshape_kernel       -- reshape with layouts: lexicographic position -> physical offsets.
 #include <type_traits>
 
+#include "async_copy.cuh"
 #include "device_common.cuh"
 #include "quant_common.cuh"
 
@@ -71,6 +75,244 @@ __global__ void __launch_bounds__(256) tile_transpose_kernel(TilePlan p, int64_t
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Tensor-copy tile transpose (4-byte elements). Tile = 64 values of the input-minor axis a (one 256-byte
+// row) x 64 of the output-minor axis b, at fixed batch coordinates; the tensor map's box is one tile,
+// so a single copy fetches the 64 strided rows (elements outside the array read as 0 and are never
+// stored). Thread t owns the 4 x 4 block (bi, bj) = (t / 16, t % 16): it reads b-rows 4bi.. (a values
+// 4bj..) as 16-byte reads, applies the prologue, and after __syncwarp writes them back in place, 16-byte
+// chunk c of row r at chunk c ^ ((r / 4) % 8) (its chunk lies in its own rows, read only by its half
+// warp). After the block barrier it reads the block (bj, bi), transposes it in registers, applies the
+// epilogue and stores output rows a = 4bi.. at b = 4bj.. with 16-byte stores. The last warp done with
+// a stage refills it with the block's item j + NS (one barrier per item).
+// ---------------------------------------------------------------------------------------------
+constexpr int kTM = 64;
+constexpr int kTmaTileStages = 4;
+constexpr int kTileWarps = 8;
+
+struct TileItem {
+  int a0, b0;         // first a and b of the tile
+  long long obase;    // output offset of the tile's batch coordinates
+};
+
+struct TileTmaShared {
+  TileItem item[kTmaTileStages];
+  int done[kTmaTileStages];
+  uint64_t full[kTmaTileStages];
+};
+
+static size_t tile_tma_smem_bytes() {
+  return 128 + (size_t)kTmaTileStages * kTM * kTM * 4 + sizeof(TileTmaShared);
+}
+
+// exp / log / tanh of four values through one out-of-line call (chains interpreted at run time)
+static __device__ __noinline__ float4 chain_unary4(int op, float4 v, bool r16, int dt, const float4* lc,
+                                                   const float2* le) {
+  if (op == OP_EXP) return make_float4(chain_exp(v.x, r16, dt), chain_exp(v.y, r16, dt), chain_exp(v.z, r16, dt),
+                                       chain_exp(v.w, r16, dt));
+  if (op == OP_LOG)
+    return make_float4(chain_log(v.x, r16, dt, lc, le), chain_log(v.y, r16, dt, lc, le),
+                       chain_log(v.z, r16, dt, lc, le), chain_log(v.w, r16, dt, lc, le));
+  return make_float4(chain_tanh(v.x, r16, dt), chain_tanh(v.y, r16, dt), chain_tanh(v.z, r16, dt),
+                     chain_tanh(v.w, r16, dt));
+}
+
+// A chain (no broadcast operand) applied to four f32 values: one dispatch per op for all four.
+__device__ __forceinline__ float4 apply_chain4(const Chain& c, float4 v, const LogTab& lt) {
+  const float4 x = v;
+  for (int k = 0; k < c.n; ++k) {
+    const int op = c.op[k];
+    const float imm = c.imm[k];
+    switch (op) {
+      case OP_EXP:
+      case OP_LOG:
+      case OP_TANH: v = chain_unary4(op, v, false, F32, lt.c, lt.e); break;
+      case OP_ABS: v = make_float4(fabsf(v.x), fabsf(v.y), fabsf(v.z), fabsf(v.w)); break;
+      case OP_NEG: v = make_float4(-v.x, -v.y, -v.z, -v.w); break;
+      case OP_ADD_CONST:
+        v = make_float4(__fadd_rn(v.x, imm), __fadd_rn(v.y, imm), __fadd_rn(v.z, imm), __fadd_rn(v.w, imm));
+        break;
+      case OP_MUL_CONST:
+        v = make_float4(__fmul_rn(v.x, imm), __fmul_rn(v.y, imm), __fmul_rn(v.z, imm), __fmul_rn(v.w, imm));
+        break;
+      case OP_ADD_IN: v = make_float4(__fadd_rn(v.x, x.x), __fadd_rn(v.y, x.y), __fadd_rn(v.z, x.z), __fadd_rn(v.w, x.w)); break;
+      case OP_MUL_IN: v = make_float4(__fmul_rn(v.x, x.x), __fmul_rn(v.y, x.y), __fmul_rn(v.z, x.z), __fmul_rn(v.w, x.w)); break;
+      default: break;
+    }
+  }
+  return v;
+}
+
+__device__ __forceinline__ float comp4(const float4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+template <bool CHAINS>
+__global__ void __launch_bounds__(256, 3)
+    tile_tma_kernel(const __grid_constant__ CUtensorMap tmap, TilePlan p, int64_t nta, int64_t ntb, int64_t n_items) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  float* stage = reinterpret_cast<float*>(base);  // [stages][64 b-rows][64 a]
+  TileTmaShared& ts = *reinterpret_cast<TileTmaShared*>(stage + kTmaTileStages * kTM * kTM);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t na = p.size[p.ax_a], nb = p.size[p.ax_b];
+  // copies item `it` (walk position j) into stage j % stages; records where its output goes
+  auto issue = [&](int64_t it, int64_t j) {
+    const int st = (int)(j % kTmaTileStages);
+    int64_t rem = it;
+    const int64_t ta = rem % nta;
+    rem /= nta;
+    const int64_t tb = rem % ntb;
+    rem /= ntb;
+    int32_t c[5] = {(int32_t)(ta * kTM), (int32_t)(tb * kTM), 0, 0, 0};
+    int64_t obase = 0;
+    for (int q = p.nbatch_axes - 1; q >= 0; --q) {  // batch coordinates, minor batch axis fastest
+      const int ax = p.batch_axis[q];
+      const int64_t i = rem % p.size[ax];
+      rem /= p.size[ax];
+      c[2 + q] = (int32_t)i;
+      obase += i * p.out_stride[ax];
+    }
+    ts.item[st].a0 = c[0];
+    ts.item[st].b0 = c[1];
+    ts.item[st].obase = obase;
+    const uint32_t bar = smem_addr(&ts.full[st]);
+    mbar_arrive_expect_tx(bar, kTM * kTM * 4);
+    float* dst = stage + st * kTM * kTM;
+    const uint64_t map = reinterpret_cast<uint64_t>(&tmap);
+    switch (2 + p.nbatch_axes) {
+      case 2:
+        asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                     ::"r"(smem_addr(dst)), "l"(map), "r"(c[0]), "r"(c[1]), "r"(bar) : "memory");
+        break;
+      case 3:
+        asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+                     ::"r"(smem_addr(dst)), "l"(map), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(bar) : "memory");
+        break;
+      case 4:
+        asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                     ::"r"(smem_addr(dst)), "l"(map), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(bar) : "memory");
+        break;
+      default:
+        asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+                     ::"r"(smem_addr(dst)), "l"(map), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar) : "memory");
+        break;
+    }
+  };
+  if (tid == 0) {
+    prefetch_tensor_map(&tmap);
+    for (int st = 0; st < kTmaTileStages; ++st) {
+      mbar_init(smem_addr(&ts.full[st]), 1);
+      ts.done[st] = 0;
+    }
+    fence_mbar_init();
+    for (int64_t j = 0; j < kTmaTileStages; ++j) {
+      const int64_t it = blockIdx.x + j * gridDim.x;
+      if (it < n_items) issue(it, j);
+    }
+  }
+  __syncthreads();
+  const LogTab lt = global_log_tables();
+  float* out = reinterpret_cast<float*>(p.out);
+  const int64_t soa = p.out_stride[p.ax_a];
+  const int bi = tid >> 4, bj = tid & 15;
+  const int own = 4 * bi * kTM + ((bj ^ (bi & 7)) << 2);  // b-row 4*bi, chunk bj (swizzled)
+  const int oth = 4 * bj * kTM + ((bi ^ (bj & 7)) << 2);  // b-row 4*bj, chunk bi (swizzled)
+  const int raw = 4 * bi * kTM + 4 * bj;                  // b-row 4*bi, a values 4*bj..
+  int64_t j = 0;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+    const int st = (int)(j % kTmaTileStages);
+    const bool arrived = mbar_wait(smem_addr(&ts.full[st]), (uint32_t)((j / kTmaTileStages) & 1));
+    const TileItem ti = ts.item[st];
+    float* tile = stage + st * kTM * kTM;
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const float4*>(tile + raw + k * kTM);
+    if (CHAINS && p.pro.n) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = apply_chain4(p.pro, v[k], lt);
+    }
+    __syncwarp();  // the half warp owning these rows has read them
+#pragma unroll
+    for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(tile + own + k * kTM) = v[k];
+    if (__syncthreads_or(arrived ? 0 : 1)) {
+      if (tid == 0) {
+        record_fault(kFaultCopyTimeout);
+        for (int64_t q = j; q < j + kTmaTileStages && blockIdx.x + q * gridDim.x < n_items; ++q)
+          mbar_wait(smem_addr(&ts.full[q % kTmaTileStages]), (uint32_t)((q / kTmaTileStages) & 1));
+      }
+      return;
+    }
+    float4 b[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) b[k] = *reinterpret_cast<const float4*>(tile + oth + k * kTM);
+    // the stage's values are in registers now: the last warp out refills it
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&ts.done[st], 1) == kTileWarps - 1) {
+        ts.done[st] = 0;
+        const int64_t nxt = item + (int64_t)kTmaTileStages * gridDim.x;
+        if (nxt < n_items) {
+          fence_proxy_async();
+          issue(nxt, j + kTmaTileStages);
+        }
+      }
+    }
+    // output row a = a0 + 4bi + k holds b = b0 + 4bj + q: element (b-row 4bj + q, a 4bi + k) of the tile
+    const int64_t b_first = ti.b0 + 4 * bj;
+    if (b_first < nb) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int64_t a = ti.a0 + 4 * bi + k;
+        if (a >= na) break;
+        float4 o = make_float4(comp4(b[0], k), comp4(b[1], k), comp4(b[2], k), comp4(b[3], k));
+        if (CHAINS && p.epi.n) o = apply_chain4(p.epi, o, lt);
+        *reinterpret_cast<float4*>(out + ti.obase + a * soa + b_first) = o;
+      }
+    }
+  }
+}
+
+// A tensor map over the canonical input: dims (a, b, batch axes...), strides in bytes, 64 x 64 boxes.
+static bool make_tile_tensor_map(const TilePlan& p, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int rank = 2 + p.nbatch_axes;
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5], es[5];
+  dims[0] = (cuuint64_t)p.size[p.ax_a];
+  dims[1] = (cuuint64_t)p.size[p.ax_b];
+  strides[0] = (cuuint64_t)p.in_stride[p.ax_b] * 4;
+  for (int q = 0; q < p.nbatch_axes; ++q) {
+    dims[2 + q] = (cuuint64_t)p.size[p.batch_axis[q]];
+    strides[1 + q] = (cuuint64_t)p.in_stride[p.batch_axis[q]] * 4;
+  }
+  for (int d = 0; d < rank; ++d) {
+    box[d] = d < 2 ? kTM : 1;
+    es[d] = 1;
+  }
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, const_cast<void*>(p.in), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-copy tile path applies: 4-byte elements (f32 chains), at most three batch axes, every input
+// stride but a's and every output stride but b's a multiple of 4 elements, dims within int32, aligned
+// buffers, and nb a multiple of 4 (so a 16-byte store never straddles the end of b).
+static bool tile_tma_ok(const TilePlan& p) {
+  if (dt_bytes(p.dt) != 4 || p.nbatch_axes > 3) return false;
+  if ((uintptr_t)p.in % 16 != 0 || (uintptr_t)p.out % 16 != 0) return false;
+  if (p.size[p.ax_b] % 4 != 0) return false;
+  if (p.in_stride[p.ax_a] != 1 || p.out_stride[p.ax_b] != 1) return false;
+  for (int j = 0; j < p.k; ++j) {
+    if (p.size[j] > 0x7FFFFFFF) return false;
+    if (j != p.ax_a && p.in_stride[j] % 4 != 0) return false;
+    if (j != p.ax_b && p.out_stride[j] % 4 != 0) return false;
+  }
+  return !chain_has_bcast_dev(p.pro) && !chain_has_bcast_dev(p.epi);
+}
+
 cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s) {
   const int64_t nta = (p.size[p.ax_a] + kTT - 1) / kTT;
   const int64_t ntb = (p.size[p.ax_b] + kTT - 1) / kTT;
@@ -78,6 +320,18 @@ cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s) {
   if (blocks == 0) return cudaSuccess;
   if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
   const bool chains = p.pro.n > 0 || p.epi.n > 0;
+  CUtensorMap map;
+  if (tile_tma_ok(p) && make_tile_tensor_map(p, &map)) {
+    const int64_t nta64 = (p.size[p.ax_a] + kTM - 1) / kTM, ntb64 = (p.size[p.ax_b] + kTM - 1) / kTM;
+    const int64_t items = nta64 * ntb64 * p.n_batch;
+    auto kernel = chains ? tile_tma_kernel<true> : tile_tma_kernel<false>;
+    const size_t smem = tile_tma_smem_bytes();
+    const int nb = kernel_blocks_per_sm((const void*)kernel, 256, smem);
+    int64_t grid = (int64_t)device_sm_count() * nb;
+    if (grid > items) grid = items;
+    kernel<<<(unsigned)grid, 256, smem, s>>>(map, p, nta64, ntb64, items);
+    return cudaGetLastError();
+  }
   if (chains) {
     tile_transpose_kernel<uint32_t, true><<<(unsigned)blocks, 256, 0, s>>>(p, nta, ntb);
   } else {
