@@ -191,6 +191,32 @@ size_t hlo_reduce_workspace_size(const hlo_array* in, const int64_t* dimensions,
                                  int32_t accum_dtype);
 
 /* ------------------------------------------------------------------------------------------------
+ * hlo_reduce_fusion_noalloc -- hlo_reduce_fusion for callers that cannot allocate device memory.
+ *
+ * No counterpart in the pages: this is a convenience of the library. Some callers cannot allocate a
+ * device workspace where they run a reduction -- for example code embedded in another runtime that owns
+ * all device memory through its own allocator, or code held to a memory budget fixed when it started.
+ * This entry point takes the same arguments as hlo_reduce_fusion without the workspace, allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine), and computes the same result: when
+ * the reduction splits its rows (see hlo_reduce_fusion's workspace), the partials go to a scratch array
+ * of 64 KiB that the library keeps in device memory on every device that loads it, until the process
+ * exits.
+ *   - A reduction that needs more than 64 KiB of scratch (hlo_reduce_workspace_size) is rejected with
+ *     HLO_ERR_WORKSPACE and a message; on this library's current plans that takes a device with far
+ *     more than 2000 SMs.
+ *   - The first call on a device that needs the scratch looks up its device address
+ *     (cudaGetSymbolAddress), once per device, with that device current; make that first call before
+ *     any stream capture.
+ *   - Every call on a device shares the one array. Nothing in it has to start at zero (each call
+ *     writes every partial before reading it), but calls whose kernels overlap on the GPU -- on
+ *     different streams, or from different host threads -- race on it and must be serialised.
+ * ---------------------------------------------------------------------------------------------- */
+hlo_status hlo_reduce_fusion_noalloc(const hlo_array* in, const void* in_ptr, const hlo_ew_chain* prologue,
+                                     const int64_t* dimensions, int32_t n_dimensions, int32_t kind,
+                                     double init_value, int32_t accum_dtype, const hlo_array* out, void* out_ptr,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------------------------------
  * hlo_transpose_fusion -- out = epilogue(transpose(prologue(in), permutation)), or with
  * self_add_epilogue != 0: out = epilogue(prologue(in) + transpose(prologue(in), permutation)).
  *

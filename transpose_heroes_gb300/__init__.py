@@ -32,7 +32,7 @@ STATUS_INVALID_ARG = 1
 STATUS = {0: "HLO_OK", 1: "HLO_ERR_INVALID_ARG", 2: "HLO_ERR_UNSUPPORTED", 3: "HLO_ERR_CUDA", 4: "HLO_ERR_WORKSPACE"}
 
 # Every function the header declares; the library must export all of them.
-EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_workspace_size", "hlo_transpose_fusion",
+EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_fusion_noalloc", "hlo_reduce_workspace_size", "hlo_transpose_fusion",
            "hlo_layout_convert",
            "hlo_quant_fusion", "hlo_quant_binary", "hlo_quant_broadcast_in_dim", "hlo_quant_reshape",
            "hlo_reduce_max_argmax", "hlo_device_faults",
@@ -86,6 +86,9 @@ def lib() -> ctypes.CDLL:
             h.hlo_reduce_fusion.argtypes = [P(Array), vp, P(EwChain), P(i64), i32, i32, ctypes.c_double, i32,
                                             P(Array), vp, vp, ctypes.c_size_t, vp]
             h.hlo_reduce_fusion.restype = ctypes.c_int
+            h.hlo_reduce_fusion_noalloc.argtypes = [P(Array), vp, P(EwChain), P(i64), i32, i32, ctypes.c_double, i32,
+                                                    P(Array), vp, vp]
+            h.hlo_reduce_fusion_noalloc.restype = ctypes.c_int
             h.hlo_reduce_workspace_size.argtypes = [P(Array), P(i64), i32, i32]
             h.hlo_reduce_workspace_size.restype = ctypes.c_size_t
             h.hlo_transpose_fusion.argtypes = [P(Array), vp, P(EwChain), P(i64), i32, P(EwChain), P(Array), vp, vp]
@@ -242,6 +245,21 @@ def reduce_fusion(inp, in_dims, in_dtype, dimensions, kind, init, out, out_dtype
     _check(lib().hlo_reduce_fusion(ctypes.byref(a), _ptr(inp), _ref(ch), dims, len(list(dimensions)),
                                    REDUCE_KINDS[kind], float(init), DTYPES["f32"], ctypes.byref(o), _ptr(out),
                                    _ptr(workspace), int(workspace_bytes), _stream(stream)))
+    return out
+
+
+def reduce_fusion_noalloc(inp, in_dims, in_dtype, dimensions, kind, init, out, out_dtype, in_m2m=None, out_m2m=None,
+                          prologue=None, stream=None):
+    """hlo_reduce_fusion_noalloc: the same reduce with no workspace argument, for callers that cannot
+    allocate device memory; split rows use the library's own 64 KiB scratch on the device."""
+    a = make_array(in_dims, in_m2m, in_dtype)
+    red = set(int(d) for d in dimensions)
+    out_dims = [d for i, d in enumerate(in_dims) if i not in red]
+    o = make_array(out_dims, out_m2m, out_dtype)
+    ch = make_chain(prologue)
+    _check(lib().hlo_reduce_fusion_noalloc(ctypes.byref(a), _ptr(inp), _ref(ch), _i64(dimensions),
+                                           len(list(dimensions)), REDUCE_KINDS[kind], float(init), DTYPES["f32"],
+                                           ctypes.byref(o), _ptr(out), _stream(stream)))
     return out
 
 

@@ -1181,3 +1181,57 @@ hlo_status hlo_quant_fusion(const hlo_array* in, const void* in_ptr, const hlo_q
 }
 
 }  // extern "C"
+
+// ---- reduce without a caller workspace ------------------------------------------------------------------
+// hlo_reduce_fusion needs a device workspace for row reductions it splits across blocks (few long rows).
+// A caller that cannot allocate device memory where it runs the reduce -- code embedded in another
+// runtime that owns all device memory through its own allocator, or running under a memory budget fixed
+// when it started -- has none to give. For those callers the library keeps one fixed scratch array per
+// device, in this file, and hlo_reduce_fusion_noalloc passes it as the workspace.
+namespace {
+constexpr size_t kNoAllocScratchBytes = 64 * 1024;  // room for 16384 f32 row-segment partials
+}  // namespace
+
+// The scratch itself: every device that loads the library holds it until the process exits. In host
+// code its name is only a host-side stand-in for the symbol; its device address comes from
+// cudaGetSymbolAddress below, once per device, and that address is what the kernels receive.
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+// Device address of the scratch on the current device, looked up on the first call per device.
+static hlo_status noalloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e, "reduce_fusion_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= 64)
+    return fail(HLO_ERR_UNSUPPORTED, "reduce_fusion_noalloc: device %d beyond the 64 this library tracks", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_status(e, "reduce_fusion_noalloc: cudaGetSymbolAddress of the scratch");
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return HLO_OK;
+}
+
+extern "C" hlo_status hlo_reduce_fusion_noalloc(const hlo_array* in, const void* in_ptr, const hlo_ew_chain* prologue,
+                                                const int64_t* dimensions, int32_t n_dimensions, int32_t kind,
+                                                double init_value, int32_t accum_dtype, const hlo_array* out,
+                                                void* out_ptr, void* stream) {
+  const size_t need = hlo_reduce_workspace_size(in, dimensions, n_dimensions, accum_dtype);
+  if (need > kNoAllocScratchBytes)
+    return fail(HLO_ERR_WORKSPACE,
+                "reduce_fusion_noalloc: this reduction needs %zu bytes of scratch, more than the %zu the library "
+                "keeps per device; use hlo_reduce_fusion with a workspace",
+                need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  if (need > 0) {
+    const hlo_status st = noalloc_scratch(&scratch);
+    if (st != HLO_OK) return st;
+  }
+  return hlo_reduce_fusion(in, in_ptr, prologue, dimensions, n_dimensions, kind, init_value, accum_dtype, out, out_ptr,
+                           scratch, scratch ? kNoAllocScratchBytes : 0, stream);
+}
