@@ -100,17 +100,24 @@ static __device__ __noinline__ float cr_expf_double(float x) {
 // Every rounding error sums to under 2^-36.5 absolute (y < 2.02; 2^-37.2 in an emulation over 4.2 M
 // arguments); with b = 2^-35 the rounding is decided by monotonicity: if yh + (yl - b) and
 // yh + (yl + b) round to the same float, so does y. Scaling by 2^e is exact in the normal range.
-__device__ __forceinline__ void expf_ff(float x, float& yh, float& yl, int& e) {
+// The reduction of both f32 passes: k = rint(64 x / ln2), x - k ln2/64 = rh + rl to about 2^-54.
+__device__ __forceinline__ void expf_reduce(float x, int& k, float& rh, float& rl) {
   const float t = __fmaf_rn(x, HLO_EXPF_INV64_LN2, 12582912.0f);
-  const int k = __float_as_int(t) - 0x4B400000;
+  k = __float_as_int(t) - 0x4B400000;
   const float kf = __fsub_rn(t, 12582912.0f);
   const float r1 = __fmaf_rn(-kf, HLO_EXPF_L1, x);  // exact
   const float p2h = __fmul_rn(kf, HLO_EXPF_L2);
   const float p2l = __fmaf_rn(kf, HLO_EXPF_L2, -p2h);  // k L2f = p2h + p2l exactly
-  const float rh = __fsub_rn(r1, p2h);                   // TwoSum(r1, -p2h)
+  rh = __fsub_rn(r1, p2h);                               // TwoSum(r1, -p2h)
   const float bb = __fsub_rn(rh, r1);
-  float rl = __fadd_rn(__fsub_rn(r1, __fsub_rn(rh, bb)), __fsub_rn(-p2h, bb));
+  rl = __fadd_rn(__fsub_rn(r1, __fsub_rn(rh, bb)), __fsub_rn(-p2h, bb));
   rl = __fmaf_rn(-kf, HLO_EXPF_L3, __fsub_rn(rl, p2l));
+}
+
+__device__ __forceinline__ void expf_ff(float x, float& yh, float& yl, int& e) {
+  int k;
+  float rh, rl;
+  expf_reduce(x, k, rh, rl);
   float q = __fmaf_rn(rh, 0x1.555556p-5f, 0x1.555556p-3f);  // 1/24, 1/6
   q = __fmaf_rn(rh, q, 0.5f);
   float pe = __fmaf_rn(__fmul_rn(rh, rh), q, rl);
@@ -125,6 +132,48 @@ __device__ __forceinline__ void expf_ff(float x, float& yh, float& yl, int& e) {
   e = k >> 6;
 }
 
+// Second f32 pass, for the arguments the first leaves open (about 1 in 2000), before any FP64 work
+// (FP64 issues at 1/64 of the FP32 rate on this part). The same reduction, then
+//   E = exp(r) - 1 = r + r^2/2 + r^3/6 + r^4/24 + r^5/120   (|r| < 2^-7.5: the r^6 term is below 2^-54)
+// as an unnormalised pair: r^2/2 from the exact FMA split of rh^2 plus rh rl, the r^3 rh-rl cross term
+// (rh^2 rl / 2), and rh^3 (1/6 + rh/24 + rh^2/120) in f32 (below 2^-25.2, relative error under 2^-22);
+// then y = (Th + Tl)(1 + E) with the Th E_hi product split exactly by FMA and Th + (Th E_hi)_hi summed
+// exactly (Th >= 1 > |Th E_hi|). Error terms: E's roundings under 2^-46.4, the table pair under 2^-48
+// relative, y's low-part roundings under 2^-45.5: all under 2^-44.4 for y < 2.02. With b = 2^-43 the
+// monotone rounding test of the first pass decides all but about 2^-19 of these arguments; those take
+// the double path.
+static __device__ __noinline__ float cr_expf_stage2(float x) {
+  int k;
+  float rh, rl;
+  expf_reduce(x, k, rh, rl);
+  const float ph = __fmul_rn(rh, rh);
+  const float pl = __fmaf_rn(rh, rh, -ph);  // rh^2 = ph + pl exactly
+  const float h = __fmul_rn(0.5f, ph), hl = __fmul_rn(0.5f, pl);  // exact
+  float q = __fmaf_rn(rh, 0x1.111112p-7f, 0x1.555556p-5f);       // 1/120, 1/24
+  q = __fmaf_rn(rh, q, 0x1.555556p-3f);                            // 1/6
+  const float c = __fmul_rn(__fmul_rn(ph, rh), q);                 // r^3/6 + r^4/24 + r^5/120
+  const float sh = __fadd_rn(rh, h);                               // Fast2Sum: |rh| > |h|
+  const float sl = __fsub_rn(h, __fsub_rn(sh, rh));
+  float t = __fmaf_rn(rh, rl, rl);                                 // rl (1 + rh)
+  t = __fmaf_rn(h, rl, t);                                         // + rh^2 rl / 2
+  t = __fadd_rn(t, hl);
+  t = __fadd_rn(t, c);
+  const float el = __fadd_rn(sl, t);                               // E = sh + el
+  const float2 T = __ldg(&kExpTf[k & 63]);
+  const float qh = __fmul_rn(T.x, sh);
+  const float qe = __fmaf_rn(T.x, sh, -qh);                        // Th sh = qh + qe exactly
+  const float yh = __fadd_rn(T.x, qh);                             // Fast2Sum: Th >= 1 > |qh|
+  const float ye = __fsub_rn(qh, __fsub_rn(yh, T.x));
+  float lo = __fmaf_rn(T.y, sh, T.y);                              // Tl (1 + E_hi)
+  lo = __fmaf_rn(T.x, el, lo);                                     // + Th E_lo
+  lo = __fadd_rn(lo, qe);
+  const float yl = __fadd_rn(ye, lo);
+  const float yp = __fadd_rn(yh, __fadd_rn(yl, 0x1p-43f));
+  const float ym = __fadd_rn(yh, __fsub_rn(yl, 0x1p-43f));
+  if (yp == ym) return __fmul_rn(yp, __int_as_float((127 + (k >> 6)) << 23));
+  return cr_expf_double(x);
+}
+
 __device__ __forceinline__ float cr_expf(float x) {
   if (x > -87.0f && x < 88.5f) {
     float yh, yl;
@@ -133,6 +182,7 @@ __device__ __forceinline__ float cr_expf(float x) {
     const float yp = __fadd_rn(yh, __fadd_rn(yl, 0x1p-35f));
     const float ym = __fadd_rn(yh, __fsub_rn(yl, 0x1p-35f));
     if (yp == ym) return __fmul_rn(yp, __int_as_float((127 + e) << 23));
+    return cr_expf_stage2(x);
   }
   return cr_expf_double(x);
 }

@@ -147,9 +147,13 @@ __device__ __forceinline__ float comp4(const float4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
-template <bool CHAINS>
+// PK: 0 -- no chains; 1 -- chains interpreted at run time; 2 -- the prologue is exactly exp (evaluated
+// inline, its rare second and third passes out of line), the epilogue interpreted at run time.
+enum TileChains : int { TK_NONE = 0, TK_RT = 1, TK_EXP = 2 };
+template <int PK>
 __global__ void __launch_bounds__(256, 3)
     tile_tma_kernel(const __grid_constant__ CUtensorMap tmap, TilePlan p, int64_t nta, int64_t ntb, int64_t n_items) {
+  constexpr bool CHAINS = PK != TK_NONE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   float* stage = reinterpret_cast<float*>(base);  // [stages][64 b-rows][64 a]
@@ -228,7 +232,10 @@ __global__ void __launch_bounds__(256, 3)
     float4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const float4*>(tile + raw + k * kTM);
-    if (CHAINS && p.pro.n) {
+    if (PK == TK_EXP) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[k] = make_float4(cr_expf(v[k].x), cr_expf(v[k].y), cr_expf(v[k].z), cr_expf(v[k].w));
+    } else if (CHAINS && p.pro.n) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) v[k] = apply_chain4(p.pro, v[k], lt);
     }
@@ -324,7 +331,8 @@ cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s) {
   if (tile_tma_ok(p) && make_tile_tensor_map(p, &map)) {
     const int64_t nta64 = (p.size[p.ax_a] + kTM - 1) / kTM, ntb64 = (p.size[p.ax_b] + kTM - 1) / kTM;
     const int64_t items = nta64 * ntb64 * p.n_batch;
-    auto kernel = chains ? tile_tma_kernel<true> : tile_tma_kernel<false>;
+    const bool exp_pro = p.pro.n == 1 && p.pro.op[0] == OP_EXP;
+    auto kernel = !chains ? tile_tma_kernel<TK_NONE> : exp_pro ? tile_tma_kernel<TK_EXP> : tile_tma_kernel<TK_RT>;
     const size_t smem = tile_tma_smem_bytes();
     const int nb = kernel_blocks_per_sm((const void*)kernel, 256, smem);
     int64_t grid = (int64_t)device_sm_count() * nb;
