@@ -437,6 +437,61 @@ def ours(args):
     return 0
 
 
+def parse_kw(text):
+    """'n=6144,dims=(3,512,2048)' -> {'n': 6144, 'dims': (3, 512, 2048)} (literals only)."""
+    import ast
+
+    out, depth, cur = {}, 0, ""
+    parts = []
+    for ch in text:
+        depth += ch in "([{"
+        depth -= ch in ")]}"
+        if ch == "," and depth == 0:
+            parts.append(cur)
+            cur = ""
+        else:
+            cur += ch
+    if cur.strip():
+        parts.append(cur)
+    for part in parts:
+        k, v = part.split("=", 1)
+        out[k.strip()] = ast.literal_eval(v.strip())
+    return out
+
+
+def one_fusion(args):
+    """Times one fusion alone (a maker of transpose_heroes_gb300.inputs, e.g. transpose_log, gelu_bf16,
+    sum_exp_f32, with --fusion-kw for its sizes): --warmup launches, then --steps launches each after an
+    L2 flush, CUDA events on the launching stream; prints one JSON line. Used for per-kernel profiles."""
+    import torch
+
+    from transpose_heroes_gb300 import build as libbuild
+    from transpose_heroes_gb300.runner import DeviceFusion
+
+    libbuild.build()
+    f = getattr(inp, args.fusion)(seed=args.seed, **parse_kw(args.fusion_kw))
+    d = DeviceFusion(f)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        d.run(stream=stream)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in evs:
+        flush.fill_(2)
+        torch.cuda._sleep(HOST_LEAD_CYCLES // 8)
+        a.record(stream)
+        d.run(stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs) if evs else 0.0
+    hbm, src = peaks()
+    gbs = f.algorithmic_bytes / (us / 1e6) / 1e9 if us else 0.0
+    print(json.dumps({"fusion": f.name, "workload": f.description, "us": us, "algorithmic_bytes": f.algorithmic_bytes,
+                      "gbs": gbs, "frac_of_" + src: gbs / hbm, "launches": args.steps}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -445,7 +500,11 @@ def main():
     ap.add_argument("--seed", type=int, default=1)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--fusion", help="time one fusion alone (a maker in transpose_heroes_gb300.inputs)")
+    ap.add_argument("--fusion-kw", default="", help="the maker's sizes, e.g. n=6144 or dims=(3,512,2048)")
     args = ap.parse_args()
+    if args.fusion:
+        return one_fusion(args)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

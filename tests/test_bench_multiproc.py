@@ -61,3 +61,10 @@ def test_gpus_flag_needs_one_process_per_gpu():
                        env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 2
     assert "torch.distributed.run" in r.stderr
+
+
+def test_fusion_kw_parsing():
+    import bench
+
+    assert bench.parse_kw("n=6144,dims=(3,512,2048)") == {"n": 6144, "dims": (3, 512, 2048)}
+    assert bench.parse_kw("") == {}

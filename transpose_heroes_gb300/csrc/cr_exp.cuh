@@ -187,6 +187,48 @@ __device__ __forceinline__ float cr_expf(float x) {
   return cr_expf_double(x);
 }
 
+// The passes after the first, for an argument the first pass left open (or outside its range).
+static __device__ __noinline__ float cr_expf_rest(float x) {
+  return (x > -87.0f && x < 88.5f) ? cr_expf_stage2(x) : cr_expf_double(x);
+}
+
+// The first pass for two arguments at once in packed f32x2 arithmetic (the same operations as
+// expf_ff and the rounding test of cr_expf, each lane rounded alike). ok0 / ok1 report a settled
+// result; an open argument, or one outside (-87, 88.5), is the caller's to finish with cr_expf_rest.
+__device__ __forceinline__ void cr_expf_first2(float x0, float x1, float& y0, float& y1, bool& ok0, bool& ok1) {
+  const float2 X = f2::pk(x0, x1);
+  const float2 T = f2::fma(X, f2::splat(HLO_EXPF_INV64_LN2), f2::splat(12582912.0f));
+  const int k0 = __float_as_int(T.x) - 0x4B400000, k1 = __float_as_int(T.y) - 0x4B400000;
+  const float2 KF = f2::add(T, f2::splat(-12582912.0f));
+  const float2 R1 = f2::fma(KF, f2::splat(-HLO_EXPF_L1), X);                  // exact
+  const float2 P2H = f2::mul(KF, f2::splat(HLO_EXPF_L2));
+  const float2 NP2H = f2::mul(P2H, f2::splat(-1.0f));                         // exact
+  const float2 P2L = f2::fma(KF, f2::splat(HLO_EXPF_L2), NP2H);               // k L2f = p2h + p2l
+  const float2 RH = f2::add(R1, NP2H);                                        // TwoSum(r1, -p2h)
+  const float2 BB = f2::sub(RH, R1);
+  float2 RL = f2::add(f2::sub(R1, f2::sub(RH, BB)), f2::sub(NP2H, BB));
+  RL = f2::fma(KF, f2::splat(-HLO_EXPF_L3), f2::sub(RL, P2L));
+  float2 Q = f2::fma(RH, f2::splat(0x1.555556p-5f), f2::splat(0x1.555556p-3f));  // 1/24, 1/6
+  Q = f2::fma(RH, Q, f2::splat(0.5f));
+  float2 PE = f2::fma(f2::mul(RH, RH), Q, RL);
+  PE = f2::fma(RL, RH, PE);
+  const float2 t0 = __ldg(&kExpTf[k0 & 63]), t1 = __ldg(&kExpTf[k1 & 63]);
+  const float2 TX = f2::pk(t0.x, t1.x), TY = f2::pk(t0.y, t1.y);
+  const float2 AH = f2::mul(TX, RH);
+  const float2 AL = f2::fma(TX, RH, f2::mul(AH, f2::splat(-1.0f)));
+  float2 LO = f2::fma(TX, PE, TY);
+  LO = f2::add(f2::fma(TY, RH, LO), AL);
+  const float2 YH = f2::add(TX, AH);  // Fast2Sum: Th >= 1 > |ah|
+  const float2 YL = f2::add(f2::sub(AH, f2::sub(YH, TX)), LO);
+  const float2 YP = f2::add(YH, f2::add(YL, f2::splat(0x1p-35f)));
+  const float2 YM = f2::add(YH, f2::sub(YL, f2::splat(0x1p-35f)));
+  const float2 Y = f2::mul(YP, f2::pk(__int_as_float((127 + (k0 >> 6)) << 23), __int_as_float((127 + (k1 >> 6)) << 23)));
+  y0 = Y.x;
+  y1 = Y.y;
+  ok0 = (x0 > -87.0f) & (x0 < 88.5f) & (YP.x == YM.x);
+  ok1 = (x1 > -87.0f) & (x1 < 88.5f) & (YP.y == YM.y);
+}
+
 // ------------------------------------------------------------------------------------------------
 // Correctly rounded f32 tanh ("StableHLO Specification", section "tanh"), the same way: CUDA's double
 // tanh (within 1 double ulp) rounded once unless it sits within 3 double ulps of an f32 boundary; then

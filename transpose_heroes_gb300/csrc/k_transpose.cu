@@ -229,19 +229,27 @@ __global__ void __launch_bounds__(256, 3)
     const bool arrived = mbar_wait(smem_addr(&ts.full[st]), (uint32_t)((j / kTmaTileStages) & 1));
     const TileItem ti = ts.item[st];
     float* tile = stage + st * kTM * kTM;
-    float4 v[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const float4*>(tile + raw + k * kTM);
-    if (PK == TK_EXP) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = make_float4(cr_expf(v[k].x), cr_expf(v[k].y), cr_expf(v[k].z), cr_expf(v[k].w));
-    } else if (CHAINS && p.pro.n) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[k] = apply_chain4(p.pro, v[k], lt);
+    // one b-row at a time: a thread's swizzled chunk of row r lies in row r, which only its own half
+    // warp reads, so a warp sync per row orders the in-place rewrite; the loop keeps the code small
+    // (fully unrolled, sixteen inline exps overflowed the instruction cache: 734 against 634 us)
+#pragma unroll 1
+    for (int k = 0; k < 4; ++k) {
+      float4 v = *reinterpret_cast<const float4*>(tile + raw + k * kTM);
+      if (PK == TK_EXP) {  // two packed first passes; open arguments (about 1 in 2000) finish out of line
+        float4 y;
+        bool ok[4];
+        cr_expf_first2(v.x, v.y, y.x, y.y, ok[0], ok[1]);
+        cr_expf_first2(v.z, v.w, y.z, y.w, ok[2], ok[3]);
+        if (!ok[0]) y.x = cr_expf_rest(v.x);
+        if (!ok[1]) y.y = cr_expf_rest(v.y);
+        if (!ok[2]) y.z = cr_expf_rest(v.z);
+        if (!ok[3]) y.w = cr_expf_rest(v.w);
+        v = y;
+      }
+      else if (CHAINS && p.pro.n) v = apply_chain4(p.pro, v, lt);
+      __syncwarp();
+      *reinterpret_cast<float4*>(tile + own + k * kTM) = v;
     }
-    __syncwarp();  // the half warp owning these rows has read them
-#pragma unroll
-    for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(tile + own + k * kTM) = v[k];
     if (__syncthreads_or(arrived ? 0 : 1)) {
       if (tid == 0) {
         record_fault(kFaultCopyTimeout);

@@ -257,6 +257,17 @@ def transpose3_exp_abs(seed: int = 1, dims=(512, 640, 680)) -> Fusion:
         description=f"abs(transpose(exp(x), {{2,1,0}})), x f32[{dims[0]},{dims[1]},{dims[2]}]{{2,1,0}} ~ U(-3,3)")
 
 
+def sum_exp_f32(seed: int = 1, n: int = 1 << 26) -> Fusion:
+    """A whole array reduced to one value: sum of exp(x) over x f32[n] ~ U(-1,1), seen as [1, n] (the
+    row reduce with a single row, which splits the row across blocks)."""
+    g = rng(seed)
+    return Fusion(
+        name=f"sum_exp_f32_{n}", kind="reduce", dims=[1, n], m2m=[1, 0], dtype="f32",
+        data=uniform_f32(g, n, -1.0, 1.0), dimensions=[1], reduce_kind="add", init=0.0,
+        prologue={"ops": ["exp"], "round_each": True}, out_dims=[1], out_m2m=[0], out_dtype="f32",
+        description=f"out f32[1] = reduce-add over dim 1 of exp(x), x f32[1,{n}] ~ U(-1,1)")
+
+
 # The five full-size workloads, in a fixed order.
 FULL = {
     "row_reduce_exp": row_reduce_exp,
