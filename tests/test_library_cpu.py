@@ -330,3 +330,33 @@ def test_reduce_workspace_rules(lib):
     st, msg = _status(lambda: hf.reduce_fusion(big_in, [1, 1 << 24], "f32", [1], "add", 0.0, big_out, "f32",
                                                workspace=ws, workspace_bytes=4, stream=0))
     assert st == 4 and "workspace" in msg
+
+
+def test_tanh_table_matches_its_generator(tmp_path):
+    """tanh_table.inc is what gen_tanh_table.py writes (Python decimal, exact bf16 rounding)."""
+    import importlib.util
+    csrc = os.path.join(ROOT, "transpose_heroes_gb300", "csrc")
+    spec = importlib.util.spec_from_file_location("gen_tanh_table", os.path.join(csrc, "gen_tanh_table.py"))
+    gen = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(gen)
+    out = tmp_path / "tanh_table.inc"
+    gen.main(str(out))
+    with open(os.path.join(csrc, "tanh_table.inc")) as f:
+        assert out.read_text() == f.read()
+
+
+def test_tanh_table_against_the_oracle():
+    """Every entry of the bf16 tanh table equals the oracle's correctly rounded bf16 tanh of that
+    argument, for both signs (the kernel copies the sign of x onto the entry of |x|)."""
+    import re
+    with open(os.path.join(ROOT, "transpose_heroes_gb300", "csrc", "tanh_table.inc")) as f:
+        tab = np.array([int(v, 16) for v in re.findall(r"0x([0-9A-F]{4})", f.read())], dtype=np.uint32)
+    assert len(tab) == 32768
+    import oracle
+    data = np.arange(1 << 16, dtype=np.uint16)
+    ref = oracle.transpose(data, [1 << 16], "bf16", [0], prologue={"ops": ["tanh"], "round_each": True})
+    ref = ref.view(np.uint16).astype(np.uint32)
+    got = tab[data & 0x7FFF] | (data.astype(np.uint32) & 0x8000)
+    bf = lambda b: (b.astype(np.uint32) << 16).view(np.float32)
+    same = (got == ref) | (np.isnan(bf(got)) & np.isnan(bf(ref)))
+    assert same.all(), np.flatnonzero(~same)[:8]

@@ -5,6 +5,10 @@
 
 #include "device_common.cuh"
 
+namespace hlo {
+#include "tanh_table.inc"  // kTanhBf16: tanh rounded to bf16 for every bf16 |x|
+}  // namespace hlo
+
 namespace cg = cooperative_groups;
 
 namespace hlo {
@@ -156,29 +160,85 @@ __device__ __forceinline__ bool bf16_clear_of_midpoint(float y, int ulps) {
   return (d > ulps || d < -ulps) || ((b & 0x7F800000u) == 0x7F800000u);
 }
 
-// exp, log or tanh of one packed bf16 pair, correctly rounded to bf16.
-__device__ __forceinline__ uint32_t bf16_fn2(int op, uint32_t w, const LogTab& lt) {
+// exp, log or tanh of one packed pair, correctly rounded to the 16-bit type, the slow way (the
+// correctly rounded per-element path); out of line, as the fast path below rarely needs it.
+template <int DT>
+static __device__ __noinline__ uint32_t fn2_exact(int op, uint32_t w, const LogTab& lt) {
+  return pk_pack<DT>(apply_op(op, pk_lo<DT>(w), 0.f, 0.f, 0.f, true, DT, lt),
+                     apply_op(op, pk_hi<DT>(w), 0.f, 0.f, 0.f, true, DT, lt));
+}
+
+// exp, log or tanh of one packed bf16 pair from an f32 approximation: returns false (and leaves w
+// unchanged) when a lane's f32 value lies too close to a bf16 rounding midpoint to decide it.
+template <int OP>
+__device__ __forceinline__ bool bf16_fn2_fast(uint32_t& w, const LogTab& lt) {
   const float a = pk_lo<BF16>(w), b = pk_hi<BF16>(w);
   float2 f;
   int ulps = 2;  // expf is within 2 ulps; cr_logf is correctly rounded
-  if (op == OP_TANH) {
+  if (OP == OP_TANH) {
     f = tanh_fast2(make_float2(a, b));
     ulps = 16;
-  } else if (op == OP_EXP) {
+  } else if (OP == OP_EXP) {
     f = make_float2(expf(a), expf(b));
   } else {
     f = make_float2(cr_logf(a, lt.c, lt.e), cr_logf(b, lt.c, lt.e));
   }
   // the f32 value's bf16 rounding is the correct one unless the bits it drops lie within `ulps`
-  // of the midpoint; then the correctly rounded 16-bit path decides
-  if (bf16_clear_of_midpoint(f.x, ulps) && bf16_clear_of_midpoint(f.y, ulps)) return pk_pack<BF16>(f.x, f.y);
-  return pk_pack<BF16>(apply_op(op, a, 0.f, 0.f, 0.f, true, BF16, lt),
-                       apply_op(op, b, 0.f, 0.f, 0.f, true, BF16, lt));
+  // of the midpoint
+  if (!(bf16_clear_of_midpoint(f.x, ulps) & bf16_clear_of_midpoint(f.y, ulps))) return false;
+  w = pk_pack<BF16>(f.x, f.y);
+  return true;
 }
 
-// The chain on kV packed pairs (2 kV elements); the op dispatch is shared by all of them.
-template <int DT, int kV>
-__device__ __forceinline__ void chain16x2(const Chain& c, uint32_t (&v)[kV], const uint32_t (&x)[kV], const LogTab& lt) {
+// One transcendental op on kV packed pairs: the fast path for every pair, then the exact path for
+// the pairs it could not decide (one branch per op, not per pair).
+template <int DT, int OP, int kV>
+__device__ __forceinline__ void fn16x2(uint32_t (&v)[kV], const LogTab& lt) {
+  if (DT == BF16) {
+    uint32_t open = 0u;
+#pragma unroll
+    for (int j = 0; j < kV; ++j) open |= (bf16_fn2_fast<OP>(v[j], lt) ? 0u : 1u) << j;
+    if (open) {
+#pragma unroll
+      for (int j = 0; j < kV; ++j)
+        if (open & (1u << j)) v[j] = fn2_exact<DT>(OP, v[j], lt);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kV; ++j) v[j] = fn2_exact<DT>(OP, v[j], lt);
+  }
+}
+
+// One pair through exp, log or tanh: the fast path, then the exact one if needed, in one out-of-line
+// call (the streaming kernel keeps its registers for the data).
+template <int DT>
+static __device__ __noinline__ uint32_t fn2_call(int op, uint32_t w, const LogTab& lt) {
+  if (DT == BF16) {
+    uint32_t r = w;
+    const bool ok = op == OP_TANH  ? bf16_fn2_fast<OP_TANH>(r, lt)
+                    : op == OP_EXP ? bf16_fn2_fast<OP_EXP>(r, lt)
+                                   : bf16_fn2_fast<OP_LOG>(r, lt);
+    if (ok) return r;
+  }
+  return fn2_exact<DT>(op, w, lt);
+}
+
+// tanh of a packed bf16 pair from the table of kTanhBf16 (in shared memory): the entry of |x|, with
+// the sign of x.
+__device__ __forceinline__ uint32_t tanh_bf16x2_tab(uint32_t w, const uint16_t* tab) {
+  const uint32_t a = w & 0x7FFF7FFFu;
+  const uint32_t lo = tab[a & 0xFFFFu], hi = tab[a >> 16];
+  return __byte_perm(lo, hi, 0x5410) | (w & 0x80008000u);
+}
+
+// The chain on kV packed pairs (2 kV elements); the op dispatch is shared by all of them. With TT,
+// bf16 tanh reads the table at `ttab` and the chain has no exp or log (the caller makes sure: their
+// code would take registers from the data); with OOL, exp, log (and tanh without the table) run out
+// of line.
+template <int DT, int kV, bool TT = false, bool OOL = false>
+__device__ __forceinline__ void chain16x2(const Chain& c, uint32_t (&v)[kV], const uint32_t (&x)[kV], const LogTab& lt,
+                                          const uint16_t* ttab = nullptr) {
+#pragma unroll 1
   for (int k = 0; k < c.n; ++k) {
     switch (c.op[k]) {
       case OP_MUL_IN:
@@ -209,39 +269,83 @@ __device__ __forceinline__ void chain16x2(const Chain& c, uint32_t (&v)[kV], con
 #pragma unroll
         for (int j = 0; j < kV; ++j) v[j] &= 0x7FFF7FFFu;
         break;
-      default: {  // exp, log, tanh
-        const int op = c.op[k];
-        if (DT == BF16) {
+      case OP_TANH:
+        if (TT && DT == BF16) {
 #pragma unroll
-          for (int j = 0; j < kV; ++j) v[j] = bf16_fn2(op, v[j], lt);
+          for (int j = 0; j < kV; ++j) v[j] = tanh_bf16x2_tab(v[j], ttab);
+        } else if (OOL) {
+#pragma unroll
+          for (int j = 0; j < kV; ++j) v[j] = fn2_call<DT>(OP_TANH, v[j], lt);
         } else {
-#pragma unroll
-          for (int j = 0; j < kV; ++j)
-            v[j] = pk_pack<DT>(apply_op(op, pk_lo<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt),
-                               apply_op(op, pk_hi<DT>(v[j]), 0.f, 0.f, 0.f, true, DT, lt));
+          fn16x2<DT, OP_TANH, kV>(v, lt);
         }
-      }
+        break;
+      default:  // exp, log
+        if (TT && DT == BF16) {
+          // not reached: chains with a table tanh have no exp or log
+        } else if (OOL) {
+          const int op = c.op[k];
+#pragma unroll
+          for (int j = 0; j < kV; ++j) v[j] = fn2_call<DT>(op, v[j], lt);
+        } else if (c.op[k] == OP_EXP) {
+          fn16x2<DT, OP_EXP, kV>(v, lt);
+        } else {
+          fn16x2<DT, OP_LOG, kV>(v, lt);
+        }
     }
   }
 }
 
-template <int DT>
-__global__ void __launch_bounds__(256) elementwise_16x2_kernel(EwPlan p) {
+// Streaming kernel: a thread takes four 16-byte vectors (32 elements) per step -- a warp 2 KiB of
+// contiguous input, each of its four loads 512 contiguous bytes -- and runs the chain on them with one
+// op dispatch per 32 elements; the vectors left after the last full round of steps go one per thread,
+// so no thread ends more than one vector behind another. With TT (a bf16 chain with tanh) each block
+// copies the 64 KiB tanh table into its shared memory while its first loads are in flight.
+constexpr int kTanhTabThreads = 1024;
+template <int DT, bool TT>
+__global__ void __launch_bounds__(TT ? kTanhTabThreads : 256, TT ? 1 : 4) elementwise_16x2_kernel(EwPlan p) {
   const LogTab lt = global_log_tables();
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t nv = p.n / 16;  // two 16-byte vectors per step
+  extern __shared__ __align__(16) uint16_t ttab[];
   const uint4* in = reinterpret_cast<const uint4*>(p.in);
   uint4* out = reinterpret_cast<uint4*>(p.out);
-  for (int64_t i = tid; i < nv; i += stride) {
-    const uint4 w0 = __ldg(in + 2 * i), w1 = __ldg(in + 2 * i + 1);
-    const uint32_t x[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    uint32_t v[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    chain16x2<DT, 8>(p.pro, v, x, lt);
-    out[2 * i] = make_uint4(v[0], v[1], v[2], v[3]);
-    out[2 * i + 1] = make_uint4(v[4], v[5], v[6], v[7]);
+  const int64_t nvec = p.n / 8;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t lane = threadIdx.x & 31, gwarp = gtid >> 5;
+  const int64_t rounds = nvec / (4 * nthreads);
+  uint32_t x[16];
+  auto load4 = [&](int64_t r) {
+    const int64_t b = r * 4 * nthreads + gwarp * 128 + lane;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint4 w = __ldg(in + b + 32 * u);
+      x[4 * u] = w.x, x[4 * u + 1] = w.y, x[4 * u + 2] = w.z, x[4 * u + 3] = w.w;
+    }
+  };
+  if (rounds > 0) load4(0);
+  if (TT) {
+    for (int i = threadIdx.x; i < 32768 / 8; i += blockDim.x)
+      reinterpret_cast<uint4*>(ttab)[i] = reinterpret_cast<const uint4*>(kTanhBf16)[i];
+    __syncthreads();
   }
-  for (int64_t e = nv * 16 + tid; e < p.n; e += stride) {
+  for (int64_t r = 0; r < rounds; ++r) {
+    if (r > 0) load4(r);
+    uint32_t v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = x[j];
+    chain16x2<DT, 16, TT, true>(p.pro, v, x, lt, ttab);
+    const int64_t b = r * 4 * nthreads + gwarp * 128 + lane;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) out[b + 32 * u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+  }
+  for (int64_t i = rounds * 4 * nthreads + gtid; i < nvec; i += nthreads) {
+    const uint4 w = __ldg(in + i);
+    const uint32_t y[4] = {w.x, w.y, w.z, w.w};
+    uint32_t v[4] = {w.x, w.y, w.z, w.w};
+    chain16x2<DT, 4, TT, true>(p.pro, v, y, lt, ttab);
+    out[i] = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+  for (int64_t e = nvec * 8 + gtid; e < p.n; e += nthreads) {
     const float r = apply_chain_rt(p.pro, load_as_f32(p.in, DT, e), 0, lt);
     store_from_f32(p.out, DT, e, r);
   }
@@ -331,15 +435,42 @@ __global__ void __launch_bounds__(kLutThreads, 1) elementwise_lut16_kernel(EwPla
   for (int64_t e = nv * 8 + tid; e < p.n; e += stride) out[e] = lut[in[e]];
 }
 
+// The table pays for a large input whose chain has an op the packed kernel evaluates slowly: exp or
+// log, or tanh other than on bf16 values (the packed kernel reads bf16 tanh from kTanhBf16).
 static bool lut16_ok(const Chain& pro, const Chain& epi, int dt, int64_t n) {
   if ((dt != BF16 && dt != F16) || n < kLutMinElems) return false;
+  const bool tanh_tab = dt == BF16 && chain16x2_ok(pro, epi, dt);
   bool costly = false;
   for (const Chain* c : {&pro, &epi})
     for (int k = 0; k < c->n; ++k) {
       if (c->op[k] == OP_ADD_BCAST) return false;
-      if (c->op[k] == OP_EXP || c->op[k] == OP_LOG || c->op[k] == OP_TANH) costly = true;
+      if (c->op[k] == OP_EXP || c->op[k] == OP_LOG || (c->op[k] == OP_TANH && !tanh_tab)) costly = true;
     }
   return costly;
+}
+
+// The packed 16-bit kernel, with the tanh table when a bf16 chain has tanh (and no exp or log):
+// 1024-thread blocks, one per SM; otherwise 256-thread blocks. Either way the grid is one full wave
+// of resident blocks (or fewer when the input is small).
+template <int DT>
+static cudaError_t launch_16x2(const EwPlan& p, cudaStream_t s) {
+  bool tanh = false, explog = false;
+  for (int k = 0; k < p.pro.n; ++k) {
+    tanh |= p.pro.op[k] == OP_TANH;
+    explog |= p.pro.op[k] == OP_EXP || p.pro.op[k] == OP_LOG;
+  }
+  constexpr bool kTab = DT == BF16;  // the table variant exists for bf16 only
+  const bool tt = kTab && tanh && !explog;
+  const int threads = tt ? kTanhTabThreads : 256;
+  const size_t smem = tt ? 32768 * sizeof(uint16_t) : 0;
+  const void* kernel = tt ? (const void*)elementwise_16x2_kernel<DT, kTab> : (const void*)elementwise_16x2_kernel<DT, false>;
+  int64_t blocks = (p.n / 32 + threads - 1) / threads;
+  const int64_t cap = (int64_t)device_sm_count() * kernel_blocks_per_sm(kernel, threads, smem);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (tt) elementwise_16x2_kernel<DT, kTab><<<(unsigned)blocks, threads, smem, s>>>(p);
+  else elementwise_16x2_kernel<DT, false><<<(unsigned)blocks, threads, 0, s>>>(p);
+  return cudaGetLastError();
 }
 
 template <int DT, bool PACKED>
@@ -405,12 +536,7 @@ cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, con
     if (chain16x2_ok(pro, epi, dt)) return dt == BF16 ? lut16_launch<BF16, true>(p, s) : lut16_launch<F16, true>(p, s);
     return dt == BF16 ? lut16_launch<BF16, false>(p, s) : lut16_launch<F16, false>(p, s);
   } else if (chain16x2_ok(pro, epi, dt) && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0) {
-    int64_t vblocks = (n / 16 + 255) / 256;
-    const int64_t vcap = (int64_t)device_sm_count() * 8;
-    if (vblocks > vcap) vblocks = vcap;
-    if (vblocks < 1) vblocks = 1;
-    if (dt == BF16) elementwise_16x2_kernel<BF16><<<(unsigned)vblocks, 256, 0, s>>>(p);
-    else elementwise_16x2_kernel<F16><<<(unsigned)vblocks, 256, 0, s>>>(p);
+    return dt == BF16 ? launch_16x2<BF16>(p, s) : launch_16x2<F16>(p, s);
   } else {
     elementwise_any_kernel<<<(unsigned)blocks, 256, 0, s>>>(p);
   }
