@@ -829,12 +829,24 @@ def _qpt(scale, zp, smin=-128, smax=127):
             "storage_max": smax}
 
 
+# Parameter sets: "packed" keeps every |r / s| small (the packed kernel for add, maximum, minimum and
+# multiply; its clamp variant, then its saturating-pack one); "wide" scales push r / s past that kernel's
+# range (the pair-table kernel for large inputs, the vector kernel for small ones).
+QB_PARAMS = {
+    "packed_clamp": (_qpt(0.0371, 4), _qpt(0.113, -9), _qpt(0.09, 2, -100, 120)),
+    "packed": (_qpt(0.0371, 4), _qpt(0.113, -9), _qpt(0.0731, -3)),
+    "wide": (_qpt(61.0, 4), _qpt(47.5, -9), _qpt(0.0013, 2, -100, 120)),
+}
+
+
+@pytest.mark.parametrize("params", list(QB_PARAMS))
 @pytest.mark.parametrize("op", ["add", "divide", "maximum", "minimum", "multiply"])
-def test_quant_binary_every_code_pair(op):
-    """All 65536 code pairs, aligned (vector kernel) and through unaligned views (per-element kernel)."""
+def test_quant_binary_every_code_pair(op, params):
+    """All 65536 code pairs, aligned (packed or vector kernel) and through unaligned views (per-element
+    kernel)."""
     codes = np.arange(-128, 128, dtype=np.int8)
     a, b = np.repeat(codes, 256), np.tile(codes, 256)
-    ql, qr, qo = _qpt(0.0371, 4), _qpt(0.113, -9), _qpt(0.09, 2, -100, 120)
+    ql, qr, qo = QB_PARAMS[params]
     ref = oracle.quant_binary(op, a, b, [a.size], ql, qr, qo)
     for shift in (0, 1):
         base_a = torch.from_numpy(np.concatenate([np.zeros(shift, np.int8), a])).cuda()
@@ -846,15 +858,17 @@ def test_quant_binary_every_code_pair(op):
         assert np.array_equal(got, ref), f"{int((got != ref).sum())} codes differ (shift {shift})"
 
 
+@pytest.mark.parametrize("params", list(QB_PARAMS))
 @pytest.mark.parametrize("op", ["add", "divide", "maximum", "minimum", "multiply"])
-def test_quant_binary_table_every_code_pair(op):
-    """Inputs large enough for the pair-table kernel (2^22 elements or more): all 65536 code pairs 64
-    times over plus a ragged tail, bit-exact against the oracle."""
+def test_quant_binary_large_every_code_pair(op, params):
+    """Inputs of 2^22 elements or more (the packed kernel, or the pair-table kernel for divide and for
+    the wide parameters): all 65536 code pairs 64 times over plus a ragged tail, bit-exact against the
+    oracle."""
     codes = np.arange(-128, 128, dtype=np.int8)
     a0, b0 = np.repeat(codes, 256), np.tile(codes, 256)
     a = np.concatenate([np.tile(a0, 64), a0[:13]])
     b = np.concatenate([np.tile(b0, 64), b0[7:20]])
-    ql, qr, qo = _qpt(0.0371, 4), _qpt(0.113, -9), _qpt(0.09, 2, -100, 120)
+    ql, qr, qo = QB_PARAMS[params]
     ref = oracle.quant_binary(op, a, b, [a.size], ql, qr, qo)
     out = torch.empty(a.size, dtype=torch.int8, device="cuda")
     hf.quant_binary(op, torch.from_numpy(a).cuda(), torch.from_numpy(b).cuda(), [a.size], ql, qr, out, qo)

@@ -2,6 +2,8 @@
 // op, quantize ("StableHLO Specification": dequantize_op_quantize(op, lhs, rhs, type(result)) for
 // add, divide, maximum, minimum, multiply). Same layout everywhere: 16 codes per 16-byte vector;
 // otherwise a thread per element with index maps.
+#include <algorithm>
+#include <cmath>
 #include <cooperative_groups.h>
 
 #include "quant_common.cuh"
@@ -65,6 +67,140 @@ __global__ void __launch_bounds__(256) quant_binary_map_kernel(QuantBinaryPlan p
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += stride)
     p.out[map_index(p.omap, i)] = (int8_t)qbin<OP>(p.lhs[map_index(p.lmap, i)], p.rhs[map_index(p.rmap, i)], p);
+}
+
+// ---- packed per-tensor kernel (add, maximum, minimum, multiply) -------------------------------------
+// Two codes of each operand per f32x2 instruction. A code c becomes the float 1.5*2^23 + (c + 128)
+// with one byte permute (the word is first xored with 0x80808080); adding -(1.5*2^23 + 128 + z) gives
+// c - z exactly, and the scale product is the dequantized value the spec defines. The op result r is
+// quantized with the bracket of the relayout kernel: y = RN(r * RN(1/s)) lies within 2^-23 |y| of
+// r / s, and RN(r / s) within 2^-24 more, so when y(1 - 2^-22) and y(1 + 2^-22) round (the magic-constant
+// FMA, ties to even) to the same integer, so does RN(r / s). The host admits only parameters that keep
+// every |y| below 2^21 (the magic constant's range) and 1/s finite; a word with an undecided code goes
+// through the exact per-element path.
+struct QbConst {
+  float2 sl, sr, zl, zr;  // scales; -(1.5*2^23 + 128 + zero point) of each operand
+  float2 io, mo;          // RN(1 / result scale); 1.5*2^23 + result zero point
+  int smin, smax;
+};
+
+template <int OP>
+__device__ __forceinline__ float2 qop2(float2 a, float2 b) {
+  if (OP == QOP_ADD) return __fadd2_rn(a, b);
+  if (OP == QOP_MULTIPLY) return __fmul2_rn(a, b);
+  if (OP == QOP_MAXIMUM) return make_float2(ieee_max(a.x, b.x), ieee_max(a.y, b.y));
+  return make_float2(ieee_min(a.x, b.x), ieee_min(a.y, b.y));
+}
+
+// Four results for the codes of words a and b; sets `open` when a code is undecided.
+template <int OP, bool CLAMP>
+__device__ __forceinline__ uint32_t qb_word(uint32_t a, uint32_t b, const QbConst& k, bool& open) {
+  const float2 kp = make_float2(1.0f + 0x1p-22f, 1.0f + 0x1p-22f), km = make_float2(1.0f - 0x1p-22f, 1.0f - 0x1p-22f);
+  a ^= 0x80808080u;
+  b ^= 0x80808080u;
+  uint32_t hi = 0u, res = 0u, dw = 0u;
+#pragma unroll
+  for (int j = 2; j >= 0; j -= 2) {  // codes 2, 3 first: their pack is the upper half of the word
+    const float2 ea = make_float2(__uint_as_float(__byte_perm(a, (uint32_t)kMagicBits, 0x7650u | j)),
+                                  __uint_as_float(__byte_perm(a, (uint32_t)kMagicBits, 0x7650u | (j + 1))));
+    const float2 eb = make_float2(__uint_as_float(__byte_perm(b, (uint32_t)kMagicBits, 0x7650u | j)),
+                                  __uint_as_float(__byte_perm(b, (uint32_t)kMagicBits, 0x7650u | (j + 1))));
+    const float2 ra = __fmul2_rn(k.sl, __fadd2_rn(ea, k.zl));
+    const float2 rb = __fmul2_rn(k.sr, __fadd2_rn(eb, k.zr));
+    const float2 y = __fmul2_rn(qop2<OP>(ra, rb), k.io);
+    const float2 tp = __ffma2_rn(y, kp, k.mo), tm = __ffma2_rn(y, km, k.mo);
+    dw |= (__float_as_uint(tp.x) ^ __float_as_uint(tm.x)) | (__float_as_uint(tp.y) ^ __float_as_uint(tm.y));
+    int q0 = __float_as_int(tp.x) - kMagicBits, q1 = __float_as_int(tp.y) - kMagicBits;
+    if (CLAMP) {
+      q0 = min(max(q0, k.smin), k.smax);
+      q1 = min(max(q1, k.smin), k.smax);
+    }
+    if (j == 2) asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(q1), "r"(q0));
+    else asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(res) : "r"(q1), "r"(q0), "r"(hi));
+  }
+  open = dw != 0u;
+  return res;
+}
+
+template <int OP, bool CLAMP>
+__global__ void __launch_bounds__(256) quant_binary_pk_kernel(QuantBinaryPlan p, QbConst k) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nv = p.n / 16;
+  const uint4* l = reinterpret_cast<const uint4*>(p.lhs);
+  const uint4* r = reinterpret_cast<const uint4*>(p.rhs);
+  uint4* o = reinterpret_cast<uint4*>(p.out);
+  constexpr int kU = 2;  // vector pairs in flight per thread
+  for (int64_t v0 = tid; v0 < nv; v0 += kU * stride) {
+    uint4 a[kU], b[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nv) {
+        a[u] = __ldg(l + v);
+        b[u] = __ldg(r + v);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t v = v0 + u * stride;
+      if (v < nv) {
+        const uint32_t wa[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, wb[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+        uint32_t res[4];
+        bool open[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) res[m] = qb_word<OP, CLAMP>(wa[m], wb[m], k, open[m]);
+        if (open[0] | open[1] | open[2] | open[3]) {  // rare: the exact definition decides those words
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            if (open[m]) res[m] = qbin4<OP>(wa[m], wb[m], p);
+        }
+        o[v] = make_uint4(res[0], res[1], res[2], res[3]);
+      }
+    }
+  }
+  for (int64_t e = nv * 16 + tid; e < p.n; e += stride) p.out[e] = (int8_t)qbin<OP>(p.lhs[e], p.rhs[e], p);
+}
+
+// The packed kernel's constants, or false when the parameters fall outside its range: finite scales,
+// a finite nonzero RN(1/s), and |r / s| < 2^21 for every pair of codes.
+static bool qb_pk_consts(const QuantBinaryPlan& p, int op, QbConst& k) {
+  const double sl = std::fabs((double)p.ql.scale), sr = std::fabs((double)p.qr.scale);
+  const double io = std::fabs((double)p.qo.inv_scale);
+  if (!(sl < 1e30 && sr < 1e30 && io < 1e30 && io > 0.0)) return false;
+  const double da = 256.0 + std::fabs((double)p.ql.zp), db = 256.0 + std::fabs((double)p.qr.zp);  // |c - z|
+  double rmax = 0.0;
+  if (op == QOP_ADD) rmax = sl * da + sr * db;
+  else if (op == QOP_MULTIPLY) rmax = sl * da * sr * db;
+  else if (op == QOP_MAXIMUM || op == QOP_MINIMUM) rmax = std::max(sl * da, sr * db);
+  else return false;
+  if (!(rmax * io * 1.01 < 2097152.0)) return false;
+  auto negm = [](int32_t z) { return -(12582912.0f + 128.0f + (float)z); };  // exact for |z| < 2^22
+  if (std::abs((int64_t)p.ql.zp) > 1000000 || std::abs((int64_t)p.qr.zp) > 1000000 || std::abs((int64_t)p.qo.zp) > 1000000)
+    return false;
+  k.sl = make_float2(p.ql.scale, p.ql.scale);
+  k.sr = make_float2(p.qr.scale, p.qr.scale);
+  k.zl = make_float2(negm(p.ql.zp), negm(p.ql.zp));
+  k.zr = make_float2(negm(p.qr.zp), negm(p.qr.zp));
+  k.io = make_float2(p.qo.inv_scale, p.qo.inv_scale);
+  const float mo = 12582912.0f + (float)p.qo.zp;
+  k.mo = make_float2(mo, mo);
+  k.smin = p.qo.smin;
+  k.smax = p.qo.smax;
+  return true;
+}
+
+template <int OP>
+static cudaError_t qb_pk_launch(const QuantBinaryPlan& p, const QbConst& k, cudaStream_t s) {
+  const bool clamp = k.smin > -128 || k.smax < 127;
+  const void* kernel = clamp ? (const void*)quant_binary_pk_kernel<OP, true> : (const void*)quant_binary_pk_kernel<OP, false>;
+  int64_t blocks = (p.n / 32 + 255) / 256;
+  const int64_t cap = (int64_t)device_sm_count() * kernel_blocks_per_sm(kernel, 256, 0);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (clamp) quant_binary_pk_kernel<OP, true><<<(unsigned)blocks, 256, 0, s>>>(p, k);
+  else quant_binary_pk_kernel<OP, false><<<(unsigned)blocks, 256, 0, s>>>(p, k);
+  return cudaGetLastError();
 }
 
 // Large same-layout inputs: the result depends on the two codes alone, so it is read from a table of
@@ -156,6 +292,9 @@ template <int OP>
 static cudaError_t qb_launch(const QuantBinaryPlan& p, cudaStream_t s) {
   const bool same = p.lmap.identity && p.rmap.identity && p.omap.identity;
   const bool aligned = ((uintptr_t)p.lhs % 16 == 0) && ((uintptr_t)p.rhs % 16 == 0) && ((uintptr_t)p.out % 16 == 0);
+  QbConst k;
+  if (OP != QOP_DIVIDE && same && aligned && qb_pk_consts(p, OP, k))
+    return qb_pk_launch<OP == QOP_DIVIDE ? QOP_ADD : OP>(p, k, s);  // (no packed divide)
   if (same && aligned && p.n >= kQbTableMinElems) return qb_table_launch<OP>(p, s);
   const int64_t per = same && aligned ? 16 : 1;
   int64_t blocks = (p.n / per + 255) / 256;
