@@ -381,6 +381,21 @@ hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const 
 hlo_status hlo_device_faults(uint32_t* faults, int32_t clear);
 hlo_status hlo_selftest_bounded_wait(void* stream);
 
+/* ------------------------------------------------------------------------------------------------
+ * Generated chain kernels ("XLA:GPU Emitters", section "Loop emitter": one kernel is emitted per
+ * fusion, its elementwise ops as straight-line code). For an identity-layout transpose fusion on
+ * bf16 / f16 of 2^20 elements or more, 16-byte aligned, whose prologue rounds every op to the element
+ * type and uses only add / multiply by the input or a constant, negate, absolute value and (bf16)
+ * tanh, hlo_transpose_fusion writes the chain as CUDA source, compiles it once per device with NVRTC
+ * (opened with dlopen on first use) and launches the result; the results are the bits the library's
+ * other kernels give. If NVRTC cannot be opened or the source does not compile, the library's fixed
+ * kernels run the call instead.
+ *
+ * hlo_jit_kernels returns the number of chain kernels built so far for the current device, or -1 when
+ * NVRTC or the driver calls it needs are unavailable (no generated kernels will run).
+ * ---------------------------------------------------------------------------------------------- */
+int32_t hlo_jit_kernels(void);
+
 /* Thread-local description of the last error returned on this thread ("" if none). */
 const char* hlo_last_error(void);
 

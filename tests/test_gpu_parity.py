@@ -695,6 +695,24 @@ def test_chain_table_every_16bit_input(dtype, ops):
     check(f, run_gpu(f), ref, None)
 
 
+@pytest.mark.parametrize("dtype,ops", [
+    ("bf16", list(inp.GELU_CHAIN)),
+    ("bf16", ["neg", ("add_const", 0.75), "tanh", "abs", ("mul_const", -3.0), "mul_input"]),
+    ("f16", ["mul_input", ("add_const", -1.5), "neg", ("mul_const", 0.3), "add_input", "abs"]),
+])
+def test_generated_chain_kernels_every_16bit_input(dtype, ops):
+    """Chains of 2^20 elements or more that the run-time generator covers (hlo_jit_kernels counts the
+    kernels it built; -1 would mean NVRTC is unavailable on the GPU machine): every bit pattern 64 times over
+    plus a ragged tail and an odd element count, bit-exact against the oracle."""
+    pats = np.arange(1 << 16, dtype=np.uint16)
+    for tail in (13, 8):
+        data = np.concatenate([np.tile(pats, 64), pats[:tail]])
+        f = _chain_fusion(data, dtype, ops)
+        ref, _ = run_oracle(f)
+        check(f, run_gpu(f), ref, None)
+    assert hf.jit_kernels() >= 1
+
+
 def test_gelu_chain_f32_bit_exact():
     """The same GELU chain on f32 (every op, tanh included, correctly rounded on both sides): bit-exact."""
     g = np.random.default_rng(13)

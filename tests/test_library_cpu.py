@@ -25,7 +25,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:hlo_status|size_t|const char\*)\s+(hlo_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:hlo_status|size_t|int32_t|const char\*)\s+(hlo_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_binding_exports():

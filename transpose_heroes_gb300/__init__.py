@@ -36,7 +36,7 @@ EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_fusion_noalloc", "hlo_reduce_workspa
            "hlo_layout_convert",
            "hlo_quant_fusion", "hlo_quant_binary", "hlo_quant_broadcast_in_dim", "hlo_quant_reshape",
            "hlo_reduce_max_argmax", "hlo_device_faults",
-           "hlo_selftest_bounded_wait", "hlo_last_error", "hlo_version")
+           "hlo_selftest_bounded_wait", "hlo_jit_kernels", "hlo_last_error", "hlo_version")
 QUANT_BINARY_OPS = {"add": 0, "divide": 1, "maximum": 2, "minimum": 3, "multiply": 4}
 
 
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
             h.hlo_device_faults.restype = ctypes.c_int
             h.hlo_selftest_bounded_wait.argtypes = [vp]
             h.hlo_selftest_bounded_wait.restype = ctypes.c_int
+            h.hlo_jit_kernels.argtypes = []
+            h.hlo_jit_kernels.restype = ctypes.c_int32
             h.hlo_last_error.restype = ctypes.c_char_p
             h.hlo_version.restype = ctypes.c_char_p
             _lib = h
@@ -309,6 +311,11 @@ def device_faults(clear: bool = False) -> int:
     f = ctypes.c_uint32(0)
     _check(lib().hlo_device_faults(ctypes.byref(f), 1 if clear else 0))
     return int(f.value)
+
+
+def jit_kernels() -> int:
+    """hlo_jit_kernels: chain kernels generated for the current device (-1: NVRTC unavailable)."""
+    return int(lib().hlo_jit_kernels())
 
 
 def selftest_bounded_wait(stream=None) -> None:

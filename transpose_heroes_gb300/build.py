@@ -70,7 +70,7 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
         objs = list(ex.map(compile_one, srcs))
     if force or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

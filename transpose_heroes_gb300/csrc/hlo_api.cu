@@ -727,6 +727,8 @@ hlo_status hlo_selftest_bounded_wait(void* stream) {
   return cuda_status(launch_wait_selftest(as_stream(stream)), "bounded-wait self test launch");
 }
 
+int32_t hlo_jit_kernels(void) { return jit_chain_kernels(); }
+
 const char* hlo_last_error(void) { return g_err.c_str(); }
 
 const char* hlo_version(void) { return "hlofusion 0.1 (sm_103a)"; }

@@ -254,6 +254,15 @@ cudaError_t launch_copy(const void* in, void* out, int64_t nbytes, cudaStream_t 
 cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, const Chain& pro, const Chain& epi,
                                cudaStream_t s);
 
+// Run-time generated 16-bit chain kernels (jit_chain.cu): whether the generator writes this chain;
+// the launch (`used` false when no kernel could be built: the caller runs the interpreter); the number
+// of kernels built for the current device (-1 when NVRTC or the driver calls are unavailable).
+bool jit_chain_ok(const Chain& pro, const Chain& epi, int dt);
+cudaError_t launch_jit_chain(const void* in, void* out, int64_t n, int dt, const Chain& pro, cudaStream_t s, bool* used);
+int jit_chain_kernels();
+// Device address of the bf16 tanh table (k_elementwise.cu), or NULL.
+const void* tanh_table_address();
+
 // Device properties cached per device (SM count, cluster support).
 int device_sm_count();
 

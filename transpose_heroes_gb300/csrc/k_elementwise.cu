@@ -3,6 +3,9 @@
 // so that writes are coalesced, with vectorized loads and stores, section "Vectorization").
 #include <cooperative_groups.h>
 
+#include <map>
+#include <mutex>
+
 #include "device_common.cuh"
 
 namespace hlo {
@@ -369,6 +372,7 @@ static bool chain16x2_ok(const Chain& pro, const Chain& epi, int dt) {
 // memory); after the cluster barrier each block streams 16-byte vectors and looks every element up
 // locally. No global memory beyond input and output.
 constexpr int kLutThreads = 1024;
+constexpr int64_t kJitMinElems = int64_t(1) << 20;  // smaller chains stay with the interpreter kernels
 constexpr int kLutEntries = 1 << 16;
 constexpr int64_t kLutMinElems = int64_t(1) << 22;  // below this the direct kernels are faster
 
@@ -520,9 +524,33 @@ cudaError_t launch_copy(const void* in, void* out, int64_t nbytes, cudaStream_t 
   return cudaGetLastError();
 }
 
+const void* tanh_table_address() {
+  static std::mutex mu;
+  static std::map<int, const void*> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  void* p = nullptr;
+  const cudaError_t pending = cudaPeekAtLastError();
+  if (cudaGetSymbolAddress(&p, kTanhBf16) != cudaSuccess) {
+    p = nullptr;
+    if (pending == cudaSuccess) cudaGetLastError();  // the query's own error
+  }
+  cache[dev] = p;
+  return p;
+}
+
 cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, const Chain& pro, const Chain& epi,
                                cudaStream_t s) {
   if (n == 0) return cudaSuccess;
+  // large 16-bit chains the generator covers: a kernel written for the chain (jit_chain.cu)
+  if (n >= kJitMinElems && jit_chain_ok(pro, epi, dt) && (uintptr_t)in % 16 == 0 && (uintptr_t)out % 16 == 0) {
+    bool used = false;
+    const cudaError_t e = launch_jit_chain(in, out, n, dt, pro, s, &used);
+    if (e != cudaSuccess || used) return e;
+  }
   EwPlan p{in, out, n, dt, pro, epi};
   int64_t blocks = (n + 1023) / 1024;
   const int64_t cap = (int64_t)device_sm_count() * 8;
