@@ -68,28 +68,39 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_record(kernel_file_hash):
+def traffic_record():
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it was taken on
-    the current kernel source."""
+    the kernel's current source: the record lists the source files the kernel is built from (its
+    translation unit and the headers under csrc/) with their SHA-256, and every one must still match."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return None
-    if d.get("source_sha256") != kernel_file_hash:
+    files = d.get("source_files") or []
+    if not files or d.get("source_sha256") != source_hash(files):
         return None
     return d
 
 
-def source_hash():
+def kernel_sources(tu):
+    """The files a kernel's translation unit is built from: the .cu file and every header in csrc/."""
+    csrc = os.path.join(ROOT, "transpose_heroes_gb300", "csrc")
+    hs = sorted(n for n in os.listdir(csrc) if n.endswith((".cuh", ".h", ".inc")))
+    return [tu] + hs
+
+
+def source_hash(files):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transpose_heroes_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h", ".inc")):
+    for name in files:
+        try:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
+        except OSError:
+            return None
     return h.hexdigest()
 
 
@@ -344,7 +355,7 @@ def ours(args):
                          "elements_per_s": f.elements / (ms / 1e3)}
     dom = max(per, key=lambda k: per[k]["us"])
     dom_gbs = per[dom]["gbs"]
-    tr = traffic_record(source_hash())
+    tr = traffic_record()
     roofline = {"bound": "hbm", "kernel": per[dom]["kernel"], "fusion": dom, "achieved": dom_gbs, "peak": hbm,
                 "peak_source": peak_src, "unit": "GB/s", "frac": dom_gbs / hbm,
                 "traffic": (tr["dram_bytes_per_launch"] if tr and tr.get("fusion") == dom else None),
