@@ -53,9 +53,9 @@ NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed), "argmax_f32": l
              "quant_add_s8": lambda seed: inp.quant_add_s8(seed=seed),
              "transpose3_exp_abs_f32": lambda seed: inp.transpose3_exp_abs(seed=seed)}
 # kernel each fusion launches (for the launch list / roofline)
-KERNELS = {"row_reduce_exp": "row_reduce_kernel", "transpose_log": "selfadd_block_kernel",
+KERNELS = {"row_reduce_exp": "row_warp_kernel", "transpose_log": "selfadd_tma_kernel",
            "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",
-           "quant_relayout": "quant_tile_kernel"}
+           "quant_relayout": "quant_tma_kernel"}
 
 
 def peaks():
