@@ -396,6 +396,15 @@ hlo_status hlo_selftest_bounded_wait(void* stream);
  * ---------------------------------------------------------------------------------------------- */
 int32_t hlo_jit_kernels(void);
 
+/* ------------------------------------------------------------------------------------------------
+ * Fault injection for tests of the error path (no counterpart in the pages: the library's own test
+ * support). When the environment variable HLOFUSION_FAULT holds an entry point's name (for example
+ * "hlo_transpose_fusion") or "all", that entry point validates its arguments as usual and then returns
+ * HLO_ERR_CUDA, with "injected fault" in hlo_last_error(), before it enqueues any work. Calls that fail
+ * validation still report their own error. The variable is read on every call; unset or empty, nothing
+ * changes.
+ * ---------------------------------------------------------------------------------------------- */
+
 /* Thread-local description of the last error returned on this thread ("" if none). */
 const char* hlo_last_error(void);
 

@@ -360,3 +360,45 @@ def test_tanh_table_against_the_oracle():
     bf = lambda b: (b.astype(np.uint32) << 16).view(np.float32)
     same = (got == ref) | (np.isnan(bf(got)) & np.isnan(bf(ref)))
     assert same.all(), np.flatnonzero(~same)[:8]
+
+
+# ---- host-side fault injection (HLOFUSION_FAULT) -----------------------------------------------------------
+def _valid_calls():
+    """One valid call per entry point that enqueues work; the pointers are never dereferenced because
+    the injected fault returns before anything is launched."""
+    q = {"scales": np.float32([0.5]), "zero_points": np.int32([0]), "quantization_dimension": None,
+         "host_scales": np.float32([0.5]), "host_zero_points": np.int32([0]), "storage_min": -128, "storage_max": 127}
+    return {
+        "hlo_reduce_fusion": lambda: hf.reduce_fusion(FAKE_IN, [4, 5], "f32", [1], "add", 0.0, FAKE_OUT, "f32", stream=0),
+        "hlo_transpose_fusion": lambda: hf.transpose_fusion(FAKE_IN, [3, 4], "f32", [1, 0], FAKE_OUT, stream=0),
+        "hlo_layout_convert": lambda: hf.layout_convert(FAKE_IN, [3, 4], "f32", [1, 0], [0, 1], FAKE_OUT, stream=0),
+        "hlo_quant_binary": lambda: hf.quant_binary("add", FAKE_IN, FAKE_IN + 4096, [64], q, q, FAKE_OUT, q, stream=0),
+    }
+
+
+@pytest.mark.parametrize("site", ["hlo_reduce_fusion", "hlo_transpose_fusion", "hlo_layout_convert", "hlo_quant_binary"])
+def test_fault_injection_by_entry_point(lib, monkeypatch, site):
+    """HLOFUSION_FAULT=<entry point> makes that call return HLO_ERR_CUDA ("injected fault") after
+    validation and before any launch; an invalid call still reports its own validation error."""
+    calls = _valid_calls()
+    monkeypatch.setenv("HLOFUSION_FAULT", site)
+    st, msg = _status(calls[site])
+    assert st == 3 and "injected fault" in msg and site in msg
+    if site == "hlo_transpose_fusion":
+        st, msg = _status(lambda: hf.transpose_fusion(FAKE_IN, [3, 4], "f32", [0, 0], FAKE_OUT, stream=0))
+        assert st == 1 and "permutation" in msg
+    monkeypatch.setenv("HLOFUSION_FAULT", "all")
+    for name, call in calls.items():
+        st, msg = _status(call)
+        assert st == 3 and "injected fault" in msg and name in msg
+
+
+def test_fault_injection_names_one_site(lib, monkeypatch):
+    """A site names one entry point: with HLOFUSION_FAULT set to another, the call goes on past the
+    injection point (here, on a host without a GPU, to the CUDA runtime's own error)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the call would really launch on a GPU host")
+    monkeypatch.setenv("HLOFUSION_FAULT", "hlo_reduce_fusion")
+    st, msg = _status(_valid_calls()["hlo_transpose_fusion"])
+    assert "injected fault" not in msg

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
@@ -182,6 +183,17 @@ IndexMap make_map(const std::vector<int64_t>& size, const std::vector<int64_t>& 
 }
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Host-side fault injection, for tests of the error path that fault no GPU: when the environment
+// variable HLOFUSION_FAULT names an entry point (or is "all"), that entry point validates its arguments
+// as usual and then returns HLO_ERR_CUDA with an "injected fault" message before it enqueues anything.
+// The variable is read on every call; unset, it costs one getenv.
+bool injected(const char* site) {
+  const char* v = std::getenv("HLOFUSION_FAULT");
+  return v && *v && (std::strcmp(v, "all") == 0 || std::strcmp(v, site) == 0);
+}
+#define HLO_INJECT(site) \
+  if (injected(site)) return fail(HLO_ERR_CUDA, "%s: injected fault (HLOFUSION_FAULT)", site)
 
 // Rows and row length of a reduce whose reduced dimensions are the minor-most physical ones (unit
 // dimensions dropped); false for any other pattern.
@@ -471,6 +483,7 @@ hlo_status hlo_quant_binary(int32_t op, const hlo_array* lhs, const void* lhs_pt
       *maps[a] = make_map(sz, std::vector<int64_t>(str, str + lhs->rank));
     }
   }
+  HLO_INJECT("hlo_quant_binary");
   return cuda_status(launch_quant_binary(p, as_stream(stream)), "quantized op launch");
 }
 
@@ -565,6 +578,7 @@ hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const 
   p.kred = make_map(rsz, rk);
   p.init_value = constant_of_type(init_value, in->dtype);
   p.init_index = (int32_t)init_index;
+  HLO_INJECT("hlo_reduce_max_argmax");
   return cuda_status(launch_argmax(p, as_stream(stream)), "argmax launch");
 }
 
@@ -609,6 +623,7 @@ hlo_status hlo_quant_broadcast_in_dim(const hlo_array* operand, const void* oper
       ranges_overlap(result_zero_points, n_params * 4, result_ptr, n_out) ||
       ranges_overlap(result_scales, n_params * 4, result_zero_points, n_params * 4))
     return fail(HLO_ERR_INVALID_ARG, "quantized broadcast_in_dim: output buffers overlap an input or each other");
+  HLO_INJECT("hlo_quant_broadcast_in_dim");
   const cudaStream_t s = as_stream(stream);
   *result_quantization_dimension = rqd;
   cudaError_t e = rqd < 0 ? launch_quant_params(nullptr, nullptr, qp.scale, qp.zp, 1, result_scales,
@@ -705,6 +720,7 @@ hlo_status hlo_quant_reshape(const hlo_array* operand, const void* operand_ptr, 
     st2.push_back(ostr[d]);
   }
   p.lex_to_in = make_map(sz, st2);
+  HLO_INJECT("hlo_quant_reshape");
   const cudaStream_t s = as_stream(stream);
   if (p.out_to_lex.identity && p.lex_to_in.identity)
     return cuda_status(launch_copy(operand_ptr, result_ptr, n * eb, s), "copy launch");
@@ -788,6 +804,7 @@ hlo_status hlo_reduce_fusion(const hlo_array* in, const void* in_ptr, const hlo_
   if (n_out > 0 && !out_ptr) return fail(HLO_ERR_INVALID_ARG, "reduce: output pointer is NULL");
   if (ranges_overlap(in_ptr, n_in * dt_bytes(in->dtype), out_ptr, n_out * dt_bytes(out->dtype)))
     return fail(HLO_ERR_INVALID_ARG, "reduce: input and output overlap");
+  HLO_INJECT("hlo_reduce_fusion");
   const cudaStream_t s = as_stream(stream);
   // init_values has the inputs' element type ("reduce" C2): the literal is rounded to it
   const float init = constant_of_type(init_value, in->dtype);
@@ -988,6 +1005,7 @@ hlo_status hlo_transpose_fusion(const hlo_array* in, const void* in_ptr, const h
   if (n > 0 && (!in_ptr || !out_ptr)) return fail(HLO_ERR_INVALID_ARG, "transpose: NULL data pointer");
   if (ranges_overlap(in_ptr, bytes, out_ptr, bytes)) return fail(HLO_ERR_INVALID_ARG, "transpose: input and output overlap");
   if (n == 0) return ok();
+  HLO_INJECT("hlo_transpose_fusion");
   const cudaStream_t s = as_stream(stream);
   const bool bcast = chain_has_bcast(pro);
 
@@ -1081,6 +1099,7 @@ hlo_status hlo_layout_convert(const hlo_array* in, const void* in_ptr, const int
   if (st != HLO_OK) return st;
   int64_t perm[HLO_MAX_RANK];
   for (int k = 0; k < in->rank; ++k) perm[k] = k;
+  HLO_INJECT("hlo_layout_convert");
   return hlo_transpose_fusion(in, in_ptr, nullptr, perm, 0, nullptr, &out, out_ptr, stream);
 }
 
@@ -1119,6 +1138,7 @@ hlo_status hlo_quant_fusion(const hlo_array* in, const void* in_ptr, const hlo_q
   if (ranges_overlap(in_ptr, n, out_ptr, n * dt_bytes(out->dtype)))
     return fail(HLO_ERR_INVALID_ARG, "quant: input and output overlap");
   if (n == 0) return ok();
+  HLO_INJECT("hlo_quant_fusion");
   const cudaStream_t s = as_stream(stream);
 
   // fast path: two non-unit dims (i major, j minor in the input), output with i minor
@@ -1229,6 +1249,7 @@ extern "C" hlo_status hlo_reduce_fusion_noalloc(const hlo_array* in, const void*
                 "reduce_fusion_noalloc: this reduction needs %zu bytes of scratch, more than the %zu the library "
                 "keeps per device; use hlo_reduce_fusion with a workspace",
                 need, kNoAllocScratchBytes);
+  HLO_INJECT("hlo_reduce_fusion_noalloc");
   void* scratch = nullptr;
   if (need > 0) {
     const hlo_status st = noalloc_scratch(&scratch);
