@@ -439,7 +439,12 @@ __global__ void __launch_bounds__(256, 4)
   const float so = p.qout.scale, io = p.qout.inv_scale;
   const int zo = p.qout.zp, smin = p.qout.smin, smax = p.qout.smax;
   const float mo = kMagic + (float)zo;
-  const float2 kp = make_float2(1.0f + 0x1p-22f, 1.0f + 0x1p-22f), km = make_float2(1.0f - 0x1p-22f, 1.0f - 0x1p-22f);
+  // The product of the input scale and RN(1/scale_out) is formed once per parameter, so y = RN(d * P),
+  // d = code - z: P is within 2^-24 of s * RN(1/s_out), which is within 2^-24 of s / s_out, and the
+  // product and RN(s d) (the dequantized value) round once more each, so y lies within 4 * 2^-24 (plus
+  // second-order terms) of RN(s d) / s_out and 5 * 2^-24 of the IEEE quotient rounded: the bracket
+  // y(1 +- 2^-21) holds it with room.
+  const float2 kp = make_float2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f), km = make_float2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
   int64_t j = 0;
   for (int64_t item = blockIdx.x; item < n_tiles; item += gridDim.x, ++j) {
     const int st = (int)(j % kQStages);
@@ -465,6 +470,9 @@ __global__ void __launch_bounds__(256, 4)
       rs[k] = QIN == 0 ? ps[lane + 32 * k] : p.qin.scale;
       rz[k] = __int_as_float((kMagicBits + 128 + zz) | (int)0x80000000u);
     }
+    float rp[4];  // per row (or tensor): scale * RN(1/scale_out)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) rp[k] = __fmul_rn(rs[k], io);
     // the bracket needs finite parameters with |scale_in / scale_out| < 2^13: known from the host copies
     // when they were given, else checked on this thread's parameters
     bool bad;
@@ -491,10 +499,10 @@ __global__ void __launch_bounds__(256, 4)
         uint32_t hi[4], dw[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
         for (int b = 2; b >= 0; b -= 2) {  // codes 2, 3 first: their pack is the upper half of the word
-          float2 cs = make_float2(0.f, 0.f), cz = cs;
+          float2 cp = make_float2(0.f, 0.f), cz = cp;
           if (QIN == 1) {
             const int jl = 16 * w + 4 * m + b;
-            cs = *reinterpret_cast<const float2*>(&ps[jl]);
+            cp = __fmul2_rn(*reinterpret_cast<const float2*>(&ps[jl]), make_float2(io, io));
             const int2 zz = *reinterpret_cast<const int2*>(&pz[jl]);
             cz = make_float2(__int_as_float((kMagicBits + 128 + zz.x) | (int)0x80000000u),
                              __int_as_float((kMagicBits + 128 + zz.y) | (int)0x80000000u));
@@ -505,8 +513,7 @@ __global__ void __launch_bounds__(256, 4)
             const float2 e = make_float2(__uint_as_float(__byte_perm(wd, (uint32_t)kMagicBits, 0x7650u | b)),
                                          __uint_as_float(__byte_perm(wd, (uint32_t)kMagicBits, 0x7650u | (b + 1))));
             const float2 df = __fadd2_rn(e, QIN == 1 ? cz : make_float2(rz[k], rz[k]));
-            const float2 real = __fmul2_rn(QIN == 1 ? cs : make_float2(rs[k], rs[k]), df);
-            const float2 y = __fmul2_rn(real, make_float2(io, io));
+            const float2 y = __fmul2_rn(QIN == 1 ? cp : make_float2(rp[k], rp[k]), df);
             const float2 tp = __ffma2_rn(y, kp, make_float2(mo, mo)), tm = __ffma2_rn(y, km, make_float2(mo, mo));
             dw[k] |= (__float_as_uint(tp.x) ^ __float_as_uint(tm.x)) | (__float_as_uint(tp.y) ^ __float_as_uint(tm.y));
             int q0 = __float_as_int(tp.x) - kMagicBits, q1 = __float_as_int(tp.y) - kMagicBits;
@@ -518,8 +525,10 @@ __global__ void __launch_bounds__(256, 4)
             else asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(o[k][m]) : "r"(q1), "r"(q0), "r"(hi[k]));
           }
         }
+        if (dw[0] | dw[1] | dw[2] | dw[3]) {  // rare: mark the words with an undecided code
 #pragma unroll
-        for (int k = 0; k < 4; ++k) redo |= (dw[k] != 0u ? 1u : 0u) << (4 * k + m);
+          for (int k = 0; k < 4; ++k) redo |= (dw[k] != 0u ? 1u : 0u) << (4 * k + m);
+        }
       }
 #pragma unroll 1
       while (redo) {  // rare: the exact definition decides the word's four codes
