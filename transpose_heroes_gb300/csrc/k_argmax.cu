@@ -2,8 +2,9 @@
 // f(max, argmax, value, index) = (value, index) if value >= max else (max, argmax), from (I_V, I_K).
 //
 //  argmax_row_kernel -- the reduced walk is contiguous in memory: a block per output, threads take
-//                       16-byte vectors in turn and fold them in increasing position, then the block
-//                       combines the thread partials (warp shuffles + shared memory).
+//                       16-byte vectors in turn (four loads in flight, each folded into its own
+//                       partial in increasing position), then the partials combine in the thread and
+//                       the block (warp shuffles + shared memory).
 //  argmax_gen_kernel -- anything else: a thread per output walks the reduced positions in order
 //                       (adjacent threads read adjacent outputs' elements, so a reduced major
 //                       dimension streams coalesced).
@@ -68,8 +69,18 @@ __global__ void __launch_bounds__(256) argmax_row_kernel(ArgmaxPlan p, int vec) 
     Best b{p.init_value, -1};
     if (vec) {
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(p.v) + base * (DT == F32 ? 4 : 2));
-      const int64_t nv = p.n_red / E;
-      for (int64_t q = threadIdx.x; q < nv; q += blockDim.x) fold_vec<DT>(b, __ldg(src + q), q * E);
+      const int64_t nv = p.n_red / E, bd = blockDim.x;
+      Best b4[4] = {b, b, b, b};
+      int64_t q = threadIdx.x;
+      for (; q + 3 * bd < nv; q += 4 * bd) {
+        const uint4 w0 = __ldg(src + q), w1 = __ldg(src + q + bd), w2 = __ldg(src + q + 2 * bd), w3 = __ldg(src + q + 3 * bd);
+        fold_vec<DT>(b4[0], w0, q * E);
+        fold_vec<DT>(b4[1], w1, (q + bd) * E);
+        fold_vec<DT>(b4[2], w2, (q + 2 * bd) * E);
+        fold_vec<DT>(b4[3], w3, (q + 3 * bd) * E);
+      }
+      for (; q < nv; q += bd) fold_vec<DT>(b4[0], __ldg(src + q), q * E);  // later positions than b4[0] holds
+      b = later_max(later_max(b4[0], b4[1]), later_max(b4[2], b4[3]));
     } else {
       for (int64_t t = threadIdx.x; t < p.n_red; t += blockDim.x) fold(b, load_as_f32(p.v, DT, base + t), t);
     }
@@ -122,9 +133,12 @@ cudaError_t launch_argmax(const ArgmaxPlan& p, cudaStream_t s) {
       for (int j = 0; j < p.vkept.n; ++j) vec = vec && (p.vkept.stride[j] % E == 0);
       if (p.vkept.identity) vec = false;  // a stride of 1 between outputs is never a whole vector
     }
-    int64_t grid = p.n_out;
-    const int64_t cap = (int64_t)device_sm_count() * 8;
-    if (grid > cap) grid = cap;
+    // one wave of resident blocks, every block with the same number of outputs (give or take one)
+    const void* kernel = p.dt == F32 ? (const void*)argmax_row_kernel<F32>
+                         : p.dt == BF16 ? (const void*)argmax_row_kernel<BF16> : (const void*)argmax_row_kernel<F16>;
+    const int64_t cap = (int64_t)device_sm_count() * kernel_blocks_per_sm(kernel, 256, 0);
+    const int64_t per = (p.n_out + cap - 1) / cap;
+    const int64_t grid = (p.n_out + per - 1) / per;
     if (p.dt == F32) argmax_row_kernel<F32><<<(unsigned)grid, 256, 0, s>>>(p, vec ? 1 : 0);
     else if (p.dt == BF16) argmax_row_kernel<BF16><<<(unsigned)grid, 256, 0, s>>>(p, vec ? 1 : 0);
     else argmax_row_kernel<F16><<<(unsigned)grid, 256, 0, s>>>(p, vec ? 1 : 0);
