@@ -344,6 +344,18 @@ __device__ __forceinline__ void block_store(float* dst, int64_t n, const float4 
 // barrier), record kFaultCopyTimeout, wait (bounded) for its copies in flight and return.
 // ---------------------------------------------------------------------------------------------
 constexpr int kPairWarps = kPairThreads / 32;
+
+// Item k of block b in the walk: round-robin (k * G + b) for the `full` = n_items / G whole rounds;
+// the last, partial round goes to the blocks in reverse (G - 1 - b), so that the blocks that take an
+// extra item are the ones whose last whole round held a (half-cost) diagonal item. -1 past the block's
+// last item.
+__device__ __forceinline__ int64_t walk_item(int64_t b, int64_t k, int64_t g, int64_t n_items, int64_t full) {
+  if (k < full) return k * g + b;
+  if (k > full) return -1;
+  const int64_t it = full * g + (g - 1 - b);
+  return it < n_items ? it : -1;
+}
+
 template <int NS>
 struct TmaShared {
   uint16_t wlist[kPairWarps][kWarpList];
@@ -436,6 +448,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
   TmaShared<NS>& ts = *reinterpret_cast<TmaShared<NS>*>(s_le + HLO_LOG_NE);
   __shared__ float l1[96];  // first-pass log table (inv_c, log(c)_hi, log(c)_lo), at a static address
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t full = n_items / gridDim.x;  // whole rounds of the walk (one division per thread)
   // copies item `it` (walk position j) into stage j % NS and records its tile pair there
   auto issue = [&](int64_t it, int64_t j) {
     int64_t I, J;
@@ -457,8 +470,8 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
     for (int w = 0; w < kPairWarps; ++w) ts.wcount[w] = 0;
     fence_mbar_init();
     for (int64_t j = 0; j < NS; ++j) {
-      const int64_t it = blockIdx.x + j * gridDim.x;
-      if (it < n_items) issue(it, j);
+      const int64_t it = walk_item(blockIdx.x, j, gridDim.x, n_items, full);
+      if (it >= 0) issue(it, j);
     }
   }
   load_log_tables(s_lc, s_le);
@@ -474,7 +487,9 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
   const int64_t goff = 4 * bi * n + 4 * bj;
   uint16_t* wl = ts.wlist[warp];
   int64_t j = 0;
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
+  for (;; ++j) {
+    const int64_t item = walk_item(blockIdx.x, j, gridDim.x, n_items, full);
+    if (item < 0) break;
     const int st = (int)(j % NS);
     const bool arrived = mbar_wait(smem_addr(&ts.full[st]), (uint32_t)((j / NS) & 1));
     const int2 ij = ts.ij[st];
@@ -492,7 +507,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
       // in flight (items j .. j + NS - 1), leave the rest of its outputs unwritten and return
       if (tid == 0) {
         record_fault(kFaultCopyTimeout);
-        for (int64_t q = j; q < j + NS && blockIdx.x + q * gridDim.x < n_items; ++q)
+        for (int64_t q = j; q < j + NS && walk_item(blockIdx.x, q, gridDim.x, n_items, full) >= 0; ++q)
           mbar_wait(smem_addr(&ts.full[q % NS]), (uint32_t)((q / NS) & 1));
       }
       return;
@@ -525,8 +540,8 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
       __threadfence_block();
       if (atomicAdd(&ts.done[st], 1) == kPairWarps - 1) {
         ts.done[st] = 0;
-        const int64_t nxt = item + (int64_t)NS * gridDim.x;
-        if (nxt < n_items) {
+        const int64_t nxt = walk_item(blockIdx.x, j + NS, gridDim.x, n_items, full);
+        if (nxt >= 0) {
           fence_proxy_async();
           issue(nxt, j + NS);
         }
