@@ -450,9 +450,18 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t full = n_items / gridDim.x;  // whole rounds of the walk (one division per thread)
   // copies item `it` (walk position j) into stage j % NS and records its tile pair there
-  auto issue = [&](int64_t it, int64_t j) {
-    int64_t I, J;
-    item_pair(it, nt, n_off, I, J);
+  // The tile pairs of the block's items, worked out 64 walk positions at a time (chunk c: positions
+  // 64c .. 64c + 63, in set c % 2) by 64 threads, so that a refill does no index arithmetic. Chunk c + 1
+  // is planned at position 64c, before that item's barrier; the refills reading chunk c - 1 (the other
+  // use of its set) all come before the previous item's barrier ends.
+  __shared__ int2 s_pairs[2][64];
+  auto plan_pairs = [&](int64_t c, int t) {  // thread t of 64 plans position 64c + t
+    const int64_t it = walk_item(blockIdx.x, 64 * c + t, gridDim.x, n_items, full);
+    int64_t I = -1, J = -1;
+    if (it >= 0) item_pair(it, nt, n_off, I, J);
+    s_pairs[c & 1][t] = make_int2((int)I, (int)J);
+  };
+  auto issue = [&](int64_t I, int64_t J, int64_t j) {
     const int st = (int)(j % NS);
     ts.ij[st] = make_int2((int)I, (int)J);
     const uint32_t bar = smem_addr(&ts.full[st]);
@@ -471,11 +480,16 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
     fence_mbar_init();
     for (int64_t j = 0; j < NS; ++j) {
       const int64_t it = walk_item(blockIdx.x, j, gridDim.x, n_items, full);
-      if (it >= 0) issue(it, j);
+      int64_t I, J;
+      if (it >= 0) {
+        item_pair(it, nt, n_off, I, J);
+        issue(I, J, j);
+      }
     }
   }
   load_log_tables(s_lc, s_le);
   load_log1_tables(l1, l1 + 32, l1 + 64);
+  if (tid < 128) plan_pairs(tid >> 6, tid & 63);  // chunks 0 and 1
   __syncthreads();
   const LogTab lt = {s_lc, s_le};
   float* out = reinterpret_cast<float*>(p.out);
@@ -490,6 +504,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
   for (;; ++j) {
     const int64_t item = walk_item(blockIdx.x, j, gridDim.x, n_items, full);
     if (item < 0) break;
+    if ((j & 63) == 0 && j > 0 && tid < 64) plan_pairs((j >> 6) + 1, tid);
     const int st = (int)(j % NS);
     const bool arrived = mbar_wait(smem_addr(&ts.full[st]), (uint32_t)((j / NS) & 1));
     const int2 ij = ts.ij[st];
@@ -540,10 +555,10 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
       __threadfence_block();
       if (atomicAdd(&ts.done[st], 1) == kPairWarps - 1) {
         ts.done[st] = 0;
-        const int64_t nxt = walk_item(blockIdx.x, j + NS, gridDim.x, n_items, full);
-        if (nxt >= 0) {
+        const int2 pr = s_pairs[((j + NS) >> 6) & 1][(j + NS) & 63];  // item j + NS, planned earlier
+        if (pr.x >= 0) {
           fence_proxy_async();
-          issue(nxt, j + NS);
+          issue(pr.x, pr.y, j + NS);
         }
       }
     }
