@@ -149,7 +149,8 @@ __device__ __forceinline__ float comp4(const float4& v, int k) {
 
 // PK: 0 -- no chains; 1 -- chains interpreted at run time; 2 -- the prologue is exactly exp (evaluated
 // inline, its rare second and third passes out of line), the epilogue interpreted at run time.
-enum TileChains : int { TK_NONE = 0, TK_RT = 1, TK_EXP = 2 };
+// TK_EXP: the prologue is exactly exp (evaluated inline); TK_EXP_ABS: that, and the epilogue exactly abs
+enum TileChains : int { TK_NONE = 0, TK_RT = 1, TK_EXP = 2, TK_EXP_ABS = 3 };
 template <int PK>
 __global__ void __launch_bounds__(256, 3)
     tile_tma_kernel(const __grid_constant__ CUtensorMap tmap, TilePlan p, int64_t nta, int64_t ntb, int64_t n_items) {
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(256, 3)
 #pragma unroll 1
     for (int k = 0; k < 4; ++k) {
       float4 v = *reinterpret_cast<const float4*>(tile + raw + k * kTM);
-      if (PK == TK_EXP) {  // two packed first passes; open arguments (about 1 in 2000) finish out of line
+      if (PK == TK_EXP || PK == TK_EXP_ABS) {  // two packed first passes; open ones (~1 in 2000) out of line
         float4 y;
         bool ok[4];
         cr_expf_first2(v.x, v.y, y.x, y.y, ok[0], ok[1]);
@@ -282,7 +283,8 @@ __global__ void __launch_bounds__(256, 3)
         const int64_t a = ti.a0 + 4 * bi + k;
         if (a >= na) break;
         float4 o = make_float4(comp4(b[0], k), comp4(b[1], k), comp4(b[2], k), comp4(b[3], k));
-        if (CHAINS && p.epi.n) o = apply_chain4(p.epi, o, lt);
+        if (PK == TK_EXP_ABS) o = make_float4(fabsf(o.x), fabsf(o.y), fabsf(o.z), fabsf(o.w));
+        else if (CHAINS && p.epi.n) o = apply_chain4(p.epi, o, lt);
         *reinterpret_cast<float4*>(out + ti.obase + a * soa + b_first) = o;
       }
     }
@@ -340,7 +342,11 @@ cudaError_t launch_tile_transpose(const TilePlan& p, cudaStream_t s) {
     const int64_t nta64 = (p.size[p.ax_a] + kTM - 1) / kTM, ntb64 = (p.size[p.ax_b] + kTM - 1) / kTM;
     const int64_t items = nta64 * ntb64 * p.n_batch;
     const bool exp_pro = p.pro.n == 1 && p.pro.op[0] == OP_EXP;
-    auto kernel = !chains ? tile_tma_kernel<TK_NONE> : exp_pro ? tile_tma_kernel<TK_EXP> : tile_tma_kernel<TK_RT>;
+    const bool abs_epi = p.epi.n == 1 && p.epi.op[0] == OP_ABS;
+    auto kernel = !chains               ? tile_tma_kernel<TK_NONE>
+                  : exp_pro && abs_epi ? tile_tma_kernel<TK_EXP_ABS>
+                  : exp_pro            ? tile_tma_kernel<TK_EXP>
+                                       : tile_tma_kernel<TK_RT>;
     const size_t smem = tile_tma_smem_bytes();
     const int nb = kernel_blocks_per_sm((const void*)kernel, 256, smem);
     int64_t grid = (int64_t)device_sm_count() * nb;
