@@ -119,6 +119,35 @@ def test_full_size_configs(name):
     assert oracle.unresolved_count() == 0
 
 
+def test_selfadd_beyond_2_to_31_elements():
+    """The self-add transpose on f32[46404, 46404]: 2.15e9 elements, past every 32-bit element count and
+    byte offset, with a ragged last tile row and column. 6144 sampled outputs (a third of them in the
+    ragged tiles) against the oracle's correctly rounded logs, and bitwise symmetry on them."""
+    n = 46404
+    g = inp.rng(77)
+    x = torch.empty(n * n, dtype=torch.float32, device="cuda")
+    chunk = 1 << 26
+    for s in range(0, n * n, chunk):
+        m = min(chunk, n * n - s)
+        x[s:s + m].copy_(torch.from_numpy(inp.uniform_f32(g, m, 0.5, 2.0)))
+    y = torch.empty_like(x)
+    hf.transpose_fusion(x, [n, n], "f32", [1, 0], y, self_add=True, prologue={"ops": ["log"]})
+    torch.cuda.synchronize()
+    rs = np.random.default_rng(78)
+    i = np.concatenate([rs.integers(0, n, 4096), rs.integers(n - 70, n, 1024), rs.integers(0, n, 1024)])
+    j = np.concatenate([rs.integers(0, n, 4096), rs.integers(0, n, 1024), rs.integers(n - 70, n, 1024)])
+    ij = torch.from_numpy(i * n + j).cuda()
+    ji = torch.from_numpy(j * n + i).cuda()
+    pij, pji = x[ij].cpu().numpy(), x[ji].cpu().numpy()
+    out_ij, out_ji = y[ij].cpu().numpy(), y[ji].cpu().numpy()
+    ref = np.array([np.float32(oracle.log(a, "f32")) + np.float32(oracle.log(b, "f32")) for a, b in zip(pij, pji)],
+                   dtype=np.float32)
+    assert np.array_equal(out_ij.view(np.uint32), ref.view(np.uint32))
+    assert np.array_equal(out_ij.view(np.uint32), out_ji.view(np.uint32))
+    del x, y
+    torch.cuda.empty_cache()
+
+
 # ---- more shapes through the same kernels -----------------------------------------------------------
 @pytest.mark.parametrize("rows,cols", [(1, 1), (1, 7), (5, 3), (3, 4096 + 8), (2, 100003), (1000, 24)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
