@@ -148,6 +148,65 @@ def test_selfadd_beyond_2_to_31_elements():
     torch.cuda.empty_cache()
 
 
+def _fill_device(n, make, dtype):
+    """A device buffer of n elements filled chunk by chunk from a host generator."""
+    x = torch.empty(n, dtype=dtype, device="cuda")
+    chunk = 1 << 26
+    for s in range(0, n, chunk):
+        m = min(chunk, n - s)
+        x[s:s + m].copy_(torch.from_numpy(make(m)))
+    return x
+
+
+def test_col_reduce_beyond_2_to_31_elements():
+    """Column reduce-max over bf16[65540, 32768] (2.15e9 elements): 64 sampled columns, the last ones
+    among them, against the oracle on the same columns."""
+    rows, cols = 65540, 32768
+    g = inp.rng(79)
+    x = _fill_device(rows * cols, lambda m: inp.normal_bf16(g, m).view(np.int16), torch.int16)
+    out = torch.empty(cols, dtype=torch.int16, device="cuda")
+    hf.reduce_fusion(x, [rows, cols], "bf16", [0], "max", float("-inf"), out, "bf16")
+    torch.cuda.synchronize()
+    cs = np.concatenate([np.random.default_rng(80).integers(0, cols, 56), np.arange(cols - 8, cols)])
+    sub = x.view(rows, cols)[:, torch.from_numpy(cs).cuda()].contiguous().cpu().numpy().view(np.uint16)
+    ref = oracle.reduce(sub.reshape(-1), [rows, len(cs)], "bf16", [0], "max", float("-inf"), "bf16")
+    assert np.array_equal(out.cpu().numpy().view(np.uint16)[cs], ref.view(np.uint16))
+    del x
+    torch.cuda.empty_cache()
+
+
+def test_quant_relayout_beyond_2_to_31_elements():
+    """Per-axis dequantize -> {0,1} -> quantize on s8[46464, 46464] (2.16e9 codes, tensor-copy tiles):
+    4096 sampled codes against the oracle's per-element dequantize and quantize."""
+    n = 46464
+    g = inp.rng(81)
+    x = _fill_device(n * n, lambda m: inp.integers(g, m, -128, 127, np.int8), torch.int8)
+    scales = inp.uniform_f32(g, n, 0.001, 0.1)
+    zps = inp.integers(g, n, -20, 20, np.int32)
+    qin = {"scales": torch.from_numpy(scales).cuda(), "zero_points": torch.from_numpy(zps).cuda(),
+           "host_scales": scales, "host_zero_points": zps, "quantization_dimension": 1,
+           "storage_min": -128, "storage_max": 127}
+    qout = {"scales": np.float32([0.05]), "zero_points": np.int32([0]), "host_scales": np.float32([0.05]),
+            "host_zero_points": np.int32([0]), "quantization_dimension": None, "storage_min": -128, "storage_max": 127}
+    y = torch.empty(n * n, dtype=torch.int8, device="cuda")
+    hf.quant_fusion(x, [n, n], qin, [0, 1], y, out_dtype="s8", out_q=qout)
+    torch.cuda.synchronize()
+    rs = np.random.default_rng(82)
+    i = np.concatenate([rs.integers(0, n, 3072), np.full(1024, n - 1)])
+    j = np.concatenate([rs.integers(0, n, 3072), rs.integers(0, n, 1024)])
+    codes = x[torch.from_numpy(i * n + j).cuda()].cpu().numpy()
+    got = y[torch.from_numpy(j * n + i).cuda()].cpu().numpy()  # output element [i, j] sits at j*n + i
+    in_spec = {"scales": scales, "zero_points": zps, "quantization_dimension": 1, "storage_min": -128,
+               "storage_max": 127}
+    out_spec = {"scales": np.float32([0.05]), "zero_points": np.int32([0]), "quantization_dimension": None,
+                "storage_min": -128, "storage_max": 127}
+    ref = np.array([oracle.quantize(out_spec, oracle.dequantize(in_spec, int(c), [int(a), int(b)]))
+                    for c, a, b in zip(codes, i, j)])
+    assert np.array_equal(got.astype(np.int64), ref.astype(np.int64))
+    del x, y
+    torch.cuda.empty_cache()
+
+
 # ---- more shapes through the same kernels -----------------------------------------------------------
 @pytest.mark.parametrize("rows,cols", [(1, 1), (1, 7), (5, 3), (3, 4096 + 8), (2, 100003), (1000, 24)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
