@@ -207,6 +207,32 @@ def test_quant_relayout_beyond_2_to_31_elements():
     torch.cuda.empty_cache()
 
 
+def test_bcast_exp_row_reduce_beyond_2_to_31_elements():
+    """add(exp(x), broadcast(b)) reduced along rows of bf16[131080, 16384] (2.15e9 elements, the
+    streaming row kernel): 32 sampled rows, the last ones among them, against the oracle within the
+    reduction tolerance."""
+    rows, cols = 131080, 16384
+    g = inp.rng(83)
+    x = _fill_device(rows * cols, lambda m: inp.normal_bf16(g, m).view(np.int16), torch.int16)
+    b = inp.uniform_bf16(g, cols, -1.0, 1.0)
+    bd = torch.from_numpy(b.view(np.int16)).cuda()
+    out = torch.empty(rows, dtype=torch.float32, device="cuda")
+    pro = {"ops": ["exp", "add_bcast"], "round_each": True,
+           "bcast": {"tensor": bd, "dims": [cols], "dtype": "bf16", "broadcast_dimensions": [1]}}
+    hf.reduce_fusion(x, [rows, cols], "bf16", [1], "add", 0.0, out, "f32", prologue=pro)
+    torch.cuda.synchronize()
+    rs = np.concatenate([np.random.default_rng(84).integers(0, rows, 28), np.arange(rows - 4, rows)])
+    sub = x.view(rows, cols)[torch.from_numpy(rs).cuda()].contiguous().cpu().numpy().view(np.uint16)
+    opro = {"ops": ["exp", "add_bcast"], "round_each": True,
+            "bcast": {"data": b, "dims": [cols], "m2m": [0], "dtype": "bf16", "broadcast_dimensions": [1]}}
+    ref, asum = oracle.reduce(sub.reshape(-1), [len(rs), cols], "bf16", [1], "add", 0.0, "f32", prologue=opro,
+                              want_abs_sum=True)
+    got = out.cpu().numpy()[rs].astype(np.float64)
+    assert np.all(np.abs(got - ref.astype(np.float64)) <= 1e-5 * asum + 1e-6)
+    del x
+    torch.cuda.empty_cache()
+
+
 # ---- more shapes through the same kernels -----------------------------------------------------------
 @pytest.mark.parametrize("rows,cols", [(1, 1), (1, 7), (5, 3), (3, 4096 + 8), (2, 100003), (1000, 24)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
