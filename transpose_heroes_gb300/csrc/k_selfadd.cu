@@ -264,15 +264,15 @@ __global__ void __launch_bounds__(kPairThreads, 4)
 //   1. it reads its block of tile A = (I,J) and of tile B = (J,I) (four 16-byte reads each), applies
 //      the prologue in registers and writes the blocks back, 16-byte chunk c of row r at chunk
 //      c ^ ((r / 4) % 8) of that row;
-//   2. its warp settles the log elements the first pass left open (a per-warp list, so no block-wide
-//      wait stands between the first pass and the settling);
+//   2. the block settles the log elements the first pass left open (one block list, a barrier, then
+//      one open element per thread);
 //   3. after a barrier it reads its block of A and block (bj, bi) of B, both as four 16-byte reads that
 //      hit 32 distinct banks per quarter-warp, transposes the latter in registers and writes block
 //      (bi, bj) of out(I,J) = A + B^T with four 16-byte stores; then out(J,I) = B + A^T alike.
 // Every element is read once, goes through the prologue once, is written to and read from shared
 // memory with one 16-byte access each way, and is stored once.
 // ---------------------------------------------------------------------------------------------
-constexpr int kWarpList = 64;
+constexpr int kBlockList = 512;  // open log elements a block settles together per item (about 150 expected)
 
 __device__ __forceinline__ float comp(const float4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
@@ -335,11 +335,12 @@ __device__ __forceinline__ void block_store(float* dst, int64_t n, const float4 
 //   wait for the stage's mbarrier; then per tile: 16-byte reads of the raw rows (a quarter warp reads
 //   128 contiguous bytes), the prologue in registers, __syncwarp, 16-byte writes of the results to
 //   the swizzled positions. A thread's swizzled chunk lies in its own four rows, which only its own
-//   half warp reads, so the warp-level sync orders the in-place rewrite; then the warp settles its
-//   open log elements; block barrier; transposed reads, add, 16-byte stores.
+//   half warp reads, so the warp-level sync orders the in-place rewrite; then the block settles its
+//   open log elements (a barrier between the list and the settling); block barrier; transposed reads,
+//   add, 16-byte stores.
 // After its stores each warp counts itself done with the stage; the last of the 8 warps refills the
 // stage with the block's item j + NS at once (it also records the item's tile pair for the readers),
-// so the copies run about NS - 1 items ahead of use and one block barrier per item suffices.
+// so the copies run about NS - 1 items ahead of use.
 // A bounded wait that runs out makes the whole block stop (the decision is made block-wide at the
 // barrier), record kFaultCopyTimeout, wait (bounded) for its copies in flight and return.
 // ---------------------------------------------------------------------------------------------
@@ -358,8 +359,8 @@ __device__ __forceinline__ int64_t walk_item(int64_t b, int64_t k, int64_t g, in
 
 template <int NS>
 struct TmaShared {
-  uint16_t wlist[kPairWarps][kWarpList];
-  int wcount[kPairWarps];  // fill of each warp's settle list
+  uint16_t blist[kBlockList];  // stage slots of the item's open log elements
+  int bcount[2];               // fill of the list, by item parity (one is cleared while the other fills)
   int done[NS];            // warps done with the stage's current item
   int2 ij[NS];             // tile pair (I, J) of the stage's current item
   uint64_t full[NS];
@@ -405,27 +406,26 @@ __device__ __forceinline__ void tma_tile_prologue(float* tile, int raw, int own,
   for (int k = 0; k < 4; ++k) *reinterpret_cast<float4*>(tile + own + k * kT) = v[k];
 }
 
-// Settles the warp's open log elements in the stage (their slots hold the input): each lane with open
-// elements reserves room in the warp's list with one shared atomic, the list is shared out one element
-// per lane, and a lane whose elements did not fit settles the rest itself.
-__device__ __forceinline__ void warp_settle_list(uint32_t open, float* tiles, int own, uint16_t* wl, int* wcount,
-                                                 const LogTab& lt) {
-  const int lane = threadIdx.x & 31;
+// Settles the block's open log elements of item j in the stage (their slots hold the input): each lane
+// with open elements reserves room in the block's list with one shared atomic, a block barrier, then
+// the list is shared out one element per thread (one correctly rounded log each, about 150 of them on
+// U(0.5, 2) inputs: five warps' worth instead of a round in each of the eight warps), and a lane whose
+// elements did not fit settles the rest itself. The list's count alternates by item parity: the count
+// of item j + 1 is cleared here, after every thread has added to item j's and read item j - 1's.
+__device__ __forceinline__ void block_settle_list(uint32_t open, float* tiles, int own, uint16_t* bl, int* bcount,
+                                                  int64_t j, const LogTab& lt) {
   const int cnt = __popc(open);
-  int pos = cnt ? atomicAdd(wcount, cnt) : 0;
-  __syncwarp();
-  const int total = *wcount;
-  if (total == 0) return;  // warp-uniform
-  while (open && pos < kWarpList) {
+  int pos = cnt ? atomicAdd(&bcount[j & 1], cnt) : 0;
+  while (open && pos < kBlockList) {
     const int b = __ffs(open) - 1;
     open &= open - 1;
-    wl[pos++] = (uint16_t)((b >> 4) * (kT * kT) + own + ((b >> 2) & 3) * kT + (b & 3));
+    bl[pos++] = (uint16_t)((b >> 4) * (kT * kT) + own + ((b >> 2) & 3) * kT + (b & 3));
   }
-  __syncwarp();  // the list and the parked inputs are visible to the whole warp
-  if (lane == 0) *wcount = 0;  // read by every lane above; next written after this warp's next prologue
-  const int listed = total < kWarpList ? total : kWarpList;
-  for (int j = lane; j < listed; j += 32) {
-    float* sl = tiles + wl[j];
+  __syncthreads();  // the list and the parked inputs are visible to the whole block
+  const int total = min(bcount[j & 1], kBlockList);
+  if (threadIdx.x == 0) bcount[(j + 1) & 1] = 0;
+  for (int q = threadIdx.x; q < total; q += kPairThreads) {
+    float* sl = tiles + bl[q];
     *sl = cr_logf(*sl, lt.c, lt.e);
   }
   while (open) {
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
   float2* s_le = reinterpret_cast<float2*>(s_lc + HLO_LOG_NC);
   TmaShared<NS>& ts = *reinterpret_cast<TmaShared<NS>*>(s_le + HLO_LOG_NE);
   __shared__ float l1[96];  // first-pass log table (inv_c, log(c)_hi, log(c)_lo), at a static address
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int64_t full = n_items / gridDim.x;  // whole rounds of the walk (one division per thread)
   // copies item `it` (walk position j) into stage j % NS and records its tile pair there
   // The tile pairs of the block's items, worked out 64 walk positions at a time (chunk c: positions
@@ -476,7 +476,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
       mbar_init(smem_addr(&ts.full[st]), 1);
       ts.done[st] = 0;
     }
-    for (int w = 0; w < kPairWarps; ++w) ts.wcount[w] = 0;
+    ts.bcount[0] = ts.bcount[1] = 0;
     fence_mbar_init();
     for (int64_t j = 0; j < NS; ++j) {
       const int64_t it = walk_item(blockIdx.x, j, gridDim.x, n_items, full);
@@ -499,7 +499,6 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
   const int oth = 4 * bj * kT + ((bi ^ (bj & 7)) << 2);  // row 4*bj, chunk bi (swizzled)
   const int raw = 4 * bi * kT + 4 * bj;                  // row 4*bi, columns 4*bj.. of a raw tile
   const int64_t goff = 4 * bi * n + 4 * bj;
-  uint16_t* wl = ts.wlist[warp];
   int64_t j = 0;
   for (;; ++j) {
     const int64_t item = walk_item(blockIdx.x, j, gridDim.x, n_items, full);
@@ -515,7 +514,7 @@ __global__ void __launch_bounds__(kPairThreads, NS == 2 ? 3 : 2)
     uint32_t open = 0;
     tma_tile_prologue<CH>(ta, raw, own, p, lt, l1, open, 0);
     if (two) tma_tile_prologue<CH>(tb, raw, own, p, lt, l1, open, 16);
-    if (CH == PC_LOG) warp_settle_list(open, ta, own, wl, &ts.wcount[warp], lt);
+    if (CH == PC_LOG) block_settle_list(open, ta, own, ts.blist, ts.bcount, j, lt);
     // every tile of item j is complete
     if (__syncthreads_or(arrived ? 0 : 1)) {
       // a copy did not arrive in time: record the fault, wait (bounded) for this block's copies still
