@@ -363,13 +363,17 @@ hlo_status hlo_reduce_max_argmax(const hlo_array* in, const void* in_ptr, const 
 /* ------------------------------------------------------------------------------------------------
  * Device-side faults. A kernel that gives up on a bounded wait records a fault bit in a word the
  * library keeps on each device (no counterpart in the pages: this is the library's own diagnostics).
- *   HLO_FAULT_COPY_TIMEOUT  the streaming row reduce waited about one second for an asynchronous
- *                           global -> shared copy without seeing it complete; that block stopped,
- *                           waited (again with a bound) for its copies in flight, wrote NaN to its
- *                           output rows and returned, so the launch itself still reports success.
+ *   HLO_FAULT_COPY_TIMEOUT  a kernel that streams tiles through shared memory (the streaming row
+ *                           reduce, the tensor-copy transposes, the quantized relayout, the generated
+ *                           chain kernels) waited about one second for an asynchronous global -> shared
+ *                           copy without seeing it complete; that block stopped, waited (again with a
+ *                           bound) for its copies in flight and returned without writing the rest of
+ *                           its outputs (the streaming row reduce writes NaN to its rows), so the
+ *                           launch itself still reports success.
  *
  * hlo_device_faults waits for all work on the current device (cudaDeviceSynchronize), then stores the
- * fault bits recorded there since the last clear in *faults (0: none) and, if clear != 0, resets them.
+ * fault bits recorded there since the last clear, by any of the library's kernels, in *faults (0: none)
+ * and, if clear != 0, resets them.
  * HLO_ERR_CUDA if the device reports an error.
  *
  * hlo_selftest_bounded_wait enqueues one block that waits, bounded to about a millisecond, on a barrier

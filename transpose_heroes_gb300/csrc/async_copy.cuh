@@ -22,13 +22,16 @@ static __device__ unsigned int g_tu_faults;
 
 __device__ __forceinline__ void record_fault(unsigned int bits) { atomicOr(&g_tu_faults, bits); }
 
-// Host side: waits for the device, copies this unit's fault word out and optionally clears it.
+// Host side: copies this unit's fault word out and optionally clears it (the caller has waited for the
+// device). Every unit that includes this header registers it when the library is loaded, so
+// hlo_device_faults reads the words of all of them.
 static inline cudaError_t read_tu_faults(unsigned int* faults, bool clear) {
   cudaError_t e = cudaMemcpyFromSymbol(faults, g_tu_faults, sizeof(unsigned int));
   if (e != cudaSuccess || !clear) return e;
   const unsigned int zero = 0;
   return cudaMemcpyToSymbol(g_tu_faults, &zero, sizeof zero);
 }
+static const int g_tu_fault_reader_index = register_fault_reader(&read_tu_faults);
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -431,6 +431,31 @@ int hlo::kernel_blocks_per_sm(const void* kernel, int threads, size_t smem) {
   return nb;
 }
 
+namespace hlo {
+namespace {
+std::vector<FaultReader>& fault_readers() {
+  static std::vector<FaultReader> readers;  // filled while the library's units are initialised
+  return readers;
+}
+}  // namespace
+
+int register_fault_reader(FaultReader r) {
+  fault_readers().push_back(r);
+  return static_cast<int>(fault_readers().size()) - 1;
+}
+
+cudaError_t read_all_faults(unsigned int* faults, bool clear) {
+  *faults = 0;
+  for (FaultReader r : fault_readers()) {
+    unsigned int f = 0;
+    const cudaError_t e = r(&f, clear);
+    if (e != cudaSuccess) return e;
+    *faults |= f;
+  }
+  return cudaSuccess;
+}
+}  // namespace hlo
+
 extern "C" {
 
 // ---- quantized elementwise binary ops ------------------------------------------------------------------
@@ -730,12 +755,11 @@ hlo_status hlo_quant_reshape(const hlo_array* operand, const void* operand_ptr, 
 hlo_status hlo_device_faults(uint32_t* faults, int32_t clear) {
   if (!faults) return fail(HLO_ERR_INVALID_ARG, "device_faults: faults is NULL");
   *faults = 0;
-  unsigned int fr = 0, ft = 0;
+  unsigned int f = 0;
   cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = read_faults_reduce(&fr, clear != 0);
-  if (e == cudaSuccess) e = read_faults_transpose(&ft, clear != 0);
+  if (e == cudaSuccess) e = read_all_faults(&f, clear != 0);
   hlo_status st = cuda_status(e, "device_faults");
-  if (st == HLO_OK) *faults = fr | ft;
+  if (st == HLO_OK) *faults = f;
   return st;
 }
 

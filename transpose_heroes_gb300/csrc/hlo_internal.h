@@ -236,10 +236,12 @@ cudaError_t launch_quant_params(const float* src_s, const int32_t* src_z, float 
                                 int32_t* dst_z, int64_t n, cudaStream_t s);
 // Device-side faults (bit mask, the same values as HLO_FAULT_* of the C ABI).
 constexpr unsigned int kFaultCopyTimeout = 1u;
-// Copy the fault word of a translation unit out (and clear it when asked); the caller has waited for
-// the device.
-cudaError_t read_faults_reduce(unsigned int* faults, bool clear);
-cudaError_t read_faults_transpose(unsigned int* faults, bool clear);
+// Every translation unit whose kernels record faults has its own device fault word; it registers a
+// reader of that word (copy out, clear when asked; the caller has waited for the device) when the
+// library is loaded. read_all_faults ORs the words of every registered unit.
+using FaultReader = cudaError_t (*)(unsigned int* faults, bool clear);
+int register_fault_reader(FaultReader r);
+cudaError_t read_all_faults(unsigned int* faults, bool clear);
 // Launches the bounded-wait self test (sets kFaultCopyTimeout after about a millisecond).
 cudaError_t launch_wait_selftest(cudaStream_t s);
 cudaError_t launch_row_reduce(const RowReducePlan& p, cudaStream_t s);

@@ -627,7 +627,6 @@ cudaError_t launch_wait_selftest(cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t read_faults_reduce(unsigned int* faults, bool clear) { return read_tu_faults(faults, clear); }
 
 // ---- column reduce --------------------------------------------------------------------------------
 constexpr int kColCluster = 8;

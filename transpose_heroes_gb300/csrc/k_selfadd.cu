@@ -596,7 +596,6 @@ static cudaError_t tma_launch(const SelfAddPlan& p, const CUtensorMap& map, cuda
   return cudaGetLastError();
 }
 
-cudaError_t read_faults_transpose(unsigned int* faults, bool clear) { return read_tu_faults(faults, clear); }
 
 static size_t pair_smem_bytes() {
   return HLO_LOG_NC * sizeof(float4) + HLO_LOG_NE * sizeof(float2) + 2 * kT * kTP * sizeof(float) +
