@@ -827,6 +827,23 @@ def test_generated_chain_kernels_every_16bit_input(dtype, ops):
     assert hf.jit_kernels() >= 1
 
 
+@pytest.mark.parametrize("dtype,ops", [
+    ("bf16", list(inp.GELU_CHAIN)),
+    ("f16", ["mul_input", ("add_const", -1.5), "neg", ("mul_const", 0.3), "add_input", "abs"]),
+])
+def test_generated_chain_kernels_many_chunks_per_block(dtype, ops):
+    """2^26 + 5 elements: each block of the generated kernel streams far more 16 KiB chunks than its ring
+    holds, so every stage is refilled many times (with and without the tanh table in shared memory), and
+    five elements sit past the last whole vector. The chain is elementwise, so the oracle's value of each
+    of the 65536 bit patterns, indexed by the input, is the expected output; bit-exact."""
+    pats = np.arange(1 << 16, dtype=np.uint16)
+    data = np.concatenate([np.tile(pats[np.random.default_rng(5).permutation(1 << 16)], 1 << 10), pats[:5]])
+    per_pattern, _ = run_oracle(_chain_fusion(pats, dtype, ops))
+    f = _chain_fusion(data, dtype, ops)
+    check(f, run_gpu(f), np.asarray(per_pattern).reshape(-1)[data], None)
+    assert hf.jit_kernels() >= 1
+
+
 def test_gelu_chain_f32_bit_exact():
     """The same GELU chain on f32 (every op, tanh included, correctly rounded on both sides): bit-exact."""
     g = np.random.default_rng(13)

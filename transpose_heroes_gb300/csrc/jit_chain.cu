@@ -25,6 +25,7 @@
 #include <string>
 #include <vector>
 
+#include "async_copy.cuh"
 #include "hlo_internal.h"
 
 namespace hlo {
@@ -100,8 +101,28 @@ const DriverApi& driver() {
   return api;
 }
 
+// The device address of this unit's fault word (the generated kernels record copy timeouts there; the
+// word is read with the library's others by hlo_device_faults), once per device.
+unsigned int* fault_word_address() {
+  static std::mutex mu;
+  static std::map<int, unsigned int*> addr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = addr.find(dev);
+  if (it != addr.end()) return it->second;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_tu_faults) != cudaSuccess) {
+    cudaGetLastError();
+    p = nullptr;
+  }
+  addr[dev] = static_cast<unsigned int*>(p);
+  return addr[dev];
+}
+
 // ---- source generation ---------------------------------------------------------------------------------
-constexpr int kJitThreads = 512;
+constexpr int kJitVecs = 2;                    // 16-byte vectors per thread and chunk
+constexpr int kJitThreads = 1024 / kJitVecs;
 
 // The packed constant of an op: the element type's bits of the value in both halves.
 uint32_t splat_bits(float v, int dt) {
@@ -149,9 +170,34 @@ std::string chain_body(const Chain& c, int dt) {
   return s;
 }
 
+// The generated kernel streams the array through shared memory in 16 KiB chunks of 1024 vectors. Block b
+// of G takes chunks b, b + G, b + 2G, ... of the whole rounds of G chunks, then an even share of what is
+// left (the remainder's vectors split G ways, so no block streams a whole extra chunk). One block per SM keeps a ring of chunks in
+// flight as 1-D bulk copies completing on mbarriers, issued up front by thread 0 (with the 64 KiB tanh
+// table, when the chain has a tanh) and refilled by the last warp to finish with a chunk, so an SM asks
+// for its first 160 KiB of input at launch rather than a few vectors per thread at a time. Each thread
+// takes kJitVecs vectors of a chunk, applies the chain and stores them straight to global memory; the
+// last n % 8 elements are read directly by the last block. Every wait is bounded: on a timeout the
+// block records the fault in the library's fault word, waits (bounded) for the copies it still has in
+// flight and returns.
+constexpr int kChunkVecs = 1024;
+constexpr int kChunkBytes = kChunkVecs * 16;
+
+int ring_stages(bool tanh) {
+  const int room = 227 * 1024 - (tanh ? 65536 : 0) - 512;  // barriers and counters in the last 512 B
+  const int ns = room / kChunkBytes;
+  return ns < 12 ? ns : 12;
+}
+
+size_t ring_smem(bool tanh) { return (tanh ? 65536 : 0) + (size_t)ring_stages(tanh) * kChunkBytes + 512; }
+
 std::string kernel_source(const Chain& c, int dt) {
   const char* ty = dt == BF16 ? "bf16" : "f16";
+  const bool tanh = has_tanh(c);
   std::string src;
+  src += "#define NS " + std::to_string(ring_stages(tanh)) + "\n";
+  src += "#define TB " + std::to_string(tanh ? 65536 : 0) + "\n";
+  src += "#define CB " + std::to_string(kChunkBytes) + "\n";
   src += "typedef unsigned int u32;\n";
   src += "struct alignas(16) v4 { u32 a, b, c, d; };\n";
   src += std::string("__device__ __forceinline__ u32 hadd(u32 a, u32 b) { u32 r; asm(\"add.rn.") + ty +
@@ -169,39 +215,110 @@ std::string kernel_source(const Chain& c, int dt) {
       "__device__ __forceinline__ v4 ld4(const v4* p) { v4 r; asm volatile(\"ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\" "
       ": \"=r\"(r.a), \"=r\"(r.b), \"=r\"(r.c), \"=r\"(r.d) : \"l\"(p)); return r; }\n"
       "__device__ __forceinline__ void st4(v4* p, v4 v) { asm volatile(\"st.global.v4.u32 [%0], {%1, %2, %3, %4};\" :: "
-      "\"l\"(p), \"r\"(v.a), \"r\"(v.b), \"r\"(v.c), \"r\"(v.d) : \"memory\"); }\n";
+      "\"l\"(p), \"r\"(v.a), \"r\"(v.b), \"r\"(v.c), \"r\"(v.d) : \"memory\"); }\n"
+      "__device__ __forceinline__ v4 lds4(u32 a) { v4 r; asm volatile(\"ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\" "
+      ": \"=r\"(r.a), \"=r\"(r.b), \"=r\"(r.c), \"=r\"(r.d) : \"r\"(a) : \"memory\"); return r; }\n"
+      // mbarriers and 1-D bulk copies
+      "__device__ __forceinline__ void bar_init(u32 b, u32 c) { asm volatile(\"mbarrier.init.shared::cta.b64 [%0], %1;\" "
+      ":: \"r\"(b), \"r\"(c)); }\n"
+      "__device__ __forceinline__ void expect(u32 b, u32 n) { asm volatile(\"mbarrier.arrive.expect_tx.shared::cta.b64 _, "
+      "[%0], %1;\" :: \"r\"(b), \"r\"(n) : \"memory\"); }\n"
+      "__device__ __forceinline__ void bulk(u32 d, const void* g, u32 n, u32 b) { asm volatile(\"cp.async.bulk.shared::"
+      "cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\" :: \"r\"(d), \"l\"(g), \"r\"(n), \"r\"(b) : "
+      "\"memory\"); }\n"
+      // waits for phase `par`; false after about a second (2^31 cycles) without it
+      "__device__ __forceinline__ bool bar_wait(u32 b, u32 par) {\n"
+      "  long long t0 = -1;\n"
+      "  while (true) {\n"
+      "    u32 d;\n"
+      "    asm volatile(\"{ .reg .pred P; mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2; selp.u32 %0, 1, 0, P; }\" "
+      ": \"=r\"(d) : \"r\"(b), \"r\"(par) : \"memory\");\n"
+      "    if (d) return true;\n"
+      "    const long long now = clock64();\n"
+      "    if (t0 < 0) t0 = now; else if (now - t0 > 2000000000LL) return false;\n"
+      "  }\n"
+      "}\n";
   src += "__device__ __forceinline__ u32 f(u32 x, const unsigned short* t) {\n  u32 v = x;\n";
   src += chain_body(c, dt);
   src += "  return v;\n}\n";
   src +=
       "__device__ __forceinline__ v4 f4(v4 w, const unsigned short* t) { return v4{f(w.a, t), f(w.b, t), f(w.c, t), f(w.d, t)}; "
       "}\n";
+  src += "#define VPT " + std::to_string(kJitVecs) + "\n#define CV " + std::to_string(kChunkVecs) + "\n";
   src += "extern \"C\" __global__ void __launch_bounds__(" + std::to_string(kJitThreads) +
-         ") hlo_jit_chain(const v4* __restrict__ in, v4* __restrict__ out, long long n, const v4* __restrict__ tg) {\n"
-         "  extern __shared__ v4 tt4[];\n"
-         "  const unsigned short* t = reinterpret_cast<const unsigned short*>(tt4);\n"
-         "  const long long nvec = n >> 3, nth = (long long)gridDim.x * blockDim.x;\n"
-         "  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;\n"
-         "  const long long base = (gt >> 5) * 128 + (threadIdx.x & 31);\n"  // a warp's four loads: 512 B each
-         "  const long long rounds = nvec / (4 * nth);\n"
-         "  v4 x0, x1, x2, x3;\n"
-         "  if (rounds > 0) { x0 = ld4(in + base); x1 = ld4(in + base + 32); x2 = ld4(in + base + 64); x3 = ld4(in + base + 96); }\n";
-  if (has_tanh(c))
-    src +=
-        "  for (int i = threadIdx.x; i < 4096; i += blockDim.x) tt4[i] = ld4(tg + i);\n"
-        "  __syncthreads();\n";
+         ", 1) hlo_jit_chain(const v4* __restrict__ in, v4* __restrict__ out, long long n, const v4* __restrict__ tg, "
+         "u32* __restrict__ fault) {\n"
+         "  extern __shared__ __align__(128) unsigned char sm[];\n"
+         "  const unsigned short* t = reinterpret_cast<const unsigned short*>(sm);\n"
+         "  const u32 ring = (u32)__cvta_generic_to_shared(sm + TB);\n"
+         "  const u32 bars = ring + NS * CB;\n"  // NS chunk barriers, then the table's
+         "  int* done = reinterpret_cast<int*>(sm + TB + NS * CB + (NS + 1) * 8);\n"
+         "  const long long nvec = n >> 3, G = gridDim.x, b = blockIdx.x;\n"
+         // whole rounds of G chunks, then block b's share [l0, l0 + ln) of the remaining vectors
+         "  const long long rounds = nvec / (G * CV), rest = nvec - rounds * G * CV;\n"
+         "  const long long lq = rest / G, lr = rest % G;\n"
+         "  const long long l0 = rounds * G * CV + b * lq + (b < lr ? b : lr), ln = lq + (b < lr ? 1 : 0);\n"
+         "  const long long mine = rounds + (ln > 0 ? 1 : 0);\n"
+         "  const int tid = threadIdx.x;\n"
+         "  if (tid == 0) {\n"
+         "    for (int s = 0; s < NS; ++s) { bar_init(bars + 8 * s, 1); done[s] = 0; }\n"
+         "    bar_init(bars + 8 * NS, 1);\n"
+         "    asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");\n";
+  if (tanh)
+    src += "    expect(bars + 8 * NS, TB); bulk((u32)__cvta_generic_to_shared(sm), tg, TB, bars + 8 * NS);\n";
   src +=
-      "  for (long long r = 0; r < rounds; ++r) {\n"
-      "    const long long b = r * 4 * nth + base;\n"
-      "    const v4 y0 = x0, y1 = x1, y2 = x2, y3 = x3;\n"
-      "    if (r + 1 < rounds) { const long long c = b + 4 * nth; x0 = ld4(in + c); x1 = ld4(in + c + 32); x2 = ld4(in + c + 64); "
-      "x3 = ld4(in + c + 96); }\n"
-      "    st4(out + b, f4(y0, t)); st4(out + b + 32, f4(y1, t)); st4(out + b + 64, f4(y2, t)); st4(out + b + 96, f4(y3, t));\n"
+      "    for (int s = 0; s < NS && s < mine; ++s) {\n"
+      "      const long long c0 = s < rounds ? (b + s * G) * CV : l0, cn = s < rounds ? CV : ln;\n"
+      "      expect(bars + 8 * s, (u32)cn * 16); bulk(ring + s * CB, in + c0, (u32)cn * 16, bars + 8 * s);\n"
+      "    }\n"
       "  }\n"
-      "  for (long long i = rounds * 4 * nth + gt; i < nvec; i += nth) st4(out + i, f4(ld4(in + i), t));\n"
-      "  const unsigned short* i16 = reinterpret_cast<const unsigned short*>(in);\n"
-      "  unsigned short* o16 = reinterpret_cast<unsigned short*>(out);\n"
-      "  for (long long e = nvec * 8 + gt; e < n; e += nth) o16[e] = (unsigned short)(f((u32)i16[e], t) & 0xFFFFu);\n"
+      "  __syncthreads();\n";
+  src += tanh ? "  bool ok = __all_sync(0xFFFFFFFFu, bar_wait(bars + 8 * NS, 0));\n" : "  bool ok = true;\n";
+  src +=
+      "  long long k = 0;\n"
+      "  int s = 0;\n"
+      "  u32 ph = 0;\n"
+      "  for (; ok && k < mine; ++k) {\n"
+      // the warp decides together (the __syncwarp below needs all of its lanes)
+      "    if (!__all_sync(0xFFFFFFFFu, bar_wait(bars + 8 * s, ph))) { ok = false; break; }\n"
+      "    const long long c0 = k < rounds ? (b + k * G) * CV : l0;\n"
+      "    const int cn = k < rounds ? CV : (int)ln;\n"
+      "    v4 x[VPT];\n"
+      "#pragma unroll\n"
+      "    for (int j = 0; j < VPT; ++j) if (tid + j * (CV / VPT) < cn) x[j] = lds4(ring + s * CB + (tid + j * (CV / VPT)) * 16);\n"
+      "#pragma unroll\n"
+      "    for (int j = 0; j < VPT; ++j) if (tid + j * (CV / VPT) < cn) st4(out + c0 + tid + j * (CV / VPT), f4(x[j], t));\n"
+      // the warp's vectors are in registers (the stores above depend on them): the last warp refills
+      "    __syncwarp();\n"
+      "    if ((tid & 31) == 0) {\n"
+      "      __threadfence_block();\n"
+      "      if (atomicAdd(&done[s], 1) == (int)(blockDim.x / 32) - 1) {\n"
+      "        done[s] = 0;\n"
+      "        const long long nk = k + NS;\n"
+      "        if (nk < mine) {\n"
+      "          const long long d0 = nk < rounds ? (b + nk * G) * CV : l0, dn = nk < rounds ? CV : ln;\n"
+      "          asm volatile(\"fence.proxy.async.shared::cta;\" ::: \"memory\");\n"
+      "          expect(bars + 8 * s, (u32)dn * 16);\n"
+      "          bulk(ring + s * CB, in + d0, (u32)dn * 16, bars + 8 * s);\n"
+      "        }\n"
+      "      }\n"
+      "    }\n"
+      "    if (++s == NS) { s = 0; ph ^= 1u; }\n"
+      "  }\n"
+      "  if (!ok) {\n"
+      // a copy did not arrive in time: record it, wait (bounded) for the copies this block may still have
+      // in flight (the table and chunks k .. k + NS - 1) and return
+      "    if (tid == 0) atomicOr(fault, 1u);\n";
+  if (tanh) src += "    bar_wait(bars + 8 * NS, 0);\n";
+  src +=
+      "    for (long long q2 = k; q2 < k + NS && q2 < mine; ++q2) bar_wait(bars + 8 * (int)(q2 % NS), (u32)((q2 / NS) & 1));\n"
+      "    return;\n"
+      "  }\n"
+      "  if (b == G - 1) {\n"
+      "    const unsigned short* i16 = reinterpret_cast<const unsigned short*>(in);\n"
+      "    unsigned short* o16 = reinterpret_cast<unsigned short*>(out);\n"
+      "    for (long long e = nvec * 8 + tid; e < n; e += blockDim.x) o16[e] = (unsigned short)(f((u32)i16[e], t) & 0xFFFFu);\n"
+      "  }\n"
       "}\n";
   return src;
 }
@@ -258,7 +375,7 @@ JitKernel build(const Chain& c, int dt, int dev) {
       CUfunction fn = nullptr;
       if (!cubin.empty() && dr.load(&mod, cubin.data()) == CUDA_SUCCESS &&
           dr.get(&fn, mod, "hlo_jit_chain") == CUDA_SUCCESS) {
-        const size_t smem = has_tanh(c) ? 32768 * sizeof(uint16_t) : 0;
+        const size_t smem = ring_smem(has_tanh(c));
         int nb = 0;
         if (dr.set_attr(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, (int)smem) == CUDA_SUCCESS &&
             dr.occupancy(&nb, fn, kJitThreads, smem) == CUDA_SUCCESS && nb > 0) {
@@ -299,12 +416,15 @@ cudaError_t launch_jit_chain(const void* in, void* out, int64_t n, int dt, const
   if (!jk.fn) return cudaSuccess;  // the interpreter takes the call
   const void* tg = has_tanh(pro) ? tanh_table_address() : nullptr;
   if (has_tanh(pro) && !tg) return cudaSuccess;
-  int64_t blocks = (n / 32 + kJitThreads - 1) / kJitThreads;
+  unsigned int* fault = fault_word_address();
+  if (!fault) return cudaSuccess;
+  // one block per SM; fewer for small arrays (at least 256 vectors, 4 KiB, per block)
+  int64_t blocks = n / 8 / 256;
   const int64_t cap = (int64_t)device_sm_count() * jk.blocks_per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   long long nn = (long long)n;
-  void* args[] = {const_cast<void**>(&in), &out, &nn, const_cast<void**>(&tg)};
+  void* args[] = {const_cast<void**>(&in), &out, &nn, const_cast<void**>(&tg), &fault};
   const CUresult r = driver().launch(jk.fn, (unsigned)blocks, 1, 1, kJitThreads, 1, 1, (unsigned)jk.smem,
                                      reinterpret_cast<CUstream>(s), args, nullptr);
   if (r != CUDA_SUCCESS) return cudaErrorLaunchFailure;
