@@ -346,6 +346,31 @@ def ours(args):
     value = all_bytes / total_s / 1e9
 
     hbm, peak_src = peaks()
+    reps = max(3, min(args.steps, 200))
+
+    def time_alone(fn):
+        """Mean CUDA-event interval of fn over `reps` launches, L2 flushed before each."""
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in evs:
+            flush.fill_(3)
+            torch.cuda._sleep(HOST_LEAD_CYCLES // 8)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    def copy_same_bytes_us(nbytes):
+        """A plain device-to-device copy (torch) moving nbytes (half read, half written), timed alone the
+        same way: what any kernel moving these bytes reaches in this timing loop."""
+        src = torch.empty(nbytes // 2, dtype=torch.uint8, device=dev)
+        dst = torch.empty_like(src)
+        us = time_alone(lambda: dst.copy_(src))
+        del src, dst
+        return us
+
     per = {}
     for i, f in enumerate(fusions):
         ms = statistics.mean(per_fusion_ms[i])
@@ -353,6 +378,8 @@ def ours(args):
         per[ORDER[i]] = {"kernel": KERNELS[ORDER[i]], "us": 1e3 * ms, "us_min": 1e3 * min(per_fusion_ms[i]),
                          "algorithmic_bytes": f.algorithmic_bytes, "gbs": gbs, "frac_of_" + peak_src: gbs / hbm,
                          "elements_per_s": f.elements / (ms / 1e3)}
+        copy_us = copy_same_bytes_us(f.algorithmic_bytes)
+        per[ORDER[i]].update({"copy_same_bytes_us": copy_us, "speed_vs_copy": copy_us / (1e3 * ms)})
     dom = max(per, key=lambda k: per[k]["us"])
     dom_gbs = per[dom]["gbs"]
     tr = traffic_record()
@@ -407,25 +434,15 @@ def ours(args):
     # fusions beyond the five workloads (the loop fusions and the rest of the path's next steps), each
     # timed alone the same way (L2 flushed before every launch, CUDA events), not part of `value`
     next_rows = {}
-    reps = max(3, min(args.steps, 200))
     for name, make in NEXT_ROWS.items():
         f = make(args.seed)
         d = DeviceFusion(f, device=dev, pin_host=False)
-        for _ in range(3):
-            d.run(stream=stream)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-        for a, b in evs:
-            flush.fill_(3)
-            torch.cuda._sleep(HOST_LEAD_CYCLES // 8)
-            a.record(stream)
-            d.run(stream=stream)
-            b.record(stream)
-        torch.cuda.synchronize()
-        us = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs)
+        us = time_alone(lambda: d.run(stream=stream))
         gbs = f.algorithmic_bytes / (us / 1e6) / 1e9
+        copy_us = copy_same_bytes_us(f.algorithmic_bytes)
         next_rows[name] = {"workload": f.description, "us": us, "algorithmic_bytes": f.algorithmic_bytes,
                            "gbs": gbs, "frac_of_" + peak_src: gbs / hbm, "elements_per_s": f.elements / (us / 1e6),
-                           "launches": reps}
+                           "launches": reps, "copy_same_bytes_us": copy_us, "speed_vs_copy": copy_us / us}
         del d
 
     if rank == 0:

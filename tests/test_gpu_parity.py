@@ -810,9 +810,11 @@ def test_chain_table_every_16bit_input(dtype, ops):
 
 
 @pytest.mark.parametrize("dtype,ops", [
-    ("bf16", list(inp.GELU_CHAIN)),
-    ("bf16", ["neg", ("add_const", 0.75), "tanh", "abs", ("mul_const", -3.0), "mul_input"]),
-    ("f16", ["mul_input", ("add_const", -1.5), "neg", ("mul_const", 0.3), "add_input", "abs"]),
+    ("bf16", list(inp.GELU_CHAIN)),  # one run table: multiply, tanh, add 1, multiply
+    ("bf16", ["neg", ("add_const", 0.75), "tanh", "abs", ("mul_const", -3.0), "mul_input"]),  # run table
+    ("bf16", ["mul_input", "tanh", "add_input", "tanh", ("mul_const", 2.0), "mul_input"]),  # two tanh runs: tanh table
+    ("bf16", ["mul_input", "tanh", "add_input"]),  # a lone tanh: tanh table
+    ("f16", ["mul_input", ("add_const", -1.5), "neg", ("mul_const", 0.3), "add_input", "abs"]),  # no table
 ])
 def test_generated_chain_kernels_every_16bit_input(dtype, ops):
     """Chains of 2^20 elements or more that the run-time generator covers (hlo_jit_kernels counts the
@@ -842,6 +844,33 @@ def test_generated_chain_kernels_many_chunks_per_block(dtype, ops):
     f = _chain_fusion(data, dtype, ops)
     check(f, run_gpu(f), np.asarray(per_pattern).reshape(-1)[data], None)
     assert hf.jit_kernels() >= 1
+
+
+def test_generated_run_tables_past_the_last_slot_and_across_streams():
+    """Twelve distinct bf16 chains whose tanh run becomes a 65536-entry table built on the device: more
+    chains than the library keeps table slots for, so the later ones read the tanh table instead. Each
+    chain's first launch goes to a side stream (the table is built there) and the second to the current
+    stream (which must wait for that table). 2^20 + 3 elements, every bit pattern 16 times; bit-exact
+    against the oracle's value of each pattern."""
+    pats = np.arange(1 << 16, dtype=np.uint16)
+    data = np.concatenate([np.tile(pats, 16), pats[:3]])
+    side = torch.cuda.Stream()
+    for k in range(12):
+        ops = ["mul_input", ("mul_const", 0.25 + k / 16), "tanh", ("add_const", 1.0), "mul_input"]
+        per_pattern, _ = run_oracle(_chain_fusion(pats, "bf16", ops))
+        expected = np.asarray(per_pattern).reshape(-1)[data]
+        f = _chain_fusion(data, "bf16", ops)
+        d = DeviceFusion(f)
+        torch.cuda.synchronize()  # the input's upload has landed
+        with torch.cuda.stream(side):
+            d.run(stream=side)
+        side.synchronize()
+        check(f, d.output_numpy(), expected, None)
+        d.out.zero_()
+        d.run()
+        torch.cuda.synchronize()
+        check(f, d.output_numpy(), expected, None)
+    assert hf.jit_kernels() >= 12
 
 
 def test_gelu_chain_f32_bit_exact():

@@ -146,10 +146,54 @@ bool has_tanh(const Chain& c) {
   return false;
 }
 
-std::string chain_body(const Chain& c, int dt) {
+bool reads_input(int op) { return op == OP_MUL_IN || op == OP_ADD_IN; }
+
+// Where the generated kernel gets a chain's tanh from. Every op of a run that does not read the input
+// x (constant adds and multiplies, negate, abs, tanh) is a function of the running 16-bit value alone,
+// so a whole such run is one 65536-entry table: the run's ops applied to every bit pattern with the
+// same instructions, once per chain, then one lookup per element instead of the run. The generator
+// does that for a bf16 chain whose tanh ops all sit in one such run of two or more ops (GELU's
+// multiply, tanh, add 1, multiply by 1/2); other chains with a tanh read the tanh table (64 KiB, indexed
+// by |x|).
+struct TablePlan {
+  int kind = 0;            // 0: no table, 1: the tanh table, 2: a table of the run [run0, run1)
+  int run0 = 0, run1 = 0;
+  int bytes() const { return kind == 0 ? 0 : kind == 1 ? 65536 : 131072; }
+};
+
+TablePlan plan_table(const Chain& c, int dt) {
+  TablePlan p;
+  if (!has_tanh(c)) return p;
+  p.kind = 1;
+  int runs_with_tanh = 0, r0 = 0, r1 = 0;
+  for (int k = 0; k < c.n;) {
+    if (reads_input(c.op[k])) {
+      ++k;
+      continue;
+    }
+    int e = k, nt = 0;
+    for (; e < c.n && !reads_input(c.op[e]); ++e) nt += c.op[e] == OP_TANH;
+    if (nt) {
+      ++runs_with_tanh;
+      r0 = k;
+      r1 = e;
+    }
+    k = e;
+  }
+  if (dt == BF16 && runs_with_tanh == 1 && r1 - r0 >= 2) {
+    p.kind = 2;
+    p.run0 = r0;
+    p.run1 = r1;
+  }
+  return p;
+}
+
+// The ops [k0, k1) of the chain as straight-line code on the packed pair v (x: the input pair, t: the
+// table).
+std::string chain_body(const Chain& c, int dt, int k0, int k1) {
   std::string s;
   char line[128];
-  for (int k = 0; k < c.n; ++k) {
+  for (int k = k0; k < k1; ++k) {
     switch (c.op[k]) {
       case OP_MUL_IN: s += "  v = hmul(v, x);\n"; break;
       case OP_ADD_IN: s += "  v = hadd(v, x);\n"; break;
@@ -183,20 +227,20 @@ std::string chain_body(const Chain& c, int dt) {
 constexpr int kChunkVecs = 1024;
 constexpr int kChunkBytes = kChunkVecs * 16;
 
-int ring_stages(bool tanh) {
-  const int room = 227 * 1024 - (tanh ? 65536 : 0) - 512;  // barriers and counters in the last 512 B
+int ring_stages(int table_bytes) {
+  const int room = 227 * 1024 - table_bytes - 512;  // barriers and counters in the last 512 B
   const int ns = room / kChunkBytes;
   return ns < 12 ? ns : 12;
 }
 
-size_t ring_smem(bool tanh) { return (tanh ? 65536 : 0) + (size_t)ring_stages(tanh) * kChunkBytes + 512; }
+size_t ring_smem(int table_bytes) { return (size_t)table_bytes + (size_t)ring_stages(table_bytes) * kChunkBytes + 512; }
 
-std::string kernel_source(const Chain& c, int dt) {
+std::string kernel_source(const Chain& c, int dt, const TablePlan& tp) {
   const char* ty = dt == BF16 ? "bf16" : "f16";
-  const bool tanh = has_tanh(c);
+  const bool tanh = tp.kind != 0;  // a table in shared memory
   std::string src;
-  src += "#define NS " + std::to_string(ring_stages(tanh)) + "\n";
-  src += "#define TB " + std::to_string(tanh ? 65536 : 0) + "\n";
+  src += "#define NS " + std::to_string(ring_stages(tp.bytes())) + "\n";
+  src += "#define TB " + std::to_string(tp.bytes()) + "\n";
   src += "#define CB " + std::to_string(kChunkBytes) + "\n";
   src += "typedef unsigned int u32;\n";
   src += "struct alignas(16) v4 { u32 a, b, c, d; };\n";
@@ -211,6 +255,10 @@ std::string kernel_source(const Chain& c, int dt) {
       "__device__ __forceinline__ u32 htanh(u32 w, const unsigned short* t) {\n"
       "  const u32 a = w & 0x7FFF7FFFu;\n"
       "  return prmt((u32)t[a & 0xFFFFu], (u32)t[a >> 16], 0x5410u) | (w & 0x80008000u);\n"
+      "}\n"
+      // a pair through the run's table (indexed by all 16 bits)
+      "__device__ __forceinline__ u32 hlook(u32 w, const unsigned short* t) {\n"
+      "  return prmt((u32)t[w & 0xFFFFu], (u32)t[w >> 16], 0x5410u);\n"
       "}\n"
       "__device__ __forceinline__ v4 ld4(const v4* p) { v4 r; asm volatile(\"ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\" "
       ": \"=r\"(r.a), \"=r\"(r.b), \"=r\"(r.c), \"=r\"(r.d) : \"l\"(p)); return r; }\n"
@@ -239,8 +287,24 @@ std::string kernel_source(const Chain& c, int dt) {
       "  }\n"
       "}\n";
   src += "__device__ __forceinline__ u32 f(u32 x, const unsigned short* t) {\n  u32 v = x;\n";
-  src += chain_body(c, dt);
+  if (tp.kind == 2) {
+    src += chain_body(c, dt, 0, tp.run0);
+    src += "  v = hlook(v, t);\n";
+    src += chain_body(c, dt, tp.run1, c.n);
+  } else {
+    src += chain_body(c, dt, 0, c.n);
+  }
   src += "  return v;\n}\n";
+  if (tp.kind == 2)  // the run's table: every bit pattern through the run's ops (tg: the tanh table)
+    src += "extern \"C\" __global__ void hlo_jit_table(const unsigned short* __restrict__ tg, unsigned short* __restrict__ dst) "
+           "{\n"
+           "  const u32 p = blockIdx.x * blockDim.x + threadIdx.x;\n"
+           "  if (p >= 65536u) return;\n"
+           "  const unsigned short* t = tg;\n"
+           "  u32 v = p | (p << 16);\n" +
+           chain_body(c, dt, tp.run0, tp.run1) +
+           "  dst[p] = (unsigned short)(v & 0xFFFFu);\n"
+           "}\n";
   src +=
       "__device__ __forceinline__ v4 f4(v4 w, const unsigned short* t) { return v4{f(w.a, t), f(w.b, t), f(w.c, t), f(w.d, t)}; "
       "}\n";
@@ -341,13 +405,35 @@ struct JitKernel {
   CUfunction fn = nullptr;  // null: the chain did not compile (the interpreter serves it)
   int blocks_per_sm = 0;
   size_t smem = 0;
+  TablePlan tp;
+  const void* table = nullptr;     // what the kernel copies into shared memory (tanh or run table)
+  cudaEvent_t ready = nullptr;     // run table: recorded after it was built, on stream built_on
+  cudaStream_t built_on = nullptr;
 };
+
+// Run tables, in this unit's device memory: a chain's table is built into a free slot the first time
+// the chain runs on a device and stays there; chains past the last slot use the tanh table instead.
+constexpr int kRunTableSlots = 8;
+static __device__ __align__(16) uint16_t g_run_tables[kRunTableSlots][65536];
+
+uint16_t* run_table_slot(int dev) {
+  static std::map<int, int> used;  // callers hold g_mu
+  int& k = used[dev];
+  if (k >= kRunTableSlots) return nullptr;
+  void* base = nullptr;
+  if (cudaGetSymbolAddress(&base, g_run_tables) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<uint16_t*>(base) + (size_t)65536 * k++;
+}
 
 std::mutex g_mu;
 std::map<std::pair<int, std::string>, JitKernel> g_cache;
 
-// Compiles the chain for the current device (or returns the cached result).
-JitKernel build(const Chain& c, int dt, int dev) {
+// Compiles the chain for the current device (or returns the cached result); a run table is built on
+// stream s.
+JitKernel build(const Chain& c, int dt, int dev, cudaStream_t s) {
   const auto key = std::make_pair(dev, chain_key(c, dt));
   std::lock_guard<std::mutex> lock(g_mu);
   auto it = g_cache.find(key);
@@ -357,9 +443,14 @@ JitKernel build(const Chain& c, int dt, int dev) {
   const NvrtcApi& nv = nvrtc();
   const DriverApi& dr = driver();
   int major = 0, minor = 0;
-  if (nv.ok && dr.ok && cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+  const void* tg = has_tanh(c) ? tanh_table_address() : nullptr;
+  TablePlan tp = plan_table(c, dt);
+  uint16_t* slot = nullptr;
+  if (tp.kind == 2 && !(slot = run_table_slot(dev))) tp = TablePlan{1, 0, 0};
+  if (nv.ok && dr.ok && (tp.kind == 0 || tg) &&
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) == cudaSuccess) {
-    const std::string src = kernel_source(c, dt);
+    const std::string src = kernel_source(c, dt, tp);
     nvrtcProgram prog = nullptr;
     if (nv.create(&prog, src.c_str(), "hlo_jit_chain.cu", 0, nullptr, nullptr) == NVRTC_SUCCESS) {
       const std::string arch = "--gpu-architecture=sm_" + std::to_string(major * 10 + minor) + (major >= 9 ? "a" : "");
@@ -372,16 +463,29 @@ JitKernel build(const Chain& c, int dt, int dev) {
       }
       nv.destroy(&prog);
       CUmodule mod = nullptr;
-      CUfunction fn = nullptr;
+      CUfunction fn = nullptr, table_fn = nullptr;
       if (!cubin.empty() && dr.load(&mod, cubin.data()) == CUDA_SUCCESS &&
-          dr.get(&fn, mod, "hlo_jit_chain") == CUDA_SUCCESS) {
-        const size_t smem = ring_smem(has_tanh(c));
+          dr.get(&fn, mod, "hlo_jit_chain") == CUDA_SUCCESS &&
+          (tp.kind != 2 || dr.get(&table_fn, mod, "hlo_jit_table") == CUDA_SUCCESS)) {
+        const size_t smem = ring_smem(tp.bytes());
         int nb = 0;
-        if (dr.set_attr(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, (int)smem) == CUDA_SUCCESS &&
-            dr.occupancy(&nb, fn, kJitThreads, smem) == CUDA_SUCCESS && nb > 0) {
+        bool ok = dr.set_attr(fn, CU_FUNC_ATTRIBUTE_MAX_DYNAMIC_SHARED_SIZE_BYTES, (int)smem) == CUDA_SUCCESS &&
+                  dr.occupancy(&nb, fn, kJitThreads, smem) == CUDA_SUCCESS && nb > 0;
+        cudaEvent_t ready = nullptr;
+        if (ok && tp.kind == 2) {  // build the run's table once, ordered before every use
+          void* targs[] = {const_cast<void**>(&tg), &slot};
+          ok = dr.launch(table_fn, 256, 1, 1, 256, 1, 1, 0, reinterpret_cast<CUstream>(s), targs, nullptr) == CUDA_SUCCESS &&
+               cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) == cudaSuccess &&
+               cudaEventRecord(ready, s) == cudaSuccess;
+        }
+        if (ok) {
           jk.fn = fn;
           jk.blocks_per_sm = nb;
           jk.smem = smem;
+          jk.tp = tp;
+          jk.table = tp.kind == 2 ? static_cast<const void*>(slot) : tg;
+          jk.ready = ready;
+          jk.built_on = s;
         }
       }
     }
@@ -412,10 +516,13 @@ cudaError_t launch_jit_chain(const void* in, void* out, int64_t n, int dt, const
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const JitKernel jk = build(pro, dt, dev);
+  const JitKernel jk = build(pro, dt, dev, s);
   if (!jk.fn) return cudaSuccess;  // the interpreter takes the call
-  const void* tg = has_tanh(pro) ? tanh_table_address() : nullptr;
-  if (has_tanh(pro) && !tg) return cudaSuccess;
+  const void* tg = jk.table;
+  if (jk.ready && s != jk.built_on) {  // the run table was built on another stream
+    e = cudaStreamWaitEvent(s, jk.ready, 0);
+    if (e != cudaSuccess) return e;
+  }
   unsigned int* fault = fault_word_address();
   if (!fault) return cudaSuccess;
   // one block per SM; fewer for small arrays (at least 256 vectors, 4 KiB, per block)
