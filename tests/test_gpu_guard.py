@@ -101,7 +101,17 @@ def _cases():
                                                                         "broadcast_dimensions": [1]}}),
         "elementwise_f32": _transpose("ew", f32(1003), [1003], "f32", [0], pro={"ops": ["tanh"], "round_each": True}),
         "elementwise_16x2": inp.gelu_bf16(seed=3, dims=(3, 7, 1001)),
-        "elementwise_lut16": inp.gelu_bf16(seed=3, dims=(64, 256, 257)),
+        # a bf16 chain with exp from 2^22 elements: the chain's table kernel (the generated kernels do
+        # not take exp)
+        "elementwise_lut16": _transpose("lut", inp.normal_bf16(g, (1 << 22) + 7), [(1 << 22) + 7], "bf16", [0],
+                                        pro={"ops": ["exp", ("mul_const", 0.5)], "round_each": True}),
+        # the generated kernels (from 2^20 elements, 16-byte aligned): GELU with its run table and a
+        # partial last chunk per block plus a 5-element tail; an f16 chain with no table
+        "generated_run_table": inp.gelu_bf16(seed=3, dims=(64, 256, 257)),
+        "generated_tail": inp.gelu_bf16(seed=3, dims=((1 << 20) + 5,)),
+        "generated_no_table": _transpose("gen_f16", (inp.uniform_f32(g, (1 << 21) + 3, -4.0, 4.0)
+                                                     .astype(np.float16).view(np.uint16)), [(1 << 21) + 3], "f16", [0],
+                                         pro={"ops": ["mul_input", ("add_const", -1.5), "abs"], "round_each": True}),
         "copy": _transpose("copy", f32(999), [999], "f32", [0]),
         "quant_tile_ragged": inp.quant_relayout(seed=3, n0=301, n1=517),
         "quant_tile_full": inp.quant_relayout(seed=3, n0=256, n1=384),
