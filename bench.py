@@ -363,8 +363,9 @@ def ours(args):
         return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs)
 
     def copy_same_bytes_us(nbytes):
-        """A plain device-to-device copy (torch) moving nbytes (half read, half written), timed alone the
-        same way: what any kernel moving these bytes reaches in this timing loop."""
+        """A plain device-to-device copy moving nbytes (half read, half written: torch's copy_ of a
+        contiguous byte tensor, a cudaMemcpyAsync), timed alone the same way: what a copy of these bytes
+        reaches in this timing loop."""
         src = torch.empty(nbytes // 2, dtype=torch.uint8, device=dev)
         dst = torch.empty_like(src)
         us = time_alone(lambda: dst.copy_(src))
