@@ -119,6 +119,31 @@ def test_full_size_configs(name):
     assert oracle.unresolved_count() == 0
 
 
+def test_full_size_step_on_concurrent_streams():
+    """The benchmark's step: the five full-size fusions each on a stream of its own (runner.
+    ConcurrentFusions), twice in a row with the outputs cleared between, every output against the
+    oracle; work queued on the caller's stream after the step sees all five outputs."""
+    from transpose_heroes_gb300.runner import ConcurrentFusions
+
+    fusions = [inp.full(n, seed=2) for n in NAMES]
+    devs = [DeviceFusion(f) for f in fusions]
+    torch.cuda.synchronize()
+    step = ConcurrentFusions(devs)
+    refs = [run_oracle(f) for f in fusions]
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        for d in devs:
+            d.out.fill_(-1)
+        step.run(stream)
+        host = [torch.empty(d.out.shape, dtype=d.out.dtype, pin_memory=True) for d in devs]
+        for h, d in zip(host, devs):
+            h.copy_(d.out, non_blocking=True)  # on the caller's stream, after the join
+        stream.synchronize()
+        view = {"f32": np.float32, "bf16": np.uint16, "f16": np.uint16, "s8": np.int8}
+        for f, h, (ref, asum) in zip(fusions, host, refs):
+            check(f, h.numpy().view(view[f.out_dtype]), ref, asum)
+
+
 def test_selfadd_beyond_2_to_31_elements():
     """The self-add transpose on f32[46404, 46404]: 2.15e9 elements, past every 32-bit element count and
     byte offset, with a ragged last tile row and column. 6144 sampled outputs (a third of them in the

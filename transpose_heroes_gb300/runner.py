@@ -131,3 +131,27 @@ class DeviceFusion:
 
     def output_numpy(self) -> np.ndarray:
         return self.out.cpu().numpy().view(_NP_OUT[self.f.out_dtype])
+
+
+class ConcurrentFusions:
+    """Independent fusions (no buffer shared between them) each enqueued on a stream of its own, forked
+    from the caller's stream by one event and joined back into it by one event per fusion: work queued
+    on the caller's stream before run() happens before every fusion, and work queued after it sees all
+    their outputs. A short fusion then fills the ramp and tail of a long one instead of waiting for it
+    to drain, and the launches themselves overlap."""
+
+    def __init__(self, fusions, device="cuda"):
+        self.fusions = list(fusions)
+        self.streams = [torch.cuda.Stream(device=device) for _ in self.fusions]
+        self.fork = torch.cuda.Event()
+        self.joins = [torch.cuda.Event() for _ in self.fusions]
+
+    def run(self, stream=None):
+        stream = torch.cuda.current_stream() if stream is None else stream
+        self.fork.record(stream)
+        for d, s, j in zip(self.fusions, self.streams, self.joins):
+            s.wait_event(self.fork)
+            d.run(stream=s)
+            j.record(s)
+        for j in self.joins:
+            stream.wait_event(j)
