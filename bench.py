@@ -10,8 +10,9 @@ runs each on a stream of its own (runner.ConcurrentFusions), launched in this or
   quant_relayout     s8[4096,4096]                      dequant (per-axis) -> {0,1} -> quant (per-tensor)
 value = algorithmic bytes of the step / step time (GB/s). The same step is then timed again with the
 fusions one after another on one stream ("sequential"), an event between each: per-fusion GB/s, fraction
-of the measured HBM copy peak and elements/s, and the roofline of the dominant kernel, come from that pass. L2 is flushed (a 256 MiB write) before every timed
-step, outside the timed interval.
+of the measured HBM copy peak and elements/s, and the roofline of the dominant kernel, come from that pass.
+L2 is flushed (a 256 MiB write) before every timed step, outside the timed interval, and the host waits
+for each timed step before it queues the next.
 
 Multi-GPU (torchrun): every rank runs its own replica of the step (weak scaling, no collective); value
 = bytes processed by all ranks / max over ranks of the timed region.
@@ -58,6 +59,8 @@ NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed), "argmax_f32": l
 KERNELS = {"row_reduce_exp": "row_warp_kernel", "transpose_log": "selfadd_tma_kernel",
            "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",
            "quant_relayout": "quant_tma_kernel"}
+STEP_SYNC_NOTE = ("the host waits for each timed step to finish before it queues the next (flush, device-side "
+                  "spin, step): with all steps queued ahead the concurrent step took ~241 us instead of ~222 us")
 SCHEDULE_NOTE = ("the five fusions of a step are independent (no buffer shared): each runs on a stream of "
                  "its own, forked from and joined back into the timing stream; the events bracket the whole "
                  "step")
@@ -350,12 +353,14 @@ def ours(args):
         ev_c[k][0].record(stream)
         concurrent.run(stream)
         ev_c[k][1].record(stream)
+        torch.cuda.synchronize()  # each step starts from an idle device (see STEP_SYNC_NOTE)
     sync_all()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(devs) + 1)] for _ in range(args.steps)]
     for k in range(args.steps):
         flush.fill_(k & 0xFF)
         torch.cuda._sleep(HOST_LEAD_CYCLES)
         sequential_step(ev[k])
+        torch.cuda.synchronize()
     sync_all()
     clocks = sampler.stop()
     per_fusion_ms = [[ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(args.steps)] for i in range(len(devs))]
@@ -383,7 +388,7 @@ def ours(args):
             a.record(stream)
             fn()
             b.record(stream)
-        torch.cuda.synchronize()
+            torch.cuda.synchronize()
         return 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs)
 
     def copy_same_bytes_us(nbytes):
@@ -476,7 +481,7 @@ def ours(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": world, "l2": L2_NOTE, "seed": args.seed,
-                       "parallelism": f"replicas{world}", "schedule": SCHEDULE_NOTE},
+                       "parallelism": f"replicas{world}", "schedule": SCHEDULE_NOTE, "host": STEP_SYNC_NOTE},
             "elements_per_s": aggregate(float(step_elems * args.steps), "sum") / total_s,
             "sequential": sequential, "per_fusion": per, "roofline": roofline, "clocks": clocks, "e2e": e2e,
             "gpu_launches": len(devs) * args.steps, "next_rows": next_rows,
@@ -536,7 +541,7 @@ def one_fusion(args):
         a.record(stream)
         d.run(stream=stream)
         b.record(stream)
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
     us = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in evs) if evs else 0.0
     hbm, src = peaks()
     gbs = f.algorithmic_bytes / (us / 1e6) / 1e9 if us else 0.0
