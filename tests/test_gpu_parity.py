@@ -898,6 +898,38 @@ def test_generated_run_tables_past_the_last_slot_and_across_streams():
     assert hf.jit_kernels() >= 12
 
 
+@pytest.mark.parametrize("dtype,ops", [
+    ("bf16", ["mul_input", ("mul_const", 0.3125), "tanh", ("add_const", 1.0), "mul_input"]),  # run table
+    ("f16", ["mul_input", ("add_const", -2.5), "abs", "mul_input"]),  # no table
+])
+def test_generated_chains_under_graph_capture(dtype, ops):
+    """A chain of 2^20 + 3 elements captured into a CUDA graph (torch.cuda.graph) on its first use, then
+    captured again after it has run outside a capture: every replay gives the oracle's values (the
+    first capture, and a chain with a run table, take the interpreter; the rest the generated kernel)."""
+    pats = np.arange(1 << 16, dtype=np.uint16)
+    data = np.concatenate([np.tile(pats, 16), pats[:3]])
+    per_pattern, _ = run_oracle(_chain_fusion(pats, dtype, ops))
+    expected = np.asarray(per_pattern).reshape(-1)[data]
+    # the interpreter's one-time setup (table address, attributes) outside a capture
+    warm = DeviceFusion(_chain_fusion(np.tile(pats, 4), dtype, ["tanh"] if dtype == "bf16" else ["abs"]))
+    warm.run()
+    f = _chain_fusion(data, dtype, ops)
+    d = DeviceFusion(f)
+    torch.cuda.synchronize()
+    for plain_run_first in (False, True):
+        if plain_run_first:
+            d.run()
+            torch.cuda.synchronize()
+        d.out.zero_()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            d.run()
+        d.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        check(f, d.output_numpy(), expected, None)
+
+
 def test_gelu_chain_f32_bit_exact():
     """The same GELU chain on f32 (every op, tanh included, correctly rounded on both sides): bit-exact."""
     g = np.random.default_rng(13)

@@ -432,12 +432,13 @@ std::mutex g_mu;
 std::map<std::pair<int, std::string>, JitKernel> g_cache;
 
 // Compiles the chain for the current device (or returns the cached result); a run table is built on
-// stream s.
-JitKernel build(const Chain& c, int dt, int dev, cudaStream_t s) {
+// stream s. With build_new false only a cached kernel is returned (a default one, no kernel, otherwise).
+JitKernel build(const Chain& c, int dt, int dev, cudaStream_t s, bool build_new) {
   const auto key = std::make_pair(dev, chain_key(c, dt));
   std::lock_guard<std::mutex> lock(g_mu);
   auto it = g_cache.find(key);
   if (it != g_cache.end()) return it->second;
+  if (!build_new) return JitKernel{};
   JitKernel jk;
   cudaSetDevice(dev);  // makes the device's primary context current for the driver calls below
   const NvrtcApi& nv = nvrtc();
@@ -516,8 +517,15 @@ cudaError_t launch_jit_chain(const void* in, void* out, int64_t n, int dt, const
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const JitKernel jk = build(pro, dt, dev, s);
-  if (!jk.fn) return cudaSuccess;  // the interpreter takes the call
+  // While s is being captured into a graph, work enqueued on it is recorded, not run: a chain's first
+  // use (which builds its run table on s) and a wait on the table's event both stay out of the capture,
+  // so the interpreter takes the call unless the chain's kernel was built before and has no run table.
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(s, &capture);
+  if (e != cudaSuccess) return e;
+  const bool capturing = capture != cudaStreamCaptureStatusNone;
+  const JitKernel jk = build(pro, dt, dev, s, !capturing);
+  if (!jk.fn || (capturing && jk.ready)) return cudaSuccess;  // the interpreter takes the call
   const void* tg = jk.table;
   if (jk.ready && s != jk.built_on) {  // the run table was built on another stream
     e = cudaStreamWaitEvent(s, jk.ready, 0);
