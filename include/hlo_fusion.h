@@ -395,6 +395,14 @@ hlo_status hlo_selftest_bounded_wait(void* stream);
  * other kernels give. If NVRTC cannot be opened or the source does not compile, the library's fixed
  * kernels run the call instead.
  *
+ * When a bf16 chain's tanh ops all lie in one run of two or more ops that do not read the input (for
+ * GELU: multiply by a constant, tanh, add 1, multiply by 1/2), the first call also builds that run's
+ * 65536-entry result table on the device, on the call's stream, into one of eight slots the library
+ * holds for the life of the process (later such chains use the tanh table instead); calls on other
+ * streams wait for it with cudaStreamWaitEvent. While the call's stream is being captured into a CUDA
+ * graph, only a chain compiled earlier and without such a table uses its generated kernel: nothing is
+ * compiled, built or waited for inside a capture.
+ *
  * hlo_jit_kernels returns the number of chain kernels built so far for the current device, or -1 when
  * NVRTC or the driver calls it needs are unavailable (no generated kernels will run).
  * ---------------------------------------------------------------------------------------------- */
