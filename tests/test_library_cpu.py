@@ -250,6 +250,57 @@ def test_expf_first_pass_error_below_its_rounding_bound():
     assert float(err.max()) < 2.0 ** -36.5
 
 
+def test_logf_first_pass_error_below_its_rounding_bound():
+    """The packed f32 log first pass (cr_log.cuh, cr_logf_first2 / cr_logf_first4), emulated step for step
+    from the committed 32-interval tables: |log x - (S + lo)| stays below 2^-33.6 on U(0.5, 2), near 1,
+    over the whole exponent range and on random normal bit patterns, so the test's bound b = 2^-33.5,
+    less the rounding of lo +- b (< 2^-37), covers it. The same emulation over every positive normal
+    float gives 2^-34.13 at most."""
+    f32 = np.float32
+    with open(os.path.join(ROOT, "transpose_heroes_gb300", "csrc", "log_table.inc")) as f:
+        txt = f.read()
+
+    def table(name):
+        body = re.search(name + r"\[32\] = \{(.*?)\};", txt, re.S).group(1)
+        return np.array([float.fromhex(v.strip().rstrip("f")) if v.strip() != "0.0f" else 0.0
+                         for v in body.split(",") if v.strip()], dtype=f32)
+
+    inv, hi, lo = table("kLog1Inv"), table("kLog1Hi"), table("kLog1Lo")
+    off = int(re.search(r"HLO_LOG1_OFF (0x[0-9A-Fa-f]+)u", txt).group(1), 16)
+    shift = int(re.search(r"HLO_LOG1_SHIFT (\d+)", txt).group(1))
+    ln2a = f32(float.fromhex(re.search(r"HLO_LOG1_LN2_A (\S+)f", txt).group(1)))
+    ln2b = f32(float.fromhex(re.search(r"HLO_LOG1_LN2_B (\S+)f", txt).group(1)))
+
+    def fma(a, b, c):  # one rounding: the f64 product is exact, the sum's error is added back (TwoSum)
+        p = np.asarray(a, np.float64) * np.asarray(b, np.float64)
+        c = np.broadcast_to(np.asarray(c, np.float64), p.shape)
+        s = p + c
+        bb = s - p
+        return (s + ((p - (s - bb)) + (c - bb))).astype(f32)
+
+    g = np.random.default_rng(21)
+    x = np.concatenate([g.uniform(0.5, 2.0, 1_500_000), 1.0 + g.uniform(-0.03, 0.03, 1_000_000),
+                        np.exp(g.uniform(-87.0, 88.0, 1_000_000))]).astype(f32)
+    x = np.concatenate([x, g.integers(0x00800000, 0x7F800000, 1_000_000, dtype=np.uint32).view(f32)])
+    ix = x.view(np.uint32)
+    t = (ix - np.uint32(off)).astype(np.uint32)
+    i = (t >> np.uint32(shift)) & np.uint32(31)
+    m = (ix - (t & np.uint32(0xFF800000))).astype(np.uint32).view(f32)
+    e = (t.view(np.int32) >> 23).astype(f32)
+    r = fma(m, inv[i], f32(-1))
+    a = fma(e, ln2a, hi[i])
+    s = (a + r).astype(f32)
+    err_sum = (r - (s - a).astype(f32)).astype(f32)
+    p = fma(r, f32(0.2), f32(-0.25))
+    p = fma(r, p, f32(0.33333334))
+    p = fma(r, p, f32(-0.5))
+    b = fma(e, ln2b, lo[i])
+    rest = fma((r * r).astype(f32), p, b)
+    lo_ = (err_sum + rest).astype(f32)
+    err = np.abs(s.astype(np.float64) + lo_.astype(np.float64) - np.log(x.astype(np.float64)))
+    assert float(err.max()) < 2.0 ** -33.6
+
+
 def test_tanhf_first_pass_errors_below_their_rounding_bounds():
     """Both branches of the f32 tanh first pass (cr_exp.cuh), emulated step for step: the Taylor branch
     (a < 2^-4) within 2^-39 a of tanh a (the test uses a 2^-37), the 1 - 2/(exp(2a) + 1) branch within

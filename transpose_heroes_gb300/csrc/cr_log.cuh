@@ -232,11 +232,13 @@ __device__ __forceinline__ float2 fma(float2 a, float2 b, float2 c) { return __f
 // First pass, two elements at a time: 32-interval table (three 32-float arrays, so a warp's lookups
 // hit distinct banks), e*ln2 from exact products:
 //   log x = S + err + rest,  S + err = A + r exactly (Fast2Sum),  A = e*LN2_A + log(c)_hi (exact),
-//   rest = r^2 (-1/2 + r/3 - r^2/4 + r^3/5 - r^4/6) + (e*LN2_B + log(c)_lo)   in f32.
-// With lo = RN(err + rest), every error (truncation r^7/7 < 2^-42, the roundings of r^2, of the
-// polynomial and of rest ~2^-36.3 each, the table and LN2_B terms below 2^-36 for all exponents, lo's
-// rounding ~2^-36.2) sums to under 2^-33.8, so |log x - (S + lo)| < b = 2^-33.5 with room for the
-// rounding of lo +- b (< 2^-37). Rounding test by monotonicity of round-to-nearest: if S + (lo - b)
+//   rest = r^2 (-1/2 + r/3 - r^2/4 + r^3/5) + (e*LN2_B + log(c)_lo)   in f32   (|r| < 2^-5.6).
+// With lo = RN(err + rest), the errors (truncation r^6/6 < 2^-36.2 of the alternating series, the
+// roundings of r^2, of the polynomial and of rest ~2^-36.3 each, the table and LN2_B terms below 2^-36
+// for all exponents, lo's rounding ~2^-36.2) stay under b = 2^-33.5 less the rounding of lo +- b
+// (< 2^-37): a step-for-step emulation of these operations over every positive normal float gives
+// |log x - (S + lo)| <= 2^-34.13 (2^-34.40 with the r^6 term kept, which costs one more packed FMA
+// per pair). Rounding test by monotonicity of round-to-nearest: if S + (lo - b)
 // and S + (lo + b) round to the same float, every value between them, the exact log among them,
 // rounds to it. About 2% of inputs in [0.5, 2) (most of those near 1) and every special operand
 // are left open (ok = false) for cr_logf.
@@ -257,8 +259,7 @@ __device__ __forceinline__ void cr_logf_first2(float x0, float x1, const float* 
   const float2 A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), f2::pk(thi[i0], thi[i1]));        // exact
   const float2 S = f2::add(A, R);                       // Fast2Sum: A = 0 or |A| >= |r|
   const float2 ERR = f2::sub(R, f2::sub(S, A));
-  float2 P = f2::fma(R, f2::splat(-0.16666667f), f2::splat(0.2f));
-  P = f2::fma(R, P, f2::splat(-0.25f));
+  float2 P = f2::fma(R, f2::splat(0.2f), f2::splat(-0.25f));
   P = f2::fma(R, P, f2::splat(0.33333334f));
   P = f2::fma(R, P, f2::splat(-0.5f));
   const float2 B = f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), f2::pk(tlo[i0], tlo[i1]));
@@ -300,8 +301,7 @@ __device__ __forceinline__ uint32_t cr_logf_first4(const float4 x, const float (
     const float2 A = f2::fma(EF, f2::splat(HLO_LOG1_LN2_A), HI);       // exact
     const float2 S = f2::add(A, R);                                     // Fast2Sum: A = 0 or |A| >= |r|
     const float2 ERR = f2::sub(R, f2::sub(S, A));
-    float2 P = f2::fma(R, f2::splat(-0.16666667f), f2::splat(0.2f));
-    P = f2::fma(R, P, f2::splat(-0.25f));
+    float2 P = f2::fma(R, f2::splat(0.2f), f2::splat(-0.25f));
     P = f2::fma(R, P, f2::splat(0.33333334f));
     P = f2::fma(R, P, f2::splat(-0.5f));
     const float2 B = f2::fma(EF, f2::splat(HLO_LOG1_LN2_B), LOT);
