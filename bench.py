@@ -59,6 +59,9 @@ NEXT_ROWS = {"gelu_bf16": lambda seed: inp.gelu_bf16(seed=seed), "argmax_f32": l
 KERNELS = {"row_reduce_exp": "row_warp_kernel", "transpose_log": "selfadd_tma_kernel",
            "col_reduce_max": "col_reduce_kernel", "bcast_exp_reduce": "row_stream_kernel",
            "quant_relayout": "quant_tma_kernel"}
+CLEAN_L2_NOTE = ("alone_clean_l2_us / clean_l2_us (not part of value): the fusion timed alone after the same "
+                 "256 MiB write followed by a 256 MiB read, so that the write's dirty lines leave L2 before the "
+                 "launch instead of during it (what ncu's cache flush leaves)")
 STEP_SYNC_NOTE = ("the host waits for each timed step to finish before it queues the next (flush, device-side "
                   "spin, step): with all steps queued ahead the concurrent step took ~241 us instead of ~222 us")
 SCHEDULE_NOTE = ("the five fusions of a step are independent (no buffer shared): each runs on a stream of "
@@ -377,13 +380,20 @@ def ours(args):
     hbm, peak_src = peaks()
     reps = max(3, min(args.steps, 200))
 
-    def time_alone(fn):
-        """Mean CUDA-event interval of fn over `reps` launches, L2 flushed before each."""
+    clean_src = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MiB read after the flush
+    clean_acc = torch.empty((), dtype=torch.float32, device=dev)
+
+    def time_alone(fn, clean=False):
+        """Mean CUDA-event interval of fn over `reps` launches, L2 flushed before each (the 256 MiB write;
+        with clean=True then a 256 MiB read, so that the write's dirty lines are written back before the
+        launch instead of during it)."""
         for _ in range(3):
             fn()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         for a, b in evs:
             flush.fill_(3)
+            if clean:
+                torch.sum(clean_src, dim=0, out=clean_acc)
             torch.cuda._sleep(HOST_LEAD_CYCLES // 8)
             a.record(stream)
             fn()
@@ -409,7 +419,8 @@ def ours(args):
                          "algorithmic_bytes": f.algorithmic_bytes, "gbs": gbs, "frac_of_" + peak_src: gbs / hbm,
                          "elements_per_s": f.elements / (ms / 1e3)}
         copy_us = copy_same_bytes_us(f.algorithmic_bytes)
-        per[ORDER[i]].update({"copy_same_bytes_us": copy_us, "speed_vs_copy": copy_us / (1e3 * ms)})
+        per[ORDER[i]].update({"copy_same_bytes_us": copy_us, "speed_vs_copy": copy_us / (1e3 * ms),
+                              "alone_clean_l2_us": time_alone(lambda d=devs[i]: d.run(stream=stream), clean=True)})
     dom = max(per, key=lambda k: per[k]["us"])
     dom_gbs = per[dom]["gbs"]
     tr = traffic_record()
@@ -472,7 +483,8 @@ def ours(args):
         copy_us = copy_same_bytes_us(f.algorithmic_bytes)
         next_rows[name] = {"workload": f.description, "us": us, "algorithmic_bytes": f.algorithmic_bytes,
                            "gbs": gbs, "frac_of_" + peak_src: gbs / hbm, "elements_per_s": f.elements / (us / 1e6),
-                           "launches": reps, "copy_same_bytes_us": copy_us, "speed_vs_copy": copy_us / us}
+                           "launches": reps, "copy_same_bytes_us": copy_us, "speed_vs_copy": copy_us / us,
+                           "clean_l2_us": time_alone(lambda: d.run(stream=stream), clean=True)}
         del d
 
     if rank == 0:
@@ -481,7 +493,8 @@ def ours(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD, "global_batch": world, "l2": L2_NOTE, "seed": args.seed,
-                       "parallelism": f"replicas{world}", "schedule": SCHEDULE_NOTE, "host": STEP_SYNC_NOTE},
+                       "parallelism": f"replicas{world}", "schedule": SCHEDULE_NOTE, "host": STEP_SYNC_NOTE,
+                       "clean_l2": CLEAN_L2_NOTE},
             "elements_per_s": aggregate(float(step_elems * args.steps), "sum") / total_s,
             "sequential": sequential, "per_fusion": per, "roofline": roofline, "clocks": clocks, "e2e": e2e,
             "gpu_launches": len(devs) * args.steps, "next_rows": next_rows,
