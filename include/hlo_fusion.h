@@ -405,8 +405,16 @@ hlo_status hlo_selftest_bounded_wait(void* stream);
  *
  * hlo_jit_kernels returns the number of chain kernels built so far for the current device, or -1 when
  * NVRTC or the driver calls it needs are unavailable (no generated kernels will run).
+ *
+ * hlo_jit_source writes the CUDA C source the library generates for `chain` on element type `dtype`
+ * (HLO_BF16 or HLO_F16) into buf, NUL-terminated, when buf_len exceeds its length; it returns the
+ * length (without the NUL), or -1 when the generator does not take the chain (another element type,
+ * intermediates not rounded, an op other than those above) or buf_len < 0, or buf is NULL with
+ * buf_len > 0. With buf NULL and buf_len 0 it only measures. The source is the one generated while a
+ * run-table slot is free. No device, NVRTC or driver call is made; the caller owns buf.
  * ---------------------------------------------------------------------------------------------- */
 int32_t hlo_jit_kernels(void);
+int64_t hlo_jit_source(const hlo_ew_chain* chain, int32_t dtype, char* buf, int64_t buf_len);
 
 /* ------------------------------------------------------------------------------------------------
  * Fault injection for tests of the error path (no counterpart in the pages: the library's own test

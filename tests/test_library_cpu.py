@@ -25,7 +25,7 @@ def lib():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:hlo_status|size_t|int32_t|const char\*)\s+(hlo_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:hlo_status|size_t|int32_t|int64_t|const char\*)\s+(hlo_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_binding_exports():
@@ -453,3 +453,77 @@ def test_fault_injection_names_one_site(lib, monkeypatch):
     monkeypatch.setenv("HLOFUSION_FAULT", "hlo_reduce_fusion")
     st, msg = _status(_valid_calls()["hlo_transpose_fusion"])
     assert "injected fault" not in msg
+
+
+# ---- the run-time chain generator (jit_chain.cu), through hlo_jit_source: no device needed ------------------
+GELU = {"ops": ["mul_input", "mul_input", ("mul_const", 0.044708), "add_input", ("mul_const", 0.79785), "tanh",
+                ("add_const", 1.0), ("mul_const", 0.5), "mul_input"], "round_each": True}
+TWO_TANH_RUNS = {"ops": ["mul_input", "tanh", "add_input", "tanh", ("mul_const", 2.0), "mul_input"], "round_each": True}
+NO_TANH_F16 = {"ops": ["mul_input", ("add_const", -1.5), "neg", ("mul_const", 0.3), "add_input", "abs"],
+               "round_each": True}
+
+
+def _defines(src):
+    return dict(re.findall(r"^#define (\w+) (\S+)$", src, re.M))
+
+
+def _chain_function(src):
+    return re.search(r"u32 f\(u32 x, const unsigned short\* t\) \{(.*?)\n\}", src, re.S).group(1)
+
+
+def test_jit_source_table_plans(lib):
+    """GELU's tanh sits in one x-free run of four ops (multiply, tanh, add 1, multiply): one 65536-entry
+    run table (128 KiB, six ring stages) and a table-building kernel that applies exactly those ops; a
+    chain with tanh in two runs reads the 64 KiB tanh table; a chain without tanh has no table."""
+    src = hf.jit_source(GELU, "bf16")
+    d = _defines(src)
+    assert (d["TB"], d["NS"], d["CB"]) == ("131072", "6", "16384")
+    body = _chain_function(src)
+    assert body.count("hmul(v, x)") == 3 and body.count("hadd(v, x)") == 1
+    assert "hlook(v, t)" in body and "htanh" not in body
+    table = re.search(r"hlo_jit_table\(.*?\{(.*?)\n\}", src, re.S).group(1)
+    run = re.findall(r"v = (\w+)\(v, (0x[0-9A-F]+u|t)\)", table)
+    # bf16 bits: 0.79785 -> 0x3F4C, 1 -> 0x3F80, 0.5 -> 0x3F00, each in both halves of the pair
+    assert run == [("hmul", "0x3F4C3F4Cu"), ("htanh", "t"), ("hadd", "0x3F803F80u"), ("hmul", "0x3F003F00u")]
+
+    src = hf.jit_source(TWO_TANH_RUNS, "bf16")
+    assert _defines(src)["TB"] == "65536" and "hlo_jit_table" not in src
+    assert _chain_function(src).count("htanh(v, t)") == 2
+
+    src = hf.jit_source(NO_TANH_F16, "f16")
+    d = _defines(src)
+    assert d["TB"] == "0" and d["NS"] == "12" and "add.rn.f16x2" in src and "bf16" not in src
+    assert "v ^= 0x80008000u" in src and "v &= 0x7FFF7FFFu" in src
+
+
+def test_jit_source_rejects_other_chains(lib):
+    """The generator takes rounded 16-bit chains of adds, multiplies, negate, abs and bf16 tanh only."""
+    assert hf.jit_source({"ops": ["exp"], "round_each": True}, "bf16") is None
+    assert hf.jit_source({"ops": ["tanh"], "round_each": True}, "f16") is None
+    assert hf.jit_source({"ops": ["abs"], "round_each": False}, "bf16") is None
+    assert hf.jit_source({"ops": ["abs"], "round_each": True}, "f32") is None
+    assert hf.jit_source({"ops": ["abs"], "round_each": True}, "bf16") is not None
+    chain = hf.make_chain({"ops": ["abs"], "round_each": True})
+    assert lib.hlo_jit_source(ctypes.byref(chain), hf.DTYPES["bf16"], None, 5) == -1  # NULL buffer, length 5
+    n = lib.hlo_jit_source(ctypes.byref(chain), hf.DTYPES["bf16"], None, 0)
+    small = ctypes.create_string_buffer(8)
+    assert lib.hlo_jit_source(ctypes.byref(chain), hf.DTYPES["bf16"], small, 8) == n and small.value == b""
+
+
+@pytest.mark.parametrize("spec,dtype", [(GELU, "bf16"), (TWO_TANH_RUNS, "bf16"), (NO_TANH_F16, "f16")])
+def test_jit_source_compiles_for_sm_103a(lib, spec, dtype, tmp_path):
+    """The generated source compiles for sm_103a (nvcc here stands in for NVRTC on the device), with no
+    register spills."""
+    import shutil
+    import subprocess
+
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not found")
+    src = tmp_path / "chain.cu"
+    src.write_text(hf.jit_source(spec, dtype))
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-std=c++17", "-Xptxas", "-v", "-c",
+                        str(src), "-o", str(tmp_path / "chain.o")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert " 0 bytes spill stores" in r.stderr and "bytes spill stores" in r.stderr
+    assert all(m == "0" for m in re.findall(r"(\d+) bytes spill stores", r.stderr))

@@ -36,7 +36,7 @@ EXPORTS = ("hlo_reduce_fusion", "hlo_reduce_fusion_noalloc", "hlo_reduce_workspa
            "hlo_layout_convert",
            "hlo_quant_fusion", "hlo_quant_binary", "hlo_quant_broadcast_in_dim", "hlo_quant_reshape",
            "hlo_reduce_max_argmax", "hlo_device_faults",
-           "hlo_selftest_bounded_wait", "hlo_jit_kernels", "hlo_last_error", "hlo_version")
+           "hlo_selftest_bounded_wait", "hlo_jit_kernels", "hlo_jit_source", "hlo_last_error", "hlo_version")
 QUANT_BINARY_OPS = {"add": 0, "divide": 1, "maximum": 2, "minimum": 3, "multiply": 4}
 
 
@@ -114,6 +114,8 @@ def lib() -> ctypes.CDLL:
             h.hlo_selftest_bounded_wait.restype = ctypes.c_int
             h.hlo_jit_kernels.argtypes = []
             h.hlo_jit_kernels.restype = ctypes.c_int32
+            h.hlo_jit_source.argtypes = [P(EwChain), i32, ctypes.c_char_p, i64]
+            h.hlo_jit_source.restype = ctypes.c_int64
             h.hlo_last_error.restype = ctypes.c_char_p
             h.hlo_version.restype = ctypes.c_char_p
             _lib = h
@@ -316,6 +318,21 @@ def device_faults(clear: bool = False) -> int:
 def jit_kernels() -> int:
     """hlo_jit_kernels: chain kernels generated for the current device (-1: NVRTC unavailable)."""
     return int(lib().hlo_jit_kernels())
+
+
+def jit_source(prologue, dtype: str):
+    """hlo_jit_source: the CUDA source generated for a 16-bit chain, or None if the generator does not
+    take it. `prologue` is a chain spec as for transpose_fusion."""
+    chain = make_chain(prologue)
+    if chain is None:
+        return None
+    n = int(lib().hlo_jit_source(ctypes.byref(chain), DTYPES[dtype], None, 0))
+    if n < 0:
+        return None
+    buf = ctypes.create_string_buffer(n + 1)
+    if int(lib().hlo_jit_source(ctypes.byref(chain), DTYPES[dtype], buf, n + 1)) != n:
+        return None
+    return buf.value.decode()
 
 
 def selftest_bounded_wait(stream=None) -> None:

@@ -769,6 +769,23 @@ hlo_status hlo_selftest_bounded_wait(void* stream) {
 
 int32_t hlo_jit_kernels(void) { return jit_chain_kernels(); }
 
+int64_t hlo_jit_source(const hlo_ew_chain* chain, int32_t dtype, char* buf, int64_t buf_len) {
+  if (buf_len < 0 || (buf_len > 0 && !buf)) return -1;
+  hlo_array arr;
+  std::memset(&arr, 0, sizeof arr);
+  arr.rank = 1;
+  arr.dtype = dtype;
+  arr.dims[0] = 1;
+  Chain pro;
+  if (dtype != HLO_BF16 && dtype != HLO_F16) return -1;
+  if (!chain || make_chain(chain, arr, false, "jit source", &pro) != HLO_OK) return -1;
+  std::string src;
+  if (!jit_chain_source(pro, dtype, &src)) return -1;
+  const int64_t len = (int64_t)src.size();
+  if (buf && buf_len > len) std::memcpy(buf, src.c_str(), (size_t)len + 1);
+  return len;
+}
+
 const char* hlo_last_error(void) { return g_err.c_str(); }
 
 const char* hlo_version(void) { return "hlofusion 0.1 (sm_103a)"; }

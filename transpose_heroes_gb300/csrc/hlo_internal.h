@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <string>
 
 #include <cuda_runtime.h>
 
@@ -262,6 +263,9 @@ cudaError_t launch_elementwise(const void* in, void* out, int64_t n, int dt, con
 bool jit_chain_ok(const Chain& pro, const Chain& epi, int dt);
 cudaError_t launch_jit_chain(const void* in, void* out, int64_t n, int dt, const Chain& pro, cudaStream_t s, bool* used);
 int jit_chain_kernels();
+// The CUDA source generated for a chain the generator takes (with a run-table slot free); false for
+// any other chain. No device work.
+bool jit_chain_source(const Chain& pro, int dt, std::string* out);
 // Device address of the bf16 tanh table (k_elementwise.cu), or NULL.
 const void* tanh_table_address();
 

@@ -547,6 +547,14 @@ cudaError_t launch_jit_chain(const void* in, void* out, int64_t n, int dt, const
   return cudaSuccess;
 }
 
+bool jit_chain_source(const Chain& pro, int dt, std::string* out) {
+  Chain none;
+  std::memset(&none, 0, sizeof none);
+  if (!jit_chain_ok(pro, none, dt)) return false;
+  *out = kernel_source(pro, dt, plan_table(pro, dt));
+  return true;
+}
+
 int jit_chain_kernels() {
   if (!nvrtc().ok || !driver().ok) return -1;
   int dev = 0;
