@@ -216,14 +216,14 @@ std::string chain_body(const Chain& c, int dt, int k0, int k1) {
 
 // The generated kernel streams the array through shared memory in 16 KiB chunks of 1024 vectors. Block b
 // of G takes chunks b, b + G, b + 2G, ... of the whole rounds of G chunks, then an even share of what is
-// left (the remainder's vectors split G ways, so no block streams a whole extra chunk). One block per SM keeps a ring of chunks in
-// flight as 1-D bulk copies completing on mbarriers, issued up front by thread 0 (with the 64 KiB tanh
-// table, when the chain has a tanh) and refilled by the last warp to finish with a chunk, so an SM asks
-// for its first 160 KiB of input at launch rather than a few vectors per thread at a time. Each thread
-// takes kJitVecs vectors of a chunk, applies the chain and stores them straight to global memory; the
-// last n % 8 elements are read directly by the last block. Every wait is bounded: on a timeout the
-// block records the fault in the library's fault word, waits (bounded) for the copies it still has in
-// flight and returns.
+// left (the remainder's vectors split G ways, so no block streams a whole extra chunk). One block per
+// SM keeps a ring of chunks in flight as 1-D bulk copies completing on mbarriers, issued up front by
+// thread 0 (with the chain's table, if any: the 64 KiB tanh table or a 128 KiB run table) and refilled
+// by the last warp to finish with a chunk, so an SM asks for its first 96-192 KiB of input at launch
+// rather than a few vectors per thread at a time. Each thread takes kJitVecs vectors of a chunk,
+// applies the chain and stores them straight to global memory; the last n % 8 elements are read
+// directly by the last block. Every wait is bounded: on a timeout the block records the fault in the
+// library's fault word, waits (bounded) for the copies it still has in flight and returns.
 constexpr int kChunkVecs = 1024;
 constexpr int kChunkBytes = kChunkVecs * 16;
 
